@@ -1,0 +1,143 @@
+"""Plant plausible mistakes in the oracle (on the CPU) and check that the
+pins catch each one: a flipped sign, an off-by-one index, swapped operands,
+a dropped term, a wrong scale, a wrong mask boundary."""
+import math
+
+import numpy as np
+import pytest
+
+import oracle_pins as P
+from oracle import relpos_oracle as orc
+
+
+def _flip_t5(orig):
+    return lambda rel, *a, **k: orig(-rel, *a, **k)
+
+
+def _shift_t5(orig):
+    return lambda rel, *a, **k: orig(rel + 1, *a, **k)
+
+
+def _t5_round(rel, bidirectional=True, num_buckets=32, max_distance=128):
+    # rounds the log position instead of truncating it
+    slots, base = num_buckets, 0
+    if bidirectional:
+        slots //= 2
+        base = slots if rel > 0 else 0
+        n = abs(rel)
+    else:
+        n = max(-rel, 0)
+    exact = slots // 2
+    if n < exact:
+        return base + n
+    wide = exact + int(round(math.log(n / exact) / math.log(max_distance / exact)
+                             * (slots - exact)))
+    return base + min(wide, slots - 1)
+
+
+def _t5_log_of_max_distance_only(rel, bidirectional=True, num_buckets=32, max_distance=128):
+    # divides by log(max_distance) instead of log(max_distance / exact)
+    slots, base = num_buckets, 0
+    if bidirectional:
+        slots //= 2
+        base = slots if rel > 0 else 0
+        n = abs(rel)
+    else:
+        n = max(-rel, 0)
+    exact = slots // 2
+    if n < exact:
+        return base + n
+    wide = exact + int(math.log(n / exact) / math.log(max_distance) * (slots - exact))
+    return base + min(wide, slots - 1)
+
+
+_ORIG_T5 = orc.t5_bucket
+
+
+def _deberta_logits_no_p2c(q, k, pk_h, pq_h, p, kclip):
+    d = q.shape[-1]
+    r = p[:, None] - np.arange(k.shape[0])[None, :]
+    d_ij = np.clip(r, -kclip, kclip - 1) + kclip
+    c2p = np.take_along_axis(q @ pk_h.T, d_ij, axis=1)
+    return (q @ k.T + c2p) / math.sqrt(3 * d)
+
+
+def _deberta_logits_swapped_tables(q, k, pk_h, pq_h, p, kclip):
+    return _ORIG_DEB(q, k, pq_h, pk_h, p, kclip)
+
+
+def _deberta_logits_same_delta(q, k, pk_h, pq_h, p, kclip):
+    # uses delta(i, j) for the p2c term as well
+    d = q.shape[-1]
+    j = np.arange(k.shape[0])
+    r = p[:, None] - j[None, :]
+    d_ij = np.clip(r, -kclip, kclip - 1) + kclip
+    c2p = np.take_along_axis(q @ pk_h.T, d_ij, axis=1)
+    p2c = (k @ pq_h.T)[j[None, :], d_ij]
+    return (q @ k.T + c2p + p2c) / math.sqrt(3 * d)
+
+
+def _deberta_logits_scale_d(q, k, pk_h, pq_h, p, kclip):
+    return _ORIG_DEB(q, k, pk_h, pq_h, p, kclip) * math.sqrt(3.0)
+
+
+_ORIG_DEB = orc.deberta_logits
+_ORIG_SHAW = orc.shaw_logits
+_ORIG_SHAW_V = orc.shaw_value_term
+_ORIG_MASK = orc._mask
+
+
+def _shaw_logits_unscaled_rel(q, k, aK, p, kclip):
+    d = q.shape[-1]
+    rel = np.arange(k.shape[0])[None, :] - p[:, None]
+    idx = np.clip(rel, -kclip, kclip) + kclip
+    return (q @ k.T) / math.sqrt(d) + np.take_along_axis(q @ aK.T, idx, axis=1)
+
+
+def _shaw_logits_flipped(q, k, aK, p, kclip):
+    return _ORIG_SHAW(q, k, aK[::-1].copy(), p, kclip)
+
+
+def _shaw_value_dropped(w, p, aV, kclip):
+    return 0.0
+
+
+def _shaw_value_flipped(w, p, aV, kclip):
+    return _ORIG_SHAW_V(w, p, aV[::-1].copy(), kclip)
+
+
+def _mask_off_by_one(logits, p, Lk, causal):
+    if causal:
+        j = np.arange(Lk)
+        logits = np.where(j[None, :] >= p[:, None], -np.inf, logits)
+        logits[:, 0] = np.where(np.all(np.isinf(logits), axis=1), 0.0, logits[:, 0])
+    return logits
+
+
+MUTATIONS = {
+    "t5_sign_flipped": ("t5_bucket", _flip_t5(_ORIG_T5)),
+    "t5_offset_off_by_one": ("t5_bucket", _shift_t5(_ORIG_T5)),
+    "t5_rounds_log": ("t5_bucket", _t5_round),
+    "t5_wrong_log_denominator": ("t5_bucket", _t5_log_of_max_distance_only),
+    "shaw_index_sign": ("shaw_index", lambda rel, k: _ORIG_SHAW_IDX(-rel, k)),
+    "deberta_delta_swapped": ("deberta_delta", lambda i, j, k: _ORIG_DELTA(j, i, k)),
+    "deberta_no_p2c": ("deberta_logits", _deberta_logits_no_p2c),
+    "deberta_tables_swapped": ("deberta_logits", _deberta_logits_swapped_tables),
+    "deberta_p2c_same_delta": ("deberta_logits", _deberta_logits_same_delta),
+    "deberta_scale_sqrt_d": ("deberta_logits", _deberta_logits_scale_d),
+    "shaw_rel_unscaled": ("shaw_logits", _shaw_logits_unscaled_rel),
+    "shaw_rel_flipped": ("shaw_logits", _shaw_logits_flipped),
+    "shaw_value_dropped": ("shaw_value_term", _shaw_value_dropped),
+    "shaw_value_flipped": ("shaw_value_term", _shaw_value_flipped),
+    "mask_off_by_one": ("_mask", _mask_off_by_one),
+}
+_ORIG_SHAW_IDX = orc.shaw_index
+_ORIG_DELTA = orc.deberta_delta
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_pins_catch_mutation(name, monkeypatch):
+    attr, fn = MUTATIONS[name]
+    monkeypatch.setattr(orc, attr, fn)
+    failed = P.run_all()
+    assert failed, f"no pin caught the planted mistake {name}"

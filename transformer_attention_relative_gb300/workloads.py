@@ -1,0 +1,148 @@
+"""Seeded synthetic workloads for relative-position attention.
+
+This module holds shapes, seeds and random draws only -- none of the
+method's arithmetic. Both the CUDA path (tests, bench) and the CPU oracle
+take their inputs from here, so the two sides always see identical values.
+
+Recipe (one per workload): a CPU ``torch.Generator`` seeded with
+``1000 + index``; draws in the order Q, K, V, table0, table1; ``randn``
+scaled by the workload's sigma; then a cast to the kernel's input dtype
+(bf16, or fp32 for the tiny fp32 case). The T5 bias table stays fp32 in
+every workload; the Shaw and DeBERTa tables are bf16.
+
+Shapes and distributions follow the five workloads the relative-position
+attention pages motivate: a tiny fp32 T5 encoder case, a T5-base-shaped
+encoder, a T5 causal decoder plus its cached-decode step, Shaw clipped
+relative keys/values at L=4096, and DeBERTa disentangled attention at
+k=256.
+"""
+from __future__ import annotations
+
+import dataclasses
+
+import torch
+
+MODE_T5, MODE_SHAW, MODE_DEBERTA = 0, 1, 2
+MODE_NAMES = {MODE_T5: "t5", MODE_SHAW: "shaw", MODE_DEBERTA: "deberta"}
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    index: int            # seed = 1000 + index
+    mode: int
+    dtype: str            # "bf16" or "fp32": the Q/K/V element type
+    B: int
+    H: int
+    Lq: int
+    Lk: int
+    d: int
+    num_buckets: int = 0  # T5 only
+    rel_param: int = 0    # T5 max_distance, Shaw / DeBERTa clip k
+    causal: bool = False
+    q_offset: int = 0
+    qkv_sigma: float = 1.0
+    table_sigma: float = 0.0
+
+    @property
+    def seed(self) -> int:
+        return 1000 + self.index
+
+    def replace(self, **kw) -> "Workload":
+        return dataclasses.replace(self, **kw)
+
+    def table_shapes(self):
+        """Shapes of table0 / table1 (None where the mode has no table)."""
+        if self.mode == MODE_T5:
+            return (self.num_buckets, self.H), None
+        if self.mode == MODE_SHAW:
+            n = 2 * self.rel_param + 1
+            return (n, self.d), (n, self.d)
+        n = 2 * self.rel_param
+        return (n, self.H, self.d), (n, self.H, self.d)
+
+    def flops(self) -> float:
+        """Algorithmic flop of one forward over this workload.
+
+        Counts the dense contractions the method requires: Q.K^T and P.V
+        (halved to the visible triangle when causal), plus Shaw's Q.a_K^T
+        and binned-P.a_V over the 2k+1 table, or DeBERTa's Q.Pk^T and
+        K.Pq^T over the 2k table. Gathers, exp and masking are not counted.
+        """
+        B, H, Lq, Lk, d = self.B, self.H, self.Lq, self.Lk, self.d
+        if self.causal:
+            pairs = 0
+            for i in range(Lq):
+                pairs += max(0, min(Lk, i + self.q_offset + 1))
+        else:
+            pairs = Lq * Lk
+        core = 4.0 * B * H * pairs * d
+        if self.mode == MODE_SHAW:
+            n = 2 * self.rel_param + 1
+            core += 4.0 * B * H * Lq * n * d
+        elif self.mode == MODE_DEBERTA:
+            n = 2 * self.rel_param
+            core += 2.0 * B * H * Lq * n * d + 2.0 * B * H * Lk * n * d
+        return core
+
+    def min_bytes(self) -> int:
+        """Bytes a forward must move at least: Q, K, V and O once, plus tables."""
+        esz = 4 if self.dtype == "fp32" else 2
+        n = self.B * self.H * self.d * esz
+        b = n * (2 * self.Lq + 2 * self.Lk)
+        t0, t1 = self.table_shapes()
+        for shp, tsz in ((t0, 4 if self.mode == MODE_T5 else 2), (t1, 2)):
+            if shp is not None:
+                c = 1
+                for s in shp:
+                    c *= s
+                b += c * tsz
+        return b
+
+
+WORKLOADS = {
+    "t5_tiny_fp32": Workload("t5_tiny_fp32", 0, MODE_T5, "fp32", 1, 4, 128, 128, 64,
+                             num_buckets=32, rel_param=128, table_sigma=0.5),
+    "t5_base_bidir": Workload("t5_base_bidir", 1, MODE_T5, "bf16", 8, 12, 512, 512, 64,
+                              num_buckets=32, rel_param=128, table_sigma=0.5),
+    "t5_causal": Workload("t5_causal", 2, MODE_T5, "bf16", 4, 16, 2048, 2048, 64,
+                          num_buckets=32, rel_param=128, causal=True, table_sigma=0.5),
+    "t5_decode": Workload("t5_decode", 2, MODE_T5, "bf16", 32, 16, 1, 4096, 64,
+                          num_buckets=32, rel_param=128, causal=True, q_offset=4095,
+                          table_sigma=0.5),
+    "shaw": Workload("shaw", 3, MODE_SHAW, "bf16", 4, 8, 4096, 4096, 64,
+                     rel_param=16, table_sigma=0.1),
+    "deberta": Workload("deberta", 4, MODE_DEBERTA, "bf16", 8, 12, 2048, 2048, 64,
+                        rel_param=256, table_sigma=0.1),
+}
+
+
+def _dtype(name: str):
+    return {"bf16": torch.bfloat16, "fp32": torch.float32}[name]
+
+
+def make_inputs(w: Workload, seed: int | None = None):
+    """Draw the workload's inputs on the CPU.
+
+    Returns a dict with Q, K, V ([B,H,Lq|Lk,d], the workload dtype) and
+    table0 / table1 (T5: fp32 bias [num_buckets, H], table1 None; Shaw:
+    bf16 a_K, a_V [2k+1, d]; DeBERTa: bf16 Pk, Pq [2k, H, d]).
+    """
+    g = torch.Generator(device="cpu")
+    g.manual_seed(w.seed if seed is None else seed)
+    dt = _dtype(w.dtype)
+
+    def draw(shape, sigma, dtype):
+        x = torch.randn(*shape, generator=g, dtype=torch.float32)
+        if sigma != 1.0:
+            x.mul_(sigma)
+        return x.to(dtype)
+
+    q = draw((w.B, w.H, w.Lq, w.d), w.qkv_sigma, dt)
+    k = draw((w.B, w.H, w.Lk, w.d), w.qkv_sigma, dt)
+    v = draw((w.B, w.H, w.Lk, w.d), w.qkv_sigma, dt)
+    s0, s1 = w.table_shapes()
+    tdt0 = torch.float32 if w.mode == MODE_T5 else torch.bfloat16
+    t0 = draw(s0, w.table_sigma, tdt0)
+    t1 = draw(s1, w.table_sigma, torch.bfloat16) if s1 is not None else None
+    return {"Q": q, "K": k, "V": v, "table0": t0, "table1": t1}
