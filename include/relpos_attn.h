@@ -1,0 +1,143 @@
+/*
+ * relpos_attn.h -- C ABI of the GB300 (sm_103a) relative-position attention
+ * forward library (librelpos_attn.so).
+ *
+ * One call computes multi-head attention whose logits carry a relative-
+ * position term that is formed inside the kernel and never written to
+ * device memory as an L x L (or L x L x d) tensor:
+ *
+ *   RELPOS_T5      per-head scalar bias looked up by bucket of the offset
+ *                  key - query ("Relative Position Embeddings, in depth",
+ *                  section "T5: one scalar per head, looked up by bucket";
+ *                  "T5 Relative-Position Bias", bucket definition and the
+ *                  cached-decoder example).
+ *                  logit = q.k / sqrt(d) + bias[bucket(j - p)][h]
+ *   RELPOS_SHAW    clipped relative key and value vectors ("Relative
+ *                  Position Embeddings, in depth", section "Shaw et al.").
+ *                  logit = q.(k_j + a_K[clip(j - p, -k, k) + k]) / sqrt(d)
+ *                  out   = sum_j softmax_j * (v_j + a_V[clip(j - p, -k, k) + k])
+ *   RELPOS_DEBERTA disentangled content/position attention ("Relative
+ *                  Position Embeddings, in depth", section "DeBERTa:
+ *                  disentangled content and position"; "DeBERTa > Relative
+ *                  Position Encoding", section "The Relative Position
+ *                  Formula" for delta).
+ *                  logit = (q_i.k_j + q_i.Pk[delta(p, j)] + k_j.Pq[delta(j, p)])
+ *                          / sqrt(3d),  delta(a, b) = clip(a - b, -k, k - 1) + k
+ *
+ * Positions: query row i sits at absolute position p = i + q_offset; key
+ * row j at position j. With causal = 1 keys j > p are masked out (and T5
+ * uses its causal bucket mapping). A query row with no visible key gets a
+ * zero output row.
+ *
+ * Conventions shared by every entry point:
+ *  - Pointers marked "device" are CUDA device pointers owned by the caller;
+ *    the library keeps no reference to them after the call returns.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream). Calls are
+ *    asynchronous on that stream unless stated otherwise.
+ *  - Return value: RELPOS_OK (0) or a negative RELPOS_ERR_* code; argument
+ *    errors are reported before anything is launched. relpos_strerror()
+ *    names a code. No entry point falls back to a CPU path.
+ */
+#ifndef RELPOS_ATTN_H_
+#define RELPOS_ATTN_H_
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* modes */
+#define RELPOS_T5 0
+#define RELPOS_SHAW 1
+#define RELPOS_DEBERTA 2
+
+/* element types of Q, K, V and out */
+#define RELPOS_BF16 0
+#define RELPOS_FP32 1
+
+/* return codes */
+#define RELPOS_OK 0
+#define RELPOS_ERR_INVALID_ARG (-1)    /* null pointer, bad size or parameter */
+#define RELPOS_ERR_UNSUPPORTED (-2)    /* valid request this build does not run (d != 64, ...) */
+#define RELPOS_ERR_CUDA (-3)           /* a CUDA runtime call or launch failed */
+#define RELPOS_ERR_DEVICE_TIMEOUT (-4) /* a kernel gave up on a bounded wait */
+
+/*
+ * relpos_attn_fwd -- attention forward with an in-kernel relative term.
+ *
+ *   mode        RELPOS_T5, RELPOS_SHAW or RELPOS_DEBERTA.
+ *   dtype       RELPOS_BF16 or RELPOS_FP32: element type of Q, K, V and out.
+ *               FP32 inputs are rounded to bf16 on the device before the
+ *               tensor-core products (fp32 accumulation); out is fp32.
+ *   Q           device, [B, H, Lq, d] row-major.
+ *   K, V        device, [B, H, Lk, d] row-major.
+ *   table0/1    device tables, row-major:
+ *                 T5:      table0 = bias [num_buckets, H] fp32; table1 unused.
+ *                 Shaw:    table0 = a_K, table1 = a_V, each [2k+1, d] bf16,
+ *                          shared by all heads.
+ *                 DeBERTa: table0 = Pk, table1 = Pq, each [2k, H, d] bf16
+ *                          (already projected per head).
+ *   B, H        batch and heads (>= 0; 0 makes the call a no-op).
+ *   Lq, Lk      query and key lengths (Lq >= 0, Lk >= 0). Lk == 0 writes
+ *               zeros.
+ *   d           head dimension; this build supports d = 64.
+ *   num_buckets T5 only: even, 4 <= num_buckets <= 128.
+ *   rel_param   T5: max_distance (> num_buckets/4 bidirectional, > num_buckets/2
+ *               causal); Shaw: clip k (1 <= k <= 64); DeBERTa: k (1 <= k <= 4096).
+ *   causal      0 or 1.
+ *   q_offset    absolute position of query row 0 (>= 0), for cached decoding.
+ *   out         device, [B, H, Lq, d], element type per dtype; written fully.
+ *   stream      cudaStream_t.
+ *
+ * Scratch: calls with dtype FP32, with DeBERTa, or that take the split-key
+ * decode path (few query rows) draw temporary device memory with
+ * cudaMallocAsync on `stream` and release it with cudaFreeAsync before
+ * returning. Nothing persists between calls.
+ * Errors: RELPOS_ERR_INVALID_ARG / _UNSUPPORTED before launch;
+ * RELPOS_ERR_CUDA if a launch or allocation fails. Device-side bounded-wait
+ * failures are reported by relpos_check_status().
+ */
+int relpos_attn_fwd(int mode, int dtype, const void* Q, const void* K, const void* V,
+                    const void* table0, const void* table1, int B, int H, int Lq, int Lk,
+                    int d, int num_buckets, int rel_param, int causal, int q_offset,
+                    void* out, void* stream);
+
+/*
+ * relpos_index_ids -- test hook: the device index generator the kernels use,
+ * run over n consecutive offsets rel_first .. rel_first + n - 1.
+ *
+ *   T5:      offsets are key - query; ids are buckets ("T5: one scalar per
+ *            head, looked up by bucket"); causal selects the causal mapping.
+ *   Shaw:    offsets are key - query; ids are clip(rel, -k, k) + k.
+ *   DeBERTa: offsets are query - key; ids are delta = clip(rel, -k, k-1) + k.
+ *   out_dev  device int32[n], written asynchronously on `stream`.
+ * Parameter checks are those of relpos_attn_fwd.
+ */
+int relpos_index_ids(int mode, int n, int rel_first, int num_buckets, int rel_param,
+                     int causal, int* out_dev, void* stream);
+
+/*
+ * relpos_check_status -- synchronize `stream` and report whether any kernel
+ * of this library hit a bounded-wait limit since the last check
+ * (RELPOS_ERR_DEVICE_TIMEOUT), or a CUDA error (RELPOS_ERR_CUDA). Clears the
+ * recorded device status. Blocking.
+ */
+int relpos_check_status(void* stream);
+
+/* relpos_strerror -- static description of a return code; never NULL. */
+const char* relpos_strerror(int code);
+
+/*
+ * relpos_selftest_wait_timeout -- runs one tiny kernel that waits, with a
+ * limit of `timeout_us` microseconds (1 .. 1000000), on a barrier that
+ * nothing completes, exactly as the attention kernels' waits do. It records
+ * RELPOS_ERR_DEVICE_TIMEOUT in the device status word and returns; the
+ * context stays usable. Used to test the failure path without faulting or
+ * hanging the GPU. Asynchronous; read the result with relpos_check_status().
+ */
+int relpos_selftest_wait_timeout(int timeout_us, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RELPOS_ATTN_H_ */

@@ -1,0 +1,149 @@
+"""Relative-position attention forward for GB300 (sm_103a).
+
+A thin ctypes binding over ``librelpos_attn.so`` (C ABI in
+``include/relpos_attn.h``). The functions named like the C entry points pass
+their arguments through unchanged; ``attention`` and ``index_ids`` only
+marshal torch tensors (device pointers, the current CUDA stream) and
+allocate the output. Every step of the computation runs in the library's
+CUDA kernels; there is no other backend. If the library has not been built
+(``transformer_attention_relative_gb300.build.build()``), every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from .workloads import MODE_DEBERTA, MODE_SHAW, MODE_T5  # noqa: F401
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "librelpos_attn.so")
+
+RELPOS_BF16, RELPOS_FP32 = 0, 1
+RELPOS_OK = 0
+RELPOS_ERR_INVALID_ARG = -1
+RELPOS_ERR_UNSUPPORTED = -2
+RELPOS_ERR_CUDA = -3
+RELPOS_ERR_DEVICE_TIMEOUT = -4
+
+EXPORTED = ("relpos_attn_fwd", "relpos_index_ids", "relpos_check_status", "relpos_strerror",
+            "relpos_selftest_wait_timeout")
+
+_lib = None
+
+
+class RelposError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {strerror(code)} ({code})")
+        self.code = code
+
+
+def load_library(path: str = LIB_PATH):
+    """Load the shared library (once) and declare the C signatures."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with "
+                           "transformer_attention_relative_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    vp, i = ctypes.c_void_p, ctypes.c_int
+    lib.relpos_attn_fwd.argtypes = [i, i, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, i, vp, vp]
+    lib.relpos_attn_fwd.restype = i
+    lib.relpos_index_ids.argtypes = [i, i, i, i, i, i, vp, vp]
+    lib.relpos_index_ids.restype = i
+    lib.relpos_check_status.argtypes = [vp]
+    lib.relpos_check_status.restype = i
+    lib.relpos_strerror.argtypes = [i]
+    lib.relpos_strerror.restype = ctypes.c_char_p
+    lib.relpos_selftest_wait_timeout.argtypes = [i, vp]
+    lib.relpos_selftest_wait_timeout.restype = i
+    _lib = lib
+    return lib
+
+
+# ---------------------------------------------------------------- raw C entry points
+
+def relpos_attn_fwd(mode, dtype, Q, K, V, table0, table1, B, H, Lq, Lk, d, num_buckets,
+                    rel_param, causal, q_offset, out, stream) -> int:
+    return load_library().relpos_attn_fwd(mode, dtype, Q, K, V, table0, table1, B, H, Lq, Lk, d,
+                                          num_buckets, rel_param, causal, q_offset, out, stream)
+
+
+def relpos_index_ids(mode, n, rel_first, num_buckets, rel_param, causal, out_dev, stream) -> int:
+    return load_library().relpos_index_ids(mode, n, rel_first, num_buckets, rel_param, causal,
+                                           out_dev, stream)
+
+
+def relpos_check_status(stream) -> int:
+    return load_library().relpos_check_status(stream)
+
+
+def relpos_strerror(code: int) -> str:
+    return load_library().relpos_strerror(code).decode()
+
+
+def relpos_selftest_wait_timeout(timeout_us: int, stream) -> int:
+    return load_library().relpos_selftest_wait_timeout(timeout_us, stream)
+
+
+strerror = relpos_strerror
+
+
+# ---------------------------------------------------------------- torch marshalling
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def attention(Q, K, V, table0, table1=None, *, mode: int = MODE_T5, num_buckets: int = 32,
+              rel_param: int = 128, causal: bool = False, q_offset: int = 0, out=None,
+              stream=None):
+    """Run ``relpos_attn_fwd`` on CUDA tensors; returns ``out`` ([B,H,Lq,64]).
+
+    Q [B,H,Lq,64] and K, V [B,H,Lk,64] are bf16 (or all fp32); tables as in
+    the C header. ``out`` is allocated like Q when not given.
+    """
+    import torch
+    B, H, Lq, d = Q.shape
+    Lk = K.shape[2]
+    if Q.dtype == torch.bfloat16:
+        dtype = RELPOS_BF16
+    elif Q.dtype == torch.float32:
+        dtype = RELPOS_FP32
+    else:
+        raise TypeError(f"unsupported dtype {Q.dtype}")
+    for t in (Q, K, V, table0, table1, out):
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("tensors must be contiguous CUDA tensors")
+    if out is None:
+        out = torch.empty_like(Q)
+    rc = relpos_attn_fwd(mode, dtype, _ptr(Q), _ptr(K), _ptr(V), _ptr(table0), _ptr(table1),
+                         B, H, Lq, Lk, d, num_buckets, rel_param, int(causal), q_offset,
+                         _ptr(out), _stream(stream))
+    if rc != RELPOS_OK:
+        raise RelposError(rc, "relpos_attn_fwd")
+    return out
+
+
+def index_ids(mode: int, rel_first: int, n: int, *, num_buckets: int = 32, rel_param: int = 128,
+              causal: bool = False, device="cuda", stream=None):
+    """Device index ids for offsets rel_first .. rel_first + n - 1 (int32 tensor)."""
+    import torch
+    out = torch.empty(n, dtype=torch.int32, device=device)
+    rc = relpos_index_ids(mode, n, rel_first, num_buckets, rel_param, int(causal), _ptr(out),
+                          _stream(stream))
+    if rc != RELPOS_OK:
+        raise RelposError(rc, "relpos_index_ids")
+    return out
+
+
+def check_status(stream=None) -> int:
+    """Synchronise and return the library's device status code (0 = ok)."""
+    return relpos_check_status(_stream(stream))

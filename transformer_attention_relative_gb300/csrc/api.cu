@@ -1,0 +1,379 @@
+// api.cu -- the C ABI (include/relpos_attn.h): argument checks, the T5
+// bucket thresholds, TMA descriptors, scratch management and dispatch to the
+// fused prefill kernel or the split-key decode kernel.
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/relpos_attn.h"
+#include "ptx.cuh"
+#include "relpos_common.cuh"
+#include "relpos_internal.h"
+
+namespace relpos {
+namespace {
+
+// Device status word: kernels record the first bounded-wait failure here.
+__device__ int g_status;
+
+constexpr int kMaxDevices = 64;
+int* g_status_ptr[kMaxDevices];
+std::mutex g_status_mu;
+
+int* status_ptr() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_status_mu);
+  if (!g_status_ptr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_status) != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = static_cast<int*>(ptr);
+  }
+  return g_status_ptr[dev];
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
+}
+
+// [rows = L, inner = 64] bf16 per (batch*head) slab, 128-row x 64-col boxes,
+// 128-byte swizzle (the operand layout of the tensor-core descriptors).
+bool make_tmap(CUtensorMap* m, const void* base, int L, int BH) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(L),
+                        static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim) * 2,
+                           static_cast<cuuint64_t>(L) * kHeadDim * 2};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(kHeadDim), 128u, 1u};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Thresholds of the T5 log buckets: thr[q] is the smallest distance n whose
+// bucket within a half is >= exact + q + 1, found by evaluating the pages'
+// formula exact + int(log(n / exact) / log(max_distance / exact) * (S - exact))
+// in double precision for n = exact, exact + 1, ... up to saturation or nmax.
+// R is the first distance of the last bucket (nmax + 1 if not reached).
+int t5_setup(int num_buckets, int max_distance, int causal, long long nmax, T5Index* ix, int* R) {
+  std::memset(ix, 0, sizeof(*ix));
+  ix->bidir = causal ? 0 : 1;
+  ix->slots = causal ? num_buckets : num_buckets / 2;
+  ix->exact = ix->slots / 2;
+  ix->nthr = ix->slots - ix->exact - 1;
+  for (int q = 0; q < kMaxT5Thresholds; ++q) ix->thr[q] = INT_MAX;
+  if (ix->nthr == 0) {
+    *R = ix->exact;
+    return RELPOS_OK;
+  }
+  const int S = ix->slots, E = ix->exact;
+  const double denom = std::log(static_cast<double>(max_distance) / static_cast<double>(E));
+  int cur = E;
+  for (long long n = E; n <= nmax && cur < S - 1; ++n) {
+    const double v = std::log(static_cast<double>(n) / static_cast<double>(E)) / denom *
+                     static_cast<double>(S - E);
+    long long large = E + static_cast<long long>(v);
+    if (large > S - 1) large = S - 1;
+    if (large < cur) return RELPOS_ERR_UNSUPPORTED;  // log not monotone here
+    while (cur < large) {
+      ++cur;
+      ix->thr[cur - E - 1] = static_cast<int>(n);
+    }
+  }
+  *R = (cur == S - 1) ? ix->thr[ix->nthr - 1] : static_cast<int>(nmax + 1);
+  return RELPOS_OK;
+}
+
+int check_rel_params(int mode, int num_buckets, int rel_param, int causal) {
+  if (causal != 0 && causal != 1) return RELPOS_ERR_INVALID_ARG;
+  if (mode == RELPOS_T5) {
+    if (num_buckets < 4 || num_buckets > 128 || (num_buckets & 1)) return RELPOS_ERR_INVALID_ARG;
+    const int S = causal ? num_buckets : num_buckets / 2;
+    if (rel_param <= S / 2) return RELPOS_ERR_INVALID_ARG;  // log(max_distance / exact) <= 0
+  } else if (mode == RELPOS_SHAW || mode == RELPOS_DEBERTA) {
+    if (rel_param < 1) return RELPOS_ERR_INVALID_ARG;
+    if (rel_param > (1 << 24)) return RELPOS_ERR_UNSUPPORTED;
+  } else {
+    return RELPOS_ERR_INVALID_ARG;
+  }
+  return RELPOS_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+__global__ void index_ids_kernel(int mode, int n, int first, T5Index ix, int k, int* out) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const int rel = first + i;
+  int id;
+  if (mode == RELPOS_T5)
+    id = t5_bucket_dev(rel, ix);
+  else if (mode == RELPOS_SHAW)
+    id = shaw_index_dev(rel, k);
+  else
+    id = deberta_delta_dev(rel, k);
+  out[i] = id;
+}
+
+__global__ void selftest_wait_kernel(unsigned long long limit_ns, int* status) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // nothing ever arrives: phase 0 cannot complete
+    if (!mbar_wait(smem_u32(&bar), 0, limit_ns)) atomicCAS(status, 0, RELPOS_ERR_DEVICE_TIMEOUT);
+  }
+}
+
+__global__ void f32_to_bf16_kernel(const float4* __restrict__ in, uint2* __restrict__ out, size_t n4) {
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n4;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const float4 v = in[i];
+    uint2 o;
+    o.x = pack_bf16x2(v.x, v.y);
+    o.y = pack_bf16x2(v.z, v.w);
+    out[i] = o;
+  }
+}
+
+cudaError_t to_bf16(const void* src, void* dst, size_t n, cudaStream_t s) {
+  const size_t n4 = n / 4;  // n is a multiple of 64
+  int blocks = static_cast<int>((n4 + 255) / 256);
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  if (blocks < 1) blocks = 1;
+  f32_to_bf16_kernel<<<blocks, 256, 0, s>>>(static_cast<const float4*>(src), static_cast<uint2*>(dst),
+                                             n4);
+  return cudaGetLastError();
+}
+
+}  // namespace
+}  // namespace relpos
+
+using namespace relpos;
+
+extern "C" const char* relpos_strerror(int code) {
+  switch (code) {
+    case RELPOS_OK: return "ok";
+    case RELPOS_ERR_INVALID_ARG: return "invalid argument";
+    case RELPOS_ERR_UNSUPPORTED: return "unsupported by this build";
+    case RELPOS_ERR_CUDA: return "CUDA error";
+    case RELPOS_ERR_DEVICE_TIMEOUT: return "device-side bounded wait timed out";
+    default: return "unknown error";
+  }
+}
+
+extern "C" int relpos_index_ids(int mode, int n, int rel_first, int num_buckets, int rel_param,
+                                int causal, int* out_dev, void* stream) {
+  int rc = check_rel_params(mode, num_buckets, rel_param, causal);
+  if (rc != RELPOS_OK) return rc;
+  if (n < 0) return RELPOS_ERR_INVALID_ARG;
+  if (n == 0) return RELPOS_OK;
+  if (!out_dev) return RELPOS_ERR_INVALID_ARG;
+  const long long last = static_cast<long long>(rel_first) + n - 1;
+  if (rel_first < -(1 << 30) || last > (1 << 30)) return RELPOS_ERR_UNSUPPORTED;
+  T5Index ix;
+  std::memset(&ix, 0, sizeof(ix));
+  if (mode == RELPOS_T5) {
+    int R = 0;
+    const long long nmax = std::max(std::llabs(static_cast<long long>(rel_first)), std::llabs(last));
+    rc = t5_setup(num_buckets, rel_param, causal, nmax, &ix, &R);
+    if (rc != RELPOS_OK) return rc;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  index_ids_kernel<<<(n + 255) / 256, 256, 0, s>>>(mode, n, rel_first, ix, rel_param, out_dev);
+  return cudaGetLastError() == cudaSuccess ? RELPOS_OK : RELPOS_ERR_CUDA;
+}
+
+extern "C" int relpos_check_status(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return RELPOS_ERR_CUDA;
+  }
+  int* sp = status_ptr();
+  if (!sp) return RELPOS_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, sp, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return RELPOS_ERR_CUDA;
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(sp, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+      return RELPOS_ERR_CUDA;
+    return RELPOS_ERR_DEVICE_TIMEOUT;
+  }
+  return RELPOS_OK;
+}
+
+extern "C" int relpos_selftest_wait_timeout(int timeout_us, void* stream) {
+  if (timeout_us < 1 || timeout_us > 1000000) return RELPOS_ERR_INVALID_ARG;
+  int* sp = status_ptr();
+  if (!sp) return RELPOS_ERR_CUDA;
+  selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<unsigned long long>(timeout_us) * 1000ull, sp);
+  return cudaGetLastError() == cudaSuccess ? RELPOS_OK : RELPOS_ERR_CUDA;
+}
+
+extern "C" int relpos_attn_fwd(int mode, int dtype, const void* Q, const void* K, const void* V,
+                               const void* table0, const void* table1, int B, int H, int Lq, int Lk,
+                               int d, int num_buckets, int rel_param, int causal, int q_offset,
+                               void* out, void* stream) {
+  if (mode != RELPOS_T5 && mode != RELPOS_SHAW && mode != RELPOS_DEBERTA)
+    return RELPOS_ERR_INVALID_ARG;
+  if (dtype != RELPOS_BF16 && dtype != RELPOS_FP32) return RELPOS_ERR_INVALID_ARG;
+  if (B < 0 || H < 0 || Lq < 0 || Lk < 0 || q_offset < 0 || d <= 0) return RELPOS_ERR_INVALID_ARG;
+  int rc = check_rel_params(mode, num_buckets, rel_param, causal);
+  if (rc != RELPOS_OK) return rc;
+  if (d != kHeadDim) return RELPOS_ERR_UNSUPPORTED;
+  if (B == 0 || H == 0 || Lq == 0) return RELPOS_OK;
+  if (!Q || !out) return RELPOS_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * H > 65535) return RELPOS_ERR_UNSUPPORTED;
+  if (Lq > (1 << 24) || Lk > (1 << 24) || q_offset > (1 << 28)) return RELPOS_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t esz = dtype == RELPOS_FP32 ? 4 : 2;
+  const size_t BH = static_cast<size_t>(B) * H;
+  if (Lk == 0) {  // no key is visible: zero rows
+    return cudaMemsetAsync(out, 0, BH * Lq * kHeadDim * esz, s) == cudaSuccess ? RELPOS_OK
+                                                                                 : RELPOS_ERR_CUDA;
+  }
+  if (!K || !V || !table0) return RELPOS_ERR_INVALID_ARG;
+  if (mode != RELPOS_T5 && !table1) return RELPOS_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(out) || !aligned16(table0) ||
+      (table1 && !aligned16(table1)))
+    return RELPOS_ERR_INVALID_ARG;
+  if (mode == RELPOS_DEBERTA) return RELPOS_ERR_UNSUPPORTED;
+  if (mode == RELPOS_SHAW && rel_param > 24) return RELPOS_ERR_UNSUPPORTED;
+
+  int* status = status_ptr();
+  if (!status) return RELPOS_ERR_CUDA;
+
+  // relative-term setup
+  T5Index t5;
+  std::memset(&t5, 0, sizeof(t5));
+  int R = 0;
+  if (mode == RELPOS_T5) {
+    const long long nmax = std::max(static_cast<long long>(Lk) - 1,
+                                    static_cast<long long>(Lq) - 1 + q_offset);
+    rc = t5_setup(num_buckets, rel_param, causal, nmax, &t5, &R);
+    if (rc != RELPOS_OK) return rc;
+  }
+  const float scale = 1.0f / std::sqrt(static_cast<float>(mode == RELPOS_DEBERTA ? 3 * d : d));
+
+  // fp32 inputs: round to bf16 scratch first
+  void* scratch = nullptr;
+  const void* Qb = Q;
+  const void* Kb = K;
+  const void* Vb = V;
+  const size_t nq = BH * Lq * kHeadDim, nk = BH * Lk * kHeadDim;
+  auto fail = [&](int code) {
+    if (scratch) cudaFreeAsync(scratch, s);
+    cudaGetLastError();
+    return code;
+  };
+  const bool decode = (mode == RELPOS_T5 && Lq <= 8);
+  const int chunk = decode_chunk_keys();
+  const int nchunks = (Lk + chunk - 1) / chunk;
+  size_t scratch_bytes = 0, off_conv = 0, off_part = 0;
+  if (dtype == RELPOS_FP32) {
+    off_conv = scratch_bytes;
+    scratch_bytes += (nq + 2 * nk) * 2;
+  }
+  if (decode) {
+    scratch_bytes = (scratch_bytes + 255) & ~static_cast<size_t>(255);
+    off_part = scratch_bytes;
+    scratch_bytes += BH * Lq * nchunks * (kHeadDim + 2) * sizeof(float);
+  }
+  if (scratch_bytes) {
+    if (cudaMallocAsync(&scratch, scratch_bytes, s) != cudaSuccess) return fail(RELPOS_ERR_CUDA);
+  }
+  if (dtype == RELPOS_FP32) {
+    uint8_t* c = static_cast<uint8_t*>(scratch) + off_conv;
+    if (to_bf16(Q, c, nq, s) != cudaSuccess || to_bf16(K, c + nq * 2, nk, s) != cudaSuccess ||
+        to_bf16(V, c + (nq + nk) * 2, nk, s) != cudaSuccess)
+      return fail(RELPOS_ERR_CUDA);
+    Qb = c;
+    Kb = c + nq * 2;
+    Vb = c + (nq + nk) * 2;
+  }
+
+  if (decode) {
+    DecodeParams dp;
+    std::memset(&dp, 0, sizeof(dp));
+    dp.Q = static_cast<const __nv_bfloat16*>(Qb);
+    dp.K = static_cast<const __nv_bfloat16*>(Kb);
+    dp.V = static_cast<const __nv_bfloat16*>(Vb);
+    dp.bias = static_cast<const float*>(table0);
+    dp.B = B;
+    dp.H = H;
+    dp.Lq = Lq;
+    dp.Lk = Lk;
+    dp.causal = causal;
+    dp.q_offset = q_offset;
+    dp.scale_log2 = scale * kLog2e;
+    dp.chunk = chunk;
+    dp.nchunks = nchunks;
+    float* part = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + off_part);
+    dp.part_o = part;
+    dp.part_ml = part + BH * Lq * nchunks * kHeadDim;
+    dp.out = out;
+    dp.out_f32 = dtype == RELPOS_FP32;
+    dp.t5 = t5;
+    if (launch_decode(dp, s) != cudaSuccess) return fail(RELPOS_ERR_CUDA);
+  } else {
+    FwdParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.B = B;
+    p.H = H;
+    p.Lq = Lq;
+    p.Lk = Lk;
+    p.causal = causal;
+    p.q_offset = q_offset;
+    p.scale_log2 = scale * kLog2e;
+    p.out = out;
+    p.status = status;
+    p.kclip = rel_param;
+    if (mode == RELPOS_T5) {
+      p.bias = static_cast<const float*>(table0);
+      p.t5 = t5;
+      p.t5_R = R;
+      p.t5_tab_off = R + 254;
+      p.t5_tab_len = 2 * R + 509;
+    } else if (mode == RELPOS_SHAW) {
+      p.aK = static_cast<const __nv_bfloat16*>(table0);
+      p.aV = static_cast<const __nv_bfloat16*>(table1);
+    }
+    if (fwd_smem_bytes(mode, p) > fwd_max_smem_bytes()) return fail(RELPOS_ERR_UNSUPPORTED);
+    CUtensorMap tq, tk, tv, to;
+    if (!make_tmap(&tq, Qb, Lq, static_cast<int>(BH)) || !make_tmap(&tk, Kb, Lk, static_cast<int>(BH)) ||
+        !make_tmap(&tv, Vb, Lk, static_cast<int>(BH)) ||
+        !make_tmap(&to, dtype == RELPOS_FP32 ? Qb : out, Lq, static_cast<int>(BH)))
+      return fail(RELPOS_ERR_CUDA);
+    if (launch_fwd(mode, dtype == RELPOS_FP32, tq, tk, tv, to, p, s) != cudaSuccess)
+      return fail(RELPOS_ERR_CUDA);
+  }
+  if (scratch && cudaFreeAsync(scratch, s) != cudaSuccess) {
+    cudaGetLastError();
+    return RELPOS_ERR_CUDA;
+  }
+  return RELPOS_OK;
+}

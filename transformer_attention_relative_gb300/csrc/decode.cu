@@ -1,0 +1,187 @@
+// decode.cu -- T5-bias attention for a few query rows against a long key
+// cache (cached decoding: "T5 Relative-Position Bias", cached-decoder
+// example; "Relative Position Embeddings, in depth", "Kernels and the KV
+// cache"). With one query row per (batch, head) the work is a stream over K
+// and V (about one flop per byte), so it runs on CUDA cores, split over key
+// chunks so that every SM keeps many 16-byte loads in flight, followed by a
+// small combine of the per-chunk (max, sum, partial output).
+//
+// Query row i sits at absolute position i + q_offset; its offsets to key j
+// are j - (i + q_offset), bucketed by the same device generator the fused
+// kernel uses.
+
+#include <cuda_bf16.h>
+
+#include <cstdint>
+
+#include "ptx.cuh"
+#include "relpos_common.cuh"
+#include "relpos_internal.h"
+
+namespace relpos {
+namespace {
+
+constexpr int kDecThreads = 128;    // 16 groups of 8 threads; a group reads one 128-byte key row
+constexpr int kDecChunk = 256;      // keys per CTA
+constexpr int kKeysPerThread = kDecChunk / 16;
+
+RP_DEVI void bf16x8_to_f32(const uint4& u, float (&f)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 v = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
+    f[2 * e] = v.x;
+    f[2 * e + 1] = v.y;
+  }
+}
+
+__global__ void __launch_bounds__(kDecThreads) relpos_decode_partial_kernel(const DecodeParams p) {
+  const int chunk = blockIdx.x;
+  const int qi = blockIdx.y;
+  const int bh = blockIdx.z;
+  const int h = bh % p.H;
+  const int tid = threadIdx.x;
+  const int grp = tid >> 3;  // 0..15: key row within a 16-row slab
+  const int sl = tid & 7;    // 8-dim slice of the head dimension
+  const int warp = tid >> 5;
+
+  __shared__ float bias_s[128];
+  __shared__ float red_s[4];
+  __shared__ float o_s[4][kHeadDim];
+
+  const int pos = qi + p.q_offset;
+  const int jb = chunk * kDecChunk;
+  int je = min(p.Lk, jb + kDecChunk);
+  if (p.causal) je = min(je, pos + 1);
+
+  const size_t row_out = static_cast<size_t>(bh) * p.Lq + qi;
+  float* po = p.part_o + (row_out * p.nchunks + chunk) * kHeadDim;
+  float* pml = p.part_ml + (row_out * p.nchunks + chunk) * 2;
+
+  if (jb >= je) {  // nothing visible in this chunk
+    if (tid < kHeadDim) po[tid] = 0.f;
+    if (tid == 0) {
+      pml[0] = -INFINITY;
+      pml[1] = 0.f;
+    }
+    return;
+  }
+
+  const int nb = p.t5.bidir ? 2 * p.t5.slots : p.t5.slots;
+  for (int b = tid; b < nb; b += kDecThreads) bias_s[b] = __ldg(p.bias + b * p.H + h) * kLog2e;
+
+  // issue every K and V load of this thread first
+  const uint4* kbase = reinterpret_cast<const uint4*>(p.K + static_cast<size_t>(bh) * p.Lk * kHeadDim);
+  const uint4* vbase = reinterpret_cast<const uint4*>(p.V + static_cast<size_t>(bh) * p.Lk * kHeadDim);
+  uint4 kv[kKeysPerThread], vv[kKeysPerThread];
+#pragma unroll
+  for (int r = 0; r < kKeysPerThread; ++r) {
+    const int j = jb + grp + 16 * r;
+    if (j < je) {
+      kv[r] = __ldg(kbase + static_cast<size_t>(j) * 8 + sl);
+      vv[r] = __ldg(vbase + static_cast<size_t>(j) * 8 + sl);
+    } else {
+      kv[r] = make_uint4(0, 0, 0, 0);
+      vv[r] = make_uint4(0, 0, 0, 0);
+    }
+  }
+  float qf[8];
+  {
+    const uint4 qv = __ldg(reinterpret_cast<const uint4*>(p.Q + row_out * kHeadDim) + sl);
+    bf16x8_to_f32(qv, qf);
+  }
+  __syncthreads();  // bias_s
+
+  float s[kKeysPerThread];
+  float mx = -INFINITY;
+#pragma unroll
+  for (int r = 0; r < kKeysPerThread; ++r) {
+    float kf[8];
+    bf16x8_to_f32(kv[r], kf);
+    float acc = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc = fmaf(qf[e], kf[e], acc);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+    const int j = jb + grp + 16 * r;
+    const float bias = bias_s[t5_bucket_dev(j - pos, p.t5)];
+    s[r] = (j < je) ? fmaf(acc, p.scale_log2, bias) : -INFINITY;
+    mx = fmaxf(mx, s[r]);
+  }
+  // max over the CTA (groups within a warp differ in lanes 8, 16)
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+  if ((tid & 31) == 0) red_s[warp] = mx;
+  __syncthreads();
+  mx = fmaxf(fmaxf(red_s[0], red_s[1]), fmaxf(red_s[2], red_s[3]));
+  __syncthreads();
+
+  float sum = 0.f;
+  float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int r = 0; r < kKeysPerThread; ++r) {
+    const float pr = ex2_approx(s[r] - mx);
+    sum += pr;
+    float vf[8];
+    bf16x8_to_f32(vv[r], vf);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) o[e] = fmaf(pr, vf[e], o[e]);
+  }
+  sum += __shfl_xor_sync(0xffffffffu, sum, 8);
+  sum += __shfl_xor_sync(0xffffffffu, sum, 16);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    o[e] += __shfl_xor_sync(0xffffffffu, o[e], 8);
+    o[e] += __shfl_xor_sync(0xffffffffu, o[e], 16);
+  }
+  if ((tid & 31) < 8) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) o_s[warp][sl * 8 + e] = o[e];
+  }
+  if ((tid & 31) == 0) red_s[warp] = sum;
+  __syncthreads();
+  if (tid < kHeadDim) po[tid] = (o_s[0][tid] + o_s[1][tid]) + (o_s[2][tid] + o_s[3][tid]);
+  if (tid == 0) {
+    pml[0] = mx;
+    pml[1] = (red_s[0] + red_s[1]) + (red_s[2] + red_s[3]);
+  }
+}
+
+// one warp per (row, 64 dims): merge the per-chunk partials
+__global__ void __launch_bounds__(64) relpos_decode_combine_kernel(const DecodeParams p) {
+  const size_t row = blockIdx.x;
+  const int d = threadIdx.x;
+  const float* ml = p.part_ml + row * p.nchunks * 2;
+  const float* po = p.part_o + row * p.nchunks * kHeadDim;
+  float M = -INFINITY;
+  for (int c = 0; c < p.nchunks; ++c) M = fmaxf(M, ml[2 * c]);
+  float l = 0.f, acc = 0.f;
+  if (M != -INFINITY) {
+    for (int c = 0; c < p.nchunks; ++c) {
+      const float w = ex2_approx(ml[2 * c] - M);
+      l = fmaf(w, ml[2 * c + 1], l);
+      acc = fmaf(w, po[c * kHeadDim + d], acc);
+    }
+  }
+  const float r = l > 0.f ? acc / l : 0.f;
+  if (p.out_f32)
+    static_cast<float*>(p.out)[row * kHeadDim + d] = r;
+  else
+    static_cast<__nv_bfloat16*>(p.out)[row * kHeadDim + d] = __float2bfloat16_rn(r);
+}
+
+}  // namespace
+
+int decode_chunk_keys() { return kDecChunk; }
+
+cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream) {
+  dim3 grid(p.nchunks, p.Lq, p.B * p.H);
+  relpos_decode_partial_kernel<<<grid, kDecThreads, 0, stream>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  relpos_decode_combine_kernel<<<p.B * p.H * p.Lq, kHeadDim, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace relpos

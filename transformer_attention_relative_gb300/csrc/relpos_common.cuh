@@ -1,0 +1,95 @@
+// relpos_common.cuh -- parameter blocks shared by the host launchers and the
+// kernels, and the device index generator (offset -> T5 bucket, Shaw clipped
+// row, DeBERTa delta) that every kernel and the index test hook call.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cstdint>
+
+namespace relpos {
+
+constexpr int kHeadDim = 64;
+constexpr int kMaxT5Thresholds = 64;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// T5 bucket generator ("Relative Position Embeddings, in depth", section
+// "T5: one scalar per head, looked up by bucket"; "T5 Relative-Position
+// Bias"). The host derives, once per call, the smallest distance at which
+// each logarithmic bucket begins (thr[]), by evaluating the pages' double-
+// precision log formula; the device then needs integer compares only, so
+// its ids equal the formula's exactly.
+struct T5Index {
+  int bidir;   // 1: bidirectional (upper half for keys after the query)
+  int slots;   // slots per direction: num_buckets / 2 (bidir) or num_buckets
+  int exact;   // slots / 2 distances with a bucket each
+  int nthr;    // slots - exact - 1 thresholds
+  int thr[kMaxT5Thresholds];  // thr[q]: first distance with bucket >= exact + q + 1
+};
+
+__host__ __device__ inline int t5_bucket_dev(int rel, const T5Index& ix) {
+  int base = 0, n;
+  if (ix.bidir) {
+    base = rel > 0 ? ix.slots : 0;
+    n = rel < 0 ? -rel : rel;
+  } else {
+    n = rel < 0 ? -rel : 0;
+  }
+  if (n < ix.exact) return base + n;
+  int b = ix.exact;
+  for (int q = 0; q < ix.nthr; ++q) b += (n >= ix.thr[q]) ? 1 : 0;
+  return base + b;
+}
+
+// Shaw ("Relative Position Embeddings, in depth", section "Shaw et al."):
+// offset key - query clipped to [-k, k], shifted to a row in [0, 2k].
+__host__ __device__ inline int shaw_index_dev(int rel, int k) {
+  int c = rel < -k ? -k : (rel > k ? k : rel);
+  return c + k;
+}
+
+// DeBERTa ("DeBERTa > Relative Position Encoding", section "The Relative
+// Position Formula"): r = i - j clipped to [-k, k - 1], shifted by k.
+__host__ __device__ inline int deberta_delta_dev(int r, int k) {
+  int c = r < -k ? -k : (r > k - 1 ? k - 1 : r);
+  return c + k;
+}
+
+struct FwdParams {
+  int B, H, Lq, Lk;
+  int causal, q_offset;
+  float scale_log2;  // softmax scale times log2(e)
+  void* out;
+  int* status;
+  // T5
+  const float* bias;  // [num_buckets, H]
+  int t5_R;           // |offset| >= R: the side's last bucket (no ordering left)
+  int t5_tab_len;     // entries of the per-head bias-by-offset table
+  int t5_tab_off;     // table index of offset 0
+  T5Index t5;
+  // Shaw
+  const __nv_bfloat16* aK;  // [2k+1, 64]
+  const __nv_bfloat16* aV;  // [2k+1, 64]
+  // DeBERTa
+  const __nv_bfloat16* Pk;  // [2k, H, 64]
+  const __nv_bfloat16* Pq;  // [2k, H, 64]
+  int kclip;                // Shaw / DeBERTa clip k
+};
+
+struct DecodeParams {
+  const __nv_bfloat16* Q;
+  const __nv_bfloat16* K;
+  const __nv_bfloat16* V;
+  const float* bias;
+  int B, H, Lq, Lk;
+  int causal, q_offset;
+  float scale_log2;
+  int chunk;     // keys per partial
+  int nchunks;
+  float* part_o;   // [B*H*Lq, nchunks, 64]
+  float* part_ml;  // [B*H*Lq, nchunks, 2]
+  void* out;
+  int out_f32;
+  T5Index t5;
+};
+
+}  // namespace relpos

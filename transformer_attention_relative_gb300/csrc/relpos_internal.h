@@ -1,0 +1,22 @@
+// relpos_internal.h -- launchers shared between the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "relpos_common.cuh"
+
+namespace relpos {
+
+uint32_t fwd_smem_bytes(int mode, const FwdParams& p);
+uint32_t fwd_max_smem_bytes();
+cudaError_t launch_fwd(int mode, bool out_f32, const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                       const CUtensorMap& tmV, const CUtensorMap& tmO, const FwdParams& p,
+                       cudaStream_t stream);
+
+int decode_chunk_keys();
+cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);
+
+}  // namespace relpos
