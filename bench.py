@@ -1,0 +1,491 @@
+#!/usr/bin/env python3
+"""Benchmark of the relative-position attention forward on GB300.
+
+One step = one forward (relpos_attn_fwd through the C ABI) over one batch of
+the workload. Default workload: the T5-base-shaped encoder (B=8, H=12,
+L=512, d=64, bf16, bidirectional buckets 32 / max distance 128). Prints one
+JSON line (rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference] [--no-others]
+
+Timing: W untimed steps, then K steps bracketed by a barrier and a device
+synchronize, timed with CUDA events on the launching stream. Consecutive
+steps rotate over several copies of the inputs whose total exceeds the L2
+cache, so every step reads its operands from HBM. SM clocks and throttle
+reasons are sampled with nvidia-smi while the steps run.
+
+Multi-GPU (torchrun): every rank runs an independent replica of the workload
+(the (batch, head) units are independent; there is no exchange step), the
+barrier is the only collective, and the value is the units of all ranks
+divided by the slowest rank's time (weak scaling).
+
+--impl reference times the fp64 CPU oracle on the host cores over a bounded
+sample of the same workload (the reference arm of this comparison).
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from transformer_attention_relative_gb300.workloads import (MODE_NAMES, MODE_T5,  # noqa: E402
+                                                            WORKLOADS, make_inputs)
+
+L2_BYTES = 129 * 1024 * 1024
+METRIC = "rel-pos attention fwd TFLOP/s (bf16) and % of GB300 dense BF16 peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ---------------------------------------------------------------- helpers
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def source_hash():
+    """Hash of the CUDA sources, to tell whether stored ncu counters are current."""
+    csrc = os.path.join(ROOT, "transformer_attention_relative_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(f.encode())
+                h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(kernel, workload):
+    """dram bytes per launch from profiles/traffic.txt if taken on these sources."""
+    p = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(p):
+        return None
+    want = source_hash()
+    with open(p) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 4 and not line.startswith("#"):
+                k, w, hsh, b = parts[:4]
+                if k == kernel and w == workload and hsh == want:
+                    return float(b)
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling in the background."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.samples = []   # (t, sm, max, hw, hw_thermal, sw_thermal, power_cap)
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.gpu)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                self.samples.append((time.time(), float(f[1]), float(f[2]),
+                                     f[5] == "Active", f[6] == "Active", f[7] == "Active",
+                                     f[8] == "Active"))
+            except ValueError:
+                pass
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0, t1):
+        win = [s for s in self.samples if t0 <= s[0] <= t1]
+        if not win:
+            return None
+        reasons = set()
+        for s in win:
+            for flag, name in zip(s[3:], ("hw_slowdown", "hw_thermal_slowdown",
+                                           "sw_thermal_slowdown", "sw_power_cap")):
+                if flag:
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(s[1] for s in win),
+                "sm_max_mhz": max(s[2] for s in win), "reasons": sorted(reasons),
+                "samples": len(win)}
+
+
+def kernels_per_step(w):
+    decode = w.mode == MODE_T5 and w.Lq <= 8
+    n = 2 if decode else 1
+    if w.dtype == "fp32":
+        n += 3
+    return n
+
+
+def dominant_kernel(w):
+    if w.mode == MODE_T5 and w.Lq <= 8:
+        return "relpos_decode_partial_kernel", "hbm"
+    return "relpos_fwd_kernel", "tensor"
+
+
+# ---------------------------------------------------------------- GPU arm
+
+class GpuRun:
+    def __init__(self, w, device, stream):
+        import torch
+        import transformer_attention_relative_gb300 as rp
+        self.rp = rp
+        self.w = w
+        self.device = device
+        self.stream = stream
+        x = make_inputs(w)
+        self.host = x
+        set_bytes = sum(t.numel() * t.element_size() for t in x.values() if t is not None)
+        out_bytes = x["Q"].numel() * x["Q"].element_size()
+        self.set_bytes = set_bytes + out_bytes
+        self.nsets = max(1, min(16, math.ceil(2.5 * L2_BYTES / self.set_bytes)))
+        self.sets = []
+        for _ in range(self.nsets):
+            d = {k: (v.to(device) if v is not None else None) for k, v in x.items()}
+            d["out"] = torch.empty_like(d["Q"])
+            self.sets.append(d)
+        torch.cuda.synchronize()
+        self.sptr = ctypes.c_void_p(stream.cuda_stream)
+        self.dtype = 1 if w.dtype == "fp32" else 0
+
+    def _call(self, d, out=None):
+        w = self.w
+        p = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())  # noqa: E731
+        rc = self.rp.relpos_attn_fwd(w.mode, self.dtype, p(d["Q"]), p(d["K"]), p(d["V"]),
+                                     p(d["table0"]), p(d["table1"]), w.B, w.H, w.Lq, w.Lk, w.d,
+                                     w.num_buckets, w.rel_param, int(w.causal), w.q_offset,
+                                     p(out if out is not None else d["out"]), self.sptr)
+        if rc != 0:
+            raise RuntimeError(f"relpos_attn_fwd failed: {rc}")
+
+    def step(self, i):
+        self._call(self.sets[i % self.nsets])
+
+    def timed(self, steps, warmup, barrier):
+        import torch
+        for i in range(warmup):
+            self.step(i)
+        torch.cuda.synchronize()
+        barrier()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        t0 = time.time()
+        e0.record(self.stream)
+        for i in range(steps):
+            self.step(i)
+        e1.record(self.stream)
+        torch.cuda.synchronize()
+        t1 = time.time()
+        barrier()
+        ms = e0.elapsed_time(e1)
+        return ms, t0, t1
+
+    def sustain(self, seconds):
+        """Run steps back to back for about `seconds` (clock sampling window)."""
+        import torch
+        t0 = time.time()
+        n = 0
+        while time.time() - t0 < seconds:
+            for _ in range(50):
+                self.step(n)
+                n += 1
+            torch.cuda.synchronize()
+        return t0, time.time()
+
+    def e2e(self, steps, warmup):
+        """Same metric through the public call with host buffers: every step copies
+        its inputs from pinned host memory and reads the output back."""
+        import torch
+        pinned = {k: (v.pin_memory() if v is not None else None) for k, v in self.host.items()}
+        out_h = torch.empty(self.host["Q"].shape, dtype=self.host["Q"].dtype).pin_memory()
+        d = self.sets[0]
+        h2d = sum(v.numel() * v.element_size() for v in pinned.values() if v is not None)
+        d2h = out_h.numel() * out_h.element_size()
+
+        def one():
+            with torch.cuda.stream(self.stream):
+                for k, v in pinned.items():
+                    if v is not None:
+                        d[k].copy_(v, non_blocking=True)
+                self._call(d)
+                out_h.copy_(d["out"], non_blocking=True)
+
+        for _ in range(warmup):
+            one()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(self.stream)
+        for _ in range(steps):
+            one()
+        e1.record(self.stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1), h2d, d2h
+
+
+def measure_workload(w, device, stream, steps, warmup, barrier):
+    g = GpuRun(w, device, stream)
+    ms, t0, t1 = g.timed(steps, warmup, barrier)
+    return g, ms, t0, t1
+
+
+def cpu_baseline(w, budget_s=12.0):
+    """Time the fp64 oracle on the host cores over a bounded sample of the
+    workload: whole (batch, head) units, as many as fit in about budget_s."""
+    import numpy as np
+    from oracle import relpos_oracle as orc
+    x = make_inputs(w)
+    Q, K, V = (x[k].double().numpy() for k in ("Q", "K", "V"))
+    t0 = x["table0"].double().numpy()
+    t1 = x["table1"].double().numpy() if x["table1"] is not None else None
+    heads = [(b, h) for b in range(w.B) for h in range(w.H)]
+    # rows per unit: whole heads unless one head alone is too slow
+    rows = None
+    start = time.perf_counter()
+    done = 0
+    n_rows_total = 0
+    for (b, h) in heads:
+        orc.attention(w.mode, Q, K, V, t0, t1, num_buckets=w.num_buckets, rel_param=w.rel_param,
+                      causal=w.causal, q_offset=w.q_offset, rows=rows, heads=[(b, h)])
+        done += 1
+        n_rows_total += w.Lq if rows is None else len(rows)
+        if time.perf_counter() - start > budget_s:
+            break
+    el = time.perf_counter() - start
+    frac = done / len(heads)
+    flops = w.flops() * frac
+    cores = len(os.sched_getaffinity(0))
+    threads = cores
+    try:
+        from threadpoolctl import threadpool_info
+        info = threadpool_info()
+        if info:
+            threads = max(i.get("num_threads", 1) for i in info)
+    except Exception:
+        pass
+    return {"value": flops / el / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{done} of {len(heads)} (batch, head) units of {w.name}, all rows, "
+                      f"fp64 numpy, {el:.1f} s"}, el, flops
+
+
+# ---------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="t5_base_bidir", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-others", action="store_true",
+                    help="skip the per-workload summary of the other workloads")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    args = ap.parse_args()
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    w = WORKLOADS[args.workload]
+    peaks, peak_src = load_peaks()
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        steps = args.steps if args.steps is not None else 3
+        warm = min(args.warmup, 1)
+        for _ in range(warm):
+            cpu_baseline(w, budget_s=2.0)
+        tot_flops, tot_s = 0.0, 0.0
+        last = None
+        for _ in range(steps):
+            cb, el, fl = cpu_baseline(w, budget_s=args.cpu_budget / max(1, steps))
+            tot_flops += fl
+            tot_s += el
+            last = cb
+        val = tot_flops / tot_s / 1e12
+        last["value"] = val
+        line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s",
+                "n_gpus": args.gpus, "steps": steps, "warmup": warm,
+                "ms_per_step": 1e3 * tot_s / steps, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": w.name, "mode": MODE_NAMES[w.mode], "B": w.B, "H": w.H,
+                           "Lq": w.Lq, "Lk": w.Lk, "d": w.d},
+                "cpu_baseline": last,
+                "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        barrier = dist.barrier
+    else:
+        barrier = lambda: None  # noqa: E731
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    import transformer_attention_relative_gb300 as rp
+    rp.load_library()
+    stream = torch.cuda.Stream(device)
+    phys = os.environ.get("CUDA_VISIBLE_DEVICES", str(local_rank)).split(",")[local_rank]
+
+    sampler = ClockSampler(phys)
+    sampler.start()
+    time.sleep(0.3)
+
+    # pick K so that the default timed region lasts about 2 s
+    g = GpuRun(w, device, stream)
+    for i in range(max(3, args.warmup)):
+        g.step(i)
+    torch.cuda.synchronize()
+    est = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    est[0].record(stream)
+    for i in range(20):
+        g.step(i)
+    est[1].record(stream)
+    torch.cuda.synchronize()
+    t_est = est[0].elapsed_time(est[1]) / 20 / 1e3
+    steps = args.steps if args.steps is not None else max(20, min(200000, int(2.0 / t_est)))
+    warmup = max(3, args.warmup)
+
+    ms, t0, t1 = g.timed(steps, warmup, barrier)
+    clocks = sampler.summary(t0 - 0.05, t1 + 0.05)
+    window = "timed region"
+    if clocks is None:
+        a, b = g.sustain(1.5)
+        clocks = sampler.summary(a, b)
+        window = "1.5 s of the same steps right after the timed region (timed region too short)"
+    if clocks is not None:
+        clocks["window"] = window
+
+    # max over ranks
+    t_ms = torch.tensor([ms], dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t_ms, op=dist.ReduceOp.MAX)
+    ms_max = float(t_ms.item())
+    ms_step = ms_max / steps
+    flops = w.flops()
+    value = flops * steps * world / (ms_max / 1e3) / 1e12
+
+    kname, bound = dominant_kernel(w)
+    avg_s = ms / steps / 1e3
+    if bound == "tensor":
+        achieved = flops / avg_s / 1e12
+        peak = peaks["bf16_tflops"]
+        unit = "TFLOP/s"
+        traffic = stored_traffic(kname, w.name)
+    else:
+        achieved = w.min_bytes() / avg_s / 1e9
+        peak = peaks["hbm_gbs"]
+        unit = "GB/s"
+        traffic = stored_traffic(kname, w.name)
+    roofline = {"bound": bound, "kernel": kname, "achieved": achieved, "peak": peak, "unit": unit,
+                "frac": achieved / peak, "traffic": traffic,
+                "peak_source": f"{peak_src} ({'bf16_tflops burst' if bound == 'tensor' else 'hbm_gbs'})",
+                "algorithmic_per_launch": flops if bound == "tensor" else w.min_bytes()}
+
+    e2e_ms, h2d, d2h = g.e2e(max(3, min(steps, 50)), 2)
+    e2e_steps = max(3, min(steps, 50))
+    e2e_val = flops * e2e_steps / (e2e_ms / 1e3) / 1e12
+
+    others = {}
+    if not args.no_others and rank == 0:
+        for name in ("t5_causal", "t5_decode", "shaw", "t5_tiny_fp32", "deberta"):
+            if name == w.name:
+                continue
+            ow = WORKLOADS[name]
+            try:
+                og = GpuRun(ow, device, stream)
+                k = 50
+                oms, _, _ = og.timed(k, 5, lambda: None)
+                per = oms / k / 1e3
+                kn, bd = dominant_kernel(ow)
+                ent = {"ms_per_step": oms / k, "tflops": ow.flops() / per / 1e12,
+                       "frac_of_bf16_peak": ow.flops() / per / 1e12 / peaks["bf16_tflops"]}
+                if bd == "hbm":
+                    ent["gbs"] = ow.min_bytes() / per / 1e9
+                    ent["frac_of_hbm_peak"] = ent["gbs"] / peaks["hbm_gbs"]
+                others[name] = ent
+                del og
+                torch.cuda.empty_cache()
+            except Exception as e:  # a mode this build does not run yet
+                others[name] = {"unavailable": str(e)[:120]}
+
+    sampler.stop()
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cpu, _, _ = cpu_baseline(w, budget_s=args.cpu_budget)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": steps, "warmup": warmup, "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "mode": MODE_NAMES[w.mode], "B": w.B, "H": w.H,
+                       "Lq": w.Lq, "Lk": w.Lk, "d": w.d, "num_buckets": w.num_buckets,
+                       "rel_param": w.rel_param, "causal": w.causal, "q_offset": w.q_offset,
+                       "parallelism": f"replicas x{world}",
+                       "l2": f"{g.nsets} rotating input sets of {g.set_bytes / 1e6:.1f} MB "
+                             f"(> 129 MB L2), no flush"},
+            "frac_of_peak": value / world / peaks["bf16_tflops"],
+            "roofline": roofline,
+            "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": steps * kernels_per_step(w),
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+            "source_hash": source_hash(),
+            "other_workloads": others,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
