@@ -20,7 +20,7 @@ SHAW = WORKLOADS["shaw"]
     (2, 3, 300, 300, 16, False, 0),
     (1, 2, 300, 300, 16, True, 0),
     (1, 2, 129, 400, 4, False, 0),
-    (1, 2, 64, 300, 24, True, 236),
+    (1, 2, 64, 300, 21, True, 236),   # the largest clip that fits shared memory
     (1, 1, 1, 500, 16, True, 499),   # one query row (decode-shaped)
     (1, 2, 256, 256, 1, False, 0),
 ])
@@ -41,3 +41,13 @@ def test_shaw_full_sampled():
     rows = np.array([0, 15, 16, 17, 2048, 4079, 4095])
     ref = G.run_oracle(w, x, rows=rows)
     G.compare(o[:, :, rows], ref, what="shaw rows")
+
+
+def test_shaw_clip_beyond_shared_memory_is_unsupported():
+    import pytest as _pt
+    import transformer_attention_relative_gb300 as rp
+    w = SHAW.replace(B=1, H=1, Lq=64, Lk=64, rel_param=22)
+    x = make_inputs(w)
+    with _pt.raises(rp.RelposError) as e:
+        G.run_gpu(w, x)
+    assert e.value.code == rp.RELPOS_ERR_UNSUPPORTED

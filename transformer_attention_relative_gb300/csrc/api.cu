@@ -40,6 +40,19 @@ int* status_ptr() {
   return g_status_ptr[dev];
 }
 
+int g_num_sms[kMaxDevices];
+
+int num_sms() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+  if (g_num_sms[dev] <= 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+    g_num_sms[dev] = n;
+  }
+  return g_num_sms[dev];
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
     void* p = nullptr;
@@ -262,7 +275,6 @@ extern "C" int relpos_attn_fwd(int mode, int dtype, const void* Q, const void* K
       (table1 && !aligned16(table1)))
     return RELPOS_ERR_INVALID_ARG;
   if (mode == RELPOS_DEBERTA) return RELPOS_ERR_UNSUPPORTED;
-  if (mode == RELPOS_SHAW && rel_param > 24) return RELPOS_ERR_UNSUPPORTED;
 
   int* status = status_ptr();
   if (!status) return RELPOS_ERR_CUDA;
@@ -352,23 +364,27 @@ extern "C" int relpos_attn_fwd(int mode, int dtype, const void* Q, const void* K
     p.out = out;
     p.status = status;
     p.kclip = rel_param;
+    p.Qg = static_cast<const __nv_bfloat16*>(Qb);
+    p.npairs = (Lq + 255) / 256;
     if (mode == RELPOS_T5) {
       p.bias = static_cast<const float*>(table0);
       p.t5 = t5;
       p.t5_R = R;
       p.t5_tab_off = R + 254;
       p.t5_tab_len = 2 * R + 509;
+      p.t5_tab_len4 = (p.t5_tab_len + 3) & ~3;
     } else if (mode == RELPOS_SHAW) {
       p.aK = static_cast<const __nv_bfloat16*>(table0);
       p.aV = static_cast<const __nv_bfloat16*>(table1);
     }
     if (fwd_smem_bytes(mode, p) > fwd_max_smem_bytes()) return fail(RELPOS_ERR_UNSUPPORTED);
-    CUtensorMap tq, tk, tv, to;
+    CUtensorMap tq, tk, tv;
     if (!make_tmap(&tq, Qb, Lq, static_cast<int>(BH)) || !make_tmap(&tk, Kb, Lk, static_cast<int>(BH)) ||
-        !make_tmap(&tv, Vb, Lk, static_cast<int>(BH)) ||
-        !make_tmap(&to, dtype == RELPOS_FP32 ? Qb : out, Lq, static_cast<int>(BH)))
+        !make_tmap(&tv, Vb, Lk, static_cast<int>(BH)))
       return fail(RELPOS_ERR_CUDA);
-    if (launch_fwd(mode, dtype == RELPOS_FP32, tq, tk, tv, to, p, s) != cudaSuccess)
+    const int sms = num_sms();
+    if (sms <= 0) return fail(RELPOS_ERR_CUDA);
+    if (launch_fwd(mode, dtype == RELPOS_FP32, tq, tk, tv, p, sms, s) != cudaSuccess)
       return fail(RELPOS_ERR_CUDA);
   }
   if (scratch && cudaFreeAsync(scratch, s) != cudaSuccess) {

@@ -1,30 +1,37 @@
 // attn_fwd.cu -- fused relative-position attention forward for sm_103a.
 //
-// One CTA owns a 128-row query tile of one (batch, head) and streams the
-// key/value tiles of that head through shared memory:
+// Persistent kernel: one CTA per SM walks a list of work items. An item is
+// a pair of 128-row query tiles (a and b) of one (batch, head); both tiles
+// share one stream of 128-key K/V tiles through shared memory:
 //
-//   warp 0      TMA producer: Q tile once, then K_j / V_j into a 3-stage ring.
-//   warp 1      tcgen05 issuer (one thread): S_j = Q K_j^T into one of two
-//               TMEM score buffers, then O += P_j V_j once the softmax has
-//               produced P_j. Also allocates / frees the 512 TMEM columns.
-//   warps 2-5   softmax warpgroup: thread t owns query row t (TMEM lane t).
-//               It reads its S row from TMEM, adds the relative term (from a
-//               shared-memory table, never a materialised L x L tensor),
-//               masks, keeps the running max / sum, writes bf16 P to shared
-//               memory for the next tensor-core product, and finally
-//               normalises O and stores it.
+//   warp 0       TMA producer: the item's two Q tiles, then K_j / V_j into a
+//                3-stage ring (running ahead into the next item).
+//   warp 1       tcgen05 issuer (one thread) and TMEM owner. Per key tile j it
+//                issues, in order, O_a += P_a V_j, S_a = Q_a K_{j+1}^T,
+//                O_b += P_b V_j, S_b = Q_b K_{j+1}^T, so the tensor cores work
+//                on one query tile while the softmax of the other runs.
+//   warps 4-7    softmax warpgroup of tile a; warps 8-11 that of tile b.
+//                Thread t owns query row t (TMEM lane t): it loads its S row
+//                from TMEM, adds the relative term, masks, keeps the running
+//                max / sum, writes the bf16 probabilities back to TMEM (the
+//                A operand of the P.V product) and, at the end of the item,
+//                normalises its O row and stores it.
+//
+// Tensor memory (512 columns): S_a 0-127, S_b 128-255, O_a 256-319,
+// O_b 320-383, P_a 384-447, P_b 448-511.
 //
 // The relative term follows "Relative Position Embeddings, in depth": T5 adds
 // a per-head scalar by bucket of the key-minus-query offset ("T5: one scalar
 // per head, looked up by bucket"); Shaw adds q_i . a_K[clip(j - i)] to the
-// logit and sum_j p_ij a_V[clip(j - i)] to the output ("Shaw et al.").
-// Because both depend on the offset only, a tile whose offsets all lie beyond
-// the saturation distance gets one constant (T5) or one per-row constant
-// (Shaw) instead of per-element lookups.
+// logit and sum_j p_ij a_V[clip(j - i)] to the output ("Shaw et al."). Both
+// depend on the offset only, so a tile whose offsets all lie beyond the
+// saturation distance needs one constant (T5) or one per-row constant (Shaw)
+// instead of per-element lookups; the per-element T5 bias comes from a
+// bias-by-offset table in shared memory, read four values per load.
 //
 // Softmax runs in the log2 domain with a lazily updated running maximum: the
-// output accumulator in TMEM is rescaled only when a row's maximum grows by
-// more than 2^8, which keeps every P value <= 256 and is exact because the
+// O accumulator in TMEM is rescaled only when a row's maximum grows by more
+// than 2^8, which bounds every probability by 256 and is exact because the
 // final division uses the same stale maximum.
 
 #include <cuda.h>
@@ -39,55 +46,89 @@
 namespace relpos {
 namespace {
 
-constexpr int kBM = 128;         // query rows per CTA
-constexpr int kBN = 128;         // keys per tile
-constexpr int kStages = 3;       // K/V ring depth
-constexpr int kThreads = 192;    // 6 warps
+constexpr int kBM = 128;       // query rows per tile (two tiles per item)
+constexpr int kBN = 128;       // keys per tile
+constexpr int kStages = 3;     // K/V ring depth
+constexpr int kThreads = 384;  // 12 warps
 constexpr uint32_t kTileBytes = kBM * kHeadDim * 2;  // 16 KB: 128 rows x 128 B
-constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffK = kOffQ + kTileBytes;
+constexpr uint32_t kOffQ = 0;                        // two Q tiles
+constexpr uint32_t kOffK = kOffQ + 2 * kTileBytes;
 constexpr uint32_t kOffV = kOffK + kStages * kTileBytes;
-constexpr uint32_t kOffP = kOffV + kStages * kTileBytes;  // 128 x 128 bf16 = 32 KB
-constexpr uint32_t kOffBar = kOffP + 2 * kTileBytes;
-constexpr uint32_t kOffAux = kOffBar + 256;
+constexpr uint32_t kOffBar = kOffV + kStages * kTileBytes;
+constexpr uint32_t kOffAux = kOffBar + 512;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemS = 0;    // two score buffers: columns 0..127, 128..255
-constexpr uint32_t kTmemO = 256;  // output accumulator: columns 256..319
+constexpr uint32_t kTmemS = 0;
+constexpr uint32_t kTmemO = 256;
+constexpr uint32_t kTmemP = 384;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
-// barrier slots (8 bytes each) inside the kOffBar block
 enum : uint32_t {
   kBarQFull = 0,
-  kBarKFull = 1,                   // + stage
-  kBarVFull = kBarKFull + kStages,  // + stage
+  kBarQEmpty = 1,
+  kBarKFull = 2,
+  kBarVFull = kBarKFull + kStages,
   kBarKVEmpty = kBarVFull + kStages,
-  kBarSFull = kBarKVEmpty + kStages,  // + buffer (2)
-  kBarPFull = kBarSFull + 2,
-  kBarODone = kBarPFull + 1,
-  kBarFinal = kBarODone + 1,
+  kBarSFull = kBarKVEmpty + kStages,  // + tile (2)
+  kBarSFree = kBarSFull + 2,  // + tile: the softmax has read S out of TMEM
+  kBarPFull = kBarSFree + 2,
+  kBarODone = kBarPFull + 2,
+  kBarOFree = kBarODone + 2,
+  kBarTab = kBarOFree + 2,
+  kBarFinal = kBarTab + 2,
   kNumBars = kBarFinal + 1,
 };
-constexpr uint32_t kOffTmemSlot = kNumBars * 8;
-constexpr uint32_t kOffAbort = kOffTmemSlot + 4;
+constexpr uint32_t kOffTmemSlot = 256;
+constexpr uint32_t kOffAbort = 260;
+static_assert(kNumBars * 8 <= kOffTmemSlot, "barrier block overflow");
 
 constexpr uint32_t kIdescQK = idesc_bf16_f32(kBM, kBN, 0, 0);       // Q, K both K-major
-constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, kHeadDim, 0, 1);  // P K-major, V MN-major
+constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, kHeadDim, 0, 1);  // P (TMEM), V MN-major
 
-// byte offset of 16-byte chunk `c` of row `r` in a 128-byte-swizzled tile
-// of 128-byte rows (the layout TMA writes and the tensor core reads)
-RP_DEVI uint32_t sw128_offset(int r, int c) {
-  return static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
+RP_DEVI void record_error(int* status) {
+  if (status) atomicCAS(status, 0, -4);
 }
 
-RP_DEVI void record_error(int* status, int code) {
-  if (status) atomicCAS(status, 0, code);
+// One work item: query rows [i0, i0 + 256) of head bh, split in tiles a / b.
+struct Item {
+  int bh, h, i0;
+  int nkv[2];  // key tiles each query tile visits (0: tile beyond Lq)
+  int nmax;
+};
+
+RP_DEVI Item make_item(const FwdParams& p, int w) {
+  Item it;
+  const int BH = p.B * p.H;
+  const int pair = p.npairs - 1 - w / BH;  // longest (causal) pairs first
+  it.bh = w % BH;
+  it.h = it.bh % p.H;
+  it.i0 = pair * 2 * kBM;
+#pragma unroll
+  for (int x = 0; x < 2; ++x) {
+    const int r0 = it.i0 + x * kBM;
+    if (r0 >= p.Lq) {
+      it.nkv[x] = 0;
+      continue;
+    }
+    int last_key = p.Lk - 1;
+    if (p.causal) last_key = min(last_key, min(r0 + kBM - 1, p.Lq - 1) + p.q_offset);
+    it.nkv[x] = last_key / kBN + 1;
+  }
+  it.nmax = max(it.nkv[0], it.nkv[1]);
+  return it;
 }
+
+// T5 per-WG bias-by-offset table: 4 copies shifted by one entry each, so any
+// run of 128 consecutive offsets starts 16-byte aligned in one of them.
+struct T5Tab {
+  float* base;  // [2 buffers][4 copies][len4]
+  int len4;
+  RP_DEVI float* copy(int buf, int k) const { return base + (buf * 4 + k) * len4; }
+};
 
 template <int MODE, bool OUT_F32>
 __global__ void __launch_bounds__(kThreads, 1)
     relpos_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
-                      const FwdParams p) {
+                      const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t sbase = (raw_addr + 1023u) & ~1023u;
@@ -95,25 +136,40 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int qt = gridDim.x - 1 - blockIdx.x;  // longest (causal) tiles first
-  const int bh = blockIdx.y;
-  const int h = bh % p.H;
-  const int i0 = qt * kBM;
-
-  // number of key tiles this query tile visits
-  int last_key = p.Lk - 1;
-  if (p.causal) {
-    const int last_row = min(i0 + kBM - 1, p.Lq - 1);
-    last_key = min(last_key, last_row + p.q_offset);
-  }
-  const int n_kv = last_key / kBN + 1;
+  const int nitems = p.B * p.H * p.npairs;
 
   auto bar = [&](uint32_t i) { return sbase + kOffBar + i * 8; };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffBar + kOffAbort);
 
+  // ---------------------------------------------------------------- setup
+  uint8_t* aux = smem + kOffAux;
+  uint8_t* bkt = aux;  // T5: head-independent bucket of each table offset
+  const int nrel = 2 * p.kclip + 1;
+  const uint32_t shaw_tbl = (static_cast<uint32_t>(nrel) * kHeadDim * 2u + 15u) & ~15u;
+  if constexpr (MODE == 0) {
+    for (int x = threadIdx.x; x < p.t5_tab_len4 + 4; x += kThreads) {
+      const int xc = min(x, p.t5_tab_len - 1);
+      bkt[x] = static_cast<uint8_t>(t5_bucket_dev(xc - p.t5_tab_off, p.t5));
+    }
+  } else if constexpr (MODE == 1) {
+    const uint4* srcK = reinterpret_cast<const uint4*>(p.aK);
+    const uint4* srcV = reinterpret_cast<const uint4*>(p.aV);
+    uint4* dK = reinterpret_cast<uint4*>(aux);
+    uint4* dV = reinterpret_cast<uint4*>(aux + shaw_tbl);
+    const int n16 = nrel * kHeadDim * 2 / 16;
+    for (int x = threadIdx.x; x < n16; x += kThreads) {
+      dK[x] = __ldg(srcK + x);
+      dV[x] = __ldg(srcV + x);
+    }
+  }
   if (threadIdx.x == 0) {
-    for (uint32_t i = 0; i < kNumBars; ++i)
-      mbar_init(bar(i), i == kBarPFull ? 128u : 1u);  // every softmax thread arrives on P
+    for (uint32_t i = 0; i < kNumBars; ++i) {
+      uint32_t cnt = 1;
+      if (i == kBarPFull || i == kBarPFull + 1 || i == kBarOFree || i == kBarOFree + 1 ||
+          i == kBarTab || i == kBarTab + 1 || i == kBarSFree || i == kBarSFree + 1)
+        cnt = 128;
+      mbar_init(bar(i), cnt);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -126,405 +182,489 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kOffBar + kOffTmemSlot);
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
-      mbar_arrive_expect_tx(bar(kBarQFull), kTileBytes);
-      tma_load_3d(sbase + kOffQ, &tmQ, bar(kBarQFull), 0, i0, bh);
-      bool err = false;
-      int issued = 0;
-      for (int j = 0; j < n_kv; ++j) {
-        const int st = j % kStages;
-        if (j >= kStages) {
-          if (!mbar_wait(bar(kBarKVEmpty + st), ((j / kStages) - 1) & 1)) {
-            err = true;
-            break;
-          }
-        }
-        mbar_arrive_expect_tx(bar(kBarKFull + st), kTileBytes);
-        tma_load_3d(sbase + kOffK + st * kTileBytes, &tmK, bar(kBarKFull + st), 0, j * kBN, bh);
-        mbar_arrive_expect_tx(bar(kBarVFull + st), kTileBytes);
-        tma_load_3d(sbase + kOffV + st * kTileBytes, &tmV, bar(kBarVFull + st), 0, j * kBN, bh);
-        issued = j + 1;
+  if (warp < 4) {
+    setmaxnreg_dec<72>();
+    if (warp == 0) {
+      // ------------------------------------------------------------ producer
+      if (lane == 0) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
       }
-      if (err) {
-        record_error(p.status, -4);
+      bool ok = true;
+      uint32_t kv_it = 0;
+      int item_cnt = 0;
+      for (int w = blockIdx.x; ok && w < nitems; w += gridDim.x, ++item_cnt) {
+        const Item it = make_item(p, w);
+        if (item_cnt > 0) ok = mbar_wait_warp(bar(kBarQEmpty), (item_cnt - 1) & 1);
+        if (!ok) break;
+        mbar_arrive_expect_tx_elect(bar(kBarQFull), (it.nkv[1] > 0 ? 2u : 1u) * kTileBytes);
+        tma_load_3d_elect(sbase + kOffQ, &tmQ, bar(kBarQFull), 0, it.i0, it.bh);
+        if (it.nkv[1] > 0)
+          tma_load_3d_elect(sbase + kOffQ + kTileBytes, &tmQ, bar(kBarQFull), 0, it.i0 + kBM, it.bh);
+        for (int j = 0; j < it.nmax; ++j, ++kv_it) {
+          const uint32_t st = kv_it % kStages;
+          if (kv_it >= kStages) {
+            ok = mbar_wait_warp(bar(kBarKVEmpty + st), ((kv_it / kStages) - 1) & 1);
+            if (!ok) break;
+          }
+          mbar_arrive_expect_tx_elect(bar(kBarKFull + st), kTileBytes);
+          tma_load_3d_elect(sbase + kOffK + st * kTileBytes, &tmK, bar(kBarKFull + st), 0, j * kBN, it.bh);
+          mbar_arrive_expect_tx_elect(bar(kBarVFull + st), kTileBytes);
+          tma_load_3d_elect(sbase + kOffV + st * kTileBytes, &tmV, bar(kBarVFull + st), 0, j * kBN, it.bh);
+        }
+      }
+      if (!ok && lane == 0) {
+        record_error(p.status);
         *abort_flag = 1;
       }
       // never leave with copies in flight: wait (bounded) for the last loads
-      for (int j = (issued > kStages ? issued - kStages : 0); j < issued; ++j) {
-        const int st = j % kStages;
-        mbar_wait(bar(kBarKFull + st), (j / kStages) & 1, 100000000ull);
-        mbar_wait(bar(kBarVFull + st), (j / kStages) & 1, 100000000ull);
+      const uint32_t first = kv_it > kStages ? kv_it - kStages : 0;
+      for (uint32_t k = first; k < kv_it; ++k) {
+        mbar_wait_warp(bar(kBarKFull + k % kStages), (k / kStages) & 1, 100000000ull);
+        mbar_wait_warp(bar(kBarVFull + k % kStages), (k / kStages) & 1, 100000000ull);
       }
-      mbar_wait(bar(kBarQFull), 0, 100000000ull);
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      bool ok = mbar_wait(bar(kBarQFull), 0);
-      tc_fence_after();
-      const uint32_t q_addr = sbase + kOffQ;
-      auto issue_qk = [&](int j) {
-        const int st = j % kStages;
-        const uint32_t k_addr = sbase + kOffK + st * kTileBytes;
-        const uint32_t d = tmem + kTmemS + (j & 1) * kBN;
+      if (item_cnt > 0) mbar_wait_warp(bar(kBarQFull), (item_cnt - 1) & 1, 100000000ull);
+    } else if (warp == 1) {
+      // ------------------------------------------------------------ MMA issuer
+      // Issue order per key tile j: S_a = Q_a K_{j+1}^T and S_b = Q_b K_{j+1}^T
+      // (as soon as each softmax has read its previous S), then O_a += P_a V_j
+      // and O_b += P_b V_j (as soon as each P is in TMEM).
+      bool ok = true;
+      uint32_t kv_it = 0;
+      uint32_t sis0 = 0, sis1 = 0;    // S products issued per query tile
+      uint32_t pvc0 = 0, pvc1 = 0;    // P.V products issued per query tile
+      uint32_t ocnt0 = 0, ocnt1 = 0;  // items finished per query tile
+      int item_cnt = 0;
+      // descriptors at K-step 0; later K-steps add the step's byte offset / 16
+      const uint64_t dq0 = smem_desc_sw128(sbase + kOffQ, 16, 1024);
+      const uint64_t dq1 = smem_desc_sw128(sbase + kOffQ + kTileBytes, 16, 1024);
+      const uint64_t dk0 = smem_desc_sw128(sbase + kOffK, 16, 1024);
+      const uint64_t dv0 = smem_desc_sw128(sbase + kOffV, 8192, 1024);
+      constexpr uint64_t kStageStep = kTileBytes >> 4;
+      auto issue_s = [&](uint32_t& sis, uint32_t x, uint64_t dq, uint32_t kslot) -> bool {
+        if (sis > 0 && !mbar_wait_warp(bar(kBarSFree + x), (sis - 1) & 1)) return false;
+        tc_fence_after();
+        const uint64_t dk = dk0 + kslot * kStageStep;
+        const uint32_t s_col = tmem + kTmemS + x * kBN;
 #pragma unroll
-        for (int kk = 0; kk < kHeadDim / 16; ++kk) {
-          const uint64_t a = smem_desc_sw128(q_addr + kk * 32, 16, 1024);
-          const uint64_t b = smem_desc_sw128(k_addr + kk * 32, 16, 1024);
-          umma_bf16_ss(d, a, b, kIdescQK, kk > 0 ? 1u : 0u);
-        }
-        tc_commit(bar(kBarSFull + (j & 1)));
+        for (int kk = 0; kk < kHeadDim / 16; ++kk)
+          umma_bf16_ss_elect(s_col, dq + 2 * kk, dk + 2 * kk, kIdescQK, kk > 0 ? 1u : 0u);
+        tc_commit_elect(bar(kBarSFull + x));
+        ++sis;
+        return true;
       };
-      if (ok) ok = mbar_wait(bar(kBarKFull + 0), 0);
-      tc_fence_after();
-      if (ok) issue_qk(0);
-      for (int j = 0; ok && j < n_kv; ++j) {
-        if (j + 1 < n_kv) {
-          const int st1 = (j + 1) % kStages;
-          ok = mbar_wait(bar(kBarKFull + st1), ((j + 1) / kStages) & 1);
-          tc_fence_after();
-          if (!ok) break;
-          issue_qk(j + 1);
-        }
-        ok = mbar_wait(bar(kBarPFull), j & 1);
+      auto issue_pv = [&](uint32_t& pvc, uint32_t ocnt, uint32_t x, int j, uint32_t st,
+                          uint32_t kvj) -> bool {
+        bool good = mbar_wait_warp(bar(kBarPFull + x), pvc & 1);
+        if (good && j == 0 && ocnt > 0) good = mbar_wait_warp(bar(kBarOFree + x), (ocnt - 1) & 1);
+        if (good) good = mbar_wait_warp(bar(kBarVFull + st), (kvj / kStages) & 1);
         tc_fence_after();
-        if (!ok) break;
-        const int st = j % kStages;
-        ok = mbar_wait(bar(kBarVFull + st), (j / kStages) & 1);
-        tc_fence_after();
-        if (!ok) break;
-        const uint32_t v_addr = sbase + kOffV + st * kTileBytes;
-        const uint32_t p_addr = sbase + kOffP;
+        if (!good) return false;
+        const uint64_t dv = dv0 + st * kStageStep;
+        const uint32_t o_col = tmem + kTmemO + x * kHeadDim;
+        const uint32_t p_col = tmem + kTmemP + x * 64;
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          const uint64_t a = smem_desc_sw128(p_addr + (kk >> 2) * kTileBytes + (kk & 3) * 32, 16, 1024);
-          const uint64_t b = smem_desc_sw128(v_addr + kk * 2048, 8192, 1024);
-          umma_bf16_ss(tmem + kTmemO, a, b, kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          umma_bf16_ts_elect(o_col, p_col + kk * 8, dv + 128 * kk, kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+        tc_commit_elect(bar(kBarODone + x));
+        ++pvc;
+        return true;
+      };
+      for (int w = blockIdx.x; ok && w < nitems; w += gridDim.x, ++item_cnt) {
+        const Item it = make_item(p, w);
+        ok = mbar_wait_warp(bar(kBarQFull), item_cnt & 1);
+        if (ok) ok = mbar_wait_warp(bar(kBarKFull + kv_it % kStages), (kv_it / kStages) & 1);
+        if (!ok) break;
+        if (ok && it.nkv[0] > 0) ok = issue_s(sis0, 0, dq0, kv_it % kStages);
+        if (ok && it.nkv[1] > 0) ok = issue_s(sis1, 1, dq1, kv_it % kStages);
+        if (ok && it.nmax == 1) tc_commit_elect(bar(kBarQEmpty));
+        for (int j = 0; ok && j < it.nmax; ++j) {
+          const uint32_t kvj = kv_it + j;
+          const uint32_t st = kvj % kStages;
+          if (j + 1 < it.nmax) {
+            const uint32_t st1 = (kvj + 1) % kStages;
+            ok = mbar_wait_warp(bar(kBarKFull + st1), ((kvj + 1) / kStages) & 1);
+            if (ok && j + 1 < it.nkv[0]) ok = issue_s(sis0, 0, dq0, st1);
+            if (ok && j + 1 < it.nkv[1]) ok = issue_s(sis1, 1, dq1, st1);
+            if (ok && j + 1 == it.nmax - 1) tc_commit_elect(bar(kBarQEmpty));
+          }
+          if (ok && j < it.nkv[0]) ok = issue_pv(pvc0, ocnt0, 0, j, st, kvj);
+          if (ok && j < it.nkv[1]) ok = issue_pv(pvc1, ocnt1, 1, j, st, kvj);
+          if (ok) tc_commit_elect(bar(kBarKVEmpty + st));
         }
-        tc_commit(bar(kBarODone));
-        tc_commit(bar(kBarKVEmpty + st));
+        kv_it += it.nmax;
+        if (it.nkv[0] > 0) ++ocnt0;
+        if (it.nkv[1] > 0) ++ocnt1;
       }
-      if (!ok) {
-        record_error(p.status, -4);
+      if (!ok && lane == 0) {
+        record_error(p.status);
         *abort_flag = 1;
       }
-      // all issued tensor-core work has finished before TMEM is released
-      tc_commit(bar(kBarFinal));
-      mbar_wait(bar(kBarFinal), 0, 100000000ull);
+      tc_commit_elect(bar(kBarFinal));
+      mbar_wait_warp(bar(kBarFinal), 0, 100000000ull);
     }
   } else {
-    // ------------------------------------------------------------ softmax
-    const int t = ((warp & 3) << 5) | lane;  // row == TMEM lane
+    setmaxnreg_inc<216>();
+    // -------------------------------------------------------------- softmax
+    const int x = (warp - 4) >> 2;                  // query tile a (0) or b (1)
+    const int t = ((warp & 3) << 5) | lane;          // row == TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const int prow = i0 + t + p.q_offset;    // absolute query position
-    const int p_lo = i0 + p.q_offset;
+    const uint32_t tS = tmem + lane_base + kTmemS + x * kBN;
+    const uint32_t tO = tmem + lane_base + kTmemO + x * kHeadDim;
+    const uint32_t tP = tmem + lane_base + kTmemP + x * 64;
     const float sl2 = p.scale_log2;
+    const float kNegInf = -INFINITY;
     bool err = false;
 
-    float* tab = reinterpret_cast<float*>(smem + kOffAux);
-    float add_left = 0.f, add_right = 0.f;
-    int kc = 0;
-    float* qa = nullptr;   // Shaw: this row's q . a_K[r] (log2 units)
-    float* wbin = nullptr; // Shaw: this row's attention mass per clipped offset
-    const __nv_bfloat16* aK_s = nullptr;
+    T5Tab tab;
+    float* qa = nullptr;    // Shaw: q . a_K[r] of this row (log2 units)
+    float* wbin = nullptr;  // Shaw: probability mass per clipped offset of this row
     const __nv_bfloat16* aV_s = nullptr;
-    float mass_l = 0.f, mass_r = 0.f;
-
     if constexpr (MODE == 0) {
-      // per-head bias by offset, offsets -t5_tab_off .. tab_len-1-t5_tab_off
-      for (int x = t; x < p.t5_tab_len; x += 128) {
-        const int b = t5_bucket_dev(x - p.t5_tab_off, p.t5);
-        tab[x] = __ldg(p.bias + b * p.H + h) * kLog2e;
-      }
-      add_left = __ldg(p.bias + t5_bucket_dev(-p.t5_R, p.t5) * p.H + h) * kLog2e;
-      add_right = __ldg(p.bias + t5_bucket_dev(p.t5_R, p.t5) * p.H + h) * kLog2e;
-      named_bar_sync(1, 128);
+      tab.len4 = p.t5_tab_len4;
+      const uint32_t bkt_bytes = (static_cast<uint32_t>(p.t5_tab_len4) + 4u + 15u) & ~15u;
+      tab.base = reinterpret_cast<float*>(aux + bkt_bytes) + x * 8 * p.t5_tab_len4;
     } else if constexpr (MODE == 1) {
-      kc = p.kclip;
-      const int nrel = 2 * kc + 1;
-      const int tbl_bytes = nrel * kHeadDim * 2;
-      uint8_t* aux = smem + kOffAux;
-      aK_s = reinterpret_cast<const __nv_bfloat16*>(aux);
-      aV_s = reinterpret_cast<const __nv_bfloat16*>(aux + ((tbl_bytes + 15) & ~15));
-      float* qa_all = reinterpret_cast<float*>(aux + 2 * ((tbl_bytes + 15) & ~15));
-      float* w_all = qa_all + 128 * nrel;
-      {
-        const uint4* srcK = reinterpret_cast<const uint4*>(p.aK);
-        const uint4* srcV = reinterpret_cast<const uint4*>(p.aV);
-        uint4* dK = reinterpret_cast<uint4*>(aux);
-        uint4* dV = reinterpret_cast<uint4*>(aux + ((tbl_bytes + 15) & ~15));
-        for (int x = t; x < tbl_bytes / 16; x += 128) {
-          dK[x] = __ldg(srcK + x);
-          dV[x] = __ldg(srcV + x);
-        }
-      }
-      named_bar_sync(1, 128);
-      qa = qa_all + t * nrel;
-      wbin = w_all + t * nrel;
-      if (!mbar_wait(bar(kBarQFull), 0)) err = true;
-      err = __any_sync(0xffffffffu, err);
-      if (!err) {
-        float qf[kHeadDim];
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint32_t a, b, cc, d;
-          ld_shared_v4(sbase + kOffQ + sw128_offset(t, c), a, b, cc, d);
-          const uint32_t w4[4] = {a, b, cc, d};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const __nv_bfloat162 v2 = *reinterpret_cast<const __nv_bfloat162*>(&w4[e]);
-            qf[c * 8 + 2 * e] = __bfloat162float(v2.x);
-            qf[c * 8 + 2 * e + 1] = __bfloat162float(v2.y);
-          }
-        }
-        for (int r = 0; r < nrel; ++r) {
-          const __nv_bfloat162* row = reinterpret_cast<const __nv_bfloat162*>(aK_s + r * kHeadDim);
-          float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll
-          for (int e = 0; e < kHeadDim / 2; ++e) {
-            const float2 f = __bfloat1622float2(row[e]);
-            acc0 = fmaf(qf[2 * e], f.x, acc0);
-            acc1 = fmaf(qf[2 * e + 1], f.y, acc1);
-          }
-          qa[r] = (acc0 + acc1) * sl2;
-          wbin[r] = 0.f;
-        }
-      }
+      aV_s = reinterpret_cast<const __nv_bfloat16*>(aux + shaw_tbl);
+      float* qa_all = reinterpret_cast<float*>(aux + 2 * shaw_tbl);
+      qa = qa_all + (x * 128 + t) * nrel;
+      wbin = qa_all + 2 * 128 * nrel + (x * 128 + t) * nrel;
     }
+    const int kc = p.kclip;
 
-    float m_run = -INFINITY;
-    float l_run = 0.f;
-    const float kNegInf = -INFINITY;
+    uint32_t cnt = 0, ocnt = 0;
+    for (int w = blockIdx.x; !err && w < nitems; w += gridDim.x) {
+      const Item it = make_item(p, w);
+      const int n_kv = it.nkv[x];
+      if (n_kv == 0) continue;
+      const int i0 = it.i0 + x * kBM;
+      const int prow = i0 + t + p.q_offset;  // absolute position of this row
+      const int p_lo = i0 + p.q_offset;      // of the tile's first row
 
-    for (int j = 0; j < n_kv && !err; ++j) {
-      const int j0 = j * kBN;
-      bool ok = mbar_wait(bar(kBarSFull + (j & 1)), (j >> 1) & 1);
-      err = __any_sync(0xffffffffu, !ok);
-      if (err) break;
-      tc_fence_after();
-
-      __syncwarp();
-      uint32_t sr[4][32];
-      const uint32_t s_addr = tmem + lane_base + kTmemS + (j & 1) * kBN;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) tmem_ld32(s_addr + q * 32, sr[q]);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) tmem_ld_wait(sr[q]);
-
-      float x[128];
-      // ---- logits in log2 units with the relative term
+      // ---- per-item relative-term setup
+      float add_l = 0.f, add_r = 0.f;
+      int buf = 0;
       if constexpr (MODE == 0) {
-        const int rel_hi = j0 + kBN - 1 - p_lo;          // largest offset in the tile
-        const int rel_lo = j0 - (p_lo + kBM - 1);        // smallest
-        const bool far_l = rel_hi <= -p.t5_R;
-        const bool far_r = p.t5.bidir && rel_lo >= p.t5_R;
-        if (far_l || far_r) {
-          const float a = far_l ? add_left : add_right;
+        buf = ocnt & 1;
+        const float* bias_h = p.bias + it.h;
+        for (int y = t; y < tab.len4; y += 128) {
 #pragma unroll
-          for (int c = 0; c < 128; ++c) x[c] = fmaf(__uint_as_float(sr[c >> 5][c & 31]), sl2, a);
-        } else {
-          const float* tp = tab + (j0 - prow + p.t5_tab_off);
-#pragma unroll
-          for (int c = 0; c < 128; ++c) x[c] = fmaf(__uint_as_float(sr[c >> 5][c & 31]), sl2, tp[c]);
+          for (int k = 0; k < 4; ++k)
+            tab.copy(buf, k)[y] = __ldg(bias_h + bkt[y + k] * p.H) * kLog2e;
         }
+        mbar_arrive(bar(kBarTab + x));
+        const bool ok = mbar_wait(bar(kBarTab + x), ocnt & 1);
+        err = __any_sync(0xffffffffu, !ok);
+        if (err) break;
+        add_l = tab.copy(buf, 0)[p.t5_tab_off - p.t5_R];
+        add_r = tab.copy(buf, 0)[p.t5_tab_off + p.t5_R];
       } else if constexpr (MODE == 1) {
-        const int rel_hi = j0 + kBN - 1 - p_lo;
-        const int rel_lo = j0 - (p_lo + kBM - 1);
-        if (rel_hi <= -kc || rel_lo >= kc) {
-          const float a = rel_hi <= -kc ? qa[0] : qa[2 * kc];
+        // q . a_K[r] for every clipped offset r, from this row of Q in global memory
+        float qf[kHeadDim];
+        const int row = i0 + t;
+        if (row < p.Lq) {
+          const uint4* src = reinterpret_cast<const uint4*>(p.Qg + (static_cast<size_t>(it.bh) * p.Lq + row) * kHeadDim);
 #pragma unroll
-          for (int c = 0; c < 128; ++c) x[c] = fmaf(__uint_as_float(sr[c >> 5][c & 31]), sl2, a);
-        } else {
-          const int r0 = j0 - prow;
+          for (int c = 0; c < 8; ++c) {
+            const uint4 u = __ldg(src + c);
+            const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-          for (int c = 0; c < 128; ++c) {
-            const int r = min(max(r0 + c, -kc), kc) + kc;
-            x[c] = fmaf(__uint_as_float(sr[c >> 5][c & 31]), sl2, qa[r]);
-          }
-        }
-      }
-
-      // ---- masking (causal, ragged key tail)
-      const bool need_mask = (p.causal && j0 + kBN - 1 > p_lo) || (j0 + kBN > p.Lk);
-      if (need_mask) {
-        int lim = p.Lk - 1 - j0;
-        if (p.causal) lim = min(lim, prow - j0);
-#pragma unroll
-        for (int c = 0; c < 128; ++c) x[c] = (c > lim) ? kNegInf : x[c];
-      }
-
-      // ---- running max with lazy rescale
-      float mx0 = kNegInf, mx1 = kNegInf, mx2 = kNegInf, mx3 = kNegInf;
-#pragma unroll
-      for (int c = 0; c < 128; c += 4) {
-        mx0 = fmaxf(mx0, x[c]);
-        mx1 = fmaxf(mx1, x[c + 1]);
-        mx2 = fmaxf(mx2, x[c + 2]);
-        mx3 = fmaxf(mx3, x[c + 3]);
-      }
-      const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
-      const float m_new = fmaxf(m_run, mx);
-      const bool resc = m_new > m_run + kRescaleThreshold;
-      float alpha = 1.f;
-      if (resc) {
-        alpha = ex2_approx(m_run - m_new);
-        m_run = m_new;
-      }
-      const float m_use = (m_run == kNegInf) ? 0.f : m_run;
-
-      float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-#pragma unroll
-      for (int c = 0; c < 128; c += 4) {
-        x[c] = ex2_approx(x[c] - m_use);
-        x[c + 1] = ex2_approx(x[c + 1] - m_use);
-        x[c + 2] = ex2_approx(x[c + 2] - m_use);
-        x[c + 3] = ex2_approx(x[c + 3] - m_use);
-        s0 += x[c];
-        s1 += x[c + 1];
-        s2 += x[c + 2];
-        s3 += x[c + 3];
-      }
-      const float tile_sum = (s0 + s1) + (s2 + s3);
-      l_run = l_run * alpha + tile_sum;
-
-      if constexpr (MODE == 1) {
-        // value-side mass per clipped offset
-        if (resc && j > 0) {
-          for (int r = 0; r < 2 * kc + 1; ++r) wbin[r] *= alpha;
-          mass_l *= alpha;
-          mass_r *= alpha;
-        }
-        const int rel_hi = j0 + kBN - 1 - p_lo;
-        const int rel_lo = j0 - (p_lo + kBM - 1);
-        if (rel_hi <= -kc) {
-          mass_l += tile_sum;
-        } else if (rel_lo >= kc) {
-          mass_r += tile_sum;
-        } else {
-          const int r0 = j0 - prow;
-#pragma unroll
-          for (int c = 0; c < 128; ++c) {
-            const int rel = r0 + c;
-            if (rel <= -kc) {
-              mass_l += x[c];
-            } else if (rel >= kc) {
-              mass_r += x[c];
-            } else {
-              wbin[rel + kc] += x[c];
+            for (int e = 0; e < 4; ++e) {
+              const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4[e]));
+              qf[c * 8 + 2 * e] = f.x;
+              qf[c * 8 + 2 * e + 1] = f.y;
             }
           }
+        } else {
+#pragma unroll
+          for (int c = 0; c < kHeadDim; ++c) qf[c] = 0.f;
         }
+        const __nv_bfloat16* aK_s = reinterpret_cast<const __nv_bfloat16*>(aux);
+        for (int r = 0; r < nrel; ++r) {
+          const __nv_bfloat162* rowk = reinterpret_cast<const __nv_bfloat162*>(aK_s + r * kHeadDim);
+          float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+          for (int e = 0; e < kHeadDim / 2; ++e) {
+            const float2 f = __bfloat1622float2(rowk[e]);
+            a0 = fmaf(qf[2 * e], f.x, a0);
+            a1 = fmaf(qf[2 * e + 1], f.y, a1);
+          }
+          qa[r] = (a0 + a1) * sl2;
+          wbin[r] = 0.f;
+        }
+        add_l = qa[0];
+        add_r = qa[2 * kc];
       }
+      float mass_l = 0.f, mass_r = 0.f;
 
-      // ---- previous P.V must be done before P and O are touched
-      if (j > 0) {
-        ok = mbar_wait(bar(kBarODone), (j - 1) & 1);
+      float m_run = kNegInf;
+      float l_run = 0.f;
+      for (int j = 0; j < n_kv; ++j, ++cnt) {
+        const int j0 = j * kBN;
+        bool ok = mbar_wait(bar(kBarSFull + x), cnt & 1);
         err = __any_sync(0xffffffffu, !ok);
         if (err) break;
         tc_fence_after();
         __syncwarp();
-        if (__any_sync(0xffffffffu, resc)) {
+
+        uint32_t sr[4][32];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tmem_ld32(tS + q * 32, sr[q]);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tmem_ld_wait(sr[q]);
+        tc_fence_before();
+        mbar_arrive(bar(kBarSFree + x));  // the next S may overwrite this buffer
+        float* xs = reinterpret_cast<float*>(&sr[0][0]);
+
+        // ---- tile class: far (one constant per row) or near (per element)
+        const int rel_hi = j0 + kBN - 1 - p_lo;    // largest key - query offset in the tile
+        const int rel_lo = j0 - (p_lo + kBM - 1);  // smallest
+        bool far_l, far_r;
+        if constexpr (MODE == 0) {
+          far_l = rel_hi <= -p.t5_R;
+          far_r = p.t5.bidir && rel_lo >= p.t5_R;
+        } else {
+          far_l = rel_hi <= -kc;
+          far_r = rel_lo >= kc;
+        }
+        const bool need_mask = (p.causal && j0 + kBN - 1 > p_lo) || (j0 + kBN > p.Lk);
+        int lim = 127;
+        if (need_mask) {
+          lim = p.Lk - 1 - j0;
+          if (p.causal) lim = min(lim, prow - j0);
+        }
+
+        float mx;
+        float addc = 0.f;  // far tiles: the constant still to add
+        const bool far = far_l || far_r;
+        if (far) {
+          // logits are s * sl2 + addc; the max is taken on raw s
+          addc = far_l ? add_l : add_r;
+          if (need_mask) {
+#pragma unroll
+            for (int c = 0; c < 128; ++c) xs[c] = (c > lim) ? kNegInf : xs[c];
+          }
+          float m0 = kNegInf, m1 = kNegInf, m2 = kNegInf, m3 = kNegInf;
+#pragma unroll
+          for (int c = 0; c < 128; c += 8) {
+            m0 = max3f(m0, xs[c], xs[c + 1]);
+            m1 = max3f(m1, xs[c + 2], xs[c + 3]);
+            m2 = max3f(m2, xs[c + 4], xs[c + 5]);
+            m3 = max3f(m3, xs[c + 6], xs[c + 7]);
+          }
+          mx = fmaf(fmaxf(fmaxf(m0, m1), fmaxf(m2, m3)), sl2, addc);
+        } else {
+          if constexpr (MODE == 0) {
+            const int s0 = j0 - prow + p.t5_tab_off;  // table index of column 0
+            const int k = s0 & 3;
+            const float4* tp = reinterpret_cast<const float4*>(tab.copy(buf, k) + (s0 - k));
+            const float2 sc2 = make_float2(sl2, sl2);
+#pragma unroll
+            for (int q = 0; q < 32; ++q) {
+              const float4 bq = tp[q];
+              float2 a = make_float2(xs[4 * q], xs[4 * q + 1]);
+              float2 b = make_float2(xs[4 * q + 2], xs[4 * q + 3]);
+              a = __ffma2_rn(a, sc2, make_float2(bq.x, bq.y));
+              b = __ffma2_rn(b, sc2, make_float2(bq.z, bq.w));
+              xs[4 * q] = a.x;
+              xs[4 * q + 1] = a.y;
+              xs[4 * q + 2] = b.x;
+              xs[4 * q + 3] = b.y;
+            }
+          } else if constexpr (MODE == 1) {
+            const int r0 = j0 - prow;
+#pragma unroll
+            for (int c = 0; c < 128; ++c) {
+              const int r = min(max(r0 + c, -kc), kc) + kc;
+              xs[c] = fmaf(xs[c], sl2, qa[r]);
+            }
+          }
+          if (need_mask) {
+#pragma unroll
+            for (int c = 0; c < 128; ++c) xs[c] = (c > lim) ? kNegInf : xs[c];
+          }
+          float m0 = kNegInf, m1 = kNegInf, m2 = kNegInf, m3 = kNegInf;
+#pragma unroll
+          for (int c = 0; c < 128; c += 8) {
+            m0 = max3f(m0, xs[c], xs[c + 1]);
+            m1 = max3f(m1, xs[c + 2], xs[c + 3]);
+            m2 = max3f(m2, xs[c + 4], xs[c + 5]);
+            m3 = max3f(m3, xs[c + 6], xs[c + 7]);
+          }
+          mx = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+        }
+
+        // ---- running max with lazy rescale
+        const float m_new = fmaxf(m_run, mx);
+        const bool resc = m_new > m_run + kRescaleThreshold;
+        float alpha = 1.f;
+        if (resc) {
+          alpha = ex2_approx(m_run - m_new);
+          m_run = m_new;
+        }
+        const float m_use = (m_run == kNegInf) ? 0.f : m_run;
+
+        // ---- probabilities (in place), row sum, bf16 pack
+        uint32_t pk[64];
+        float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+        if (far) {
+          const float2 sc2 = make_float2(sl2, sl2);
+          const float2 off2 = make_float2(addc - m_use, addc - m_use);
+#pragma unroll
+          for (int c = 0; c < 128; c += 4) {
+            float2 a = __ffma2_rn(make_float2(xs[c], xs[c + 1]), sc2, off2);
+            float2 b = __ffma2_rn(make_float2(xs[c + 2], xs[c + 3]), sc2, off2);
+            a.x = ex2_approx(a.x);
+            a.y = ex2_approx(a.y);
+            b.x = ex2_approx(b.x);
+            b.y = ex2_approx(b.y);
+            acc0 = __fadd2_rn(acc0, a);
+            acc1 = __fadd2_rn(acc1, b);
+            pk[c / 2] = pack_bf16x2(a.x, a.y);
+            pk[c / 2 + 1] = pack_bf16x2(b.x, b.y);
+            if constexpr (MODE == 1) {
+              xs[c] = a.x;
+              xs[c + 1] = a.y;
+              xs[c + 2] = b.x;
+              xs[c + 3] = b.y;
+            }
+          }
+        } else {
+          const float2 neg = make_float2(-m_use, -m_use);
+#pragma unroll
+          for (int c = 0; c < 128; c += 4) {
+            float2 a = __fadd2_rn(make_float2(xs[c], xs[c + 1]), neg);
+            float2 b = __fadd2_rn(make_float2(xs[c + 2], xs[c + 3]), neg);
+            a.x = ex2_approx(a.x);
+            a.y = ex2_approx(a.y);
+            b.x = ex2_approx(b.x);
+            b.y = ex2_approx(b.y);
+            acc0 = __fadd2_rn(acc0, a);
+            acc1 = __fadd2_rn(acc1, b);
+            pk[c / 2] = pack_bf16x2(a.x, a.y);
+            pk[c / 2 + 1] = pack_bf16x2(b.x, b.y);
+            if constexpr (MODE == 1) {
+              xs[c] = a.x;
+              xs[c + 1] = a.y;
+              xs[c + 2] = b.x;
+              xs[c + 3] = b.y;
+            }
+          }
+        }
+        const float tile_sum = (acc0.x + acc0.y) + (acc1.x + acc1.y);
+        l_run = l_run * alpha + tile_sum;
+
+        if constexpr (MODE == 1) {
+          if (resc && j > 0) {
+            for (int r = 0; r < nrel; ++r) wbin[r] *= alpha;
+            mass_l *= alpha;
+            mass_r *= alpha;
+          }
+          if (far_l) {
+            mass_l += tile_sum;
+          } else if (far_r) {
+            mass_r += tile_sum;
+          } else {
+            const int r0 = j0 - prow;
+#pragma unroll
+            for (int c = 0; c < 128; ++c) {
+              const int rel = r0 + c;
+              if (rel <= -kc) {
+                mass_l += xs[c];
+              } else if (rel >= kc) {
+                mass_r += xs[c];
+              } else {
+                wbin[rel + kc] += xs[c];
+              }
+            }
+          }
+        }
+
+        // ---- the previous P.V of this tile must be done before P / O change
+        if (cnt > 0) {
+          ok = mbar_wait(bar(kBarODone + x), (cnt - 1) & 1);
+          err = __any_sync(0xffffffffu, !ok);
+          if (err) break;
+          tc_fence_after();
+        }
+        __syncwarp();
+        if (j > 0 && __any_sync(0xffffffffu, resc)) {
           uint32_t o[2][32];
-          const uint32_t o_addr = tmem + lane_base + kTmemO;
-          tmem_ld32(o_addr, o[0]);
-          tmem_ld32(o_addr + 32, o[1]);
+          tmem_ld32(tO, o[0]);
+          tmem_ld32(tO + 32, o[1]);
           tmem_ld_wait(o[0]);
           tmem_ld_wait(o[1]);
 #pragma unroll
           for (int q = 0; q < 2; ++q)
 #pragma unroll
             for (int c = 0; c < 32; ++c) o[q][c] = __float_as_uint(__uint_as_float(o[q][c]) * alpha);
-          tmem_st32(o_addr, o[0]);
-          tmem_st32(o_addr + 32, o[1]);
-          tmem_st_wait();
+          tmem_st32(tO, o[0]);
+          tmem_st32(tO + 32, o[1]);
         }
+        tmem_st32(tP, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+        tmem_st32(tP + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(kBarPFull + x));
       }
+      if (err) break;
 
-      // ---- bf16 P into the 128-byte-swizzled K-major operand tile
-#pragma unroll
-      for (int ch = 0; ch < 16; ++ch) {
-        const uint32_t addr = sbase + kOffP + (ch >> 3) * kTileBytes + sw128_offset(t, ch & 7);
-        st_shared_v4(addr, pack_bf16x2(x[ch * 8 + 0], x[ch * 8 + 1]),
-                     pack_bf16x2(x[ch * 8 + 2], x[ch * 8 + 3]),
-                     pack_bf16x2(x[ch * 8 + 4], x[ch * 8 + 5]),
-                     pack_bf16x2(x[ch * 8 + 6], x[ch * 8 + 7]));
+      // ---- epilogue of this item
+      {
+        const bool ok = mbar_wait(bar(kBarODone + x), (cnt - 1) & 1);
+        err = __any_sync(0xffffffffu, !ok);
+        if (err) break;
       }
-      fence_async_smem();
-      tc_fence_before();
-      mbar_arrive(bar(kBarPFull));
-    }
-
-    // ------------------------------------------------------------ epilogue
-    if (!err) {
-      const bool ok = mbar_wait(bar(kBarODone), (n_kv - 1) & 1);
-      err = __any_sync(0xffffffffu, !ok);
-    }
-    if (err) {
-      record_error(p.status, -4);
-      *abort_flag = 1;
-    }
-    float o[kHeadDim];
-    if (!err) {
       tc_fence_after();
       __syncwarp();
       uint32_t orr[2][32];
-      const uint32_t o_addr = tmem + lane_base + kTmemO;
-      tmem_ld32(o_addr, orr[0]);
-      tmem_ld32(o_addr + 32, orr[1]);
+      tmem_ld32(tO, orr[0]);
+      tmem_ld32(tO + 32, orr[1]);
       tmem_ld_wait(orr[0]);
       tmem_ld_wait(orr[1]);
-#pragma unroll
-      for (int c = 0; c < kHeadDim; ++c) o[c] = __uint_as_float(orr[c >> 5][c & 31]);
+      tc_fence_before();
+      mbar_arrive(bar(kBarOFree + x));  // the next item's P.V may overwrite O
+      ++ocnt;
+      float* o = reinterpret_cast<float*>(&orr[0][0]);
       if constexpr (MODE == 1) {
         wbin[0] += mass_l;
         wbin[2 * kc] += mass_r;
-        for (int r = 0; r < 2 * kc + 1; ++r) {
-          const float w = wbin[r];
-          const __nv_bfloat162* row = reinterpret_cast<const __nv_bfloat162*>(aV_s + r * kHeadDim);
+        for (int r = 0; r < nrel; ++r) {
+          const float wr = wbin[r];
+          const __nv_bfloat162* rowv = reinterpret_cast<const __nv_bfloat162*>(aV_s + r * kHeadDim);
 #pragma unroll
           for (int e = 0; e < kHeadDim / 2; ++e) {
-            const float2 f = __bfloat1622float2(row[e]);
-            o[2 * e] = fmaf(w, f.x, o[2 * e]);
-            o[2 * e + 1] = fmaf(w, f.y, o[2 * e + 1]);
+            const float2 f = __bfloat1622float2(rowv[e]);
+            o[2 * e] = fmaf(wr, f.x, o[2 * e]);
+            o[2 * e + 1] = fmaf(wr, f.y, o[2 * e + 1]);
           }
         }
       }
       const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
-#pragma unroll
-      for (int c = 0; c < kHeadDim; ++c) o[c] *= inv_l;
-    } else {
-#pragma unroll
-      for (int c = 0; c < kHeadDim; ++c) o[c] = 0.f;
-    }
-    if constexpr (OUT_F32) {
       const int row = i0 + t;
-      if (!err && row < p.Lq) {
-        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) +
-                                                (static_cast<size_t>(bh) * p.Lq + row) * kHeadDim);
+      if (row < p.Lq) {
+        if constexpr (OUT_F32) {
+          float* dst = static_cast<float*>(p.out) + (static_cast<size_t>(it.bh) * p.Lq + row) * kHeadDim;
 #pragma unroll
-        for (int c = 0; c < kHeadDim / 4; ++c)
-          dst[c] = make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
-      }
-    } else {
-      // stage the bf16 tile in the (now idle) Q buffer, then one TMA store
+          for (int c = 0; c < kHeadDim; c += 4)
+            st_global_v4(dst + c, __float_as_uint(o[c] * inv_l), __float_as_uint(o[c + 1] * inv_l),
+                         __float_as_uint(o[c + 2] * inv_l), __float_as_uint(o[c + 3] * inv_l));
+        } else {
+          __nv_bfloat16* dst =
+              static_cast<__nv_bfloat16*>(p.out) + (static_cast<size_t>(it.bh) * p.Lq + row) * kHeadDim;
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        st_shared_v4(sbase + kOffQ + sw128_offset(t, c), pack_bf16x2(o[8 * c], o[8 * c + 1]),
-                     pack_bf16x2(o[8 * c + 2], o[8 * c + 3]), pack_bf16x2(o[8 * c + 4], o[8 * c + 5]),
-                     pack_bf16x2(o[8 * c + 6], o[8 * c + 7]));
+          for (int c = 0; c < kHeadDim; c += 8)
+            st_global_v4(dst + c, pack_bf16x2(o[c] * inv_l, o[c + 1] * inv_l),
+                         pack_bf16x2(o[c + 2] * inv_l, o[c + 3] * inv_l),
+                         pack_bf16x2(o[c + 4] * inv_l, o[c + 5] * inv_l),
+                         pack_bf16x2(o[c + 6] * inv_l, o[c + 7] * inv_l));
+        }
       }
-      fence_async_smem();
-      named_bar_sync(1, 128);
-      if (t == 0 && *abort_flag == 0) {
-        tma_store_3d(&tmO, sbase + kOffQ, 0, i0, bh);
-        tma_store_commit();
-        tma_store_wait_read_all();
-      }
+    }
+    if (err) {
+      record_error(p.status);
+      *abort_flag = 1;
     }
   }
 
@@ -542,23 +682,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 uint32_t fwd_smem_bytes(int mode, const FwdParams& p) {
   uint32_t aux = 0;
   if (mode == 0) {
-    aux = static_cast<uint32_t>(p.t5_tab_len) * 4u;
+    const uint32_t bkt_bytes = (static_cast<uint32_t>(p.t5_tab_len4) + 4u + 15u) & ~15u;
+    aux = bkt_bytes + 2u * 8u * static_cast<uint32_t>(p.t5_tab_len4) * 4u;
   } else if (mode == 1) {
     const uint32_t nrel = 2u * p.kclip + 1u;
     const uint32_t tbl = (nrel * kHeadDim * 2u + 15u) & ~15u;
-    aux = 2u * tbl + 2u * 128u * nrel * 4u;
+    aux = 2u * tbl + 4u * 128u * nrel * 4u;
   }
   return 1024u + kOffAux + ((aux + 15u) & ~15u);
 }
 
+uint32_t fwd_max_smem_bytes() { return 232448u; }
+
+int fwd_num_items(const FwdParams& p) { return p.B * p.H * p.npairs; }
+
 cudaError_t launch_fwd(int mode, bool out_f32, const CUtensorMap& tmQ, const CUtensorMap& tmK,
-                       const CUtensorMap& tmV, const CUtensorMap& tmO, const FwdParams& p,
-                       cudaStream_t stream) {
+                       const CUtensorMap& tmV, const FwdParams& p, int num_sms, cudaStream_t stream) {
   const uint32_t smem = fwd_smem_bytes(mode, p);
-  dim3 grid((p.Lq + kBM - 1) / kBM, p.B * p.H);
+  const int nitems = fwd_num_items(p);
+  dim3 grid(nitems < num_sms ? nitems : num_sms);
   dim3 block(kThreads);
-  void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap,
-               const FwdParams) = nullptr;
+  void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const FwdParams) = nullptr;
   if (mode == 0) {
     kern = out_f32 ? relpos_fwd_kernel<0, true> : relpos_fwd_kernel<0, false>;
   } else if (mode == 1) {
@@ -569,10 +713,8 @@ cudaError_t launch_fwd(int mode, bool out_f32, const CUtensorMap& tmQ, const CUt
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  kern<<<grid, block, smem, stream>>>(tmQ, tmK, tmV, tmO, p);
+  kern<<<grid, block, smem, stream>>>(tmQ, tmK, tmV, p);
   return cudaGetLastError();
 }
-
-uint32_t fwd_max_smem_bytes() { return 232448u; }
 
 }  // namespace relpos

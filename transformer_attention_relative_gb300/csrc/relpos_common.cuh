@@ -65,7 +65,10 @@ struct FwdParams {
   int t5_R;           // |offset| >= R: the side's last bucket (no ordering left)
   int t5_tab_len;     // entries of the per-head bias-by-offset table
   int t5_tab_off;     // table index of offset 0
+  int t5_tab_len4;    // t5_tab_len rounded up to a multiple of 4
   T5Index t5;
+  int npairs;         // 256-row query-tile pairs per head
+  const __nv_bfloat16* Qg;  // Q in global memory (bf16 [B,H,Lq,64])
   // Shaw
   const __nv_bfloat16* aK;  // [2k+1, 64]
   const __nv_bfloat16* aV;  // [2k+1, 64]

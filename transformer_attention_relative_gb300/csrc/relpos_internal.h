@@ -12,9 +12,9 @@ namespace relpos {
 
 uint32_t fwd_smem_bytes(int mode, const FwdParams& p);
 uint32_t fwd_max_smem_bytes();
+int fwd_num_items(const FwdParams& p);
 cudaError_t launch_fwd(int mode, bool out_f32, const CUtensorMap& tmQ, const CUtensorMap& tmK,
-                       const CUtensorMap& tmV, const CUtensorMap& tmO, const FwdParams& p,
-                       cudaStream_t stream);
+                       const CUtensorMap& tmV, const FwdParams& p, int num_sms, cudaStream_t stream);
 
 int decode_chunk_keys();
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);
