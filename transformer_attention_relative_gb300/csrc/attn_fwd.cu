@@ -4,12 +4,14 @@
 // a pair of 128-row query tiles (a and b) of one (batch, head); both tiles
 // share one stream of 128-key K/V tiles through shared memory:
 //
-//   warp 0       TMA producer: the item's two Q tiles, then K_j / V_j into a
-//                3-stage ring (running ahead into the next item).
-//   warp 1       tcgen05 issuer (one thread) and TMEM owner. Per key tile j it
-//                issues, in order, O_a += P_a V_j, S_a = Q_a K_{j+1}^T,
-//                O_b += P_b V_j, S_b = Q_b K_{j+1}^T, so the tensor cores work
-//                on one query tile while the softmax of the other runs.
+//   warp 0       TMA producer: the item's two Q tiles and the 3-stage K ring
+//                (running ahead into the next item).
+//   warp 2       TMA producer of the V ring.
+//   warps 1, 3   tcgen05 issuers of tiles a and b (warp 1 also owns TMEM). For
+//                each key tile j an issuer computes S = Q K_{j+1}^T as soon as
+//                its softmax has read S_j out of TMEM, and O += P_j V_j as soon
+//                as P_j is back in TMEM, so the scores of the next key tile are
+//                ready when the softmax finishes the current one.
 //   warps 4-7    softmax warpgroup of tile a; warps 8-11 that of tile b.
 //                Thread t owns query row t (TMEM lane t): it loads its S row
 //                from TMEM, adds the relative term, masks, keeps the running
@@ -67,8 +69,9 @@ enum : uint32_t {
   kBarQEmpty = 1,
   kBarKFull = 2,
   kBarVFull = kBarKFull + kStages,
-  kBarKVEmpty = kBarVFull + kStages,
-  kBarSFull = kBarKVEmpty + kStages,  // + tile (2)
+  kBarKEmpty = kBarVFull + kStages,   // K stage read by every S product of its tile
+  kBarVEmpty = kBarKEmpty + kStages,  // V stage read by every P.V product of its tile
+  kBarSFull = kBarVEmpty + kStages,   // + tile (2)
   kBarSFree = kBarSFull + 2,  // + tile: the softmax has read S out of TMEM
   kBarPFull = kBarSFree + 2,
   kBarODone = kBarPFull + 2,
@@ -167,7 +170,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t cnt = 1;
       if (i == kBarPFull || i == kBarPFull + 1 || i == kBarOFree || i == kBarOFree + 1 ||
           i == kBarTab || i == kBarTab + 1 || i == kBarSFree || i == kBarSFree + 1)
-        cnt = 128;
+        cnt = 128;  // every thread of a softmax warpgroup
+      if (i == kBarQEmpty || i == kBarFinal || (i >= kBarKEmpty && i < kBarVEmpty + kStages))
+        cnt = 2;    // both MMA issuers
       mbar_init(bar(i), cnt);
     }
     *abort_flag = 0;
@@ -184,34 +189,39 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < 4) {
     setmaxnreg_dec<72>();
-    if (warp == 0) {
-      // ------------------------------------------------------------ producer
+    if (warp == 0 || warp == 2) {
+      // ------------------------------------------------------------ producers
+      // warp 0: each item's Q tiles and the K ring; warp 2: the V ring
+      const bool kq = warp == 0;
       if (lane == 0) {
-        tma_prefetch_desc(&tmQ);
-        tma_prefetch_desc(&tmK);
-        tma_prefetch_desc(&tmV);
+        tma_prefetch_desc(kq ? &tmK : &tmV);
+        if (kq) tma_prefetch_desc(&tmQ);
       }
+      const uint32_t full0 = kq ? kBarKFull : kBarVFull;
+      const uint32_t empty0 = kq ? kBarKEmpty : kBarVEmpty;
+      const uint32_t ring = kq ? kOffK : kOffV;
+      const void* tmap = kq ? static_cast<const void*>(&tmK) : static_cast<const void*>(&tmV);
       bool ok = true;
-      uint32_t kv_it = 0;
+      uint32_t it_cnt = 0;
       int item_cnt = 0;
       for (int w = blockIdx.x; ok && w < nitems; w += gridDim.x, ++item_cnt) {
         const Item it = make_item(p, w);
-        if (item_cnt > 0) ok = mbar_wait_warp(bar(kBarQEmpty), (item_cnt - 1) & 1);
-        if (!ok) break;
-        mbar_arrive_expect_tx_elect(bar(kBarQFull), (it.nkv[1] > 0 ? 2u : 1u) * kTileBytes);
-        tma_load_3d_elect(sbase + kOffQ, &tmQ, bar(kBarQFull), 0, it.i0, it.bh);
-        if (it.nkv[1] > 0)
-          tma_load_3d_elect(sbase + kOffQ + kTileBytes, &tmQ, bar(kBarQFull), 0, it.i0 + kBM, it.bh);
-        for (int j = 0; j < it.nmax; ++j, ++kv_it) {
-          const uint32_t st = kv_it % kStages;
-          if (kv_it >= kStages) {
-            ok = mbar_wait_warp(bar(kBarKVEmpty + st), ((kv_it / kStages) - 1) & 1);
+        if (kq) {
+          if (item_cnt > 0) ok = mbar_wait_warp(bar(kBarQEmpty), (item_cnt - 1) & 1);
+          if (!ok) break;
+          mbar_arrive_expect_tx_elect(bar(kBarQFull), (it.nkv[1] > 0 ? 2u : 1u) * kTileBytes);
+          tma_load_3d_elect(sbase + kOffQ, &tmQ, bar(kBarQFull), 0, it.i0, it.bh);
+          if (it.nkv[1] > 0)
+            tma_load_3d_elect(sbase + kOffQ + kTileBytes, &tmQ, bar(kBarQFull), 0, it.i0 + kBM, it.bh);
+        }
+        for (int j = 0; j < it.nmax; ++j, ++it_cnt) {
+          const uint32_t st = it_cnt % kStages;
+          if (it_cnt >= kStages) {
+            ok = mbar_wait_warp(bar(empty0 + st), ((it_cnt / kStages) - 1) & 1);
             if (!ok) break;
           }
-          mbar_arrive_expect_tx_elect(bar(kBarKFull + st), kTileBytes);
-          tma_load_3d_elect(sbase + kOffK + st * kTileBytes, &tmK, bar(kBarKFull + st), 0, j * kBN, it.bh);
-          mbar_arrive_expect_tx_elect(bar(kBarVFull + st), kTileBytes);
-          tma_load_3d_elect(sbase + kOffV + st * kTileBytes, &tmV, bar(kBarVFull + st), 0, j * kBN, it.bh);
+          mbar_arrive_expect_tx_elect(bar(full0 + st), kTileBytes);
+          tma_load_3d_elect(sbase + ring + st * kTileBytes, tmap, bar(full0 + st), 0, j * kBN, it.bh);
         }
       }
       if (!ok && lane == 0) {
@@ -219,34 +229,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 1;
       }
       // never leave with copies in flight: wait (bounded) for the last loads
-      const uint32_t first = kv_it > kStages ? kv_it - kStages : 0;
-      for (uint32_t k = first; k < kv_it; ++k) {
-        mbar_wait_warp(bar(kBarKFull + k % kStages), (k / kStages) & 1, 100000000ull);
-        mbar_wait_warp(bar(kBarVFull + k % kStages), (k / kStages) & 1, 100000000ull);
-      }
-      if (item_cnt > 0) mbar_wait_warp(bar(kBarQFull), (item_cnt - 1) & 1, 100000000ull);
-    } else if (warp == 1) {
-      // ------------------------------------------------------------ MMA issuer
-      // Issue order per key tile j: S_a = Q_a K_{j+1}^T and S_b = Q_b K_{j+1}^T
-      // (as soon as each softmax has read its previous S), then O_a += P_a V_j
-      // and O_b += P_b V_j (as soon as each P is in TMEM).
+      const uint32_t first = it_cnt > kStages ? it_cnt - kStages : 0;
+      for (uint32_t k = first; k < it_cnt; ++k)
+        mbar_wait_warp(bar(full0 + k % kStages), (k / kStages) & 1, 100000000ull);
+      if (kq && item_cnt > 0) mbar_wait_warp(bar(kBarQFull), (item_cnt - 1) & 1, 100000000ull);
+    } else if (warp == 1 || warp == 3) {
+      // ------------------------------------------------------------ MMA issuers
+      // Warp 1 issues the products of query tile a, warp 3 those of tile b, so
+      // each reacts only to its own softmax warpgroup. Per key tile j: S = Q K_{j+1}^T
+      // as soon as the softmax has read its previous S, then O += P V_j as soon as P
+      // is in TMEM. K / V stages and the Q tiles are released once both issuers are
+      // done with them (barriers counting two arrivals).
+      const uint32_t x = warp == 1 ? 0u : 1u;
       bool ok = true;
       uint32_t kv_it = 0;
-      uint32_t sis0 = 0, sis1 = 0;    // S products issued per query tile
-      uint32_t pvc0 = 0, pvc1 = 0;    // P.V products issued per query tile
-      uint32_t ocnt0 = 0, ocnt1 = 0;  // items finished per query tile
+      uint32_t sis = 0;   // S products issued
+      uint32_t pvc = 0;   // P.V products issued
+      uint32_t ocnt = 0;  // items finished
       int item_cnt = 0;
       // descriptors at K-step 0; later K-steps add the step's byte offset / 16
-      const uint64_t dq0 = smem_desc_sw128(sbase + kOffQ, 16, 1024);
-      const uint64_t dq1 = smem_desc_sw128(sbase + kOffQ + kTileBytes, 16, 1024);
+      const uint64_t dq = smem_desc_sw128(sbase + kOffQ + x * kTileBytes, 16, 1024);
       const uint64_t dk0 = smem_desc_sw128(sbase + kOffK, 16, 1024);
       const uint64_t dv0 = smem_desc_sw128(sbase + kOffV, 8192, 1024);
       constexpr uint64_t kStageStep = kTileBytes >> 4;
-      auto issue_s = [&](uint32_t& sis, uint32_t x, uint64_t dq, uint32_t kslot) -> bool {
+      const uint32_t s_col = tmem + kTmemS + x * kBN;
+      const uint32_t o_col = tmem + kTmemO + x * kHeadDim;
+      const uint32_t p_col = tmem + kTmemP + x * 64;
+      auto issue_s = [&](uint32_t kslot) -> bool {
         if (sis > 0 && !mbar_wait_warp(bar(kBarSFree + x), (sis - 1) & 1)) return false;
         tc_fence_after();
         const uint64_t dk = dk0 + kslot * kStageStep;
-        const uint32_t s_col = tmem + kTmemS + x * kBN;
 #pragma unroll
         for (int kk = 0; kk < kHeadDim / 16; ++kk)
           umma_bf16_ss_elect(s_col, dq + 2 * kk, dk + 2 * kk, kIdescQK, kk > 0 ? 1u : 0u);
@@ -254,48 +266,65 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++sis;
         return true;
       };
-      auto issue_pv = [&](uint32_t& pvc, uint32_t ocnt, uint32_t x, int j, uint32_t st,
-                          uint32_t kvj) -> bool {
-        bool good = mbar_wait_warp(bar(kBarPFull + x), pvc & 1);
-        if (good && j == 0 && ocnt > 0) good = mbar_wait_warp(bar(kBarOFree + x), (ocnt - 1) & 1);
-        if (good) good = mbar_wait_warp(bar(kBarVFull + st), (kvj / kStages) & 1);
-        tc_fence_after();
-        if (!good) return false;
-        const uint64_t dv = dv0 + st * kStageStep;
-        const uint32_t o_col = tmem + kTmemO + x * kHeadDim;
-        const uint32_t p_col = tmem + kTmemP + x * 64;
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          umma_bf16_ts_elect(o_col, p_col + kk * 8, dv + 128 * kk, kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
-        tc_commit_elect(bar(kBarODone + x));
-        ++pvc;
-        return true;
-      };
       for (int w = blockIdx.x; ok && w < nitems; w += gridDim.x, ++item_cnt) {
         const Item it = make_item(p, w);
+        const int nkv = it.nkv[x];
         ok = mbar_wait_warp(bar(kBarQFull), item_cnt & 1);
-        if (ok) ok = mbar_wait_warp(bar(kBarKFull + kv_it % kStages), (kv_it / kStages) & 1);
         if (!ok) break;
-        if (ok && it.nkv[0] > 0) ok = issue_s(sis0, 0, dq0, kv_it % kStages);
-        if (ok && it.nkv[1] > 0) ok = issue_s(sis1, 1, dq1, kv_it % kStages);
-        if (ok && it.nmax == 1) tc_commit_elect(bar(kBarQEmpty));
+        if (nkv == 0 && lane == 0) mbar_arrive(bar(kBarQEmpty));
         for (int j = 0; ok && j < it.nmax; ++j) {
           const uint32_t kvj = kv_it + j;
           const uint32_t st = kvj % kStages;
+          const uint32_t ph = (kvj / kStages) & 1;
+          if (j == 0) {
+            ok = mbar_wait_warp(bar(kBarKFull + st), ph);
+            if (!ok) break;
+            if (nkv > 0) {
+              ok = issue_s(st);
+              if (!ok) break;
+              tc_commit_elect(bar(kBarKEmpty + st));
+              if (nkv == 1) tc_commit_elect(bar(kBarQEmpty));
+            } else if (lane == 0) {
+              mbar_arrive(bar(kBarKEmpty + st));
+            }
+          }
+          // look ahead: the next key tile's scores
           if (j + 1 < it.nmax) {
             const uint32_t st1 = (kvj + 1) % kStages;
             ok = mbar_wait_warp(bar(kBarKFull + st1), ((kvj + 1) / kStages) & 1);
-            if (ok && j + 1 < it.nkv[0]) ok = issue_s(sis0, 0, dq0, st1);
-            if (ok && j + 1 < it.nkv[1]) ok = issue_s(sis1, 1, dq1, st1);
-            if (ok && j + 1 == it.nmax - 1) tc_commit_elect(bar(kBarQEmpty));
+            if (!ok) break;
+            if (j + 1 < nkv) {
+              ok = issue_s(st1);
+              if (!ok) break;
+              tc_commit_elect(bar(kBarKEmpty + st1));
+              if (j + 1 == nkv - 1) tc_commit_elect(bar(kBarQEmpty));
+            } else if (lane == 0) {
+              mbar_arrive(bar(kBarKEmpty + st1));
+            }
           }
-          if (ok && j < it.nkv[0]) ok = issue_pv(pvc0, ocnt0, 0, j, st, kvj);
-          if (ok && j < it.nkv[1]) ok = issue_pv(pvc1, ocnt1, 1, j, st, kvj);
-          if (ok) tc_commit_elect(bar(kBarKVEmpty + st));
+          // this key tile's P.V
+          if (j < nkv) {
+            ok = mbar_wait_warp(bar(kBarPFull + x), pvc & 1);
+            if (ok && j == 0 && ocnt > 0) ok = mbar_wait_warp(bar(kBarOFree + x), (ocnt - 1) & 1);
+            if (ok) ok = mbar_wait_warp(bar(kBarVFull + st), ph);
+            tc_fence_after();
+            if (!ok) break;
+            const uint64_t dv = dv0 + st * kStageStep;
+#pragma unroll
+            for (int kk = 0; kk < kBN / 16; ++kk)
+              umma_bf16_ts_elect(o_col, p_col + kk * 8, dv + 128 * kk, kIdescPV,
+                                 (j > 0 || kk > 0) ? 1u : 0u);
+            tc_commit_elect(bar(kBarODone + x));
+            tc_commit_elect(bar(kBarVEmpty + st));
+            ++pvc;
+          } else {
+            ok = mbar_wait_warp(bar(kBarVFull + st), ph);
+            if (!ok) break;
+            if (lane == 0) mbar_arrive(bar(kBarVEmpty + st));
+          }
         }
         kv_it += it.nmax;
-        if (it.nkv[0] > 0) ++ocnt0;
-        if (it.nkv[1] > 0) ++ocnt1;
+        if (nkv > 0) ++ocnt;
       }
       if (!ok && lane == 0) {
         record_error(p.status);
