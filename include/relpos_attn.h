@@ -60,6 +60,8 @@ extern "C" {
 #define RELPOS_ERR_UNSUPPORTED (-2)    /* valid request this build does not run (d != 64, ...) */
 #define RELPOS_ERR_CUDA (-3)           /* a CUDA runtime call or launch failed */
 #define RELPOS_ERR_DEVICE_TIMEOUT (-4) /* a kernel gave up on a bounded wait */
+#define RELPOS_ERR_SCRATCH_LIMIT (-5)  /* request needs more than the fixed scratch of
+                                          relpos_t5_decode_noalloc */
 
 /*
  * relpos_attn_fwd -- attention forward with an in-kernel relative term.
@@ -135,6 +137,37 @@ const char* relpos_strerror(int code);
  * hanging the GPU. Asynchronous; read the result with relpos_check_status().
  */
 int relpos_selftest_wait_timeout(int timeout_us, void* stream);
+
+/*
+ * relpos_t5_decode_noalloc -- T5-bias cached decoding that allocates nothing.
+ *
+ * The pages have no counterpart to this call: it exists for callers that
+ * cannot allocate device memory while they run -- code working inside a
+ * memory budget planned ahead, or a serving loop that must keep the
+ * allocator (cudaMallocAsync can synchronize or fail once the pool is
+ * exhausted) off its hot path. It computes exactly what relpos_attn_fwd
+ * computes for mode RELPOS_T5, dtype RELPOS_BF16 and Lq <= 8 (the split-key
+ * decode path), but keeps the per-chunk partial results in one static
+ * device array of 4 MiB built into the library, which every GPU that loads
+ * the library holds until the process exits.
+ *
+ *   Q, K, V, bias, out, B, H, Lq, Lk, num_buckets, max_distance, causal,
+ *   q_offset, stream: as for relpos_attn_fwd (bf16 Q/K/V/out, d = 64, fp32
+ *   bias [num_buckets, H]); Lq must be <= 8 (RELPOS_ERR_UNSUPPORTED otherwise).
+ * Limit: B * H * Lq * ceil(Lk / 256) * 264 bytes must fit in the 4 MiB array
+ *   (for example B * H = 512 single-row queries over 4096 keys take 2.2 MiB);
+ *   larger requests return RELPOS_ERR_SCRATCH_LIMIT before anything launches.
+ * No cudaMalloc, cudaFree or allocating library routine is called. The first
+ * call on each device looks up the array's device address (with that device
+ * current); make that first call before any stream capture. Every call
+ * shares the one array, so calls whose kernels overlap on the GPU (other
+ * streams, other host threads) race and corrupt each other's results; order
+ * them on one stream. Each call overwrites every partial it reads, so nothing
+ * has to be cleared between calls. Asynchronous on `stream`.
+ */
+int relpos_t5_decode_noalloc(const void* Q, const void* K, const void* V, const void* bias, int B,
+                             int H, int Lq, int Lk, int num_buckets, int max_distance, int causal,
+                             int q_offset, void* out, void* stream);
 
 #ifdef __cplusplus
 }

@@ -1,0 +1,75 @@
+"""The no-allocation decode entry point against the allocating one.
+
+relpos_t5_decode_noalloc serves callers that cannot allocate device memory
+while they run (a pre-planned memory budget, an allocator-free serving hot
+path): its partial results live in a fixed 4 MiB device array inside the
+library. This file runs last (pytest collects it after the others) so that a
+run stopping at the first failure has already run every other test; it
+passes both alone in a fresh process and after the rest of the suite.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import gpu_util as G
+import transformer_attention_relative_gb300 as rp
+from transformer_attention_relative_gb300.workloads import WORKLOADS, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    G.ensure_built()
+
+
+def _p(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _noalloc(w, d, out):
+    s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    return rp.relpos_t5_decode_noalloc(_p(d["Q"]), _p(d["K"]), _p(d["V"]), _p(d["table0"]),
+                                       w.B, w.H, w.Lq, w.Lk, w.num_buckets, w.rel_param,
+                                       int(w.causal), w.q_offset, _p(out), s)
+
+
+def test_noalloc_matches_allocating_entry_point_twice_in_a_row():
+    """Two consecutive calls (different inputs, so the shared array is reused)
+    each match relpos_attn_fwd within the parity tolerance."""
+    base = WORKLOADS["t5_decode"]
+    cases = [base.replace(B=8, H=16),                                  # 4096 keys, 16 chunks
+             base.replace(B=4, H=8, Lq=3, Lk=1500, q_offset=2000)]     # ragged, several rows
+    dev = torch.device("cuda")
+    for k, w in enumerate(cases):
+        x = make_inputs(w, seed=7000 + k)
+        d = {n: (t.to(dev) if t is not None else None) for n, t in x.items()}
+        want = rp.attention(d["Q"], d["K"], d["V"], d["table0"], mode=w.mode,
+                            num_buckets=w.num_buckets, rel_param=w.rel_param, causal=w.causal,
+                            q_offset=w.q_offset)
+        got = torch.full_like(want, float("nan"))
+        assert _noalloc(w, d, got) == rp.RELPOS_OK
+        torch.cuda.synchronize()
+        assert rp.check_status() == 0
+        G.compare(got.float().cpu().double().numpy(), want.float().cpu().double().numpy(),
+                  what=f"noalloc case {k}")
+
+
+def test_noalloc_rejects_requests_beyond_its_scratch():
+    """B*H*Lq*ceil(Lk/256) partials of 264 bytes must fit in 4 MiB; beyond
+    that the call answers RELPOS_ERR_SCRATCH_LIMIT before launching."""
+    w = WORKLOADS["t5_decode"].replace(B=64, H=16, Lq=2, Lk=4096, q_offset=4094)
+    dev = torch.device("cuda")
+    q = torch.zeros(w.B, w.H, w.Lq, 64, dtype=torch.bfloat16, device=dev)
+    kv = torch.zeros(1, 1, 1, 64, dtype=torch.bfloat16, device=dev)
+    bias = torch.zeros(32, w.H, device=dev)
+    out = torch.zeros_like(q)
+    s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    rc = rp.relpos_t5_decode_noalloc(_p(q), _p(kv), _p(kv), _p(bias), w.B, w.H, w.Lq, w.Lk, 32,
+                                     128, 1, w.q_offset, _p(out), s)
+    assert rc == rp.RELPOS_ERR_SCRATCH_LIMIT
+    assert "scratch" in rp.relpos_strerror(rc)
+    assert torch.count_nonzero(out).item() == 0
+    assert np.isfinite(out.float().cpu().numpy()).all()

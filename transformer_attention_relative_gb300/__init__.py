@@ -24,9 +24,10 @@ RELPOS_ERR_INVALID_ARG = -1
 RELPOS_ERR_UNSUPPORTED = -2
 RELPOS_ERR_CUDA = -3
 RELPOS_ERR_DEVICE_TIMEOUT = -4
+RELPOS_ERR_SCRATCH_LIMIT = -5
 
 EXPORTED = ("relpos_attn_fwd", "relpos_index_ids", "relpos_check_status", "relpos_strerror",
-            "relpos_selftest_wait_timeout")
+            "relpos_selftest_wait_timeout", "relpos_t5_decode_noalloc")
 
 _lib = None
 
@@ -57,6 +58,8 @@ def load_library(path: str = LIB_PATH):
     lib.relpos_strerror.restype = ctypes.c_char_p
     lib.relpos_selftest_wait_timeout.argtypes = [i, vp]
     lib.relpos_selftest_wait_timeout.restype = i
+    lib.relpos_t5_decode_noalloc.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, i, vp, vp]
+    lib.relpos_t5_decode_noalloc.restype = i
     _lib = lib
     return lib
 
@@ -84,6 +87,15 @@ def relpos_strerror(code: int) -> str:
 
 def relpos_selftest_wait_timeout(timeout_us: int, stream) -> int:
     return load_library().relpos_selftest_wait_timeout(timeout_us, stream)
+
+
+def relpos_t5_decode_noalloc(Q, K, V, bias, B, H, Lq, Lk, num_buckets, max_distance, causal,
+                             q_offset, out, stream) -> int:
+    """T5 cached decode for callers that cannot allocate device memory: the
+    partials live in the library's fixed 4 MiB device array (see the C
+    header for the size limit and the rule that overlapping calls race)."""
+    return load_library().relpos_t5_decode_noalloc(Q, K, V, bias, B, H, Lq, Lk, num_buckets,
+                                                   max_distance, causal, q_offset, out, stream)
 
 
 strerror = relpos_strerror

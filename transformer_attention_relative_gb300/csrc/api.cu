@@ -83,6 +83,8 @@ bool make_tmap(CUtensorMap* m, const void* base, int L, int BH) {
   return r == CUDA_SUCCESS;
 }
 
+}  // namespace
+
 // Thresholds of the T5 log buckets: thr[q] is the smallest distance n whose
 // bucket within a half is >= exact + q + 1, found by evaluating the pages'
 // formula exact + int(log(n / exact) / log(max_distance / exact) * (S - exact))
@@ -131,6 +133,8 @@ int check_rel_params(int mode, int num_buckets, int rel_param, int causal) {
   }
   return RELPOS_OK;
 }
+
+namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -194,6 +198,7 @@ extern "C" const char* relpos_strerror(int code) {
     case RELPOS_ERR_UNSUPPORTED: return "unsupported by this build";
     case RELPOS_ERR_CUDA: return "CUDA error";
     case RELPOS_ERR_DEVICE_TIMEOUT: return "device-side bounded wait timed out";
+    case RELPOS_ERR_SCRATCH_LIMIT: return "request exceeds the fixed scratch of the no-allocation decode";
     default: return "unknown error";
   }
 }

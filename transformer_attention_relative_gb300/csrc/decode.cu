@@ -12,8 +12,13 @@
 
 #include <cuda_bf16.h>
 
+#include <algorithm>
+#include <cmath>
 #include <cstdint>
+#include <cstring>
+#include <mutex>
 
+#include "../../include/relpos_attn.h"
 #include "ptx.cuh"
 #include "relpos_common.cuh"
 #include "relpos_internal.h"
@@ -185,3 +190,100 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream) {
 }
 
 }  // namespace relpos
+
+// ---------------------------------------------------------------------------
+// Decode without allocation. Some callers cannot allocate device memory at
+// call time: code running inside a pre-planned memory budget, or a serving
+// loop that must not touch the allocator on the hot path (cudaMallocAsync
+// can synchronize or fail when the pool is exhausted). This variant of the
+// split-key decode keeps its per-chunk partials in a fixed static device
+// array instead of drawing scratch from the stream's pool.
+
+namespace relpos {
+namespace {
+
+// Partials of at most kNoAllocScratchBytes: each (query row, key chunk) pair
+// needs 66 floats (64 output values, max, sum). Every GPU that loads the
+// library holds this array until the process exits.
+constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;  // 4 MiB
+__device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kNoAllocMaxDevices = 64;
+float* g_noalloc_ptr[kNoAllocMaxDevices];
+std::mutex g_noalloc_mu;
+
+// Device address of the static scratch on the current device, looked up once
+// per device with that device current (host code cannot use the symbol).
+float* noalloc_scratch() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    g_noalloc_ptr[dev] = static_cast<float*>(ptr);
+  }
+  return g_noalloc_ptr[dev];
+}
+
+}  // namespace
+}  // namespace relpos
+
+extern "C" int relpos_t5_decode_noalloc(const void* Q, const void* K, const void* V,
+                                        const void* bias, int B, int H, int Lq, int Lk,
+                                        int num_buckets, int max_distance, int causal,
+                                        int q_offset, void* out, void* stream) {
+  using namespace relpos;
+  int rc = check_rel_params(RELPOS_T5, num_buckets, max_distance, causal);
+  if (rc != RELPOS_OK) return rc;
+  if (B < 0 || H < 0 || Lq < 0 || Lk < 0 || q_offset < 0) return RELPOS_ERR_INVALID_ARG;
+  if (Lq > 8) return RELPOS_ERR_UNSUPPORTED;  // decode shapes only
+  if (B == 0 || H == 0 || Lq == 0) return RELPOS_OK;
+  if (static_cast<long long>(B) * H > 65535 || Lk > (1 << 24) || q_offset > (1 << 28))
+    return RELPOS_ERR_UNSUPPORTED;
+  if (!Q || !out) return RELPOS_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t rows = static_cast<size_t>(B) * H * Lq;
+  if (Lk == 0)
+    return cudaMemsetAsync(out, 0, rows * kHeadDim * 2, s) == cudaSuccess ? RELPOS_OK
+                                                                           : RELPOS_ERR_CUDA;
+  if (!K || !V || !bias) return RELPOS_ERR_INVALID_ARG;
+  const int chunk = decode_chunk_keys();
+  const int nchunks = (Lk + chunk - 1) / chunk;
+  const size_t need = rows * nchunks * (kHeadDim + 2) * sizeof(float);
+  if (need > kNoAllocScratchBytes) return RELPOS_ERR_SCRATCH_LIMIT;
+  float* scratch = noalloc_scratch();
+  if (!scratch) return RELPOS_ERR_CUDA;
+
+  T5Index t5;
+  int R = 0;
+  const long long nmax = std::max(static_cast<long long>(Lk) - 1,
+                                  static_cast<long long>(Lq) - 1 + q_offset);
+  rc = t5_setup(num_buckets, max_distance, causal, nmax, &t5, &R);
+  if (rc != RELPOS_OK) return rc;
+
+  DecodeParams dp;
+  std::memset(&dp, 0, sizeof(dp));
+  dp.Q = static_cast<const __nv_bfloat16*>(Q);
+  dp.K = static_cast<const __nv_bfloat16*>(K);
+  dp.V = static_cast<const __nv_bfloat16*>(V);
+  dp.bias = static_cast<const float*>(bias);
+  dp.B = B;
+  dp.H = H;
+  dp.Lq = Lq;
+  dp.Lk = Lk;
+  dp.causal = causal;
+  dp.q_offset = q_offset;
+  dp.scale_log2 = (1.0f / std::sqrt(static_cast<float>(kHeadDim))) * kLog2e;
+  dp.chunk = chunk;
+  dp.nchunks = nchunks;
+  dp.part_o = scratch;
+  dp.part_ml = scratch + rows * nchunks * kHeadDim;
+  dp.out = out;
+  dp.out_f32 = 0;
+  dp.t5 = t5;
+  return launch_decode(dp, s) == cudaSuccess ? RELPOS_OK : RELPOS_ERR_CUDA;
+}

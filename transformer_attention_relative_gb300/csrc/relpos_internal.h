@@ -16,6 +16,11 @@ int fwd_num_items(const FwdParams& p);
 cudaError_t launch_fwd(int mode, bool out_f32, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                        const CUtensorMap& tmV, const FwdParams& p, int num_sms, cudaStream_t stream);
 
+// T5 bucket thresholds for offsets up to nmax (see api.cu) and the shared
+// relative-parameter checks; both return RELPOS_* codes.
+int t5_setup(int num_buckets, int max_distance, int causal, long long nmax, T5Index* ix, int* R);
+int check_rel_params(int mode, int num_buckets, int rel_param, int causal);
+
 int decode_chunk_keys();
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);
 
