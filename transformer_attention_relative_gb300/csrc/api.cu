@@ -83,6 +83,22 @@ bool make_tmap(CUtensorMap* m, const void* base, int L, int BH) {
   return r == CUDA_SUCCESS;
 }
 
+// DeBERTa table [rows = 2k, H, 64] bf16: boxes of 256 table rows of one head
+bool make_tmap_table(CUtensorMap* m, const void* base, int H, int rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(H),
+                        static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim) * 2,
+                           static_cast<cuuint64_t>(H) * kHeadDim * 2};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(kHeadDim), 1u, 256u};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 // Thresholds of the T5 log buckets: thr[q] is the smallest distance n whose
@@ -279,7 +295,7 @@ extern "C" int relpos_attn_fwd(int mode, int dtype, const void* Q, const void* K
   if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(out) || !aligned16(table0) ||
       (table1 && !aligned16(table1)))
     return RELPOS_ERR_INVALID_ARG;
-  if (mode == RELPOS_DEBERTA) return RELPOS_ERR_UNSUPPORTED;
+  if (mode == RELPOS_DEBERTA && rel_param > 4096) return RELPOS_ERR_UNSUPPORTED;
 
   int* status = status_ptr();
   if (!status) return RELPOS_ERR_CUDA;
@@ -319,6 +335,19 @@ extern "C" int relpos_attn_fwd(int mode, int dtype, const void* Q, const void* K
     scratch_bytes = (scratch_bytes + 255) & ~static_cast<size_t>(255);
     off_part = scratch_bytes;
     scratch_bytes += BH * Lq * nchunks * (kHeadDim + 2) * sizeof(float);
+  }
+  // DeBERTa: C2P [BH, Lq, 2k], P2C [BH, Lk, 2k] (bf16) and P2C's end columns
+  const size_t n2k = 2 * static_cast<size_t>(rel_param);
+  const int ends_pitch = (Lk + 127) & ~127;
+  size_t off_c2p = 0, off_p2c = 0, off_ends = 0;
+  if (mode == RELPOS_DEBERTA) {
+    scratch_bytes = (scratch_bytes + 255) & ~static_cast<size_t>(255);
+    off_c2p = scratch_bytes;
+    scratch_bytes += ((BH * Lq * n2k * 2) + 255) & ~static_cast<size_t>(255);
+    off_p2c = scratch_bytes;
+    scratch_bytes += ((BH * Lk * n2k * 2) + 255) & ~static_cast<size_t>(255);
+    off_ends = scratch_bytes;
+    scratch_bytes += BH * 2 * static_cast<size_t>(ends_pitch) * sizeof(float);
   }
   if (scratch_bytes) {
     if (cudaMallocAsync(&scratch, scratch_bytes, s) != cudaSuccess) return fail(RELPOS_ERR_CUDA);
@@ -383,6 +412,35 @@ extern "C" int relpos_attn_fwd(int mode, int dtype, const void* Q, const void* K
       p.aV = static_cast<const __nv_bfloat16*>(table1);
     }
     if (fwd_smem_bytes(mode, p) > fwd_max_smem_bytes()) return fail(RELPOS_ERR_UNSUPPORTED);
+    if (mode == RELPOS_DEBERTA) {
+      uint8_t* sc = static_cast<uint8_t*>(scratch);
+      p.c2p = reinterpret_cast<const __nv_bfloat16*>(sc + off_c2p);
+      p.p2c = reinterpret_cast<const __nv_bfloat16*>(sc + off_p2c);
+      p.p2c_ends = reinterpret_cast<const float*>(sc + off_ends);
+      p.ends_pitch = ends_pitch;
+      CUtensorMap ta, tpk, tpq;
+      ProjParams pp;
+      std::memset(&pp, 0, sizeof(pp));
+      pp.BH = static_cast<int>(BH);
+      pp.H = H;
+      pp.k = rel_param;
+      pp.scale = scale * kLog2e;
+      pp.status = status;
+      if (!make_tmap_table(&tpk, table0, H, static_cast<int>(n2k)) ||
+          !make_tmap_table(&tpq, table1, H, static_cast<int>(n2k)) ||
+          !make_tmap(&ta, Qb, Lq, static_cast<int>(BH)))
+        return fail(RELPOS_ERR_CUDA);
+      pp.L = Lq;
+      pp.out = reinterpret_cast<__nv_bfloat16*>(sc + off_c2p);
+      pp.ends = nullptr;
+      if (launch_deberta_proj(false, ta, tpk, pp, s) != cudaSuccess) return fail(RELPOS_ERR_CUDA);
+      if (!make_tmap(&ta, Kb, Lk, static_cast<int>(BH))) return fail(RELPOS_ERR_CUDA);
+      pp.L = Lk;
+      pp.out = reinterpret_cast<__nv_bfloat16*>(sc + off_p2c);
+      pp.ends = reinterpret_cast<float*>(sc + off_ends);
+      pp.ends_pitch = ends_pitch;
+      if (launch_deberta_proj(true, ta, tpq, pp, s) != cudaSuccess) return fail(RELPOS_ERR_CUDA);
+    }
     CUtensorMap tq, tk, tv;
     if (!make_tmap(&tq, Qb, Lq, static_cast<int>(BH)) || !make_tmap(&tk, Kb, Lk, static_cast<int>(BH)) ||
         !make_tmap(&tv, Vb, Lk, static_cast<int>(BH)))

@@ -425,6 +425,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         add_l = qa[0];
         add_r = qa[2 * kc];
       }
+      const __nv_bfloat16* c2p_row = nullptr;  // DeBERTa: this row of C2P (log2 units)
+      const __nv_bfloat16* p2c_head = nullptr;  // DeBERTa: this head's P2C
+      if constexpr (MODE == 2) {
+        const int n2k = 2 * kc;
+        const int rowc = min(i0 + t, p.Lq - 1);
+        c2p_row = p.c2p + (static_cast<size_t>(it.bh) * p.Lq + rowc) * n2k;
+        p2c_head = p.p2c + static_cast<size_t>(it.bh) * p.Lk * n2k;
+        // keys far behind (i - j >= k) take delta(i, j) = 2k - 1; far ahead, 0
+        add_l = __bfloat162float(c2p_row[n2k - 1]);
+        add_r = __bfloat162float(c2p_row[0]);
+      }
       float mass_l = 0.f, mass_r = 0.f;
 
       float m_run = kNegInf;
@@ -466,7 +477,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         float mx;
         float addc = 0.f;  // far tiles: the constant still to add
-        const bool far = far_l || far_r;
+        // DeBERTa tiles beyond the band still carry a per-key term, so every
+        // DeBERTa tile takes the per-element path below
+        const bool far = MODE != 2 && (far_l || far_r);
         if (far) {
           // logits are s * sl2 + addc; the max is taken on raw s
           addc = far_l ? add_l : add_r;
@@ -507,6 +520,42 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < 128; ++c) {
               const int r = min(max(r0 + c, -kc), kc) + kc;
               xs[c] = fmaf(xs[c], sl2, qa[r]);
+            }
+          } else if constexpr (MODE == 2) {
+            if (far_l || far_r) {
+              // c2p: one value per row; p2c: the saturated end column of every key
+              const float rc = far_l ? add_l : add_r;
+              const float4* ce = reinterpret_cast<const float4*>(
+                  p.p2c_ends + (static_cast<size_t>(it.bh) * 2 + (far_l ? 0 : 1)) * p.ends_pitch + j0);
+              const float2 sc2 = make_float2(sl2, sl2);
+              const float2 rc2 = make_float2(rc, rc);
+#pragma unroll
+              for (int q = 0; q < 32; ++q) {
+                const float4 e = __ldg(ce + q);
+                float2 a = __ffma2_rn(make_float2(xs[4 * q], xs[4 * q + 1]), sc2,
+                                      __fadd2_rn(make_float2(e.x, e.y), rc2));
+                float2 b = __ffma2_rn(make_float2(xs[4 * q + 2], xs[4 * q + 3]), sc2,
+                                      __fadd2_rn(make_float2(e.z, e.w), rc2));
+                xs[4 * q] = a.x;
+                xs[4 * q + 1] = a.y;
+                xs[4 * q + 2] = b.x;
+                xs[4 * q + 3] = b.y;
+              }
+            } else {
+              // band: c2p = C2P[i][delta(i, j)], p2c = P2C[j][delta(j, i)]
+              const int n2k = 2 * kc;
+              const int r0 = j0 - prow;  // key - query offset of column 0
+              const int jmax = p.Lk - 1 - j0;
+#pragma unroll
+              for (int c = 0; c < 128; ++c) {
+                const int rel = r0 + c;
+                const int d_ij = min(max(-rel, -kc), kc - 1) + kc;
+                const int d_ji = min(max(rel, -kc), kc - 1) + kc;
+                const int jj = j0 + min(c, jmax);
+                const float a = __bfloat162float(c2p_row[d_ij]);
+                const float b = __bfloat162float(p2c_head[static_cast<size_t>(jj) * n2k + d_ji]);
+                xs[c] = fmaf(xs[c], sl2, a + b);
+              }
             }
           }
           if (need_mask) {
@@ -736,6 +785,8 @@ cudaError_t launch_fwd(int mode, bool out_f32, const CUtensorMap& tmQ, const CUt
     kern = out_f32 ? relpos_fwd_kernel<0, true> : relpos_fwd_kernel<0, false>;
   } else if (mode == 1) {
     kern = out_f32 ? relpos_fwd_kernel<1, true> : relpos_fwd_kernel<1, false>;
+  } else if (mode == 2) {
+    kern = out_f32 ? relpos_fwd_kernel<2, true> : relpos_fwd_kernel<2, false>;
   } else {
     return cudaErrorNotSupported;
   }

@@ -75,7 +75,21 @@ struct FwdParams {
   // DeBERTa
   const __nv_bfloat16* Pk;  // [2k, H, 64]
   const __nv_bfloat16* Pq;  // [2k, H, 64]
-  int kclip;                // Shaw / DeBERTa clip k
+  const __nv_bfloat16* c2p;  // [B*H, Lq, 2k]: log2-scaled q_i . Pk[r]
+  const __nv_bfloat16* p2c;  // [B*H, Lk, 2k]: log2-scaled k_j . Pq[r]
+  const float* p2c_ends;     // [B*H, 2, ends_pitch]: P2C columns 0 and 2k - 1
+  int ends_pitch;            // Lk rounded up to a multiple of 128
+  int kclip;                 // Shaw / DeBERTa clip k
+};
+
+// DeBERTa relative products (deberta_proj.cu)
+struct ProjParams {
+  int BH, H, L, k;
+  float scale;          // applied to every product (softmax scale times log2 e)
+  __nv_bfloat16* out;   // [BH, L, 2k]
+  float* ends;          // [BH, 2, ends_pitch] or null
+  int ends_pitch;
+  int* status;
 };
 
 struct DecodeParams {
