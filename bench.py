@@ -10,7 +10,9 @@ JSON line (rank 0).
                     [--impl ours|reference] [--no-others]
 
 Timing: W untimed steps, then K steps bracketed by a barrier and a device
-synchronize, timed with CUDA events on the launching stream. Consecutive
+synchronize, timed with CUDA events on the launching stream; the K steps are
+replayed from CUDA graphs that captured the library calls' launches, so the
+host's launch rate does not limit the measurement. Consecutive
 steps rotate over several copies of the inputs whose total exceeds the L2
 cache, so every step reads its operands from HBM. SM clocks and throttle
 reasons are sampled with nvidia-smi while the steps run.
@@ -200,20 +202,45 @@ class GpuRun:
     def step(self, i):
         self._call(self.sets[i % self.nsets])
 
+    def _graph(self, n, first):
+        """CUDA graph of n consecutive steps (steps first .. first + n - 1)."""
+        import torch
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=self.stream):
+            for i in range(n):
+                self.step(first + i)
+        return g
+
     def timed(self, steps, warmup, barrier):
+        """Time exactly `steps` steps. The steps are replayed from CUDA graphs
+        (the launch sequence of the library calls, captured once), so the
+        number measures the device, not the host's launch rate."""
         import torch
         for i in range(warmup):
             self.step(i)
+        torch.cuda.synchronize()
+        per = self.nsets * max(1, math.ceil(32 / self.nsets))
+        per = min(per, steps)
+        reps, rem = divmod(steps, per)
+        g_main = self._graph(per, 0)
+        g_rem = self._graph(rem, 0) if rem else None
+        with torch.cuda.stream(self.stream):  # replay() launches on the current stream
+            g_main.replay()
+            if g_rem is not None:
+                g_rem.replay()
         torch.cuda.synchronize()
         barrier()
         torch.cuda.synchronize()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         t0 = time.time()
-        e0.record(self.stream)
-        for i in range(steps):
-            self.step(i)
-        e1.record(self.stream)
+        with torch.cuda.stream(self.stream):
+            e0.record(self.stream)
+            for _ in range(reps):
+                g_main.replay()
+            if g_rem is not None:
+                g_rem.replay()
+            e1.record(self.stream)
         torch.cuda.synchronize()
         t1 = time.time()
         barrier()
@@ -223,12 +250,12 @@ class GpuRun:
     def sustain(self, seconds):
         """Run steps back to back for about `seconds` (clock sampling window)."""
         import torch
+        g = self._graph(self.nsets * max(1, math.ceil(32 / self.nsets)), 0)
         t0 = time.time()
-        n = 0
         while time.time() - t0 < seconds:
-            for _ in range(50):
-                self.step(n)
-                n += 1
+            with torch.cuda.stream(self.stream):
+                for _ in range(20):
+                    g.replay()
             torch.cuda.synchronize()
         return t0, time.time()
 
@@ -380,13 +407,8 @@ def main():
     for i in range(max(3, args.warmup)):
         g.step(i)
     torch.cuda.synchronize()
-    est = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    est[0].record(stream)
-    for i in range(20):
-        g.step(i)
-    est[1].record(stream)
-    torch.cuda.synchronize()
-    t_est = est[0].elapsed_time(est[1]) / 20 / 1e3
+    ms_est, _, _ = g.timed(g.nsets * max(1, math.ceil(32 / g.nsets)), 1, lambda: None)
+    t_est = ms_est / (g.nsets * max(1, math.ceil(32 / g.nsets))) / 1e3
     steps = args.steps if args.steps is not None else max(20, min(200000, int(2.0 / t_est)))
     warmup = max(3, args.warmup)
 

@@ -39,6 +39,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include <atomic>
 #include <cstdint>
 
 #include "ptx.cuh"
@@ -118,6 +119,14 @@ RP_DEVI Item make_item(const FwdParams& p, int w) {
   }
   it.nmax = max(it.nkv[0], it.nkv[1]);
   return it;
+}
+
+// The item a CTA takes in round r: items are ordered longest first, and the
+// CTAs sweep them in alternating directions (round 0 left to right, round 1
+// right to left, ...) so that long and short causal items pair up.
+RP_DEVI int item_at(int r) {
+  const int g = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+  return r * g + ((r & 1) ? g - 1 - c : c);
 }
 
 // T5 per-WG bias-by-offset table: 4 copies shifted by one entry each, so any
@@ -204,7 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       uint32_t it_cnt = 0;
       int item_cnt = 0;
-      for (int w = blockIdx.x; ok && w < nitems; w += gridDim.x, ++item_cnt) {
+      for (int rr = 0, w = item_at(0); ok && w < nitems; w = item_at(++rr), ++item_cnt) {
         const Item it = make_item(p, w);
         if (kq) {
           if (item_cnt > 0) ok = mbar_wait_warp(bar(kBarQEmpty), (item_cnt - 1) & 1);
@@ -266,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++sis;
         return true;
       };
-      for (int w = blockIdx.x; ok && w < nitems; w += gridDim.x, ++item_cnt) {
+      for (int rr = 0, w = item_at(0); ok && w < nitems; w = item_at(++rr), ++item_cnt) {
         const Item it = make_item(p, w);
         const int nkv = it.nkv[x];
         ok = mbar_wait_warp(bar(kBarQFull), item_cnt & 1);
@@ -363,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int kc = p.kclip;
 
     uint32_t cnt = 0, ocnt = 0;
-    for (int w = blockIdx.x; !err && w < nitems; w += gridDim.x) {
+    for (int rr = 0, w = item_at(0); !err && w < nitems; w = item_at(++rr)) {
       const Item it = make_item(p, w);
       const int n_kv = it.nkv[x];
       if (n_kv == 0) continue;
@@ -790,9 +799,19 @@ cudaError_t launch_fwd(int mode, bool out_f32, const CUtensorMap& tmQ, const CUt
   } else {
     return cudaErrorNotSupported;
   }
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
+  // raise the kernel's shared-memory limit once per device (the maximum, so
+  // that every later launch fits)
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+  const int slot = mode * 2 + (out_f32 ? 1 : 0);
+  static std::atomic<uint64_t> attr_set[6];
+  const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
+  if (!bit || !(attr_set[slot].load() & bit)) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(fwd_max_smem_bytes()));
+    if (e != cudaSuccess) return e;
+    attr_set[slot].fetch_or(bit);
+  }
   kern<<<grid, block, smem, stream>>>(tmQ, tmK, tmV, p);
   return cudaGetLastError();
 }
