@@ -49,7 +49,7 @@ __global__ void __launch_bounds__(128, 1)
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t sbase = (raw_addr + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (sbase - raw_addr);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
   const int t = threadIdx.x;
   const int i0 = blockIdx.x * kRows;
   const int bh = blockIdx.y;
