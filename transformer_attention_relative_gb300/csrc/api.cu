@@ -384,6 +384,7 @@ extern "C" int relpos_attn_fwd(int mode, int dtype, const void* Q, const void* K
     dp.out = out;
     dp.out_f32 = dtype == RELPOS_FP32;
     dp.t5 = t5;
+    dp.t5_R = R;
     if (launch_decode(dp, s) != cudaSuccess) return fail(RELPOS_ERR_CUDA);
   } else {
     FwdParams p;

@@ -40,7 +40,7 @@ RP_DEVI void bf16x8_to_f32(const uint4& u, float (&f)[8]) {
   }
 }
 
-__global__ void __launch_bounds__(kDecThreads) relpos_decode_partial_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kDecThreads, 3) relpos_decode_partial_kernel(const DecodeParams p) {
   const int chunk = blockIdx.x;
   const int qi = blockIdx.y;
   const int bh = blockIdx.z;
@@ -50,7 +50,7 @@ __global__ void __launch_bounds__(kDecThreads) relpos_decode_partial_kernel(cons
   const int sl = tid & 7;    // 8-dim slice of the head dimension
   const int warp = tid >> 5;
 
-  __shared__ float bias_s[128];
+  __shared__ float bias_s[kDecChunk];  // log2-scaled bias of each key of the chunk
   __shared__ float red_s[4];
   __shared__ float o_s[4][kHeadDim];
 
@@ -72,8 +72,21 @@ __global__ void __launch_bounds__(kDecThreads) relpos_decode_partial_kernel(cons
     return;
   }
 
-  const int nb = p.t5.bidir ? 2 * p.t5.slots : p.t5.slots;
-  for (int b = tid; b < nb; b += kDecThreads) bias_s[b] = __ldg(p.bias + b * p.H + h) * kLog2e;
+  // The chunk's offsets run from jb - pos to je - 1 - pos. Past the saturation
+  // distance R every key of a side takes that side's last bucket, so a chunk
+  // lying wholly beyond R needs one bias; otherwise each key's bias is looked
+  // up once here rather than by every thread that shares the key.
+  const int rel_first = jb - pos, rel_last = je - 1 - pos;
+  const bool sat_l = rel_last <= -p.t5_R;
+  const bool sat_r = p.t5.bidir && rel_first >= p.t5_R;
+  float bias_const = 0.f;
+  if (sat_l || sat_r) {
+    bias_const = __ldg(p.bias + t5_bucket_dev(sat_l ? -p.t5_R : p.t5_R, p.t5) * p.H + h) * kLog2e;
+  } else {
+    for (int r = tid; r < kDecChunk; r += kDecThreads)
+      bias_s[r] = __ldg(p.bias + t5_bucket_dev(jb + r - pos, p.t5) * p.H + h) * kLog2e;
+  }
+  const bool sat = sat_l || sat_r;
 
   // issue every K and V load of this thread first
   const uint4* kbase = reinterpret_cast<const uint4*>(p.K + static_cast<size_t>(bh) * p.Lk * kHeadDim);
@@ -110,7 +123,7 @@ __global__ void __launch_bounds__(kDecThreads) relpos_decode_partial_kernel(cons
     acc += __shfl_xor_sync(0xffffffffu, acc, 2);
     acc += __shfl_xor_sync(0xffffffffu, acc, 4);
     const int j = jb + grp + 16 * r;
-    const float bias = bias_s[t5_bucket_dev(j - pos, p.t5)];
+    const float bias = sat ? bias_const : bias_s[grp + 16 * r];
     s[r] = (j < je) ? fmaf(acc, p.scale_log2, bias) : -INFINITY;
     mx = fmaxf(mx, s[r]);
   }
@@ -285,5 +298,6 @@ extern "C" int relpos_t5_decode_noalloc(const void* Q, const void* K, const void
   dp.out = out;
   dp.out_f32 = 0;
   dp.t5 = t5;
+  dp.t5_R = R;
   return launch_decode(dp, s) == cudaSuccess ? RELPOS_OK : RELPOS_ERR_CUDA;
 }

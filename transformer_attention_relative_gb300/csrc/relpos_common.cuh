@@ -106,6 +106,7 @@ struct DecodeParams {
   float* part_ml;  // [B*H*Lq, nchunks, 2]
   void* out;
   int out_f32;
+  int t5_R;  // |offset| >= R: the side's last bucket
   T5Index t5;
 };
 
