@@ -405,6 +405,7 @@ extern "C" int relpos_attn_fwd(int mode, int dtype, const void* Q, const void* K
       p.bias = static_cast<const float*>(table0);
       p.t5 = t5;
       p.t5_R = R;
+      p.t5_nb = num_buckets;
       p.t5_tab_off = R + 254;
       p.t5_tab_len = 2 * R + 509;
       p.t5_tab_len4 = (p.t5_tab_len + 3) & ~3;

@@ -129,13 +129,34 @@ RP_DEVI int item_at(int r) {
   return r * g + ((r & 1) ? g - 1 - c : c);
 }
 
+// Head of the first item from round r on in which query tile x has rows, or -1.
+RP_DEVI int next_head(const FwdParams& p, int x, int r, int nitems) {
+  for (int w = item_at(r); w < nitems; w = item_at(++r))
+    if (make_item(p, w).nkv[x] > 0) return (w % (p.B * p.H)) % p.H;
+  return -1;
+}
+
 // T5 per-WG bias-by-offset table: 4 copies shifted by one entry each, so any
-// run of 128 consecutive offsets starts 16-byte aligned in one of them.
+// run of 128 consecutive offsets starts 16-byte aligned in one of them. A lane
+// reads copy (s & 3) for its window start s, and the lanes of a quarter-warp
+// hold 8 consecutive starts. Copy k is placed off[k] 16-byte chunks into its
+// 128-byte-aligned slot so that those 8 reads land on 8 distinct bank groups:
+// with r = (lowest start of the quarter) & 3, the rank q = (k - r) & 3 takes
+// chunk offset 2q, minus one for the copies whose windows begin one chunk
+// further on (k < r).
 struct T5Tab {
-  float* base;  // [2 buffers][4 copies][len4]
-  int len4;
-  RP_DEVI float* copy(int buf, int k) const { return base + (buf * 4 + k) * len4; }
+  float* base;  // [2 buffers][4 copies][stride]
+  int len4;     // entries per copy
+  int stride;   // floats per copy slot (multiple of 32, >= len4 + 28)
+  int r;
+  RP_DEVI float* copy(int buf, int k) const {
+    const int q = (k - r) & 3;
+    const int off = (2 * q - (k < r ? 1 : 0)) & 7;
+    return base + (buf * 4 + k) * stride + 4 * off;
+  }
 };
+
+RP_DEVI int t5_copy_stride(int len4) { return (len4 + 28 + 31) & ~31; }
 
 template <int MODE, bool OUT_F32>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -356,13 +377,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool err = false;
 
     T5Tab tab;
+    float* hbias = nullptr;  // T5: this head's bias per bucket (log2 units)
+    float hb_next = 0.f;     // T5: thread t < num_buckets holds entry t of the next table's row
     float* qa = nullptr;    // Shaw: q . a_K[r] of this row (log2 units)
     float* wbin = nullptr;  // Shaw: probability mass per clipped offset of this row
     const __nv_bfloat16* aV_s = nullptr;
     if constexpr (MODE == 0) {
       tab.len4 = p.t5_tab_len4;
-      const uint32_t bkt_bytes = (static_cast<uint32_t>(p.t5_tab_len4) + 4u + 15u) & ~15u;
-      tab.base = reinterpret_cast<float*>(aux + bkt_bytes) + x * 8 * p.t5_tab_len4;
+      tab.stride = t5_copy_stride(p.t5_tab_len4);
+      // every window start is j0 - (i0 + 32 w + lane + q_offset) + tab_off with
+      // j0, i0, 32 w multiples of 4: the lowest start of a quarter-warp is
+      // (tab_off - q_offset - 7) mod 4
+      tab.r = (((p.t5_tab_off - p.q_offset - 7) % 4) + 4) % 4;
+      const uint32_t bkt_bytes = (static_cast<uint32_t>(p.t5_tab_len4) + 4u + 127u) & ~127u;
+      tab.base = reinterpret_cast<float*>(aux + bkt_bytes) + x * 8 * tab.stride;
+      hbias = reinterpret_cast<float*>(aux + bkt_bytes) + 2 * 8 * tab.stride + x * 128;
     } else if constexpr (MODE == 1) {
       aV_s = reinterpret_cast<const __nv_bfloat16*>(aux + shaw_tbl);
       float* qa_all = reinterpret_cast<float*>(aux + 2 * shaw_tbl);
@@ -370,6 +399,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       wbin = qa_all + 2 * 128 * nrel + (x * 128 + t) * nrel;
     }
     const int kc = p.kclip;
+
+    // T5: fill table buffer b from the bias row in hb_next. The Tab barrier
+    // completes twice per table: once the row is staged in shared memory, and
+    // once every entry is written (awaited when the item starts).
+    auto t5_build = [&](int b) -> bool {
+      if (t < p.t5_nb) hbias[t] = hb_next * kLog2e;
+      mbar_arrive(bar(kBarTab + x));
+      if (!mbar_wait(bar(kBarTab + x), 0)) return false;
+      for (int y = 4 * t; y < tab.len4; y += 4 * 128) {
+        const uint32_t w0 = *reinterpret_cast<const uint32_t*>(bkt + y);
+        const uint32_t w1 = *reinterpret_cast<const uint32_t*>(bkt + y + 4);
+        float v[7];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) v[e] = hbias[(w0 >> (8 * e)) & 0xffu];
+#pragma unroll
+        for (int e = 0; e < 3; ++e) v[4 + e] = hbias[(w1 >> (8 * e)) & 0xffu];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          *reinterpret_cast<float4*>(tab.copy(b, k) + y) = make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]);
+      }
+      mbar_arrive(bar(kBarTab + x));
+      return true;
+    };
+    if constexpr (MODE == 0) {
+      const int h0 = next_head(p, x, 0, nitems);
+      if (h0 >= 0) {
+        if (t < p.t5_nb) hb_next = __ldg(p.bias + t * p.H + h0);
+        if (!t5_build(0)) err = true;
+      }
+    }
 
     uint32_t cnt = 0, ocnt = 0;
     for (int rr = 0, w = item_at(0); !err && w < nitems; w = item_at(++rr)) {
@@ -382,17 +441,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       // ---- per-item relative-term setup
       float add_l = 0.f, add_r = 0.f;
-      int buf = 0;
+      int buf = 0, next_h = -1;
       if constexpr (MODE == 0) {
+        // this item's table was filled at the end of the previous item (or in
+        // the prologue); fetch the next item's bias row meanwhile
         buf = ocnt & 1;
-        const float* bias_h = p.bias + it.h;
-        for (int y = t; y < tab.len4; y += 128) {
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            tab.copy(buf, k)[y] = __ldg(bias_h + bkt[y + k] * p.H) * kLog2e;
-        }
-        mbar_arrive(bar(kBarTab + x));
-        const bool ok = mbar_wait(bar(kBarTab + x), ocnt & 1);
+        next_h = next_head(p, x, rr + 1, nitems);
+        if (t < p.t5_nb && next_h >= 0) hb_next = __ldg(p.bias + t * p.H + next_h);
+        const bool ok = mbar_wait(bar(kBarTab + x), 1);
         err = __any_sync(0xffffffffu, !ok);
         if (err) break;
         add_l = tab.copy(buf, 0)[p.t5_tab_off - p.t5_R];
@@ -696,6 +752,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(bar(kBarPFull + x));
       }
       if (err) break;
+      if constexpr (MODE == 0) {
+        // the next item's table, while the last P.V of this one runs
+        if (next_h >= 0 && !t5_build((ocnt + 1) & 1)) {
+          err = true;
+          break;
+        }
+      }
 
       // ---- epilogue of this item
       {
@@ -769,8 +832,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 uint32_t fwd_smem_bytes(int mode, const FwdParams& p) {
   uint32_t aux = 0;
   if (mode == 0) {
-    const uint32_t bkt_bytes = (static_cast<uint32_t>(p.t5_tab_len4) + 4u + 15u) & ~15u;
-    aux = bkt_bytes + 2u * 8u * static_cast<uint32_t>(p.t5_tab_len4) * 4u;
+    const uint32_t bkt_bytes = (static_cast<uint32_t>(p.t5_tab_len4) + 4u + 127u) & ~127u;
+    const uint32_t stride = (static_cast<uint32_t>(p.t5_tab_len4) + 28u + 31u) & ~31u;
+    aux = bkt_bytes + 2u * 8u * stride * 4u + 2u * 128u * 4u;
   } else if (mode == 1) {
     const uint32_t nrel = 2u * p.kclip + 1u;
     const uint32_t tbl = (nrel * kHeadDim * 2u + 15u) & ~15u;

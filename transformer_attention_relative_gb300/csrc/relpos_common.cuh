@@ -66,6 +66,7 @@ struct FwdParams {
   int t5_tab_len;     // entries of the per-head bias-by-offset table
   int t5_tab_off;     // table index of offset 0
   int t5_tab_len4;    // t5_tab_len rounded up to a multiple of 4
+  int t5_nb;          // num_buckets (<= 128)
   T5Index t5;
   int npairs;         // 256-row query-tile pairs per head
   const __nv_bfloat16* Qg;  // Q in global memory (bf16 [B,H,Lq,64])
