@@ -38,15 +38,16 @@ RP_DEVI void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 // One bounded try: returns at once if the phase has completed, otherwise the
-// thread may sleep (up to ~1 ms) until it completes, instead of spinning.
+// thread may be suspended for a short, hardware-chosen time (woken early when
+// the phase completes) instead of spinning.
 RP_DEVI bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(1000000u)
+      : "r"(bar), "r"(parity)
       : "memory");
   return ok != 0;
 }
