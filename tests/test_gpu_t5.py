@@ -27,6 +27,8 @@ BASE = WORKLOADS["t5_base_bidir"]
     (1, 2, 200, 437, True, 237),    # causal with a cached prefix (q_offset)
     (1, 1, 40, 1000, True, 960),
     (2, 2, 513, 513, True, 0),
+    (1, 2, 256, 100, False, 0),     # one key tile: split items without a merge
+    (2, 2, 512, 384, False, 0),     # three key tiles: split 2 + 1, merged
 ])
 def test_t5_small(B, H, Lq, Lk, causal, qoff):
     w = BASE.replace(B=B, H=H, Lq=Lq, Lk=Lk, causal=causal, q_offset=qoff)

@@ -401,6 +401,7 @@ extern "C" int relpos_attn_fwd(int mode, int dtype, const void* Q, const void* K
     p.kclip = rel_param;
     p.Qg = static_cast<const __nv_bfloat16*>(Qb);
     p.npairs = (Lq + 255) / 256;
+    p.nsplit = fwd_split_items(B * H * p.npairs, B * H, Lq, causal, num_sms());
     if (mode == RELPOS_T5) {
       p.bias = static_cast<const float*>(table0);
       p.t5 = t5;
@@ -413,6 +414,7 @@ extern "C" int relpos_attn_fwd(int mode, int dtype, const void* Q, const void* K
       p.aK = static_cast<const __nv_bfloat16*>(table0);
       p.aV = static_cast<const __nv_bfloat16*>(table1);
     }
+    if (p.nsplit > 0 && fwd_smem_bytes(mode, p) > fwd_max_smem_bytes()) p.nsplit = 0;
     if (fwd_smem_bytes(mode, p) > fwd_max_smem_bytes()) return fail(RELPOS_ERR_UNSUPPORTED);
     if (mode == RELPOS_DEBERTA) {
       uint8_t* sc = static_cast<uint8_t*>(scratch);

@@ -59,6 +59,7 @@ constexpr uint32_t kOffK = kOffQ + 2 * kTileBytes;
 constexpr uint32_t kOffV = kOffK + kStages * kTileBytes;
 constexpr uint32_t kOffBar = kOffV + kStages * kTileBytes;
 constexpr uint32_t kOffAux = kOffBar + 512;
+constexpr uint32_t kCombBytes = 2 * 128 * 8;  // split items: (m, l) of every row, per tile
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemS = 0;
 constexpr uint32_t kTmemO = 256;
@@ -78,7 +79,8 @@ enum : uint32_t {
   kBarODone = kBarPFull + 2,
   kBarOFree = kBarODone + 2,
   kBarTab = kBarOFree + 2,
-  kBarFinal = kBarTab + 2,
+  kBarComb = kBarTab + 2,  // both softmax warpgroups have published a split item's partial state
+  kBarFinal = kBarComb + 1,
   kNumBars = kBarFinal + 1,
 };
 constexpr uint32_t kOffTmemSlot = 256;
@@ -92,34 +94,79 @@ RP_DEVI void record_error(int* status) {
   if (status) atomicCAS(status, 0, -4);
 }
 
-// One work item: query rows [i0, i0 + 256) of head bh, split in tiles a / b.
+// One work item. A pair item holds query rows [i0, i0 + 256) of head bh as
+// tiles a (rows from i0) and b (rows from i0 + 128); both visit the same key
+// tiles, which stream through shared memory once. A split item holds a single
+// 128-row query tile whose key tiles are divided between the two softmax
+// warpgroups: a takes [0, na), b takes [na, n), and their partial softmax
+// states are merged when both are done. The last items of the list (the
+// shortest pairs) are split when that shortens the final round of the grid.
 struct Item {
-  int bh, h, i0;
-  int nkv[2];  // key tiles each query tile visits (0: tile beyond Lq)
-  int nmax;
+  int bh, h;
+  int row0[2];       // first query row of tile a / b
+  int lo[2], hi[2];  // key tiles [lo, hi) of tile a / b (none when lo == hi)
+  int ns;            // key tiles streamed through shared memory for the item
+  bool split;
 };
 
+// Key tiles [0, n) one 128-row query tile starting at row r0 visits.
+RP_DEVI int tile_keys(const FwdParams& p, int r0) {
+  if (r0 >= p.Lq) return 0;
+  int last_key = p.Lk - 1;
+  if (p.causal) last_key = min(last_key, min(r0 + kBM - 1, p.Lq - 1) + p.q_offset);
+  return last_key / kBN + 1;
+}
+
+// SPLIT: the launch has split items (p.nsplit > 0); without, the split paths
+// compile away.
+template <bool SPLIT>
 RP_DEVI Item make_item(const FwdParams& p, int w) {
   Item it;
   const int BH = p.B * p.H;
-  const int pair = p.npairs - 1 - w / BH;  // longest (causal) pairs first
-  it.bh = w % BH;
-  it.h = it.bh % p.H;
-  it.i0 = pair * 2 * kBM;
-#pragma unroll
-  for (int x = 0; x < 2; ++x) {
-    const int r0 = it.i0 + x * kBM;
-    if (r0 >= p.Lq) {
-      it.nkv[x] = 0;
-      continue;
-    }
-    int last_key = p.Lk - 1;
-    if (p.causal) last_key = min(last_key, min(r0 + kBM - 1, p.Lq - 1) + p.q_offset);
-    it.nkv[x] = last_key / kBN + 1;
+  const int whole = p.npairs * BH - (SPLIT ? p.nsplit : 0);  // pair items kept whole
+  int wp = w, xs = -1;
+  if (SPLIT && w >= whole) {
+    wp = whole + ((w - whole) >> 1);
+    xs = (w - whole) & 1;
   }
-  it.nmax = max(it.nkv[0], it.nkv[1]);
+  const int pair = p.npairs - 1 - wp / BH;  // longest (causal) pairs first
+  it.bh = wp % BH;
+  it.h = it.bh % p.H;
+  const int i0 = pair * 2 * kBM;
+  if (xs < 0) {
+    it.split = false;
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+      it.row0[x] = i0 + x * kBM;
+      it.lo[x] = 0;
+      it.hi[x] = tile_keys(p, it.row0[x]);
+    }
+    it.ns = max(it.hi[0], it.hi[1]);
+  } else {
+    it.split = true;
+    const int r0 = i0 + xs * kBM;
+    const int n = tile_keys(p, r0);
+    const int na = (n + 1) >> 1;
+    it.row0[0] = it.row0[1] = r0;
+    it.lo[0] = 0;
+    it.hi[0] = na;
+    it.lo[1] = na;
+    it.hi[1] = n;
+    it.ns = n;
+  }
   return it;
 }
+
+// Stream position s of an item: the key tile loaded there, and whether query
+// tile x uses it. A split item alternates a's and b's key tiles.
+RP_DEVI int stream_key(const Item& it, int s) {
+  return it.split ? ((s & 1) ? it.lo[1] + (s >> 1) : (s >> 1)) : s;
+}
+RP_DEVI bool stream_uses(const Item& it, int x, int s) {
+  return it.split ? (s & 1) == x : s < (x ? it.hi[1] : it.hi[0]);
+}
+// Field x of an item, selected without indexing (keeps the item in registers).
+RP_DEVI int sel(const int (&v)[2], int x) { return x ? v[1] : v[0]; }
 
 // The item a CTA takes in round r: items are ordered longest first, and the
 // CTAs sweep them in alternating directions (round 0 left to right, round 1
@@ -129,10 +176,14 @@ RP_DEVI int item_at(int r) {
   return r * g + ((r & 1) ? g - 1 - c : c);
 }
 
-// Head of the first item from round r on in which query tile x has rows, or -1.
+// Head of the first item from round r on in which query tile x has key tiles,
+// or -1.
+template <bool SPLIT>
 RP_DEVI int next_head(const FwdParams& p, int x, int r, int nitems) {
-  for (int w = item_at(r); w < nitems; w = item_at(++r))
-    if (make_item(p, w).nkv[x] > 0) return (w % (p.B * p.H)) % p.H;
+  for (int w = item_at(r); w < nitems; w = item_at(++r)) {
+    const Item it = make_item<SPLIT>(p, w);
+    if (sel(it.hi, x) > sel(it.lo, x)) return it.h;
+  }
   return -1;
 }
 
@@ -158,7 +209,23 @@ struct T5Tab {
 
 RP_DEVI int t5_copy_stride(int len4) { return (len4 + 28 + 31) & ~31; }
 
-template <int MODE, bool OUT_F32>
+// Bytes of the mode's relative-term tables after kOffAux (16-byte multiple);
+// the split-item (m, l) exchange follows them.
+__host__ __device__ inline uint32_t fwd_aux_bytes(int mode, const FwdParams& p) {
+  uint32_t aux = 0;
+  if (mode == 0) {
+    const uint32_t bkt_bytes = (static_cast<uint32_t>(p.t5_tab_len4) + 4u + 127u) & ~127u;
+    const uint32_t stride = (static_cast<uint32_t>(p.t5_tab_len4) + 28u + 31u) & ~31u;
+    aux = bkt_bytes + 2u * 8u * stride * 4u + 2u * 128u * 4u;
+  } else if (mode == 1) {
+    const uint32_t nrel = 2u * p.kclip + 1u;
+    const uint32_t tbl = (nrel * kHeadDim * 2u + 15u) & ~15u;
+    aux = 2u * tbl + 4u * 128u * nrel * 4u;
+  }
+  return (aux + 15u) & ~15u;
+}
+
+template <int MODE, bool OUT_F32, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     relpos_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -169,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int nitems = p.B * p.H * p.npairs;
+  const int nitems = p.B * p.H * p.npairs + p.nsplit;
 
   auto bar = [&](uint32_t i) { return sbase + kOffBar + i * 8; };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffBar + kOffAbort);
@@ -198,9 +265,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (uint32_t i = 0; i < kNumBars; ++i) {
       uint32_t cnt = 1;
-      if (i == kBarPFull || i == kBarPFull + 1 || i == kBarOFree || i == kBarOFree + 1 ||
-          i == kBarTab || i == kBarTab + 1 || i == kBarSFree || i == kBarSFree + 1)
+      if (i == kBarPFull || i == kBarPFull + 1 || i == kBarTab || i == kBarTab + 1 ||
+          i == kBarSFree || i == kBarSFree + 1)
         cnt = 128;  // every thread of a softmax warpgroup
+      if (i == kBarOFree || i == kBarOFree + 1 || i == kBarComb)
+        cnt = 256;  // both softmax warpgroups (or one, arriving twice)
       if (i == kBarQEmpty || i == kBarFinal || (i >= kBarKEmpty && i < kBarVEmpty + kStages))
         cnt = 2;    // both MMA issuers
       mbar_init(bar(i), cnt);
@@ -218,7 +287,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kOffBar + kOffTmemSlot);
 
   if (warp < 4) {
-    setmaxnreg_dec<72>();
+    // register split (4 x 32 x dec + 8 x 32 x inc <= 384 x 168): T5 needs
+    // fewer in the softmax and gives its issuers room
+    if constexpr (MODE == 0) {
+      setmaxnreg_dec<88>();
+    } else {
+      setmaxnreg_dec<72>();
+    }
     if (warp == 0 || warp == 2) {
       // ------------------------------------------------------------ producers
       // warp 0: each item's Q tiles and the K ring; warp 2: the V ring
@@ -235,23 +310,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t it_cnt = 0;
       int item_cnt = 0;
       for (int rr = 0, w = item_at(0); ok && w < nitems; w = item_at(++rr), ++item_cnt) {
-        const Item it = make_item(p, w);
+        const Item it = make_item<SPLIT>(p, w);
         if (kq) {
           if (item_cnt > 0) ok = mbar_wait_warp(bar(kBarQEmpty), (item_cnt - 1) & 1);
           if (!ok) break;
-          mbar_arrive_expect_tx_elect(bar(kBarQFull), (it.nkv[1] > 0 ? 2u : 1u) * kTileBytes);
-          tma_load_3d_elect(sbase + kOffQ, &tmQ, bar(kBarQFull), 0, it.i0, it.bh);
-          if (it.nkv[1] > 0)
-            tma_load_3d_elect(sbase + kOffQ + kTileBytes, &tmQ, bar(kBarQFull), 0, it.i0 + kBM, it.bh);
+          // a split item's single query tile goes to the Q_a buffer
+          const bool two = !it.split && it.hi[1] > 0;
+          mbar_arrive_expect_tx_elect(bar(kBarQFull), (two ? 2u : 1u) * kTileBytes);
+          tma_load_3d_elect(sbase + kOffQ, &tmQ, bar(kBarQFull), 0, it.row0[0], it.bh);
+          if (two)
+            tma_load_3d_elect(sbase + kOffQ + kTileBytes, &tmQ, bar(kBarQFull), 0, it.row0[1], it.bh);
         }
-        for (int j = 0; j < it.nmax; ++j, ++it_cnt) {
+        for (int j = 0; j < it.ns; ++j, ++it_cnt) {
           const uint32_t st = it_cnt % kStages;
           if (it_cnt >= kStages) {
             ok = mbar_wait_warp(bar(empty0 + st), ((it_cnt / kStages) - 1) & 1);
             if (!ok) break;
           }
           mbar_arrive_expect_tx_elect(bar(full0 + st), kTileBytes);
-          tma_load_3d_elect(sbase + ring + st * kTileBytes, tmap, bar(full0 + st), 0, j * kBN, it.bh);
+          tma_load_3d_elect(sbase + ring + st * kTileBytes, tmap, bar(full0 + st), 0,
+                            stream_key(it, j) * kBN, it.bh);
         }
       }
       if (!ok && lane == 0) {
@@ -266,95 +344,102 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1 || warp == 3) {
       // ------------------------------------------------------------ MMA issuers
       // Warp 1 issues the products of query tile a, warp 3 those of tile b, so
-      // each reacts only to its own softmax warpgroup. Per key tile j: S = Q K_{j+1}^T
-      // as soon as the softmax has read its previous S, then O += P V_j as soon as P
-      // is in TMEM. K / V stages and the Q tiles are released once both issuers are
+      // each reacts only to its own softmax warpgroup. For its key tiles in
+      // stream order: S = Q K^T of the next tile as soon as the softmax has
+      // read the previous S, then O += P V of the current tile as soon as P is
+      // in TMEM. Stream positions of the other tile only are released without
+      // use. K / V stages and the Q buffers are freed once both issuers are
       // done with them (barriers counting two arrivals).
       const uint32_t x = warp == 1 ? 0u : 1u;
       bool ok = true;
-      uint32_t kv_it = 0;
-      uint32_t sis = 0;   // S products issued
-      uint32_t pvc = 0;   // P.V products issued
-      uint32_t ocnt = 0;  // items finished
+      uint32_t kv_it = 0;  // ring position of the item's first key tile
+      uint32_t sis = 0;    // S products issued
+      uint32_t pvc = 0;    // P.V products issued
+      uint32_t ocnt = 0;   // items whose O accumulator this issuer used
       int item_cnt = 0;
       // descriptors at K-step 0; later K-steps add the step's byte offset / 16
-      const uint64_t dq = smem_desc_sw128(sbase + kOffQ + x * kTileBytes, 16, 1024);
+      const uint64_t dq_a = smem_desc_sw128(sbase + kOffQ, 16, 1024);
       const uint64_t dk0 = smem_desc_sw128(sbase + kOffK, 16, 1024);
       const uint64_t dv0 = smem_desc_sw128(sbase + kOffV, 8192, 1024);
       constexpr uint64_t kStageStep = kTileBytes >> 4;
       const uint32_t s_col = tmem + kTmemS + x * kBN;
       const uint32_t o_col = tmem + kTmemO + x * kHeadDim;
       const uint32_t p_col = tmem + kTmemP + x * 64;
-      auto issue_s = [&](uint32_t kslot) -> bool {
-        if (sis > 0 && !mbar_wait_warp(bar(kBarSFree + x), (sis - 1) & 1)) return false;
-        tc_fence_after();
-        const uint64_t dk = dk0 + kslot * kStageStep;
-#pragma unroll
-        for (int kk = 0; kk < kHeadDim / 16; ++kk)
-          umma_bf16_ss_elect(s_col, dq + 2 * kk, dk + 2 * kk, kIdescQK, kk > 0 ? 1u : 0u);
-        tc_commit_elect(bar(kBarSFull + x));
-        ++sis;
-        return true;
-      };
       for (int rr = 0, w = item_at(0); ok && w < nitems; w = item_at(++rr), ++item_cnt) {
-        const Item it = make_item(p, w);
-        const int nkv = it.nkv[x];
+        const Item it = make_item<SPLIT>(p, w);
+        const int mine = sel(it.hi, x) - sel(it.lo, x);
+        const uint64_t dq = dq_a + ((it.split ? 0u : x) * kStageStep);
         ok = mbar_wait_warp(bar(kBarQFull), item_cnt & 1);
         if (!ok) break;
-        if (nkv == 0 && lane == 0) mbar_arrive(bar(kBarQEmpty));
-        for (int j = 0; ok && j < it.nmax; ++j) {
-          const uint32_t kvj = kv_it + j;
-          const uint32_t st = kvj % kStages;
-          const uint32_t ph = (kvj / kStages) & 1;
-          if (j == 0) {
-            ok = mbar_wait_warp(bar(kBarKFull + st), ph);
-            if (!ok) break;
-            if (nkv > 0) {
-              ok = issue_s(st);
-              if (!ok) break;
-              tc_commit_elect(bar(kBarKEmpty + st));
-              if (nkv == 1) tc_commit_elect(bar(kBarQEmpty));
-            } else if (lane == 0) {
-              mbar_arrive(bar(kBarKEmpty + st));
-            }
+        if (mine == 0 && lane == 0) mbar_arrive(bar(kBarQEmpty));
+        int kpos = 0, vpos = 0;  // next stream positions of the K and V rings
+        // Release the K (or V) stages of the other tile's positions up to this
+        // tile's next one; returns that position, or it.ns when none is left.
+        auto advance = [&](int& pos, uint32_t full0, uint32_t empty0) -> int {
+          while (pos < it.ns && !stream_uses(it, x, pos)) {
+            const uint32_t r = kv_it + pos;
+            ok = mbar_wait_warp(bar(full0 + r % kStages), (r / kStages) & 1);
+            if (!ok) return it.ns;
+            if (lane == 0) mbar_arrive(bar(empty0 + r % kStages));
+            ++pos;
           }
-          // look ahead: the next key tile's scores
-          if (j + 1 < it.nmax) {
-            const uint32_t st1 = (kvj + 1) % kStages;
-            ok = mbar_wait_warp(bar(kBarKFull + st1), ((kvj + 1) / kStages) & 1);
+          return pos;
+        };
+        // S of this tile's i-th key tile (at the K cursor)
+        auto issue_s = [&](int i) -> bool {
+          const int pos = advance(kpos, kBarKFull, kBarKEmpty);
+          if (!ok) return false;
+          const uint32_t r = kv_it + pos;
+          const uint32_t st = r % kStages;
+          if (!mbar_wait_warp(bar(kBarKFull + st), (r / kStages) & 1)) return false;
+          if (sis > 0 && !mbar_wait_warp(bar(kBarSFree + x), (sis - 1) & 1)) return false;
+          tc_fence_after();
+          const uint64_t dk = dk0 + st * kStageStep;
+#pragma unroll
+          for (int kk = 0; kk < kHeadDim / 16; ++kk)
+            umma_bf16_ss_elect(s_col, dq + 2 * kk, dk + 2 * kk, kIdescQK, kk > 0 ? 1u : 0u);
+          tc_commit_elect(bar(kBarSFull + x));
+          tc_commit_elect(bar(kBarKEmpty + st));
+          if (i == mine - 1) tc_commit_elect(bar(kBarQEmpty));
+          ++sis;
+          ++kpos;
+          return true;
+        };
+        if (mine > 0) ok = issue_s(0);
+        for (int i = 0; ok && i < mine; ++i) {
+          // look ahead: the next key tile's scores (after the last one, free
+          // the other tile's remaining K stages at once)
+          if (i + 1 < mine) {
+            ok = issue_s(i + 1);
             if (!ok) break;
-            if (j + 1 < nkv) {
-              ok = issue_s(st1);
-              if (!ok) break;
-              tc_commit_elect(bar(kBarKEmpty + st1));
-              if (j + 1 == nkv - 1) tc_commit_elect(bar(kBarQEmpty));
-            } else if (lane == 0) {
-              mbar_arrive(bar(kBarKEmpty + st1));
-            }
+          } else {
+            advance(kpos, kBarKFull, kBarKEmpty);
+            if (!ok) break;
           }
           // this key tile's P.V
-          if (j < nkv) {
-            ok = mbar_wait_warp(bar(kBarPFull + x), pvc & 1);
-            if (ok && j == 0 && ocnt > 0) ok = mbar_wait_warp(bar(kBarOFree + x), (ocnt - 1) & 1);
-            if (ok) ok = mbar_wait_warp(bar(kBarVFull + st), ph);
-            tc_fence_after();
-            if (!ok) break;
-            const uint64_t dv = dv0 + st * kStageStep;
+          const int pos = advance(vpos, kBarVFull, kBarVEmpty);
+          if (!ok) break;
+          const uint32_t r = kv_it + pos;
+          const uint32_t st = r % kStages;
+          ok = mbar_wait_warp(bar(kBarPFull + x), pvc & 1);
+          if (ok && i == 0 && ocnt > 0) ok = mbar_wait_warp(bar(kBarOFree + x), (ocnt - 1) & 1);
+          if (ok) ok = mbar_wait_warp(bar(kBarVFull + st), (r / kStages) & 1);
+          tc_fence_after();
+          if (!ok) break;
+          const uint64_t dv = dv0 + st * kStageStep;
 #pragma unroll
-            for (int kk = 0; kk < kBN / 16; ++kk)
-              umma_bf16_ts_elect(o_col, p_col + kk * 8, dv + 128 * kk, kIdescPV,
-                                 (j > 0 || kk > 0) ? 1u : 0u);
-            tc_commit_elect(bar(kBarODone + x));
-            tc_commit_elect(bar(kBarVEmpty + st));
-            ++pvc;
-          } else {
-            ok = mbar_wait_warp(bar(kBarVFull + st), ph);
-            if (!ok) break;
-            if (lane == 0) mbar_arrive(bar(kBarVEmpty + st));
-          }
+          for (int kk = 0; kk < kBN / 16; ++kk)
+            umma_bf16_ts_elect(o_col, p_col + kk * 8, dv + 128 * kk, kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
+          tc_commit_elect(bar(kBarODone + x));
+          tc_commit_elect(bar(kBarVEmpty + st));
+          ++pvc;
+          ++vpos;
         }
-        kv_it += it.nmax;
-        if (nkv > 0) ++ocnt;
+        // the other tile's remaining positions
+        if (ok) advance(kpos, kBarKFull, kBarKEmpty);
+        if (ok) advance(vpos, kBarVFull, kBarVEmpty);
+        kv_it += it.ns;
+        if (mine > 0) ++ocnt;
       }
       if (!ok && lane == 0) {
         record_error(p.status);
@@ -364,7 +449,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait_warp(bar(kBarFinal), 0, 100000000ull);
     }
   } else {
-    setmaxnreg_inc<216>();
+    if constexpr (MODE == 0) {
+      setmaxnreg_inc<200>();
+    } else {
+      setmaxnreg_inc<216>();
+    }
     // -------------------------------------------------------------- softmax
     const int x = (warp - 4) >> 2;                  // query tile a (0) or b (1)
     const int t = ((warp & 3) << 5) | lane;          // row == TMEM lane
@@ -376,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float kNegInf = -INFINITY;
     bool err = false;
 
-    T5Tab tab;
+    T5Tab tab{};
     float* hbias = nullptr;  // T5: this head's bias per bucket (log2 units)
     float hb_next = 0.f;     // T5: thread t < num_buckets holds entry t of the next table's row
     float* qa = nullptr;    // Shaw: q . a_K[r] of this row (log2 units)
@@ -423,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       return true;
     };
     if constexpr (MODE == 0) {
-      const int h0 = next_head(p, x, 0, nitems);
+      const int h0 = next_head<SPLIT>(p, x, 0, nitems);
       if (h0 >= 0) {
         if (t < p.t5_nb) hb_next = __ldg(p.bias + t * p.H + h0);
         if (!t5_build(0)) err = true;
@@ -431,11 +520,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     uint32_t cnt = 0, ocnt = 0;
+    uint32_t ccnt = 0;  // split items merged with the other warpgroup
+    float2* ml = reinterpret_cast<float2*>(aux + fwd_aux_bytes(MODE, p));
     for (int rr = 0, w = item_at(0); !err && w < nitems; w = item_at(++rr)) {
-      const Item it = make_item(p, w);
-      const int n_kv = it.nkv[x];
+      const Item it = make_item<SPLIT>(p, w);
+      const int lo_x = sel(it.lo, x);
+      const int n_kv = sel(it.hi, x) - lo_x;
       if (n_kv == 0) continue;
-      const int i0 = it.i0 + x * kBM;
+      const int i0 = sel(it.row0, x);
       const int prow = i0 + t + p.q_offset;  // absolute position of this row
       const int p_lo = i0 + p.q_offset;      // of the tile's first row
 
@@ -446,7 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // this item's table was filled at the end of the previous item (or in
         // the prologue); fetch the next item's bias row meanwhile
         buf = ocnt & 1;
-        next_h = next_head(p, x, rr + 1, nitems);
+        next_h = next_head<SPLIT>(p, x, rr + 1, nitems);
         if (t < p.t5_nb && next_h >= 0) hb_next = __ldg(p.bias + t * p.H + next_h);
         const bool ok = mbar_wait(bar(kBarTab + x), 1);
         err = __any_sync(0xffffffffu, !ok);
@@ -506,7 +598,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float m_run = kNegInf;
       float l_run = 0.f;
       for (int j = 0; j < n_kv; ++j, ++cnt) {
-        const int j0 = j * kBN;
+        const int j0 = (lo_x + j) * kBN;
         bool ok = mbar_wait(bar(kBarSFull + x), cnt & 1);
         err = __any_sync(0xffffffffu, !ok);
         if (err) break;
@@ -540,28 +632,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (p.causal) lim = min(lim, prow - j0);
         }
 
-        float mx;
-        float addc = 0.f;  // far tiles: the constant still to add
+        // Far tiles keep the raw scores s (logit = s * sl2 + addc, one constant
+        // per row); near tiles get their per-element logits in place. Masking,
+        // the maximum and the exponentials are then shared: the maximum is
+        // taken on xs and mapped to logit units, and each probability is
+        // 2^(xs * xscale + xoff - m).
         // DeBERTa tiles beyond the band still carry a per-key term, so every
-        // DeBERTa tile takes the per-element path below
+        // DeBERTa tile takes the per-element path.
         const bool far = MODE != 2 && (far_l || far_r);
-        if (far) {
-          // logits are s * sl2 + addc; the max is taken on raw s
-          addc = far_l ? add_l : add_r;
-          if (need_mask) {
-#pragma unroll
-            for (int c = 0; c < 128; ++c) xs[c] = (c > lim) ? kNegInf : xs[c];
-          }
-          float m0 = kNegInf, m1 = kNegInf, m2 = kNegInf, m3 = kNegInf;
-#pragma unroll
-          for (int c = 0; c < 128; c += 8) {
-            m0 = max3f(m0, xs[c], xs[c + 1]);
-            m1 = max3f(m1, xs[c + 2], xs[c + 3]);
-            m2 = max3f(m2, xs[c + 4], xs[c + 5]);
-            m3 = max3f(m3, xs[c + 6], xs[c + 7]);
-          }
-          mx = fmaf(fmaxf(fmaxf(m0, m1), fmaxf(m2, m3)), sl2, addc);
-        } else {
+        const float addc = far ? (far_l ? add_l : add_r) : 0.f;
+        if (!far) {
           if constexpr (MODE == 0) {
             const int s0 = j0 - prow + p.t5_tab_off;  // table index of column 0
             const int k = s0 & 3;
@@ -623,10 +703,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             }
           }
-          if (need_mask) {
+        }
+        if (need_mask) {
 #pragma unroll
-            for (int c = 0; c < 128; ++c) xs[c] = (c > lim) ? kNegInf : xs[c];
-          }
+          for (int c = 0; c < 128; ++c) xs[c] = (c > lim) ? kNegInf : xs[c];
+        }
+        float mx;
+        {
           float m0 = kNegInf, m1 = kNegInf, m2 = kNegInf, m3 = kNegInf;
 #pragma unroll
           for (int c = 0; c < 128; c += 8) {
@@ -636,6 +719,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             m3 = max3f(m3, xs[c + 6], xs[c + 7]);
           }
           mx = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+          if (far) mx = fmaf(mx, sl2, addc);
         }
 
         // ---- running max with lazy rescale
@@ -648,37 +732,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const float m_use = (m_run == kNegInf) ? 0.f : m_run;
 
-        // ---- probabilities (in place), row sum, bf16 pack
+        // ---- probabilities (in place for Shaw), row sum, bf16 pack; x * 1 + c
+        // is exact, so near tiles round exactly as a plain subtraction would
         uint32_t pk[64];
         float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-        if (far) {
-          const float2 sc2 = make_float2(sl2, sl2);
-          const float2 off2 = make_float2(addc - m_use, addc - m_use);
+        {
+          const float2 sc2 = far ? make_float2(sl2, sl2) : make_float2(1.f, 1.f);
+          const float off = (far ? addc : 0.f) - m_use;
+          const float2 off2 = make_float2(off, off);
 #pragma unroll
           for (int c = 0; c < 128; c += 4) {
             float2 a = __ffma2_rn(make_float2(xs[c], xs[c + 1]), sc2, off2);
             float2 b = __ffma2_rn(make_float2(xs[c + 2], xs[c + 3]), sc2, off2);
-            a.x = ex2_approx(a.x);
-            a.y = ex2_approx(a.y);
-            b.x = ex2_approx(b.x);
-            b.y = ex2_approx(b.y);
-            acc0 = __fadd2_rn(acc0, a);
-            acc1 = __fadd2_rn(acc1, b);
-            pk[c / 2] = pack_bf16x2(a.x, a.y);
-            pk[c / 2 + 1] = pack_bf16x2(b.x, b.y);
-            if constexpr (MODE == 1) {
-              xs[c] = a.x;
-              xs[c + 1] = a.y;
-              xs[c + 2] = b.x;
-              xs[c + 3] = b.y;
-            }
-          }
-        } else {
-          const float2 neg = make_float2(-m_use, -m_use);
-#pragma unroll
-          for (int c = 0; c < 128; c += 4) {
-            float2 a = __fadd2_rn(make_float2(xs[c], xs[c + 1]), neg);
-            float2 b = __fadd2_rn(make_float2(xs[c + 2], xs[c + 3]), neg);
             a.x = ex2_approx(a.x);
             a.y = ex2_approx(a.y);
             b.x = ex2_approx(b.x);
@@ -768,18 +833,77 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       __syncwarp();
-      uint32_t orr[2][32];
-      tmem_ld32(tO, orr[0]);
-      tmem_ld32(tO + 32, orr[1]);
-      tmem_ld_wait(orr[0]);
-      tmem_ld_wait(orr[1]);
-      tc_fence_before();
-      mbar_arrive(bar(kBarOFree + x));  // the next item's P.V may overwrite O
-      ++ocnt;
-      float* o = reinterpret_cast<float*>(&orr[0][0]);
       if constexpr (MODE == 1) {
         wbin[0] += mass_l;
         wbin[2 * kc] += mass_r;
+      }
+      // A split item whose other half also has key tiles: merge the two
+      // partial states. Each warpgroup publishes its rows' (m, l), then writes
+      // 32 of the 64 output columns from both O accumulators, each scaled
+      // from its own running maximum to the common one.
+      const bool merge = it.split && sel(it.hi, x ^ 1) > sel(it.lo, x ^ 1);
+      float sa = 1.f, sb = 0.f, l_row = l_run;
+      const int c0 = merge ? x * 32 : 0;
+      if (merge) {
+        if constexpr (MODE == 1) {
+          // fold this half's relative-value term into its O first
+          uint32_t of[2][32];
+          tmem_ld32(tO, of[0]);
+          tmem_ld32(tO + 32, of[1]);
+          tmem_ld_wait(of[0]);
+          tmem_ld_wait(of[1]);
+          float* f = reinterpret_cast<float*>(&of[0][0]);
+          for (int r = 0; r < nrel; ++r) {
+            const float wr = wbin[r];
+            const __nv_bfloat162* rowv = reinterpret_cast<const __nv_bfloat162*>(aV_s + r * kHeadDim);
+#pragma unroll
+            for (int e = 0; e < kHeadDim / 2; ++e) {
+              const float2 v2 = __bfloat1622float2(rowv[e]);
+              f[2 * e] = fmaf(wr, v2.x, f[2 * e]);
+              f[2 * e + 1] = fmaf(wr, v2.y, f[2 * e + 1]);
+            }
+          }
+          tmem_st32(tO, of[0]);
+          tmem_st32(tO + 32, of[1]);
+          tmem_st_wait();
+          tc_fence_before();
+        }
+        // (one buffer suffices: the partner writes it again only after a P.V
+        // that waits for this warpgroup's release of the accumulators below)
+        float2* slot = ml;
+        slot[x * 128 + t] = make_float2(m_run, l_run);
+        mbar_arrive(bar(kBarComb));
+        const bool ok = mbar_wait(bar(kBarComb), ccnt & 1);
+        ++ccnt;
+        err = __any_sync(0xffffffffu, !ok);
+        if (err) break;
+        tc_fence_after();
+        const float2 other = slot[(x ^ 1) * 128 + t];
+        const float m = fmaxf(m_run, other.x);
+        sa = m_run == kNegInf ? 0.f : ex2_approx(m_run - m);
+        sb = other.x == kNegInf ? 0.f : ex2_approx(other.x - m);
+        l_row = l_run * sa + other.y * sb;
+      }
+      uint32_t orr[2][32];
+      if (merge) {
+        tmem_ld32(tO + c0, orr[0]);
+        tmem_ld32(tmem + lane_base + kTmemO + (x ^ 1) * kHeadDim + c0, orr[1]);
+      } else {
+        tmem_ld32(tO, orr[0]);
+        tmem_ld32(tO + 32, orr[1]);
+      }
+      tmem_ld_wait(orr[0]);
+      tmem_ld_wait(orr[1]);
+      tc_fence_before();
+      // the next items' P.V may overwrite the accumulators read here
+      mbar_arrive(bar(kBarOFree + x));
+      mbar_arrive(bar(kBarOFree + (merge ? (x ^ 1) : x)));
+      ++ocnt;
+      float* o = reinterpret_cast<float*>(&orr[0][0]);
+      if (merge) {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) o[c] = o[c] * sa + o[32 + c] * sb;
+      } else if constexpr (MODE == 1) {
         for (int r = 0; r < nrel; ++r) {
           const float wr = wbin[r];
           const __nv_bfloat162* rowv = reinterpret_cast<const __nv_bfloat162*>(aV_s + r * kHeadDim);
@@ -791,24 +915,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
+      const float inv_l = l_row > 0.f ? 1.f / l_row : 0.f;
       const int row = i0 + t;
       if (row < p.Lq) {
+        const size_t base = (static_cast<size_t>(it.bh) * p.Lq + row) * kHeadDim + c0;
+        const int ncol = merge ? 32 : kHeadDim;
         if constexpr (OUT_F32) {
-          float* dst = static_cast<float*>(p.out) + (static_cast<size_t>(it.bh) * p.Lq + row) * kHeadDim;
+          float* dst = static_cast<float*>(p.out) + base;
 #pragma unroll
           for (int c = 0; c < kHeadDim; c += 4)
-            st_global_v4(dst + c, __float_as_uint(o[c] * inv_l), __float_as_uint(o[c + 1] * inv_l),
-                         __float_as_uint(o[c + 2] * inv_l), __float_as_uint(o[c + 3] * inv_l));
+            if (c < ncol)
+              st_global_v4(dst + c, __float_as_uint(o[c] * inv_l), __float_as_uint(o[c + 1] * inv_l),
+                           __float_as_uint(o[c + 2] * inv_l), __float_as_uint(o[c + 3] * inv_l));
         } else {
-          __nv_bfloat16* dst =
-              static_cast<__nv_bfloat16*>(p.out) + (static_cast<size_t>(it.bh) * p.Lq + row) * kHeadDim;
+          __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + base;
 #pragma unroll
           for (int c = 0; c < kHeadDim; c += 8)
-            st_global_v4(dst + c, pack_bf16x2(o[c] * inv_l, o[c + 1] * inv_l),
-                         pack_bf16x2(o[c + 2] * inv_l, o[c + 3] * inv_l),
-                         pack_bf16x2(o[c + 4] * inv_l, o[c + 5] * inv_l),
-                         pack_bf16x2(o[c + 6] * inv_l, o[c + 7] * inv_l));
+            if (c < ncol)
+              st_global_v4(dst + c, pack_bf16x2(o[c] * inv_l, o[c + 1] * inv_l),
+                           pack_bf16x2(o[c + 2] * inv_l, o[c + 3] * inv_l),
+                           pack_bf16x2(o[c + 4] * inv_l, o[c + 5] * inv_l),
+                           pack_bf16x2(o[c + 6] * inv_l, o[c + 7] * inv_l));
         }
       }
     }
@@ -830,22 +957,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 uint32_t fwd_smem_bytes(int mode, const FwdParams& p) {
-  uint32_t aux = 0;
-  if (mode == 0) {
-    const uint32_t bkt_bytes = (static_cast<uint32_t>(p.t5_tab_len4) + 4u + 127u) & ~127u;
-    const uint32_t stride = (static_cast<uint32_t>(p.t5_tab_len4) + 28u + 31u) & ~31u;
-    aux = bkt_bytes + 2u * 8u * stride * 4u + 2u * 128u * 4u;
-  } else if (mode == 1) {
-    const uint32_t nrel = 2u * p.kclip + 1u;
-    const uint32_t tbl = (nrel * kHeadDim * 2u + 15u) & ~15u;
-    aux = 2u * tbl + 4u * 128u * nrel * 4u;
-  }
-  return 1024u + kOffAux + ((aux + 15u) & ~15u);
+  return 1024u + kOffAux + fwd_aux_bytes(mode, p) + (p.nsplit > 0 ? kCombBytes : 0u);
 }
 
 uint32_t fwd_max_smem_bytes() { return 232448u; }
 
-int fwd_num_items(const FwdParams& p) { return p.B * p.H * p.npairs; }
+int fwd_num_items(const FwdParams& p) { return p.B * p.H * p.npairs + p.nsplit; }
+
+// The grid runs ceil(items / num_sms) rounds. When the pair items left for the
+// last round fill at most half the grid, running each as two split items
+// (half the key tiles per softmax warpgroup) halves that round. This holds
+// when every pair costs the same (no causal mask; causal items are ordered
+// longest first, so the last round's are the shortest and splitting them
+// only unbalances the grid). A converted pair must hold two query tiles; the
+// tail holds the lowest pair rows, and the highest converted row is checked.
+int fwd_split_items(int npair_items, int BH, int Lq, int causal, int num_sms) {
+  if (causal || num_sms <= 0 || npair_items <= 0) return 0;
+  const int rem = npair_items % num_sms;
+  if (rem == 0 || 2 * rem > num_sms) return 0;
+  const int npairs = npair_items / BH;
+  const int top_pair = npairs - 1 - (npair_items - rem) / BH;  // highest converted pair row
+  if ((2 * top_pair + 1) * kBM >= Lq) return 0;
+  return rem;
+}
 
 cudaError_t launch_fwd(int mode, bool out_f32, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                        const CUtensorMap& tmV, const FwdParams& p, int num_sms, cudaStream_t stream) {
@@ -854,12 +988,16 @@ cudaError_t launch_fwd(int mode, bool out_f32, const CUtensorMap& tmQ, const CUt
   dim3 grid(nitems < num_sms ? nitems : num_sms);
   dim3 block(kThreads);
   void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const FwdParams) = nullptr;
+  const bool split = p.nsplit > 0;
   if (mode == 0) {
-    kern = out_f32 ? relpos_fwd_kernel<0, true> : relpos_fwd_kernel<0, false>;
+    kern = out_f32 ? (split ? relpos_fwd_kernel<0, true, true> : relpos_fwd_kernel<0, true, false>)
+                   : (split ? relpos_fwd_kernel<0, false, true> : relpos_fwd_kernel<0, false, false>);
   } else if (mode == 1) {
-    kern = out_f32 ? relpos_fwd_kernel<1, true> : relpos_fwd_kernel<1, false>;
+    kern = out_f32 ? (split ? relpos_fwd_kernel<1, true, true> : relpos_fwd_kernel<1, true, false>)
+                   : (split ? relpos_fwd_kernel<1, false, true> : relpos_fwd_kernel<1, false, false>);
   } else if (mode == 2) {
-    kern = out_f32 ? relpos_fwd_kernel<2, true> : relpos_fwd_kernel<2, false>;
+    kern = out_f32 ? (split ? relpos_fwd_kernel<2, true, true> : relpos_fwd_kernel<2, true, false>)
+                   : (split ? relpos_fwd_kernel<2, false, true> : relpos_fwd_kernel<2, false, false>);
   } else {
     return cudaErrorNotSupported;
   }
@@ -867,8 +1005,8 @@ cudaError_t launch_fwd(int mode, bool out_f32, const CUtensorMap& tmQ, const CUt
   // that every later launch fits)
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
-  const int slot = mode * 2 + (out_f32 ? 1 : 0);
-  static std::atomic<uint64_t> attr_set[6];
+  const int slot = mode * 4 + (out_f32 ? 2 : 0) + (split ? 1 : 0);
+  static std::atomic<uint64_t> attr_set[12];
   const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
   if (!bit || !(attr_set[slot].load() & bit)) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -69,6 +69,7 @@ struct FwdParams {
   int t5_nb;          // num_buckets (<= 128)
   T5Index t5;
   int npairs;         // 256-row query-tile pairs per head
+  int nsplit;         // trailing pair items run as two split items each
   const __nv_bfloat16* Qg;  // Q in global memory (bf16 [B,H,Lq,64])
   // Shaw
   const __nv_bfloat16* aK;  // [2k+1, 64]

@@ -13,6 +13,9 @@ namespace relpos {
 uint32_t fwd_smem_bytes(int mode, const FwdParams& p);
 uint32_t fwd_max_smem_bytes();
 int fwd_num_items(const FwdParams& p);
+// How many trailing pair items (of npair_items, with BH items per pair row)
+// to run as two split items each on a grid of num_sms persistent CTAs.
+int fwd_split_items(int npair_items, int BH, int Lq, int causal, int num_sms);
 cudaError_t launch_fwd(int mode, bool out_f32, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                        const CUtensorMap& tmV, const FwdParams& p, int num_sms, cudaStream_t stream);
 
