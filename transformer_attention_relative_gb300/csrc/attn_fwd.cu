@@ -242,6 +242,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffBar + kOffAbort);
 
   // ---------------------------------------------------------------- setup
+  // Nothing before griddep_wait() below reads or writes global memory, so a
+  // launch that follows in the stream may run this part early.
+  griddep_launch_dependents();
   uint8_t* aux = smem + kOffAux;
   uint8_t* bkt = aux;  // T5: head-independent bucket of each table offset
   const int nrel = 2 * p.kclip + 1;
@@ -250,16 +253,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int x = threadIdx.x; x < p.t5_tab_len4 + 4; x += kThreads) {
       const int xc = min(x, p.t5_tab_len - 1);
       bkt[x] = static_cast<uint8_t>(t5_bucket_dev(xc - p.t5_tab_off, p.t5));
-    }
-  } else if constexpr (MODE == 1) {
-    const uint4* srcK = reinterpret_cast<const uint4*>(p.aK);
-    const uint4* srcV = reinterpret_cast<const uint4*>(p.aV);
-    uint4* dK = reinterpret_cast<uint4*>(aux);
-    uint4* dV = reinterpret_cast<uint4*>(aux + shaw_tbl);
-    const int n16 = nrel * kHeadDim * 2 / 16;
-    for (int x = threadIdx.x; x < n16; x += kThreads) {
-      dK[x] = __ldg(srcK + x);
-      dV[x] = __ldg(srcV + x);
     }
   }
   if (threadIdx.x == 0) {
@@ -280,6 +273,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     tmem_alloc(sbase + kOffBar + kOffTmemSlot, kTmemCols);
     tmem_relinquish();
+  }
+  griddep_wait();
+  if constexpr (MODE == 1) {
+    const uint4* srcK = reinterpret_cast<const uint4*>(p.aK);
+    const uint4* srcV = reinterpret_cast<const uint4*>(p.aV);
+    uint4* dK = reinterpret_cast<uint4*>(aux);
+    uint4* dV = reinterpret_cast<uint4*>(aux + shaw_tbl);
+    const int n16 = nrel * kHeadDim * 2 / 16;
+    for (int x = threadIdx.x; x < n16; x += kThreads) {
+      dK[x] = __ldg(srcK + x);
+      dV[x] = __ldg(srcV + x);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -1014,8 +1019,20 @@ cudaError_t launch_fwd(int mode, bool out_f32, const CUtensorMap& tmQ, const CUt
     if (e != cudaSuccess) return e;
     attr_set[slot].fetch_or(bit);
   }
-  kern<<<grid, block, smem, stream>>>(tmQ, tmK, tmV, p);
-  return cudaGetLastError();
+  // programmatic dependent launch: the setup of this launch may overlap the
+  // end of the previous kernel in the stream (the kernel waits for it before
+  // its first global-memory access)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tmQ, tmK, tmV, p);
 }
 
 }  // namespace relpos

@@ -63,6 +63,13 @@ RP_DEVI bool mbar_wait(uint32_t bar, uint32_t parity,
   }
 }
 
+// ------------------------------------------------------------------ launch order
+// Programmatic dependent launch: let the next kernel of the stream start its
+// global-memory-free setup, and wait until the previous one has completed
+// (and its writes are visible) before touching global memory.
+RP_DEVI void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+RP_DEVI void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ------------------------------------------------------------------ TMA
 RP_DEVI void tma_prefetch_desc(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
