@@ -54,6 +54,7 @@ __global__ void __launch_bounds__(kDecThreads, 3) relpos_decode_partial_kernel(c
   __shared__ float red_s[4];
   __shared__ float o_s[4][kHeadDim];
 
+  griddep_wait();  // the previous kernel of the stream has completed
   const int pos = qi + p.q_offset;
   const int jb = chunk * kDecChunk;
   int je = min(p.Lk, jb + kDecChunk);
@@ -164,10 +165,13 @@ __global__ void __launch_bounds__(kDecThreads, 3) relpos_decode_partial_kernel(c
     pml[0] = mx;
     pml[1] = (red_s[0] + red_s[1]) + (red_s[2] + red_s[3]);
   }
+  griddep_launch_dependents();  // the combine may be scheduled now
 }
 
 // one warp per (row, 64 dims): merge the per-chunk partials
 __global__ void __launch_bounds__(64) relpos_decode_combine_kernel(const DecodeParams p) {
+  griddep_launch_dependents();
+  griddep_wait();  // every partial has been written
   const size_t row = blockIdx.x;
   const int d = threadIdx.x;
   const float* ml = p.part_ml + row * p.nchunks * 2;
@@ -193,13 +197,24 @@ __global__ void __launch_bounds__(64) relpos_decode_combine_kernel(const DecodeP
 
 int decode_chunk_keys() { return kDecChunk; }
 
+// Both kernels use programmatic dependent launch: each may be scheduled
+// while the kernel before it in the stream finishes, and waits for it before
+// touching global memory.
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream) {
-  dim3 grid(p.nchunks, p.Lq, p.B * p.H);
-  relpos_decode_partial_kernel<<<grid, kDecThreads, 0, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.nchunks, p.Lq, p.B * p.H);
+  cfg.blockDim = dim3(kDecThreads);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, relpos_decode_partial_kernel, p);
   if (e != cudaSuccess) return e;
-  relpos_decode_combine_kernel<<<p.B * p.H * p.Lq, kHeadDim, 0, stream>>>(p);
-  return cudaGetLastError();
+  cfg.gridDim = dim3(p.B * p.H * p.Lq);
+  cfg.blockDim = dim3(kHeadDim);
+  return cudaLaunchKernelEx(&cfg, relpos_decode_combine_kernel, p);
 }
 
 }  // namespace relpos
