@@ -692,18 +692,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 xs[4 * q + 3] = b.y;
               }
             } else {
-              // band: c2p = C2P[i][delta(i, j)], p2c = P2C[j][delta(j, i)]
+              // band: c2p = C2P[i][delta(i, j)], p2c = P2C[j][delta(j, i)];
+              // with rel = j - i = r0 + c, delta(i, j) = clamp(k - rel, 0, 2k - 1)
+              // and delta(j, i) = clamp(k + rel, 0, 2k - 1)
               const int n2k = 2 * kc;
               const int r0 = j0 - prow;  // key - query offset of column 0
-              const int jmax = p.Lk - 1 - j0;
+              const int jmax = p.Lk - 1 - j0;  // last key of the tile (ragged tail)
+              const int dij0 = kc - r0, dji0 = kc + r0;
+              const __nv_bfloat16* p2c_tile = p2c_head + static_cast<size_t>(j0) * n2k;
 #pragma unroll
               for (int c = 0; c < 128; ++c) {
-                const int rel = r0 + c;
-                const int d_ij = min(max(-rel, -kc), kc - 1) + kc;
-                const int d_ji = min(max(rel, -kc), kc - 1) + kc;
-                const int jj = j0 + min(c, jmax);
+                const int d_ij = min(max(dij0 - c, 0), n2k - 1);
+                const int d_ji = min(max(dji0 + c, 0), n2k - 1);
                 const float a = __bfloat162float(c2p_row[d_ij]);
-                const float b = __bfloat162float(p2c_head[static_cast<size_t>(jj) * n2k + d_ji]);
+                const float b = __bfloat162float(p2c_tile[min(c, jmax) * n2k + d_ji]);
                 xs[c] = fmaf(xs[c], sl2, a + b);
               }
             }
