@@ -83,7 +83,7 @@ bool make_tmap(CUtensorMap* m, const void* base, int L, int BH) {
   return r == CUDA_SUCCESS;
 }
 
-// DeBERTa table [rows = 2k, H, 64] bf16: boxes of 256 table rows of one head
+// DeBERTa table [rows = 2k, H, 64] bf16: boxes of 128 table rows of one head
 bool make_tmap_table(CUtensorMap* m, const void* base, int H, int rows) {
   auto fn = encode_fn();
   if (!fn) return false;
@@ -91,7 +91,7 @@ bool make_tmap_table(CUtensorMap* m, const void* base, int H, int rows) {
                         static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim) * 2,
                            static_cast<cuuint64_t>(H) * kHeadDim * 2};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(kHeadDim), 1u, 256u};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(kHeadDim), 1u, 128u};
   cuuint32_t estr[3] = {1u, 1u, 1u};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -422,7 +422,7 @@ extern "C" int relpos_attn_fwd(int mode, int dtype, const void* Q, const void* K
       p.p2c = reinterpret_cast<const __nv_bfloat16*>(sc + off_p2c);
       p.p2c_ends = reinterpret_cast<const float*>(sc + off_ends);
       p.ends_pitch = ends_pitch;
-      CUtensorMap ta, tpk, tpq;
+      CUtensorMap tqa, tka, tpk, tpq;
       ProjParams pp;
       std::memset(&pp, 0, sizeof(pp));
       pp.BH = static_cast<int>(BH);
@@ -432,18 +432,15 @@ extern "C" int relpos_attn_fwd(int mode, int dtype, const void* Q, const void* K
       pp.status = status;
       if (!make_tmap_table(&tpk, table0, H, static_cast<int>(n2k)) ||
           !make_tmap_table(&tpq, table1, H, static_cast<int>(n2k)) ||
-          !make_tmap(&ta, Qb, Lq, static_cast<int>(BH)))
+          !make_tmap(&tqa, Qb, Lq, static_cast<int>(BH)) || !make_tmap(&tka, Kb, Lk, static_cast<int>(BH)))
         return fail(RELPOS_ERR_CUDA);
-      pp.L = Lq;
-      pp.out = reinterpret_cast<__nv_bfloat16*>(sc + off_c2p);
-      pp.ends = nullptr;
-      if (launch_deberta_proj(false, ta, tpk, pp, s) != cudaSuccess) return fail(RELPOS_ERR_CUDA);
-      if (!make_tmap(&ta, Kb, Lk, static_cast<int>(BH))) return fail(RELPOS_ERR_CUDA);
-      pp.L = Lk;
-      pp.out = reinterpret_cast<__nv_bfloat16*>(sc + off_p2c);
+      pp.L[0] = Lq;
+      pp.L[1] = Lk;
+      pp.out[0] = reinterpret_cast<__nv_bfloat16*>(sc + off_c2p);
+      pp.out[1] = reinterpret_cast<__nv_bfloat16*>(sc + off_p2c);
       pp.ends = reinterpret_cast<float*>(sc + off_ends);
       pp.ends_pitch = ends_pitch;
-      if (launch_deberta_proj(true, ta, tpq, pp, s) != cudaSuccess) return fail(RELPOS_ERR_CUDA);
+      if (launch_deberta_proj(tqa, tpk, tka, tpq, pp, s) != cudaSuccess) return fail(RELPOS_ERR_CUDA);
     }
     CUtensorMap tq, tk, tv;
     if (!make_tmap(&tq, Qb, Lq, static_cast<int>(BH)) || !make_tmap(&tk, Kb, Lk, static_cast<int>(BH)) ||

@@ -85,11 +85,14 @@ struct FwdParams {
 };
 
 // DeBERTa relative products (deberta_proj.cu)
+// Both products in one launch: side 0 = C2P (rows of Q, table Pk), side 1 =
+// P2C (rows of K, table Pq, with the fp32 end columns).
 struct ProjParams {
-  int BH, H, L, k;
-  float scale;          // applied to every product (softmax scale times log2 e)
-  __nv_bfloat16* out;   // [BH, L, 2k]
-  float* ends;          // [BH, 2, ends_pitch] or null
+  int BH, H, k;
+  int L[2];              // rows of each side
+  float scale;           // applied to every product (softmax scale times log2 e)
+  __nv_bfloat16* out[2]; // [BH, L, 2k] per side
+  float* ends;           // side 1: [BH, 2, ends_pitch]
   int ends_pitch;
   int* status;
 };
