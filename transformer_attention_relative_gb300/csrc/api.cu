@@ -83,7 +83,7 @@ bool make_tmap(CUtensorMap* m, const void* base, int L, int BH) {
   return r == CUDA_SUCCESS;
 }
 
-// DeBERTa table [rows = 2k, H, 64] bf16: boxes of 128 table rows of one head
+// DeBERTa table [rows = 2k, H, 64] bf16: boxes of 64 table rows of one head
 bool make_tmap_table(CUtensorMap* m, const void* base, int H, int rows) {
   auto fn = encode_fn();
   if (!fn) return false;
@@ -91,7 +91,7 @@ bool make_tmap_table(CUtensorMap* m, const void* base, int H, int rows) {
                         static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim) * 2,
                            static_cast<cuuint64_t>(H) * kHeadDim * 2};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(kHeadDim), 1u, 128u};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(kHeadDim), 1u, 64u};
   cuuint32_t estr[3] = {1u, 1u, 1u};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

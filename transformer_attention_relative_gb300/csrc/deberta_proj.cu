@@ -12,13 +12,12 @@
 // as ends[bh][0 | 1][j].
 //
 // One launch computes both products (grid z: C2P, P2C). One CTA (128
-// threads, two per SM) per 128-row tile of one head: TMA brings
-// the Q (or K) tile and 128-row chunks of the table (two buffers);
-// tcgen05.mma M128 N128 K16 accumulates a chunk into one half of a 256-column
-// TMEM allocation while the four warps drain the other half. The output is a
-// 1 KB-per-row matrix, so each warp stages its 32 rows of a chunk in shared
-// memory (128-byte rows, 16-byte chunks swizzled by row) and stores them back
-// two rows (512 contiguous bytes) per instruction.
+// threads, four per SM) per 128-row tile of one head: TMA brings the Q (or
+// K) tile and 64-row chunks of the table (two buffers); tcgen05.mma M128 N64
+// K16 accumulates a chunk into one half of a 128-column TMEM allocation while
+// the four warps drain the other half. Each warp stages its 32 rows of a
+// chunk in shared memory (128-byte rows, 16-byte pieces swizzled by row) and
+// stores them back four whole row segments per instruction.
 
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -33,10 +32,12 @@ namespace relpos {
 namespace {
 
 constexpr int kRows = 128;
-constexpr int kChunk = 128;  // table rows per MMA group (N)
+constexpr int kChunk = 64;  // table rows per MMA group (N)
 constexpr uint32_t kATile = kRows * kHeadDim * 2;   // 16 KB
 constexpr uint32_t kBTile = kChunk * kHeadDim * 2;  // 16 KB
-constexpr uint32_t kWarpStage = 32 * kChunk * 2;    // 8 KB: 32 rows x 128 bf16
+constexpr uint32_t kWarpStage = 32 * kChunk * 2;    // 32 rows x kChunk bf16
+constexpr int kLanesPerRow = kChunk / 8;            // 16-byte pieces of a staged row
+constexpr int kRowsPerStore = 32 / kLanesPerRow;    // rows one warp store covers
 constexpr uint32_t kOffA = 0;
 constexpr uint32_t kOffB = kATile;                  // two chunk buffers
 constexpr uint32_t kOffStage = kOffB + 2 * kBTile;  // four warps' staging
@@ -48,7 +49,7 @@ constexpr uint32_t kTmemCols = 2 * kChunk;
 enum : uint32_t { kBarA = 0, kBarB = 1, kBarDone = 3, kBarFinal = 5, kNBar = 6 };
 constexpr uint32_t kOffSlot = kNBar * 8;
 
-__global__ void __launch_bounds__(128, 2)
+__global__ void __launch_bounds__(128, 4)
     deberta_proj_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmPk,
                         const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmPq,
                         const ProjParams pp) {
@@ -165,12 +166,12 @@ __global__ void __launch_bounds__(128, 2)
       }
     }
     if (vec_ok) {
-      // two rows (16 lanes x 16 bytes each) per store instruction
+      // kRowsPerStore whole row segments per store instruction
       __syncwarp();
 #pragma unroll 4
-      for (int it = 0; it < 16; ++it) {
-        const int r = 2 * it + (lane >> 4);
-        const int cc = lane & 15;
+      for (int it = 0; it < 32 / kRowsPerStore; ++it) {
+        const int r = kRowsPerStore * it + lane / kLanesPerRow;
+        const int cc = lane % kLanesPerRow;
         const int grow = i0 + warp * 32 + r;
         const int gcol = c * kChunk + cc * 8;
         uint32_t w0, w1, w2, w3;
