@@ -242,8 +242,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffBar + kOffAbort);
 
   // ---------------------------------------------------------------- setup
-  // Nothing before griddep_wait() below reads or writes global memory, so a
-  // launch that follows in the stream may run this part early.
+  // Nothing before griddep_wait() below loads from or writes to global memory
+  // (only L2 prefetches of the first tiles), so a launch that follows in the
+  // stream may run this part early.
   griddep_launch_dependents();
   uint8_t* aux = smem + kOffAux;
   uint8_t* bkt = aux;  // T5: head-independent bucket of each table offset
@@ -273,6 +274,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     tmem_alloc(sbase + kOffBar + kOffTmemSlot, kTmemCols);
     tmem_relinquish();
+  }
+  if (threadIdx.x == 0 && static_cast<int>(blockIdx.x) < nitems) {
+    // warm L2 with this CTA's first Q, K and V tiles while the previous kernel
+    // finishes (L2 is coherent, so the loads after the wait see its writes)
+    const Item it0 = make_item<SPLIT>(p, item_at(0));
+    tma_prefetch_l2_3d(&tmQ, 0, it0.row0[0], it0.bh);
+    if (!it0.split && it0.hi[1] > 0) tma_prefetch_l2_3d(&tmQ, 0, it0.row0[1], it0.bh);
+    const int nk = it0.ns < kStages ? it0.ns : kStages;
+    for (int s = 0; s < nk; ++s) {
+      tma_prefetch_l2_3d(&tmK, 0, stream_key(it0, s) * kBN, it0.bh);
+      tma_prefetch_l2_3d(&tmV, 0, stream_key(it0, s) * kBN, it0.bh);
+    }
   }
   griddep_wait();
   if constexpr (MODE == 1) {

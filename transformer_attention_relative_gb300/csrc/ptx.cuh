@@ -74,6 +74,12 @@ RP_DEVI void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory");
 RP_DEVI void tma_prefetch_desc(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
+// Bring a tile into L2 ahead of its load (no shared memory, no completion).
+RP_DEVI void tma_prefetch_l2_3d(const void* tmap, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(tmap), "r"(c0),
+               "r"(c1), "r"(c2)
+               : "memory");
+}
 RP_DEVI void tma_load_3d(uint32_t dst, const void* tmap, uint32_t bar, int c0, int c1, int c2) {
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
