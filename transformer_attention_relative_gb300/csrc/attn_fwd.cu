@@ -798,13 +798,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int c = 0; c < 128; ++c) {
               const int rel = r0 + c;
-              if (rel <= -kc) {
-                mass_l += xs[c];
-              } else if (rel >= kc) {
-                mass_r += xs[c];
-              } else {
-                wbin[rel + kc] += xs[c];
-              }
+              // branch-free: masses beyond the clip in registers, in-band
+              // offsets (-k < rel < k) into their bins
+              const float v = xs[c];
+              mass_l += rel <= -kc ? v : 0.f;
+              mass_r += rel >= kc ? v : 0.f;
+              if (static_cast<unsigned>(rel + kc - 1) < static_cast<unsigned>(2 * kc - 1)) wbin[rel + kc] += v;
             }
           }
         }
