@@ -414,6 +414,9 @@ extern "C" int relpos_attn_fwd(int mode, int dtype, const void* Q, const void* K
       p.aK = static_cast<const __nv_bfloat16*>(table0);
       p.aV = static_cast<const __nv_bfloat16*>(table1);
     }
+    // Shaw per-row tables: padded rows when shared memory allows
+    p.row_stride = 2 * rel_param + 2;
+    if (mode == RELPOS_SHAW && fwd_smem_bytes(mode, p) > fwd_max_smem_bytes()) p.row_stride = 2 * rel_param + 1;
     if (p.nsplit > 0 && fwd_smem_bytes(mode, p) > fwd_max_smem_bytes()) p.nsplit = 0;
     if (fwd_smem_bytes(mode, p) > fwd_max_smem_bytes()) return fail(RELPOS_ERR_UNSUPPORTED);
     if (mode == RELPOS_DEBERTA) {

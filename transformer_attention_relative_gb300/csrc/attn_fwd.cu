@@ -220,7 +220,7 @@ __host__ __device__ inline uint32_t fwd_aux_bytes(int mode, const FwdParams& p) 
   } else if (mode == 1) {
     const uint32_t nrel = 2u * p.kclip + 1u;
     const uint32_t tbl = (nrel * kHeadDim * 2u + 15u) & ~15u;
-    aux = 2u * tbl + 4u * 128u * nrel * 4u;
+    aux = 2u * tbl + 4u * 128u * static_cast<uint32_t>(p.row_stride) * 4u;
   }
   return (aux + 15u) & ~15u;
 }
@@ -502,8 +502,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if constexpr (MODE == 1) {
       aV_s = reinterpret_cast<const __nv_bfloat16*>(aux + shaw_tbl);
       float* qa_all = reinterpret_cast<float*>(aux + 2 * shaw_tbl);
-      qa = qa_all + (x * 128 + t) * nrel;
-      wbin = qa_all + 2 * 128 * nrel + (x * 128 + t) * nrel;
+      // rows p.row_stride floats apart: with 2k + 2 (even), the lanes of a
+      // near tile, which read offsets r0 - t + c of their rows, hit distinct
+      // banks (with 2k + 1 they are 2k words apart: one bank)
+      qa = qa_all + (x * 128 + t) * p.row_stride;
+      wbin = qa_all + 2 * 128 * p.row_stride + (x * 128 + t) * p.row_stride;
     }
     const int kc = p.kclip;
 

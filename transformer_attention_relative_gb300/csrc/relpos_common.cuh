@@ -82,6 +82,7 @@ struct FwdParams {
   const float* p2c_ends;     // [B*H, 2, ends_pitch]: P2C columns 0 and 2k - 1
   int ends_pitch;            // Lk rounded up to a multiple of 128
   int kclip;                 // Shaw / DeBERTa clip k
+  int row_stride;            // Shaw: floats per row of the per-row tables (2k + 1 or 2k + 2)
 };
 
 // DeBERTa relative products (deberta_proj.cu)
