@@ -337,6 +337,25 @@ def cpu_baseline(w, budget_s=12.0):
 
 # ---------------------------------------------------------------- main
 
+def max_over_ranks(value, world):
+    """The largest value over all ranks (for times: the slowest rank's)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    dev = (torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl"
+           else torch.device("cpu"))
+    t = torch.tensor([float(value)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(flops_per_step, steps, world, ms_max):
+    """Whole-job TFLOP/s: every rank ran `steps` steps of the workload (weak
+    scaling), the job took the slowest rank's time."""
+    return flops_per_step * steps * world / (ms_max / 1e3) / 1e12
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -423,14 +442,10 @@ def main():
         clocks["window"] = window
 
     # max over ranks
-    t_ms = torch.tensor([ms], dtype=torch.float64, device=device)
-    if world > 1:
-        import torch.distributed as dist
-        dist.all_reduce(t_ms, op=dist.ReduceOp.MAX)
-    ms_max = float(t_ms.item())
+    ms_max = max_over_ranks(ms, world)
     ms_step = ms_max / steps
     flops = w.flops()
-    value = flops * steps * world / (ms_max / 1e3) / 1e12
+    value = job_value(flops, steps, world, ms_max)
 
     kname, bound = dominant_kernel(w)
     avg_s = ms / steps / 1e3
