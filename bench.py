@@ -260,32 +260,63 @@ class GpuRun:
         return t0, time.time()
 
     def e2e(self, steps, warmup):
-        """Same metric through the public call with host buffers: every step copies
-        its inputs from pinned host memory and reads the output back."""
+        """Same metric through the public call with host buffers: every step
+        copies its inputs from pinned host memory and reads its output back.
+        Steps run as a serving loop would run them: copies in (one stream per
+        device buffer set, two sets alternating), the call and the copy out on
+        streams of their own, so that one step's copies overlap the
+        neighbouring steps' copies and work."""
         import torch
         pinned = {k: (v.pin_memory() if v is not None else None) for k, v in self.host.items()}
-        out_h = torch.empty(self.host["Q"].shape, dtype=self.host["Q"].dtype).pin_memory()
-        d = self.sets[0]
+        nbuf = 2
+        outs_h = [torch.empty(self.host["Q"].shape, dtype=self.host["Q"].dtype).pin_memory()
+                  for _ in range(nbuf)]
+        dsets = [self.sets[b % self.nsets] for b in range(nbuf)]
+        if self.nsets < nbuf:  # one resident set only (large inputs): add a second
+            d = {k: (v.to(self.device) if v is not None else None) for k, v in self.host.items()}
+            d["out"] = torch.empty_like(d["Q"])
+            dsets[1] = d
         h2d = sum(v.numel() * v.element_size() for v in pinned.values() if v is not None)
-        d2h = out_h.numel() * out_h.element_size()
+        d2h = outs_h[0].numel() * outs_h[0].element_size()
+        s_ins = [torch.cuda.Stream(self.device) for _ in range(nbuf)]
+        s_out = torch.cuda.Stream(self.device)
+        s_c = self.stream
+        ev_in = [torch.cuda.Event() for _ in range(nbuf)]
+        ev_c = [torch.cuda.Event() for _ in range(nbuf)]
+        ev_out = [torch.cuda.Event() for _ in range(nbuf)]
 
-        def one():
-            with torch.cuda.stream(self.stream):
+        def one(i):
+            b = i % nbuf
+            d = dsets[b]
+            s_in = s_ins[b]
+            with torch.cuda.stream(s_in):
+                s_in.wait_event(ev_c[b])  # the call two steps back has read this set
                 for k, v in pinned.items():
                     if v is not None:
                         d[k].copy_(v, non_blocking=True)
-                self._call(d)
-                out_h.copy_(d["out"], non_blocking=True)
+                ev_in[b].record(s_in)
+            s_c.wait_event(ev_in[b])
+            s_c.wait_event(ev_out[b])  # its output has been read back
+            self._call(d)
+            ev_c[b].record(s_c)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_c[b])
+                outs_h[b].copy_(d["out"], non_blocking=True)
+                ev_out[b].record(s_out)
 
-        for _ in range(warmup):
-            one()
+        for i in range(warmup):
+            one(i)
         torch.cuda.synchronize()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(self.stream)
-        for _ in range(steps):
-            one()
-        e1.record(self.stream)
+        e0.record(s_c)
+        for st in s_ins + [s_out]:
+            st.wait_stream(s_c)  # the timed region starts at e0 on every stream
+        for i in range(steps):
+            one(warmup + i)
+        for st in s_ins + [s_c]:
+            s_out.wait_stream(st)
+        e1.record(s_out)
         torch.cuda.synchronize()
         return e0.elapsed_time(e1), h2d, d2h
 
