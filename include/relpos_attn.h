@@ -85,6 +85,12 @@ extern "C" {
  *   num_buckets T5 only: even, 4 <= num_buckets <= 128.
  *   rel_param   T5: max_distance (> num_buckets/4 bidirectional, > num_buckets/2
  *               causal); Shaw: clip k (1 <= k <= 64); DeBERTa: k (1 <= k <= 4096).
+ *               Shaw's per-row tables and T5's bias-by-offset table live in
+ *               shared memory: this build runs Shaw k <= 21, and T5 as long as
+ *               the distance at which the last bucket starts (about
+ *               max_distance, or the longest offset of the call if shorter)
+ *               is at most about 480; beyond, the call returns
+ *               RELPOS_ERR_UNSUPPORTED.
  *   causal      0 or 1.
  *   q_offset    absolute position of query row 0 (>= 0), for cached decoding.
  *   out         device, [B, H, Lq, d], element type per dtype; written fully.
