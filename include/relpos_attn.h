@@ -89,7 +89,8 @@ extern "C" {
  *               shared memory: this build runs Shaw k <= 21, and T5 as long as
  *               the distance at which the last bucket starts (about
  *               max_distance, or the longest offset of the call if shorter)
- *               is at most about 480; beyond, the call returns
+ *               is at most about 2500 (beyond about 480 through a slower
+ *               single-copy table); beyond, the call returns
  *               RELPOS_ERR_UNSUPPORTED.
  *   causal      0 or 1.
  *   q_offset    absolute position of query row 0 (>= 0), for cached decoding.

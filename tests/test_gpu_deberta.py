@@ -25,6 +25,7 @@ DEB = WORKLOADS["deberta"]
     (1, 1, 1, 500, 8, True, 499),       # one query row
     (2, 2, 512, 512, 3, False, 0),      # odd, tiny clip
     (1, 2, 384, 384, 300, False, 0),    # 2k not a multiple of 256
+    (1, 2, 1100, 1100, 64, False, 0),   # odd query tiles, many key tiles: a pair with no tile b
 ])
 def test_deberta_small(B, H, Lq, Lk, k, causal, qoff):
     w = DEB.replace(B=B, H=H, Lq=Lq, Lk=Lk, rel_param=k, causal=causal, q_offset=qoff)

@@ -29,9 +29,18 @@ BASE = WORKLOADS["t5_base_bidir"]
     (2, 2, 513, 513, True, 0),
     (1, 2, 256, 100, False, 0),     # one key tile: split items without a merge
     (2, 2, 512, 384, False, 0),     # three key tiles: split 2 + 1, merged
+    (1, 2, 1100, 1100, False, 0),   # odd query tiles, many key tiles: a pair with no tile b
 ])
 def test_t5_small(B, H, Lq, Lk, causal, qoff):
     w = BASE.replace(B=B, H=H, Lq=Lq, Lk=Lk, causal=causal, q_offset=qoff)
+    G.parity(w)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_t5_long_saturation_single_copy_table(causal):
+    """max_distance beyond what the four shifted bias-table copies fit in
+    shared memory: the kernel keeps one copy and reads it entry by entry."""
+    w = BASE.replace(B=1, H=2, Lq=1100, Lk=1100, rel_param=2048, causal=causal)
     G.parity(w)
 
 

@@ -417,6 +417,8 @@ extern "C" int relpos_attn_fwd(int mode, int dtype, const void* Q, const void* K
     // Shaw per-row tables: padded rows when shared memory allows
     p.row_stride = 2 * rel_param + 2;
     if (mode == RELPOS_SHAW && fwd_smem_bytes(mode, p) > fwd_max_smem_bytes()) p.row_stride = 2 * rel_param + 1;
+    // T5: one table copy when the four shifted copies do not fit
+    if (mode == RELPOS_T5 && fwd_smem_bytes(mode, p) > fwd_max_smem_bytes()) p.t5_compact = 1;
     if (p.nsplit > 0 && fwd_smem_bytes(mode, p) > fwd_max_smem_bytes()) p.nsplit = 0;
     if (fwd_smem_bytes(mode, p) > fwd_max_smem_bytes()) return fail(RELPOS_ERR_UNSUPPORTED);
     if (mode == RELPOS_DEBERTA) {

@@ -195,15 +195,18 @@ RP_DEVI int next_head(const FwdParams& p, int x, int r, int nitems) {
 // with r = (lowest start of the quarter) & 3, the rank q = (k - r) & 3 takes
 // chunk offset 2q, minus one for the copies whose windows begin one chunk
 // further on (k < r).
+// When the four copies do not fit shared memory (long saturation distance),
+// the table is kept as one copy read one entry per load ("compact").
 struct T5Tab {
-  float* base;  // [2 buffers][4 copies][stride]
+  float* base;  // [2 buffers][ncopy copies][stride]
   int len4;     // entries per copy
   int stride;   // floats per copy slot (multiple of 32, >= len4 + 28)
+  int ncopy;    // 4, or 1 (compact)
   int r;
   RP_DEVI float* copy(int buf, int k) const {
     const int q = (k - r) & 3;
     const int off = (2 * q - (k < r ? 1 : 0)) & 7;
-    return base + (buf * 4 + k) * stride + 4 * off;
+    return base + (buf * ncopy + k) * stride + 4 * off;
   }
 };
 
@@ -216,7 +219,8 @@ __host__ __device__ inline uint32_t fwd_aux_bytes(int mode, const FwdParams& p) 
   if (mode == 0) {
     const uint32_t bkt_bytes = (static_cast<uint32_t>(p.t5_tab_len4) + 4u + 127u) & ~127u;
     const uint32_t stride = (static_cast<uint32_t>(p.t5_tab_len4) + 28u + 31u) & ~31u;
-    aux = bkt_bytes + 2u * 8u * stride * 4u + 2u * 128u * 4u;
+    const uint32_t ncopy = p.t5_compact ? 1u : 4u;
+    aux = bkt_bytes + 2u * 2u * ncopy * stride * 4u + 2u * 128u * 4u;
   } else if (mode == 1) {
     const uint32_t nrel = 2u * p.kclip + 1u;
     const uint32_t tbl = (nrel * kHeadDim * 2u + 15u) & ~15u;
@@ -453,9 +457,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++pvc;
           ++vpos;
         }
-        // the other tile's remaining positions
-        if (ok) advance(kpos, kBarKFull, kBarKEmpty);
-        if (ok) advance(vpos, kBarVFull, kBarVEmpty);
+        // The other tile's remaining positions, K and V stage of each position
+        // together: releasing every K stage first could wait for a K load that
+        // needs a V stage this warp has not released yet (through the other
+        // issuer, whose P.V waits for that V stage).
+        for (int pos = min(kpos, vpos); ok && pos < it.ns; ++pos) {
+          const uint32_t r = kv_it + pos;
+          if (pos >= kpos) {
+            ok = mbar_wait_warp(bar(kBarKFull + r % kStages), (r / kStages) & 1);
+            if (ok && lane == 0) mbar_arrive(bar(kBarKEmpty + r % kStages));
+          }
+          if (ok && pos >= vpos) {
+            ok = mbar_wait_warp(bar(kBarVFull + r % kStages), (r / kStages) & 1);
+            if (ok && lane == 0) mbar_arrive(bar(kBarVEmpty + r % kStages));
+          }
+        }
         kv_it += it.ns;
         if (mine > 0) ++ocnt;
       }
@@ -497,8 +513,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // (tab_off - q_offset - 7) mod 4
       tab.r = (((p.t5_tab_off - p.q_offset - 7) % 4) + 4) % 4;
       const uint32_t bkt_bytes = (static_cast<uint32_t>(p.t5_tab_len4) + 4u + 127u) & ~127u;
-      tab.base = reinterpret_cast<float*>(aux + bkt_bytes) + x * 8 * tab.stride;
-      hbias = reinterpret_cast<float*>(aux + bkt_bytes) + 2 * 8 * tab.stride + x * 128;
+      tab.ncopy = p.t5_compact ? 1 : 4;
+      tab.base = reinterpret_cast<float*>(aux + bkt_bytes) + x * 2 * tab.ncopy * tab.stride;
+      hbias = reinterpret_cast<float*>(aux + bkt_bytes) + 2 * 2 * tab.ncopy * tab.stride + x * 128;
     } else if constexpr (MODE == 1) {
       aV_s = reinterpret_cast<const __nv_bfloat16*>(aux + shaw_tbl);
       float* qa_all = reinterpret_cast<float*>(aux + 2 * shaw_tbl);
@@ -527,7 +544,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = 0; e < 3; ++e) v[4 + e] = hbias[(w1 >> (8 * e)) & 0xffu];
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          *reinterpret_cast<float4*>(tab.copy(b, k) + y) = make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]);
+          if (k < tab.ncopy)
+            *reinterpret_cast<float4*>(tab.copy(b, k) + y) = make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]);
       }
       mbar_arrive(bar(kBarTab + x));
       return true;
@@ -663,7 +681,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool far = MODE != 2 && (far_l || far_r);
         const float addc = far ? (far_l ? add_l : add_r) : 0.f;
         if (!far) {
-          if constexpr (MODE == 0) {
+          if (MODE == 0 && p.t5_compact) {
+            const float* tb = tab.copy(buf, 0) + (j0 - prow + p.t5_tab_off);
+#pragma unroll
+            for (int c = 0; c < 128; ++c) xs[c] = fmaf(xs[c], sl2, tb[c]);
+          } else if constexpr (MODE == 0) {
             const int s0 = j0 - prow + p.t5_tab_off;  // table index of column 0
             const int k = s0 & 3;
             const float4* tp = reinterpret_cast<const float4*>(tab.copy(buf, k) + (s0 - k));

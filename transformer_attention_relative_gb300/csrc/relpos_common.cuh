@@ -67,6 +67,7 @@ struct FwdParams {
   int t5_tab_off;     // table index of offset 0
   int t5_tab_len4;    // t5_tab_len rounded up to a multiple of 4
   int t5_nb;          // num_buckets (<= 128)
+  int t5_compact;     // one table copy read per entry (the four do not fit)
   T5Index t5;
   int npairs;         // 256-row query-tile pairs per head
   int nsplit;         // trailing pair items run as two split items each
