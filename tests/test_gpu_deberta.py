@@ -26,6 +26,7 @@ DEB = WORKLOADS["deberta"]
     (2, 2, 512, 512, 3, False, 0),      # odd, tiny clip
     (1, 2, 384, 384, 300, False, 0),    # 2k not a multiple of 256
     (1, 2, 1100, 1100, 64, False, 0),   # odd query tiles, many key tiles: a pair with no tile b
+    (2, 2, 1, 4096, 256, True, 4095),   # one query row against many key tiles
 ])
 def test_deberta_small(B, H, Lq, Lk, k, causal, qoff):
     w = DEB.replace(B=B, H=H, Lq=Lq, Lk=Lk, rel_param=k, causal=causal, q_offset=qoff)

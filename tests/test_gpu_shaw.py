@@ -24,6 +24,7 @@ SHAW = WORKLOADS["shaw"]
     (1, 1, 1, 500, 16, True, 499),   # one query row (decode-shaped)
     (1, 2, 256, 256, 1, False, 0),
     (1, 2, 1100, 1100, 8, False, 0),   # odd query tiles, many key tiles: a pair with no tile b
+    (2, 2, 1, 4096, 16, True, 4095),   # one query row against many key tiles
 ])
 def test_shaw_small(B, H, Lq, Lk, k, causal, qoff):
     w = SHAW.replace(B=B, H=H, Lq=Lq, Lk=Lk, rel_param=k, causal=causal, q_offset=qoff)
