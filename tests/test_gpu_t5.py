@@ -107,6 +107,30 @@ def test_t5_fp32_ragged_causal():
     G.parity(w)
 
 
+@pytest.mark.parametrize("fp32", [False, True])
+def test_output_only_16_byte_aligned(fp32):
+    """An output buffer 16 bytes past a 32-byte boundary takes the 16-byte
+    store path; it must give the same bits as an aligned buffer (split items
+    with a merge write half rows, so both row layouts are covered)."""
+    w = (WORKLOADS["t5_tiny_fp32"] if fp32 else BASE).replace(B=2, H=2, Lq=512, Lk=384)
+    x = make_inputs(w)
+    aligned = run_gpu_out(w, x, 0)
+    shifted = run_gpu_out(w, x, 16)
+    assert torch.equal(aligned, shifted)
+    ref = G.run_oracle(w, x)
+    G.compare(shifted.float().cpu().double().numpy(), ref, what="16-byte aligned output")
+
+
+def run_gpu_out(w, x, offset_bytes):
+    dt = x["Q"].dtype
+    n = x["Q"].numel()
+    pad = offset_bytes // x["Q"].element_size()
+    buf = torch.empty(n + 64, dtype=dt, device="cuda")
+    assert buf.data_ptr() % 256 == 0
+    out = buf[pad:pad + n].view(x["Q"].shape)
+    return G.run_gpu(w, x, out=out).clone()
+
+
 def test_empty_keys_give_zero_rows():
     dev = torch.device("cuda")
     Q = torch.randn(1, 2, 5, 64, device=dev).to(torch.bfloat16)

@@ -397,6 +397,7 @@ extern "C" int relpos_attn_fwd(int mode, int dtype, const void* Q, const void* K
     p.q_offset = q_offset;
     p.scale_log2 = scale * kLog2e;
     p.out = out;
+    p.out_v8 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0;
     p.status = status;
     p.kclip = rel_param;
     p.Qg = static_cast<const __nv_bfloat16*>(Qb);

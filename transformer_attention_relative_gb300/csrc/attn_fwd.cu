@@ -168,19 +168,22 @@ RP_DEVI bool stream_uses(const Item& it, int x, int s) {
 // Field x of an item, selected without indexing (keeps the item in registers).
 RP_DEVI int sel(const int (&v)[2], int x) { return x ? v[1] : v[0]; }
 
-// The item a CTA takes in round r: items are ordered longest first, and the
-// CTAs sweep them in alternating directions (round 0 left to right, round 1
-// right to left, ...) so that long and short causal items pair up.
-RP_DEVI int item_at(int r) {
+// The item a CTA takes in round r: items are ordered longest first. With
+// causal masking the CTAs sweep them in alternating directions (round 0 left
+// to right, round 1 right to left, ...) so that long and short items pair
+// up. Otherwise every item is equally long and every round goes left to
+// right: CTAs are dispatched in index order, so the lowest indices start
+// first and those take the extra items of a final partial round.
+RP_DEVI int item_at(int r, bool snake) {
   const int g = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
-  return r * g + ((r & 1) ? g - 1 - c : c);
+  return r * g + ((snake && (r & 1)) ? g - 1 - c : c);
 }
 
 // Head of the first item from round r on in which query tile x has key tiles,
 // or -1.
 template <bool SPLIT>
 RP_DEVI int next_head(const FwdParams& p, int x, int r, int nitems) {
-  for (int w = item_at(r); w < nitems; w = item_at(++r)) {
+  for (int w = item_at(r, p.causal); w < nitems; w = item_at(++r, p.causal)) {
     const Item it = make_item<SPLIT>(p, w);
     if (sel(it.hi, x) > sel(it.lo, x)) return it.h;
   }
@@ -246,9 +249,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffBar + kOffAbort);
 
   // ---------------------------------------------------------------- setup
-  // Nothing before griddep_wait() below loads from or writes to global memory
-  // (only L2 prefetches of the first tiles), so a launch that follows in the
-  // stream may run this part early.
+  // Nothing here loads from or writes to global memory (only L2 prefetches of
+  // the first tiles), so a launch that follows in the stream may run it
+  // early. Each role waits for the previous kernel (griddep_wait) just before
+  // its own first global access: the producers before their first load, the
+  // softmax warpgroups before their first table read; the MMA issuers touch
+  // global memory only to report an error.
   griddep_launch_dependents();
   uint8_t* aux = smem + kOffAux;
   uint8_t* bkt = aux;  // T5: head-independent bucket of each table offset
@@ -279,28 +285,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(sbase + kOffBar + kOffTmemSlot, kTmemCols);
     tmem_relinquish();
   }
-  if (threadIdx.x == 0 && static_cast<int>(blockIdx.x) < nitems) {
-    // warm L2 with this CTA's first Q, K and V tiles while the previous kernel
-    // finishes (L2 is coherent, so the loads after the wait see its writes)
-    const Item it0 = make_item<SPLIT>(p, item_at(0));
+  // This CTA's first item: its Q tile(s) and first K / V ring stages are
+  // warmed in L2 while the previous kernel finishes (L2 is coherent, so the
+  // loads after the wait see its writes), then loaded by this thread as soon
+  // as the inputs may be read; the producer loops start after them.
+  const bool first_loads = threadIdx.x == 0 && static_cast<int>(blockIdx.x) < nitems;
+  Item it0{};
+  bool two0 = false;
+  int nk0 = 0;
+  if (first_loads) {
+    it0 = make_item<SPLIT>(p, item_at(0, p.causal));
+    two0 = !it0.split && it0.hi[1] > 0;
+    nk0 = it0.ns < kStages ? it0.ns : kStages;
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
     tma_prefetch_l2_3d(&tmQ, 0, it0.row0[0], it0.bh);
-    if (!it0.split && it0.hi[1] > 0) tma_prefetch_l2_3d(&tmQ, 0, it0.row0[1], it0.bh);
-    const int nk = it0.ns < kStages ? it0.ns : kStages;
-    for (int s = 0; s < nk; ++s) {
+    if (two0) tma_prefetch_l2_3d(&tmQ, 0, it0.row0[1], it0.bh);
+    for (int s = 0; s < nk0; ++s) {
       tma_prefetch_l2_3d(&tmK, 0, stream_key(it0, s) * kBN, it0.bh);
       tma_prefetch_l2_3d(&tmV, 0, stream_key(it0, s) * kBN, it0.bh);
     }
-  }
-  griddep_wait();
-  if constexpr (MODE == 1) {
-    const uint4* srcK = reinterpret_cast<const uint4*>(p.aK);
-    const uint4* srcV = reinterpret_cast<const uint4*>(p.aV);
-    uint4* dK = reinterpret_cast<uint4*>(aux);
-    uint4* dV = reinterpret_cast<uint4*>(aux + shaw_tbl);
-    const int n16 = nrel * kHeadDim * 2 / 16;
-    for (int x = threadIdx.x; x < n16; x += kThreads) {
-      dK[x] = __ldg(srcK + x);
-      dV[x] = __ldg(srcV + x);
+    if constexpr (MODE == 0) {
+      // the bias rows, read by the softmax warpgroups first thing
+      const int lines = min((p.t5_nb * p.H * 4 + 127) / 128, 64);
+      for (int l = 0; l < lines; ++l) prefetch_l2(reinterpret_cast<const char*>(p.bias) + l * 128);
     }
   }
   tc_fence_before();
@@ -320,9 +329,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ------------------------------------------------------------ producers
       // warp 0: each item's Q tiles and the K ring; warp 2: the V ring
       const bool kq = warp == 0;
-      if (lane == 0) {
-        tma_prefetch_desc(kq ? &tmK : &tmV);
-        if (kq) tma_prefetch_desc(&tmQ);
+      griddep_wait();
+      if (first_loads) {
+        mbar_arrive_expect_tx(bar(kBarQFull), (two0 ? 2u : 1u) * kTileBytes);
+        tma_load_3d(sbase + kOffQ, &tmQ, bar(kBarQFull), 0, it0.row0[0], it0.bh);
+        if (two0) tma_load_3d(sbase + kOffQ + kTileBytes, &tmQ, bar(kBarQFull), 0, it0.row0[1], it0.bh);
+        for (int s = 0; s < nk0; ++s) {
+          const int key0 = stream_key(it0, s) * kBN;
+          mbar_arrive_expect_tx(bar(kBarKFull + s), kTileBytes);
+          tma_load_3d(sbase + kOffK + s * kTileBytes, &tmK, bar(kBarKFull + s), 0, key0, it0.bh);
+          mbar_arrive_expect_tx(bar(kBarVFull + s), kTileBytes);
+          tma_load_3d(sbase + kOffV + s * kTileBytes, &tmV, bar(kBarVFull + s), 0, key0, it0.bh);
+        }
       }
       const uint32_t full0 = kq ? kBarKFull : kBarVFull;
       const uint32_t empty0 = kq ? kBarKEmpty : kBarVEmpty;
@@ -331,10 +349,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       uint32_t it_cnt = 0;
       int item_cnt = 0;
-      for (int rr = 0, w = item_at(0); ok && w < nitems; w = item_at(++rr), ++item_cnt) {
+      for (int rr = 0, w = item_at(0, p.causal); ok && w < nitems; w = item_at(++rr, p.causal), ++item_cnt) {
         const Item it = make_item<SPLIT>(p, w);
-        if (kq) {
-          if (item_cnt > 0) ok = mbar_wait_warp(bar(kBarQEmpty), (item_cnt - 1) & 1);
+        // the first item's Q and first ring stages were loaded in the setup
+        const int pre = item_cnt == 0 ? min(it.ns, kStages) : 0;
+        if (kq && item_cnt > 0) {
+          ok = mbar_wait_warp(bar(kBarQEmpty), (item_cnt - 1) & 1);
           if (!ok) break;
           // a split item's single query tile goes to the Q_a buffer
           const bool two = !it.split && it.hi[1] > 0;
@@ -344,6 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_3d_elect(sbase + kOffQ + kTileBytes, &tmQ, bar(kBarQFull), 0, it.row0[1], it.bh);
         }
         for (int j = 0; j < it.ns; ++j, ++it_cnt) {
+          if (j < pre) continue;
           const uint32_t st = it_cnt % kStages;
           if (it_cnt >= kStages) {
             ok = mbar_wait_warp(bar(empty0 + st), ((it_cnt / kStages) - 1) & 1);
@@ -387,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t s_col = tmem + kTmemS + x * kBN;
       const uint32_t o_col = tmem + kTmemO + x * kHeadDim;
       const uint32_t p_col = tmem + kTmemP + x * 64;
-      for (int rr = 0, w = item_at(0); ok && w < nitems; w = item_at(++rr), ++item_cnt) {
+      for (int rr = 0, w = item_at(0, p.causal); ok && w < nitems; w = item_at(++rr, p.causal), ++item_cnt) {
         const Item it = make_item<SPLIT>(p, w);
         const int mine = sel(it.hi, x) - sel(it.lo, x);
         const uint64_t dq = dq_a + ((it.split ? 0u : x) * kStageStep);
@@ -476,6 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (mine > 0) ++ocnt;
       }
       if (!ok && lane == 0) {
+        griddep_wait();
         record_error(p.status);
         *abort_flag = 1;
       }
@@ -498,6 +520,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = p.scale_log2;
     const float kNegInf = -INFINITY;
     bool err = false;
+    if constexpr (MODE == 1) {
+      // the relative key / value tables, read only by the softmax warpgroups
+      griddep_wait();
+      const uint4* srcK = reinterpret_cast<const uint4*>(p.aK);
+      const uint4* srcV = reinterpret_cast<const uint4*>(p.aV);
+      uint4* dK = reinterpret_cast<uint4*>(aux);
+      uint4* dV = reinterpret_cast<uint4*>(aux + shaw_tbl);
+      const int n16 = nrel * kHeadDim * 2 / 16;
+      for (int i = static_cast<int>(threadIdx.x) - 128; i < n16; i += 256) {
+        dK[i] = __ldg(srcK + i);
+        dV[i] = __ldg(srcV + i);
+      }
+      named_bar_sync(1, 256);
+    }
 
     T5Tab tab{};
     float* hbias = nullptr;  // T5: this head's bias per bucket (log2 units)
@@ -552,16 +588,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     if constexpr (MODE == 0) {
       const int h0 = next_head<SPLIT>(p, x, 0, nitems);
+      griddep_wait();
       if (h0 >= 0) {
         if (t < p.t5_nb) hb_next = __ldg(p.bias + t * p.H + h0);
         if (!t5_build(0)) err = true;
       }
     }
 
+    if constexpr (MODE == 2) griddep_wait();
     uint32_t cnt = 0, ocnt = 0;
     uint32_t ccnt = 0;  // split items merged with the other warpgroup
     float2* ml = reinterpret_cast<float2*>(aux + fwd_aux_bytes(MODE, p));
-    for (int rr = 0, w = item_at(0); !err && w < nitems; w = item_at(++rr)) {
+    for (int rr = 0, w = item_at(0, p.causal); !err && w < nitems; w = item_at(++rr, p.causal)) {
       const Item it = make_item<SPLIT>(p, w);
       const int lo_x = sel(it.lo, x);
       const int n_kv = sel(it.hi, x) - lo_x;
@@ -964,22 +1002,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (row < p.Lq) {
         const size_t base = (static_cast<size_t>(it.bh) * p.Lq + row) * kHeadDim + c0;
         const int ncol = merge ? 32 : kHeadDim;
+        // each store instruction of a warp touches 32 rows, one line each:
+        // 32-byte stores halve those line writes when the output allows them
         if constexpr (OUT_F32) {
           float* dst = static_cast<float*>(p.out) + base;
+          auto w = [&](int c) { return __float_as_uint(o[c] * inv_l); };
+          if (p.out_v8) {
 #pragma unroll
-          for (int c = 0; c < kHeadDim; c += 4)
-            if (c < ncol)
-              st_global_v4(dst + c, __float_as_uint(o[c] * inv_l), __float_as_uint(o[c + 1] * inv_l),
-                           __float_as_uint(o[c + 2] * inv_l), __float_as_uint(o[c + 3] * inv_l));
+            for (int c = 0; c < kHeadDim; c += 8)
+              if (c < ncol) st_global_v8(dst + c, w(c), w(c + 1), w(c + 2), w(c + 3), w(c + 4), w(c + 5), w(c + 6), w(c + 7));
+          } else {
+#pragma unroll
+            for (int c = 0; c < kHeadDim; c += 4)
+              if (c < ncol) st_global_v4(dst + c, w(c), w(c + 1), w(c + 2), w(c + 3));
+          }
         } else {
           __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + base;
+          auto w = [&](int c) { return pack_bf16x2(o[c] * inv_l, o[c + 1] * inv_l); };
+          if (p.out_v8) {
 #pragma unroll
-          for (int c = 0; c < kHeadDim; c += 8)
-            if (c < ncol)
-              st_global_v4(dst + c, pack_bf16x2(o[c] * inv_l, o[c + 1] * inv_l),
-                           pack_bf16x2(o[c + 2] * inv_l, o[c + 3] * inv_l),
-                           pack_bf16x2(o[c + 4] * inv_l, o[c + 5] * inv_l),
-                           pack_bf16x2(o[c + 6] * inv_l, o[c + 7] * inv_l));
+            for (int c = 0; c < kHeadDim; c += 16)
+              if (c < ncol)
+                st_global_v8(dst + c, w(c), w(c + 2), w(c + 4), w(c + 6), w(c + 8), w(c + 10), w(c + 12), w(c + 14));
+          } else {
+#pragma unroll
+            for (int c = 0; c < kHeadDim; c += 8)
+              if (c < ncol) st_global_v4(dst + c, w(c), w(c + 2), w(c + 4), w(c + 6));
+          }
         }
       }
     }

@@ -74,6 +74,8 @@ RP_DEVI void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory");
 RP_DEVI void tma_prefetch_desc(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
+// Bring one 128-byte line into L2 ahead of its load.
+RP_DEVI void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
 // Bring a tile into L2 ahead of its load (no shared memory, no completion).
 RP_DEVI void tma_prefetch_l2_3d(const void* tmap, int c0, int c1, int c2) {
   asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(tmap), "r"(c0),
@@ -255,6 +257,13 @@ RP_DEVI void setmaxnreg_dec() {
 
 RP_DEVI void st_global_v4(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+// 32-byte store (the address must be 32-byte aligned)
+RP_DEVI void st_global_v8(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d, uint32_t e, uint32_t f,
+                          uint32_t g, uint32_t h) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a), "r"(b), "r"(c),
+               "r"(d), "r"(e), "r"(f), "r"(g), "r"(h)
                : "memory");
 }
 

@@ -59,6 +59,7 @@ struct FwdParams {
   int causal, q_offset;
   float scale_log2;  // softmax scale times log2(e)
   void* out;
+  int out_v8;  // out is 32-byte aligned: rows are written with 32-byte stores
   int* status;
   // T5
   const float* bias;  // [num_buckets, H]
