@@ -398,6 +398,7 @@ extern "C" int relpos_attn_fwd(int mode, int dtype, const void* Q, const void* K
     p.scale_log2 = scale * kLog2e;
     p.out = out;
     p.out_v8 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0;
+    p.stagger = mode == RELPOS_T5 && causal;  // long items of mostly far tiles
     p.status = status;
     p.kclip = rel_param;
     p.Qg = static_cast<const __nv_bfloat16*>(Qb);

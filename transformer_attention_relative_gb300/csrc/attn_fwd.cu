@@ -80,7 +80,8 @@ enum : uint32_t {
   kBarOFree = kBarODone + 2,
   kBarTab = kBarOFree + 2,
   kBarComb = kBarTab + 2,  // both softmax warpgroups have published a split item's partial state
-  kBarFinal = kBarComb + 1,
+  kBarStag = kBarComb + 1,  // + item parity: warpgroup a is past the maximum of its first tile
+  kBarFinal = kBarStag + 2,
   kNumBars = kBarFinal + 1,
 };
 constexpr uint32_t kOffTmemSlot = 256;
@@ -232,10 +233,14 @@ __host__ __device__ inline uint32_t fwd_aux_bytes(int mode, const FwdParams& p) 
   return (aux + 15u) & ~15u;
 }
 
-template <int MODE, bool OUT_F32, bool SPLIT>
+// VAR 0: pair items only; 1: with split items (p.nsplit > 0); 2: pair items
+// with the two softmax warpgroups staggered (p.stagger).
+template <int MODE, bool OUT_F32, int VAR>
 __global__ void __launch_bounds__(kThreads, 1)
     relpos_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+  constexpr bool SPLIT = VAR == 1;
+  constexpr bool STAG = VAR == 2;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t sbase = (raw_addr + 1023u) & ~1023u;
@@ -270,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (uint32_t i = 0; i < kNumBars; ++i) {
       uint32_t cnt = 1;
       if (i == kBarPFull || i == kBarPFull + 1 || i == kBarTab || i == kBarTab + 1 ||
-          i == kBarSFree || i == kBarSFree + 1)
+          i == kBarSFree || i == kBarSFree + 1 || i == kBarStag || i == kBarStag + 1)
         cnt = 128;  // every thread of a softmax warpgroup
       if (i == kBarOFree || i == kBarOFree + 1 || i == kBarComb)
         cnt = 256;  // both softmax warpgroups (or one, arriving twice)
@@ -598,11 +603,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     if constexpr (MODE == 2) griddep_wait();
     uint32_t cnt = 0, ocnt = 0;
     uint32_t ccnt = 0;  // split items merged with the other warpgroup
+    // With STAG, warpgroup b starts each item once warpgroup a has its
+    // first tile's maximum, so that the two run about half a tile apart and
+    // their exponential phases (MUFU) overlap the other's score and maximum
+    // phases instead of each other. It pays on long items of mostly far
+    // tiles (causal T5); on short items the later start of b costs more.
+    // `stag` counts the items in which a has key tiles; the item's turn goes
+    // to one of two alternating barriers: a can lead b by at most two items
+    // (b has started the last tile of item n - 2 before a's item n has its
+    // Q tiles), so two barriers keep the parities apart.
+    uint32_t stag = 0;
     float2* ml = reinterpret_cast<float2*>(aux + fwd_aux_bytes(MODE, p));
     for (int rr = 0, w = item_at(0, p.causal); !err && w < nitems; w = item_at(++rr, p.causal)) {
       const Item it = make_item<SPLIT>(p, w);
       const int lo_x = sel(it.lo, x);
       const int n_kv = sel(it.hi, x) - lo_x;
+      const uint32_t stag_it = stag;
+      const bool a_has = it.hi[0] > it.lo[0];
+      if (x == 0 ? n_kv > 0 : a_has) ++stag;
       if (n_kv == 0) continue;
       const int i0 = sel(it.row0, x);
       const int prow = i0 + t + p.q_offset;  // absolute position of this row
@@ -674,6 +692,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       float m_run = kNegInf;
       float l_run = 0.f;
+      if (STAG && x == 1 && a_has) {
+        const bool ok = mbar_wait(bar(kBarStag + (stag_it & 1)), (stag_it >> 1) & 1);
+        err = __any_sync(0xffffffffu, !ok);
+        if (err) break;
+      }
       for (int j = 0; j < n_kv; ++j, ++cnt) {
         const int j0 = (lo_x + j) * kBN;
         bool ok = mbar_wait(bar(kBarSFull + x), cnt & 1);
@@ -804,6 +827,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mx = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
           if (far) mx = fmaf(mx, sl2, addc);
         }
+        if (STAG && x == 0 && j == 0) mbar_arrive(bar(kBarStag + (stag_it & 1)));
 
         // ---- running max with lazy rescale
         const float m_new = fmaxf(m_run, mx);
@@ -1081,16 +1105,19 @@ cudaError_t launch_fwd(int mode, bool out_f32, const CUtensorMap& tmQ, const CUt
   dim3 grid(nitems < num_sms ? nitems : num_sms);
   dim3 block(kThreads);
   void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const FwdParams) = nullptr;
-  const bool split = p.nsplit > 0;
+  const int var = p.nsplit > 0 ? 1 : (p.stagger ? 2 : 0);
   if (mode == 0) {
-    kern = out_f32 ? (split ? relpos_fwd_kernel<0, true, true> : relpos_fwd_kernel<0, true, false>)
-                   : (split ? relpos_fwd_kernel<0, false, true> : relpos_fwd_kernel<0, false, false>);
-  } else if (mode == 1) {
-    kern = out_f32 ? (split ? relpos_fwd_kernel<1, true, true> : relpos_fwd_kernel<1, true, false>)
-                   : (split ? relpos_fwd_kernel<1, false, true> : relpos_fwd_kernel<1, false, false>);
-  } else if (mode == 2) {
-    kern = out_f32 ? (split ? relpos_fwd_kernel<2, true, true> : relpos_fwd_kernel<2, true, false>)
-                   : (split ? relpos_fwd_kernel<2, false, true> : relpos_fwd_kernel<2, false, false>);
+    if (var == 2)
+      kern = out_f32 ? relpos_fwd_kernel<0, true, 2> : relpos_fwd_kernel<0, false, 2>;
+    else
+      kern = out_f32 ? (var ? relpos_fwd_kernel<0, true, 1> : relpos_fwd_kernel<0, true, 0>)
+                     : (var ? relpos_fwd_kernel<0, false, 1> : relpos_fwd_kernel<0, false, 0>);
+  } else if (mode == 1 && var < 2) {
+    kern = out_f32 ? (var ? relpos_fwd_kernel<1, true, 1> : relpos_fwd_kernel<1, true, 0>)
+                   : (var ? relpos_fwd_kernel<1, false, 1> : relpos_fwd_kernel<1, false, 0>);
+  } else if (mode == 2 && var < 2) {
+    kern = out_f32 ? (var ? relpos_fwd_kernel<2, true, 1> : relpos_fwd_kernel<2, true, 0>)
+                   : (var ? relpos_fwd_kernel<2, false, 1> : relpos_fwd_kernel<2, false, 0>);
   } else {
     return cudaErrorNotSupported;
   }
@@ -1098,8 +1125,8 @@ cudaError_t launch_fwd(int mode, bool out_f32, const CUtensorMap& tmQ, const CUt
   // that every later launch fits)
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
-  const int slot = mode * 4 + (out_f32 ? 2 : 0) + (split ? 1 : 0);
-  static std::atomic<uint64_t> attr_set[12];
+  const int slot = mode * 6 + (out_f32 ? 3 : 0) + var;
+  static std::atomic<uint64_t> attr_set[18];
   const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
   if (!bit || !(attr_set[slot].load() & bit)) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -60,6 +60,7 @@ struct FwdParams {
   float scale_log2;  // softmax scale times log2(e)
   void* out;
   int out_v8;  // out is 32-byte aligned: rows are written with 32-byte stores
+  int stagger;  // offset the two softmax warpgroups by about half a tile
   int* status;
   // T5
   const float* bias;  // [num_buckets, H]
