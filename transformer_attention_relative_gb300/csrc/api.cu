@@ -336,16 +336,23 @@ extern "C" int relpos_attn_fwd(int mode, int dtype, const void* Q, const void* K
     off_part = scratch_bytes;
     scratch_bytes += BH * Lq * nchunks * (kHeadDim + 2) * sizeof(float);
   }
-  // DeBERTa: C2P [BH, Lq, 2k], P2C [BH, Lk, 2k] (bf16) and P2C's end columns
+  // DeBERTa: the band array [BH, Lq, band_pitch] (bf16, with kBandPad bytes
+  // before and after it: the attention kernel reads whole 128-key windows
+  // that may start up to 254 columns before a row and end up to 261 after
+  // the band, the part outside being replaced by the far terms), C2P's two
+  // saturated columns per query row and P2C's per key (fp32)
   const size_t n2k = 2 * static_cast<size_t>(rel_param);
+  const int band_pitch = static_cast<int>((n2k + 8 + 7) & ~static_cast<size_t>(7));
+  const int const_pitch = (Lq + 127) & ~127;
   const int ends_pitch = (Lk + 127) & ~127;
-  size_t off_c2p = 0, off_p2c = 0, off_ends = 0;
+  constexpr size_t kBandPad = 1024;
+  size_t off_band = 0, off_const = 0, off_ends = 0;
   if (mode == RELPOS_DEBERTA) {
     scratch_bytes = (scratch_bytes + 255) & ~static_cast<size_t>(255);
-    off_c2p = scratch_bytes;
-    scratch_bytes += ((BH * Lq * n2k * 2) + 255) & ~static_cast<size_t>(255);
-    off_p2c = scratch_bytes;
-    scratch_bytes += ((BH * Lk * n2k * 2) + 255) & ~static_cast<size_t>(255);
+    off_band = scratch_bytes + kBandPad;
+    scratch_bytes += ((BH * Lq * band_pitch * 2 + 2 * kBandPad) + 255) & ~static_cast<size_t>(255);
+    off_const = scratch_bytes;
+    scratch_bytes += BH * 2 * static_cast<size_t>(const_pitch) * sizeof(float);
     off_ends = scratch_bytes;
     scratch_bytes += BH * 2 * static_cast<size_t>(ends_pitch) * sizeof(float);
   }
@@ -425,29 +432,36 @@ extern "C" int relpos_attn_fwd(int mode, int dtype, const void* Q, const void* K
     if (fwd_smem_bytes(mode, p) > fwd_max_smem_bytes()) return fail(RELPOS_ERR_UNSUPPORTED);
     if (mode == RELPOS_DEBERTA) {
       uint8_t* sc = static_cast<uint8_t*>(scratch);
-      p.c2p = reinterpret_cast<const __nv_bfloat16*>(sc + off_c2p);
-      p.p2c = reinterpret_cast<const __nv_bfloat16*>(sc + off_p2c);
-      p.p2c_ends = reinterpret_cast<const float*>(sc + off_ends);
+      BandParams bp;
+      std::memset(&bp, 0, sizeof(bp));
+      bp.BH = static_cast<int>(BH);
+      bp.H = H;
+      bp.k = rel_param;
+      bp.Lq = Lq;
+      bp.Lk = Lk;
+      bp.q_offset = q_offset;
+      bp.scale = scale * kLog2e;
+      bp.K = static_cast<const __nv_bfloat16*>(Kb);
+      bp.Pq = static_cast<const __nv_bfloat16*>(table1);
+      bp.band = reinterpret_cast<__nv_bfloat16*>(sc + off_band);
+      bp.band_pitch = band_pitch;
+      bp.c2p_const = reinterpret_cast<float*>(sc + off_const);
+      bp.const_pitch = const_pitch;
+      bp.ends = reinterpret_cast<float*>(sc + off_ends);
+      bp.ends_pitch = ends_pitch;
+      bp.status = status;
+      p.band = bp.band;
+      p.band_pitch = band_pitch;
+      p.c2p_const = bp.c2p_const;
+      p.const_pitch = const_pitch;
+      p.p2c_ends = bp.ends;
       p.ends_pitch = ends_pitch;
       CUtensorMap tqa, tka, tpk, tpq;
-      ProjParams pp;
-      std::memset(&pp, 0, sizeof(pp));
-      pp.BH = static_cast<int>(BH);
-      pp.H = H;
-      pp.k = rel_param;
-      pp.scale = scale * kLog2e;
-      pp.status = status;
       if (!make_tmap_table(&tpk, table0, H, static_cast<int>(n2k)) ||
           !make_tmap_table(&tpq, table1, H, static_cast<int>(n2k)) ||
           !make_tmap(&tqa, Qb, Lq, static_cast<int>(BH)) || !make_tmap(&tka, Kb, Lk, static_cast<int>(BH)))
         return fail(RELPOS_ERR_CUDA);
-      pp.L[0] = Lq;
-      pp.L[1] = Lk;
-      pp.out[0] = reinterpret_cast<__nv_bfloat16*>(sc + off_c2p);
-      pp.out[1] = reinterpret_cast<__nv_bfloat16*>(sc + off_p2c);
-      pp.ends = reinterpret_cast<float*>(sc + off_ends);
-      pp.ends_pitch = ends_pitch;
-      if (launch_deberta_proj(tqa, tpk, tka, tpq, pp, s) != cudaSuccess) return fail(RELPOS_ERR_CUDA);
+      if (launch_deberta_band(tqa, tka, tpk, tpq, bp, s) != cudaSuccess) return fail(RELPOS_ERR_CUDA);
     }
     CUtensorMap tq, tk, tv;
     if (!make_tmap(&tq, Qb, Lq, static_cast<int>(BH)) || !make_tmap(&tk, Kb, Lk, static_cast<int>(BH)) ||

@@ -677,16 +677,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         add_l = qa[0];
         add_r = qa[2 * kc];
       }
-      const __nv_bfloat16* c2p_row = nullptr;  // DeBERTa: this row of C2P (log2 units)
-      const __nv_bfloat16* p2c_head = nullptr;  // DeBERTa: this head's P2C
+      const __nv_bfloat16* band_row = nullptr;  // DeBERTa: this row's band values (log2 units)
+      int band_sh = 0;                          // and its shift
       if constexpr (MODE == 2) {
-        const int n2k = 2 * kc;
+        // rows past Lq read row Lq - 1 (their results are not stored); the
+        // shift follows the row's own position, which keeps every window
+        // 16-byte aligned
         const int rowc = min(i0 + t, p.Lq - 1);
-        c2p_row = p.c2p + (static_cast<size_t>(it.bh) * p.Lq + rowc) * n2k;
-        p2c_head = p.p2c + static_cast<size_t>(it.bh) * p.Lk * n2k;
-        // keys far behind (i - j >= k) take delta(i, j) = 2k - 1; far ahead, 0
-        add_l = __bfloat162float(c2p_row[n2k - 1]);
-        add_r = __bfloat162float(c2p_row[0]);
+        band_row = p.band + (static_cast<size_t>(it.bh) * p.Lq + rowc) * p.band_pitch;
+        band_sh = (prow - kc) & 7;
+        // keys far behind (i - j >= k) take C2P[i][2k - 1]; far ahead, C2P[i][0]
+        const float* cc = p.c2p_const + static_cast<size_t>(it.bh) * 2 * p.const_pitch + rowc;
+        add_l = cc[0];
+        add_r = cc[p.const_pitch];
       }
       float mass_l = 0.f, mass_r = 0.f;
 
@@ -791,21 +794,53 @@ __global__ void __launch_bounds__(kThreads, 1)
                 xs[4 * q + 3] = b.y;
               }
             } else {
-              // band: c2p = C2P[i][delta(i, j)], p2c = P2C[j][delta(j, i)];
-              // with rel = j - i = r0 + c, delta(i, j) = clamp(k - rel, 0, 2k - 1)
-              // and delta(j, i) = clamp(k + rel, 0, 2k - 1)
-              const int n2k = 2 * kc;
-              const int r0 = j0 - prow;  // key - query offset of column 0
-              const int jmax = p.Lk - 1 - j0;  // last key of the tile (ragged tail)
-              const int dij0 = kc - r0, dji0 = kc + r0;
-              const __nv_bfloat16* p2c_tile = p2c_head + static_cast<size_t>(j0) * n2k;
+              // band: column c is key j = j0 + c, at band offset m = j - i + k
+              // = m0 + c. For 1 <= m <= 2k - 1 the row's band array holds
+              // c2p + p2c; beyond, the far terms of its side apply. The window
+              // starts 16-byte aligned (band_sh + m0 is a multiple of 8).
+              const int m0 = j0 - prow + kc;
+              const uint4* bw = reinterpret_cast<const uint4*>(band_row + (band_sh + m0));
+              const float2 sc2 = make_float2(sl2, sl2);
+              if (rel_lo > -kc && rel_hi < kc) {
+                // the whole tile lies inside the band
 #pragma unroll
-              for (int c = 0; c < 128; ++c) {
-                const int d_ij = min(max(dij0 - c, 0), n2k - 1);
-                const int d_ji = min(max(dji0 + c, 0), n2k - 1);
-                const float a = __bfloat162float(c2p_row[d_ij]);
-                const float b = __bfloat162float(p2c_tile[min(c, jmax) * n2k + d_ji]);
-                xs[c] = fmaf(xs[c], sl2, a + b);
+                for (int q = 0; q < 16; ++q) {
+                  const uint4 u = __ldg(bw + q);
+                  const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                  for (int e = 0; e < 4; ++e) {
+                    const int c = 8 * q + 2 * e;
+                    const float2 bv = make_float2(__uint_as_float(w4[e] << 16), __uint_as_float(w4[e] & 0xffff0000u));
+                    const float2 a = __ffma2_rn(make_float2(xs[c], xs[c + 1]), sc2, bv);
+                    xs[c] = a.x;
+                    xs[c + 1] = a.y;
+                  }
+                }
+              } else {
+                const float4* e0 = reinterpret_cast<const float4*>(
+                    p.p2c_ends + static_cast<size_t>(it.bh) * 2 * p.ends_pitch + j0);
+                const float4* e1 = e0 + p.ends_pitch / 4;
+                const int clo = 1 - m0, chi = 2 * kc - 1 - m0;  // in-band columns
+#pragma unroll
+                for (int q = 0; q < 16; ++q) {
+                  const uint4 u = __ldg(bw + q);
+                  const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                  for (int g = 0; g < 2; ++g) {
+                    const float4 f0 = __ldg(e0 + 2 * q + g);
+                    const float4 f1 = __ldg(e1 + 2 * q + g);
+                    const float l4[4] = {f0.x, f0.y, f0.z, f0.w};
+                    const float r4[4] = {f1.x, f1.y, f1.z, f1.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                      const int c = 8 * q + 4 * g + e;
+                      const uint32_t w = w4[2 * g + (e >> 1)];
+                      const float bv = __uint_as_float((e & 1) ? (w & 0xffff0000u) : (w << 16));
+                      const float far_v = c < clo ? add_l + l4[e] : add_r + r4[e];
+                      xs[c] = fmaf(xs[c], sl2, (c >= clo && c <= chi) ? bv : far_v);
+                    }
+                  }
+                }
               }
             }
           }

@@ -80,23 +80,31 @@ struct FwdParams {
   // DeBERTa
   const __nv_bfloat16* Pk;  // [2k, H, 64]
   const __nv_bfloat16* Pq;  // [2k, H, 64]
-  const __nv_bfloat16* c2p;  // [B*H, Lq, 2k]: log2-scaled q_i . Pk[r]
-  const __nv_bfloat16* p2c;  // [B*H, Lk, 2k]: log2-scaled k_j . Pq[r]
-  const float* p2c_ends;     // [B*H, 2, ends_pitch]: P2C columns 0 and 2k - 1
-  int ends_pitch;            // Lk rounded up to a multiple of 128
+  // DeBERTa (log2-scaled): band[bh][i][sh(i) + m] = c2p + p2c for key
+  // j = i + m - k with 1 <= m <= 2k - 1, sh(i) = (i + q_offset - k) mod 8;
+  // beyond the band c2p_const (C2P[i][2k - 1], C2P[i][0]) and p2c_ends
+  // (P2C[j][0], P2C[j][2k - 1]) apply
+  const __nv_bfloat16* band;  // [B*H, Lq, band_pitch]
+  int band_pitch;             // 2k + 8 rounded up to a multiple of 8
+  const float* c2p_const;     // [B*H, 2, const_pitch]
+  int const_pitch;            // Lq rounded up to a multiple of 128
+  const float* p2c_ends;      // [B*H, 2, ends_pitch]
+  int ends_pitch;             // Lk rounded up to a multiple of 128
   int kclip;                 // Shaw / DeBERTa clip k
   int row_stride;            // Shaw: floats per row of the per-row tables (2k + 1 or 2k + 2)
 };
 
-// DeBERTa relative products (deberta_proj.cu)
-// Both products in one launch: side 0 = C2P (rows of Q, table Pk), side 1 =
-// P2C (rows of K, table Pq, with the fp32 end columns).
-struct ProjParams {
-  int BH, H, k;
-  int L[2];              // rows of each side
-  float scale;           // applied to every product (softmax scale times log2 e)
-  __nv_bfloat16* out[2]; // [BH, L, 2k] per side
-  float* ends;           // side 1: [BH, 2, ends_pitch]
+// DeBERTa band pre-pass (deberta_band.cu)
+struct BandParams {
+  int BH, H, k, Lq, Lk, q_offset;
+  float scale;                // applied to every product (softmax scale times log2 e)
+  const __nv_bfloat16* K;     // [BH, Lk, 64]
+  const __nv_bfloat16* Pq;    // [2k, H, 64]
+  __nv_bfloat16* band;        // [BH, Lq, band_pitch]
+  int band_pitch;
+  float* c2p_const;           // [BH, 2, const_pitch]
+  int const_pitch;
+  float* ends;                // [BH, 2, ends_pitch]
   int ends_pitch;
   int* status;
 };

@@ -24,8 +24,8 @@ cudaError_t launch_fwd(int mode, bool out_f32, const CUtensorMap& tmQ, const CUt
 int t5_setup(int num_buckets, int max_distance, int causal, long long nmax, T5Index* ix, int* R);
 int check_rel_params(int mode, int num_buckets, int rel_param, int causal);
 
-cudaError_t launch_deberta_proj(const CUtensorMap& tmQ, const CUtensorMap& tmPk, const CUtensorMap& tmK,
-                                const CUtensorMap& tmPq, const ProjParams& pp, cudaStream_t stream);
+cudaError_t launch_deberta_band(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmPk,
+                                const CUtensorMap& tmPq, const BandParams& bp, cudaStream_t stream);
 
 int decode_chunk_keys();
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);
