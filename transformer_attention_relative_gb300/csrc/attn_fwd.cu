@@ -743,7 +743,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // DeBERTa tiles beyond the band still carry a per-key term, so every
         // DeBERTa tile takes the per-element path.
         const bool far = MODE != 2 && (far_l || far_r);
-        const float addc = far ? (far_l ? add_l : add_r) : 0.f;
+        // a row constant added with the maximum: the far constant of a far
+        // tile, and for DeBERTa tiles beyond the band the saturated c2p term
+        // (their per-key p2c term goes into the scaled scores)
+        const float addc = (far_l || far_r) ? (far_l ? add_l : add_r) : 0.f;
         if (!far) {
           if (MODE == 0 && p.t5_compact) {
             const float* tb = tab.copy(buf, 0) + (j0 - prow + p.t5_tab_off);
@@ -775,19 +778,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           } else if constexpr (MODE == 2) {
             if (far_l || far_r) {
-              // c2p: one value per row; p2c: the saturated end column of every key
-              const float rc = far_l ? add_l : add_r;
+              // p2c: the saturated end column of every key; the c2p row
+              // constant is addc
               const float4* ce = reinterpret_cast<const float4*>(
                   p.p2c_ends + (static_cast<size_t>(it.bh) * 2 + (far_l ? 0 : 1)) * p.ends_pitch + j0);
               const float2 sc2 = make_float2(sl2, sl2);
-              const float2 rc2 = make_float2(rc, rc);
 #pragma unroll
               for (int q = 0; q < 32; ++q) {
                 const float4 e = __ldg(ce + q);
-                float2 a = __ffma2_rn(make_float2(xs[4 * q], xs[4 * q + 1]), sc2,
-                                      __fadd2_rn(make_float2(e.x, e.y), rc2));
-                float2 b = __ffma2_rn(make_float2(xs[4 * q + 2], xs[4 * q + 3]), sc2,
-                                      __fadd2_rn(make_float2(e.z, e.w), rc2));
+                float2 a = __ffma2_rn(make_float2(xs[4 * q], xs[4 * q + 1]), sc2, make_float2(e.x, e.y));
+                float2 b = __ffma2_rn(make_float2(xs[4 * q + 2], xs[4 * q + 3]), sc2, make_float2(e.z, e.w));
                 xs[4 * q] = a.x;
                 xs[4 * q + 1] = a.y;
                 xs[4 * q + 2] = b.x;
@@ -860,7 +860,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             m3 = max3f(m3, xs[c + 6], xs[c + 7]);
           }
           mx = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
-          if (far) mx = fmaf(mx, sl2, addc);
+          mx = far ? fmaf(mx, sl2, addc) : mx + addc;
         }
         if (STAG && x == 0 && j == 0) mbar_arrive(bar(kBarStag + (stag_it & 1)));
 
@@ -880,7 +880,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
         {
           const float2 sc2 = far ? make_float2(sl2, sl2) : make_float2(1.f, 1.f);
-          const float off = (far ? addc : 0.f) - m_use;
+          const float off = addc - m_use;
           const float2 off2 = make_float2(off, off);
 #pragma unroll
           for (int c = 0; c < 128; c += 4) {
