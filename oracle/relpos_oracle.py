@@ -18,6 +18,8 @@ Sources (three web pages on relative position in attention):
 * [DRP] "DeBERTa > Relative Position Encoding" -- sections "The Relative
   Position Formula" (the delta(i, j) cases), "Why 2k Embeddings?" and the
   relative-position module.
+* ALiBi: [RPE] "ALiBi and RoPE: the two endpoints" -- T5 with the table
+  removed, a fixed slope per head times the distance, no maximum distance.
 
 Conventions (readings where the pages leave a step open are marked R#):
 
@@ -29,7 +31,9 @@ Conventions (readings where the pages leave a step open are marked R#):
   formula).
 * Scale: 1/sqrt(d) for T5 (R1: added bias after scaling) and Shaw (R7:
   the a_K term is inside the scaled dot product); 1/sqrt(3d) for DeBERTa
-  ([RPE] DeBERTa: three summed terms).
+  ([RPE] DeBERTa: three summed terms); ALiBi as T5 (R11: the bias
+  -slope_h * |j - p| is added after scaling; the slopes are an input, one
+  per head, since the pages fix no values).
 * Causal: keys with j > p are masked (-inf) before the softmax; a row with
   no visible key yields zeros (R10).
 * Everything is computed in float64 from the values given (already rounded
@@ -45,7 +49,7 @@ import math
 
 import numpy as np
 
-MODE_T5, MODE_SHAW, MODE_DEBERTA = 0, 1, 2
+MODE_T5, MODE_SHAW, MODE_DEBERTA, MODE_ALIBI = 0, 1, 2, 3
 
 
 # --------------------------------------------------------------------------
@@ -119,7 +123,8 @@ def index_ids(mode: int, rels, num_buckets: int = 32, rel_param: int = 128,
 
     T5: ``rels`` are key-minus-query offsets, ids are buckets. Shaw: same
     offsets, ids are clipped table rows. DeBERTa: ``rels`` are query-minus-
-    key offsets r = i - j, ids are delta (computed as delta(r, 0)).
+    key offsets r = i - j, ids are delta (computed as delta(r, 0)). ALiBi:
+    key-minus-query offsets, ids are the distances |rel|.
     """
     out = np.empty(len(rels), dtype=np.int64)
     for n, r in enumerate(rels):
@@ -128,6 +133,8 @@ def index_ids(mode: int, rels, num_buckets: int = 32, rel_param: int = 128,
             out[n] = t5_bucket(r, not causal, num_buckets, rel_param)
         elif mode == MODE_SHAW:
             out[n] = shaw_index(r, rel_param)
+        elif mode == MODE_ALIBI:
+            out[n] = abs(r)
         else:
             out[n] = deberta_delta(r, 0, rel_param)
     return out
@@ -250,13 +257,28 @@ def deberta_logits(q, k, pk_h, pq_h, p, kclip):
     return (q @ k.T + c2p + p2c) / math.sqrt(3 * d)
 
 
+def alibi_logits(q, k, slope_h, p):
+    """Scaled ALiBi logits q_i . k_j / sqrt(d) - slope_h * |j - p_i|.
+
+    [RPE] "ALiBi and RoPE: the two endpoints": the T5 bias with the table
+    removed, a fixed slope per head times the distance and no maximum
+    distance (R11). With causal masking only keys j <= p_i remain, whose
+    distance is p_i - j.
+    """
+    d = q.shape[1]
+    j = np.arange(k.shape[0])
+    dist = np.abs(j[None, :] - p[:, None]).astype(np.float64)
+    return q @ k.T / math.sqrt(d) - slope_h * dist
+
+
 def attention(mode: int, Q, K, V, table0, table1=None, *, num_buckets: int = 32,
               rel_param: int = 128, causal: bool = False, q_offset: int = 0,
               rows=None, heads=None) -> np.ndarray:
     """Forward relative-position attention in fp64.
 
     Q [B,H,Lq,d], K/V [B,H,Lk,d]. Tables: T5 bias [num_buckets, H];
-    Shaw a_K, a_V [2k+1, d]; DeBERTa Pk, Pq [2k, H, d]. ``rows`` limits the
+    Shaw a_K, a_V [2k+1, d]; DeBERTa Pk, Pq [2k, H, d]; ALiBi slopes [H].
+    ``rows`` limits the
     computation to some query rows (the result then has len(rows) rows);
     ``heads`` to some (b, h) pairs (result [len(heads), rows, d]).
     Returns [B, H, rows, d] (or the ``heads`` form) in float64.
@@ -282,6 +304,8 @@ def attention(mode: int, Q, K, V, table0, table1=None, *, num_buckets: int = 32,
             lg = t5_logits(q, k, t0[:, h], p, num_buckets, rel_param, causal)
         elif mode == MODE_SHAW:
             lg = shaw_logits(q, k, t0, p, rel_param)
+        elif mode == MODE_ALIBI:
+            lg = alibi_logits(q, k, t0[h], p)
         else:
             lg = deberta_logits(q, k, t0[:, h, :], t1[:, h, :], p, rel_param)
         w = _softmax_rows(_mask(lg, p, Lk, causal))

@@ -8,6 +8,7 @@ and checks that at least one pin fails for each.
 
 Page names: [RPE] "Relative Position Embeddings, in depth"; [T5B] "T5
 Relative-Position Bias"; [DRP] "DeBERTa > Relative Position Encoding".
+ALiBi follows [RPE] "ALiBi and RoPE: the two endpoints".
 """
 from __future__ import annotations
 
@@ -374,12 +375,68 @@ def check_query_offset_consistency():
         assert np.max(np.abs(dec[:, :, 0] - full[:, :, L - 1])) < 1e-12
 
 
+# ---------------------------------------------------------------- ALiBi
+
+def check_alibi_zero_slopes_are_sdpa():
+    """ALiBi with every slope zero is plain softmax attention, scale 1/sqrt(d)."""
+    rng = _rng(21)
+    B, H, d = 2, 3, 16
+    for causal, qoff, Lq, Lk in ((False, 0, 11, 11), (True, 0, 13, 13), (True, 7, 4, 11)):
+        Q, K, V = (rng.standard_normal((B, H, n, d)) for n in (Lq, Lk, Lk))
+        a = orc.attention(orc.MODE_ALIBI, Q, K, V, np.zeros(H), causal=causal, q_offset=qoff)
+        b = _sdpa(Q, K, V, 1 / math.sqrt(d), causal, qoff)
+        assert np.max(np.abs(a - b)) < 1e-12, causal
+
+
+def _geo(r, m0, m1):
+    """Sum of r^m and of m r^m for m = m0 .. m1, by the closed forms of the
+    geometric and arithmetico-geometric series."""
+    if m1 < m0:
+        return 0.0, 0.0
+
+    def upto(M):  # m = 0 .. M
+        s0 = (1 - r ** (M + 1)) / (1 - r)
+        s1 = r * (1 - (M + 1) * r ** M + M * r ** (M + 1)) / (1 - r) ** 2
+        return s0, s1
+    a0, a1 = upto(m1)
+    if m0 == 0:
+        return a0, a1
+    b0, b1 = upto(m0 - 1)
+    return a0 - b0, a1 - b1
+
+
+def check_alibi_closed_form():
+    """With zero content scores the ALiBi weights of query position a are
+    proportional to r^|j - a|, r = exp(-slope): with v_j = j the output is
+    sum_j j r^|j - a| / sum_j r^|j - a|, summed in closed form over the keys
+    left of a (j = a - m, m = 1 .. a) and right of it (j = a + m, m = 0 ..
+    L - 1 - a); causal attention keeps the left part and m = 0."""
+    L, d = 23, 4
+    slopes = np.array([0.05, 0.3, 1.7])
+    H = len(slopes)
+    Q = np.zeros((1, H, L, d))
+    K = _rng(22).standard_normal((1, H, L, d))
+    V = np.zeros((1, H, L, d))
+    V[0, :, :, 0] = np.arange(L)
+    for causal in (False, True):
+        out = orc.attention(orc.MODE_ALIBI, Q, K, V, slopes, causal=causal)
+        for h, s in enumerate(slopes):
+            r = math.exp(-s)
+            for a in range(L):
+                l0, l1 = _geo(r, 1, a)             # sum r^m, sum m r^m, keys left
+                n0, n1 = _geo(r, 0, 0 if causal else L - 1 - a)
+                num = (a * l0 - l1) + (a * n0 + n1)
+                den = l0 + n0
+                assert abs(out[0, h, a, 0] - num / den) < 1e-10, (causal, h, a)
+
+
 ALL_CHECKS = [
     check_t5_golden, check_t5_unused_bucket, check_t5_64_buckets, check_deberta_delta,
     check_shaw_index, check_skew_identity, check_shaw_logits_vs_skew,
     check_shaw_gather_vs_naive, check_deberta_gather_vs_naive, check_zero_tables_are_sdpa,
     check_deberta_constant_tables, check_shaw_constant_tables, check_t5_constant_table,
     check_t5_two_token, check_shaw_sign, check_deberta_sign, check_query_offset_consistency,
+    check_alibi_zero_slopes_are_sdpa, check_alibi_closed_form,
 ]
 
 

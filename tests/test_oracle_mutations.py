@@ -114,6 +114,24 @@ def _mask_off_by_one(logits, p, Lk, causal):
     return logits
 
 
+def _alibi_sign_flipped(q, k, slope_h, p):
+    return _ORIG_ALIBI(q, k, -slope_h, p)
+
+
+def _alibi_no_abs(q, k, slope_h, p):
+    d = q.shape[1]
+    j = np.arange(k.shape[0])
+    return q @ k.T / np.sqrt(d) - slope_h * (j[None, :] - p[:, None])
+
+
+def _alibi_bias_scaled(q, k, slope_h, p):
+    return _ORIG_ALIBI(q, k, slope_h / np.sqrt(q.shape[1]), p)
+
+
+def _alibi_position_off_by_one(q, k, slope_h, p):
+    return _ORIG_ALIBI(q, k, slope_h, p + 1)
+
+
 MUTATIONS = {
     "t5_sign_flipped": ("t5_bucket", _flip_t5(_ORIG_T5)),
     "t5_offset_off_by_one": ("t5_bucket", _shift_t5(_ORIG_T5)),
@@ -130,7 +148,12 @@ MUTATIONS = {
     "shaw_value_dropped": ("shaw_value_term", _shaw_value_dropped),
     "shaw_value_flipped": ("shaw_value_term", _shaw_value_flipped),
     "mask_off_by_one": ("_mask", _mask_off_by_one),
+    "alibi_sign_flipped": ("alibi_logits", _alibi_sign_flipped),
+    "alibi_no_abs": ("alibi_logits", _alibi_no_abs),
+    "alibi_bias_scaled": ("alibi_logits", _alibi_bias_scaled),
+    "alibi_position_off_by_one": ("alibi_logits", _alibi_position_off_by_one),
 }
+_ORIG_ALIBI = orc.alibi_logits
 _ORIG_SHAW_IDX = orc.shaw_index
 _ORIG_DELTA = orc.deberta_delta
 
