@@ -501,7 +501,7 @@ def main():
 
     others = {}
     if not args.no_others and rank == 0:
-        for name in ("t5_causal", "t5_decode", "shaw", "t5_tiny_fp32", "deberta"):
+        for name in ("t5_causal", "t5_decode", "shaw", "t5_tiny_fp32", "deberta", "alibi_bidir", "alibi_causal"):
             if name == w.name:
                 continue
             ow = WORKLOADS[name]

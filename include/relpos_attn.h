@@ -23,6 +23,10 @@
  *                  Formula" for delta).
  *                  logit = (q_i.k_j + q_i.Pk[delta(p, j)] + k_j.Pq[delta(j, p)])
  *                          / sqrt(3d),  delta(a, b) = clip(a - b, -k, k - 1) + k
+ *   RELPOS_ALIBI   a fixed slope per head times the distance, no table and
+ *                  no maximum distance ("Relative Position Embeddings, in
+ *                  depth", section "ALiBi and RoPE: the two endpoints").
+ *                  logit = q.k / sqrt(d) - slope[h] * |j - p|
  *
  * Positions: query row i sits at absolute position p = i + q_offset; key
  * row j at position j. With causal = 1 keys j > p are masked out (and T5
@@ -49,6 +53,7 @@ extern "C" {
 #define RELPOS_T5 0
 #define RELPOS_SHAW 1
 #define RELPOS_DEBERTA 2
+#define RELPOS_ALIBI 3
 
 /* element types of Q, K, V and out */
 #define RELPOS_BF16 0
@@ -66,7 +71,7 @@ extern "C" {
 /*
  * relpos_attn_fwd -- attention forward with an in-kernel relative term.
  *
- *   mode        RELPOS_T5, RELPOS_SHAW or RELPOS_DEBERTA.
+ *   mode        RELPOS_T5, RELPOS_SHAW, RELPOS_DEBERTA or RELPOS_ALIBI.
  *   dtype       RELPOS_BF16 or RELPOS_FP32: element type of Q, K, V and out.
  *               FP32 inputs are rounded to bf16 on the device before the
  *               tensor-core products (fp32 accumulation); out is fp32.
@@ -78,13 +83,16 @@ extern "C" {
  *                          shared by all heads.
  *                 DeBERTa: table0 = Pk, table1 = Pq, each [2k, H, d] bf16
  *                          (already projected per head).
+ *                 ALiBi:   table0 = slopes [H] fp32 (any values the caller
+ *                          chooses); table1 unused.
  *   B, H        batch and heads (>= 0; 0 makes the call a no-op).
  *   Lq, Lk      query and key lengths (Lq >= 0, Lk >= 0). Lk == 0 writes
  *               zeros.
  *   d           head dimension; this build supports d = 64.
- *   num_buckets T5 only: even, 4 <= num_buckets <= 128.
+ *   num_buckets T5 only: even, 4 <= num_buckets <= 128 (ignored otherwise).
  *   rel_param   T5: max_distance (> num_buckets/4 bidirectional, > num_buckets/2
- *               causal); Shaw: clip k (1 <= k <= 64); DeBERTa: k (1 <= k <= 4096).
+ *               causal); Shaw: clip k (1 <= k <= 64); DeBERTa: k (1 <= k <= 4096);
+ *               ALiBi: ignored.
  *               Shaw's per-row tables and T5's bias-by-offset table live in
  *               shared memory: this build runs Shaw k <= 21, and T5 as long as
  *               the distance at which the last bucket starts (about
@@ -118,6 +126,7 @@ int relpos_attn_fwd(int mode, int dtype, const void* Q, const void* K, const voi
  *            head, looked up by bucket"); causal selects the causal mapping.
  *   Shaw:    offsets are key - query; ids are clip(rel, -k, k) + k.
  *   DeBERTa: offsets are query - key; ids are delta = clip(rel, -k, k-1) + k.
+ *   ALiBi:   offsets are key - query; ids are the distances |rel|.
  *   out_dev  device int32[n], written asynchronously on `stream`.
  * Parameter checks are those of relpos_attn_fwd.
  */

@@ -50,3 +50,11 @@ def test_deberta_ids(k, L):
     got = rp.index_ids(rp.MODE_DEBERTA, first, n, rel_param=k)
     ref = orc.index_ids(orc.MODE_DEBERTA, range(first, first + n), rel_param=k)
     assert np.array_equal(got.cpu().numpy().astype(np.int64), ref)
+
+
+@pytest.mark.parametrize("L", [2048, 5])
+def test_alibi_ids(L):
+    first, n = -(L - 1), 2 * L - 1
+    got = rp.index_ids(rp.MODE_ALIBI, first, n)
+    ref = orc.index_ids(orc.MODE_ALIBI, range(first, first + n))
+    assert np.array_equal(got.cpu().numpy().astype(np.int64), ref)

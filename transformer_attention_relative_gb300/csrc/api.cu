@@ -144,7 +144,7 @@ int check_rel_params(int mode, int num_buckets, int rel_param, int causal) {
   } else if (mode == RELPOS_SHAW || mode == RELPOS_DEBERTA) {
     if (rel_param < 1) return RELPOS_ERR_INVALID_ARG;
     if (rel_param > (1 << 24)) return RELPOS_ERR_UNSUPPORTED;
-  } else {
+  } else if (mode != RELPOS_ALIBI) {
     return RELPOS_ERR_INVALID_ARG;
   }
   return RELPOS_OK;
@@ -163,6 +163,8 @@ __global__ void index_ids_kernel(int mode, int n, int first, T5Index ix, int k, 
     id = t5_bucket_dev(rel, ix);
   else if (mode == RELPOS_SHAW)
     id = shaw_index_dev(rel, k);
+  else if (mode == RELPOS_ALIBI)
+    id = rel < 0 ? -rel : rel;
   else
     id = deberta_delta_dev(rel, k);
   out[i] = id;
@@ -272,7 +274,7 @@ extern "C" int relpos_attn_fwd(int mode, int dtype, const void* Q, const void* K
                                const void* table0, const void* table1, int B, int H, int Lq, int Lk,
                                int d, int num_buckets, int rel_param, int causal, int q_offset,
                                void* out, void* stream) {
-  if (mode != RELPOS_T5 && mode != RELPOS_SHAW && mode != RELPOS_DEBERTA)
+  if (mode != RELPOS_T5 && mode != RELPOS_SHAW && mode != RELPOS_DEBERTA && mode != RELPOS_ALIBI)
     return RELPOS_ERR_INVALID_ARG;
   if (dtype != RELPOS_BF16 && dtype != RELPOS_FP32) return RELPOS_ERR_INVALID_ARG;
   if (B < 0 || H < 0 || Lq < 0 || Lk < 0 || q_offset < 0 || d <= 0) return RELPOS_ERR_INVALID_ARG;
@@ -291,7 +293,7 @@ extern "C" int relpos_attn_fwd(int mode, int dtype, const void* Q, const void* K
                                                                                  : RELPOS_ERR_CUDA;
   }
   if (!K || !V || !table0) return RELPOS_ERR_INVALID_ARG;
-  if (mode != RELPOS_T5 && !table1) return RELPOS_ERR_INVALID_ARG;
+  if ((mode == RELPOS_SHAW || mode == RELPOS_DEBERTA) && !table1) return RELPOS_ERR_INVALID_ARG;
   if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(out) || !aligned16(table0) ||
       (table1 && !aligned16(table1)))
     return RELPOS_ERR_INVALID_ARG;
@@ -422,6 +424,8 @@ extern "C" int relpos_attn_fwd(int mode, int dtype, const void* Q, const void* K
     } else if (mode == RELPOS_SHAW) {
       p.aK = static_cast<const __nv_bfloat16*>(table0);
       p.aV = static_cast<const __nv_bfloat16*>(table1);
+    } else if (mode == RELPOS_ALIBI) {
+      p.slopes = static_cast<const float*>(table0);
     }
     // Shaw per-row tables: padded rows when shared memory allows
     p.row_stride = 2 * rel_param + 2;

@@ -600,7 +600,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
 
-    if constexpr (MODE == 2) griddep_wait();
+    if constexpr (MODE >= 2) griddep_wait();
     uint32_t cnt = 0, ocnt = 0;
     uint32_t ccnt = 0;  // split items merged with the other warpgroup
     // With STAG, warpgroup b starts each item once warpgroup a has its
@@ -629,6 +629,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---- per-item relative-term setup
       float add_l = 0.f, add_r = 0.f;
       int buf = 0, next_h = -1;
+      float alibi_k = 0.f;  // ALiBi: this head's slope in raw-score units (slope / scale)
+      if constexpr (MODE == 3) alibi_k = __ldg(p.slopes + it.h) * kLog2e / sl2;
       if constexpr (MODE == 0) {
         // this item's table was filled at the end of the previous item (or in
         // the prologue); fetch the next item's bias row meanwhile
@@ -724,6 +726,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (MODE == 0) {
           far_l = rel_hi <= -p.t5_R;
           far_r = p.t5.bidir && rel_lo >= p.t5_R;
+        } else if constexpr (MODE == 3) {
+          far_l = far_r = false;  // ALiBi never saturates
         } else {
           far_l = rel_hi <= -kc;
           far_r = rel_lo >= kc;
@@ -742,11 +746,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         // 2^(xs * xscale + xoff - m).
         // DeBERTa tiles beyond the band still carry a per-key term, so every
         // DeBERTa tile takes the per-element path.
-        const bool far = MODE != 2 && (far_l || far_r);
+        const bool far = MODE == 3 || (MODE != 2 && (far_l || far_r));
         // a row constant added with the maximum: the far constant of a far
-        // tile, and for DeBERTa tiles beyond the band the saturated c2p term
-        // (their per-key p2c term goes into the scaled scores)
-        const float addc = (far_l || far_r) ? (far_l ? add_l : add_r) : 0.f;
+        // tile, for DeBERTa tiles beyond the band the saturated c2p term
+        // (their per-key p2c term goes into the scaled scores), for ALiBi
+        // tiles on one side of the diagonal the distance term of column 0
+        float addc = (far_l || far_r) ? (far_l ? add_l : add_r) : 0.f;
+        if constexpr (MODE == 3) {
+          // bias = -slope |r0 + c| with r0 = j0 - p the offset of column 0:
+          // keys all ahead, -slope r0 - slope c; all behind, slope r0 + slope c;
+          // a tile across the diagonal takes the whole term per column. The
+          // column part goes into the raw scores in their own units (alibi_k
+          // = slope / scale), which the exponent's FMA then scales.
+          const float r0f = static_cast<float>(j0 - prow);
+          if (rel_lo >= 0 || rel_hi <= 0) {
+            const float sgn = rel_lo >= 0 ? -1.f : 1.f;
+            addc = sgn * alibi_k * sl2 * r0f;
+            const float2 cs2 = make_float2(sgn * alibi_k, sgn * alibi_k);
+#pragma unroll
+            for (int c = 0; c < 128; c += 2) {
+              const float2 a = __ffma2_rn(make_float2(static_cast<float>(c), static_cast<float>(c + 1)), cs2,
+                                          make_float2(xs[c], xs[c + 1]));
+              xs[c] = a.x;
+              xs[c + 1] = a.y;
+            }
+          } else {
+            const float2 nk2 = make_float2(-alibi_k, -alibi_k);
+#pragma unroll
+            for (int c = 0; c < 128; c += 2) {
+              const float2 dist = make_float2(fabsf(r0f + static_cast<float>(c)), fabsf(r0f + static_cast<float>(c + 1)));
+              const float2 a = __ffma2_rn(dist, nk2, make_float2(xs[c], xs[c + 1]));
+              xs[c] = a.x;
+              xs[c + 1] = a.y;
+            }
+          }
+        }
         if (!far) {
           if (MODE == 0 && p.t5_compact) {
             const float* tb = tab.copy(buf, 0) + (j0 - prow + p.t5_tab_off);
@@ -1153,6 +1187,9 @@ cudaError_t launch_fwd(int mode, bool out_f32, const CUtensorMap& tmQ, const CUt
   } else if (mode == 2 && var < 2) {
     kern = out_f32 ? (var ? relpos_fwd_kernel<2, true, 1> : relpos_fwd_kernel<2, true, 0>)
                    : (var ? relpos_fwd_kernel<2, false, 1> : relpos_fwd_kernel<2, false, 0>);
+  } else if (mode == 3 && var < 2) {
+    kern = out_f32 ? (var ? relpos_fwd_kernel<3, true, 1> : relpos_fwd_kernel<3, true, 0>)
+                   : (var ? relpos_fwd_kernel<3, false, 1> : relpos_fwd_kernel<3, false, 0>);
   } else {
     return cudaErrorNotSupported;
   }
@@ -1161,7 +1198,7 @@ cudaError_t launch_fwd(int mode, bool out_f32, const CUtensorMap& tmQ, const CUt
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
   const int slot = mode * 6 + (out_f32 ? 3 : 0) + var;
-  static std::atomic<uint64_t> attr_set[18];
+  static std::atomic<uint64_t> attr_set[24];
   const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
   if (!bit || !(attr_set[slot].load() & bit)) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,

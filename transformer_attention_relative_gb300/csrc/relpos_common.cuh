@@ -62,6 +62,8 @@ struct FwdParams {
   int out_v8;  // out is 32-byte aligned: rows are written with 32-byte stores
   int stagger;  // offset the two softmax warpgroups by about half a tile
   int* status;
+  // ALiBi
+  const float* slopes;  // [H]
   // T5
   const float* bias;  // [num_buckets, H]
   int t5_R;           // |offset| >= R: the side's last bucket (no ordering left)

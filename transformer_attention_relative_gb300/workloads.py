@@ -8,13 +8,15 @@ Recipe (one per workload): a CPU ``torch.Generator`` seeded with
 ``1000 + index``; draws in the order Q, K, V, table0, table1; ``randn``
 scaled by the workload's sigma; then a cast to the kernel's input dtype
 (bf16, or fp32 for the tiny fp32 case). The T5 bias table stays fp32 in
-every workload; the Shaw and DeBERTa tables are bf16.
+every workload; the Shaw and DeBERTa tables are bf16. ALiBi has no drawn
+table: its per-head slopes (fp32) are the geometric sequence 2^(-8(h+1)/H)
+commonly used with it (the pages fix no values).
 
 Shapes and distributions follow the five workloads the relative-position
 attention pages motivate: a tiny fp32 T5 encoder case, a T5-base-shaped
 encoder, a T5 causal decoder plus its cached-decode step, Shaw clipped
 relative keys/values at L=4096, and DeBERTa disentangled attention at
-k=256.
+k=256; plus ALiBi at the T5-base and T5-causal shapes.
 """
 from __future__ import annotations
 
@@ -22,8 +24,8 @@ import dataclasses
 
 import torch
 
-MODE_T5, MODE_SHAW, MODE_DEBERTA = 0, 1, 2
-MODE_NAMES = {MODE_T5: "t5", MODE_SHAW: "shaw", MODE_DEBERTA: "deberta"}
+MODE_T5, MODE_SHAW, MODE_DEBERTA, MODE_ALIBI = 0, 1, 2, 3
+MODE_NAMES = {MODE_T5: "t5", MODE_SHAW: "shaw", MODE_DEBERTA: "deberta", MODE_ALIBI: "alibi"}
 
 
 @dataclasses.dataclass(frozen=True)
@@ -58,6 +60,8 @@ class Workload:
         if self.mode == MODE_SHAW:
             n = 2 * self.rel_param + 1
             return (n, self.d), (n, self.d)
+        if self.mode == MODE_ALIBI:
+            return (self.H,), None
         n = 2 * self.rel_param
         return (n, self.H, self.d), (n, self.H, self.d)
 
@@ -91,7 +95,7 @@ class Workload:
         n = self.B * self.H * self.d * esz
         b = n * (2 * self.Lq + 2 * self.Lk)
         t0, t1 = self.table_shapes()
-        for shp, tsz in ((t0, 4 if self.mode == MODE_T5 else 2), (t1, 2)):
+        for shp, tsz in ((t0, 4 if self.mode in (MODE_T5, MODE_ALIBI) else 2), (t1, 2)):
             if shp is not None:
                 c = 1
                 for s in shp:
@@ -114,6 +118,9 @@ WORKLOADS = {
                      rel_param=16, table_sigma=0.1),
     "deberta": Workload("deberta", 4, MODE_DEBERTA, "bf16", 8, 12, 2048, 2048, 64,
                         rel_param=256, table_sigma=0.1),
+    "alibi_bidir": Workload("alibi_bidir", 5, MODE_ALIBI, "bf16", 8, 12, 512, 512, 64),
+    "alibi_causal": Workload("alibi_causal", 6, MODE_ALIBI, "bf16", 4, 16, 2048, 2048, 64,
+                             causal=True),
 }
 
 
@@ -126,7 +133,8 @@ def make_inputs(w: Workload, seed: int | None = None):
 
     Returns a dict with Q, K, V ([B,H,Lq|Lk,d], the workload dtype) and
     table0 / table1 (T5: fp32 bias [num_buckets, H], table1 None; Shaw:
-    bf16 a_K, a_V [2k+1, d]; DeBERTa: bf16 Pk, Pq [2k, H, d]).
+    bf16 a_K, a_V [2k+1, d]; DeBERTa: bf16 Pk, Pq [2k, H, d]; ALiBi: fp32
+    slopes [H], table1 None).
     """
     g = torch.Generator(device="cpu")
     g.manual_seed(w.seed if seed is None else seed)
@@ -142,6 +150,9 @@ def make_inputs(w: Workload, seed: int | None = None):
     k = draw((w.B, w.H, w.Lk, w.d), w.qkv_sigma, dt)
     v = draw((w.B, w.H, w.Lk, w.d), w.qkv_sigma, dt)
     s0, s1 = w.table_shapes()
+    if w.mode == MODE_ALIBI:
+        t0 = torch.tensor([2.0 ** (-8.0 * (h + 1) / w.H) for h in range(w.H)], dtype=torch.float32)
+        return {"Q": q, "K": k, "V": v, "table0": t0, "table1": None}
     tdt0 = torch.float32 if w.mode == MODE_T5 else torch.bfloat16
     t0 = draw(s0, w.table_sigma, tdt0)
     t1 = draw(s1, w.table_sigma, torch.bfloat16) if s1 is not None else None
