@@ -318,6 +318,38 @@ def attention(mode: int, Q, K, V, table0, table1=None, *, num_buckets: int = 32,
     return out
 
 
+def t5_attention_key_positions(Q, K, V, bias, key_pos, *, num_buckets: int = 32,
+                               max_distance: int = 128, causal: bool = False,
+                               q_offset: int = 0) -> np.ndarray:
+    """T5-bias attention over keys at explicit positions, in fp64.
+
+    [RPE] "Kernels and the KV cache": with a bias that depends only on the
+    offset, a cache that evicts middle tokens needs nothing rewritten; each
+    kept key keeps its original position. R12: ``key_pos`` [B, H, Lk] holds
+    those positions; query row i is at q_offset + i; the offset is key
+    position minus query position, and causal masking drops keys whose
+    position lies after the query's.
+    """
+    Q = np.asarray(Q, dtype=np.float64)
+    K = np.asarray(K, dtype=np.float64)
+    V = np.asarray(V, dtype=np.float64)
+    bias = np.asarray(bias, dtype=np.float64)
+    key_pos = np.asarray(key_pos, dtype=np.int64)
+    B, H, Lq, d = Q.shape
+    p = np.arange(Lq) + q_offset
+    out = np.zeros((B, H, Lq, d))
+    for b in range(B):
+        for h in range(H):
+            rel = key_pos[b, h][None, :] - p[:, None]
+            ids = np.array([[t5_bucket(int(r), not causal, num_buckets, max_distance) for r in row]
+                            for row in rel], dtype=np.int64).reshape(rel.shape)
+            lg = Q[b, h] @ K[b, h].T / math.sqrt(d) + bias[ids, h]
+            if causal:
+                lg = np.where(rel > 0, -np.inf, lg)
+            out[b, h] = _softmax_rows(lg) @ V[b, h]
+    return out
+
+
 def shaw_naive(Q, K, V, aK, aV, kclip, causal=False, q_offset=0) -> np.ndarray:
     """Shaw attention with the full L x L x d relative tensors built.
 

@@ -430,6 +430,59 @@ def check_alibi_closed_form():
                 assert abs(out[0, h, a, 0] - num / den) < 1e-10, (causal, h, a)
 
 
+# ------------------------------------------------- explicit key positions
+
+def check_key_positions_contiguous():
+    """Keys at positions 0 .. Lk-1 are the plain T5 computation."""
+    rng = _rng(31)
+    B, H, d, Lk = 1, 2, 16, 40
+    for causal, qoff, Lq in ((False, 0, 40), (True, 0, 40), (True, 37, 3)):
+        Q, K, V = (rng.standard_normal((B, H, n, d)) for n in (Lq, Lk, Lk))
+        bias = rng.standard_normal((32, H))
+        kp = np.broadcast_to(np.arange(Lk), (B, H, Lk))
+        a = orc.t5_attention_key_positions(Q, K, V, bias, kp, causal=causal, q_offset=qoff)
+        b = orc.attention(orc.MODE_T5, Q, K, V, bias, causal=causal, q_offset=qoff)
+        assert np.max(np.abs(a - b)) < 1e-12, causal
+
+
+def check_key_positions_eviction():
+    """A cache that evicted some keys, each kept key at its original position,
+    gives the full cache's result with the evicted keys masked: masking is
+    done here by making those keys' scores -1e6 (their weight underflows to
+    zero in fp64) and running the plain computation over the full cache."""
+    rng = _rng(32)
+    d, L = 16, 300
+    keep = np.sort(rng.choice(L - 1, 60, replace=False))
+    keep = np.append(keep, L - 1)  # the newest key stays
+    for causal in (False, True):
+        q = rng.standard_normal((1, 1, 1, d))
+        Kf, Vf = rng.standard_normal((1, 1, L, d)), rng.standard_normal((1, 1, L, d))
+        bias = rng.standard_normal((32, 1)) * 2
+        Km = Kf.copy()
+        gone = np.setdiff1d(np.arange(L), keep)
+        qv = q[0, 0, 0]
+        Km[0, 0, gone] = -1e6 * math.sqrt(d) * qv / (qv @ qv)
+        full = orc.attention(orc.MODE_T5, q, Km, Vf, bias, causal=causal, q_offset=L - 1)
+        kp = keep[None, None, :]
+        part = orc.t5_attention_key_positions(q, Kf[:, :, keep], Vf[:, :, keep], bias, kp,
+                                              causal=causal, q_offset=L - 1)
+        assert np.max(np.abs(part - full)) < 1e-10, causal
+
+
+def check_key_positions_shift():
+    """[RPE] failure modes: shifting every position by a constant leaves an
+    offset-only bias unchanged (query offset and key positions together)."""
+    rng = _rng(33)
+    B, H, d, Lq, Lk = 1, 2, 16, 5, 30
+    Q, K, V = (rng.standard_normal((B, H, n, d)) for n in (Lq, Lk, Lk))
+    bias = rng.standard_normal((32, H)) * 2
+    kp = np.sort(rng.choice(200, Lk, replace=False))[None, None, :].repeat(H, axis=1)
+    for causal in (False, True):
+        a = orc.t5_attention_key_positions(Q, K, V, bias, kp, causal=causal, q_offset=150)
+        b = orc.t5_attention_key_positions(Q, K, V, bias, kp + 1000, causal=causal, q_offset=1150)
+        assert np.max(np.abs(a - b)) < 1e-12
+
+
 ALL_CHECKS = [
     check_t5_golden, check_t5_unused_bucket, check_t5_64_buckets, check_deberta_delta,
     check_shaw_index, check_skew_identity, check_shaw_logits_vs_skew,
@@ -437,6 +490,7 @@ ALL_CHECKS = [
     check_deberta_constant_tables, check_shaw_constant_tables, check_t5_constant_table,
     check_t5_two_token, check_shaw_sign, check_deberta_sign, check_query_offset_consistency,
     check_alibi_zero_slopes_are_sdpa, check_alibi_closed_form,
+    check_key_positions_contiguous, check_key_positions_eviction, check_key_positions_shift,
 ]
 
 

@@ -132,6 +132,18 @@ def _alibi_position_off_by_one(q, k, slope_h, p):
     return _ORIG_ALIBI(q, k, slope_h, p + 1)
 
 
+def _kpos_index_not_position(Q, K, V, bias, key_pos, **kw):
+    Lk = np.asarray(K).shape[2]
+    kp = np.broadcast_to(np.arange(Lk), np.asarray(key_pos).shape)
+    return _ORIG_KPOS(Q, K, V, bias, kp, **kw)
+
+
+def _kpos_no_query_offset(Q, K, V, bias, key_pos, **kw):
+    kw = dict(kw)
+    kw["q_offset"] = 0
+    return _ORIG_KPOS(Q, K, V, bias, key_pos, **kw)
+
+
 MUTATIONS = {
     "t5_sign_flipped": ("t5_bucket", _flip_t5(_ORIG_T5)),
     "t5_offset_off_by_one": ("t5_bucket", _shift_t5(_ORIG_T5)),
@@ -152,7 +164,10 @@ MUTATIONS = {
     "alibi_no_abs": ("alibi_logits", _alibi_no_abs),
     "alibi_bias_scaled": ("alibi_logits", _alibi_bias_scaled),
     "alibi_position_off_by_one": ("alibi_logits", _alibi_position_off_by_one),
+    "kpos_index_not_position": ("t5_attention_key_positions", _kpos_index_not_position),
+    "kpos_no_query_offset": ("t5_attention_key_positions", _kpos_no_query_offset),
 }
+_ORIG_KPOS = orc.t5_attention_key_positions
 _ORIG_ALIBI = orc.alibi_logits
 _ORIG_SHAW_IDX = orc.shaw_index
 _ORIG_DELTA = orc.deberta_delta
