@@ -192,6 +192,14 @@ class GpuRun:
     def _call(self, d, out=None):
         w = self.w
         p = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())  # noqa: E731
+        if w.cache_len:  # keys at explicit positions
+            rc = self.rp.relpos_t5_decode_positions(
+                p(d["Q"]), p(d["K"]), p(d["V"]), p(d["table0"]), p(d["key_pos"]), w.B, w.H, w.Lq,
+                w.Lk, w.num_buckets, w.rel_param, int(w.causal), w.q_offset,
+                p(out if out is not None else d["out"]), self.sptr)
+            if rc != 0:
+                raise RuntimeError(f"relpos_t5_decode_positions failed: {rc}")
+            return
         rc = self.rp.relpos_attn_fwd(w.mode, self.dtype, p(d["Q"]), p(d["K"]), p(d["V"]),
                                      p(d["table0"]), p(d["table1"]), w.B, w.H, w.Lq, w.Lk, w.d,
                                      w.num_buckets, w.rel_param, int(w.causal), w.q_offset,
@@ -343,8 +351,15 @@ def cpu_baseline(w, budget_s=12.0):
     done = 0
     n_rows_total = 0
     for (b, h) in heads:
-        orc.attention(w.mode, Q, K, V, t0, t1, num_buckets=w.num_buckets, rel_param=w.rel_param,
-                      causal=w.causal, q_offset=w.q_offset, rows=rows, heads=[(b, h)])
+        if w.cache_len:
+            kp = x["key_pos"].numpy()
+            orc.t5_attention_key_positions(Q[b:b + 1, h:h + 1], K[b:b + 1, h:h + 1], V[b:b + 1, h:h + 1],
+                                           t0[:, h:h + 1], kp[b:b + 1, h:h + 1],
+                                           num_buckets=w.num_buckets, max_distance=w.rel_param,
+                                           causal=w.causal, q_offset=w.q_offset)
+        else:
+            orc.attention(w.mode, Q, K, V, t0, t1, num_buckets=w.num_buckets, rel_param=w.rel_param,
+                          causal=w.causal, q_offset=w.q_offset, rows=rows, heads=[(b, h)])
         done += 1
         n_rows_total += w.Lq if rows is None else len(rows)
         if time.perf_counter() - start > budget_s:
@@ -501,7 +516,8 @@ def main():
 
     others = {}
     if not args.no_others and rank == 0:
-        for name in ("t5_causal", "t5_decode", "shaw", "t5_tiny_fp32", "deberta", "alibi_bidir", "alibi_causal"):
+        for name in ("t5_causal", "t5_decode", "t5_decode_evicted", "shaw", "t5_tiny_fp32", "deberta",
+                     "alibi_bidir", "alibi_causal"):
             if name == w.name:
                 continue
             ow = WORKLOADS[name]

@@ -185,6 +185,29 @@ int relpos_t5_decode_noalloc(const void* Q, const void* K, const void* V, const 
                              int H, int Lq, int Lk, int num_buckets, int max_distance, int causal,
                              int q_offset, void* out, void* stream);
 
+/*
+ * relpos_t5_decode_positions -- T5-bias cached decoding over keys at explicit
+ * positions: a cache that evicted tokens keeps each remaining key at its
+ * original position, and since the bias depends only on the offset nothing
+ * stored needs rewriting ("Relative Position Embeddings, in depth", section
+ * "Kernels and the KV cache").
+ *
+ *   key_pos     device, int32 [B, H, Lk]: the position of each key row, in
+ *               any order, each in [0, 2^28]. The offset of key j to query
+ *               row i is key_pos[b, h, j] - (i + q_offset); with causal = 1 a
+ *               key whose position lies after the query's is masked out. A
+ *               query row with no visible key gets a zero row.
+ *   Q, K, V, bias, out, B, H, Lq, Lk, num_buckets, max_distance, causal,
+ *   q_offset, stream: as for relpos_attn_fwd with mode RELPOS_T5 and dtype
+ *   RELPOS_BF16 (d = 64); Lq must be <= 8 (RELPOS_ERR_UNSUPPORTED otherwise).
+ * Scratch: the per-chunk partials (B * H * Lq * ceil(Lk / 256) * 264 bytes)
+ * come from cudaMallocAsync on `stream` and go back with cudaFreeAsync before
+ * the call returns. Asynchronous on `stream`.
+ */
+int relpos_t5_decode_positions(const void* Q, const void* K, const void* V, const void* bias,
+                               const int* key_pos, int B, int H, int Lq, int Lk, int num_buckets,
+                               int max_distance, int causal, int q_offset, void* out, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -27,7 +27,7 @@ RELPOS_ERR_DEVICE_TIMEOUT = -4
 RELPOS_ERR_SCRATCH_LIMIT = -5
 
 EXPORTED = ("relpos_attn_fwd", "relpos_index_ids", "relpos_check_status", "relpos_strerror",
-            "relpos_selftest_wait_timeout", "relpos_t5_decode_noalloc")
+            "relpos_selftest_wait_timeout", "relpos_t5_decode_noalloc", "relpos_t5_decode_positions")
 
 _lib = None
 
@@ -60,6 +60,8 @@ def load_library(path: str = LIB_PATH):
     lib.relpos_selftest_wait_timeout.restype = i
     lib.relpos_t5_decode_noalloc.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, i, vp, vp]
     lib.relpos_t5_decode_noalloc.restype = i
+    lib.relpos_t5_decode_positions.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, vp, vp]
+    lib.relpos_t5_decode_positions.restype = i
     _lib = lib
     return lib
 
@@ -96,6 +98,14 @@ def relpos_t5_decode_noalloc(Q, K, V, bias, B, H, Lq, Lk, num_buckets, max_dista
     header for the size limit and the rule that overlapping calls race)."""
     return load_library().relpos_t5_decode_noalloc(Q, K, V, bias, B, H, Lq, Lk, num_buckets,
                                                    max_distance, causal, q_offset, out, stream)
+
+
+def relpos_t5_decode_positions(Q, K, V, bias, key_pos, B, H, Lq, Lk, num_buckets, max_distance,
+                               causal, q_offset, out, stream) -> int:
+    """T5 cached decode over keys at explicit positions (an evicted cache)."""
+    return load_library().relpos_t5_decode_positions(Q, K, V, bias, key_pos, B, H, Lq, Lk,
+                                                     num_buckets, max_distance, causal, q_offset,
+                                                     out, stream)
 
 
 strerror = relpos_strerror
@@ -159,3 +169,28 @@ def index_ids(mode: int, rel_first: int, n: int, *, num_buckets: int = 32, rel_p
 def check_status(stream=None) -> int:
     """Synchronise and return the library's device status code (0 = ok)."""
     return relpos_check_status(_stream(stream))
+
+
+def t5_decode_positions(Q, K, V, bias, key_pos, *, num_buckets: int = 32, max_distance: int = 128,
+                        causal: bool = True, q_offset: int = 0, out=None, stream=None):
+    """Run ``relpos_t5_decode_positions`` on CUDA tensors; returns ``out``.
+
+    Q [B,H,Lq,64] (Lq <= 8), K, V [B,H,Lk,64] bf16; bias [num_buckets, H]
+    fp32; key_pos [B,H,Lk] int32 positions of the kept keys.
+    """
+    import torch
+    B, H, Lq, _ = Q.shape
+    Lk = K.shape[2]
+    for t in (Q, K, V, bias, key_pos, out):
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("tensors must be contiguous CUDA tensors")
+    if key_pos.dtype != torch.int32:
+        raise TypeError("key_pos must be int32")
+    if out is None:
+        out = torch.empty_like(Q)
+    rc = relpos_t5_decode_positions(_ptr(Q), _ptr(K), _ptr(V), _ptr(bias), _ptr(key_pos), B, H, Lq,
+                                    Lk, num_buckets, max_distance, int(causal), q_offset, _ptr(out),
+                                    _stream(stream))
+    if rc != RELPOS_OK:
+        raise RelposError(rc, "relpos_t5_decode_positions")
+    return out

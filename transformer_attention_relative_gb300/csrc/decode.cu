@@ -57,8 +57,11 @@ __global__ void __launch_bounds__(kDecThreads, 3) relpos_decode_partial_kernel(c
   griddep_wait();  // the previous kernel of the stream has completed
   const int pos = qi + p.q_offset;
   const int jb = chunk * kDecChunk;
+  // explicit key positions (a cache that evicted keys): visibility follows
+  // the positions, not the key index
+  const int* kpos = p.key_pos ? p.key_pos + static_cast<size_t>(bh) * p.Lk : nullptr;
   int je = min(p.Lk, jb + kDecChunk);
-  if (p.causal) je = min(je, pos + 1);
+  if (p.causal && !kpos) je = min(je, pos + 1);
 
   const size_t row_out = static_cast<size_t>(bh) * p.Lq + qi;
   float* po = p.part_o + (row_out * p.nchunks + chunk) * kHeadDim;
@@ -78,11 +81,21 @@ __global__ void __launch_bounds__(kDecThreads, 3) relpos_decode_partial_kernel(c
   // lying wholly beyond R needs one bias; otherwise each key's bias is looked
   // up once here rather than by every thread that shares the key.
   const int rel_first = jb - pos, rel_last = je - 1 - pos;
-  const bool sat_l = rel_last <= -p.t5_R;
-  const bool sat_r = p.t5.bidir && rel_first >= p.t5_R;
+  const bool sat_l = !kpos && rel_last <= -p.t5_R;
+  const bool sat_r = !kpos && p.t5.bidir && rel_first >= p.t5_R;
   float bias_const = 0.f;
   if (sat_l || sat_r) {
     bias_const = __ldg(p.bias + t5_bucket_dev(sat_l ? -p.t5_R : p.t5_R, p.t5) * p.H + h) * kLog2e;
+  } else if (kpos) {
+    // per key: the bias of its own offset, -inf for a key after the query
+    for (int r = tid; r < kDecChunk; r += kDecThreads) {
+      float b = -INFINITY;
+      if (jb + r < je) {
+        const int rel = __ldg(kpos + jb + r) - pos;
+        if (!p.causal || rel <= 0) b = __ldg(p.bias + t5_bucket_dev(rel, p.t5) * p.H + h) * kLog2e;
+      }
+      bias_s[r] = b;
+    }
   } else {
     for (int r = tid; r < kDecChunk; r += kDecThreads)
       bias_s[r] = __ldg(p.bias + t5_bucket_dev(jb + r - pos, p.t5) * p.H + h) * kLog2e;
@@ -135,6 +148,14 @@ __global__ void __launch_bounds__(kDecThreads, 3) relpos_decode_partial_kernel(c
   __syncthreads();
   mx = fmaxf(fmaxf(red_s[0], red_s[1]), fmaxf(red_s[2], red_s[3]));
   __syncthreads();
+  if (mx == -INFINITY) {  // every key of the chunk masked by its position
+    if (tid < kHeadDim) po[tid] = 0.f;
+    if (tid == 0) {
+      pml[0] = -INFINITY;
+      pml[1] = 0.f;
+    }
+    return;
+  }
 
   float sum = 0.f;
   float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -315,4 +336,75 @@ extern "C" int relpos_t5_decode_noalloc(const void* Q, const void* K, const void
   dp.t5 = t5;
   dp.t5_R = R;
   return launch_decode(dp, s) == cudaSuccess ? RELPOS_OK : RELPOS_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------------------
+// Decode over keys at explicit positions: a cache that evicted tokens keeps
+// each remaining key at its original position, and an offset-only bias needs
+// nothing rewritten ("Relative Position Embeddings, in depth", section
+// "Kernels and the KV cache"). Same split-key kernels, with each key's offset
+// and causal visibility taken from key_pos.
+
+extern "C" int relpos_t5_decode_positions(const void* Q, const void* K, const void* V,
+                                          const void* bias, const int* key_pos, int B, int H,
+                                          int Lq, int Lk, int num_buckets, int max_distance,
+                                          int causal, int q_offset, void* out, void* stream) {
+  using namespace relpos;
+  int rc = check_rel_params(RELPOS_T5, num_buckets, max_distance, causal);
+  if (rc != RELPOS_OK) return rc;
+  if (B < 0 || H < 0 || Lq < 0 || Lk < 0 || q_offset < 0) return RELPOS_ERR_INVALID_ARG;
+  if (Lq > 8) return RELPOS_ERR_UNSUPPORTED;  // decode shapes only
+  if (B == 0 || H == 0 || Lq == 0) return RELPOS_OK;
+  if (static_cast<long long>(B) * H > 65535 || Lk > (1 << 24) || q_offset > (1 << 28))
+    return RELPOS_ERR_UNSUPPORTED;
+  if (!Q || !out) return RELPOS_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t rows = static_cast<size_t>(B) * H * Lq;
+  if (Lk == 0)
+    return cudaMemsetAsync(out, 0, rows * kHeadDim * 2, s) == cudaSuccess ? RELPOS_OK
+                                                                           : RELPOS_ERR_CUDA;
+  if (!K || !V || !bias || !key_pos) return RELPOS_ERR_INVALID_ARG;
+
+  // thresholds for every offset a position in [0, 2^28] can produce
+  T5Index t5;
+  int R = 0;
+  rc = t5_setup(num_buckets, max_distance, causal, (1ll << 28) + 8, &t5, &R);
+  if (rc != RELPOS_OK) return rc;
+
+  const int chunk = decode_chunk_keys();
+  const int nchunks = (Lk + chunk - 1) / chunk;
+  float* scratch = nullptr;
+  if (cudaMallocAsync(&scratch, rows * nchunks * (kHeadDim + 2) * sizeof(float), s) != cudaSuccess) {
+    cudaGetLastError();
+    return RELPOS_ERR_CUDA;
+  }
+  DecodeParams dp;
+  std::memset(&dp, 0, sizeof(dp));
+  dp.Q = static_cast<const __nv_bfloat16*>(Q);
+  dp.K = static_cast<const __nv_bfloat16*>(K);
+  dp.V = static_cast<const __nv_bfloat16*>(V);
+  dp.bias = static_cast<const float*>(bias);
+  dp.B = B;
+  dp.H = H;
+  dp.Lq = Lq;
+  dp.Lk = Lk;
+  dp.causal = causal;
+  dp.q_offset = q_offset;
+  dp.scale_log2 = (1.0f / std::sqrt(static_cast<float>(kHeadDim))) * kLog2e;
+  dp.chunk = chunk;
+  dp.nchunks = nchunks;
+  dp.part_o = scratch;
+  dp.part_ml = scratch + rows * nchunks * kHeadDim;
+  dp.out = out;
+  dp.out_f32 = 0;
+  dp.t5 = t5;
+  dp.t5_R = R;
+  dp.key_pos = key_pos;
+  const bool ok = launch_decode(dp, s) == cudaSuccess;
+  const bool freed = cudaFreeAsync(scratch, s) == cudaSuccess;
+  if (!ok || !freed) {
+    cudaGetLastError();
+    return RELPOS_ERR_CUDA;
+  }
+  return RELPOS_OK;
 }

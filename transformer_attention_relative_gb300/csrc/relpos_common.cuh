@@ -127,6 +127,7 @@ struct DecodeParams {
   int out_f32;
   int t5_R;  // |offset| >= R: the side's last bucket
   T5Index t5;
+  const int* key_pos;  // [B*H, Lk] explicit key positions, or null (key j at position j)
 };
 
 }  // namespace relpos

@@ -14,7 +14,8 @@ commonly used with it (the pages fix no values).
 
 Shapes and distributions follow the five workloads the relative-position
 attention pages motivate: a tiny fp32 T5 encoder case, a T5-base-shaped
-encoder, a T5 causal decoder plus its cached-decode step, Shaw clipped
+encoder, a T5 causal decoder plus its cached-decode step (also over a cache
+that evicted half its tokens, keys at explicit positions), Shaw clipped
 relative keys/values at L=4096, and DeBERTa disentangled attention at
 k=256; plus ALiBi at the T5-base and T5-causal shapes.
 """
@@ -45,6 +46,7 @@ class Workload:
     q_offset: int = 0
     qkv_sigma: float = 1.0
     table_sigma: float = 0.0
+    cache_len: int = 0    # > 0: the Lk keys sit at distinct positions of a cache of this length
 
     @property
     def seed(self) -> int:
@@ -94,6 +96,8 @@ class Workload:
         esz = 4 if self.dtype == "fp32" else 2
         n = self.B * self.H * self.d * esz
         b = n * (2 * self.Lq + 2 * self.Lk)
+        if self.cache_len:
+            b += self.B * self.H * self.Lk * 4  # key positions
         t0, t1 = self.table_shapes()
         for shp, tsz in ((t0, 4 if self.mode in (MODE_T5, MODE_ALIBI) else 2), (t1, 2)):
             if shp is not None:
@@ -118,6 +122,9 @@ WORKLOADS = {
                      rel_param=16, table_sigma=0.1),
     "deberta": Workload("deberta", 4, MODE_DEBERTA, "bf16", 8, 12, 2048, 2048, 64,
                         rel_param=256, table_sigma=0.1),
+    "t5_decode_evicted": Workload("t5_decode_evicted", 7, MODE_T5, "bf16", 32, 16, 1, 2048, 64,
+                                  num_buckets=32, rel_param=128, causal=True, q_offset=4095,
+                                  table_sigma=0.5, cache_len=4096),
     "alibi_bidir": Workload("alibi_bidir", 5, MODE_ALIBI, "bf16", 8, 12, 512, 512, 64),
     "alibi_causal": Workload("alibi_causal", 6, MODE_ALIBI, "bf16", 4, 16, 2048, 2048, 64,
                              causal=True),
@@ -156,4 +163,15 @@ def make_inputs(w: Workload, seed: int | None = None):
     tdt0 = torch.float32 if w.mode == MODE_T5 else torch.bfloat16
     t0 = draw(s0, w.table_sigma, tdt0)
     t1 = draw(s1, w.table_sigma, torch.bfloat16) if s1 is not None else None
-    return {"Q": q, "K": k, "V": v, "table0": t0, "table1": t1}
+    x = {"Q": q, "K": k, "V": v, "table0": t0, "table1": t1}
+    if w.cache_len:
+        # a cache that kept Lk of its cache_len tokens, always the newest one,
+        # each (batch, head) its own choice, in position order
+        kp = torch.empty(w.B, w.H, w.Lk, dtype=torch.int32)
+        for b in range(w.B):
+            for h in range(w.H):
+                keep = torch.randperm(w.cache_len - 1, generator=g)[:w.Lk - 1].sort().values
+                kp[b, h, :-1] = keep.to(torch.int32)
+                kp[b, h, -1] = w.cache_len - 1
+        x["key_pos"] = kp
+    return x
