@@ -31,7 +31,7 @@ Conventions (readings where the pages leave a step open are marked R#):
   formula).
 * Scale: 1/sqrt(d) for T5 (R1: added bias after scaling) and Shaw (R7:
   the a_K term is inside the scaled dot product); 1/sqrt(3d) for DeBERTa
-  ([RPE] DeBERTa: three summed terms); ALiBi as T5 (R11: the bias
+  ([RPE] DeBERTa: three summed terms); ALiBi as T5 (R15: the bias
   -slope_h * |j - p| is added after scaling; the slopes are an input, one
   per head, since the pages fix no values).
 * Causal: keys with j > p are masked (-inf) before the softmax; a row with
@@ -262,7 +262,7 @@ def alibi_logits(q, k, slope_h, p):
 
     [RPE] "ALiBi and RoPE: the two endpoints": the T5 bias with the table
     removed, a fixed slope per head times the distance and no maximum
-    distance (R11). With causal masking only keys j <= p_i remain, whose
+    distance (R15). With causal masking only keys j <= p_i remain, whose
     distance is p_i - j.
     """
     d = q.shape[1]
