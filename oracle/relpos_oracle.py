@@ -325,7 +325,7 @@ def t5_attention_key_positions(Q, K, V, bias, key_pos, *, num_buckets: int = 32,
 
     [RPE] "Kernels and the KV cache": with a bias that depends only on the
     offset, a cache that evicts middle tokens needs nothing rewritten; each
-    kept key keeps its original position. R12: ``key_pos`` [B, H, Lk] holds
+    kept key keeps its original position. R16: ``key_pos`` [B, H, Lk] holds
     those positions; query row i is at q_offset + i; the offset is key
     position minus query position, and causal masking drops keys whose
     position lies after the query's.
