@@ -33,6 +33,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -61,15 +62,24 @@ def load_peaks():
     return FALLBACK_PEAKS, "fallback"
 
 
+def _code_only(text):
+    """C/C++ source without its comments and blank lines: what the compiler
+    sees (the sources hold no string literal with comment markers)."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def source_hash():
-    """Hash of the CUDA sources, to tell whether stored ncu counters are current."""
+    """Hash of the CUDA sources' code (comments excluded), to tell whether
+    stored ncu counters were taken on the code that runs."""
     csrc = os.path.join(ROOT, "transformer_attention_relative_gb300", "csrc")
     h = hashlib.sha256()
     for f in sorted(os.listdir(csrc)):
         if f.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, f), "rb") as fh:
+            with open(os.path.join(csrc, f), encoding="utf-8") as fh:
                 h.update(f.encode())
-                h.update(fh.read())
+                h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

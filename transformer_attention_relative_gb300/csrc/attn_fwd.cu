@@ -29,7 +29,13 @@
 // depend on the offset only, so a tile whose offsets all lie beyond the
 // saturation distance needs one constant (T5) or one per-row constant (Shaw)
 // instead of per-element lookups; the per-element T5 bias comes from a
-// bias-by-offset table in shared memory, read four values per load.
+// bias-by-offset table in shared memory, read four values per load. DeBERTa
+// ("DeBERTa: disentangled content and position") reads, for tiles inside the
+// band, the c2p + p2c values its pre-pass wrote per query row and key offset
+// (16-byte aligned windows), and beyond the band one saturated c2p value per
+// row plus one saturated p2c value per key. ALiBi ("ALiBi and RoPE: the two
+// endpoints") needs no table: the slope times the distance is a row constant
+// plus a per-column term, exact per column across the diagonal.
 //
 // Softmax runs in the log2 domain with a lazily updated running maximum: the
 // O accumulator in TMEM is rescaled only when a row's maximum grows by more
