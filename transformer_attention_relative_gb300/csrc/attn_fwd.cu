@@ -698,6 +698,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float* cc = p.c2p_const + static_cast<size_t>(it.bh) * 2 * p.const_pitch + rowc;
         add_l = cc[0];
         add_r = cc[p.const_pitch];
+        // bring this row's windows of the item's band tiles (the pre-pass
+        // wrote the array well before: DRAM) into L2 ahead of their loads
+        for (int j = 0; j < n_kv; ++j) {
+          const int j0 = (lo_x + j) * kBN;
+          if (j0 + kBN - 1 - p_lo <= -kc || j0 - (p_lo + kBM - 1) >= kc) continue;  // beyond the band
+          const char* wnd = reinterpret_cast<const char*>(band_row + (band_sh + j0 - prow + kc));
+          prefetch_l2(wnd);
+          prefetch_l2(wnd + 128);
+          prefetch_l2(wnd + 255);
+        }
       }
       float mass_l = 0.f, mass_r = 0.f;
 
