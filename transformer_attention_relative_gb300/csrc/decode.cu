@@ -76,6 +76,17 @@ __global__ void __launch_bounds__(kDecThreads, 3) relpos_decode_partial_kernel(c
     return;
   }
 
+  // start the chunk's K and V rows towards L2 now: the bias setup below (for
+  // explicit positions a dependent position load, bucket and gather per key)
+  // then overlaps their DRAM latency, and no register is held meanwhile
+  {
+    const char* kr = reinterpret_cast<const char*>(p.K + (static_cast<size_t>(bh) * p.Lk + jb) * kHeadDim);
+    const char* vr = reinterpret_cast<const char*>(p.V + (static_cast<size_t>(bh) * p.Lk + jb) * kHeadDim);
+    for (int r = tid; r < je - jb; r += kDecThreads) {
+      prefetch_l2(kr + static_cast<size_t>(r) * kHeadDim * 2);
+      prefetch_l2(vr + static_cast<size_t>(r) * kHeadDim * 2);
+    }
+  }
   // The chunk's offsets run from jb - pos to je - 1 - pos. Past the saturation
   // distance R every key of a side takes that side's last bucket, so a chunk
   // lying wholly beyond R needs one bias; otherwise each key's bias is looked
