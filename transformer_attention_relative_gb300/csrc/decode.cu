@@ -98,15 +98,20 @@ __global__ void __launch_bounds__(kDecThreads, 3) relpos_decode_partial_kernel(c
   if (sat_l || sat_r) {
     bias_const = __ldg(p.bias + t5_bucket_dev(sat_l ? -p.t5_R : p.t5_R, p.t5) * p.H + h) * kLog2e;
   } else if (kpos) {
-    // per key: the bias of its own offset, -inf for a key after the query
-    for (int r = tid; r < kDecChunk; r += kDecThreads) {
-      float b = -INFINITY;
-      if (jb + r < je) {
-        const int rel = __ldg(kpos + jb + r) - pos;
-        if (!p.causal || rel <= 0) b = __ldg(p.bias + t5_bucket_dev(rel, p.t5) * p.H + h) * kLog2e;
-      }
-      bias_s[r] = b;
-    }
+    // per key: the bias of its own offset, -inf for a key after the query.
+    // A thread's two keys are written out side by side so that both position
+    // loads, then both table loads, are in flight together.
+    static_assert(kDecChunk == 2 * kDecThreads, "two keys per thread");
+    const int r0 = tid, r1 = tid + kDecThreads;
+    const bool in0 = jb + r0 < je, in1 = jb + r1 < je;
+    const int rel0 = (in0 ? __ldg(kpos + jb + r0) : pos) - pos;
+    const int rel1 = (in1 ? __ldg(kpos + jb + r1) : pos) - pos;
+    const bool vis0 = in0 && (!p.causal || rel0 <= 0);
+    const bool vis1 = in1 && (!p.causal || rel1 <= 0);
+    const float b0 = vis0 ? __ldg(p.bias + t5_bucket_dev(rel0, p.t5) * p.H + h) : 0.f;
+    const float b1 = vis1 ? __ldg(p.bias + t5_bucket_dev(rel1, p.t5) * p.H + h) : 0.f;
+    bias_s[r0] = vis0 ? b0 * kLog2e : -INFINITY;
+    bias_s[r1] = vis1 ? b1 * kLog2e : -INFINITY;
   } else {
     for (int r = tid; r < kDecChunk; r += kDecThreads)
       bias_s[r] = __ldg(p.bias + t5_bucket_dev(jb + r - pos, p.t5) * p.H + h) * kLog2e;
