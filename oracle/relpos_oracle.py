@@ -413,3 +413,57 @@ def deberta_naive(Q, K, V, Pk, Pq, kclip, causal=False, q_offset=0) -> np.ndarra
                 out[b, h, i] = w @ V[b, h]
     return out
 
+
+
+# --------------------------------------------------------------------------
+# backward of the T5-bias attention
+# --------------------------------------------------------------------------
+
+def t5_attention_backward(Q, K, V, bias, dO, *, num_buckets: int = 32, max_distance: int = 128,
+                          causal: bool = False, q_offset: int = 0):
+    """Gradients (dQ, dK, dV, dbias) of the T5-bias attention forward, fp64.
+
+    The pages print no backward pass. What they fix is that the bias is a
+    learned parameter: [RPE] T5 gives it as an embedding of num_buckets rows
+    and one column per head, and [T5B] says a learned table maps each bucket
+    to one bias per head, every offset of a bucket sharing that value. So
+    the table's gradient gathers the logit gradients of every (batch, query,
+    key) whose offset falls in the bucket (R17: the [num_buckets, H] table is
+    shared by the whole batch, as the forward takes it). The other steps are
+    the chain rule through the forward, last step first, for one (b, h):
+
+      O = P V               ->  dV = P^T dO,   dP = dO V^T
+      P = softmax_row(S)    ->  dS_ij = P_ij (dP_ij - sum_l P_il dP_il)
+      S = Q K^T / sqrt(d) + bias[bucket(j - p_i), h], masked
+                            ->  dQ = dS K / sqrt(d),   dK = dS^T Q / sqrt(d),
+                                dbias[bucket(j - p_i), h] += dS_ij
+
+    A masked entry has P = 0, hence dS = 0; a row with no visible key (R10)
+    contributes nothing.
+    """
+    Q = np.asarray(Q, dtype=np.float64)
+    K = np.asarray(K, dtype=np.float64)
+    V = np.asarray(V, dtype=np.float64)
+    bias = np.asarray(bias, dtype=np.float64)
+    dO = np.asarray(dO, dtype=np.float64)
+    B, H, Lq, d = Q.shape
+    Lk = K.shape[2]
+    rows, p = _positions(Lq, q_offset, None)
+    rel = np.arange(Lk)[None, :] - p[:, None]
+    ids = np.array([[t5_bucket(int(r), not causal, num_buckets, max_distance) for r in row]
+                    for row in rel], dtype=np.int64).reshape(rel.shape)
+    dQ = np.zeros_like(Q)
+    dK = np.zeros_like(K)
+    dV = np.zeros_like(V)
+    dbias = np.zeros_like(bias)
+    for b in range(B):
+        for h in range(H):
+            lg = t5_logits(Q[b, h], K[b, h], bias[:, h], p, num_buckets, max_distance, causal)
+            P = _softmax_rows(_mask(lg, p, Lk, causal))
+            dV[b, h] = P.T @ dO[b, h]
+            dP = dO[b, h] @ V[b, h].T
+            dS = P * (dP - np.sum(P * dP, axis=1, keepdims=True))
+            dQ[b, h] = dS @ K[b, h] / math.sqrt(d)
+            dK[b, h] = dS.T @ Q[b, h] / math.sqrt(d)
+            np.add.at(dbias[:, h], ids.reshape(-1), dS.reshape(-1))
+    return dQ, dK, dV, dbias

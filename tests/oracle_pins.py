@@ -483,6 +483,106 @@ def check_key_positions_shift():
         assert np.max(np.abs(a - b)) < 1e-12
 
 
+# ---------------------------------------------------------------- backward pins
+
+# (causal, q_offset, num_buckets, max_distance): small tables whose log
+# buckets are reached by the offsets of a 5 x 7 score matrix
+_BWD_CASES = ((False, 0, 8, 5), (True, 2, 8, 6))
+
+
+def _bwd_inputs(seed, B=2, H=2, Lq=5, Lk=7, d=4, nb=8):
+    rng = _rng(seed)
+    Q = rng.standard_normal((B, H, Lq, d))
+    K = rng.standard_normal((B, H, Lk, d))
+    V = rng.standard_normal((B, H, Lk, d))
+    dO = rng.standard_normal((B, H, Lq, d))
+    bias = rng.standard_normal((nb, H))
+    return Q, K, V, dO, bias
+
+
+def check_t5_backward_finite_differences():
+    """Every gradient entry against a central difference of the pinned
+    forward: loss = sum(dO * O), perturbed one input entry at a time."""
+    h = 1e-5
+    for seed, (causal, qoff, nb, md) in enumerate(_BWD_CASES):
+        Q, K, V, dO, bias = _bwd_inputs(40 + seed, nb=nb)
+        kw = dict(num_buckets=nb, max_distance=md, causal=causal, q_offset=qoff)
+
+        def loss(Q_, K_, V_, b_):
+            return float(np.sum(dO * orc.attention(orc.MODE_T5, Q_, K_, V_, b_, None, num_buckets=nb,
+                                                   rel_param=md, causal=causal, q_offset=qoff)))
+
+        grads = orc.t5_attention_backward(Q, K, V, bias, dO, **kw)
+        for which, g in enumerate(grads):
+            x = (Q, K, V, bias)[which]
+            fd = np.zeros_like(x)
+            for idx in np.ndindex(x.shape):
+                args = [Q, K, V, bias]
+                xp, xm = x.copy(), x.copy()
+                xp[idx] += h
+                xm[idx] -= h
+                args[which] = xp
+                lp = loss(*args)
+                args[which] = xm
+                lm = loss(*args)
+                fd[idx] = (lp - lm) / (2 * h)
+            assert np.max(np.abs(fd - g)) < 1e-7 * max(1.0, np.max(np.abs(g))), (causal, which)
+
+
+def check_t5_backward_vs_autograd():
+    """dQ, dK, dV against torch autograd through scaled_dot_product_attention
+    (fp64) with the T5 bias expanded to a float mask by the pinned bucket
+    function; causal masking enters the mask as -inf."""
+    for seed, (causal, qoff, nb, md) in enumerate(_BWD_CASES):
+        Q, K, V, dO, bias = _bwd_inputs(50 + seed, nb=nb)
+        B, H, Lq, d = Q.shape
+        Lk = K.shape[2]
+        pos = np.arange(Lq) + qoff
+        rel = np.arange(Lk)[None, :] - pos[:, None]
+        ids = np.vectorize(lambda r: orc.t5_bucket(int(r), not causal, nb, md))(rel)
+        mask = np.stack([bias[ids, hh] for hh in range(H)])[None]  # [1, H, Lq, Lk]
+        if causal:
+            mask = np.where(rel[None, None] > 0, -np.inf, mask)
+        q, k, v = (torch.from_numpy(x.copy()).requires_grad_(True) for x in (Q, K, V))
+        out = torch.nn.functional.scaled_dot_product_attention(
+            q, k, v, attn_mask=torch.from_numpy(mask), scale=1 / math.sqrt(d))
+        out.backward(torch.from_numpy(dO))
+        dQ, dK, dV, _ = orc.t5_attention_backward(Q, K, V, bias, dO, num_buckets=nb,
+                                                  max_distance=md, causal=causal, q_offset=qoff)
+        for a, t in ((dQ, q), (dK, k), (dV, v)):
+            assert np.max(np.abs(a - t.grad.numpy())) < 1e-10, causal
+
+
+def check_t5_backward_invariants():
+    """Closed forms: adding one constant to every bias of a head, or one
+    vector to every key, shifts each row's logits uniformly, so the summed
+    gradients vanish; the probabilities of a row sum to one, so the value
+    gradients sum to the output gradients of the rows."""
+    for seed, (causal, qoff, nb, md) in enumerate(_BWD_CASES):
+        Q, K, V, dO, bias = _bwd_inputs(60 + seed, Lq=9, Lk=12, d=8, nb=nb)
+        dQ, dK, dV, db = orc.t5_attention_backward(Q, K, V, bias, dO, num_buckets=nb,
+                                                   max_distance=md, causal=causal, q_offset=qoff)
+        assert np.max(np.abs(db.sum(axis=0))) < 1e-12
+        assert np.max(np.abs(dK.sum(axis=2))) < 1e-12
+        assert np.max(np.abs(dV.sum(axis=2) - dO.sum(axis=2))) < 1e-12
+        assert np.max(np.abs(db)) > 1e-3  # not trivially zero
+
+
+def check_t5_backward_unused_bucket():
+    """[T5B]: bidirectional bucket 16 is never selected, so its bias gets no
+    gradient; with a single query and key the softmax is constant, so every
+    gradient but dV (= dO) is zero."""
+    Q, K, V, dO, _ = _bwd_inputs(70, Lq=20, Lk=20, d=4)
+    bias = _rng(71).standard_normal((32, 2))
+    _, _, _, db = orc.t5_attention_backward(Q, K, V, bias, dO, num_buckets=32, max_distance=128)
+    assert np.all(db[16] == 0.0) and np.all(db[15] == 0.0)  # 15 starts at distance 91
+    assert np.max(np.abs(db[1])) > 0
+    Q, K, V, dO, _ = _bwd_inputs(72, Lq=1, Lk=1, d=4)
+    dQ, dK, dV, db = orc.t5_attention_backward(Q, K, V, bias, dO)
+    assert np.all(dQ == 0) and np.all(dK == 0) and np.all(db == 0)
+    assert np.array_equal(dV, dO)
+
+
 ALL_CHECKS = [
     check_t5_golden, check_t5_unused_bucket, check_t5_64_buckets, check_deberta_delta,
     check_shaw_index, check_skew_identity, check_shaw_logits_vs_skew,
@@ -491,6 +591,8 @@ ALL_CHECKS = [
     check_t5_two_token, check_shaw_sign, check_deberta_sign, check_query_offset_consistency,
     check_alibi_zero_slopes_are_sdpa, check_alibi_closed_form,
     check_key_positions_contiguous, check_key_positions_eviction, check_key_positions_shift,
+    check_t5_backward_finite_differences, check_t5_backward_vs_autograd,
+    check_t5_backward_invariants, check_t5_backward_unused_bucket,
 ]
 
 

@@ -1,6 +1,8 @@
 """Plant plausible mistakes in the oracle (on the CPU) and check that the
 pins catch each one: a flipped sign, an off-by-one index, swapped operands,
-a dropped term, a wrong scale, a wrong mask boundary."""
+a dropped term, a wrong scale, a wrong mask boundary, and in the backward a
+dropped or misplaced softmax row term, a missing scale, the wrong operand,
+an incomplete or mis-indexed table gradient."""
 import math
 
 import numpy as np
@@ -144,6 +146,41 @@ def _kpos_no_query_offset(Q, K, V, bias, key_pos, **kw):
     return _ORIG_KPOS(Q, K, V, bias, key_pos, **kw)
 
 
+def _bwd_mutant(kind):
+    """The backward with one planted mistake (the forward part is the oracle's)."""
+    def bwd(Q, K, V, bias, dO, *, num_buckets=32, max_distance=128, causal=False, q_offset=0):
+        B, H, Lq, d = Q.shape
+        Lk = K.shape[2]
+        p = np.arange(Lq) + q_offset
+        rel = np.arange(Lk)[None, :] - p[:, None]
+        ids = np.vectorize(lambda r: orc.t5_bucket(int(r), not causal, num_buckets, max_distance))(rel)
+        dQ, dK, dV, db = (np.zeros_like(x, dtype=np.float64) for x in (Q, K, V, bias))
+        for b in range(B):
+            for h in range(H):
+                lg = orc.t5_logits(Q[b, h], K[b, h], bias[:, h], p, num_buckets, max_distance, causal)
+                P = orc._softmax_rows(orc._mask(lg, p, Lk, causal))
+                dV[b, h] = P.T @ dO[b, h]
+                dP = dO[b, h] @ V[b, h].T
+                if kind == "no_row_term":
+                    dS = P * dP
+                elif kind == "row_term_over_keys":
+                    dS = P * (dP - np.sum(P * dP, axis=0, keepdims=True))
+                else:
+                    dS = P * (dP - np.sum(P * dP, axis=1, keepdims=True))
+                sc = 1.0 if kind == "unscaled_dq" else 1 / math.sqrt(d)
+                dQ[b, h] = dS @ K[b, h] * sc
+                dK[b, h] = (dS.T @ Q[b, h] if kind != "dk_from_p" else P.T @ Q[b, h]) / math.sqrt(d)
+                if kind == "dbias_last_batch_only" and b != B - 1:
+                    continue
+                tgt = ids if kind != "dbias_transposed_offset" else np.vectorize(
+                    lambda r: orc.t5_bucket(int(-r), not causal, num_buckets, max_distance))(rel)
+                np.add.at(db[:, h], tgt.reshape(-1), dS.reshape(-1))
+        if kind == "dv_from_dp":
+            dV = dV * 0 + np.einsum("bhij,bhid->bhjd", np.ones((B, H, Lq, Lk)), dO) / Lq
+        return dQ, dK, dV, db
+    return bwd
+
+
 MUTATIONS = {
     "t5_sign_flipped": ("t5_bucket", _flip_t5(_ORIG_T5)),
     "t5_offset_off_by_one": ("t5_bucket", _shift_t5(_ORIG_T5)),
@@ -166,6 +203,13 @@ MUTATIONS = {
     "alibi_position_off_by_one": ("alibi_logits", _alibi_position_off_by_one),
     "kpos_index_not_position": ("t5_attention_key_positions", _kpos_index_not_position),
     "kpos_no_query_offset": ("t5_attention_key_positions", _kpos_no_query_offset),
+    "bwd_no_row_term": ("t5_attention_backward", _bwd_mutant("no_row_term")),
+    "bwd_row_term_over_keys": ("t5_attention_backward", _bwd_mutant("row_term_over_keys")),
+    "bwd_unscaled_dq": ("t5_attention_backward", _bwd_mutant("unscaled_dq")),
+    "bwd_dk_from_p": ("t5_attention_backward", _bwd_mutant("dk_from_p")),
+    "bwd_dbias_last_batch_only": ("t5_attention_backward", _bwd_mutant("dbias_last_batch_only")),
+    "bwd_dbias_transposed_offset": ("t5_attention_backward", _bwd_mutant("dbias_transposed_offset")),
+    "bwd_dv_uniform_weights": ("t5_attention_backward", _bwd_mutant("dv_from_dp")),
 }
 _ORIG_KPOS = orc.t5_attention_key_positions
 _ORIG_ALIBI = orc.alibi_logits
