@@ -208,6 +208,42 @@ int relpos_t5_decode_positions(const void* Q, const void* K, const void* V, cons
                                const int* key_pos, int B, int H, int Lq, int Lk, int num_buckets,
                                int max_distance, int causal, int q_offset, void* out, void* stream);
 
+/*
+ * relpos_t5_attn_bwd -- gradients of the T5-bias attention forward
+ * (relpos_attn_fwd with mode RELPOS_T5, dtype RELPOS_BF16). The bias is a
+ * learned table ("Relative Position Embeddings, in depth", section "T5: one
+ * scalar per head, looked up by bucket"; "T5 Relative-Position Bias": every
+ * offset of a bucket shares the bucket's value), so its gradient gathers the
+ * logit gradients dS_ij = P_ij (dP_ij - sum_l P_il dP_il) of every (batch, i, j)
+ * whose offset falls in the bucket. The pages print no backward pass; the
+ * other gradients follow from the chain rule through the forward:
+ * dV = P^T dO, dQ = dS K / sqrt(d), dK = dS^T Q / sqrt(d). The row term
+ * sum_j P_ij dP_ij is formed from P and dP themselves (not from the forward's
+ * output), so no output of the forward is needed.
+ *
+ *   Q, K, V, bias, B, H, Lq, Lk, d, num_buckets, max_distance, causal,
+ *   q_offset, stream: the forward call's arguments (bf16 Q [B,H,Lq,64], K, V
+ *               [B,H,Lk,64]; fp32 bias [num_buckets, H]; d must be 64).
+ *   dO          device, bf16 [B,H,Lq,64]: gradient of the loss w.r.t. O.
+ *   dQ          device, bf16 [B,H,Lq,64], written.
+ *   dK, dV      device, bf16 [B,H,Lk,64], written (rows no query sees: zero).
+ *   dbias       device, fp32 [num_buckets, H], overwritten with the sum over
+ *               the whole batch (the table is shared by it).
+ * All pointers 16-byte aligned and caller-owned; the outputs must not overlap
+ * the inputs. Limits: the distance R at which the last bucket starts (or the
+ * largest offset present, if smaller) must be <= 4096
+ * (RELPOS_ERR_UNSUPPORTED otherwise; max_distance 128 gives R = 91
+ * bidirectional, 113 causal). Scratch: 8 * B * H * Lq bytes of row statistics
+ * from cudaMallocAsync on `stream`, freed with cudaFreeAsync before the call
+ * returns. dbias is accumulated with floating-point atomics, so its last bits
+ * may differ between runs. Asynchronous on `stream`; device timeouts surface
+ * through relpos_check_status().
+ */
+int relpos_t5_attn_bwd(const void* Q, const void* K, const void* V, const void* dO,
+                       const void* bias, int B, int H, int Lq, int Lk, int d, int num_buckets,
+                       int max_distance, int causal, int q_offset, void* dQ, void* dK, void* dV,
+                       void* dbias, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

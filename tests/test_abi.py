@@ -93,3 +93,37 @@ def test_index_ids_argument_errors(lib):
         rp.RELPOS_ERR_INVALID_ARG
     assert rp.relpos_selftest_wait_timeout(0, None) == rp.RELPOS_ERR_INVALID_ARG
 
+
+
+def _bwd(**kw):
+    a = dict(Q=16, K=32, V=48, dO=80, bias=96, B=1, H=1, Lq=4, Lk=4, d=64, nb=32, md=128,
+             causal=0, qoff=0, dQ=112, dK=128, dV=144, dbias=160, stream=None)
+    a.update(kw)
+    v = lambda x: ctypes.c_void_p(x) if x else None  # noqa: E731
+    return rp.relpos_t5_attn_bwd(v(a["Q"]), v(a["K"]), v(a["V"]), v(a["dO"]), v(a["bias"]),
+                                 a["B"], a["H"], a["Lq"], a["Lk"], a["d"], a["nb"], a["md"],
+                                 a["causal"], a["qoff"], v(a["dQ"]), v(a["dK"]), v(a["dV"]),
+                                 v(a["dbias"]), a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(B=-1), rp.RELPOS_ERR_INVALID_ARG),
+    (dict(Lk=-2), rp.RELPOS_ERR_INVALID_ARG),
+    (dict(qoff=-1), rp.RELPOS_ERR_INVALID_ARG),
+    (dict(d=0), rp.RELPOS_ERR_INVALID_ARG),
+    (dict(d=128), rp.RELPOS_ERR_UNSUPPORTED),
+    (dict(nb=31), rp.RELPOS_ERR_INVALID_ARG),
+    (dict(md=8), rp.RELPOS_ERR_INVALID_ARG),
+    (dict(causal=3), rp.RELPOS_ERR_INVALID_ARG),
+    (dict(bias=0), rp.RELPOS_ERR_INVALID_ARG),      # null table
+    (dict(dbias=0), rp.RELPOS_ERR_INVALID_ARG),     # null table gradient
+    (dict(dbias=160 + 8), rp.RELPOS_ERR_INVALID_ARG),
+    (dict(B=300, H=300), rp.RELPOS_ERR_UNSUPPORTED),  # B * H beyond the grid
+])
+def test_backward_argument_errors_before_launch(lib, kw, code):
+    assert _bwd(**kw) == code
+
+
+def test_backward_empty_batch_is_noop(lib):
+    assert _bwd(B=0, Q=0, K=0, V=0, dO=0, dQ=0, dK=0, dV=0, bias=0, dbias=0) == rp.RELPOS_OK
+    assert _bwd(H=0) == rp.RELPOS_OK

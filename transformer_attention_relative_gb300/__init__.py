@@ -1,4 +1,4 @@
-"""Relative-position attention forward for GB300 (sm_103a).
+"""Relative-position attention for GB300 (sm_103a): forward, and the T5 backward.
 
 A thin ctypes binding over ``librelpos_attn.so`` (C ABI in
 ``include/relpos_attn.h``). The functions named like the C entry points pass
@@ -27,7 +27,8 @@ RELPOS_ERR_DEVICE_TIMEOUT = -4
 RELPOS_ERR_SCRATCH_LIMIT = -5
 
 EXPORTED = ("relpos_attn_fwd", "relpos_index_ids", "relpos_check_status", "relpos_strerror",
-            "relpos_selftest_wait_timeout", "relpos_t5_decode_noalloc", "relpos_t5_decode_positions")
+            "relpos_selftest_wait_timeout", "relpos_t5_decode_noalloc", "relpos_t5_decode_positions",
+            "relpos_t5_attn_bwd")
 
 _lib = None
 
@@ -62,6 +63,8 @@ def load_library(path: str = LIB_PATH):
     lib.relpos_t5_decode_noalloc.restype = i
     lib.relpos_t5_decode_positions.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, vp, vp]
     lib.relpos_t5_decode_positions.restype = i
+    lib.relpos_t5_attn_bwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, i, vp, vp, vp, vp, vp]
+    lib.relpos_t5_attn_bwd.restype = i
     _lib = lib
     return lib
 
@@ -106,6 +109,13 @@ def relpos_t5_decode_positions(Q, K, V, bias, key_pos, B, H, Lq, Lk, num_buckets
     return load_library().relpos_t5_decode_positions(Q, K, V, bias, key_pos, B, H, Lq, Lk,
                                                      num_buckets, max_distance, causal, q_offset,
                                                      out, stream)
+
+
+def relpos_t5_attn_bwd(Q, K, V, dO, bias, B, H, Lq, Lk, d, num_buckets, max_distance, causal,
+                       q_offset, dQ, dK, dV, dbias, stream) -> int:
+    """Gradients of the T5-bias attention: dQ, dK, dV and the bias table's."""
+    return load_library().relpos_t5_attn_bwd(Q, K, V, dO, bias, B, H, Lq, Lk, d, num_buckets,
+                                             max_distance, causal, q_offset, dQ, dK, dV, dbias, stream)
 
 
 strerror = relpos_strerror
@@ -194,3 +204,29 @@ def t5_decode_positions(Q, K, V, bias, key_pos, *, num_buckets: int = 32, max_di
     if rc != RELPOS_OK:
         raise RelposError(rc, "relpos_t5_decode_positions")
     return out
+
+
+def t5_attention_backward(Q, K, V, dO, bias, *, num_buckets: int = 32, max_distance: int = 128,
+                          causal: bool = False, q_offset: int = 0, stream=None):
+    """Run ``relpos_t5_attn_bwd`` on CUDA tensors; returns (dQ, dK, dV, dbias).
+
+    Q, dO [B,H,Lq,64] and K, V [B,H,Lk,64] bf16; bias [num_buckets, H] fp32. dQ / dK / dV come back bf16 like their
+    inputs, dbias fp32 like the table.
+    """
+    import torch
+    B, H, Lq, d = Q.shape
+    Lk = K.shape[2]
+    for t in (Q, K, V, dO, bias):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("tensors must be contiguous CUDA tensors")
+    if any(t.dtype != torch.bfloat16 for t in (Q, K, V, dO)) or bias.dtype != torch.float32:
+        raise TypeError("Q, K, V, dO must be bf16 and bias fp32")
+    dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
+    dbias = torch.empty_like(bias)
+    rc = relpos_t5_attn_bwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(dO), _ptr(bias), B, H, Lq, Lk, d,
+                            num_buckets, max_distance, int(causal), q_offset, _ptr(dQ), _ptr(dK),
+                            _ptr(dV), _ptr(dbias), _stream(stream))
+    if rc != RELPOS_OK:
+        raise RelposError(rc, "relpos_t5_attn_bwd")
+    return dQ, dK, dV, dbias
+

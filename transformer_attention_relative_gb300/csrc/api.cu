@@ -482,3 +482,83 @@ extern "C" int relpos_attn_fwd(int mode, int dtype, const void* Q, const void* K
   }
   return RELPOS_OK;
 }
+
+extern "C" int relpos_t5_attn_bwd(const void* Q, const void* K, const void* V, const void* dO,
+                                  const void* bias, int B, int H, int Lq, int Lk, int d, int num_buckets,
+                                  int max_distance, int causal, int q_offset, void* dQ, void* dK, void* dV,
+                                  void* dbias, void* stream) {
+  if (B < 0 || H < 0 || Lq < 0 || Lk < 0 || q_offset < 0 || d <= 0) return RELPOS_ERR_INVALID_ARG;
+  int rc = check_rel_params(RELPOS_T5, num_buckets, max_distance, causal);
+  if (rc != RELPOS_OK) return rc;
+  if (d != kHeadDim) return RELPOS_ERR_UNSUPPORTED;
+  if (B == 0 || H == 0) return RELPOS_OK;
+  if (!bias || !dbias || !aligned16(bias) || !aligned16(dbias)) return RELPOS_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * H > 65535) return RELPOS_ERR_UNSUPPORTED;
+  if (Lq > (1 << 24) || Lk > (1 << 24) || q_offset > (1 << 28)) return RELPOS_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t BH = static_cast<size_t>(B) * H;
+  const size_t row_bytes = kHeadDim * 2;
+  if (cudaMemsetAsync(dbias, 0, static_cast<size_t>(num_buckets) * H * 4, s) != cudaSuccess)
+    return RELPOS_ERR_CUDA;
+  if (Lq == 0 || Lk == 0) {  // no score: every gradient is zero
+    if (Lq > 0 && (!dQ || !aligned16(dQ))) return RELPOS_ERR_INVALID_ARG;
+    if (Lk > 0 && (!dK || !dV || !aligned16(dK) || !aligned16(dV))) return RELPOS_ERR_INVALID_ARG;
+    bool ok = true;
+    if (Lq > 0) ok = ok && cudaMemsetAsync(dQ, 0, BH * Lq * row_bytes, s) == cudaSuccess;
+    if (Lk > 0) ok = ok && cudaMemsetAsync(dK, 0, BH * Lk * row_bytes, s) == cudaSuccess &&
+                      cudaMemsetAsync(dV, 0, BH * Lk * row_bytes, s) == cudaSuccess;
+    return ok ? RELPOS_OK : RELPOS_ERR_CUDA;
+  }
+  if (!Q || !K || !V || !dO || !dQ || !dK || !dV) return RELPOS_ERR_INVALID_ARG;
+  for (const void* ptr : {Q, K, V, dO, static_cast<const void*>(dQ), static_cast<const void*>(dK),
+                          static_cast<const void*>(dV)})
+    if (!aligned16(ptr)) return RELPOS_ERR_INVALID_ARG;
+
+  T5Index t5;
+  int R = 0;
+  const long long nmax = std::max(static_cast<long long>(Lk) - 1, static_cast<long long>(Lq) - 1 + q_offset);
+  rc = t5_setup(num_buckets, max_distance, causal, nmax, &t5, &R);
+  if (rc != RELPOS_OK) return rc;
+  if (R < 1 || R > bwd_max_R()) return RELPOS_ERR_UNSUPPORTED;
+  int* status = status_ptr();
+  if (!status) return RELPOS_ERR_CUDA;
+
+  float* stats = nullptr;
+  if (cudaMallocAsync(reinterpret_cast<void**>(&stats), 2 * BH * Lq * sizeof(float), s) != cudaSuccess) {
+    cudaGetLastError();
+    return RELPOS_ERR_CUDA;
+  }
+  auto done = [&](int code) {
+    if (cudaFreeAsync(stats, s) != cudaSuccess && code == RELPOS_OK) code = RELPOS_ERR_CUDA;
+    if (code != RELPOS_OK) cudaGetLastError();
+    return code;
+  };
+  CUtensorMap tq, tk, tv, tdo;
+  if (!make_tmap(&tq, Q, Lq, static_cast<int>(BH)) || !make_tmap(&tk, K, Lk, static_cast<int>(BH)) ||
+      !make_tmap(&tv, V, Lk, static_cast<int>(BH)) || !make_tmap(&tdo, dO, Lq, static_cast<int>(BH)))
+    return done(RELPOS_ERR_CUDA);
+  BwdParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.B = B;
+  p.H = H;
+  p.Lq = Lq;
+  p.Lk = Lk;
+  p.causal = causal;
+  p.q_offset = q_offset;
+  p.scale = 1.0f / std::sqrt(static_cast<float>(d));
+  p.scale_log2 = p.scale * kLog2e;
+  p.bias = static_cast<const float*>(bias);
+  p.nb = num_buckets;
+  p.R = R;
+  p.t5 = t5;
+  p.lse = stats;
+  p.Dr = stats + BH * Lq;
+  p.dQ = static_cast<__nv_bfloat16*>(dQ);
+  p.dK = static_cast<__nv_bfloat16*>(dK);
+  p.dV = static_cast<__nv_bfloat16*>(dV);
+  p.dbias = static_cast<float*>(dbias);
+  p.status = status;
+  if (launch_bwd(tq, tk, tv, tdo, p, s) != cudaSuccess) return done(RELPOS_ERR_CUDA);
+  return done(RELPOS_OK);
+}
+

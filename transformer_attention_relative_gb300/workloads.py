@@ -10,7 +10,9 @@ scaled by the workload's sigma; then a cast to the kernel's input dtype
 (bf16, or fp32 for the tiny fp32 case). The T5 bias table stays fp32 in
 every workload; the Shaw and DeBERTa tables are bf16. ALiBi has no drawn
 table: its per-head slopes (fp32) are the geometric sequence 2^(-8(h+1)/H)
-commonly used with it (the pages fix no values).
+commonly used with it (the pages fix no values). The backward's output
+gradient dO [B,H,Lq,d] comes from its own generator seeded with
+``5000 + index``: ``randn`` (sigma 1), cast to the workload dtype.
 
 Shapes and distributions follow the five workloads the relative-position
 attention pages motivate: a tiny fp32 T5 encoder case, a T5-base-shaped
@@ -175,3 +177,13 @@ def make_inputs(w: Workload, seed: int | None = None):
                 kp[b, h, -1] = w.cache_len - 1
         x["key_pos"] = kp
     return x
+
+
+def make_grad_output(w: Workload, seed: int | None = None):
+    """Draw dO [B,H,Lq,d] (the gradient arriving at the attention output) for
+    the backward: standard normal, in the workload dtype, from a generator of
+    its own so that the forward inputs do not change."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed((w.seed if seed is None else seed) + 4000)
+    return torch.randn(w.B, w.H, w.Lq, w.d, generator=g, dtype=torch.float32).to(_dtype(w.dtype))
+
