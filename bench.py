@@ -44,7 +44,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from transformer_attention_relative_gb300.workloads import (MODE_NAMES, MODE_T5,  # noqa: E402
-                                                            WORKLOADS, make_inputs)
+                                                            WORKLOADS, make_grad_output, make_inputs)
 
 L2_BYTES = 129 * 1024 * 1024
 METRIC = "rel-pos attention fwd TFLOP/s (bf16) and % of GB300 dense BF16 peak"
@@ -70,25 +70,51 @@ def _code_only(text):
     return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
 
 
-def source_hash():
-    """Hash of the CUDA sources' code (comments excluded), to tell whether
-    stored ncu counters were taken on the code that runs."""
-    csrc = os.path.join(ROOT, "transformer_attention_relative_gb300", "csrc")
+CSRC = os.path.join(ROOT, "transformer_attention_relative_gb300", "csrc")
+# the library headers every kernel's translation unit includes, and each
+# kernel's own source files
+COMMON_HEADERS = ("ptx.cuh", "relpos_common.cuh", "relpos_internal.h")
+KERNEL_SOURCES = {
+    "relpos_fwd_kernel": ("attn_fwd.cu",),
+    "deberta_band_kernel": ("deberta_band.cu",),
+    "relpos_decode_partial_kernel": ("decode.cu",),
+    "relpos_bwd_dq_kernel": ("attn_bwd.cu", "relpos_bwd.cuh"),
+    "relpos_bwd_dkdv_kernel": ("attn_bwd.cu", "relpos_bwd.cuh"),
+}
+
+
+def _read_csrc(name):
+    with open(os.path.join(CSRC, name), encoding="utf-8") as fh:
+        return fh.read()
+
+
+def _hash_files(names, read=_read_csrc):
     h = hashlib.sha256()
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, f), encoding="utf-8") as fh:
-                h.update(f.encode())
-                h.update(_code_only(fh.read()).encode())
+    for f in sorted(names):
+        h.update(f.encode())
+        h.update(_code_only(read(f)).encode())
     return h.hexdigest()[:16]
 
 
+def source_hash():
+    """Hash of all CUDA sources' code (comments excluded)."""
+    return _hash_files([f for f in os.listdir(CSRC) if f.endswith((".cu", ".cuh", ".h"))])
+
+
+def kernel_hash(kernel, read=_read_csrc):
+    """Hash of the code (comments excluded) that the kernel's translation unit
+    compiles -- its own source files and the library headers -- to tell
+    whether stored ncu counters were taken on the code that runs."""
+    return _hash_files(KERNEL_SOURCES[kernel] + COMMON_HEADERS, read)
+
+
 def stored_traffic(kernel, workload):
-    """dram bytes per launch from profiles/traffic.txt if taken on these sources."""
+    """dram bytes per launch from profiles/traffic.txt if taken on the code
+    the kernel is compiled from now."""
     p = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(p):
         return None
-    want = source_hash()
+    want = kernel_hash(kernel)
     with open(p) as f:
         for line in f:
             parts = line.split()
@@ -339,6 +365,44 @@ class GpuRun:
         return e0.elapsed_time(e1), h2d, d2h
 
 
+class BwdRun(GpuRun):
+    """The T5 backward on the same inputs plus a drawn output gradient dO:
+    one step is one relpos_t5_attn_bwd call (dQ, dK, dV, dbias)."""
+
+    def __init__(self, w, device, stream):
+        import torch
+        super().__init__(w, device, stream)
+        dO = make_grad_output(w)
+        extra = 4 * dO.numel() * dO.element_size()  # dO, dQ, dK, dV
+        self.nsets = max(1, min(16, math.ceil(2.5 * L2_BYTES / (self.set_bytes + extra))))
+        self.sets = self.sets[:self.nsets]
+        for d in self.sets:
+            d["dO"] = dO.to(device)
+            d["dQ"] = torch.empty_like(d["Q"])
+            d["dK"] = torch.empty_like(d["K"])
+            d["dV"] = torch.empty_like(d["V"])
+            d["dbias"] = torch.empty_like(d["table0"])
+        torch.cuda.synchronize()
+
+    def _call(self, d, out=None):
+        w = self.w
+        p = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+        rc = self.rp.relpos_t5_attn_bwd(p(d["Q"]), p(d["K"]), p(d["V"]), p(d["dO"]), p(d["table0"]),
+                                        w.B, w.H, w.Lq, w.Lk, w.d, w.num_buckets, w.rel_param,
+                                        int(w.causal), w.q_offset, p(d["dQ"]), p(d["dK"]),
+                                        p(d["dV"]), p(d["dbias"]), self.sptr)
+        if rc != 0:
+            raise RuntimeError(f"relpos_t5_attn_bwd failed: {rc}")
+
+
+def bwd_flops(w):
+    """Algorithmic flops of the T5 backward: the four gradient products
+    (dV = P^T dO, dP = dO V^T, dQ = dS K, dK = dS^T Q) over the visible
+    (query, key) pairs, twice the forward's two products; the recomputation
+    of S is not counted."""
+    return 2.0 * w.flops()
+
+
 def measure_workload(w, device, stream, steps, warmup, barrier):
     g = GpuRun(w, device, stream)
     ms, t0, t1 = g.timed(steps, warmup, barrier)
@@ -516,7 +580,7 @@ def main():
         unit = "GB/s"
         traffic = stored_traffic(kname, w.name)
     roofline = {"bound": bound, "kernel": kname, "achieved": achieved, "peak": peak, "unit": unit,
-                "frac": achieved / peak, "traffic": traffic,
+                "frac": achieved / peak, "traffic": traffic, "kernel_hash": kernel_hash(kname),
                 "peak_source": f"{peak_src} ({'bf16_tflops burst' if bound == 'tensor' else 'hbm_gbs'})",
                 "algorithmic_per_launch": flops if bound == "tensor" else w.min_bytes()}
 
@@ -547,6 +611,20 @@ def main():
                 torch.cuda.empty_cache()
             except Exception as e:  # a mode this build does not run yet
                 others[name] = {"unavailable": str(e)[:120]}
+        for name in ("t5_base_bidir", "t5_causal"):
+            ow = WORKLOADS[name]
+            try:
+                og = BwdRun(ow, device, stream)
+                k = 30
+                oms, _, _ = og.timed(k, 3, lambda: None)
+                per = oms / k / 1e3
+                tf = bwd_flops(ow) / per / 1e12
+                others[name + "_backward"] = {"ms_per_step": oms / k, "tflops": tf,
+                                              "frac_of_bf16_peak": tf / peaks["bf16_tflops"]}
+                del og
+                torch.cuda.empty_cache()
+            except Exception as e:
+                others[name + "_backward"] = {"unavailable": str(e)[:120]}
 
     sampler.stop()
 

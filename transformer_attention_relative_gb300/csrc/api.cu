@@ -15,6 +15,7 @@
 
 #include "../../include/relpos_attn.h"
 #include "ptx.cuh"
+#include "relpos_bwd.cuh"
 #include "relpos_common.cuh"
 #include "relpos_internal.h"
 

@@ -43,8 +43,8 @@
 #include <cstdint>
 
 #include "ptx.cuh"
+#include "relpos_bwd.cuh"
 #include "relpos_common.cuh"
-#include "relpos_internal.h"
 
 namespace relpos {
 namespace {

@@ -1,0 +1,54 @@
+// relpos_bwd.cuh -- parameter block, launcher and tcgen05 helper of the T5
+// attention backward (attn_bwd.cu), kept apart from the headers the forward
+// and decode kernels compile.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "ptx.cuh"
+#include "relpos_common.cuh"
+
+namespace relpos {
+
+constexpr int kMaxT5Buckets = 128;
+
+// Backward of the T5-bias attention (attn_bwd.cu)
+struct BwdParams {
+  int B, H, Lq, Lk;
+  int causal, q_offset;
+  float scale;       // 1 / sqrt(d)
+  float scale_log2;  // scale times log2(e)
+  const float* bias;  // [nb, H]
+  int nb;
+  int R;  // |offset| >= R: the side's last bucket; offsets in (-R, R) get a table entry each
+  T5Index t5;
+  float* lse;  // [B*H, Lq] row log-sum-exp of the log2-scaled logits (written by the dQ kernel)
+  float* Dr;   // [B*H, Lq] D_i = sum_j P_ij dP_ij
+  __nv_bfloat16* dQ;  // [B*H, Lq, 64]
+  __nv_bfloat16* dK;  // [B*H, Lk, 64]
+  __nv_bfloat16* dV;  // [B*H, Lk, 64]
+  float* dbias;       // [nb, H], zeroed before the dQ kernel, accumulated by it
+  int* status;
+};
+
+// T5 backward: the dQ kernel (row statistics, dQ, dbias), then the dK / dV
+// kernel; bwd_max_R is the largest saturation distance R they support
+int bwd_max_R();
+cudaError_t launch_bwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                       const CUtensorMap& tmdO, const BwdParams& p, cudaStream_t stream);
+
+// 16 consecutive 32-bit TMEM columns of this thread's lane.
+RP_DEVI void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
+      : "memory");
+}
+
+}  // namespace relpos

@@ -10,7 +10,6 @@ namespace relpos {
 
 constexpr int kHeadDim = 64;
 constexpr int kMaxT5Thresholds = 64;
-constexpr int kMaxT5Buckets = 128;
 constexpr float kLog2e = 1.4426950408889634f;
 
 // T5 bucket generator ("Relative Position Embeddings, in depth", section
@@ -109,25 +108,6 @@ struct BandParams {
   int const_pitch;
   float* ends;                // [BH, 2, ends_pitch]
   int ends_pitch;
-  int* status;
-};
-
-// Backward of the T5-bias attention (attn_bwd.cu)
-struct BwdParams {
-  int B, H, Lq, Lk;
-  int causal, q_offset;
-  float scale;       // 1 / sqrt(d)
-  float scale_log2;  // scale times log2(e)
-  const float* bias;  // [nb, H]
-  int nb;
-  int R;  // |offset| >= R: the side's last bucket; offsets in (-R, R) get a table entry each
-  T5Index t5;
-  float* lse;  // [B*H, Lq] row log-sum-exp of the log2-scaled logits (written by the dQ kernel)
-  float* Dr;   // [B*H, Lq] D_i = sum_j P_ij dP_ij
-  __nv_bfloat16* dQ;  // [B*H, Lq, 64]
-  __nv_bfloat16* dK;  // [B*H, Lk, 64]
-  __nv_bfloat16* dV;  // [B*H, Lk, 64]
-  float* dbias;       // [nb, H], zeroed before the dQ kernel, accumulated by it
   int* status;
 };
 

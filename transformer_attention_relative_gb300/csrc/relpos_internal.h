@@ -27,12 +27,6 @@ int check_rel_params(int mode, int num_buckets, int rel_param, int causal);
 cudaError_t launch_deberta_band(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmPk,
                                 const CUtensorMap& tmPq, const BandParams& bp, cudaStream_t stream);
 
-// T5 backward: the dQ kernel (row statistics, dQ, dbias), then the dK / dV
-// kernel; bwd_max_R is the largest saturation distance R they support
-int bwd_max_R();
-cudaError_t launch_bwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                       const CUtensorMap& tmdO, const BwdParams& p, cudaStream_t stream);
-
 int decode_chunk_keys();
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);
 
