@@ -467,3 +467,89 @@ def t5_attention_backward(Q, K, V, bias, dO, *, num_buckets: int = 32, max_dista
             dK[b, h] = dS.T @ Q[b, h] / math.sqrt(d)
             np.add.at(dbias[:, h], ids.reshape(-1), dS.reshape(-1))
     return dQ, dK, dV, dbias
+
+
+def attention_backward(mode: int, Q, K, V, table0, table1, dO, *, num_buckets: int = 32,
+                       rel_param: int = 128, causal: bool = False, q_offset: int = 0):
+    """Gradients of the forward ``attention`` for every mode, fp64:
+    (dQ, dK, dV, dtable0, dtable1) with dtable1 None where there is no table1.
+
+    The steps are the chain rule through each mode's forward, as for
+    ``t5_attention_backward`` (which this calls for T5): with P the softmax
+    weights, dP_ij = dO_i . dvalue_ij, dS = P * (dP - sum_l P_il dP_il), and
+    the logit's parts give the rest. Reading R17 carries over: a table
+    shared by the batch (and for Shaw by the heads too) gathers the
+    gradients of every score that read it.
+
+    * Shaw ([RPE] "Shaw et al."): logit = q_i . (k_j + a_K[r]) / sqrt(d),
+      value = v_j + a_V[r] with r = clip(j - p_i) + k. So dQ_i = sum_j dS_ij
+      (k_j + a_K[r]) / sqrt(d), dK_j = sum_i dS_ij q_i / sqrt(d),
+      da_K[r] = sum of dS_ij q_i / sqrt(d) over the scores with that r,
+      dV_j = sum_i P_ij dO_i, da_V[r] = sum of P_ij dO_i over them.
+    * DeBERTa ([RPE] DeBERTa, [DRP] the delta cases; reading R8):
+      logit = (q_i . k_j + q_i . Pk[delta(i, j)] + k_j . Pq[delta(j, i)])
+      / sqrt(3d). So dQ_i = sum_j dS_ij (k_j + Pk[delta(i, j)]) / sqrt(3d),
+      dK_j = sum_i dS_ij (q_i + Pq[delta(j, i)]) / sqrt(3d), dPk[r, h] = sum
+      of dS_ij q_i / sqrt(3d) over delta(i, j) = r, dPq[r, h] = sum of
+      dS_ij k_j / sqrt(3d) over delta(j, i) = r.
+    * ALiBi ([RPE] "ALiBi and RoPE"; reading R15): logit = q_i . k_j /
+      sqrt(d) - slope_h |j - p_i|, so dslope_h = -sum dS_ij |j - p_i|.
+    """
+    if mode == MODE_T5:
+        dQ, dK, dV, db = t5_attention_backward(Q, K, V, table0, dO, num_buckets=num_buckets,
+                                               max_distance=rel_param, causal=causal,
+                                               q_offset=q_offset)
+        return dQ, dK, dV, db, None
+    Q = np.asarray(Q, dtype=np.float64)
+    K = np.asarray(K, dtype=np.float64)
+    V = np.asarray(V, dtype=np.float64)
+    dO = np.asarray(dO, dtype=np.float64)
+    t0 = np.asarray(table0, dtype=np.float64)
+    t1 = None if table1 is None else np.asarray(table1, dtype=np.float64)
+    B, H, Lq, d = Q.shape
+    Lk = K.shape[2]
+    rows, p = _positions(Lq, q_offset, None)
+    j = np.arange(Lk)
+    dQ, dK, dV = np.zeros_like(Q), np.zeros_like(K), np.zeros_like(V)
+    dt0 = np.zeros_like(t0)
+    dt1 = None if t1 is None else np.zeros_like(t1)
+    kc = rel_param
+    for b in range(B):
+        for h in range(H):
+            q, k, v, g = Q[b, h], K[b, h], V[b, h], dO[b, h]
+            if mode == MODE_SHAW:
+                lg = shaw_logits(q, k, t0, p, kc)
+                r = np.clip(j[None, :] - p[:, None], -kc, kc) + kc
+            elif mode == MODE_ALIBI:
+                lg = alibi_logits(q, k, t0[h], p)
+            else:
+                lg = deberta_logits(q, k, t0[:, h, :], t1[:, h, :], p, kc)
+                rr = p[:, None] - j[None, :]
+                d_ij = np.clip(rr, -kc, kc - 1) + kc
+                d_ji = np.clip(-rr, -kc, kc - 1) + kc
+            P = _softmax_rows(_mask(lg, p, Lk, causal))
+            dV[b, h] = P.T @ g
+            dP = g @ v.T
+            if mode == MODE_SHAW:  # the value of key j for row i is v_j + a_V[r_ij]
+                dP = dP + np.einsum("id,ijd->ij", g, t1[r])
+            dS = P * (dP - np.sum(P * dP, axis=1, keepdims=True))
+            if mode == MODE_SHAW:
+                sc = 1 / math.sqrt(d)
+                dQ[b, h] = (dS @ k + np.einsum("ij,ijd->id", dS, t0[r])) * sc
+                dK[b, h] = dS.T @ q * sc
+                for i in range(len(p)):
+                    np.add.at(dt0, r[i], dS[i][:, None] * q[i][None, :] * sc)
+                    np.add.at(dt1, r[i], P[i][:, None] * g[i][None, :])
+            elif mode == MODE_ALIBI:
+                sc = 1 / math.sqrt(d)
+                dQ[b, h] = dS @ k * sc
+                dK[b, h] = dS.T @ q * sc
+                dt0[h] += -np.sum(dS * np.abs(j[None, :] - p[:, None]))
+            else:
+                sc = 1 / math.sqrt(3 * d)
+                dQ[b, h] = (dS @ k + np.einsum("ij,ijd->id", dS, t0[d_ij, h, :])) * sc
+                dK[b, h] = (dS.T @ q + np.einsum("ij,ijd->jd", dS, t1[d_ji, h, :])) * sc
+                for i in range(len(p)):
+                    np.add.at(dt0[:, h, :], d_ij[i], dS[i][:, None] * q[i][None, :] * sc)
+                    np.add.at(dt1[:, h, :], d_ji[i], dS[i][:, None] * k * sc)
+    return dQ, dK, dV, dt0, dt1

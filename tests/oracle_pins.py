@@ -583,6 +583,93 @@ def check_t5_backward_unused_bucket():
     assert np.array_equal(dV, dO)
 
 
+# Shaw (k = 3, 7 rows), DeBERTa (k = 3, 6 rows) and ALiBi tables for the
+# backward pins of the other modes
+def _mode_tables(mode, rng, H, d):
+    if mode == orc.MODE_SHAW:
+        return rng.standard_normal((7, d)), rng.standard_normal((7, d)), 3
+    if mode == orc.MODE_DEBERTA:
+        return rng.standard_normal((6, H, d)), rng.standard_normal((6, H, d)), 3
+    return np.array([0.3, 0.7][:H]), None, 0
+
+
+def check_backward_finite_differences_all_modes():
+    """Shaw, DeBERTa and ALiBi: every entry of dQ, dK, dV and of the table
+    gradients against a central difference of the pinned forward."""
+    h = 1e-5
+    for mode in (orc.MODE_SHAW, orc.MODE_DEBERTA, orc.MODE_ALIBI):
+        for causal, qoff in ((False, 0), (True, 2)):
+            rng = _rng(80 + mode)
+            Q, K, V, dO, _ = _bwd_inputs(80 + mode, B=1, Lq=4, Lk=6, d=3)
+            t0, t1, kc = _mode_tables(mode, rng, 2, 3)
+            kw = dict(rel_param=kc, causal=causal, q_offset=qoff)
+            grads = orc.attention_backward(mode, Q, K, V, t0, t1, dO, **kw)
+
+            def loss(*a):
+                return float(np.sum(dO * orc.attention(mode, *a, **kw)))
+
+            for which, x in enumerate((Q, K, V, t0, t1)):
+                if x is None:
+                    continue
+                fd = np.zeros_like(x)
+                for idx in np.ndindex(x.shape):
+                    args = [Q, K, V, t0, t1]
+                    xp, xm = x.copy(), x.copy()
+                    xp[idx] += h
+                    xm[idx] -= h
+                    args[which] = xp
+                    lp = loss(*args)
+                    args[which] = xm
+                    fd[idx] = (lp - loss(*args)) / (2 * h)
+                g = grads[which]
+                assert np.max(np.abs(fd - g)) < 1e-7 * max(1.0, np.max(np.abs(g))), (mode, causal, which)
+
+
+def check_backward_zero_tables_vs_autograd():
+    """With zero tables (zero slopes) every mode is plain softmax attention:
+    dQ, dK, dV equal torch autograd through SDPA in fp64 (scale 1/sqrt(d),
+    DeBERTa 1/sqrt(3d)); the value table's gradient is then still the
+    weight mass per offset times dO, which sums to sum_i dO_i."""
+    rng = _rng(90)
+    B, H, Lq, Lk, d = 2, 2, 5, 8, 4
+    for causal, qoff in ((False, 0), (True, 3)):
+        Q, K, V, dO = (rng.standard_normal((B, H, n, d)) for n in (Lq, Lk, Lk, Lq))
+        for mode, t0, t1, kc, scale in (
+                (orc.MODE_SHAW, np.zeros((7, d)), np.zeros((7, d)), 3, 1 / math.sqrt(d)),
+                (orc.MODE_DEBERTA, np.zeros((6, H, d)), np.zeros((6, H, d)), 3, 1 / math.sqrt(3 * d)),
+                (orc.MODE_ALIBI, np.zeros(H), None, 0, 1 / math.sqrt(d))):
+            q, k, v = (torch.from_numpy(x.copy()).requires_grad_(True) for x in (Q, K, V))
+            mask = None
+            if causal:
+                mask = torch.arange(Lk)[None, :] <= (torch.arange(Lq)[:, None] + qoff)
+            out = torch.nn.functional.scaled_dot_product_attention(q, k, v, attn_mask=mask, scale=scale)
+            out.backward(torch.from_numpy(dO))
+            got = orc.attention_backward(mode, Q, K, V, t0, t1, dO, rel_param=kc, causal=causal,
+                                         q_offset=qoff)
+            for a, t in zip(got[:3], (q, k, v)):
+                assert np.max(np.abs(a - t.grad.numpy())) < 1e-10, (mode, causal)
+            if mode == orc.MODE_SHAW:
+                assert np.max(np.abs(got[4].sum(axis=0) - dO.sum(axis=(0, 1, 2)))) < 1e-10
+
+
+def check_backward_table_sums():
+    """Closed forms: one vector added to every a_K row (Shaw) or to every Pk
+    row of a head (DeBERTa) shifts each row's logits uniformly, so those
+    table gradients sum to zero over the rows; the a_V gradient sums to
+    sum_i dO_i (each row's weights sum to one)."""
+    rng = _rng(95)
+    Q, K, V, dO, _ = _bwd_inputs(95, B=2, Lq=6, Lk=9, d=4)
+    for causal, qoff in ((False, 0), (True, 3)):
+        for mode in (orc.MODE_SHAW, orc.MODE_DEBERTA):
+            t0, t1, kc = _mode_tables(mode, rng, 2, 4)
+            _, _, _, d0, d1 = orc.attention_backward(mode, Q, K, V, t0, t1, dO, rel_param=kc,
+                                                     causal=causal, q_offset=qoff)
+            assert np.max(np.abs(d0.sum(axis=0))) < 1e-12
+            if mode == orc.MODE_SHAW:
+                assert np.max(np.abs(d1.sum(axis=0) - dO.sum(axis=(0, 1, 2)))) < 1e-12
+            assert np.max(np.abs(d0)) > 1e-3 and np.max(np.abs(d1)) > 1e-3
+
+
 ALL_CHECKS = [
     check_t5_golden, check_t5_unused_bucket, check_t5_64_buckets, check_deberta_delta,
     check_shaw_index, check_skew_identity, check_shaw_logits_vs_skew,
@@ -593,15 +680,20 @@ ALL_CHECKS = [
     check_key_positions_contiguous, check_key_positions_eviction, check_key_positions_shift,
     check_t5_backward_finite_differences, check_t5_backward_vs_autograd,
     check_t5_backward_invariants, check_t5_backward_unused_bucket,
+    check_backward_finite_differences_all_modes, check_backward_zero_tables_vs_autograd,
+    check_backward_table_sums,
 ]
 
 
-def run_all():
-    """Run every pin; return the names of those that fail."""
+def run_all(stop_at_first=False):
+    """Run every pin; return the names of those that fail (only the first
+    one with stop_at_first)."""
     failed = []
     for fn in ALL_CHECKS:
         try:
             fn()
         except Exception:  # an assertion, or a crash on out-of-range ids
             failed.append(fn.__name__)
+            if stop_at_first:
+                break
     return failed

@@ -181,6 +181,32 @@ def _bwd_mutant(kind):
     return bwd
 
 
+_ORIG_BWD = orc.attention_backward
+
+
+def _abwd_mutant(kind):
+    """attention_backward with one planted mistake in a mode's gradients."""
+    def bwd(mode, Q, K, V, t0, t1, dO, **kw):
+        dQ, dK, dV, d0, d1 = _ORIG_BWD(mode, Q, K, V, t0, t1, dO, **kw)
+        d = Q.shape[-1]
+        if kind == "shaw_dak_unscaled" and mode == orc.MODE_SHAW:
+            d0 = d0 * math.sqrt(d)
+        elif kind == "shaw_dav_reversed" and mode == orc.MODE_SHAW:
+            d1 = d1[::-1].copy()
+        elif kind == "shaw_dav_from_ds" and mode == orc.MODE_SHAW:
+            d1 = d1 * 0.0
+        elif kind == "deberta_dpq_reversed" and mode == orc.MODE_DEBERTA:
+            d1 = d1[::-1].copy()
+        elif kind == "deberta_dk_scale_sqrt_d" and mode == orc.MODE_DEBERTA:
+            dK = dK * math.sqrt(3.0)
+        elif kind == "deberta_tables_swapped" and mode == orc.MODE_DEBERTA:
+            d0, d1 = d1, d0
+        elif kind == "alibi_slope_sign" and mode == orc.MODE_ALIBI:
+            d0 = -d0
+        return dQ, dK, dV, d0, d1
+    return bwd
+
+
 MUTATIONS = {
     "t5_sign_flipped": ("t5_bucket", _flip_t5(_ORIG_T5)),
     "t5_offset_off_by_one": ("t5_bucket", _shift_t5(_ORIG_T5)),
@@ -210,6 +236,13 @@ MUTATIONS = {
     "bwd_dbias_last_batch_only": ("t5_attention_backward", _bwd_mutant("dbias_last_batch_only")),
     "bwd_dbias_transposed_offset": ("t5_attention_backward", _bwd_mutant("dbias_transposed_offset")),
     "bwd_dv_uniform_weights": ("t5_attention_backward", _bwd_mutant("dv_from_dp")),
+    "bwd_shaw_dak_unscaled": ("attention_backward", _abwd_mutant("shaw_dak_unscaled")),
+    "bwd_shaw_dav_reversed": ("attention_backward", _abwd_mutant("shaw_dav_reversed")),
+    "bwd_shaw_dav_dropped": ("attention_backward", _abwd_mutant("shaw_dav_from_ds")),
+    "bwd_deberta_dpq_reversed": ("attention_backward", _abwd_mutant("deberta_dpq_reversed")),
+    "bwd_deberta_dk_scale": ("attention_backward", _abwd_mutant("deberta_dk_scale_sqrt_d")),
+    "bwd_deberta_tables_swapped": ("attention_backward", _abwd_mutant("deberta_tables_swapped")),
+    "bwd_alibi_slope_sign": ("attention_backward", _abwd_mutant("alibi_slope_sign")),
 }
 _ORIG_KPOS = orc.t5_attention_key_positions
 _ORIG_ALIBI = orc.alibi_logits
@@ -221,5 +254,5 @@ _ORIG_DELTA = orc.deberta_delta
 def test_pins_catch_mutation(name, monkeypatch):
     attr, fn = MUTATIONS[name]
     monkeypatch.setattr(orc, attr, fn)
-    failed = P.run_all()
+    failed = P.run_all(stop_at_first=True)
     assert failed, f"no pin caught the planted mistake {name}"
