@@ -20,6 +20,8 @@ Sources (three web pages on relative position in attention):
   relative-position module.
 * ALiBi: [RPE] "ALiBi and RoPE: the two endpoints" -- T5 with the table
   removed, a fixed slope per head times the distance, no maximum distance.
+* Transformer-XL: [RPE] "Transformer-XL: four terms and two global biases"
+  -- content and position keys with separate projections, the biases u, v.
 
 Conventions (readings where the pages leave a step open are marked R#):
 
@@ -49,7 +51,7 @@ import math
 
 import numpy as np
 
-MODE_T5, MODE_SHAW, MODE_DEBERTA, MODE_ALIBI = 0, 1, 2, 3
+MODE_T5, MODE_SHAW, MODE_DEBERTA, MODE_ALIBI, MODE_TXL = 0, 1, 2, 3, 4
 
 
 # --------------------------------------------------------------------------
@@ -271,13 +273,51 @@ def alibi_logits(q, k, slope_h, p):
     return q @ k.T / math.sqrt(d) - slope_h * dist
 
 
+def sinusoid(t, d: int) -> np.ndarray:
+    """The fixed sinusoidal encoding R(t) of an offset t, length d.
+
+    [RPE] "Transformer-XL: four terms and two global biases": R is a fixed
+    sinusoidal encoding of the offset. The page gives no frequencies; R18
+    takes the usual Transformer ones: R[2m] = sin(t w_m), R[2m+1] =
+    cos(t w_m), w_m = 10000^(-2m/d).
+    """
+    m = np.arange(d // 2)
+    w = 10000.0 ** (-2.0 * m / d)
+    out = np.empty(d)
+    out[0::2] = np.sin(t * w)
+    out[1::2] = np.cos(t * w)
+    return out
+
+
+def txl_logits(q, k, u_h, v_h, rk_h, p):
+    """Scaled Transformer-XL logits of one head.
+
+    [RPE] Transformer-XL: content to content q_i . k_j, content-dependent
+    position q_i . r(i - j), global content bias u . k_j and global position
+    bias v . r(i - j), where r(t) is the key-projected sinusoidal encoding of
+    the offset t = query position - key position; (a) and (c) combine as
+    (q_i + u) against the keys, (b) and (d) as (q_i + v) against r. R18:
+    ``rk_h`` [Lk + max(p), d] holds r(t) for t = -(Lk - 1) ... max(p) at row
+    t + Lk - 1 (the projection is the caller's); the whole logit is scaled by
+    1/sqrt(d) like the other modes.
+    """
+    d = q.shape[-1]
+    Lk = k.shape[0]
+    t = p[:, None] - np.arange(Lk)[None, :]
+    pos = np.einsum("id,ijd->ij", q + v_h[None, :], rk_h[t + Lk - 1])
+    return ((q + u_h[None, :]) @ k.T + pos) / math.sqrt(d)
+
+
 def attention(mode: int, Q, K, V, table0, table1=None, *, num_buckets: int = 32,
               rel_param: int = 128, causal: bool = False, q_offset: int = 0,
               rows=None, heads=None) -> np.ndarray:
     """Forward relative-position attention in fp64.
 
     Q [B,H,Lq,d], K/V [B,H,Lk,d]. Tables: T5 bias [num_buckets, H];
-    Shaw a_K, a_V [2k+1, d]; DeBERTa Pk, Pq [2k, H, d]; ALiBi slopes [H].
+    Shaw a_K, a_V [2k+1, d]; DeBERTa Pk, Pq [2k, H, d]; ALiBi slopes [H];
+    Transformer-XL projected encodings r [Lk + Lq - 1 + q_offset, H, d]
+    (row t + Lk - 1 for the offset t = query - key position) and the biases
+    [2, H, d] (u, then v).
     ``rows`` limits the
     computation to some query rows (the result then has len(rows) rows);
     ``heads`` to some (b, h) pairs (result [len(heads), rows, d]).
@@ -306,6 +346,8 @@ def attention(mode: int, Q, K, V, table0, table1=None, *, num_buckets: int = 32,
             lg = shaw_logits(q, k, t0, p, rel_param)
         elif mode == MODE_ALIBI:
             lg = alibi_logits(q, k, t0[h], p)
+        elif mode == MODE_TXL:
+            lg = txl_logits(q, k, t1[0, h], t1[1, h], t0[:, h, :], p)
         else:
             lg = deberta_logits(q, k, t0[:, h, :], t1[:, h, :], p, rel_param)
         w = _softmax_rows(_mask(lg, p, Lk, causal))

@@ -670,6 +670,80 @@ def check_backward_table_sums():
             assert np.max(np.abs(d0)) > 1e-3 and np.max(np.abs(d1)) > 1e-3
 
 
+# ---------------------------------------------------------------- Transformer-XL pins
+
+def check_txl_reductions():
+    """[RPE] Transformer-XL: (a) and (c) combine as (q_i + u) against the
+    keys. With no position encodings (r = 0), or with r the same vector for
+    every offset (the position term is then a row constant, which the
+    softmax ignores), the output is plain attention of Q + u (SDPA, fp64)."""
+    rng = _rng(100)
+    B, H, d = 2, 3, 8
+    for causal, qoff, Lq, Lk in ((False, 0, 6, 9), (True, 3, 6, 9), (True, 0, 7, 7)):
+        Q, K, V = (rng.standard_normal((B, H, n, d)) for n in (Lq, Lk, Lk))
+        uv = rng.standard_normal((2, H, d))
+        want = _sdpa(Q + uv[0][None, :, None, :], K, V, 1 / math.sqrt(d), causal, qoff)
+        n_off = Lk + Lq - 1 + qoff
+        for rk in (np.zeros((n_off, H, d)), np.broadcast_to(rng.standard_normal((1, H, d)), (n_off, H, d))):
+            got = orc.attention(orc.MODE_TXL, Q, K, V, np.ascontiguousarray(rk), uv, causal=causal,
+                                q_offset=qoff)
+            assert np.max(np.abs(got - want)) < 1e-12, causal
+
+
+def check_txl_skew():
+    """The page forms (b) + (d) with the same skew as Music Transformer: with
+    K = 0 and u = 0 the causal logits times sqrt(d) are (q_i + v) . r(i - j),
+    which is skew((Q + v) E^T)[i, j] on and below the diagonal for
+    E[c] = r(L - 1 - c) (the embedding of distance c - (L - 1) = j - i)."""
+    rng = _rng(101)
+    L, d = 7, 5
+    q = rng.standard_normal((L, d))
+    v = rng.standard_normal(d)
+    rk = rng.standard_normal((2 * L - 1, d))  # r(t) at row t + L - 1
+    p = np.arange(L)
+    lg = orc.txl_logits(q, np.zeros((L, d)), np.zeros(d), v, rk, p) * math.sqrt(d)
+    E = np.stack([rk[(L - 1 - c) + L - 1] for c in range(L)])
+    sk = orc.skew((q + v) @ E.T)
+    low = np.tril(np.ones((L, L), dtype=bool))
+    assert np.max(np.abs(lg[low] - sk[low])) < 1e-12
+
+
+def check_txl_two_token():
+    """Sign: r is indexed by query minus key position ([RPE]: R(i - j)).
+    Two tokens, causal, q = k = u = 0, v = e_0, r(1) = 8 e_0 (the key one
+    behind), r(0) = r(-1) = 0, d = 4: the second query's logits are 4 and 0,
+    so its weight on the first key is e^4 / (1 + e^4)."""
+    d = 4
+    Q = np.zeros((1, 1, 2, d))
+    K = np.zeros((1, 1, 2, d))
+    V = np.zeros((1, 1, 2, d))
+    V[0, 0, 0, 0] = 1.0
+    rk = np.zeros((3, 1, d))
+    rk[2, 0, 0] = 8.0  # t = 1 at row t + Lk - 1 = 2
+    uv = np.zeros((2, 1, d))
+    uv[1, 0, 0] = 1.0
+    out = orc.attention(orc.MODE_TXL, Q, K, V, rk, uv, causal=True)
+    assert abs(out[0, 0, 1, 0] - math.exp(4) / (1 + math.exp(4))) < 1e-12
+    assert abs(out[0, 0, 0, 0] - 1.0) < 1e-12  # the first query sees only its own key
+
+
+def check_sinusoid():
+    """R(0) alternates 0, 1; each (sin, cos) pair has unit norm, so
+    |R(t)|^2 = d / 2; R(t) . R(t + delta) does not depend on t (the dot
+    product of two encodings depends only on their offset difference)."""
+    d = 16
+    assert np.array_equal(orc.sinusoid(0, d), np.tile([0.0, 1.0], d // 2))
+    for t in (0, 3, 17, -250):
+        assert abs(orc.sinusoid(t, d) @ orc.sinusoid(t, d) - d / 2) < 1e-12
+    for delta in (1, 5, 40):
+        dots = [orc.sinusoid(t, d) @ orc.sinusoid(t + delta, d) for t in (-9, 0, 11, 1000)]
+        assert max(dots) - min(dots) < 1e-9
+    # the lowest frequency pair is (sin t, cos t); the highest has period 2 pi 10000^((d-2)/d)
+    assert abs(orc.sinusoid(1.0, d)[0] - math.sin(1.0)) < 1e-15
+    per = 2 * math.pi * 10000.0 ** ((d - 2) / d)
+    assert abs(orc.sinusoid(per, d)[d - 2]) < 1e-9 and abs(orc.sinusoid(per / 4, d)[d - 2] - 1) < 1e-9
+
+
 ALL_CHECKS = [
     check_t5_golden, check_t5_unused_bucket, check_t5_64_buckets, check_deberta_delta,
     check_shaw_index, check_skew_identity, check_shaw_logits_vs_skew,
@@ -681,7 +755,8 @@ ALL_CHECKS = [
     check_t5_backward_finite_differences, check_t5_backward_vs_autograd,
     check_t5_backward_invariants, check_t5_backward_unused_bucket,
     check_backward_finite_differences_all_modes, check_backward_zero_tables_vs_autograd,
-    check_backward_table_sums,
+    check_backward_table_sums, check_txl_reductions, check_txl_skew, check_txl_two_token,
+    check_sinusoid,
 ]
 
 

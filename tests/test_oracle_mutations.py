@@ -207,6 +207,39 @@ def _abwd_mutant(kind):
     return bwd
 
 
+_ORIG_TXL = orc.txl_logits
+_ORIG_SIN = orc.sinusoid
+
+
+def _txl_offset_sign(q, k, u_h, v_h, rk_h, p):
+    d, Lk = q.shape[-1], k.shape[0]
+    t = np.arange(Lk)[None, :] - p[:, None]  # key minus query
+    t = np.clip(t + Lk - 1, 0, rk_h.shape[0] - 1)
+    pos = np.einsum("id,ijd->ij", q + v_h[None, :], rk_h[t])
+    return ((q + u_h[None, :]) @ k.T + pos) / math.sqrt(d)
+
+
+def _txl_position_unscaled(q, k, u_h, v_h, rk_h, p):
+    d, Lk = q.shape[-1], k.shape[0]
+    t = p[:, None] - np.arange(Lk)[None, :]
+    pos = np.einsum("id,ijd->ij", q + v_h[None, :], rk_h[t + Lk - 1])
+    return (q + u_h[None, :]) @ k.T / math.sqrt(d) + pos
+
+
+def _sinusoid_swapped(t, d):
+    r = _ORIG_SIN(t, d)
+    return np.concatenate([r[1::2, None], r[0::2, None]], axis=1).reshape(-1)
+
+
+def _sinusoid_base_1000(t, d):
+    m = np.arange(d // 2)
+    w = 1000.0 ** (-2.0 * m / d)
+    out = np.empty(d)
+    out[0::2] = np.sin(t * w)
+    out[1::2] = np.cos(t * w)
+    return out
+
+
 MUTATIONS = {
     "t5_sign_flipped": ("t5_bucket", _flip_t5(_ORIG_T5)),
     "t5_offset_off_by_one": ("t5_bucket", _shift_t5(_ORIG_T5)),
@@ -243,6 +276,12 @@ MUTATIONS = {
     "bwd_deberta_dk_scale": ("attention_backward", _abwd_mutant("deberta_dk_scale_sqrt_d")),
     "bwd_deberta_tables_swapped": ("attention_backward", _abwd_mutant("deberta_tables_swapped")),
     "bwd_alibi_slope_sign": ("attention_backward", _abwd_mutant("alibi_slope_sign")),
+    "txl_offset_sign": ("txl_logits", _txl_offset_sign),
+    "txl_u_v_swapped": ("txl_logits", lambda q, k, u, v, r, p: _ORIG_TXL(q, k, v, u, r, p)),
+    "txl_no_u": ("txl_logits", lambda q, k, u, v, r, p: _ORIG_TXL(q, k, 0 * u, v, r, p)),
+    "txl_position_unscaled": ("txl_logits", _txl_position_unscaled),
+    "sinusoid_sin_cos_swapped": ("sinusoid", _sinusoid_swapped),
+    "sinusoid_base_1000": ("sinusoid", _sinusoid_base_1000),
 }
 _ORIG_KPOS = orc.t5_attention_key_positions
 _ORIG_ALIBI = orc.alibi_logits
