@@ -28,7 +28,7 @@ Conventions (readings where the pages leave a step open are marked R#):
 * Q, K, V are [B, H, L, d]; query row i sits at absolute position
   p = i + q_offset (R9: the same shift for every mode).
 * T5 and Shaw offsets are key minus query, rel = j - p ([RPE] T5, Shaw;
-  [T5B] "offset = key position - query position").
+  [T5B]: the offset is the key's position minus the query's).
 * DeBERTa offsets are query minus key, i - j ([DRP] relative position
   formula).
 * Scale: 1/sqrt(d) for T5 (R1: added bias after scaling) and Shaw (R7:
@@ -208,7 +208,7 @@ def t5_logits(q, k, bias_h, p, num_buckets, max_distance, causal):
 def shaw_logits(q, k, aK, p, kclip):
     """Scaled Shaw logits q_i . (k_j + a_K[clip(j - p_i)]) / sqrt(d).
 
-    [RPE] "Shaw et al.": the relative key term is formed the "workable"
+    [RPE] "Shaw et al.": the relative key term is formed the practical
     way -- Q times the 2k + 1 table (an L x (2k+1) matrix) gathered into the
     L x L layout by clipped offset.
     """
