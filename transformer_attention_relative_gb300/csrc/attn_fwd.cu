@@ -107,7 +107,7 @@ RP_DEVI void record_error(int* status) {
 // 128-row query tile whose key tiles are divided between the two softmax
 // warpgroups: a takes [0, na), b takes [na, n), and their partial softmax
 // states are merged when both are done. The last items of the list (the
-// shortest pairs) are split when that shortens the final round of the grid.
+// shortest pairs) are split when that shortens the grid's final pass.
 struct Item {
   int bh, h;
   int row0[2];       // first query row of tile a / b
@@ -175,18 +175,19 @@ RP_DEVI bool stream_uses(const Item& it, int x, int s) {
 // Field x of an item, selected without indexing (keeps the item in registers).
 RP_DEVI int sel(const int (&v)[2], int x) { return x ? v[1] : v[0]; }
 
-// The item a CTA takes in round r: items are ordered longest first. With
-// causal masking the CTAs sweep them in alternating directions (round 0 left
-// to right, round 1 right to left, ...) so that long and short items pair
-// up. Otherwise every item is equally long and every round goes left to
+// The item a CTA takes in its r-th pass over the grid (pass r covers items
+// r * grid ... r * grid + grid - 1): items are ordered longest first. With
+// causal masking the CTAs sweep them in alternating directions (pass 0 left
+// to right, pass 1 right to left, ...) so that long and short items pair
+// up. Otherwise every item is equally long and every pass goes left to
 // right: CTAs are dispatched in index order, so the lowest indices start
-// first and those take the extra items of a final partial round.
+// first and those take the extra items of a final partial pass.
 RP_DEVI int item_at(int r, bool snake) {
   const int g = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
   return r * g + ((snake && (r & 1)) ? g - 1 - c : c);
 }
 
-// Head of the first item from round r on in which query tile x has key tiles,
+// Head of the first item from pass r on in which query tile x has key tiles,
 // or -1.
 template <bool SPLIT>
 RP_DEVI int next_head(const FwdParams& p, int x, int r, int nitems) {
@@ -1166,11 +1167,11 @@ uint32_t fwd_max_smem_bytes() { return 232448u; }
 
 int fwd_num_items(const FwdParams& p) { return p.B * p.H * p.npairs + p.nsplit; }
 
-// The grid runs ceil(items / num_sms) rounds. When the pair items left for the
-// last round fill at most half the grid, running each as two split items
-// (half the key tiles per softmax warpgroup) halves that round. This holds
+// The grid runs ceil(items / num_sms) passes. When the pair items left for the
+// last pass fill at most half the grid, running each as two split items
+// (half the key tiles per softmax warpgroup) halves that pass. This holds
 // when every pair costs the same (no causal mask; causal items are ordered
-// longest first, so the last round's are the shortest and splitting them
+// longest first, so the last pass's are the shortest and splitting them
 // only unbalances the grid). A converted pair must hold two query tiles; the
 // tail holds the lowest pair rows, and the highest converted row is checked.
 int fwd_split_items(int npair_items, int BH, int Lq, int causal, int num_sms) {
