@@ -398,8 +398,8 @@ class BwdRun(GpuRun):
 def bwd_flops(w):
     """Algorithmic flops of the T5 backward: the four gradient products
     (dV = P^T dO, dP = dO V^T, dQ = dS K, dK = dS^T Q) over the visible
-    (query, key) pairs, twice the forward's two products; the recomputation
-    of S is not counted."""
+    (query, key) pairs, twice the forward's two products; the kernels'
+    extra recomputations of S and dP are not counted."""
     return 2.0 * w.flops()
 
 
