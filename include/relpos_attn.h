@@ -1,8 +1,9 @@
 /*
  * relpos_attn.h -- C ABI of the GB300 (sm_103a) relative-position attention
- * forward library (librelpos_attn.so).
+ * library (librelpos_attn.so): the forward pass, the T5 cached decode and the
+ * T5 backward pass (relpos_t5_attn_bwd, at the end of this header).
  *
- * One call computes multi-head attention whose logits carry a relative-
+ * One forward call computes multi-head attention whose logits carry a relative-
  * position term that is formed inside the kernel and never written to
  * device memory as an L x L (or L x L x d) tensor:
  *
