@@ -310,7 +310,7 @@ def txl_logits(q, k, u_h, v_h, rk_h, p):
 
 def attention(mode: int, Q, K, V, table0, table1=None, *, num_buckets: int = 32,
               rel_param: int = 128, causal: bool = False, q_offset: int = 0,
-              rows=None, heads=None) -> np.ndarray:
+              rows=None, heads=None, lengths=None) -> np.ndarray:
     """Forward relative-position attention in fp64.
 
     Q [B,H,Lq,d], K/V [B,H,Lk,d]. Tables: T5 bias [num_buckets, H];
@@ -321,6 +321,10 @@ def attention(mode: int, Q, K, V, table0, table1=None, *, num_buckets: int = 32,
     ``rows`` limits the
     computation to some query rows (the result then has len(rows) rows);
     ``heads`` to some (b, h) pairs (result [len(heads), rows, d]).
+    ``lengths`` [B] (R19) right-pads a batch of shorter sequences: batch
+    element b holds lengths[b] valid query rows and keys; keys from
+    lengths[b] on are masked for every row, and the padded query rows
+    (i >= lengths[b]) give zero rows.
     Returns [B, H, rows, d] (or the ``heads`` form) in float64.
 
     out_i = sum_j softmax_j(logit_ij) * v_j, plus for Shaw the value term
@@ -350,7 +354,12 @@ def attention(mode: int, Q, K, V, table0, table1=None, *, num_buckets: int = 32,
             lg = txl_logits(q, k, t1[0, h], t1[1, h], t0[:, h, :], p)
         else:
             lg = deberta_logits(q, k, t0[:, h, :], t1[:, h, :], p, rel_param)
-        w = _softmax_rows(_mask(lg, p, Lk, causal))
+        lg = _mask(lg, p, Lk, causal)
+        if lengths is not None:
+            n_b = int(lengths[b])
+            lg = np.where(np.arange(Lk)[None, :] >= n_b, -np.inf, lg)
+            lg = np.where((rows >= n_b)[:, None], -np.inf, lg)
+        w = _softmax_rows(lg)
         o = w @ v
         if mode == MODE_SHAW:
             o = o + shaw_value_term(w, p, t1, rel_param)

@@ -744,6 +744,31 @@ def check_sinusoid():
     assert abs(orc.sinusoid(per, d)[d - 2]) < 1e-9 and abs(orc.sinusoid(per / 4, d)[d - 2] - 1) < 1e-9
 
 
+# ---------------------------------------------------------------- padded batches
+
+def check_padded_batch_is_each_sequence_alone():
+    """R19: a right-padded batch gives, for every element, what that
+    sequence alone (its first lengths[b] rows and keys, nothing padded)
+    gives, and zero rows in the padding, in every mode, with and without
+    causal masking; the padded rows and keys may hold anything."""
+    rng = _rng(110)
+    B, H, L, d = 3, 2, 9, 4
+    lengths = [9, 5, 1]
+    Q, K, V = (rng.standard_normal((B, H, L, d)) for _ in range(3))
+    tabs = {orc.MODE_T5: (rng.standard_normal((32, H)), None, 128),
+            orc.MODE_SHAW: (rng.standard_normal((7, d)), rng.standard_normal((7, d)), 3),
+            orc.MODE_DEBERTA: (rng.standard_normal((6, H, d)), rng.standard_normal((6, H, d)), 3),
+            orc.MODE_ALIBI: (np.array([0.2, 0.9]), None, 0)}
+    for mode, (t0, t1, rp_) in tabs.items():
+        for causal in (False, True):
+            got = orc.attention(mode, Q, K, V, t0, t1, rel_param=rp_, causal=causal, lengths=lengths)
+            for b, n in enumerate(lengths):
+                alone = orc.attention(mode, Q[b:b + 1, :, :n], K[b:b + 1, :, :n], V[b:b + 1, :, :n],
+                                      t0, t1, rel_param=rp_, causal=causal)
+                assert np.max(np.abs(got[b, :, :n] - alone[0])) < 1e-12, (mode, causal, b)
+                assert np.all(got[b, :, n:] == 0.0)
+
+
 ALL_CHECKS = [
     check_t5_golden, check_t5_unused_bucket, check_t5_64_buckets, check_deberta_delta,
     check_shaw_index, check_skew_identity, check_shaw_logits_vs_skew,
@@ -756,7 +781,7 @@ ALL_CHECKS = [
     check_t5_backward_invariants, check_t5_backward_unused_bucket,
     check_backward_finite_differences_all_modes, check_backward_zero_tables_vs_autograd,
     check_backward_table_sums, check_txl_reductions, check_txl_skew, check_txl_two_token,
-    check_sinusoid,
+    check_sinusoid, check_padded_batch_is_each_sequence_alone,
 ]
 
 

@@ -240,6 +240,16 @@ def _sinusoid_base_1000(t, d):
     return out
 
 
+_ORIG_ATT = orc.attention
+
+
+def _lengths_off_by_one(mode, Q, K, V, t0, t1=None, **kw):
+    if kw.get("lengths") is not None:
+        kw = dict(kw)
+        kw["lengths"] = [n + 1 for n in kw["lengths"]]  # one padded key still visible
+    return _ORIG_ATT(mode, Q, K, V, t0, t1, **kw)
+
+
 MUTATIONS = {
     "t5_sign_flipped": ("t5_bucket", _flip_t5(_ORIG_T5)),
     "t5_offset_off_by_one": ("t5_bucket", _shift_t5(_ORIG_T5)),
@@ -282,6 +292,7 @@ MUTATIONS = {
     "txl_position_unscaled": ("txl_logits", _txl_position_unscaled),
     "sinusoid_sin_cos_swapped": ("sinusoid", _sinusoid_swapped),
     "sinusoid_base_1000": ("sinusoid", _sinusoid_base_1000),
+    "padding_mask_off_by_one": ("attention", _lengths_off_by_one),
 }
 _ORIG_KPOS = orc.t5_attention_key_positions
 _ORIG_ALIBI = orc.alibi_logits
