@@ -308,6 +308,25 @@ def txl_logits(q, k, u_h, v_h, rk_h, p):
     return ((q + u_h[None, :]) @ k.T + pos) / math.sqrt(d)
 
 
+def txl_position_table(W_kr, Lq: int, Lk: int, q_offset: int = 0) -> np.ndarray:
+    """The key-projected encodings r(t) = W_KR R(t) of every offset a call
+    reaches, per head.
+
+    [RPE] "Transformer-XL: four terms and two global biases": term (b) dots
+    q_i with W_KR R(i - j), R the fixed sinusoidal encoding of the offset and
+    W_KR its own key projection. ``W_kr`` [H, d, d] holds one projection per
+    head (output index first: r[e] = sum_f W_kr[h, e, f] R(t)[f]). Returns
+    r [Lk + Lq - 1 + q_offset, H, d] with r(t) at row t + Lk - 1 for
+    t = -(Lk - 1) ... Lq - 1 + q_offset (query minus key position), the
+    table ``attention(MODE_TXL, ...)`` takes.
+    """
+    W = np.asarray(W_kr, dtype=np.float64)
+    H, d, d_r = W.shape
+    ts = np.arange(-(Lk - 1), Lq + q_offset)
+    R = np.stack([sinusoid(t, d_r) for t in ts])        # [n, d_r]
+    return np.einsum("hef,nf->nhe", W, R)
+
+
 def attention(mode: int, Q, K, V, table0, table1=None, *, num_buckets: int = 32,
               rel_param: int = 128, causal: bool = False, q_offset: int = 0,
               rows=None, heads=None, lengths=None) -> np.ndarray:

@@ -744,6 +744,29 @@ def check_sinusoid():
     assert abs(orc.sinusoid(per, d)[d - 2]) < 1e-9 and abs(orc.sinusoid(per / 4, d)[d - 2] - 1) < 1e-9
 
 
+def check_txl_position_table():
+    """r(t) = W_KR R(t) per head at row t + Lk - 1: with W the identity the
+    rows are the sinusoid itself, first row t = -(Lk - 1), last row
+    t = Lq - 1 + q_offset; a W with the single entry W[h, e, f] = 1 puts
+    R(t)[f] in r[e] of head h and nothing elsewhere (the projection's
+    output index comes first)."""
+    H, d, Lq, Lk, qoff = 2, 8, 3, 5, 4
+    eye = np.broadcast_to(np.eye(d), (H, d, d))
+    r = orc.txl_position_table(eye, Lq, Lk, qoff)
+    assert r.shape == (Lk + Lq - 1 + qoff, H, d)
+    for row, t in ((0, -(Lk - 1)), (Lk - 1, 0), (r.shape[0] - 1, Lq - 1 + qoff)):
+        for h in range(H):
+            assert np.max(np.abs(r[row, h] - orc.sinusoid(t, d))) < 1e-15
+    W = np.zeros((H, d, d))
+    W[1, 2, 5] = 1.0
+    r = orc.txl_position_table(W, Lq, Lk, qoff)
+    for row in range(r.shape[0]):
+        t = row - (Lk - 1)
+        assert abs(r[row, 1, 2] - orc.sinusoid(t, d)[5]) < 1e-15
+    r[:, 1, 2] = 0.0
+    assert np.all(r == 0.0)
+
+
 # ---------------------------------------------------------------- padded batches
 
 def check_padded_batch_is_each_sequence_alone():
@@ -781,7 +804,7 @@ ALL_CHECKS = [
     check_t5_backward_invariants, check_t5_backward_unused_bucket,
     check_backward_finite_differences_all_modes, check_backward_zero_tables_vs_autograd,
     check_backward_table_sums, check_txl_reductions, check_txl_skew, check_txl_two_token,
-    check_sinusoid, check_padded_batch_is_each_sequence_alone,
+    check_sinusoid, check_txl_position_table, check_padded_batch_is_each_sequence_alone,
 ]
 
 

@@ -240,6 +240,18 @@ def _sinusoid_base_1000(t, d):
     return out
 
 
+_ORIG_TXL_TAB = orc.txl_position_table
+
+
+def _txl_table_transposed(W_kr, Lq, Lk, q_offset=0):
+    return _ORIG_TXL_TAB(np.swapaxes(np.asarray(W_kr), 1, 2), Lq, Lk, q_offset)
+
+
+def _txl_table_row_shift(W_kr, Lq, Lk, q_offset=0):
+    r = _ORIG_TXL_TAB(W_kr, Lq, Lk, q_offset + 1)
+    return r[1:]  # row n holds r(t + 1)
+
+
 _ORIG_ATT = orc.attention
 
 
@@ -293,6 +305,8 @@ MUTATIONS = {
     "sinusoid_sin_cos_swapped": ("sinusoid", _sinusoid_swapped),
     "sinusoid_base_1000": ("sinusoid", _sinusoid_base_1000),
     "padding_mask_off_by_one": ("attention", _lengths_off_by_one),
+    "txl_table_transposed": ("txl_position_table", _txl_table_transposed),
+    "txl_table_row_shift": ("txl_position_table", _txl_table_row_shift),
 }
 _ORIG_KPOS = orc.t5_attention_key_positions
 _ORIG_ALIBI = orc.alibi_logits
