@@ -2,12 +2,16 @@
 """Benchmark of the relative-position attention forward on GB300.
 
 One step = one forward (relpos_attn_fwd through the C ABI) over one batch of
-the workload. Default workload: the T5-base-shaped encoder (B=8, H=12,
-L=512, d=64, bf16, bidirectional buckets 32 / max distance 128). Prints one
-JSON line (rank 0).
+the workload. Default workload: the largest configuration, Shaw clipped
+relative keys and values (B=4, H=8, L=4096, d=64, bf16, k=16). Prints one
+JSON line (rank 0): the headline workload's numbers at the top level, and a
+block of the same form (value, roofline of its dominant kernel, e2e through
+the C ABI with host buffers, the fp64 CPU oracle on a bounded sample, clocks)
+for every other configuration under "workloads", each timed as long as the
+headline, plus the T5 backward.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                    [--impl ours|reference] [--no-others]
+                    [--impl ours|reference] [--no-others] [--seconds S]
 
 Timing: W untimed steps, then K steps bracketed by a barrier and a device
 synchronize, timed with CUDA events on the launching stream; the K steps are
@@ -43,8 +47,9 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from transformer_attention_relative_gb300.workloads import (MODE_NAMES, MODE_T5,  # noqa: E402
-                                                            WORKLOADS, make_grad_output, make_inputs)
+from transformer_attention_relative_gb300.workloads import (MODE_DEBERTA, MODE_NAMES,  # noqa: E402
+                                                            MODE_T5, MODE_TXL, WORKLOADS,
+                                                            make_grad_output, make_inputs)
 
 L2_BYTES = 129 * 1024 * 1024
 METRIC = "rel-pos attention fwd TFLOP/s (bf16) and % of GB300 dense BF16 peak"
@@ -186,15 +191,22 @@ class ClockSampler:
                 "samples": len(win)}
 
 
-def kernels_per_step(w):
+def kernels_per_step(w, backward=False):
+    """This library's kernels launched by one call (memsets not counted)."""
+    if backward:
+        return 2
     decode = w.mode == MODE_T5 and w.Lq <= 8
     n = 2 if decode else 1
+    if w.mode in (MODE_DEBERTA, MODE_TXL):
+        n += 1  # the band / operand pre-pass
     if w.dtype == "fp32":
         n += 3
     return n
 
 
-def dominant_kernel(w):
+def dominant_kernel(w, backward=False):
+    if backward:
+        return "relpos_bwd_dkdv_kernel", "tensor"
     if w.mode == MODE_T5 and w.Lq <= 8:
         return "relpos_decode_partial_kernel", "hbm"
     return "relpos_fwd_kernel", "tensor"
@@ -403,27 +415,19 @@ def bwd_flops(w):
     return 2.0 * w.flops()
 
 
-def measure_workload(w, device, stream, steps, warmup, barrier):
-    g = GpuRun(w, device, stream)
-    ms, t0, t1 = g.timed(steps, warmup, barrier)
-    return g, ms, t0, t1
-
-
 def cpu_baseline(w, budget_s=12.0):
     """Time the fp64 oracle on the host cores over a bounded sample of the
     workload: whole (batch, head) units, as many as fit in about budget_s."""
-    import numpy as np
     from oracle import relpos_oracle as orc
     x = make_inputs(w)
     Q, K, V = (x[k].double().numpy() for k in ("Q", "K", "V"))
     t0 = x["table0"].double().numpy()
     t1 = x["table1"].double().numpy() if x["table1"] is not None else None
-    heads = [(b, h) for b in range(w.B) for h in range(w.H)]
-    # rows per unit: whole heads unless one head alone is too slow
-    rows = None
     start = time.perf_counter()
+    if w.mode == MODE_TXL:  # the oracle takes the projected encodings r(t) = W R(t)
+        t0 = orc.txl_position_table(t0, w.Lq, w.Lk, w.q_offset)
+    heads = [(b, h) for b in range(w.B) for h in range(w.H)]
     done = 0
-    n_rows_total = 0
     for (b, h) in heads:
         if w.cache_len:
             kp = x["key_pos"].numpy()
@@ -433,16 +437,15 @@ def cpu_baseline(w, budget_s=12.0):
                                            causal=w.causal, q_offset=w.q_offset)
         else:
             orc.attention(w.mode, Q, K, V, t0, t1, num_buckets=w.num_buckets, rel_param=w.rel_param,
-                          causal=w.causal, q_offset=w.q_offset, rows=rows, heads=[(b, h)])
+                          causal=w.causal, q_offset=w.q_offset, heads=[(b, h)])
         done += 1
-        n_rows_total += w.Lq if rows is None else len(rows)
         if time.perf_counter() - start > budget_s:
             break
     el = time.perf_counter() - start
     frac = done / len(heads)
-    flops = w.flops() * frac
-    cores = len(os.sched_getaffinity(0))
-    threads = cores
+    hbm = dominant_kernel(w)[1] == "hbm"
+    work = (w.min_bytes() if hbm else w.flops()) * frac
+    threads = len(os.sched_getaffinity(0))
     try:
         from threadpoolctl import threadpool_info
         info = threadpool_info()
@@ -450,9 +453,10 @@ def cpu_baseline(w, budget_s=12.0):
             threads = max(i.get("num_threads", 1) for i in info)
     except Exception:
         pass
-    return {"value": flops / el / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+    value = work / el / (1e9 if hbm else 1e12)
+    return {"value": value, "unit": "GB/s" if hbm else "TFLOP/s", "cores": threads, "kind": "oracle",
             "sample": f"{done} of {len(heads)} (batch, head) units of {w.name}, all rows, "
-                      f"fp64 numpy, {el:.1f} s"}, el, flops
+                      f"fp64 numpy, {el:.1f} s"}, el, work
 
 
 # ---------------------------------------------------------------- main
@@ -476,15 +480,105 @@ def job_value(flops_per_step, steps, world, ms_max):
     return flops_per_step * steps * world / (ms_max / 1e3) / 1e12
 
 
+def metric_of(w, backward=False):
+    """(metric, unit, work per step, scale to the unit) of a workload."""
+    if backward:
+        return ("rel-pos attention bwd TFLOP/s (bf16): dQ, dK, dV and the table gradient",
+                "TFLOP/s", bwd_flops(w), 1e12)
+    if dominant_kernel(w)[1] == "hbm":
+        return ("rel-pos attention cached-decode GB/s (bf16) and % of GB300 HBM bandwidth",
+                "GB/s", float(w.min_bytes()), 1e9)
+    return METRIC, "TFLOP/s", w.flops(), 1e12
+
+
+def measure_block(w, device, stream, peaks, peak_src, sampler, barrier, world, *, steps=None,
+                  warmup=5, seconds=2.0, cpu_budget=0.0, backward=False):
+    """Time one workload and return its block: value, ms_per_step, roofline
+    of the dominant kernel, e2e through the C ABI with host buffers, clocks
+    during the timed region and, with cpu_budget > 0, the CPU oracle."""
+    import torch
+    g = BwdRun(w, device, stream) if backward else GpuRun(w, device, stream)
+    for i in range(max(3, warmup)):
+        g.step(i)
+    torch.cuda.synchronize()
+    n_est = g.nsets * max(1, math.ceil(32 / g.nsets))
+    ms_est, _, _ = g.timed(n_est, 1, lambda: None)
+    t_est = ms_est / n_est / 1e3
+    if steps is None:
+        steps = max(20, min(200000, int(seconds / t_est)))
+    warmup = max(3, warmup)
+    ms, t0, t1 = g.timed(steps, warmup, barrier)
+    clocks = sampler.summary(t0 - 0.05, t1 + 0.05)
+    window = "timed region"
+    if clocks is None:
+        a, b = g.sustain(1.0)
+        clocks = sampler.summary(a, b)
+        window = "1 s of the same steps right after the timed region (timed region too short)"
+    if clocks is not None:
+        clocks["window"] = window
+    ms_max = max_over_ranks(ms, world)
+    metric, unit, work, scale = metric_of(w, backward)
+    value = work * steps * world / (ms_max / 1e3) / scale
+    kname, bound = dominant_kernel(w, backward)
+    avg_s = ms / steps / 1e3
+    achieved = work / avg_s / scale
+    peak = peaks["bf16_tflops"] if bound == "tensor" else peaks["hbm_gbs"]
+    roofline = {"bound": bound, "kernel": kname, "achieved": achieved, "peak": peak, "unit": unit,
+                "frac": achieved / peak, "traffic": stored_traffic(kname, w.name + ("_backward" if backward else "")),
+                "kernel_hash": kernel_hash(kname),
+                "peak_source": f"{peak_src} ({'bf16_tflops burst' if bound == 'tensor' else 'hbm_gbs'})",
+                "algorithmic_per_launch": work,
+                "timed_as": "whole step (every kernel of the call) / steps"}
+    if kernels_per_step(w, backward) > 1:
+        roofline["note"] = (f"{kernels_per_step(w, backward)} kernels per step: achieved divides by "
+                            "the whole step's time, a lower bound for the dominant kernel alone")
+    e2e_steps = max(3, min(steps, 50))
+    e2e_ms, h2d, d2h = g.e2e(e2e_steps, 2)
+    block = {"metric": metric, "value": value, "unit": unit, "steps": steps, "warmup": warmup,
+             "ms_per_step": ms_max / steps, "higher_is_better": True,
+             "config": config_of(w, world, g, backward), "roofline": roofline,
+             "e2e": {"value": work * e2e_steps / (e2e_ms / 1e3) / scale, "unit": unit,
+                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+             "gpu_launches": steps * kernels_per_step(w, backward), "clocks": clocks}
+    if cpu_budget > 0 and not backward:
+        block["cpu_baseline"], _, _ = cpu_baseline(w, budget_s=cpu_budget)
+    del g
+    torch.cuda.empty_cache()
+    return block
+
+
+def config_of(w, world, g, backward=False):
+    c = {"workload": w.name + ("_backward" if backward else ""), "mode": MODE_NAMES[w.mode],
+         "B": w.B, "H": w.H, "Lq": w.Lq, "Lk": w.Lk, "d": w.d, "causal": w.causal,
+         "q_offset": w.q_offset, "parallelism": f"replicas x{world}",
+         "l2": f"{g.nsets} rotating input sets of {g.set_bytes / 1e6:.1f} MB "
+               f"(> 129 MB L2), no flush"}
+    if w.mode == MODE_T5:
+        c["num_buckets"] = w.num_buckets
+    if w.rel_param:
+        c["rel_param"] = w.rel_param
+    if w.cache_len:
+        c["cache_len"] = w.cache_len
+    return c
+
+
+# every configuration gets a block of its own in the bench line
+BLOCK_WORKLOADS = ("t5_base_bidir", "t5_causal", "shaw", "deberta", "txl_mem", "t5_decode",
+                   "t5_decode_evicted", "alibi_bidir", "alibi_causal", "t5_tiny_fp32")
+BACKWARD_WORKLOADS = ("t5_base_bidir", "t5_causal")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="t5_base_bidir", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default="shaw", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-others", action="store_true",
-                    help="skip the per-workload summary of the other workloads")
+                    help="time the headline workload only")
+    ap.add_argument("--seconds", type=float, default=2.0,
+                    help="timed region per workload when --steps is not given")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     args = ap.parse_args()
@@ -502,23 +596,24 @@ def main():
         warm = min(args.warmup, 1)
         for _ in range(warm):
             cpu_baseline(w, budget_s=2.0)
-        tot_flops, tot_s = 0.0, 0.0
+        tot_work, tot_s = 0.0, 0.0
         last = None
         for _ in range(steps):
-            cb, el, fl = cpu_baseline(w, budget_s=args.cpu_budget / max(1, steps))
-            tot_flops += fl
+            cb, el, work = cpu_baseline(w, budget_s=args.cpu_budget / max(1, steps))
+            tot_work += work
             tot_s += el
             last = cb
-        val = tot_flops / tot_s / 1e12
+        metric, unit, _, scale = metric_of(w)
+        val = tot_work / tot_s / scale
         last["value"] = val
-        line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s",
+        line = {"impl": "reference", "metric": metric, "value": val, "unit": unit,
                 "n_gpus": args.gpus, "steps": steps, "warmup": warm,
                 "ms_per_step": 1e3 * tot_s / steps, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "f64", "data": "synthetic",
                 "config": {"workload": w.name, "mode": MODE_NAMES[w.mode], "B": w.B, "H": w.H,
                            "Lq": w.Lq, "Lk": w.Lk, "d": w.d},
                 "cpu_baseline": last,
-                "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "e2e": {"value": val, "unit": unit, "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
         return
@@ -541,117 +636,42 @@ def main():
     sampler.start()
     time.sleep(0.3)
 
-    # pick K so that the default timed region lasts about 2 s
-    g = GpuRun(w, device, stream)
-    for i in range(max(3, args.warmup)):
-        g.step(i)
-    torch.cuda.synchronize()
-    ms_est, _, _ = g.timed(g.nsets * max(1, math.ceil(32 / g.nsets)), 1, lambda: None)
-    t_est = ms_est / (g.nsets * max(1, math.ceil(32 / g.nsets))) / 1e3
-    steps = args.steps if args.steps is not None else max(20, min(200000, int(2.0 / t_est)))
-    warmup = max(3, args.warmup)
-
-    ms, t0, t1 = g.timed(steps, warmup, barrier)
-    clocks = sampler.summary(t0 - 0.05, t1 + 0.05)
-    window = "timed region"
-    if clocks is None:
-        a, b = g.sustain(1.5)
-        clocks = sampler.summary(a, b)
-        window = "1.5 s of the same steps right after the timed region (timed region too short)"
-    if clocks is not None:
-        clocks["window"] = window
-
-    # max over ranks
-    ms_max = max_over_ranks(ms, world)
-    ms_step = ms_max / steps
-    flops = w.flops()
-    value = job_value(flops, steps, world, ms_max)
-
-    kname, bound = dominant_kernel(w)
-    avg_s = ms / steps / 1e3
-    if bound == "tensor":
-        achieved = flops / avg_s / 1e12
-        peak = peaks["bf16_tflops"]
-        unit = "TFLOP/s"
-        traffic = stored_traffic(kname, w.name)
-    else:
-        achieved = w.min_bytes() / avg_s / 1e9
-        peak = peaks["hbm_gbs"]
-        unit = "GB/s"
-        traffic = stored_traffic(kname, w.name)
-    roofline = {"bound": bound, "kernel": kname, "achieved": achieved, "peak": peak, "unit": unit,
-                "frac": achieved / peak, "traffic": traffic, "kernel_hash": kernel_hash(kname),
-                "peak_source": f"{peak_src} ({'bf16_tflops burst' if bound == 'tensor' else 'hbm_gbs'})",
-                "algorithmic_per_launch": flops if bound == "tensor" else w.min_bytes()}
-
-    e2e_ms, h2d, d2h = g.e2e(max(3, min(steps, 50)), 2)
-    e2e_steps = max(3, min(steps, 50))
-    e2e_val = flops * e2e_steps / (e2e_ms / 1e3) / 1e12
-
-    others = {}
+    cpu_on = rank == 0 and world == 1 and not args.no_cpu
+    head = measure_block(w, device, stream, peaks, peak_src, sampler, barrier, world,
+                         steps=args.steps, warmup=args.warmup, seconds=args.seconds,
+                         cpu_budget=args.cpu_budget if cpu_on else 0.0)
+    blocks = {}
     if not args.no_others and rank == 0:
-        for name in ("t5_causal", "t5_decode", "t5_decode_evicted", "shaw", "t5_tiny_fp32", "deberta",
-                     "alibi_bidir", "alibi_causal"):
+        for name in BLOCK_WORKLOADS:
             if name == w.name:
                 continue
-            ow = WORKLOADS[name]
             try:
-                og = GpuRun(ow, device, stream)
-                k = 50
-                oms, _, _ = og.timed(k, 5, lambda: None)
-                per = oms / k / 1e3
-                kn, bd = dominant_kernel(ow)
-                ent = {"ms_per_step": oms / k, "tflops": ow.flops() / per / 1e12,
-                       "frac_of_bf16_peak": ow.flops() / per / 1e12 / peaks["bf16_tflops"]}
-                if bd == "hbm":
-                    ent["gbs"] = ow.min_bytes() / per / 1e9
-                    ent["frac_of_hbm_peak"] = ent["gbs"] / peaks["hbm_gbs"]
-                others[name] = ent
-                del og
-                torch.cuda.empty_cache()
-            except Exception as e:  # a mode this build does not run yet
-                others[name] = {"unavailable": str(e)[:120]}
-        for name in ("t5_base_bidir", "t5_causal"):
-            ow = WORKLOADS[name]
+                blocks[name] = measure_block(WORKLOADS[name], device, stream, peaks, peak_src, sampler,
+                                             lambda: None, 1, steps=args.steps, warmup=args.warmup,
+                                             seconds=args.seconds,
+                                             cpu_budget=min(5.0, args.cpu_budget) if cpu_on else 0.0)
+            except Exception as e:  # a configuration this build does not run
+                blocks[name] = {"unavailable": str(e)[:160]}
+        for name in BACKWARD_WORKLOADS:
             try:
-                og = BwdRun(ow, device, stream)
-                k = 30
-                oms, _, _ = og.timed(k, 3, lambda: None)
-                per = oms / k / 1e3
-                tf = bwd_flops(ow) / per / 1e12
-                others[name + "_backward"] = {"ms_per_step": oms / k, "tflops": tf,
-                                              "frac_of_bf16_peak": tf / peaks["bf16_tflops"]}
-                del og
-                torch.cuda.empty_cache()
+                blocks[name + "_backward"] = measure_block(
+                    WORKLOADS[name], device, stream, peaks, peak_src, sampler, lambda: None, 1,
+                    steps=args.steps, warmup=args.warmup, seconds=args.seconds, backward=True)
             except Exception as e:
-                others[name + "_backward"] = {"unavailable": str(e)[:120]}
-
+                blocks[name + "_backward"] = {"unavailable": str(e)[:160]}
     sampler.stop()
-
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu:
-        cpu, _, _ = cpu_baseline(w, budget_s=args.cpu_budget)
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
-            "steps": steps, "warmup": warmup, "ms_per_step": ms_step, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": w.name, "mode": MODE_NAMES[w.mode], "B": w.B, "H": w.H,
-                       "Lq": w.Lq, "Lk": w.Lk, "d": w.d, "num_buckets": w.num_buckets,
-                       "rel_param": w.rel_param, "causal": w.causal, "q_offset": w.q_offset,
-                       "parallelism": f"replicas x{world}",
-                       "l2": f"{g.nsets} rotating input sets of {g.set_bytes / 1e6:.1f} MB "
-                             f"(> 129 MB L2), no flush"},
-            "frac_of_peak": value / world / peaks["bf16_tflops"],
-            "roofline": roofline,
-            "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h},
-            "gpu_launches": steps * kernels_per_step(w),
-            "clocks": clocks,
-            "cpu_baseline": cpu,
-            "source_hash": source_hash(),
-            "other_workloads": others,
+            "metric": head["metric"], "value": head["value"], "unit": head["unit"], "n_gpus": world,
+            "steps": head["steps"], "warmup": head["warmup"], "ms_per_step": head["ms_per_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": head["config"],
+            "frac_of_peak": head["value"] / world / (peaks["bf16_tflops"] if head["unit"] == "TFLOP/s"
+                                                      else peaks["hbm_gbs"]),
+            "roofline": head["roofline"], "e2e": head["e2e"], "gpu_launches": head["gpu_launches"],
+            "clocks": head["clocks"], "cpu_baseline": head.get("cpu_baseline"),
+            "source_hash": source_hash(), "workloads": blocks,
         }
         print(json.dumps(line))
     if world > 1:

@@ -28,6 +28,14 @@
  *                  no maximum distance ("Relative Position Embeddings, in
  *                  depth", section "ALiBi and RoPE: the two endpoints").
  *                  logit = q.k / sqrt(d) - slope[h] * |j - p|
+ *   RELPOS_TXL     Transformer-XL: content and position keys with their own
+ *                  projections and two global biases u, v ("Relative
+ *                  Position Embeddings, in depth", section "Transformer-XL:
+ *                  four terms and two global biases").
+ *                  logit = ((q + u[h]).k_j + (q + v[h]).W[h] R(p - j)) / sqrt(d)
+ *                  with R(t) the fixed sinusoidal encoding of the offset
+ *                  t = query - key position: R[2m] = sin(w_m t),
+ *                  R[2m+1] = cos(w_m t), w_m = 10000^(-2m/d).
  *
  * Positions: query row i sits at absolute position p = i + q_offset; key
  * row j at position j. With causal = 1 keys j > p are masked out (and T5
@@ -55,6 +63,7 @@ extern "C" {
 #define RELPOS_SHAW 1
 #define RELPOS_DEBERTA 2
 #define RELPOS_ALIBI 3
+#define RELPOS_TXL 4
 
 /* element types of Q, K, V and out */
 #define RELPOS_BF16 0
@@ -72,7 +81,7 @@ extern "C" {
 /*
  * relpos_attn_fwd -- attention forward with an in-kernel relative term.
  *
- *   mode        RELPOS_T5, RELPOS_SHAW, RELPOS_DEBERTA or RELPOS_ALIBI.
+ *   mode        RELPOS_T5, RELPOS_SHAW, RELPOS_DEBERTA, RELPOS_ALIBI or RELPOS_TXL.
  *   dtype       RELPOS_BF16 or RELPOS_FP32: element type of Q, K, V and out.
  *               FP32 inputs are rounded to bf16 on the device before the
  *               tensor-core products (fp32 accumulation); out is fp32.
@@ -86,6 +95,12 @@ extern "C" {
  *                          (already projected per head).
  *                 ALiBi:   table0 = slopes [H] fp32 (any values the caller
  *                          chooses); table1 unused.
+ *                 TXL:     table0 = W [H, d, d] fp32, the key projection of
+ *                          the sinusoid per head, output index first
+ *                          (r[e] = sum_f W[h][e][f] R[f]); table1 = [2, H, d]
+ *                          fp32, u then v. Memory (cached keys of the
+ *                          previous segment) is ordinary keys at positions
+ *                          0 .. mem - 1 with q_offset = mem.
  *   B, H        batch and heads (>= 0; 0 makes the call a no-op).
  *   Lq, Lk      query and key lengths (Lq >= 0, Lk >= 0). Lk == 0 writes
  *               zeros.
@@ -93,7 +108,7 @@ extern "C" {
  *   num_buckets T5 only: even, 4 <= num_buckets <= 128 (ignored otherwise).
  *   rel_param   T5: max_distance (> num_buckets/4 bidirectional, > num_buckets/2
  *               causal); Shaw: clip k (1 <= k <= 64); DeBERTa: k (1 <= k <= 4096);
- *               ALiBi: ignored.
+ *               ALiBi, TXL: ignored.
  *               Shaw's per-row tables and T5's bias-by-offset table live in
  *               shared memory: this build runs Shaw k <= 21, and T5 as long as
  *               the distance at which the last bucket starts (about
@@ -106,7 +121,9 @@ extern "C" {
  *   out         device, [B, H, Lq, d], element type per dtype; written fully.
  *   stream      cudaStream_t.
  *
- * Scratch: calls with dtype FP32, with DeBERTa, or that take the split-key
+ * Scratch: calls with dtype FP32, with DeBERTa or TXL (the rows
+ * [q + u | W^T (q + v) rotated by the query's angles], 256 bytes per query
+ * row, and the keys' sinusoid table), or that take the split-key
  * decode path (few query rows) draw temporary device memory with
  * cudaMallocAsync on `stream` and release it with cudaFreeAsync before
  * returning. Nothing persists between calls.
@@ -128,6 +145,8 @@ int relpos_attn_fwd(int mode, int dtype, const void* Q, const void* K, const voi
  *   Shaw:    offsets are key - query; ids are clip(rel, -k, k) + k.
  *   DeBERTa: offsets are query - key; ids are delta = clip(rel, -k, k-1) + k.
  *   ALiBi:   offsets are key - query; ids are the distances |rel|.
+ *   TXL:     offsets are key - query; ids are t = query - key = -rel, the
+ *            argument of the sinusoidal encoding R(t).
  *   out_dev  device int32[n], written asynchronously on `stream`.
  * Parameter checks are those of relpos_attn_fwd.
  */

@@ -32,10 +32,21 @@ def run_gpu(w, x, out=None):
     return o
 
 
-def run_oracle(w, x, rows=None, heads=None):
+def oracle_tables(w, x):
+    """The oracle's tables for a workload's inputs: the library's own, except
+    Transformer-XL, whose library call takes the projection W and whose
+    oracle takes the projected encodings r(t) = W R(t) of every offset."""
+    t0 = x["table0"].double().numpy()
     t1 = x["table1"].double().numpy() if x["table1"] is not None else None
+    if w.mode == orc.MODE_TXL:
+        t0 = orc.txl_position_table(t0, w.Lq, w.Lk, w.q_offset)
+    return t0, t1
+
+
+def run_oracle(w, x, rows=None, heads=None):
+    t0, t1 = oracle_tables(w, x)
     return orc.attention(w.mode, x["Q"].double().numpy(), x["K"].double().numpy(),
-                         x["V"].double().numpy(), x["table0"].double().numpy(), t1,
+                         x["V"].double().numpy(), t0, t1,
                          num_buckets=w.num_buckets, rel_param=w.rel_param, causal=w.causal,
                          q_offset=w.q_offset, rows=rows, heads=heads)
 

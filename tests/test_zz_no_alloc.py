@@ -37,11 +37,13 @@ def _noalloc(w, d, out):
 
 
 def test_noalloc_matches_allocating_entry_point_twice_in_a_row():
-    """Two consecutive calls (different inputs, so the shared array is reused)
-    each match relpos_attn_fwd within the parity tolerance."""
+    """Two consecutive calls each match relpos_attn_fwd within the parity
+    tolerance. The small, ragged case runs first and the 16-chunk case
+    second, so the second call reads partials of the shared array that the
+    first call left behind wherever its own kernels fail to overwrite them."""
     base = WORKLOADS["t5_decode"]
-    cases = [base.replace(B=8, H=16),                                  # 4096 keys, 16 chunks
-             base.replace(B=4, H=8, Lq=3, Lk=1500, q_offset=2000)]     # ragged, several rows
+    cases = [base.replace(B=4, H=8, Lq=3, Lk=1500, q_offset=2000),    # ragged, several rows
+             base.replace(B=8, H=16)]                                  # 4096 keys, 16 chunks
     dev = torch.device("cuda")
     for k, w in enumerate(cases):
         x = make_inputs(w, seed=7000 + k)
@@ -55,6 +57,55 @@ def test_noalloc_matches_allocating_entry_point_twice_in_a_row():
         assert rp.check_status() == 0
         G.compare(got.float().cpu().double().numpy(), want.float().cpu().double().numpy(),
                   what=f"noalloc case {k}")
+
+
+def test_noalloc_matches_the_oracle():
+    """The no-allocation call against the fp64 oracle directly (not only
+    against the allocating call, which runs the same kernels), on a case with
+    keys on both sides of the query rows and on the causal decode shape."""
+    base = WORKLOADS["t5_decode"]
+    cases = [base.replace(B=2, H=4, Lq=5, Lk=900, q_offset=300, causal=False),
+             base.replace(B=2, H=16)]
+    dev = torch.device("cuda")
+    for k, w in enumerate(cases):
+        x = make_inputs(w, seed=7100 + k)
+        d = {n: (t.to(dev) if t is not None else None) for n, t in x.items()}
+        got = torch.full_like(d["Q"], float("nan"))
+        assert _noalloc(w, d, got) == rp.RELPOS_OK
+        torch.cuda.synchronize()
+        assert rp.check_status() == 0
+        G.compare(got.float().cpu().double().numpy(), G.run_oracle(w, x), what=f"noalloc vs oracle {k}")
+
+
+def test_noalloc_rejects_misaligned_tensors():
+    """The kernels read Q, K, V and write out in 16-byte vectors: a view that
+    starts one element in is refused on the host (nothing launches, out is
+    left as it was)."""
+    w = WORKLOADS["t5_decode"].replace(B=1, H=2, Lk=300, q_offset=299)
+    x = make_inputs(w, seed=7200)
+    dev = torch.device("cuda")
+    d = {n: (t.to(dev) if t is not None else None) for n, t in x.items()}
+    s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    out = torch.zeros(d["Q"].numel() + 8, dtype=torch.bfloat16, device=dev)
+    for bad in ("Q", "K", "V", "out"):
+        args = {}
+        for n in ("Q", "K", "V"):
+            buf = torch.zeros(d[n].numel() + 8, dtype=torch.bfloat16, device=dev)
+            buf[1:1 + d[n].numel()] = d[n].flatten() if n == bad else 0
+            args[n] = buf[1:] if n == bad else d[n]
+        o = out[1:] if bad == "out" else out
+        rc = rp.relpos_t5_decode_noalloc(_p(args["Q"]), _p(args["K"]), _p(args["V"]), _p(d["table0"]),
+                                         w.B, w.H, w.Lq, w.Lk, w.num_buckets, w.rel_param,
+                                         int(w.causal), w.q_offset, _p(o), s)
+        assert rc == rp.RELPOS_ERR_INVALID_ARG, bad
+        kp = torch.arange(w.Lk, dtype=torch.int32, device=dev).expand(w.B, w.H, w.Lk).contiguous()
+        rc = rp.relpos_t5_decode_positions(_p(args["Q"]), _p(args["K"]), _p(args["V"]),
+                                           _p(d["table0"]), _p(kp), w.B, w.H, w.Lq, w.Lk,
+                                           w.num_buckets, w.rel_param, int(w.causal), w.q_offset,
+                                           _p(o), s)
+        assert rc == rp.RELPOS_ERR_INVALID_ARG, bad
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(out).item() == 0
 
 
 def test_noalloc_rejects_requests_beyond_its_scratch():

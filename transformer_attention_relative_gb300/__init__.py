@@ -13,7 +13,7 @@ from __future__ import annotations
 import ctypes
 import os
 
-from .workloads import MODE_ALIBI, MODE_DEBERTA, MODE_SHAW, MODE_T5  # noqa: F401
+from .workloads import MODE_ALIBI, MODE_DEBERTA, MODE_SHAW, MODE_T5, MODE_TXL  # noqa: F401
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "librelpos_attn.so")

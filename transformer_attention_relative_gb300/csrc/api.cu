@@ -69,13 +69,15 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // [rows = L, inner = 64] bf16 per (batch*head) slab, 128-row x 64-col boxes,
 // 128-byte swizzle (the operand layout of the tensor-core descriptors).
-bool make_tmap(CUtensorMap* m, const void* base, int L, int BH) {
+// `inner` columns per row (64, or 128 for Transformer-XL's query rows, read
+// as two 64-column boxes).
+bool make_tmap(CUtensorMap* m, const void* base, int L, int BH, int inner = kHeadDim) {
   auto fn = encode_fn();
   if (!fn) return false;
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(L),
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(L),
                         static_cast<cuuint64_t>(BH)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim) * 2,
-                           static_cast<cuuint64_t>(L) * kHeadDim * 2};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner) * 2,
+                           static_cast<cuuint64_t>(L) * inner * 2};
   cuuint32_t box[3] = {static_cast<cuuint32_t>(kHeadDim), 128u, 1u};
   cuuint32_t estr[3] = {1u, 1u, 1u};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
@@ -145,15 +147,13 @@ int check_rel_params(int mode, int num_buckets, int rel_param, int causal) {
   } else if (mode == RELPOS_SHAW || mode == RELPOS_DEBERTA) {
     if (rel_param < 1) return RELPOS_ERR_INVALID_ARG;
     if (rel_param > (1 << 24)) return RELPOS_ERR_UNSUPPORTED;
-  } else if (mode != RELPOS_ALIBI) {
+  } else if (mode != RELPOS_ALIBI && mode != RELPOS_TXL) {
     return RELPOS_ERR_INVALID_ARG;
   }
   return RELPOS_OK;
 }
 
 namespace {
-
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 __global__ void index_ids_kernel(int mode, int n, int first, T5Index ix, int k, int* out) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
@@ -166,6 +166,8 @@ __global__ void index_ids_kernel(int mode, int n, int first, T5Index ix, int k, 
     id = shaw_index_dev(rel, k);
   else if (mode == RELPOS_ALIBI)
     id = rel < 0 ? -rel : rel;
+  else if (mode == RELPOS_TXL)
+    id = -rel;
   else
     id = deberta_delta_dev(rel, k);
   out[i] = id;
@@ -275,7 +277,8 @@ extern "C" int relpos_attn_fwd(int mode, int dtype, const void* Q, const void* K
                                const void* table0, const void* table1, int B, int H, int Lq, int Lk,
                                int d, int num_buckets, int rel_param, int causal, int q_offset,
                                void* out, void* stream) {
-  if (mode != RELPOS_T5 && mode != RELPOS_SHAW && mode != RELPOS_DEBERTA && mode != RELPOS_ALIBI)
+  if (mode != RELPOS_T5 && mode != RELPOS_SHAW && mode != RELPOS_DEBERTA && mode != RELPOS_ALIBI &&
+      mode != RELPOS_TXL)
     return RELPOS_ERR_INVALID_ARG;
   if (dtype != RELPOS_BF16 && dtype != RELPOS_FP32) return RELPOS_ERR_INVALID_ARG;
   if (B < 0 || H < 0 || Lq < 0 || Lk < 0 || q_offset < 0 || d <= 0) return RELPOS_ERR_INVALID_ARG;
@@ -294,7 +297,8 @@ extern "C" int relpos_attn_fwd(int mode, int dtype, const void* Q, const void* K
                                                                                  : RELPOS_ERR_CUDA;
   }
   if (!K || !V || !table0) return RELPOS_ERR_INVALID_ARG;
-  if ((mode == RELPOS_SHAW || mode == RELPOS_DEBERTA) && !table1) return RELPOS_ERR_INVALID_ARG;
+  if ((mode == RELPOS_SHAW || mode == RELPOS_DEBERTA || mode == RELPOS_TXL) && !table1)
+    return RELPOS_ERR_INVALID_ARG;
   if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(out) || !aligned16(table0) ||
       (table1 && !aligned16(table1)))
     return RELPOS_ERR_INVALID_ARG;
@@ -327,8 +331,6 @@ extern "C" int relpos_attn_fwd(int mode, int dtype, const void* Q, const void* K
     return code;
   };
   const bool decode = (mode == RELPOS_T5 && Lq <= 8);
-  const int chunk = decode_chunk_keys();
-  const int nchunks = (Lk + chunk - 1) / chunk;
   size_t scratch_bytes = 0, off_conv = 0, off_part = 0;
   if (dtype == RELPOS_FP32) {
     off_conv = scratch_bytes;
@@ -337,7 +339,7 @@ extern "C" int relpos_attn_fwd(int mode, int dtype, const void* Q, const void* K
   if (decode) {
     scratch_bytes = (scratch_bytes + 255) & ~static_cast<size_t>(255);
     off_part = scratch_bytes;
-    scratch_bytes += BH * Lq * nchunks * (kHeadDim + 2) * sizeof(float);
+    scratch_bytes += decode_partial_floats(BH * Lq, Lk) * sizeof(float);
   }
   // DeBERTa: the band array [BH, Lq, band_pitch] (bf16, with kBandPad bytes
   // before and after it: the attention kernel reads whole 128-key windows
@@ -359,6 +361,17 @@ extern "C" int relpos_attn_fwd(int mode, int dtype, const void* Q, const void* K
     off_ends = scratch_bytes;
     scratch_bytes += BH * 2 * static_cast<size_t>(ends_pitch) * sizeof(float);
   }
+  // Transformer-XL: the 128-wide query rows [BH, Lq, 128] and the keys'
+  // sinusoid table [Lk, 64] (bf16)
+  size_t off_q2 = 0, off_sin = 0;
+  if (mode == RELPOS_TXL) {
+    scratch_bytes = (scratch_bytes + 255) & ~static_cast<size_t>(255);
+    off_q2 = scratch_bytes;
+    scratch_bytes += BH * Lq * 2 * kHeadDim * 2;
+    scratch_bytes = (scratch_bytes + 255) & ~static_cast<size_t>(255);
+    off_sin = scratch_bytes;
+    scratch_bytes += static_cast<size_t>(Lk) * kHeadDim * 2;
+  }
   if (scratch_bytes) {
     if (cudaMallocAsync(&scratch, scratch_bytes, s) != cudaSuccess) return fail(RELPOS_ERR_CUDA);
   }
@@ -373,28 +386,10 @@ extern "C" int relpos_attn_fwd(int mode, int dtype, const void* Q, const void* K
   }
 
   if (decode) {
-    DecodeParams dp;
-    std::memset(&dp, 0, sizeof(dp));
-    dp.Q = static_cast<const __nv_bfloat16*>(Qb);
-    dp.K = static_cast<const __nv_bfloat16*>(Kb);
-    dp.V = static_cast<const __nv_bfloat16*>(Vb);
-    dp.bias = static_cast<const float*>(table0);
-    dp.B = B;
-    dp.H = H;
-    dp.Lq = Lq;
-    dp.Lk = Lk;
-    dp.causal = causal;
-    dp.q_offset = q_offset;
-    dp.scale_log2 = scale * kLog2e;
-    dp.chunk = chunk;
-    dp.nchunks = nchunks;
     float* part = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + off_part);
-    dp.part_o = part;
-    dp.part_ml = part + BH * Lq * nchunks * kHeadDim;
-    dp.out = out;
-    dp.out_f32 = dtype == RELPOS_FP32;
-    dp.t5 = t5;
-    dp.t5_R = R;
+    const DecodeParams dp = make_decode_params(Qb, Kb, Vb, table0, nullptr, B, H, Lq, Lk, causal,
+                                               q_offset, scale * kLog2e, t5, R, part, out,
+                                               dtype == RELPOS_FP32);
     if (launch_decode(dp, s) != cudaSuccess) return fail(RELPOS_ERR_CUDA);
   } else {
     FwdParams p;
@@ -468,13 +463,36 @@ extern "C" int relpos_attn_fwd(int mode, int dtype, const void* Q, const void* K
         return fail(RELPOS_ERR_CUDA);
       if (launch_deberta_band(tqa, tka, tpk, tpq, bp, s) != cudaSuccess) return fail(RELPOS_ERR_CUDA);
     }
-    CUtensorMap tq, tk, tv;
-    if (!make_tmap(&tq, Qb, Lq, static_cast<int>(BH)) || !make_tmap(&tk, Kb, Lk, static_cast<int>(BH)) ||
-        !make_tmap(&tv, Vb, Lk, static_cast<int>(BH)))
+    CUtensorMap tq, tk, tv, ts;
+    if (mode == RELPOS_TXL) {
+      uint8_t* sc = static_cast<uint8_t*>(scratch);
+      TxlParams tp;
+      std::memset(&tp, 0, sizeof(tp));
+      tp.BH = static_cast<int>(BH);
+      tp.H = H;
+      tp.Lq = Lq;
+      tp.Lk = Lk;
+      tp.q_offset = q_offset;
+      tp.Q = static_cast<const __nv_bfloat16*>(Qb);
+      tp.W = static_cast<const float*>(table0);
+      tp.uv = static_cast<const float*>(table1);
+      tp.Q2 = reinterpret_cast<__nv_bfloat16*>(sc + off_q2);
+      tp.Ksin = reinterpret_cast<__nv_bfloat16*>(sc + off_sin);
+      for (int m = 0; m < kHeadDim / 2; ++m)
+        tp.omega[m] = static_cast<float>(std::pow(10000.0, -2.0 * m / kHeadDim));
+      if (launch_txl_prep(tp, s) != cudaSuccess) return fail(RELPOS_ERR_CUDA);
+      if (!make_tmap(&tq, tp.Q2, Lq, static_cast<int>(BH), 2 * kHeadDim) ||
+          !make_tmap(&ts, tp.Ksin, Lk, 1))
+        return fail(RELPOS_ERR_CUDA);
+    } else if (!make_tmap(&tq, Qb, Lq, static_cast<int>(BH))) {
       return fail(RELPOS_ERR_CUDA);
+    }
+    if (!make_tmap(&tk, Kb, Lk, static_cast<int>(BH)) || !make_tmap(&tv, Vb, Lk, static_cast<int>(BH)))
+      return fail(RELPOS_ERR_CUDA);
+    if (mode != RELPOS_TXL) ts = tk;  // unused
     const int sms = num_sms();
     if (sms <= 0) return fail(RELPOS_ERR_CUDA);
-    if (launch_fwd(mode, dtype == RELPOS_FP32, tq, tk, tv, p, sms, s) != cudaSuccess)
+    if (launch_fwd(mode, dtype == RELPOS_FP32, tq, tk, tv, ts, p, sms, s) != cudaSuccess)
       return fail(RELPOS_ERR_CUDA);
   }
   if (scratch && cudaFreeAsync(scratch, s) != cudaSuccess) {
@@ -496,31 +514,32 @@ extern "C" int relpos_t5_attn_bwd(const void* Q, const void* K, const void* V, c
   if (!bias || !dbias || !aligned16(bias) || !aligned16(dbias)) return RELPOS_ERR_INVALID_ARG;
   if (static_cast<long long>(B) * H > 65535) return RELPOS_ERR_UNSUPPORTED;
   if (Lq > (1 << 24) || Lk > (1 << 24) || q_offset > (1 << 28)) return RELPOS_ERR_UNSUPPORTED;
+  // every pointer is checked before anything (the dbias clear included) is queued
+  if (Lq > 0 && (!dQ || !aligned16(dQ))) return RELPOS_ERR_INVALID_ARG;
+  if (Lk > 0 && (!dK || !dV || !aligned16(dK) || !aligned16(dV))) return RELPOS_ERR_INVALID_ARG;
+  if (Lq > 0 && Lk > 0) {
+    for (const void* ptr : {Q, K, V, dO})
+      if (!ptr || !aligned16(ptr)) return RELPOS_ERR_INVALID_ARG;
+  }
+  T5Index t5;
+  int R = 0;
+  const long long nmax = std::max(static_cast<long long>(Lk) - 1, static_cast<long long>(Lq) - 1 + q_offset);
+  rc = t5_setup(num_buckets, max_distance, causal, nmax, &t5, &R);
+  if (rc != RELPOS_OK) return rc;
+  if (Lq > 0 && Lk > 0 && (R < 1 || R > bwd_max_R())) return RELPOS_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t BH = static_cast<size_t>(B) * H;
   const size_t row_bytes = kHeadDim * 2;
   if (cudaMemsetAsync(dbias, 0, static_cast<size_t>(num_buckets) * H * 4, s) != cudaSuccess)
     return RELPOS_ERR_CUDA;
   if (Lq == 0 || Lk == 0) {  // no score: every gradient is zero
-    if (Lq > 0 && (!dQ || !aligned16(dQ))) return RELPOS_ERR_INVALID_ARG;
-    if (Lk > 0 && (!dK || !dV || !aligned16(dK) || !aligned16(dV))) return RELPOS_ERR_INVALID_ARG;
     bool ok = true;
     if (Lq > 0) ok = ok && cudaMemsetAsync(dQ, 0, BH * Lq * row_bytes, s) == cudaSuccess;
     if (Lk > 0) ok = ok && cudaMemsetAsync(dK, 0, BH * Lk * row_bytes, s) == cudaSuccess &&
                       cudaMemsetAsync(dV, 0, BH * Lk * row_bytes, s) == cudaSuccess;
     return ok ? RELPOS_OK : RELPOS_ERR_CUDA;
   }
-  if (!Q || !K || !V || !dO || !dQ || !dK || !dV) return RELPOS_ERR_INVALID_ARG;
-  for (const void* ptr : {Q, K, V, dO, static_cast<const void*>(dQ), static_cast<const void*>(dK),
-                          static_cast<const void*>(dV)})
-    if (!aligned16(ptr)) return RELPOS_ERR_INVALID_ARG;
 
-  T5Index t5;
-  int R = 0;
-  const long long nmax = std::max(static_cast<long long>(Lk) - 1, static_cast<long long>(Lq) - 1 + q_offset);
-  rc = t5_setup(num_buckets, max_distance, causal, nmax, &t5, &R);
-  if (rc != RELPOS_OK) return rc;
-  if (R < 1 || R > bwd_max_R()) return RELPOS_ERR_UNSUPPORTED;
   int* status = status_ptr();
   if (!status) return RELPOS_ERR_CUDA;
 

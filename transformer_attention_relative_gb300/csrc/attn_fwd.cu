@@ -60,11 +60,21 @@ constexpr int kBN = 128;       // keys per tile
 constexpr int kStages = 3;     // K/V ring depth
 constexpr int kThreads = 384;  // 12 warps
 constexpr uint32_t kTileBytes = kBM * kHeadDim * 2;  // 16 KB: 128 rows x 128 B
-constexpr uint32_t kOffQ = 0;                        // two Q tiles
-constexpr uint32_t kOffK = kOffQ + 2 * kTileBytes;
-constexpr uint32_t kOffV = kOffK + kStages * kTileBytes;
-constexpr uint32_t kOffBar = kOffV + kStages * kTileBytes;
-constexpr uint32_t kOffAux = kOffBar + 512;
+// Shared-memory layout: the item's two query tiles, the K ring, the V ring,
+// the barriers, then the mode's tables. Transformer-XL (MODE 4) scores
+// against a 128-wide contraction (content and position halves), so its query
+// tiles and K stages hold two 64-column halves of kTileBytes each.
+template <int MODE>
+struct Smem {
+  static constexpr uint32_t kHalves = MODE == 4 ? 2u : 1u;
+  static constexpr uint32_t kQBytes = kHalves * kTileBytes;  // one query tile
+  static constexpr uint32_t kKBytes = kHalves * kTileBytes;  // one K stage
+  static constexpr uint32_t kOffQ = 0;
+  static constexpr uint32_t kOffK = kOffQ + 2 * kQBytes;
+  static constexpr uint32_t kOffV = kOffK + kStages * kKBytes;
+  static constexpr uint32_t kOffBar = kOffV + kStages * kTileBytes;
+  static constexpr uint32_t kOffAux = kOffBar + 512;
+};
 constexpr uint32_t kCombBytes = 2 * 128 * 8;  // split items: (m, l) of every row, per tile
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemS = 0;
@@ -242,12 +252,41 @@ __host__ __device__ inline uint32_t fwd_aux_bytes(int mode, const FwdParams& p) 
 
 // VAR 0: pair items only; 1: with split items (p.nsplit > 0); 2: pair items
 // with the two softmax warpgroups staggered (p.stagger).
+// Loads one query tile (both halves for Transformer-XL) on barrier `bar`.
+template <int MODE, bool ELECT>
+RP_DEVI void load_q_tile(uint32_t dst, const CUtensorMap* tmQ, uint32_t bar, int row0, int bh) {
+#pragma unroll
+  for (uint32_t h = 0; h < Smem<MODE>::kHalves; ++h) {
+    if constexpr (ELECT)
+      tma_load_3d_elect(dst + h * kTileBytes, tmQ, bar, static_cast<int>(h) * kHeadDim, row0, bh);
+    else
+      tma_load_3d(dst + h * kTileBytes, tmQ, bar, static_cast<int>(h) * kHeadDim, row0, bh);
+  }
+}
+// Loads one K stage: the key tile and, for Transformer-XL, the keys'
+// sinusoid rows (one [Lk, 64] table for every head) as the second half.
+template <int MODE, bool ELECT>
+RP_DEVI void load_k_stage(uint32_t dst, const CUtensorMap* tmK, const CUtensorMap* tmS, uint32_t bar,
+                          int key0, int bh) {
+  if constexpr (ELECT) {
+    tma_load_3d_elect(dst, tmK, bar, 0, key0, bh);
+    if constexpr (MODE == 4) tma_load_3d_elect(dst + kTileBytes, tmS, bar, 0, key0, 0);
+  } else {
+    tma_load_3d(dst, tmK, bar, 0, key0, bh);
+    if constexpr (MODE == 4) tma_load_3d(dst + kTileBytes, tmS, bar, 0, key0, 0);
+  }
+}
+
 template <int MODE, bool OUT_F32, int VAR>
 __global__ void __launch_bounds__(kThreads, 1)
     relpos_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                      const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmS,
+                      const FwdParams p) {
   constexpr bool SPLIT = VAR == 1;
   constexpr bool STAG = VAR == 2;
+  using L = Smem<MODE>;
+  constexpr uint32_t kOffQ = L::kOffQ, kOffK = L::kOffK, kOffV = L::kOffV, kOffBar = L::kOffBar,
+                     kOffAux = L::kOffAux;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t sbase = (raw_addr + 1023u) & ~1023u;
@@ -312,8 +351,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
-    tma_prefetch_l2_3d(&tmQ, 0, it0.row0[0], it0.bh);
-    if (two0) tma_prefetch_l2_3d(&tmQ, 0, it0.row0[1], it0.bh);
+    if constexpr (MODE == 4) tma_prefetch_desc(&tmS);
+    for (uint32_t hf = 0; hf < L::kHalves; ++hf) {
+      tma_prefetch_l2_3d(&tmQ, hf * kHeadDim, it0.row0[0], it0.bh);
+      if (two0) tma_prefetch_l2_3d(&tmQ, hf * kHeadDim, it0.row0[1], it0.bh);
+    }
     for (int s = 0; s < nk0; ++s) {
       tma_prefetch_l2_3d(&tmK, 0, stream_key(it0, s) * kBN, it0.bh);
       tma_prefetch_l2_3d(&tmV, 0, stream_key(it0, s) * kBN, it0.bh);
@@ -343,13 +385,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool kq = warp == 0;
       griddep_wait();
       if (first_loads) {
-        mbar_arrive_expect_tx(bar(kBarQFull), (two0 ? 2u : 1u) * kTileBytes);
-        tma_load_3d(sbase + kOffQ, &tmQ, bar(kBarQFull), 0, it0.row0[0], it0.bh);
-        if (two0) tma_load_3d(sbase + kOffQ + kTileBytes, &tmQ, bar(kBarQFull), 0, it0.row0[1], it0.bh);
+        mbar_arrive_expect_tx(bar(kBarQFull), (two0 ? 2u : 1u) * L::kQBytes);
+        load_q_tile<MODE, false>(sbase + kOffQ, &tmQ, bar(kBarQFull), it0.row0[0], it0.bh);
+        if (two0) load_q_tile<MODE, false>(sbase + kOffQ + L::kQBytes, &tmQ, bar(kBarQFull), it0.row0[1], it0.bh);
         for (int s = 0; s < nk0; ++s) {
           const int key0 = stream_key(it0, s) * kBN;
-          mbar_arrive_expect_tx(bar(kBarKFull + s), kTileBytes);
-          tma_load_3d(sbase + kOffK + s * kTileBytes, &tmK, bar(kBarKFull + s), 0, key0, it0.bh);
+          mbar_arrive_expect_tx(bar(kBarKFull + s), L::kKBytes);
+          load_k_stage<MODE, false>(sbase + kOffK + s * L::kKBytes, &tmK, &tmS, bar(kBarKFull + s), key0, it0.bh);
           mbar_arrive_expect_tx(bar(kBarVFull + s), kTileBytes);
           tma_load_3d(sbase + kOffV + s * kTileBytes, &tmV, bar(kBarVFull + s), 0, key0, it0.bh);
         }
@@ -357,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t full0 = kq ? kBarKFull : kBarVFull;
       const uint32_t empty0 = kq ? kBarKEmpty : kBarVEmpty;
       const uint32_t ring = kq ? kOffK : kOffV;
-      const void* tmap = kq ? static_cast<const void*>(&tmK) : static_cast<const void*>(&tmV);
+      const uint32_t stage_bytes = kq ? L::kKBytes : kTileBytes;
       bool ok = true;
       uint32_t it_cnt = 0;
       int item_cnt = 0;
@@ -370,10 +412,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
           // a split item's single query tile goes to the Q_a buffer
           const bool two = !it.split && it.hi[1] > 0;
-          mbar_arrive_expect_tx_elect(bar(kBarQFull), (two ? 2u : 1u) * kTileBytes);
-          tma_load_3d_elect(sbase + kOffQ, &tmQ, bar(kBarQFull), 0, it.row0[0], it.bh);
-          if (two)
-            tma_load_3d_elect(sbase + kOffQ + kTileBytes, &tmQ, bar(kBarQFull), 0, it.row0[1], it.bh);
+          mbar_arrive_expect_tx_elect(bar(kBarQFull), (two ? 2u : 1u) * L::kQBytes);
+          load_q_tile<MODE, true>(sbase + kOffQ, &tmQ, bar(kBarQFull), it.row0[0], it.bh);
+          if (two) load_q_tile<MODE, true>(sbase + kOffQ + L::kQBytes, &tmQ, bar(kBarQFull), it.row0[1], it.bh);
         }
         for (int j = 0; j < it.ns; ++j, ++it_cnt) {
           if (j < pre) continue;
@@ -382,9 +423,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = mbar_wait_warp(bar(empty0 + st), ((it_cnt / kStages) - 1) & 1);
             if (!ok) break;
           }
-          mbar_arrive_expect_tx_elect(bar(full0 + st), kTileBytes);
-          tma_load_3d_elect(sbase + ring + st * kTileBytes, tmap, bar(full0 + st), 0,
-                            stream_key(it, j) * kBN, it.bh);
+          mbar_arrive_expect_tx_elect(bar(full0 + st), stage_bytes);
+          if (kq)
+            load_k_stage<MODE, true>(sbase + ring + st * stage_bytes, &tmK, &tmS, bar(full0 + st),
+                                     stream_key(it, j) * kBN, it.bh);
+          else
+            tma_load_3d_elect(sbase + ring + st * stage_bytes, &tmV, bar(full0 + st), 0,
+                              stream_key(it, j) * kBN, it.bh);
         }
       }
       if (!ok && lane == 0) {
@@ -416,14 +461,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dq_a = smem_desc_sw128(sbase + kOffQ, 16, 1024);
       const uint64_t dk0 = smem_desc_sw128(sbase + kOffK, 16, 1024);
       const uint64_t dv0 = smem_desc_sw128(sbase + kOffV, 8192, 1024);
-      constexpr uint64_t kStageStep = kTileBytes >> 4;
+      constexpr uint64_t kStageStep = kTileBytes >> 4;  // one 64-column tile
+      constexpr uint64_t kQStep = L::kQBytes >> 4, kKStep = L::kKBytes >> 4;
       const uint32_t s_col = tmem + kTmemS + x * kBN;
       const uint32_t o_col = tmem + kTmemO + x * kHeadDim;
       const uint32_t p_col = tmem + kTmemP + x * 64;
       for (int rr = 0, w = item_at(0, p.causal); ok && w < nitems; w = item_at(++rr, p.causal), ++item_cnt) {
         const Item it = make_item<SPLIT>(p, w);
         const int mine = sel(it.hi, x) - sel(it.lo, x);
-        const uint64_t dq = dq_a + ((it.split ? 0u : x) * kStageStep);
+        const uint64_t dq = dq_a + ((it.split ? 0u : x) * kQStep);
         ok = mbar_wait_warp(bar(kBarQFull), item_cnt & 1);
         if (!ok) break;
         if (mine == 0 && lane == 0) mbar_arrive(bar(kBarQEmpty));
@@ -449,10 +495,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!mbar_wait_warp(bar(kBarKFull + st), (r / kStages) & 1)) return false;
           if (sis > 0 && !mbar_wait_warp(bar(kBarSFree + x), (sis - 1) & 1)) return false;
           tc_fence_after();
-          const uint64_t dk = dk0 + st * kStageStep;
+          const uint64_t dk = dk0 + st * kKStep;
+          // K-steps of 16: 4 per 64-column half (Transformer-XL: content, then position)
 #pragma unroll
-          for (int kk = 0; kk < kHeadDim / 16; ++kk)
-            umma_bf16_ss_elect(s_col, dq + 2 * kk, dk + 2 * kk, kIdescQK, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < static_cast<int>(L::kHalves) * (kHeadDim / 16); ++kk) {
+            const uint64_t off = (kk >> 2) * kStageStep + 2 * (kk & 3);
+            umma_bf16_ss_elect(s_col, dq + off, dk + off, kIdescQK, kk > 0 ? 1u : 0u);
+          }
           tc_commit_elect(bar(kBarSFull + x));
           tc_commit_elect(bar(kBarKEmpty + st));
           if (i == mine - 1) tc_commit_elect(bar(kBarQEmpty));
@@ -743,8 +792,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (MODE == 0) {
           far_l = rel_hi <= -p.t5_R;
           far_r = p.t5.bidir && rel_lo >= p.t5_R;
-        } else if constexpr (MODE == 3) {
-          far_l = far_r = false;  // ALiBi never saturates
+        } else if constexpr (MODE == 3 || MODE == 4) {
+          far_l = far_r = false;  // ALiBi never saturates; Transformer-XL's term is in the scores
         } else {
           far_l = rel_hi <= -kc;
           far_r = rel_lo >= kc;
@@ -763,7 +812,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // 2^(xs * xscale + xoff - m).
         // DeBERTa tiles beyond the band still carry a per-key term, so every
         // DeBERTa tile takes the per-element path.
-        const bool far = MODE == 3 || (MODE != 2 && (far_l || far_r));
+        const bool far = MODE == 3 || MODE == 4 || (MODE != 2 && (far_l || far_r));
         // a row constant added with the maximum: the far constant of a far
         // tile, for DeBERTa tiles beyond the band the saturated c2p term
         // (their per-key p2c term goes into the scaled scores), for ALiBi
@@ -1160,7 +1209,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 uint32_t fwd_smem_bytes(int mode, const FwdParams& p) {
-  return 1024u + kOffAux + fwd_aux_bytes(mode, p) + (p.nsplit > 0 ? kCombBytes : 0u);
+  const uint32_t aux0 = mode == 4 ? Smem<4>::kOffAux : Smem<0>::kOffAux;
+  return 1024u + aux0 + fwd_aux_bytes(mode, p) + (p.nsplit > 0 ? kCombBytes : 0u);
 }
 
 uint32_t fwd_max_smem_bytes() { return 232448u; }
@@ -1185,12 +1235,14 @@ int fwd_split_items(int npair_items, int BH, int Lq, int causal, int num_sms) {
 }
 
 cudaError_t launch_fwd(int mode, bool out_f32, const CUtensorMap& tmQ, const CUtensorMap& tmK,
-                       const CUtensorMap& tmV, const FwdParams& p, int num_sms, cudaStream_t stream) {
+                       const CUtensorMap& tmV, const CUtensorMap& tmS, const FwdParams& p, int num_sms,
+                       cudaStream_t stream) {
   const uint32_t smem = fwd_smem_bytes(mode, p);
   const int nitems = fwd_num_items(p);
   dim3 grid(nitems < num_sms ? nitems : num_sms);
   dim3 block(kThreads);
-  void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const FwdParams) = nullptr;
+  void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, const FwdParams) =
+      nullptr;
   const int var = p.nsplit > 0 ? 1 : (p.stagger ? 2 : 0);
   if (mode == 0) {
     if (var == 2)
@@ -1207,6 +1259,9 @@ cudaError_t launch_fwd(int mode, bool out_f32, const CUtensorMap& tmQ, const CUt
   } else if (mode == 3 && var < 2) {
     kern = out_f32 ? (var ? relpos_fwd_kernel<3, true, 1> : relpos_fwd_kernel<3, true, 0>)
                    : (var ? relpos_fwd_kernel<3, false, 1> : relpos_fwd_kernel<3, false, 0>);
+  } else if (mode == 4 && var < 2) {
+    kern = out_f32 ? (var ? relpos_fwd_kernel<4, true, 1> : relpos_fwd_kernel<4, true, 0>)
+                   : (var ? relpos_fwd_kernel<4, false, 1> : relpos_fwd_kernel<4, false, 0>);
   } else {
     return cudaErrorNotSupported;
   }
@@ -1215,7 +1270,7 @@ cudaError_t launch_fwd(int mode, bool out_f32, const CUtensorMap& tmQ, const CUt
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
   const int slot = mode * 6 + (out_f32 ? 3 : 0) + var;
-  static std::atomic<uint64_t> attr_set[24];
+  static std::atomic<uint64_t> attr_set[30];
   const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
   if (!bit || !(attr_set[slot].load() & bit)) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1236,7 +1291,7 @@ cudaError_t launch_fwd(int mode, bool out_f32, const CUtensorMap& tmQ, const CUt
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, tmQ, tmK, tmV, p);
+  return cudaLaunchKernelEx(&cfg, kern, tmQ, tmK, tmV, tmS, p);
 }
 
 }  // namespace relpos

@@ -294,7 +294,72 @@ float* noalloc_scratch() {
   return g_noalloc_ptr[dev];
 }
 
+// Checks shared by the two decode-only entry points, before anything is
+// launched: RELPOS_OK to go on, a return code otherwise. *noop is set when
+// there is nothing to compute (no query row).
+int decode_entry_check(const void* Q, const void* K, const void* V, const void* bias,
+                       const void* key_pos, bool need_key_pos, const void* out, int B, int H,
+                       int Lq, int Lk, int num_buckets, int max_distance, int causal,
+                       int q_offset, bool* noop) {
+  *noop = false;
+  int rc = check_rel_params(RELPOS_T5, num_buckets, max_distance, causal);
+  if (rc != RELPOS_OK) return rc;
+  if (B < 0 || H < 0 || Lq < 0 || Lk < 0 || q_offset < 0) return RELPOS_ERR_INVALID_ARG;
+  if (Lq > 8) return RELPOS_ERR_UNSUPPORTED;  // decode shapes only
+  if (B == 0 || H == 0 || Lq == 0) {
+    *noop = true;
+    return RELPOS_OK;
+  }
+  if (static_cast<long long>(B) * H > 65535 || Lk > (1 << 24) || q_offset > (1 << 28))
+    return RELPOS_ERR_UNSUPPORTED;
+  // the kernels read Q, K, V and write out in 16-byte vectors
+  if (!Q || !out || !aligned16(Q) || !aligned16(out)) return RELPOS_ERR_INVALID_ARG;
+  if (Lk > 0) {
+    if (!K || !V || !bias || !aligned16(K) || !aligned16(V)) return RELPOS_ERR_INVALID_ARG;
+    if (need_key_pos && (!key_pos || (reinterpret_cast<uintptr_t>(key_pos) & 3u)))
+      return RELPOS_ERR_INVALID_ARG;
+  }
+  return RELPOS_OK;
+}
+
 }  // namespace
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t decode_partial_floats(size_t rows, int Lk) {
+  const size_t nchunks = (static_cast<size_t>(Lk) + kDecChunk - 1) / kDecChunk;
+  return rows * nchunks * (kHeadDim + 2);
+}
+
+DecodeParams make_decode_params(const void* Q, const void* K, const void* V, const void* bias,
+                                const int* key_pos, int B, int H, int Lq, int Lk, int causal,
+                                int q_offset, float scale_log2, const T5Index& t5, int R,
+                                float* part, void* out, bool out_f32) {
+  DecodeParams dp;
+  std::memset(&dp, 0, sizeof(dp));
+  dp.Q = static_cast<const __nv_bfloat16*>(Q);
+  dp.K = static_cast<const __nv_bfloat16*>(K);
+  dp.V = static_cast<const __nv_bfloat16*>(V);
+  dp.bias = static_cast<const float*>(bias);
+  dp.key_pos = key_pos;
+  dp.B = B;
+  dp.H = H;
+  dp.Lq = Lq;
+  dp.Lk = Lk;
+  dp.causal = causal;
+  dp.q_offset = q_offset;
+  dp.scale_log2 = scale_log2;
+  dp.chunk = kDecChunk;
+  dp.nchunks = (Lk + kDecChunk - 1) / kDecChunk;
+  dp.part_o = part;
+  dp.part_ml = part + static_cast<size_t>(B) * H * Lq * dp.nchunks * kHeadDim;
+  dp.out = out;
+  dp.out_f32 = out_f32 ? 1 : 0;
+  dp.t5 = t5;
+  dp.t5_R = R;
+  return dp;
+}
+
 }  // namespace relpos
 
 extern "C" int relpos_t5_decode_noalloc(const void* Q, const void* K, const void* V,
@@ -302,56 +367,33 @@ extern "C" int relpos_t5_decode_noalloc(const void* Q, const void* K, const void
                                         int num_buckets, int max_distance, int causal,
                                         int q_offset, void* out, void* stream) {
   using namespace relpos;
-  int rc = check_rel_params(RELPOS_T5, num_buckets, max_distance, causal);
-  if (rc != RELPOS_OK) return rc;
-  if (B < 0 || H < 0 || Lq < 0 || Lk < 0 || q_offset < 0) return RELPOS_ERR_INVALID_ARG;
-  if (Lq > 8) return RELPOS_ERR_UNSUPPORTED;  // decode shapes only
-  if (B == 0 || H == 0 || Lq == 0) return RELPOS_OK;
-  if (static_cast<long long>(B) * H > 65535 || Lk > (1 << 24) || q_offset > (1 << 28))
-    return RELPOS_ERR_UNSUPPORTED;
-  if (!Q || !out) return RELPOS_ERR_INVALID_ARG;
+  bool noop = false;
+  int rc = decode_entry_check(Q, K, V, bias, nullptr, false, out, B, H, Lq, Lk, num_buckets,
+                              max_distance, causal, q_offset, &noop);
+  if (rc != RELPOS_OK || noop) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t rows = static_cast<size_t>(B) * H * Lq;
   if (Lk == 0)
     return cudaMemsetAsync(out, 0, rows * kHeadDim * 2, s) == cudaSuccess ? RELPOS_OK
                                                                            : RELPOS_ERR_CUDA;
-  if (!K || !V || !bias) return RELPOS_ERR_INVALID_ARG;
-  const int chunk = decode_chunk_keys();
-  const int nchunks = (Lk + chunk - 1) / chunk;
-  const size_t need = rows * nchunks * (kHeadDim + 2) * sizeof(float);
-  if (need > kNoAllocScratchBytes) return RELPOS_ERR_SCRATCH_LIMIT;
-  float* scratch = noalloc_scratch();
-  if (!scratch) return RELPOS_ERR_CUDA;
-
+  if (decode_partial_floats(rows, Lk) * sizeof(float) > kNoAllocScratchBytes)
+    return RELPOS_ERR_SCRATCH_LIMIT;
   T5Index t5;
   int R = 0;
   const long long nmax = std::max(static_cast<long long>(Lk) - 1,
                                   static_cast<long long>(Lq) - 1 + q_offset);
   rc = t5_setup(num_buckets, max_distance, causal, nmax, &t5, &R);
   if (rc != RELPOS_OK) return rc;
-
-  DecodeParams dp;
-  std::memset(&dp, 0, sizeof(dp));
-  dp.Q = static_cast<const __nv_bfloat16*>(Q);
-  dp.K = static_cast<const __nv_bfloat16*>(K);
-  dp.V = static_cast<const __nv_bfloat16*>(V);
-  dp.bias = static_cast<const float*>(bias);
-  dp.B = B;
-  dp.H = H;
-  dp.Lq = Lq;
-  dp.Lk = Lk;
-  dp.causal = causal;
-  dp.q_offset = q_offset;
-  dp.scale_log2 = (1.0f / std::sqrt(static_cast<float>(kHeadDim))) * kLog2e;
-  dp.chunk = chunk;
-  dp.nchunks = nchunks;
-  dp.part_o = scratch;
-  dp.part_ml = scratch + rows * nchunks * kHeadDim;
-  dp.out = out;
-  dp.out_f32 = 0;
-  dp.t5 = t5;
-  dp.t5_R = R;
-  return launch_decode(dp, s) == cudaSuccess ? RELPOS_OK : RELPOS_ERR_CUDA;
+  float* scratch = noalloc_scratch();
+  if (!scratch) return RELPOS_ERR_CUDA;
+  const float scale_log2 = (1.0f / std::sqrt(static_cast<float>(kHeadDim))) * kLog2e;
+  const DecodeParams dp = make_decode_params(Q, K, V, bias, nullptr, B, H, Lq, Lk, causal, q_offset,
+                                             scale_log2, t5, R, scratch, out, false);
+  if (launch_decode(dp, s) != cudaSuccess) {
+    cudaGetLastError();
+    return RELPOS_ERR_CUDA;
+  }
+  return RELPOS_OK;
 }
 
 // ---------------------------------------------------------------------------
@@ -366,56 +408,28 @@ extern "C" int relpos_t5_decode_positions(const void* Q, const void* K, const vo
                                           int Lq, int Lk, int num_buckets, int max_distance,
                                           int causal, int q_offset, void* out, void* stream) {
   using namespace relpos;
-  int rc = check_rel_params(RELPOS_T5, num_buckets, max_distance, causal);
-  if (rc != RELPOS_OK) return rc;
-  if (B < 0 || H < 0 || Lq < 0 || Lk < 0 || q_offset < 0) return RELPOS_ERR_INVALID_ARG;
-  if (Lq > 8) return RELPOS_ERR_UNSUPPORTED;  // decode shapes only
-  if (B == 0 || H == 0 || Lq == 0) return RELPOS_OK;
-  if (static_cast<long long>(B) * H > 65535 || Lk > (1 << 24) || q_offset > (1 << 28))
-    return RELPOS_ERR_UNSUPPORTED;
-  if (!Q || !out) return RELPOS_ERR_INVALID_ARG;
+  bool noop = false;
+  int rc = decode_entry_check(Q, K, V, bias, key_pos, true, out, B, H, Lq, Lk, num_buckets,
+                              max_distance, causal, q_offset, &noop);
+  if (rc != RELPOS_OK || noop) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t rows = static_cast<size_t>(B) * H * Lq;
   if (Lk == 0)
     return cudaMemsetAsync(out, 0, rows * kHeadDim * 2, s) == cudaSuccess ? RELPOS_OK
                                                                            : RELPOS_ERR_CUDA;
-  if (!K || !V || !bias || !key_pos) return RELPOS_ERR_INVALID_ARG;
-
   // thresholds for every offset a position in [0, 2^28] can produce
   T5Index t5;
   int R = 0;
   rc = t5_setup(num_buckets, max_distance, causal, (1ll << 28) + 8, &t5, &R);
   if (rc != RELPOS_OK) return rc;
-
-  const int chunk = decode_chunk_keys();
-  const int nchunks = (Lk + chunk - 1) / chunk;
   float* scratch = nullptr;
-  if (cudaMallocAsync(&scratch, rows * nchunks * (kHeadDim + 2) * sizeof(float), s) != cudaSuccess) {
+  if (cudaMallocAsync(&scratch, decode_partial_floats(rows, Lk) * sizeof(float), s) != cudaSuccess) {
     cudaGetLastError();
     return RELPOS_ERR_CUDA;
   }
-  DecodeParams dp;
-  std::memset(&dp, 0, sizeof(dp));
-  dp.Q = static_cast<const __nv_bfloat16*>(Q);
-  dp.K = static_cast<const __nv_bfloat16*>(K);
-  dp.V = static_cast<const __nv_bfloat16*>(V);
-  dp.bias = static_cast<const float*>(bias);
-  dp.B = B;
-  dp.H = H;
-  dp.Lq = Lq;
-  dp.Lk = Lk;
-  dp.causal = causal;
-  dp.q_offset = q_offset;
-  dp.scale_log2 = (1.0f / std::sqrt(static_cast<float>(kHeadDim))) * kLog2e;
-  dp.chunk = chunk;
-  dp.nchunks = nchunks;
-  dp.part_o = scratch;
-  dp.part_ml = scratch + rows * nchunks * kHeadDim;
-  dp.out = out;
-  dp.out_f32 = 0;
-  dp.t5 = t5;
-  dp.t5_R = R;
-  dp.key_pos = key_pos;
+  const float scale_log2 = (1.0f / std::sqrt(static_cast<float>(kHeadDim))) * kLog2e;
+  const DecodeParams dp = make_decode_params(Q, K, V, bias, key_pos, B, H, Lq, Lk, causal, q_offset,
+                                             scale_log2, t5, R, scratch, out, false);
   const bool ok = launch_decode(dp, s) == cudaSuccess;
   const bool freed = cudaFreeAsync(scratch, s) == cudaSuccess;
   if (!ok || !freed) {

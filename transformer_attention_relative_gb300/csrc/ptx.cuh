@@ -89,16 +89,6 @@ RP_DEVI void tma_load_3d(uint32_t dst, const void* tmap, uint32_t bar, int c0, i
       "l"(tmap), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
 }
-RP_DEVI void tma_store_3d(const void* tmap, uint32_t src, int c0, int c1, int c2) {
-  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
-                   tmap),
-               "r"(src), "r"(c0), "r"(c1), "r"(c2)
-               : "memory");
-}
-RP_DEVI void tma_store_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-RP_DEVI void tma_store_wait_read_all() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
 // Make generic-proxy shared-memory writes visible to the async proxy
 // (tensor cores, TMA).
 RP_DEVI void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
@@ -212,17 +202,6 @@ RP_DEVI uint32_t pack_bf16x2(float lo, float hi) {
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
-RP_DEVI void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
-               "r"(d)
-               : "memory");
-}
-RP_DEVI void ld_shared_v4(uint32_t addr, uint32_t& a, uint32_t& b, uint32_t& c, uint32_t& d) {
-  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(a), "=r"(b), "=r"(c), "=r"(d)
-               : "r"(addr)
-               : "memory");
-}
 
 }  // namespace relpos
 
@@ -323,85 +302,6 @@ RP_DEVI bool mbar_wait_warp(uint32_t bar, uint32_t parity,
                             unsigned long long limit_ns = kWaitTimeoutNs) {
   const bool ok = mbar_wait(bar, parity, limit_ns);
   return __all_sync(0xffffffffu, ok);
-}
-
-}  // namespace relpos
-
-namespace relpos {
-
-// 2^t for a pair of values on the FMA pipe instead of the MUFU: a Cody-Waite
-// split t = n + f with n the nearest integer (the 1.5 * 2^23 addition rounds
-// t to an integer in the low mantissa bits) and |f| <= 1/2, a cubic fitted to
-// 2^f on [-1/2, 1/2] by reweighted least squares (relative error below 2e-4,
-// far under the bf16 rounding the probabilities get), and 2^n added into the
-// exponent field. Inputs below -126 (masked scores) give about 2^-126.
-RP_DEVI float2 exp2_poly2(float2 t) {
-  constexpr float c0 = 0.999954515f, c1 = 0.693549487f, c2 = 0.242283948f, c3 = 0.0532418609f;
-  t.x = fmaxf(t.x, -126.f);
-  t.y = fmaxf(t.y, -126.f);
-  const float2 r = __fadd2_rn(t, make_float2(12582912.f, 12582912.f));
-  const float2 n = __fadd2_rn(r, make_float2(-12582912.f, -12582912.f));
-  const float2 f = __ffma2_rn(n, make_float2(-1.f, -1.f), t);
-  float2 q = __ffma2_rn(f, make_float2(c3, c3), make_float2(c2, c2));
-  q = __ffma2_rn(q, f, make_float2(c1, c1));
-  q = __ffma2_rn(q, f, make_float2(c0, c0));
-  float2 out;
-  out.x = __int_as_float(__float_as_int(q.x) + (__float_as_int(r.x) << 23));
-  out.y = __int_as_float(__float_as_int(q.y) + (__float_as_int(r.y) << 23));
-  return out;
-}
-
-}  // namespace relpos
-
-namespace relpos {
-
-// 32 consecutive fp32 TMEM columns of this thread's lane, returned as 16
-// register pairs (element 2i in the low half, 2i + 1 in the high half) so that
-// packed f32x2 arithmetic can use them without re-pairing moves.
-RP_DEVI void tmem_ld32_pairs(uint32_t taddr, uint64_t (&r)[16]) {
-  asm volatile(
-      "{\n\t.reg .b32 t0,t1,t2,t3,t4,t5,t6,t7,t8,t9,t10,t11,t12,t13,t14,t15,t16,t17,t18,t19,t20,t21,t22,t23,t24,t25,t26,t27,t28,t29,t30,t31;\n\t"
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {t0,t1,t2,t3,t4,t5,t6,t7,t8,t9,t10,t11,t12,t13,t14,t15,t16,t17,t18,t19,t20,t21,t22,t23,t24,t25,t26,t27,t28,t29,t30,t31}, [%16];\n\t"
-      "mov.b64 %0, {t0, t1};\n\t"
-      "mov.b64 %1, {t2, t3};\n\t"
-      "mov.b64 %2, {t4, t5};\n\t"
-      "mov.b64 %3, {t6, t7};\n\t"
-      "mov.b64 %4, {t8, t9};\n\t"
-      "mov.b64 %5, {t10, t11};\n\t"
-      "mov.b64 %6, {t12, t13};\n\t"
-      "mov.b64 %7, {t14, t15};\n\t"
-      "mov.b64 %8, {t16, t17};\n\t"
-      "mov.b64 %9, {t18, t19};\n\t"
-      "mov.b64 %10, {t20, t21};\n\t"
-      "mov.b64 %11, {t22, t23};\n\t"
-      "mov.b64 %12, {t24, t25};\n\t"
-      "mov.b64 %13, {t26, t27};\n\t"
-      "mov.b64 %14, {t28, t29};\n\t"
-      "mov.b64 %15, {t30, t31};\n\t"
-      "}"
-      : "=l"(r[0]),"=l"(r[1]),"=l"(r[2]),"=l"(r[3]),"=l"(r[4]),"=l"(r[5]),"=l"(r[6]),"=l"(r[7]),"=l"(r[8]),"=l"(r[9]),"=l"(r[10]),"=l"(r[11]),"=l"(r[12]),"=l"(r[13]),"=l"(r[14]),"=l"(r[15])
-      : "r"(taddr));
-}
-RP_DEVI void tmem_ld_wait_pairs(uint64_t (&r)[16]) {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" : "+l"(r[0]),"+l"(r[1]),"+l"(r[2]),"+l"(r[3]),"+l"(r[4]),"+l"(r[5]),"+l"(r[6]),"+l"(r[7]),"+l"(r[8]),"+l"(r[9]),"+l"(r[10]),"+l"(r[11]),"+l"(r[12]),"+l"(r[13]),"+l"(r[14]),"+l"(r[15])::"memory");
-}
-// 2^x for both halves of a pair on the MUFU, result as a pair.
-RP_DEVI float2 ex2_pair(float2 v) {
-  uint64_t in = (static_cast<uint64_t>(__float_as_uint(v.y)) << 32) | __float_as_uint(v.x);
-  uint64_t out;
-  asm("{\n\t.reg .f32 lo, hi;\n\t"
-      "mov.b64 {lo, hi}, %1;\n\t"
-      "ex2.approx.ftz.f32 lo, lo;\n\t"
-      "ex2.approx.ftz.f32 hi, hi;\n\t"
-      "mov.b64 %0, {lo, hi};\n\t}"
-      : "=l"(out)
-      : "l"(in));
-  return make_float2(__uint_as_float(static_cast<uint32_t>(out)),
-                     __uint_as_float(static_cast<uint32_t>(out >> 32)));
-}
-RP_DEVI float2 as_float2(uint64_t v) {
-  return make_float2(__uint_as_float(static_cast<uint32_t>(v)),
-                     __uint_as_float(static_cast<uint32_t>(v >> 32)));
 }
 
 }  // namespace relpos

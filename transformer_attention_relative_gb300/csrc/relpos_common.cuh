@@ -111,6 +111,17 @@ struct BandParams {
   int* status;
 };
 
+// Transformer-XL operand pre-pass (txl_prep.cu)
+struct TxlParams {
+  int BH, H, Lq, Lk, q_offset;
+  const __nv_bfloat16* Q;  // [BH, Lq, 64]
+  const float* W;          // [H, 64, 64]: r(t) = W R(t), output index first
+  const float* uv;         // [2, H, 64]: u, then v
+  __nv_bfloat16* Q2;       // [BH, Lq, 128]: q + u, then a = W^T (q + v) rotated by w p
+  __nv_bfloat16* Ksin;     // [Lk, 64]: (cos w_m j, sin w_m j)
+  float omega[kHeadDim / 2];  // w_m = 10000^(-2m/64)
+};
+
 struct DecodeParams {
   const __nv_bfloat16* Q;
   const __nv_bfloat16* K;

@@ -8,7 +8,8 @@ Recipe (one per workload): a CPU ``torch.Generator`` seeded with
 ``1000 + index``; draws in the order Q, K, V, table0, table1; ``randn``
 scaled by the workload's sigma; then a cast to the kernel's input dtype
 (bf16, or fp32 for the tiny fp32 case). The T5 bias table stays fp32 in
-every workload; the Shaw and DeBERTa tables are bf16. ALiBi has no drawn
+every workload; the Shaw and DeBERTa tables are bf16; Transformer-XL's
+projection W [H, d, d] and biases u, v [2, H, d] are fp32. ALiBi has no drawn
 table: its per-head slopes (fp32) are the geometric sequence 2^(-8(h+1)/H)
 commonly used with it (the pages fix no values). The backward's output
 gradient dO [B,H,Lq,d] comes from its own generator seeded with
@@ -19,7 +20,8 @@ attention pages motivate: a tiny fp32 T5 encoder case, a T5-base-shaped
 encoder, a T5 causal decoder plus its cached-decode step (also over a cache
 that evicted half its tokens, keys at explicit positions), Shaw clipped
 relative keys/values at L=4096, and DeBERTa disentangled attention at
-k=256; plus ALiBi at the T5-base and T5-causal shapes.
+k=256; plus ALiBi at the T5-base and T5-causal shapes, and Transformer-XL
+over a segment and the cached memory of the previous one.
 """
 from __future__ import annotations
 
@@ -27,8 +29,9 @@ import dataclasses
 
 import torch
 
-MODE_T5, MODE_SHAW, MODE_DEBERTA, MODE_ALIBI = 0, 1, 2, 3
-MODE_NAMES = {MODE_T5: "t5", MODE_SHAW: "shaw", MODE_DEBERTA: "deberta", MODE_ALIBI: "alibi"}
+MODE_T5, MODE_SHAW, MODE_DEBERTA, MODE_ALIBI, MODE_TXL = 0, 1, 2, 3, 4
+MODE_NAMES = {MODE_T5: "t5", MODE_SHAW: "shaw", MODE_DEBERTA: "deberta", MODE_ALIBI: "alibi",
+              MODE_TXL: "txl"}
 
 
 @dataclasses.dataclass(frozen=True)
@@ -66,6 +69,8 @@ class Workload:
             return (n, self.d), (n, self.d)
         if self.mode == MODE_ALIBI:
             return (self.H,), None
+        if self.mode == MODE_TXL:
+            return (self.H, self.d, self.d), (2, self.H, self.d)
         n = 2 * self.rel_param
         return (n, self.H, self.d), (n, self.H, self.d)
 
@@ -75,7 +80,9 @@ class Workload:
         Counts the dense contractions the method requires: Q.K^T and P.V
         (halved to the visible triangle when causal), plus Shaw's Q.a_K^T
         and binned-P.a_V over the 2k+1 table, or DeBERTa's Q.Pk^T and
-        K.Pq^T over the 2k table. Gathers, exp and masking are not counted.
+        K.Pq^T over the 2k table. Transformer-XL's position term
+        (q_i + v) . r(i - j) is one more d-long product per visible pair.
+        Gathers, exp and masking are not counted.
         """
         B, H, Lq, Lk, d = self.B, self.H, self.Lq, self.Lk, self.d
         if self.causal:
@@ -85,6 +92,8 @@ class Workload:
         else:
             pairs = Lq * Lk
         core = 4.0 * B * H * pairs * d
+        if self.mode == MODE_TXL:
+            core += 2.0 * B * H * pairs * d
         if self.mode == MODE_SHAW:
             n = 2 * self.rel_param + 1
             core += 4.0 * B * H * Lq * n * d
@@ -101,7 +110,8 @@ class Workload:
         if self.cache_len:
             b += self.B * self.H * self.Lk * 4  # key positions
         t0, t1 = self.table_shapes()
-        for shp, tsz in ((t0, 4 if self.mode in (MODE_T5, MODE_ALIBI) else 2), (t1, 2)):
+        fp32_tables = self.mode in (MODE_T5, MODE_ALIBI, MODE_TXL)
+        for shp, tsz in ((t0, 4 if fp32_tables else 2), (t1, 4 if self.mode == MODE_TXL else 2)):
             if shp is not None:
                 c = 1
                 for s in shp:
@@ -130,6 +140,11 @@ WORKLOADS = {
     "alibi_bidir": Workload("alibi_bidir", 5, MODE_ALIBI, "bf16", 8, 12, 512, 512, 64),
     "alibi_causal": Workload("alibi_causal", 6, MODE_ALIBI, "bf16", 4, 16, 2048, 2048, 64,
                              causal=True),
+    # Transformer-XL: a 2048-token segment attending to itself and to the
+    # 2048 cached positions of the previous segment (keys 0 .. 4095, queries
+    # at positions 2048 .. 4095)
+    "txl_mem": Workload("txl_mem", 8, MODE_TXL, "bf16", 4, 16, 2048, 4096, 64, causal=True,
+                        q_offset=2048, table_sigma=0.1),
 }
 
 
@@ -143,7 +158,8 @@ def make_inputs(w: Workload, seed: int | None = None):
     Returns a dict with Q, K, V ([B,H,Lq|Lk,d], the workload dtype) and
     table0 / table1 (T5: fp32 bias [num_buckets, H], table1 None; Shaw:
     bf16 a_K, a_V [2k+1, d]; DeBERTa: bf16 Pk, Pq [2k, H, d]; ALiBi: fp32
-    slopes [H], table1 None).
+    slopes [H], table1 None; Transformer-XL: fp32 key projections of the
+    sinusoid W [H, d, d] and the biases u, v [2, H, d]).
     """
     g = torch.Generator(device="cpu")
     g.manual_seed(w.seed if seed is None else seed)
@@ -162,9 +178,10 @@ def make_inputs(w: Workload, seed: int | None = None):
     if w.mode == MODE_ALIBI:
         t0 = torch.tensor([2.0 ** (-8.0 * (h + 1) / w.H) for h in range(w.H)], dtype=torch.float32)
         return {"Q": q, "K": k, "V": v, "table0": t0, "table1": None}
-    tdt0 = torch.float32 if w.mode == MODE_T5 else torch.bfloat16
+    tdt0 = torch.float32 if w.mode in (MODE_T5, MODE_TXL) else torch.bfloat16
+    tdt1 = torch.float32 if w.mode == MODE_TXL else torch.bfloat16
     t0 = draw(s0, w.table_sigma, tdt0)
-    t1 = draw(s1, w.table_sigma, torch.bfloat16) if s1 is not None else None
+    t1 = draw(s1, w.table_sigma, tdt1) if s1 is not None else None
     x = {"Q": q, "K": k, "V": v, "table0": t0, "table1": t1}
     if w.cache_len:
         # a cache that kept Lk of its cache_len tokens, always the newest one,
