@@ -1,7 +1,8 @@
 /*
  * relpos_attn.h -- C ABI of the GB300 (sm_103a) relative-position attention
- * library (librelpos_attn.so): the forward pass, the T5 cached decode and the
- * T5 backward pass (relpos_t5_attn_bwd, at the end of this header).
+ * library (librelpos_attn.so): the forward pass (also over right-padded
+ * batches), the T5 cached decode and the T5 backward pass
+ * (relpos_t5_attn_bwd, at the end of this header).
  *
  * One forward call computes multi-head attention whose logits carry a relative-
  * position term that is formed inside the kernel and never written to
@@ -135,6 +136,29 @@ int relpos_attn_fwd(int mode, int dtype, const void* Q, const void* K, const voi
                     const void* table0, const void* table1, int B, int H, int Lq, int Lk,
                     int d, int num_buckets, int rel_param, int causal, int q_offset,
                     void* out, void* stream);
+
+/*
+ * relpos_attn_fwd_padded -- relpos_attn_fwd over a right-padded batch of
+ * sequences of different lengths. The pages do not treat padding; the
+ * reading here: batch element b holds lengths[b] valid query rows and keys
+ * (its first rows of Q, K and V), so its output equals that sequence
+ * computed alone, and its rows from lengths[b] on are written as zeros.
+ * Keys from lengths[b] on are masked for every row of element b; the rows and
+ * keys in the padding may hold anything. Positions and q_offset are as for
+ * relpos_attn_fwd (the relative offsets are the unpadded ones).
+ *
+ *   lengths     device, int32 [B], 4-byte aligned: read by the kernels, so
+ *               the host does not check its values; a negative length counts
+ *               as 0 (all rows zero), one beyond Lq / Lk as no padding.
+ *   all other arguments as for relpos_attn_fwd. Calls with T5 and Lq <= 8
+ *   run the fused kernel, not the split-key decode.
+ * Errors: as relpos_attn_fwd; RELPOS_ERR_INVALID_ARG for a null or
+ * misaligned lengths.
+ */
+int relpos_attn_fwd_padded(int mode, int dtype, const void* Q, const void* K, const void* V,
+                           const void* table0, const void* table1, const int* lengths, int B,
+                           int H, int Lq, int Lk, int d, int num_buckets, int rel_param, int causal,
+                           int q_offset, void* out, void* stream);
 
 /*
  * relpos_index_ids -- test hook: the device index generator the kernels use,

@@ -26,7 +26,7 @@ RELPOS_ERR_CUDA = -3
 RELPOS_ERR_DEVICE_TIMEOUT = -4
 RELPOS_ERR_SCRATCH_LIMIT = -5
 
-EXPORTED = ("relpos_attn_fwd", "relpos_index_ids", "relpos_check_status", "relpos_strerror",
+EXPORTED = ("relpos_attn_fwd", "relpos_attn_fwd_padded", "relpos_index_ids", "relpos_check_status", "relpos_strerror",
             "relpos_selftest_wait_timeout", "relpos_t5_decode_noalloc", "relpos_t5_decode_positions",
             "relpos_t5_attn_bwd")
 
@@ -51,6 +51,8 @@ def load_library(path: str = LIB_PATH):
     vp, i = ctypes.c_void_p, ctypes.c_int
     lib.relpos_attn_fwd.argtypes = [i, i, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, i, vp, vp]
     lib.relpos_attn_fwd.restype = i
+    lib.relpos_attn_fwd_padded.argtypes = [i, i, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, i, vp, vp]
+    lib.relpos_attn_fwd_padded.restype = i
     lib.relpos_index_ids.argtypes = [i, i, i, i, i, i, vp, vp]
     lib.relpos_index_ids.restype = i
     lib.relpos_check_status.argtypes = [vp]
@@ -75,6 +77,14 @@ def relpos_attn_fwd(mode, dtype, Q, K, V, table0, table1, B, H, Lq, Lk, d, num_b
                     rel_param, causal, q_offset, out, stream) -> int:
     return load_library().relpos_attn_fwd(mode, dtype, Q, K, V, table0, table1, B, H, Lq, Lk, d,
                                           num_buckets, rel_param, causal, q_offset, out, stream)
+
+
+def relpos_attn_fwd_padded(mode, dtype, Q, K, V, table0, table1, lengths, B, H, Lq, Lk, d,
+                           num_buckets, rel_param, causal, q_offset, out, stream) -> int:
+    """relpos_attn_fwd over a right-padded batch (lengths: device int32 [B])."""
+    return load_library().relpos_attn_fwd_padded(mode, dtype, Q, K, V, table0, table1, lengths, B, H,
+                                                 Lq, Lk, d, num_buckets, rel_param, causal, q_offset,
+                                                 out, stream)
 
 
 def relpos_index_ids(mode, n, rel_first, num_buckets, rel_param, causal, out_dev, stream) -> int:
@@ -136,11 +146,13 @@ def _stream(stream):
 
 def attention(Q, K, V, table0, table1=None, *, mode: int = MODE_T5, num_buckets: int = 32,
               rel_param: int = 128, causal: bool = False, q_offset: int = 0, out=None,
-              stream=None):
+              stream=None, lengths=None):
     """Run ``relpos_attn_fwd`` on CUDA tensors; returns ``out`` ([B,H,Lq,64]).
 
     Q [B,H,Lq,64] and K, V [B,H,Lk,64] are bf16 (or all fp32); tables as in
-    the C header. ``out`` is allocated like Q when not given.
+    the C header. ``out`` is allocated like Q when not given. ``lengths``
+    (int32 CUDA tensor [B]) makes it ``relpos_attn_fwd_padded``: a
+    right-padded batch, rows past each length zero.
     """
     import torch
     B, H, Lq, d = Q.shape
@@ -156,6 +168,15 @@ def attention(Q, K, V, table0, table1=None, *, mode: int = MODE_T5, num_buckets:
             raise ValueError("tensors must be contiguous CUDA tensors")
     if out is None:
         out = torch.empty_like(Q)
+    if lengths is not None:
+        if lengths.dtype != torch.int32 or not lengths.is_cuda or not lengths.is_contiguous():
+            raise TypeError("lengths must be a contiguous int32 CUDA tensor")
+        rc = relpos_attn_fwd_padded(mode, dtype, _ptr(Q), _ptr(K), _ptr(V), _ptr(table0),
+                                    _ptr(table1), _ptr(lengths), B, H, Lq, Lk, d, num_buckets,
+                                    rel_param, int(causal), q_offset, _ptr(out), _stream(stream))
+        if rc != RELPOS_OK:
+            raise RelposError(rc, "relpos_attn_fwd_padded")
+        return out
     rc = relpos_attn_fwd(mode, dtype, _ptr(Q), _ptr(K), _ptr(V), _ptr(table0), _ptr(table1),
                          B, H, Lq, Lk, d, num_buckets, rel_param, int(causal), q_offset,
                          _ptr(out), _stream(stream))

@@ -273,10 +273,15 @@ extern "C" int relpos_selftest_wait_timeout(int timeout_us, void* stream) {
   return cudaGetLastError() == cudaSuccess ? RELPOS_OK : RELPOS_ERR_CUDA;
 }
 
-extern "C" int relpos_attn_fwd(int mode, int dtype, const void* Q, const void* K, const void* V,
-                               const void* table0, const void* table1, int B, int H, int Lq, int Lk,
-                               int d, int num_buckets, int rel_param, int causal, int q_offset,
-                               void* out, void* stream) {
+namespace relpos {
+namespace {
+
+// relpos_attn_fwd and relpos_attn_fwd_padded; lengths (device int32 [B]) is
+// null for an unpadded batch.
+int attn_fwd_impl(int mode, int dtype, const void* Q, const void* K, const void* V,
+                  const void* table0, const void* table1, const int* lengths, int B, int H, int Lq,
+                  int Lk, int d, int num_buckets, int rel_param, int causal, int q_offset, void* out,
+                  void* stream) {
   if (mode != RELPOS_T5 && mode != RELPOS_SHAW && mode != RELPOS_DEBERTA && mode != RELPOS_ALIBI &&
       mode != RELPOS_TXL)
     return RELPOS_ERR_INVALID_ARG;
@@ -330,7 +335,7 @@ extern "C" int relpos_attn_fwd(int mode, int dtype, const void* Q, const void* K
     cudaGetLastError();
     return code;
   };
-  const bool decode = (mode == RELPOS_T5 && Lq <= 8);
+  const bool decode = (mode == RELPOS_T5 && Lq <= 8 && !lengths);
   size_t scratch_bytes = 0, off_conv = 0, off_part = 0;
   if (dtype == RELPOS_FP32) {
     off_conv = scratch_bytes;
@@ -408,7 +413,9 @@ extern "C" int relpos_attn_fwd(int mode, int dtype, const void* Q, const void* K
     p.kclip = rel_param;
     p.Qg = static_cast<const __nv_bfloat16*>(Qb);
     p.npairs = (Lq + 255) / 256;
-    p.nsplit = fwd_split_items(B * H * p.npairs, B * H, Lq, causal, num_sms());
+    p.lengths = lengths;
+    // split items balance a last pass of equally long items: not with padding
+    p.nsplit = lengths ? 0 : fwd_split_items(B * H * p.npairs, B * H, Lq, causal, num_sms());
     if (mode == RELPOS_T5) {
       p.bias = static_cast<const float*>(table0);
       p.t5 = t5;
@@ -500,6 +507,27 @@ extern "C" int relpos_attn_fwd(int mode, int dtype, const void* Q, const void* K
     return RELPOS_ERR_CUDA;
   }
   return RELPOS_OK;
+}
+
+}  // namespace
+}  // namespace relpos
+
+extern "C" int relpos_attn_fwd(int mode, int dtype, const void* Q, const void* K, const void* V,
+                               const void* table0, const void* table1, int B, int H, int Lq, int Lk,
+                               int d, int num_buckets, int rel_param, int causal, int q_offset,
+                               void* out, void* stream) {
+  return attn_fwd_impl(mode, dtype, Q, K, V, table0, table1, nullptr, B, H, Lq, Lk, d, num_buckets,
+                       rel_param, causal, q_offset, out, stream);
+}
+
+extern "C" int relpos_attn_fwd_padded(int mode, int dtype, const void* Q, const void* K,
+                                      const void* V, const void* table0, const void* table1,
+                                      const int* lengths, int B, int H, int Lq, int Lk, int d,
+                                      int num_buckets, int rel_param, int causal, int q_offset,
+                                      void* out, void* stream) {
+  if (!lengths || (reinterpret_cast<uintptr_t>(lengths) & 3u)) return RELPOS_ERR_INVALID_ARG;
+  return attn_fwd_impl(mode, dtype, Q, K, V, table0, table1, lengths, B, H, Lq, Lk, d, num_buckets,
+                       rel_param, causal, q_offset, out, stream);
 }
 
 extern "C" int relpos_t5_attn_bwd(const void* Q, const void* K, const void* V, const void* dO,

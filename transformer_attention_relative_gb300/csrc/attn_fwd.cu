@@ -126,11 +126,22 @@ struct Item {
   bool split;
 };
 
-// Key tiles [0, n) one 128-row query tile starting at row r0 visits.
-RP_DEVI int tile_keys(const FwdParams& p, int r0) {
-  if (r0 >= p.Lq) return 0;
-  int last_key = p.Lk - 1;
-  if (p.causal) last_key = min(last_key, min(r0 + kBM - 1, p.Lq - 1) + p.q_offset);
+// Valid query rows and keys of (batch, head) bh: the batch element's length
+// in a right-padded batch, otherwise no limit.
+RP_DEVI int seq_len(const FwdParams& p, int bh) {
+  if (!p.lengths) return 0x7fffffff;
+  const int n = __ldg(p.lengths + bh / p.H);
+  return n < 0 ? 0 : n;
+}
+
+// Key tiles [0, n) one 128-row query tile starting at row r0 visits, for a
+// sequence of nlen valid rows and keys (a padded batch element; rows from
+// nlen on give zero rows).
+RP_DEVI int tile_keys(const FwdParams& p, int r0, int nlen) {
+  const int lq = min(p.Lq, nlen), lk = min(p.Lk, nlen);
+  if (r0 >= lq || lk <= 0) return 0;
+  int last_key = lk - 1;
+  if (p.causal) last_key = min(last_key, min(r0 + kBM - 1, lq - 1) + p.q_offset);
   return last_key / kBN + 1;
 }
 
@@ -150,19 +161,20 @@ RP_DEVI Item make_item(const FwdParams& p, int w) {
   it.bh = wp % BH;
   it.h = it.bh % p.H;
   const int i0 = pair * 2 * kBM;
+  const int nlen = seq_len(p, it.bh);
   if (xs < 0) {
     it.split = false;
 #pragma unroll
     for (int x = 0; x < 2; ++x) {
       it.row0[x] = i0 + x * kBM;
       it.lo[x] = 0;
-      it.hi[x] = tile_keys(p, it.row0[x]);
+      it.hi[x] = tile_keys(p, it.row0[x], nlen);
     }
     it.ns = max(it.hi[0], it.hi[1]);
   } else {
     it.split = true;
     const int r0 = i0 + xs * kBM;
-    const int n = tile_keys(p, r0);
+    const int n = tile_keys(p, r0, nlen);
     const int na = (n + 1) >> 1;
     it.row0[0] = it.row0[1] = r0;
     it.lo[0] = 0;
@@ -307,6 +319,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // softmax warpgroups before their first table read; the MMA issuers touch
   // global memory only to report an error.
   griddep_launch_dependents();
+  // a padded batch's lengths are read by every role's item walk, the setup's
+  // included: wait for the previous kernel before anything else
+  if (p.lengths) griddep_wait();
   uint8_t* aux = smem + kOffAux;
   uint8_t* bkt = aux;  // T5: head-independent bucket of each table offset
   const int nrel = 2 * p.kclip + 1;
@@ -677,8 +692,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t stag_it = stag;
       const bool a_has = it.hi[0] > it.lo[0];
       if (x == 0 ? n_kv > 0 : a_has) ++stag;
-      if (n_kv == 0) continue;
+      const int nlen = seq_len(p, it.bh);  // valid rows and keys (padded batches)
+      if (n_kv == 0) {
+        // a padded batch element's query tile past its length: zero rows
+        const int r0 = sel(it.row0, x);
+        if (p.lengths && r0 < p.Lq && (!it.split || x == 0)) {
+          const int row = r0 + t;
+          if (row < p.Lq) {
+            const size_t base = (static_cast<size_t>(it.bh) * p.Lq + row) * kHeadDim;
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) + base * (OUT_F32 ? 4 : 2));
+#pragma unroll
+            for (int c = 0; c < (OUT_F32 ? 16 : 8); ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+        continue;
+      }
       const int i0 = sel(it.row0, x);
+      const int lk_eff = min(p.Lk, nlen);
       const int prow = i0 + t + p.q_offset;  // absolute position of this row
       const int p_lo = i0 + p.q_offset;      // of the tile's first row
 
@@ -798,10 +828,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           far_l = rel_hi <= -kc;
           far_r = rel_lo >= kc;
         }
-        const bool need_mask = (p.causal && j0 + kBN - 1 > p_lo) || (j0 + kBN > p.Lk);
+        const bool need_mask = (p.causal && j0 + kBN - 1 > p_lo) || (j0 + kBN > lk_eff);
         int lim = 127;
         if (need_mask) {
-          lim = p.Lk - 1 - j0;
+          lim = lk_eff - 1 - j0;
           if (p.causal) lim = min(lim, prow - j0);
         }
 
@@ -1156,8 +1186,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      const float inv_l = l_row > 0.f ? 1.f / l_row : 0.f;
       const int row = i0 + t;
+      // rows past a padded element's length are zero rows
+      const float inv_l = (l_row > 0.f && row < nlen) ? 1.f / l_row : 0.f;
       if (row < p.Lq) {
         const size_t base = (static_cast<size_t>(it.bh) * p.Lq + row) * kHeadDim + c0;
         const int ncol = merge ? 32 : kHeadDim;

@@ -62,6 +62,7 @@ struct FwdParams {
   int out_v8;  // out is 32-byte aligned: rows are written with 32-byte stores
   int stagger;  // offset the two softmax warpgroups by about half a tile
   int* status;
+  const int* lengths;  // [B] valid rows and keys per batch element (right-padded batch), or null
   // ALiBi
   const float* slopes;  // [H]
   // T5
