@@ -1,8 +1,8 @@
 /*
  * relpos_attn.h -- C ABI of the GB300 (sm_103a) relative-position attention
  * library (librelpos_attn.so): the forward pass (also over right-padded
- * batches), the T5 cached decode and the T5 backward pass
- * (relpos_t5_attn_bwd, at the end of this header).
+ * batches), the T5 cached decode and the T5 and ALiBi backward passes
+ * (relpos_t5_attn_bwd, relpos_alibi_attn_bwd, at the end of this header).
  *
  * One forward call computes multi-head attention whose logits carry a relative-
  * position term that is formed inside the kernel and never written to
@@ -275,18 +275,38 @@ int relpos_t5_decode_positions(const void* Q, const void* K, const void* V, cons
  *               the whole batch (the table is shared by it).
  * All pointers 16-byte aligned and caller-owned; the outputs must not overlap
  * the inputs. Limits: the distance R at which the last bucket starts (or the
- * largest offset present, if smaller) must be <= 4096
+ * largest offset present, if smaller) must be <= 2048
  * (RELPOS_ERR_UNSUPPORTED otherwise; max_distance 128 gives R = 91
- * bidirectional, 113 causal). Scratch: 8 * B * H * Lq bytes of row statistics
- * from cudaMallocAsync on `stream`, freed with cudaFreeAsync before the call
- * returns. dbias is accumulated with floating-point atomics, so its last bits
- * may differ between runs. Asynchronous on `stream`; device timeouts surface
- * through relpos_check_status().
+ * bidirectional, 113 causal). Scratch: about 264 * B * H * Lq bytes (an
+ * fp32 dQ accumulator and the row statistics, padded to 128-row tiles) from cudaMallocAsync on `stream`,
+ * freed with cudaFreeAsync before the call returns. dQ and dbias are
+ * accumulated with floating-point atomics, so their last bits may differ
+ * between runs. Asynchronous on `stream`; device timeouts surface through
+ * relpos_check_status().
  */
 int relpos_t5_attn_bwd(const void* Q, const void* K, const void* V, const void* dO,
                        const void* bias, int B, int H, int Lq, int Lk, int d, int num_buckets,
                        int max_distance, int causal, int q_offset, void* dQ, void* dK, void* dV,
                        void* dbias, void* stream);
+
+/*
+ * relpos_alibi_attn_bwd -- gradients of the ALiBi attention forward
+ * (relpos_attn_fwd with mode RELPOS_ALIBI, dtype RELPOS_BF16; "Relative
+ * Position Embeddings, in depth", section "ALiBi and RoPE: the two
+ * endpoints"). The pages treat the slopes as fixed; their gradient is still
+ * returned, dslope_h = -sum_{b,i,j} dS_ij |j - p_i|, with dS, dQ, dK, dV as
+ * for relpos_t5_attn_bwd.
+ *
+ *   Q, K, V, dO, B, H, Lq, Lk, d, causal, q_offset, dQ, dK, dV, stream: as for
+ *               relpos_t5_attn_bwd.
+ *   slopes      device, fp32 [H]: the forward call's slopes.
+ *   dslopes     device, fp32 [H], overwritten with the sum over the batch.
+ * Scratch, limits and errors as relpos_t5_attn_bwd (no saturation-distance
+ * limit). dslopes is accumulated with floating-point atomics.
+ */
+int relpos_alibi_attn_bwd(const void* Q, const void* K, const void* V, const void* dO,
+                          const void* slopes, int B, int H, int Lq, int Lk, int d, int causal,
+                          int q_offset, void* dQ, void* dK, void* dV, void* dslopes, void* stream);
 
 #ifdef __cplusplus
 }

@@ -1,7 +1,7 @@
-"""T5 attention backward on the GPU vs the fp64 oracle: dQ, dK, dV and the
-bias-table gradient, bidirectional and causal, ragged shapes, a cached prefix,
-saturated far tiles, other bucket parameters, empty inputs and the T5-base
-encoder workload in full.
+"""T5 and ALiBi attention backward on the GPU vs the fp64 oracle: dQ, dK, dV
+and the bias-table (slope) gradient, bidirectional and causal, ragged shapes,
+a cached prefix, saturated far tiles, other bucket parameters, empty inputs,
+the T5-base encoder workload in full and the causal decoder shape sampled.
 
 The gradients' magnitudes grow with L and differ between tensors, so each is
 compared after division by the oracle's largest magnitude for that tensor:
@@ -108,3 +108,58 @@ def test_backward_empty_inputs():
     torch.cuda.synchronize()
     assert torch.count_nonzero(dK) == 0 and torch.count_nonzero(dV) == 0
     assert torch.count_nonzero(db) == 0 and rp.check_status() == 0
+
+
+def run_alibi_backward(w, seed=None):
+    x = make_inputs(w, seed=seed)
+    dO = make_grad_output(w, seed=seed)
+    dev = torch.device("cuda")
+    Q, K, V, sl = (x[k].to(dev) for k in ("Q", "K", "V", "table0"))
+    got = rp.alibi_attention_backward(Q, K, V, dO.to(dev), sl, causal=w.causal, q_offset=w.q_offset)
+    torch.cuda.synchronize()
+    assert rp.check_status() == 0
+    got = [t.float().cpu().double().numpy() for t in got]
+    ref = orc.attention_backward(orc.MODE_ALIBI, x["Q"].double().numpy(), x["K"].double().numpy(),
+                                 x["V"].double().numpy(), x["table0"].double().numpy(), None,
+                                 dO.double().numpy(), causal=w.causal, q_offset=w.q_offset)
+    return got, list(ref[:4])
+
+
+@pytest.mark.parametrize("B,H,Lq,Lk,causal,qoff", [
+    (2, 3, 300, 300, False, 0),
+    (2, 3, 300, 300, True, 0),
+    (1, 2, 129, 517, False, 0),
+    (1, 2, 200, 437, True, 237),
+    (1, 2, 700, 700, True, 0),
+])
+def test_alibi_backward(B, H, Lq, Lk, causal, qoff):
+    w = WORKLOADS["alibi_bidir"].replace(B=B, H=H, Lq=Lq, Lk=Lk, causal=causal, q_offset=qoff)
+    got, ref = run_alibi_backward(w)
+    check(got, ref, w.name)
+
+
+def test_alibi_backward_full():
+    """ALiBi at the T5-base shape (B=8, H=12, L=512), every gradient entry."""
+    got, ref = run_alibi_backward(WORKLOADS["alibi_bidir"])
+    check(got, ref, "alibi_bidir")
+
+
+def test_backward_t5_causal_sampled():
+    """The T5 causal decoder shape (B=4, H=16, L=2048): dQ, dK and dV of batch
+    element 0 (every head) against the oracle run on that element alone."""
+    w = WORKLOADS["t5_causal"]
+    x = make_inputs(w)
+    dO = make_grad_output(w)
+    dev = torch.device("cuda")
+    got = rp.t5_attention_backward(*(x[k].to(dev) for k in ("Q", "K", "V")), dO.to(dev),
+                                   x["table0"].to(dev), num_buckets=w.num_buckets,
+                                   max_distance=w.rel_param, causal=True)
+    torch.cuda.synchronize()
+    assert rp.check_status() == 0
+    ref = orc.t5_attention_backward(*(x[k][:1].double().numpy() for k in ("Q", "K", "V")),
+                                    x["table0"].double().numpy(), dO[:1].double().numpy(),
+                                    max_distance=w.rel_param, causal=True)
+    for name, a, b in zip(("dQ", "dK", "dV"), got[:3], ref[:3]):
+        a = a[:1].float().cpu().double().numpy()
+        scale = max(float(np.max(np.abs(b))), 1e-30)
+        G.compare(a / scale, b / scale, what=f"t5_causal {name}")

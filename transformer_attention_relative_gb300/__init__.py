@@ -28,7 +28,7 @@ RELPOS_ERR_SCRATCH_LIMIT = -5
 
 EXPORTED = ("relpos_attn_fwd", "relpos_attn_fwd_padded", "relpos_index_ids", "relpos_check_status", "relpos_strerror",
             "relpos_selftest_wait_timeout", "relpos_t5_decode_noalloc", "relpos_t5_decode_positions",
-            "relpos_t5_attn_bwd")
+            "relpos_t5_attn_bwd", "relpos_alibi_attn_bwd")
 
 _lib = None
 
@@ -67,6 +67,8 @@ def load_library(path: str = LIB_PATH):
     lib.relpos_t5_decode_positions.restype = i
     lib.relpos_t5_attn_bwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, i, vp, vp, vp, vp, vp]
     lib.relpos_t5_attn_bwd.restype = i
+    lib.relpos_alibi_attn_bwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, vp, vp, vp, vp, vp]
+    lib.relpos_alibi_attn_bwd.restype = i
     _lib = lib
     return lib
 
@@ -126,6 +128,13 @@ def relpos_t5_attn_bwd(Q, K, V, dO, bias, B, H, Lq, Lk, d, num_buckets, max_dist
     """Gradients of the T5-bias attention: dQ, dK, dV and the bias table's."""
     return load_library().relpos_t5_attn_bwd(Q, K, V, dO, bias, B, H, Lq, Lk, d, num_buckets,
                                              max_distance, causal, q_offset, dQ, dK, dV, dbias, stream)
+
+
+def relpos_alibi_attn_bwd(Q, K, V, dO, slopes, B, H, Lq, Lk, d, causal, q_offset, dQ, dK, dV,
+                          dslopes, stream) -> int:
+    """Gradients of the ALiBi attention: dQ, dK, dV and the slopes'."""
+    return load_library().relpos_alibi_attn_bwd(Q, K, V, dO, slopes, B, H, Lq, Lk, d, causal,
+                                                q_offset, dQ, dK, dV, dslopes, stream)
 
 
 strerror = relpos_strerror
@@ -251,3 +260,27 @@ def t5_attention_backward(Q, K, V, dO, bias, *, num_buckets: int = 32, max_dista
         raise RelposError(rc, "relpos_t5_attn_bwd")
     return dQ, dK, dV, dbias
 
+
+
+def alibi_attention_backward(Q, K, V, dO, slopes, *, causal: bool = False, q_offset: int = 0,
+                             stream=None):
+    """Run ``relpos_alibi_attn_bwd`` on CUDA tensors; returns (dQ, dK, dV, dslopes).
+
+    Q, dO [B,H,Lq,64] and K, V [B,H,Lk,64] bf16; slopes [H] fp32.
+    """
+    import torch
+    B, H, Lq, d = Q.shape
+    Lk = K.shape[2]
+    for t in (Q, K, V, dO, slopes):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("tensors must be contiguous CUDA tensors")
+    if any(t.dtype != torch.bfloat16 for t in (Q, K, V, dO)) or slopes.dtype != torch.float32:
+        raise TypeError("Q, K, V, dO must be bf16 and slopes fp32")
+    dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
+    dslopes = torch.empty_like(slopes)
+    rc = relpos_alibi_attn_bwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(dO), _ptr(slopes), B, H, Lq, Lk, d,
+                               int(causal), q_offset, _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(dslopes),
+                               _stream(stream))
+    if rc != RELPOS_OK:
+        raise RelposError(rc, "relpos_alibi_attn_bwd")
+    return dQ, dK, dV, dslopes

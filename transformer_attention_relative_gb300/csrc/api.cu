@@ -102,6 +102,23 @@ bool make_tmap_table(CUtensorMap* m, const void* base, int H, int rows) {
   return r == CUDA_SUCCESS;
 }
 
+// fp32 [rows = L, inner = 64] per (batch*head) slab, 128-row x 32-column
+// boxes, 128-byte swizzle (the backward's dQ accumulator)
+bool make_tmap_acc(CUtensorMap* m, const void* base, int L, int BH) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(L),
+                        static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim) * 4,
+                           static_cast<cuuint64_t>(L) * kHeadDim * 4};
+  cuuint32_t box[3] = {32u, 128u, 1u};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 // Thresholds of the T5 log buckets: thr[q] is the smallest distance n whose
@@ -530,19 +547,25 @@ extern "C" int relpos_attn_fwd_padded(int mode, int dtype, const void* Q, const 
                        rel_param, causal, q_offset, out, stream);
 }
 
-extern "C" int relpos_t5_attn_bwd(const void* Q, const void* K, const void* V, const void* dO,
-                                  const void* bias, int B, int H, int Lq, int Lk, int d, int num_buckets,
-                                  int max_distance, int causal, int q_offset, void* dQ, void* dK, void* dV,
-                                  void* dbias, void* stream) {
+namespace relpos {
+namespace {
+
+// relpos_t5_attn_bwd (mode 0: table = bias [nb, H], dtable = dbias) and
+// relpos_alibi_attn_bwd (mode 3: table = slopes [H], dtable = dslopes).
+int attn_bwd_impl(int mode, const void* Q, const void* K, const void* V, const void* dO,
+                  const void* table, int B, int H, int Lq, int Lk, int d, int num_buckets,
+                  int max_distance, int causal, int q_offset, void* dQ, void* dK, void* dV,
+                  void* dtable, void* stream) {
   if (B < 0 || H < 0 || Lq < 0 || Lk < 0 || q_offset < 0 || d <= 0) return RELPOS_ERR_INVALID_ARG;
-  int rc = check_rel_params(RELPOS_T5, num_buckets, max_distance, causal);
+  int rc = check_rel_params(mode, num_buckets, max_distance, causal);
   if (rc != RELPOS_OK) return rc;
   if (d != kHeadDim) return RELPOS_ERR_UNSUPPORTED;
   if (B == 0 || H == 0) return RELPOS_OK;
-  if (!bias || !dbias || !aligned16(bias) || !aligned16(dbias)) return RELPOS_ERR_INVALID_ARG;
+  if (!table || !dtable || !aligned16(table) || !aligned16(dtable)) return RELPOS_ERR_INVALID_ARG;
   if (static_cast<long long>(B) * H > 65535) return RELPOS_ERR_UNSUPPORTED;
   if (Lq > (1 << 24) || Lk > (1 << 24) || q_offset > (1 << 28)) return RELPOS_ERR_UNSUPPORTED;
-  // every pointer is checked before anything (the dbias clear included) is queued
+  // every pointer is checked before anything (the table gradient's clear
+  // included) is queued
   if (Lq > 0 && (!dQ || !aligned16(dQ))) return RELPOS_ERR_INVALID_ARG;
   if (Lk > 0 && (!dK || !dV || !aligned16(dK) || !aligned16(dV))) return RELPOS_ERR_INVALID_ARG;
   if (Lq > 0 && Lk > 0) {
@@ -550,16 +573,21 @@ extern "C" int relpos_t5_attn_bwd(const void* Q, const void* K, const void* V, c
       if (!ptr || !aligned16(ptr)) return RELPOS_ERR_INVALID_ARG;
   }
   T5Index t5;
+  std::memset(&t5, 0, sizeof(t5));
   int R = 0;
-  const long long nmax = std::max(static_cast<long long>(Lk) - 1, static_cast<long long>(Lq) - 1 + q_offset);
-  rc = t5_setup(num_buckets, max_distance, causal, nmax, &t5, &R);
-  if (rc != RELPOS_OK) return rc;
-  if (Lq > 0 && Lk > 0 && (R < 1 || R > bwd_max_R())) return RELPOS_ERR_UNSUPPORTED;
+  if (mode == RELPOS_T5) {
+    const long long nmax =
+        std::max(static_cast<long long>(Lk) - 1, static_cast<long long>(Lq) - 1 + q_offset);
+    rc = t5_setup(num_buckets, max_distance, causal, nmax, &t5, &R);
+    if (rc != RELPOS_OK) return rc;
+    if (Lq > 0 && Lk > 0 && (R < 1 || R > bwd_max_R())) return RELPOS_ERR_UNSUPPORTED;
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t BH = static_cast<size_t>(B) * H;
   const size_t row_bytes = kHeadDim * 2;
-  if (cudaMemsetAsync(dbias, 0, static_cast<size_t>(num_buckets) * H * 4, s) != cudaSuccess)
-    return RELPOS_ERR_CUDA;
+  const size_t dtable_bytes =
+      (mode == RELPOS_T5 ? static_cast<size_t>(num_buckets) * H : static_cast<size_t>(H)) * sizeof(float);
+  if (cudaMemsetAsync(dtable, 0, dtable_bytes, s) != cudaSuccess) return RELPOS_ERR_CUDA;
   if (Lq == 0 || Lk == 0) {  // no score: every gradient is zero
     bool ok = true;
     if (Lq > 0) ok = ok && cudaMemsetAsync(dQ, 0, BH * Lq * row_bytes, s) == cudaSuccess;
@@ -567,23 +595,28 @@ extern "C" int relpos_t5_attn_bwd(const void* Q, const void* K, const void* V, c
                       cudaMemsetAsync(dV, 0, BH * Lk * row_bytes, s) == cudaSuccess;
     return ok ? RELPOS_OK : RELPOS_ERR_CUDA;
   }
-
   int* status = status_ptr();
   if (!status) return RELPOS_ERR_CUDA;
 
-  float* stats = nullptr;
-  if (cudaMallocAsync(reinterpret_cast<void**>(&stats), 2 * BH * Lq * sizeof(float), s) != cudaSuccess) {
+  // scratch: the fp32 dQ accumulator, then the row statistics (lse, D) with
+  // rows padded to whole 128-row query tiles
+  const int lq_pad = (Lq + 127) & ~127;
+  const size_t n_acc = BH * Lq * kHeadDim, n_stats = 2 * BH * static_cast<size_t>(lq_pad);
+  float* scratch = nullptr;
+  if (cudaMallocAsync(reinterpret_cast<void**>(&scratch), (n_acc + n_stats) * sizeof(float), s) != cudaSuccess) {
     cudaGetLastError();
     return RELPOS_ERR_CUDA;
   }
   auto done = [&](int code) {
-    if (cudaFreeAsync(stats, s) != cudaSuccess && code == RELPOS_OK) code = RELPOS_ERR_CUDA;
+    if (cudaFreeAsync(scratch, s) != cudaSuccess && code == RELPOS_OK) code = RELPOS_ERR_CUDA;
     if (code != RELPOS_OK) cudaGetLastError();
     return code;
   };
-  CUtensorMap tq, tk, tv, tdo;
+  if (cudaMemsetAsync(scratch, 0, n_acc * sizeof(float), s) != cudaSuccess) return done(RELPOS_ERR_CUDA);
+  CUtensorMap tq, tk, tv, tdo, tacc;
   if (!make_tmap(&tq, Q, Lq, static_cast<int>(BH)) || !make_tmap(&tk, K, Lk, static_cast<int>(BH)) ||
-      !make_tmap(&tv, V, Lk, static_cast<int>(BH)) || !make_tmap(&tdo, dO, Lq, static_cast<int>(BH)))
+      !make_tmap(&tv, V, Lk, static_cast<int>(BH)) || !make_tmap(&tdo, dO, Lq, static_cast<int>(BH)) ||
+      !make_tmap_acc(&tacc, scratch, Lq, static_cast<int>(BH)))
     return done(RELPOS_ERR_CUDA);
   BwdParams p;
   std::memset(&p, 0, sizeof(p));
@@ -595,18 +628,43 @@ extern "C" int relpos_t5_attn_bwd(const void* Q, const void* K, const void* V, c
   p.q_offset = q_offset;
   p.scale = 1.0f / std::sqrt(static_cast<float>(d));
   p.scale_log2 = p.scale * kLog2e;
-  p.bias = static_cast<const float*>(bias);
-  p.nb = num_buckets;
-  p.R = R;
-  p.t5 = t5;
-  p.lse = stats;
-  p.Dr = stats + BH * Lq;
+  if (mode == RELPOS_T5) {
+    p.bias = static_cast<const float*>(table);
+    p.nb = num_buckets;
+    p.R = R;
+    p.t5 = t5;
+    p.dbias = static_cast<float*>(dtable);
+  } else {
+    p.slopes = static_cast<const float*>(table);
+    p.dslopes = static_cast<float*>(dtable);
+  }
+  p.dQacc = scratch;
+  p.lse = scratch + n_acc;  // n_acc is a multiple of 64 floats: 256-byte aligned
+  p.Dr = scratch + n_acc + BH * lq_pad;
+  p.lq_pad = lq_pad;
   p.dQ = static_cast<__nv_bfloat16*>(dQ);
   p.dK = static_cast<__nv_bfloat16*>(dK);
   p.dV = static_cast<__nv_bfloat16*>(dV);
-  p.dbias = static_cast<float*>(dbias);
   p.status = status;
-  if (launch_bwd(tq, tk, tv, tdo, p, s) != cudaSuccess) return done(RELPOS_ERR_CUDA);
+  if (launch_bwd(mode, tq, tk, tv, tdo, tacc, p, s) != cudaSuccess) return done(RELPOS_ERR_CUDA);
   return done(RELPOS_OK);
 }
 
+}  // namespace
+}  // namespace relpos
+
+extern "C" int relpos_t5_attn_bwd(const void* Q, const void* K, const void* V, const void* dO,
+                                  const void* bias, int B, int H, int Lq, int Lk, int d, int num_buckets,
+                                  int max_distance, int causal, int q_offset, void* dQ, void* dK, void* dV,
+                                  void* dbias, void* stream) {
+  return attn_bwd_impl(RELPOS_T5, Q, K, V, dO, bias, B, H, Lq, Lk, d, num_buckets, max_distance, causal,
+                       q_offset, dQ, dK, dV, dbias, stream);
+}
+
+extern "C" int relpos_alibi_attn_bwd(const void* Q, const void* K, const void* V, const void* dO,
+                                     const void* slopes, int B, int H, int Lq, int Lk, int d, int causal,
+                                     int q_offset, void* dQ, void* dK, void* dV, void* dslopes,
+                                     void* stream) {
+  return attn_bwd_impl(RELPOS_ALIBI, Q, K, V, dO, slopes, B, H, Lq, Lk, d, 0, 0, causal, q_offset, dQ, dK,
+                       dV, dslopes, stream);
+}

@@ -1,40 +1,41 @@
-// attn_bwd.cu -- backward of the T5-bias relative-position attention, sm_103a.
+// attn_bwd.cu -- backward of the T5-bias and the ALiBi relative-position
+// attention, sm_103a.
 //
-// The forward ("Relative Position Embeddings, in depth", section "T5: one
-// scalar per head, looked up by bucket") is, per (batch, head),
-//   S = Q K^T / sqrt(d) + bias[bucket(j - p_i), h]  (masked), P = softmax_row(S), O = P V.
-// The chain rule gives
+// The forward ("Relative Position Embeddings, in depth", sections "T5: one
+// scalar per head, looked up by bucket" and "ALiBi and RoPE: the two
+// endpoints") is, per (batch, head),
+//   S = Q K^T / sqrt(d) + b(j - p_i)  (masked), P = softmax_row(S), O = P V,
+// with b the head's bias of the key-minus-query offset: the learned
+// bias[bucket(offset), h] (T5) or -slope_h |offset| (ALiBi). The chain rule
+// gives
 //   dV = P^T dO,  dP = dO V^T,  dS = P * (dP - D)  with D_i = sum_j P_ij dP_ij,
 //   dQ = dS K / sqrt(d),  dK = dS^T Q / sqrt(d),
 //   dbias[b, h] = the sum of dS_ij over every (batch, i, j) whose offset falls
-//   in bucket b (the table is learned and every offset of a bucket shares its
-//   value: "T5 Relative-Position Bias").
+//   in bucket b (every offset of a bucket shares its value: "T5
+//   Relative-Position Bias"), dslope_h = -sum dS_ij |j - p_i|.
 //
-// Two kernels, one CTA of four warps per 128-row tile; thread t owns TMEM lane t.
-//   relpos_bwd_dq_kernel    one query tile. Two passes over the visible K / V
-//                           tiles, each computing S = Q K^T and dP = dO V^T into
-//                           TMEM. Pass 1 keeps, per row, the running maximum,
-//                           sum and P-weighted sum of dP: the log-sum-exp and D
-//                           (D straight from its definition, exact to fp32, so
-//                           every row's dS sums to zero and nothing leaks into
-//                           the saturated buckets' gradients). Pass 2 forms dS
-//                           in registers, writes it (bf16) back to TMEM and
-//                           accumulates dQ += dS K with A read from TMEM. It
-//                           writes the row statistics for the second kernel and
-//                           adds its dS to dbias (per offset in shared memory,
-//                           then per bucket).
-//   relpos_bwd_dkdv_kernel  one key tile against the query tiles that see it:
-//                           S^T = K Q^T and dP^T = V dO^T, P^T and dS^T (bf16)
-//                           into TMEM, dV += P^T dO and dK += dS^T Q.
-// Every product has a shape of the forward's: the score-type products take two
-// K-major 128 x 64 tiles, the accumulating ones take A from TMEM and an
-// MN-major 128 x 64 tile as B. Streamed tiles pass through a two-stage ring
-// filled by TMA. Thread 0 issues the copies and the products; every wait has a
-// time limit, after which the kernel records RELPOS_ERR_DEVICE_TIMEOUT and
-// winds down (all threads leave the step loop together).
-//
-// Tensor memory (512 columns): S 0-127, dP 128-255, P (bf16 pairs) 256-319,
-// dS (bf16 pairs) 320-383, accumulators 384-447 (dQ, or dV) and 448-511 (dK).
+// Three kernels:
+//   relpos_bwd_stats_kernel  one 128-row query tile per CTA: lse_i (log2
+//     units) and D_i, straight from their definitions over S = Q K^T and
+//     dP = dO V^T (so every row's dS sums to zero up to rounding, and nothing
+//     leaks into a saturated bucket's gradient). Warp 0 loads (TMA), warp 1
+//     issues both products per key tile into one of two TMEM buffers, and two
+//     compute warpgroups take the key tiles alternately (thread t = query row
+//     t), each keeping running statistics; the two are merged at the end.
+//   relpos_bwd_dkdv_kernel   one 128-key tile per CTA against every query tile
+//     that sees it, taken in 64-row halves ("sub-steps"): S^T = K Q_h^T and
+//     dP^T = V dO_h^T into the half's TMEM buffer; the half's compute warpgroup
+//     (thread t = key t) forms P^T and dS^T = P^T (dP^T - D) in bf16 over the
+//     buffer's first 32 columns for dV += P^T dO_h and dK += dS^T Q_h, and dS
+//     itself into shared memory (query-major, the A operand of
+//     dQ_i = dS K, one product per query tile). A fourth warpgroup adds each
+//     dQ_i, scaled, into an fp32 accumulator in global memory. The bias
+//     gradient is summed per offset in shared memory (T5) or per thread
+//     (ALiBi's slope) and added once per CTA.
+//   relpos_bwd_dq_convert_kernel  the dQ accumulator to bf16.
+// Products of one CTA queue on the tensor core while the compute warpgroups
+// work on the other buffer. Every wait has a time limit, after which the kernel
+// records RELPOS_ERR_DEVICE_TIMEOUT and winds down without hanging.
 
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -50,505 +51,924 @@ namespace relpos {
 namespace {
 
 constexpr int kBT = 128;  // rows per tile, queries or keys
-constexpr int kBwdThreads = 128;
-constexpr int kMaxR = 4096;
+constexpr int kMaxR = 2048;
 constexpr uint32_t kTile = kBT * kHeadDim * 2;  // 16 KB
-constexpr uint32_t kOffBars = 6 * kTile;        // six tiles, then the barriers
-constexpr uint32_t kOffSlot = kOffBars + 64;
-constexpr uint32_t kOffAbort = kOffBars + 68;
-constexpr uint32_t kOffAux = kOffBars + 128;
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0, kColDP = 128, kColP = 256, kColDS = 320, kColAcc0 = 384, kColAcc1 = 448;
-// barriers: 0 the resident tiles, 1 / 2 ring stage full, 3 scores done, 4 all products done
-enum : int { kBarInit = 0, kBarFull = 1, kBarS = 3, kBarFin = 4, kNumBwdBars = 5 };
+constexpr uint32_t kHalfTile = kTile / 2;       // 64 rows
 
-constexpr uint32_t kIdScore = idesc_bf16_f32(kBT, kBT, 0, 0);     // both K-major
-constexpr uint32_t kIdAcc = idesc_bf16_f32(kBT, kHeadDim, 0, 1);  // A in TMEM, B MN-major
+constexpr uint32_t kIdS128 = idesc_bf16_f32(kBT, kBT, 0, 0);        // S = Q K^T (stats)
+constexpr uint32_t kIdS64 = idesc_bf16_f32(kBT, 64, 0, 0);          // S^T = K Q_h^T (64 queries)
+constexpr uint32_t kIdAcc = idesc_bf16_f32(kBT, kHeadDim, 0, 1);    // A from TMEM or K-major smem, B MN-major
 
 RP_DEVI void bwd_error(int* status) {
   if (status) atomicCAS(status, 0, -4);
 }
 
-// D (TMEM, 128 columns) = A B^T over the 64-wide head dimension: A and B are
-// 128-row tiles in shared memory, K-major (TMA's 128-byte swizzled rows).
-RP_DEVI void mma_scores(uint32_t d, uint32_t a_smem, uint32_t b_smem) {
-  const uint64_t da = smem_desc_sw128(a_smem, 16, 1024);
-  const uint64_t db = smem_desc_sw128(b_smem, 16, 1024);
-#pragma unroll
-  for (int kk = 0; kk < kHeadDim / 16; ++kk) umma_bf16_ss(d, da + 2 * kk, db + 2 * kk, kIdScore, kk > 0 ? 1u : 0u);
-}
-
-// D (TMEM, 64 columns) (+)= A B: A = 128 x 128 bf16 in TMEM (pairs per
-// column), B = a 128-row tile in shared memory read MN-major (its rows are the
-// reduction index, its 64 columns the output columns).
-RP_DEVI void mma_accum(uint32_t d, uint32_t a_tmem, uint32_t b_smem, bool acc) {
-  const uint64_t db = smem_desc_sw128(b_smem, 8192, 1024);
-#pragma unroll
-  for (int kk = 0; kk < kBT / 16; ++kk)
-    umma_bf16_ts(d, a_tmem + kk * 8, db + 128 * kk, kIdAcc, (acc || kk > 0) ? 1u : 0u);
-}
-
-// Store one 64-wide fp32 row (two 32-column TMEM loads) times `mul` as bf16.
-RP_DEVI void store_row_bf16(__nv_bfloat16* dst, const uint32_t (&a)[32], const uint32_t (&b)[32], float mul) {
-  uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (int v = 0; v < 8; ++v) {
-    const uint32_t* r = v < 4 ? &a[v * 8] : &b[(v - 4) * 8];
-    uint32_t w[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e)
-      w[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * mul, __uint_as_float(r[2 * e + 1]) * mul);
-    d4[v] = make_uint4(w[0], w[1], w[2], w[3]);
-  }
-}
-
-// The bias of every offset in [-R, R] (log2-scaled) for head h; entries 0 and
+// The head's log2-scaled bias of every offset in [-R, R] (T5); entries 0 and
 // 2R serve every offset beyond on their side.
-RP_DEVI void build_bias_table(float* tab, const BwdParams& p, int h) {
-  for (int x = threadIdx.x; x <= 2 * p.R; x += kBwdThreads)
+RP_DEVI void build_bias_table(float* tab, const BwdParams& p, int h, int tid, int nthreads) {
+  for (int x = tid; x <= 2 * p.R; x += nthreads)
     tab[x] = __ldg(p.bias + t5_bucket_dev(x - p.R, p.t5) * p.H + h) * kLog2e;
 }
 
-// Bounded wait for the copies thread 0 issued and nobody waited on (only on the
-// way out after a timeout): the CTA must not exit with a copy in flight.
-RP_DEVI void drain_copies(uint32_t sb, bool init_waited, int issued, int consumed) {
-  if (!init_waited) mbar_wait(sb + kOffBars + 8u * kBarInit, 0, 100000000ull);
-  for (int k = consumed; k < issued; ++k)
-    mbar_wait(sb + kOffBars + 8u * (kBarFull + (k & 1)), (k >> 1) & 1, 100000000ull);
+// Tiled bulk reduction shared -> global: element-wise fp32 add of a staged
+// box into the tensor (rows past its end are dropped); completion through a
+// bulk async-group of the issuing thread.
+RP_DEVI void tma_reduce_add_3d(const void* tmap, uint32_t src, int c0, int c1, int c2) {
+  asm volatile("cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   tmap),
+               "r"(src), "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+RP_DEVI void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// the bulk groups' shared-memory reads are done (the source may be reused)
+RP_DEVI void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+RP_DEVI void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// 8 consecutive 32-bit TMEM columns of this thread's lane.
+RP_DEVI void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
+               "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
 }
 
-// ---------------------------------------------------------------- dQ kernel
-// Shared memory: tile 0 Q, 1 dO, 2-3 K ring, 4-5 V ring; then the bias table,
-// the dS sums per offset and per bucket.
-__global__ void __launch_bounds__(kBwdThreads, 1)
-    relpos_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                         const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                         const BwdParams p) {
+// Untiled bulk copy global -> shared (16-byte aligned, size a multiple of 16)
+// completing on an mbarrier's transaction count.
+RP_DEVI void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+RP_DEVI void st_shared_u16(uint32_t addr, uint16_t v) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+
+// ================================================================ stats kernel
+// 12 warps: 0 TMA producer, 1 MMA issuer (TMEM owner), 2-3 idle, 4-7 and 8-11
+// the compute warpgroups of TMEM buffers 0 and 1 (even / odd key tiles).
+constexpr int kStThreads = 384;
+constexpr uint32_t kStOffQ = 0, kStOffdO = kTile, kStOffRing = 2 * kTile;  // ring: 2 x (K, V)
+constexpr uint32_t kStOffBar = kStOffRing + 4 * kTile;
+constexpr uint32_t kStOffAux = kStOffBar + 256;
+enum : uint32_t {
+  kStBarQ = 0,
+  kStBarFull = 1,   // + stage
+  kStBarEmpty = 3,  // + stage
+  kStBarS = 5,      // + buffer
+  kStBarSFree = 7,  // + buffer
+  kStNumBars = 9,
+};
+constexpr uint32_t kStSlot = 128, kStAbort = 132;
+
+template <int MODE>
+__global__ void __launch_bounds__(kStThreads, 1)
+    relpos_bwd_stats_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                            const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                            const BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sb = (raw + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (sb - raw);
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5;
-  const int bh = blockIdx.y;
-  const int h = bh % p.H;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int bh = blockIdx.y, h = bh % p.H;
   const int i0 = blockIdx.x * kBT;
-  const int R = p.R;
-  float* tab = reinterpret_cast<float*>(smem + kOffAux);
-  float* hist = tab + (2 * R + 1);   // dS summed per offset in (-R, R)
-  float* hist_b = hist + (2 * R + 1);  // per bucket
-  volatile int* abort_f = reinterpret_cast<volatile int*>(smem + kOffAbort);
-  auto bar = [&](int i) { return sb + kOffBars + 8u * i; };
+  auto bar = [&](uint32_t i) { return sb + kStOffBar + 8u * i; };
+  volatile int* abort_f = reinterpret_cast<volatile int*>(smem + kStOffBar + kStAbort);
+  float* tab = reinterpret_cast<float*>(smem + kStOffAux);                 // T5 bias by offset
+  float* mrg = tab + (MODE == 0 ? ((2 * p.R + 1 + 3) & ~3) : 0);           // [3][128] merge
 
   const int last_row = min(i0 + kBT, p.Lq) - 1;
   int n_kv = (p.Lk + kBT - 1) / kBT;
   if (p.causal) n_kv = min(n_kv, (last_row + p.q_offset) / kBT + 1);
-  const int nsteps = 2 * n_kv;  // pass 1, then pass 2, over the same key tiles
 
   if (tid == 0) {
-    for (int i = 0; i < kNumBwdBars; ++i) mbar_init(bar(i), 1);
+    for (uint32_t i = 0; i < kStNumBars; ++i)
+      mbar_init(bar(i), (i == kStBarSFree || i == kStBarSFree + 1) ? 128u : 1u);
     *abort_f = 0;
     fence_mbar_init();
   }
-  if (warp == 0) {
-    tmem_alloc(sb + kOffSlot, kTmemCols);
+  if (warp == 1) {
+    tmem_alloc(sb + kStOffBar + kStSlot, 512);
     tmem_relinquish();
   }
-  build_bias_table(tab, p, h);
-  for (int x = tid; x <= 2 * R; x += kBwdThreads) hist[x] = 0.f;
-  for (int x = tid; x < p.nb; x += kBwdThreads) hist_b[x] = 0.f;
+  griddep_wait();
+  if constexpr (MODE == 0) build_bias_table(tab, p, h, tid, kStThreads);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kOffSlot);
-  const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kStOffBar + kStSlot);
 
-  bool init_waited = false;
-  int issued = 0, consumed = 0;  // ring copies issued / waited for (thread 0)
-  if (tid == 0) {
-    tma_prefetch_desc(&tmQ);
-    tma_prefetch_desc(&tmK);
-    tma_prefetch_desc(&tmV);
-    tma_prefetch_desc(&tmdO);
-    mbar_arrive_expect_tx(bar(kBarInit), 2 * kTile);
-    tma_load_3d(sb + 0 * kTile, &tmQ, bar(kBarInit), 0, i0, bh);
-    tma_load_3d(sb + 1 * kTile, &tmdO, bar(kBarInit), 0, i0, bh);
-    mbar_arrive_expect_tx(bar(kBarFull), 2 * kTile);
-    tma_load_3d(sb + 2 * kTile, &tmK, bar(kBarFull), 0, 0, bh);
-    tma_load_3d(sb + 4 * kTile, &tmV, bar(kBarFull), 0, 0, bh);
-    issued = 1;
-  }
-
-  const int row = i0 + tid;
-  const bool row_ok = row < p.Lq;
-  const int prow = row + p.q_offset;
-  float m = -INFINITY, l = 0.f, dsum = 0.f, lse2 = 0.f, Drow = 0.f;
-  float sumL = 0.f, sumR = 0.f;  // dS of the offsets <= -R and >= R
-
-  for (int s = 0; s < nsteps; ++s) {
-    const bool pass2 = s >= n_kv;
-    const int kt = pass2 ? s - n_kv : s;
-    const int j0 = kt * kBT;
-    const int st = s & 1;
-    if (tid == 0 && !*abort_f) {
-      bool ok = true;
-      if (!init_waited) ok = init_waited = mbar_wait(bar(kBarInit), 0);
-      if (ok) ok = mbar_wait(bar(kBarFull + st), (s >> 1) & 1);
-      if (ok) {
-        ++consumed;
-        tc_fence_after();
-        mma_scores(tmem + kColS, sb + 0 * kTile, sb + (2 + st) * kTile);
-        mma_scores(tmem + kColDP, sb + 1 * kTile, sb + (4 + st) * kTile);
-        tc_commit(bar(kBarS));
-      } else {
-        *abort_f = 1;
+  // registers: the loading and issuing warps need few, the compute
+  // warpgroups hold 64 columns of S and dP at a time (4 x 32 x 56 + 8 x 32 x 224 <= 384 x 168)
+  if (warp < 4) {
+    setmaxnreg_dec<56>();
+  if (warp == 0) {
+    // ---------------------------------------------------------- producer
+    int issued = 0;
+    bool ok = true;
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmdO);
+      mbar_arrive_expect_tx(bar(kStBarQ), 2 * kTile);
+      tma_load_3d(sb + kStOffQ, &tmQ, bar(kStBarQ), 0, i0, bh);
+      tma_load_3d(sb + kStOffdO, &tmdO, bar(kStBarQ), 0, i0, bh);
+      for (int j = 0; j < n_kv; ++j) {
+        const uint32_t st = j & 1;
+        if (j >= 2 && !(ok = mbar_wait(bar(kStBarEmpty + st), ((j >> 1) - 1) & 1))) break;
+        mbar_arrive_expect_tx(bar(kStBarFull + st), 2 * kTile);
+        tma_load_3d(sb + kStOffRing + st * 2 * kTile, &tmK, bar(kStBarFull + st), 0, j * kBT, bh);
+        tma_load_3d(sb + kStOffRing + st * 2 * kTile + kTile, &tmV, bar(kStBarFull + st), 0, j * kBT, bh);
+        ++issued;
       }
+      if (!ok) {
+        *abort_f = 1;
+        bwd_error(p.status);
+      }
+      // never leave with copies in flight
+      mbar_wait(bar(kStBarQ), 0, 100000000ull);
+      for (int j = issued > 2 ? issued - 2 : 0; j < issued; ++j)
+        mbar_wait(bar(kStBarFull + (j & 1)), (j >> 1) & 1, 100000000ull);
     }
-    if (!mbar_wait(bar(kBarS), s & 1)) *abort_f = 1;
-    tc_fence_after();
-    // the next step's tiles go to the other stage, whose last readers (the
-    // products of step s - 1) completed before the scores of step s
-    if (tid == 0 && s + 1 < nsteps && !*abort_f) {
-      const int s1 = s + 1, st1 = s1 & 1;
-      const int kt1 = s1 >= n_kv ? s1 - n_kv : s1;
-      mbar_arrive_expect_tx(bar(kBarFull + st1), 2 * kTile);
-      tma_load_3d(sb + (2 + st1) * kTile, &tmK, bar(kBarFull + st1), 0, kt1 * kBT, bh);
-      tma_load_3d(sb + (4 + st1) * kTile, &tmV, bar(kBarFull + st1), 0, kt1 * kBT, bh);
-      ++issued;
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    bool ok = mbar_wait_warp(bar(kStBarQ), 0);
+    const uint64_t dq = smem_desc_sw128(sb + kStOffQ, 16, 1024);
+    const uint64_t ddo = smem_desc_sw128(sb + kStOffdO, 16, 1024);
+    for (int j = 0; ok && j < n_kv; ++j) {
+      const uint32_t st = j & 1, x = j & 1;
+      ok = mbar_wait_warp(bar(kStBarFull + st), (j >> 1) & 1);
+      if (ok && j >= 2) ok = mbar_wait_warp(bar(kStBarSFree + x), ((j >> 1) - 1) & 1);
+      if (!ok || __any_sync(0xffffffffu, *abort_f != 0)) break;
+      tc_fence_after();
+      const uint64_t dk = smem_desc_sw128(sb + kStOffRing + st * 2 * kTile, 16, 1024);
+      const uint64_t dv = smem_desc_sw128(sb + kStOffRing + st * 2 * kTile + kTile, 16, 1024);
+#pragma unroll
+      for (int kk = 0; kk < kHeadDim / 16; ++kk)
+        umma_bf16_ss_elect(tmem + x * 256, dq + 2 * kk, dk + 2 * kk, kIdS128, kk > 0 ? 1u : 0u);
+#pragma unroll
+      for (int kk = 0; kk < kHeadDim / 16; ++kk)
+        umma_bf16_ss_elect(tmem + x * 256 + 128, ddo + 2 * kk, dv + 2 * kk, kIdS128, kk > 0 ? 1u : 0u);
+      tc_commit_elect(bar(kStBarS + x));
+      tc_commit_elect(bar(kStBarEmpty + st));
     }
-    const int rb = j0 - prow;  // offset of column 0 for this row
+    if (!ok && lane == 0) {
+      *abort_f = 1;
+      bwd_error(p.status);
+    }
+  }
+  } else {
+    setmaxnreg_inc<224>();
+    // ---------------------------------------------------------- compute
+    const int x = (warp - 4) >> 2;  // TMEM buffer / parity of the key tiles taken
+    const int t = ((warp & 3) << 5) | lane;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const int row = i0 + t;
+    const int prow = row + p.q_offset;
+    const int R = p.R;
+    float alibi = 0.f;  // ALiBi: slope (log2 units) per unit of distance
+    if constexpr (MODE == 3) alibi = __ldg(p.slopes + h) * kLog2e;
+    // running row statistics in log2 units: maximum m (raised lazily, by more
+    // than kRescale at a time, which bounds every term by 2^kRescale), sum l
+    // of 2^(x - m) and dsum of 2^(x - m) dP
+    float m = -INFINITY;
+    float2 l2 = make_float2(0.f, 0.f), d2 = make_float2(0.f, 0.f);
+    const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+    bool err = false;
+    int cnt = 0;
+    for (int j = x; j < n_kv; j += 2, ++cnt) {
+      const bool ok = mbar_wait(bar(kStBarS + x), cnt & 1);
+      err = __any_sync(0xffffffffu, !ok);
+      // leave together: the TMEM loads below are warp-collective
+      if (err || __any_sync(0xffffffffu, *abort_f != 0)) break;
+      tc_fence_after();
+      const int j0 = j * kBT;
+      // tile classes (uniform over the CTA): offsets key - query position
+      // run from rel_lo to rel_hi; rows past Lq are not masked (their
+      // statistics are never used)
+      const int rel_hi = j0 + kBT - 1 - (i0 + p.q_offset), rel_lo = j0 - (i0 + kBT - 1 + p.q_offset);
+      const bool nomask = j0 + kBT <= p.Lk && (!p.causal || rel_hi <= 0);
+      const bool far_l = MODE == 0 && rel_hi <= -R;
+      const bool far_r = MODE == 0 && p.t5.bidir && rel_lo >= R;
+      // one row constant: T5 beyond the saturation distance; ALiBi with
+      // every key on one side (the rest is linear in the column)
+      const bool fast = nomask && (MODE == 0 ? (far_l || far_r) : (rel_hi <= 0 || rel_lo >= 0));
 #pragma unroll 1
-    for (int c0 = 0; c0 < kBT; c0 += 32) {
-      uint32_t sr[32], dr[32];
-      tmem_ld32(tmem + lane_base + kColS + c0, sr);
-      tmem_ld32(tmem + lane_base + kColDP + c0, dr);
-      tmem_ld_wait(sr);
-      tmem_ld_wait(dr);
-      if (!pass2) {
-        float x[32];
-        float cm = -INFINITY;
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int rel = rb + c0 + e;
-          const bool valid = row_ok && j0 + c0 + e < p.Lk && (!p.causal || rel <= 0);
-          const int idx = min(max(rel + R, 0), 2 * R);
-          x[e] = valid ? fmaf(__uint_as_float(sr[e]), p.scale_log2, tab[idx]) : -INFINITY;
-          cm = fmaxf(cm, x[e]);
+      for (int c0 = 0; c0 < kBT; c0 += 64) {
+        uint32_t sr[64], dr[64];
+        tmem_ld32(tmem + lane_base + x * 256 + c0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+        tmem_ld32(tmem + lane_base + x * 256 + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+        tmem_ld32(tmem + lane_base + x * 256 + 128 + c0, *reinterpret_cast<uint32_t(*)[32]>(&dr[0]));
+        tmem_ld32(tmem + lane_base + x * 256 + 128 + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(&dr[32]));
+        tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+        tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+        tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(&dr[0]));
+        tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(&dr[32]));
+        if (c0 + 64 == kBT) {  // the buffer is read: the products of tile j + 2 may overwrite it
+          tc_fence_before();
+          mbar_arrive(bar(kStBarSFree + x));
         }
-        const float mn = fmaxf(m, cm);
-        if (mn != -INFINITY) {
-          float acc = 0.f, accd = 0.f;
+        float* xv = reinterpret_cast<float*>(sr);
+        float bc = 0.f;  // the row constant of a fast tile (log2 units)
+        float mx;
+        if (fast) {
+          if constexpr (MODE == 0) {
+            bc = far_l ? tab[0] : tab[2 * R];
+          } else {
+            // -slope |j - p| = g (j - p) with g = slope (keys behind) or -slope (ahead):
+            // scaled scores plus g c, then the row constant g (j0 + c0 - p)
+            const float g = rel_hi <= 0 ? alibi : -alibi;
+            bc = g * static_cast<float>(j0 + c0 - prow);
+            const float2 g2 = make_float2(g, g);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const float w = ex2_approx(x[e] - mn);
-            acc += w;
-            accd = fmaf(w, __uint_as_float(dr[e]), accd);
-          }
-          const float rs = ex2_approx(m - mn);
-          l = fmaf(l, rs, acc);
-          dsum = fmaf(dsum, rs, accd);
-          m = mn;
-        }
-      } else {
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float ds2[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int rel = rb + c0 + e + u;
-            const bool valid = row_ok && j0 + c0 + e + u < p.Lk && (!p.causal || rel <= 0);
-            const int idx = min(max(rel + R, 0), 2 * R);
-            const float s2 = fmaf(__uint_as_float(sr[e + u]), p.scale_log2, tab[idx]);
-            const float pv = valid ? ex2_approx(s2 - lse2) : 0.f;
-            const float ds = pv * (__uint_as_float(dr[e + u]) - Drow);
-            ds2[u] = ds;
-            if (valid) {
-              if (rel <= -R)
-                sumL += ds;
-              else if (rel >= R)
-                sumR += ds;
-              else
-                atomicAdd(&hist[rel + R], ds);
+            for (int c = 0; c < 64; c += 2) {
+              const float2 v = __ffma2_rn(make_float2(static_cast<float>(c), static_cast<float>(c + 1)), g2,
+                                          __fmul2_rn(make_float2(xv[c], xv[c + 1]), sc2));
+              xv[c] = v.x;
+              xv[c + 1] = v.y;
             }
           }
-          pk[e / 2] = pack_bf16x2(ds2[0], ds2[1]);
-        }
-        tmem_st16(tmem + lane_base + kColDS + c0 / 2, pk);
-      }
-    }
-    if (pass2) tmem_st_wait();
-    if (s == n_kv - 1) {  // end of pass 1: the row statistics
-      lse2 = m == -INFINITY ? 0.f : m + log2f(l);
-      Drow = m == -INFINITY ? 0.f : dsum / l;
-      if (row_ok) {
-        p.lse[static_cast<size_t>(bh) * p.Lq + row] = lse2;
-        p.Dr[static_cast<size_t>(bh) * p.Lq + row] = Drow;
-      }
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (*abort_f) break;
-    if (pass2 && tid == 0) mma_accum(tmem + kColAcc0, tmem + kColDS, sb + (2 + st) * kTile, kt > 0);
-  }
-
-  // ---------------------------------------------------------------- epilogue
-  if (tid == 0) tc_commit(bar(kBarFin));
-  if (!mbar_wait(bar(kBarFin), 0)) *abort_f = 1;
-  tc_fence_after();
-  {
-    uint32_t a[32], b[32];
-    tmem_ld32(tmem + lane_base + kColAcc0, a);
-    tmem_ld32(tmem + lane_base + kColAcc0 + 32, b);
-    tmem_ld_wait(a);
-    tmem_ld_wait(b);
-    if (row_ok && !*abort_f)
-      store_row_bf16(p.dQ + (static_cast<size_t>(bh) * p.Lq + row) * kHeadDim, a, b, p.scale);
-  }
-  // dbias: the saturated sides per warp, then every offset's sum to its bucket
+          float m0 = -INFINITY, m1 = -INFINITY;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    sumL += __shfl_xor_sync(0xffffffffu, sumL, o);
-    sumR += __shfl_xor_sync(0xffffffffu, sumR, o);
-  }
-  if ((tid & 31) == 0) {
-    if (sumL != 0.f) atomicAdd(&hist_b[t5_bucket_dev(-R, p.t5)], sumL);
-    if (sumR != 0.f) atomicAdd(&hist_b[t5_bucket_dev(R, p.t5)], sumR);
-  }
-  __syncthreads();
-  for (int x = tid; x <= 2 * R; x += kBwdThreads)
-    if (hist[x] != 0.f) atomicAdd(&hist_b[t5_bucket_dev(x - R, p.t5)], hist[x]);
-  __syncthreads();
-  if (!*abort_f)
-    for (int x = tid; x < p.nb; x += kBwdThreads)
-      if (hist_b[x] != 0.f) atomicAdd(p.dbias + x * p.H + h, hist_b[x]);
-
-  if (tid == 0 && *abort_f) {
-    drain_copies(sb, init_waited, issued, consumed);
-    bwd_error(p.status);
+          for (int c = 0; c < 64; c += 4) {
+            m0 = max3f(m0, xv[c], xv[c + 1]);
+            m1 = max3f(m1, xv[c + 2], xv[c + 3]);
+          }
+          mx = MODE == 0 ? fmaf(fmaxf(m0, m1), p.scale_log2, bc) : fmaxf(m0, m1) + bc;
+        } else {
+          float m0 = -INFINITY, m1 = -INFINITY;
+#pragma unroll
+          for (int c = 0; c < 64; ++c) {
+            const int rel = j0 + c0 + c - prow;
+            const bool valid = j0 + c0 + c < p.Lk && (!p.causal || rel <= 0);
+            float b;
+            if constexpr (MODE == 0)
+              b = tab[min(max(rel + R, 0), 2 * R)];
+            else
+              b = -alibi * fabsf(static_cast<float>(rel));
+            xv[c] = valid ? fmaf(xv[c], p.scale_log2, b) : -INFINITY;
+            if (c & 1)
+              m1 = fmaxf(m1, xv[c]);
+            else
+              m0 = fmaxf(m0, xv[c]);
+          }
+          mx = fmaxf(m0, m1);
+        }
+        // lazy maximum: rescale the sums only when it grows by more than 2^8
+        if (mx > m + 8.f) {
+          const float a = ex2_approx(m - mx);  // 0 while m = -inf
+          l2 = __fmul2_rn(l2, make_float2(a, a));
+          d2 = __fmul2_rn(d2, make_float2(a, a));
+          m = mx;
+        }
+        const float mu = m == -INFINITY ? 0.f : m;
+        // 2^(x - m): fast tiles scale the raw scores (T5) inside the FMA
+        const float2 mul2 = (MODE == 0 && fast) ? sc2 : make_float2(1.f, 1.f);
+        const float off = bc - mu;
+        const float2 off2 = make_float2(off, off);
+#pragma unroll
+        for (int c = 0; c < 64; c += 2) {
+          float2 e = __ffma2_rn(make_float2(xv[c], xv[c + 1]), mul2, off2);
+          e.x = ex2_approx(e.x);
+          e.y = ex2_approx(e.y);
+          l2 = __fadd2_rn(l2, e);
+          d2 = __ffma2_rn(e, make_float2(__uint_as_float(dr[c]), __uint_as_float(dr[c + 1])), d2);
+        }
+      }
+    }
+    const float l = l2.x + l2.y, dsum = d2.x + d2.y;
+    if (err) {
+      *abort_f = 1;
+      bwd_error(p.status);
+    }
+    // merge the two warpgroups' statistics (buffer 1's into buffer 0's)
+    if (x == 1) {
+      mrg[t] = m;
+      mrg[128 + t] = l;
+      mrg[256 + t] = dsum;
+    }
+    named_bar_sync(1, 256);
+    if (x == 0 && !*abort_f) {
+      const float m1 = mrg[t], l1 = mrg[128 + t], d1 = mrg[256 + t];
+      const float M = fmaxf(m, m1);
+      float lse = 0.f, D = 0.f;
+      if (M != -INFINITY) {
+        const float a0 = m == -INFINITY ? 0.f : ex2_approx(m - M);
+        const float a1 = m1 == -INFINITY ? 0.f : ex2_approx(m1 - M);
+        const float lt = l * a0 + l1 * a1;
+        lse = M + log2f(lt);
+        D = (dsum * a0 + d1 * a1) / lt;
+      }
+      // rows past Lq (zero-filled Q and dO: D = 0) fill the padding that the
+      // dK / dV kernel reads whole
+      p.lse[static_cast<size_t>(bh) * p.lq_pad + row] = lse;
+      p.Dr[static_cast<size_t>(bh) * p.lq_pad + row] = D;
+    }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc(tmem, 512);
   }
 }
 
-// ---------------------------------------------------------------- dK / dV kernel
-// Shared memory: tile 0 K, 1 V, 2-3 Q ring, 4-5 dO ring; then the bias table
-// and the row statistics (log-sum-exp, D) of the current query tile, two
-// buffers.
-__global__ void __launch_bounds__(kBwdThreads, 1)
+// ================================================================ dK / dV kernel
+// 16 warps: 0 TMA producer, 1 MMA issuer (TMEM owner), 2-3 idle, 4-7 and 8-11
+// the compute warpgroups of query halves 0 and 1, 12-15 the dQ warpgroup.
+constexpr int kKvThreads = 512;
+constexpr uint32_t kKvOffK = 0, kKvOffV = kTile;
+// a ring stage: the query tile's Q and dO, then its 128 lse and 128 D values
+constexpr uint32_t kKvStage = 2 * kTile + 1024;
+constexpr uint32_t kKvOffRing = 2 * kTile;                    // 2 stages
+constexpr uint32_t kKvOffDS = kKvOffRing + 2 * kKvStage;       // 2 buffers x 2 key halves (K-major)
+constexpr uint32_t kKvOffBar = kKvOffDS + 4 * kTile;
+constexpr uint32_t kKvOffAux = kKvOffBar + 256;
+static_assert(kKvStage % 1024 == 0 && kKvOffDS % 1024 == 0, "swizzled tiles start on 1024-byte boundaries");
+enum : uint32_t {
+  kKvBarKV = 0,
+  kKvBarFull = 1,     // + stage: Q_i, dO_i
+  kKvBarEmpty = 3,    // + stage
+  kKvBarS = 5,        // + buffer: S^T, dP^T in TMEM
+  kKvBarP = 7,        // + buffer: P^T, dS^T written (128 arrivals)
+  kKvBarXFree = 9,    // + buffer: dV, dK products of the buffer done
+  kKvBarDsFree = 11,  // + dS buffer: the dQ tile staged there has been read by its reduction
+  kKvBarDqFull = 13,
+  kKvBarDqFree = 14,  // 128 arrivals
+  kKvBarFin = 15,
+  kKvBarDqStage = 16,  // the dQ warpgroup has staged a dQ tile (128 arrivals)
+  kKvNumBars = 17,
+};
+constexpr uint32_t kKvSlot = 192, kKvAbort = 196;
+// TMEM columns: S^T buffers 0-63 / 64-127, dP^T 128-191 / 192-255, dV 256,
+// dK 320, dQ tile 384. P^T and dS^T (bf16 pairs, 32 columns) overwrite the
+// first half of their buffer's S^T and dP^T.
+constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 320, kColDQ = 384;
+
+template <int MODE>
+__global__ void __launch_bounds__(kKvThreads, 1)
     relpos_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                            const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                           const BwdParams p) {
+                           const __grid_constant__ CUtensorMap tmAcc, const BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sb = (raw + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (sb - raw);
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5;
-  const int bh = blockIdx.y;
-  const int h = bh % p.H;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int bh = blockIdx.y, h = bh % p.H;
   const int j0 = blockIdx.x * kBT;
   const int R = p.R;
-  float* tab = reinterpret_cast<float*>(smem + kOffAux);
-  float* lse_s = tab + (2 * R + 1);  // [2][128]
-  float* d_s = lse_s + 2 * kBT;      // [2][128]
-  volatile int* abort_f = reinterpret_cast<volatile int*>(smem + kOffAbort);
-  auto bar = [&](int i) { return sb + kOffBars + 8u * i; };
+  auto bar = [&](uint32_t i) { return sb + kKvOffBar + 8u * i; };
+  volatile int* abort_f = reinterpret_cast<volatile int*>(smem + kKvOffBar + kKvAbort);
+  float* tab = reinterpret_cast<float*>(smem + kKvOffAux);   // T5 bias by offset (log2 units)
+  float* hist = tab + (2 * R + 1);                           // T5: dS per offset in (-R, R)
+  float* hist_b = hist + (2 * R + 1);                        // T5: per bucket
+  float* red = hist_b + kMaxT5Buckets;                       // side sums / ALiBi slope partials
 
   // query tiles that see a key of this tile: rows i with i + q_offset >= j0
   const int nqt = (p.Lq + kBT - 1) / kBT;
   int first = 0;
   if (p.causal && j0 - p.q_offset > 0) first = (j0 - p.q_offset) / kBT;
-  const int nsteps = nqt > first ? nqt - first : 0;
+  const int ntiles = nqt > first ? nqt - first : 0;
+  const int nsub = 2 * ntiles;
 
   if (tid == 0) {
-    for (int i = 0; i < kNumBwdBars; ++i) mbar_init(bar(i), 1);
+    for (uint32_t i = 0; i < kKvNumBars; ++i) {
+      uint32_t c = 1;
+      if (i == kKvBarP || i == kKvBarP + 1 || i == kKvBarDqFree || i == kKvBarDqStage) c = 128;
+      mbar_init(bar(i), c);
+    }
     *abort_f = 0;
     fence_mbar_init();
   }
-  if (warp == 0) {
-    tmem_alloc(sb + kOffSlot, kTmemCols);
+  if (warp == 1) {
+    tmem_alloc(sb + kKvOffBar + kKvSlot, 512);
     tmem_relinquish();
   }
-  build_bias_table(tab, p, h);
+  griddep_wait();
+  if constexpr (MODE == 0) {
+    build_bias_table(tab, p, h, tid, kKvThreads);
+    for (int x = tid; x <= 2 * R; x += kKvThreads) hist[x] = 0.f;
+    for (int x = tid; x < kMaxT5Buckets; x += kKvThreads) hist_b[x] = 0.f;
+  }
+  if (tid < 16) red[tid] = 0.f;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kOffSlot);
-  const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kKvOffBar + kKvSlot);
 
-  bool init_waited = nsteps == 0;
-  int issued = 0, consumed = 0;
-  if (tid == 0 && nsteps > 0) {
-    tma_prefetch_desc(&tmQ);
-    tma_prefetch_desc(&tmK);
-    tma_prefetch_desc(&tmV);
-    tma_prefetch_desc(&tmdO);
-    mbar_arrive_expect_tx(bar(kBarInit), 2 * kTile);
-    tma_load_3d(sb + 0 * kTile, &tmK, bar(kBarInit), 0, j0, bh);
-    tma_load_3d(sb + 1 * kTile, &tmV, bar(kBarInit), 0, j0, bh);
-    mbar_arrive_expect_tx(bar(kBarFull), 2 * kTile);
-    tma_load_3d(sb + 2 * kTile, &tmQ, bar(kBarFull), 0, first * kBT, bh);
-    tma_load_3d(sb + 4 * kTile, &tmdO, bar(kBarFull), 0, first * kBT, bh);
-    issued = 1;
-  }
-
-  const int key = j0 + tid;
-  const bool key_ok = key < p.Lk;
-  for (int s = 0; s < nsteps; ++s) {
-    const int i0 = (first + s) * kBT;
-    const int st = s & 1;
-    {  // this query tile's statistics (the buffer's last readers were two steps ago)
-      const int i = i0 + tid;
-      lse_s[st * kBT + tid] = i < p.Lq ? __ldg(p.lse + static_cast<size_t>(bh) * p.Lq + i) : 0.f;
-      d_s[st * kBT + tid] = i < p.Lq ? __ldg(p.Dr + static_cast<size_t>(bh) * p.Lq + i) : 0.f;
-    }
-    if (tid == 0 && !*abort_f) {
-      bool ok = true;
-      if (!init_waited) ok = init_waited = mbar_wait(bar(kBarInit), 0);
-      if (ok) ok = mbar_wait(bar(kBarFull + st), (s >> 1) & 1);
-      if (ok) {
-        ++consumed;
-        tc_fence_after();
-        mma_scores(tmem + kColS, sb + 0 * kTile, sb + (2 + st) * kTile);   // S^T = K Q^T
-        mma_scores(tmem + kColDP, sb + 1 * kTile, sb + (4 + st) * kTile);  // dP^T = V dO^T
-        tc_commit(bar(kBarS));
-      } else {
-        *abort_f = 1;
-      }
-    }
-    __syncthreads();  // the statistics
-    if (!mbar_wait(bar(kBarS), s & 1)) *abort_f = 1;
-    tc_fence_after();
-    if (tid == 0 && s + 1 < nsteps && !*abort_f) {
-      const int st1 = (s + 1) & 1;
-      mbar_arrive_expect_tx(bar(kBarFull + st1), 2 * kTile);
-      tma_load_3d(sb + (2 + st1) * kTile, &tmQ, bar(kBarFull + st1), 0, i0 + kBT, bh);
-      tma_load_3d(sb + (4 + st1) * kTile, &tmdO, bar(kBarFull + st1), 0, i0 + kBT, bh);
-      ++issued;
-    }
-    const int rb = key - i0 - p.q_offset;  // offset of column 0 for this key
-    const float* lse_t = lse_s + st * kBT;
-    const float* d_t = d_s + st * kBT;
-#pragma unroll 1
-    for (int c0 = 0; c0 < kBT; c0 += 32) {
-      uint32_t sr[32], dr[32];
-      tmem_ld32(tmem + lane_base + kColS + c0, sr);
-      tmem_ld32(tmem + lane_base + kColDP + c0, dr);
-      tmem_ld_wait(sr);
-      tmem_ld_wait(dr);
-      uint32_t pp[16], pd[16];
-#pragma unroll
-      for (int e = 0; e < 32; e += 2) {
-        float pv2[2], ds2[2];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int c = c0 + e + u;
-          const int rel = rb - c;
-          const bool valid = i0 + c < p.Lq && (!p.causal || rel <= 0);
-          const int idx = min(max(rel + R, 0), 2 * R);
-          const float s2 = fmaf(__uint_as_float(sr[e + u]), p.scale_log2, tab[idx]);
-          const float pv = valid ? ex2_approx(s2 - lse_t[c]) : 0.f;
-          pv2[u] = pv;
-          ds2[u] = pv * (__uint_as_float(dr[e + u]) - d_t[c]);
+  if (warp < 4) {
+    setmaxnreg_dec<56>();
+    if (warp == 0) {
+      // -------------------------------------------------------- producer
+      if (lane == 0 && ntiles > 0) {
+        bool ok = true;
+        int issued = 0;
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+        tma_prefetch_desc(&tmdO);
+        mbar_arrive_expect_tx(bar(kKvBarKV), 2 * kTile);
+        tma_load_3d(sb + kKvOffK, &tmK, bar(kKvBarKV), 0, j0, bh);
+        tma_load_3d(sb + kKvOffV, &tmV, bar(kKvBarKV), 0, j0, bh);
+        for (int i = 0; i < ntiles; ++i) {
+          const uint32_t st = i & 1;
+          if (i >= 2 && !(ok = mbar_wait(bar(kKvBarEmpty + st), ((i >> 1) - 1) & 1))) break;
+          const int q0 = (first + i) * kBT;
+          const uint32_t dst = sb + kKvOffRing + st * kKvStage;
+          const size_t so = static_cast<size_t>(bh) * p.lq_pad + q0;  // 512-byte aligned rows
+          mbar_arrive_expect_tx(bar(kKvBarFull + st), 2 * kTile + 1024);
+          tma_load_3d(dst, &tmQ, bar(kKvBarFull + st), 0, q0, bh);
+          tma_load_3d(dst + kTile, &tmdO, bar(kKvBarFull + st), 0, q0, bh);
+          bulk_load(dst + 2 * kTile, p.lse + so, 512, bar(kKvBarFull + st));
+          bulk_load(dst + 2 * kTile + 512, p.Dr + so, 512, bar(kKvBarFull + st));
+          ++issued;
         }
-        pp[e / 2] = pack_bf16x2(pv2[0], pv2[1]);
-        pd[e / 2] = pack_bf16x2(ds2[0], ds2[1]);
+        if (!ok) {
+          *abort_f = 1;
+          bwd_error(p.status);
+        }
+        mbar_wait(bar(kKvBarKV), 0, 100000000ull);
+        for (int i = issued > 2 ? issued - 2 : 0; i < issued; ++i)
+          mbar_wait(bar(kKvBarFull + (i & 1)), (i >> 1) & 1, 100000000ull);
       }
-      tmem_st16(tmem + lane_base + kColP + c0 / 2, pp);
-      tmem_st16(tmem + lane_base + kColDS + c0 / 2, pd);
+    } else if (warp == 1) {
+      // -------------------------------------------------------- MMA issuer
+      bool ok = ntiles == 0 || mbar_wait_warp(bar(kKvBarKV), 0);
+      const uint64_t dk_a = smem_desc_sw128(sb + kKvOffK, 16, 1024);    // K as K-major A / B
+      const uint64_t dv_a = smem_desc_sw128(sb + kKvOffV, 16, 1024);
+      const uint64_t dk_mn = smem_desc_sw128(sb + kKvOffK, 8192, 1024);  // K as MN-major B (dQ)
+      // S^T and dP^T of sub-step s into buffer s & 1
+      auto issue_scores = [&](int s) -> bool {
+        const int i = s >> 1, hf = s & 1;
+        const uint32_t st = i & 1;
+        if (hf == 0 && !mbar_wait_warp(bar(kKvBarFull + st), (i >> 1) & 1)) return false;
+        if (s >= 2 && !mbar_wait_warp(bar(kKvBarXFree + hf), ((s >> 1) - 1) & 1)) return false;
+        tc_fence_after();
+        const uint32_t qa = sb + kKvOffRing + st * kKvStage + hf * kHalfTile;
+        const uint64_t dqh = smem_desc_sw128(qa, 16, 1024);
+        const uint64_t ddoh = smem_desc_sw128(qa + kTile, 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < kHeadDim / 16; ++kk)
+          umma_bf16_ss_elect(tmem + kColS + hf * 64, dk_a + 2 * kk, dqh + 2 * kk, kIdS64, kk > 0 ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < kHeadDim / 16; ++kk)
+          umma_bf16_ss_elect(tmem + kColDP + hf * 64, dv_a + 2 * kk, ddoh + 2 * kk, kIdS64, kk > 0 ? 1u : 0u);
+        tc_commit_elect(bar(kKvBarS + hf));
+        return true;
+      };
+      if (ok && nsub > 0) ok = issue_scores(0);
+      if (ok && nsub > 1) ok = issue_scores(1);
+      for (int s = 0; ok && s < nsub; ++s) {
+        const int i = s >> 1, hf = s & 1;
+        const uint32_t st = i & 1;
+        ok = mbar_wait_warp(bar(kKvBarP + hf), (s >> 1) & 1);
+        if (!ok || __any_sync(0xffffffffu, *abort_f != 0)) break;
+        tc_fence_after();
+        // dV += P^T dO_h, dK += dS^T Q_h (A from TMEM, B = the half's 64 rows, MN-major)
+        const uint32_t qa = sb + kKvOffRing + st * kKvStage + hf * kHalfTile;
+        const uint64_t bq = smem_desc_sw128(qa, 8192, 1024);
+        const uint64_t bdo = smem_desc_sw128(qa + kTile, 8192, 1024);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          umma_bf16_ts_elect(tmem + kColDV, tmem + kColS + hf * 64 + kk * 8, bdo + 128 * kk, kIdAcc,
+                             (s > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          umma_bf16_ts_elect(tmem + kColDK, tmem + kColDP + hf * 64 + kk * 8, bq + 128 * kk, kIdAcc,
+                             (s > 0 || kk > 0) ? 1u : 0u);
+        tc_commit_elect(bar(kKvBarXFree + hf));
+        if (hf == 1) {
+          // dQ_i = dS K: A = dS (query-major, two 64-key halves), B = K MN-major
+          if (i > 0) ok = mbar_wait_warp(bar(kKvBarDqFree), (i - 1) & 1);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t ds = sb + kKvOffDS + (i & 1) * 2 * kTile;
+#pragma unroll
+          for (int kk = 0; kk < kBT / 16; ++kk) {
+            const uint64_t da = smem_desc_sw128(ds + (kk >> 2) * kTile, 16, 1024) + 2 * (kk & 3);
+            umma_bf16_ss_elect(tmem + kColDQ, da, dk_mn + 128 * kk, kIdAcc, kk > 0 ? 1u : 0u);
+          }
+          tc_commit_elect(bar(kKvBarDqFull));
+          tc_commit_elect(bar(kKvBarEmpty + st));  // the tile's Q and dO are read
+        }
+        if (s + 2 < nsub) {
+          ok = issue_scores(s + 2);
+          if (!ok) break;
+        }
+      }
+      if (!ok && lane == 0) {
+        *abort_f = 1;
+        bwd_error(p.status);
+      }
+      tc_commit_elect(bar(kKvBarFin));
     }
-    tmem_st_wait();
-    tc_fence_before();
-    __syncthreads();
+  } else if (warp < 12) {
+    setmaxnreg_inc<200>();
+    // ---------------------------------------------------------- compute
+    const int hf = (warp - 4) >> 2;  // query half 0 / 1 of every tile = TMEM buffer
+    const int t = ((warp & 3) << 5) | lane;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const int key = j0 + t;
+    const bool key_ok = key < p.Lk;
+    float alibi = 0.f;
+    if constexpr (MODE == 3) alibi = __ldg(p.slopes + h) * kLog2e;
+    float sumL = 0.f, sumR = 0.f, dsl = 0.f;  // T5 saturated sides; ALiBi slope gradient
+    const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+    bool err = false;
+    for (int s = hf, c = 0; s < nsub; s += 2, ++c) {
+      const int i = s >> 1;
+      const int q0 = (first + i) * kBT + hf * 64;  // first query of the sub-step
+      bool ok = mbar_wait(bar(kKvBarS + hf), c & 1);
+      err = __any_sync(0xffffffffu, !ok);
+      // leave together: the TMEM loads and stores below are warp-collective
+      if (err || __any_sync(0xffffffffu, *abort_f != 0)) break;
+      tc_fence_after();
+      // this sub-step's lse and D, staged with the query tile
+      const float* lse_s = reinterpret_cast<const float*>(smem + kKvOffRing + (i & 1) * kKvStage + 2 * kTile) + hf * 64;
+      const float* dd_s = lse_s + 128;
+      uint32_t sr[64], dr[64];
+      tmem_ld32(tmem + lane_base + kColS + hf * 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+      tmem_ld32(tmem + lane_base + kColS + hf * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+      tmem_ld32(tmem + lane_base + kColDP + hf * 64, *reinterpret_cast<uint32_t(*)[32]>(&dr[0]));
+      tmem_ld32(tmem + lane_base + kColDP + hf * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&dr[32]));
+      tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+      tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+      tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(&dr[0]));
+      tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(&dr[32]));
+      // offsets key - query position: rb - c for column c, rel_lo .. rel_hi
+      // over the sub-step (uniform classes)
+      const int rb = key - q0 - p.q_offset;
+      const int rel_hi = j0 + kBT - 1 - (q0 + p.q_offset), rel_lo = j0 - (q0 + 63 + p.q_offset);
+      const bool nomask = j0 + kBT <= p.Lk && q0 + 64 <= p.Lq && (!p.causal || rel_hi <= 0);
+      const bool far_l = MODE == 0 && rel_hi <= -R;
+      const bool far_r = MODE == 0 && p.t5.bidir && rel_lo >= R;
+      // dS goes to shared memory as it is formed: the dQ product of tile
+      // i - 2 must have read this buffer
+      if (i >= 2) {
+        ok = mbar_wait(bar(kKvBarDsFree + (i & 1)), ((i >> 1) - 1) & 1);
+        err = __any_sync(0xffffffffu, !ok);
+        if (err) break;
+      }
+      // Every 16 columns: P^T and dS^T (bf16 pairs) over the first half of
+      // the buffer's S^T and dP^T columns, and dS into the query-major tile
+      // (row q = query, key t in half t / 64, K-major, 128-byte swizzle).
+      const uint32_t ds_base = sb + kKvOffDS + (i & 1) * 2 * kTile + (t >> 6) * kTile +
+                               static_cast<uint32_t>(t & 7) * 2u + static_cast<uint32_t>(hf) * 64u * 128u;
+      const uint32_t kc = static_cast<uint32_t>((t & 63) >> 3);
+      auto emit = [&](int g, const uint32_t (&pp)[8], const uint32_t (&pd)[8]) {
+        tmem_st8(tmem + lane_base + kColS + hf * 64 + 8 * g, pp);
+        tmem_st8(tmem + lane_base + kColDP + hf * 64 + 8 * g, pd);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const uint32_t q = static_cast<uint32_t>(16 * g + 2 * e + u);  // row within the half
+            st_shared_u16(ds_base + q * 128u + ((kc ^ (q & 7u)) << 4),
+                          static_cast<uint16_t>(u ? (pd[e] >> 16) : (pd[e] & 0xffffu)));
+          }
+        }
+      };
+      if (nomask && (MODE == 0 ? (far_l || far_r) : (rel_hi <= 0 || rel_lo >= 0))) {
+        // one bias per row (T5 beyond the saturation distance), or ALiBi with
+        // every key on one side: the logit is s * scale + g (c - rb) with
+        // g = -slope (keys behind: |rel| = c - rb) or +slope (ahead: rb - c)
+        const float bc = MODE == 0 ? (far_l ? tab[0] : tab[2 * R]) : 0.f;
+        const float g = MODE == 0 ? 0.f : (rel_hi <= 0 ? -alibi : alibi);
+        const float2 g2 = make_float2(g, g);
+        const float nrb = -static_cast<float>(rb);
+        float2 acc = make_float2(0.f, 0.f);  // T5: dS of the side; ALiBi: sum dS (c - rb)
+#pragma unroll
+        for (int gi = 0; gi < 4; ++gi) {
+          uint32_t pp[8], pd[8];
+#pragma unroll
+          for (int qq = 0; qq < 4; ++qq) {
+            const int q = 4 * gi + qq;
+            const float4 L = *reinterpret_cast<const float4*>(lse_s + 4 * q);
+            const float4 D = *reinterpret_cast<const float4*>(dd_s + 4 * q);
+            float2 off0 = make_float2(bc - L.x, bc - L.y), off1 = make_float2(bc - L.z, bc - L.w);
+            float2 cm0 = make_float2(0.f, 0.f), cm1 = make_float2(0.f, 0.f);
+            if constexpr (MODE == 3) {
+              cm0 = __fadd2_rn(make_float2(static_cast<float>(4 * q), static_cast<float>(4 * q + 1)),
+                               make_float2(nrb, nrb));
+              cm1 = __fadd2_rn(make_float2(static_cast<float>(4 * q + 2), static_cast<float>(4 * q + 3)),
+                               make_float2(nrb, nrb));
+              off0 = __ffma2_rn(cm0, g2, off0);
+              off1 = __ffma2_rn(cm1, g2, off1);
+            }
+            float2 e0 = __ffma2_rn(make_float2(__uint_as_float(sr[4 * q]), __uint_as_float(sr[4 * q + 1])), sc2, off0);
+            float2 e1 =
+                __ffma2_rn(make_float2(__uint_as_float(sr[4 * q + 2]), __uint_as_float(sr[4 * q + 3])), sc2, off1);
+            e0.x = ex2_approx(e0.x);
+            e0.y = ex2_approx(e0.y);
+            e1.x = ex2_approx(e1.x);
+            e1.y = ex2_approx(e1.y);
+            const float2 t0 = __fadd2_rn(make_float2(__uint_as_float(dr[4 * q]), __uint_as_float(dr[4 * q + 1])),
+                                         make_float2(-D.x, -D.y));
+            const float2 t1 = __fadd2_rn(
+                make_float2(__uint_as_float(dr[4 * q + 2]), __uint_as_float(dr[4 * q + 3])), make_float2(-D.z, -D.w));
+            const float2 d0 = __fmul2_rn(e0, t0), d1 = __fmul2_rn(e1, t1);
+            if constexpr (MODE == 0) {
+              acc = __fadd2_rn(acc, __fadd2_rn(d0, d1));
+            } else {
+              acc = __ffma2_rn(d0, cm0, acc);
+              acc = __ffma2_rn(d1, cm1, acc);
+            }
+            pp[2 * qq] = pack_bf16x2(e0.x, e0.y);
+            pp[2 * qq + 1] = pack_bf16x2(e1.x, e1.y);
+            pd[2 * qq] = pack_bf16x2(d0.x, d0.y);
+            pd[2 * qq + 1] = pack_bf16x2(d1.x, d1.y);
+          }
+          emit(gi, pp, pd);
+        }
+        const float a = acc.x + acc.y;
+        if constexpr (MODE == 0) {
+          if (far_l)
+            sumL += a;
+          else
+            sumR += a;
+        } else {
+          dsl += rel_hi <= 0 ? a : -a;  // |rel| = c - rb behind, rb - c ahead
+        }
+      } else {
+        // per element: masks, the bias of each offset, T5 offsets inside the
+        // saturation distance summed per offset in shared memory
+#pragma unroll
+        for (int gi = 0; gi < 4; ++gi) {
+          uint32_t pp[8], pd[8];
+#pragma unroll
+          for (int e = 0; e < 16; e += 2) {
+            float pv[2], dsv[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int cc = 16 * gi + e + u;
+              const int rel = rb - cc;
+              const bool valid = key_ok && q0 + cc < p.Lq && (!p.causal || rel <= 0);
+              float b;
+              if constexpr (MODE == 0)
+                b = tab[min(max(rel + R, 0), 2 * R)];
+              else
+                b = -alibi * fabsf(static_cast<float>(rel));
+              const float s2 = fmaf(__uint_as_float(sr[cc]), p.scale_log2, b - lse_s[cc]);
+              const float pr = valid ? ex2_approx(s2) : 0.f;
+              const float ds = pr * (__uint_as_float(dr[cc]) - dd_s[cc]);
+              pv[u] = pr;
+              dsv[u] = ds;
+              if constexpr (MODE == 0) {
+                sumL += rel <= -R ? ds : 0.f;
+                sumR += rel >= R ? ds : 0.f;
+                if (valid && rel > -R && rel < R) atomicAdd(&hist[rel + R], ds);
+              } else {
+                dsl = fmaf(ds, fabsf(static_cast<float>(rel)), dsl);
+              }
+            }
+            pp[e / 2] = pack_bf16x2(pv[0], pv[1]);
+            pd[e / 2] = pack_bf16x2(dsv[0], dsv[1]);
+          }
+          emit(gi, pp, pd);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      fence_async_smem();
+      mbar_arrive(bar(kKvBarP + hf));
+    }
+    if (err) {
+      *abort_f = 1;
+      bwd_error(p.status);
+    }
+    // ---- the bias gradient of this CTA
+    named_bar_sync(3, 256);  // every histogram add of both warpgroups is done
+    if constexpr (MODE == 0) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        sumL += __shfl_xor_sync(0xffffffffu, sumL, o);
+        sumR += __shfl_xor_sync(0xffffffffu, sumR, o);
+      }
+      if (lane == 0) {
+        atomicAdd(&red[0], sumL);
+        atomicAdd(&red[1], sumR);
+      }
+      const int ct = tid - 128;  // 0 .. 255
+      for (int xo = ct; xo <= 2 * R; xo += 256)
+        if (hist[xo] != 0.f) atomicAdd(&hist_b[t5_bucket_dev(xo - R, p.t5)], hist[xo]);
+      named_bar_sync(3, 256);
+      if (ct == 0) {
+        atomicAdd(&hist_b[t5_bucket_dev(-R, p.t5)], red[0]);
+        atomicAdd(&hist_b[t5_bucket_dev(R, p.t5)], red[1]);
+      }
+      named_bar_sync(3, 256);
+      if (!*abort_f)
+        for (int xb = ct; xb < p.nb; xb += 256)
+          if (hist_b[xb] != 0.f) atomicAdd(p.dbias + xb * p.H + h, hist_b[xb]);
+    } else {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) dsl += __shfl_xor_sync(0xffffffffu, dsl, o);
+      if (lane == 0) atomicAdd(&red[2], dsl);
+      named_bar_sync(3, 256);
+      if (tid == 128 && !*abort_f && red[2] != 0.f) atomicAdd(p.dslopes + h, -red[2]);
+    }
+    // ---- dV (warpgroup 0) and dK (warpgroup 1)
+    // warp-uniform: the TMEM loads below are warp-collective
+    const bool fin = __all_sync(0xffffffffu, mbar_wait(bar(kKvBarFin), 0) && *abort_f == 0);
     tc_fence_after();
-    if (*abort_f) break;
-    if (tid == 0) {
-      mma_accum(tmem + kColAcc0, tmem + kColP, sb + (4 + st) * kTile, s > 0);   // dV += P^T dO
-      mma_accum(tmem + kColAcc1, tmem + kColDS, sb + (2 + st) * kTile, s > 0);  // dK += dS^T Q
+    __nv_bfloat16* dst = (hf == 0 ? p.dV : p.dK) + (static_cast<size_t>(bh) * p.Lk + key) * kHeadDim;
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+    if (nsub > 0 && fin) {
+      uint32_t a[32], b[32];  // every lane loads (warp-collective); rows past Lk are not stored
+      tmem_ld32(tmem + lane_base + (hf == 0 ? kColDV : kColDK), a);
+      tmem_ld32(tmem + lane_base + (hf == 0 ? kColDV : kColDK) + 32, b);
+      tmem_ld_wait(a);
+      tmem_ld_wait(b);
+      const float mul = hf == 0 ? 1.f : p.scale;
+      if (key_ok) {
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          const uint32_t* r = v < 4 ? &a[v * 8] : &b[(v - 4) * 8];
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            w[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * mul, __uint_as_float(r[2 * e + 1]) * mul);
+          d4[v] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+    } else if (nsub == 0 && key_ok) {  // no query sees this key
+#pragma unroll
+      for (int v = 0; v < 8; ++v) d4[v] = make_uint4(0u, 0u, 0u, 0u);
     }
+    if (!fin && lane == 0) bwd_error(p.status);
+  } else {
+    setmaxnreg_dec<56>();
+    // ---------------------------------------------------------- dQ accumulation
+    // Each dQ_i (fp32, scaled) goes through the tile's dS buffer, which its
+    // dQ product has finished reading, as two 128 x 32 boxes (128-byte
+    // swizzle, conflict-free row writes), and one thread adds them into the
+    // fp32 accumulator with bulk tensor reductions; once those have read the
+    // buffer, it is released to the compute warpgroups (DsFree).
+    const int t = ((warp & 3) << 5) | lane;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    bool pending = false;  // thread 0 of the warpgroup has bulk reductions in flight
+    for (int i = 0; i < ntiles; ++i) {
+      const bool ok = mbar_wait(bar(kKvBarDqFull), i & 1);
+      if (__any_sync(0xffffffffu, !ok || *abort_f != 0)) {  // the whole warp leaves
+        if (!ok) bwd_error(p.status);
+        *abort_f = 1;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t buf = sb + kKvOffDS + (i & 1) * 2 * kTile;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {  // columns 32 half .. 32 half + 31: box `half`
+        uint32_t a[32];
+        tmem_ld32(tmem + lane_base + kColDQ + 32 * half, a);
+        tmem_ld_wait(a);
+        if (half == 1) {
+          tc_fence_before();
+          mbar_arrive(bar(kKvBarDqFree));  // the issuer may write the next dQ tile
+        }
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          const uint32_t off = static_cast<uint32_t>(half) * kTile + static_cast<uint32_t>(t) * 128u +
+                               ((static_cast<uint32_t>(ch) ^ (t & 7u)) << 4);
+          const float sc = p.scale;
+          asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(buf + off),
+                       "f"(__uint_as_float(a[4 * ch]) * sc), "f"(__uint_as_float(a[4 * ch + 1]) * sc),
+                       "f"(__uint_as_float(a[4 * ch + 2]) * sc), "f"(__uint_as_float(a[4 * ch + 3]) * sc)
+                       : "memory");
+        }
+      }
+      fence_async_smem();
+      mbar_arrive(bar(kKvBarDqStage));
+      if (t == 0) {
+        bool staged = mbar_wait(bar(kKvBarDqStage), i & 1);
+        if (staged) {
+          const int q0 = (first + i) * kBT;
+          tma_reduce_add_3d(&tmAcc, buf, 0, q0, bh);
+          tma_reduce_add_3d(&tmAcc, buf + kTile, 32, q0, bh);
+          bulk_commit();
+          pending = true;
+          bulk_wait_read();
+        } else {
+          *abort_f = 1;
+          bwd_error(p.status);
+        }
+        mbar_arrive(bar(kKvBarDsFree + (i & 1)));
+      }
+    }
+    if (t == 0 && pending) bulk_wait_all();  // no bulk operation outlives the CTA
   }
 
-  // ---------------------------------------------------------------- epilogue
-  if (tid == 0) tc_commit(bar(kBarFin));
-  if (!mbar_wait(bar(kBarFin), 0)) *abort_f = 1;
-  tc_fence_after();
-  __nv_bfloat16* dv_row = p.dV + (static_cast<size_t>(bh) * p.Lk + key) * kHeadDim;
-  __nv_bfloat16* dk_row = p.dK + (static_cast<size_t>(bh) * p.Lk + key) * kHeadDim;
-  if (nsteps > 0) {
-    uint32_t a[32], b[32];
-    tmem_ld32(tmem + lane_base + kColAcc0, a);
-    tmem_ld32(tmem + lane_base + kColAcc0 + 32, b);
-    tmem_ld_wait(a);
-    tmem_ld_wait(b);
-    if (key_ok && !*abort_f) store_row_bf16(dv_row, a, b, 1.f);
-    tmem_ld32(tmem + lane_base + kColAcc1, a);
-    tmem_ld32(tmem + lane_base + kColAcc1 + 32, b);
-    tmem_ld_wait(a);
-    tmem_ld_wait(b);
-    if (key_ok && !*abort_f) store_row_bf16(dk_row, a, b, p.scale);
-  } else if (key_ok) {  // no query sees this key
-    uint4* v4 = reinterpret_cast<uint4*>(dv_row);
-    uint4* k4 = reinterpret_cast<uint4*>(dk_row);
-#pragma unroll
-    for (int v = 0; v < 8; ++v) {
-      v4[v] = make_uint4(0, 0, 0, 0);
-      k4[v] = make_uint4(0, 0, 0, 0);
-    }
-  }
-  if (tid == 0 && *abort_f) {
-    drain_copies(sb, init_waited, issued, consumed);
-    bwd_error(p.status);
-  }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc(tmem, 512);
   }
 }
 
-// One CTA per SM: the 512 TMEM columns a CTA allocates are all there are.
-uint32_t bwd_smem_bytes(int R) {
-  const uint32_t tab = (2u * static_cast<uint32_t>(R) + 1u) * 4u;
-  const uint32_t dq_aux = 2u * tab + static_cast<uint32_t>(kMaxT5Buckets) * 4u;
-  const uint32_t dkdv_aux = tab + 4u * kBT * 4u;
-  const uint32_t need = 1024u + kOffAux + (dq_aux > dkdv_aux ? dq_aux : dkdv_aux);
-  constexpr uint32_t kOneCtaPerSm = 120u * 1024u;
-  return need > kOneCtaPerSm ? need : kOneCtaPerSm;
+// ================================================================ dQ to bf16
+__global__ void relpos_bwd_dq_convert_kernel(const float4* __restrict__ acc, uint2* __restrict__ dq, size_t n4) {
+  griddep_wait();
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n4;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const float4 v = acc[i];
+    dq[i] = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+  }
+}
+
+uint32_t stats_smem_bytes(int mode, int R) {
+  const uint32_t tab = mode == 0 ? ((2u * static_cast<uint32_t>(R) + 1u + 3u) & ~3u) * 4u : 0u;
+  return 1024u + kStOffAux + tab + 3u * 128u * 4u;
+}
+
+// bias table and histogram (2R + 1 each; one entry each for ALiBi, R = 0),
+// bucket sums, then 16 floats of side / slope partials
+uint32_t dkdv_smem_bytes(int R) {
+  const uint32_t aux = (2u * (2u * static_cast<uint32_t>(R) + 1u) + kMaxT5Buckets + 16u) * 4u;
+  return 1024u + kKvOffAux + aux;
+}
+
+template <typename K>
+cudaError_t launch_pdl(K kern, dim3 grid, dim3 block, uint32_t smem, cudaStream_t stream, const CUtensorMap& a,
+                       const CUtensorMap& b, const CUtensorMap& c, const CUtensorMap& d, const BwdParams& p) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, a, b, c, d, p);
+}
+
+template <int MODE>
+cudaError_t launch_bwd_mode(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                            const CUtensorMap& tmdO, const CUtensorMap& tmAcc, const BwdParams& p,
+                            cudaStream_t stream) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+  static std::atomic<uint64_t> attr_set{0};
+  const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
+  if (!bit || !(attr_set.load() & bit)) {
+    cudaError_t e = cudaFuncSetAttribute(relpos_bwd_stats_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(stats_smem_bytes(MODE, kMaxR)));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(relpos_bwd_dkdv_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(dkdv_smem_bytes(kMaxR)));
+    if (e != cudaSuccess) return e;
+    attr_set.fetch_or(bit);
+  }
+  const unsigned BH = static_cast<unsigned>(p.B * p.H);
+  cudaError_t e = launch_pdl(relpos_bwd_stats_kernel<MODE>, dim3((p.Lq + kBT - 1) / kBT, BH), dim3(kStThreads),
+                             stats_smem_bytes(MODE, p.R), stream, tmQ, tmK, tmV, tmdO, p);
+  if (e != cudaSuccess) return e;
+  {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((p.Lk + kBT - 1) / kBT, BH);
+    cfg.blockDim = dim3(kKvThreads);
+    cfg.dynamicSmemBytes = dkdv_smem_bytes(p.R);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, relpos_bwd_dkdv_kernel<MODE>, tmQ, tmK, tmV, tmdO, tmAcc, p);
+    if (e != cudaSuccess) return e;
+  }
+  const size_t n4 = static_cast<size_t>(BH) * p.Lq * kHeadDim / 4;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  size_t blocks = (n4 + 255) / 256;
+  if (blocks > 152 * 8) blocks = 152 * 8;
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks > 0 ? blocks : 1));
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, relpos_bwd_dq_convert_kernel, reinterpret_cast<const float4*>(p.dQacc),
+                            reinterpret_cast<uint2*>(p.dQ), n4);
 }
 
 }  // namespace
 
 int bwd_max_R() { return kMaxR; }
 
-cudaError_t launch_bwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                       const CUtensorMap& tmdO, const BwdParams& p, cudaStream_t stream) {
-  if (p.R < 1 || p.R > kMaxR || p.nb > kMaxT5Buckets) return cudaErrorInvalidValue;
-  const uint32_t smem = bwd_smem_bytes(p.R);
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
-  static std::atomic<uint64_t> attr_set{0};
-  const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
-  if (!bit || !(attr_set.load() & bit)) {
-    const int most = static_cast<int>(bwd_smem_bytes(kMaxR));
-    cudaError_t e = cudaFuncSetAttribute(relpos_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(relpos_bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
-    if (e != cudaSuccess) return e;
-    attr_set.fetch_or(bit);
+cudaError_t launch_bwd(int mode, const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                       const CUtensorMap& tmdO, const CUtensorMap& tmAcc, const BwdParams& p,
+                       cudaStream_t stream) {
+  if (mode == 0) {
+    if (p.R < 1 || p.R > kMaxR || p.nb > kMaxT5Buckets) return cudaErrorInvalidValue;
+    return launch_bwd_mode<0>(tmQ, tmK, tmV, tmdO, tmAcc, p, stream);
   }
-  const unsigned BH = static_cast<unsigned>(p.B * p.H);
-  relpos_bwd_dq_kernel<<<dim3((p.Lq + kBT - 1) / kBT, BH), kBwdThreads, smem, stream>>>(tmQ, tmK, tmV, tmdO, p);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  relpos_bwd_dkdv_kernel<<<dim3((p.Lk + kBT - 1) / kBT, BH), kBwdThreads, smem, stream>>>(tmQ, tmK, tmV, tmdO, p);
-  return cudaGetLastError();
+  if (mode == 3) return launch_bwd_mode<3>(tmQ, tmK, tmV, tmdO, tmAcc, p, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace relpos

@@ -127,9 +127,11 @@ struct Item {
 };
 
 // Valid query rows and keys of (batch, head) bh: the batch element's length
-// in a right-padded batch, otherwise no limit.
+// in a right-padded batch (PAD: the launch variant that takes lengths),
+// otherwise no limit.
+template <bool PAD>
 RP_DEVI int seq_len(const FwdParams& p, int bh) {
-  if (!p.lengths) return 0x7fffffff;
+  if constexpr (!PAD) return 0x7fffffff;
   const int n = __ldg(p.lengths + bh / p.H);
   return n < 0 ? 0 : n;
 }
@@ -137,17 +139,19 @@ RP_DEVI int seq_len(const FwdParams& p, int bh) {
 // Key tiles [0, n) one 128-row query tile starting at row r0 visits, for a
 // sequence of nlen valid rows and keys (a padded batch element; rows from
 // nlen on give zero rows).
+template <bool PAD>
 RP_DEVI int tile_keys(const FwdParams& p, int r0, int nlen) {
-  const int lq = min(p.Lq, nlen), lk = min(p.Lk, nlen);
-  if (r0 >= lq || lk <= 0) return 0;
+  const int lq = PAD ? min(p.Lq, nlen) : p.Lq;
+  const int lk = PAD ? min(p.Lk, nlen) : p.Lk;
+  if (r0 >= lq || (PAD && lk <= 0)) return 0;
   int last_key = lk - 1;
   if (p.causal) last_key = min(last_key, min(r0 + kBM - 1, lq - 1) + p.q_offset);
   return last_key / kBN + 1;
 }
 
 // SPLIT: the launch has split items (p.nsplit > 0); without, the split paths
-// compile away.
-template <bool SPLIT>
+// compile away. PAD: a right-padded batch (p.lengths).
+template <bool SPLIT, bool PAD>
 RP_DEVI Item make_item(const FwdParams& p, int w) {
   Item it;
   const int BH = p.B * p.H;
@@ -161,20 +165,20 @@ RP_DEVI Item make_item(const FwdParams& p, int w) {
   it.bh = wp % BH;
   it.h = it.bh % p.H;
   const int i0 = pair * 2 * kBM;
-  const int nlen = seq_len(p, it.bh);
+  const int nlen = seq_len<PAD>(p, it.bh);
   if (xs < 0) {
     it.split = false;
 #pragma unroll
     for (int x = 0; x < 2; ++x) {
       it.row0[x] = i0 + x * kBM;
       it.lo[x] = 0;
-      it.hi[x] = tile_keys(p, it.row0[x], nlen);
+      it.hi[x] = tile_keys<PAD>(p, it.row0[x], nlen);
     }
     it.ns = max(it.hi[0], it.hi[1]);
   } else {
     it.split = true;
     const int r0 = i0 + xs * kBM;
-    const int n = tile_keys(p, r0, nlen);
+    const int n = tile_keys<PAD>(p, r0, nlen);
     const int na = (n + 1) >> 1;
     it.row0[0] = it.row0[1] = r0;
     it.lo[0] = 0;
@@ -211,10 +215,10 @@ RP_DEVI int item_at(int r, bool snake) {
 
 // Head of the first item from pass r on in which query tile x has key tiles,
 // or -1.
-template <bool SPLIT>
+template <bool SPLIT, bool PAD>
 RP_DEVI int next_head(const FwdParams& p, int x, int r, int nitems) {
   for (int w = item_at(r, p.causal); w < nitems; w = item_at(++r, p.causal)) {
-    const Item it = make_item<SPLIT>(p, w);
+    const Item it = make_item<SPLIT, PAD>(p, w);
     if (sel(it.hi, x) > sel(it.lo, x)) return it.h;
   }
   return -1;
@@ -263,7 +267,8 @@ __host__ __device__ inline uint32_t fwd_aux_bytes(int mode, const FwdParams& p) 
 }
 
 // VAR 0: pair items only; 1: with split items (p.nsplit > 0); 2: pair items
-// with the two softmax warpgroups staggered (p.stagger).
+// with the two softmax warpgroups staggered (p.stagger); 3: pair items of a
+// right-padded batch (p.lengths).
 // Loads one query tile (both halves for Transformer-XL) on barrier `bar`.
 template <int MODE, bool ELECT>
 RP_DEVI void load_q_tile(uint32_t dst, const CUtensorMap* tmQ, uint32_t bar, int row0, int bh) {
@@ -296,6 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const FwdParams p) {
   constexpr bool SPLIT = VAR == 1;
   constexpr bool STAG = VAR == 2;
+  constexpr bool PAD = VAR == 3;
   using L = Smem<MODE>;
   constexpr uint32_t kOffQ = L::kOffQ, kOffK = L::kOffK, kOffV = L::kOffV, kOffBar = L::kOffBar,
                      kOffAux = L::kOffAux;
@@ -321,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   griddep_launch_dependents();
   // a padded batch's lengths are read by every role's item walk, the setup's
   // included: wait for the previous kernel before anything else
-  if (p.lengths) griddep_wait();
+  if constexpr (PAD) griddep_wait();
   uint8_t* aux = smem + kOffAux;
   uint8_t* bkt = aux;  // T5: head-independent bucket of each table offset
   const int nrel = 2 * p.kclip + 1;
@@ -360,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   bool two0 = false;
   int nk0 = 0;
   if (first_loads) {
-    it0 = make_item<SPLIT>(p, item_at(0, p.causal));
+    it0 = make_item<SPLIT, PAD>(p, item_at(0, p.causal));
     two0 = !it0.split && it0.hi[1] > 0;
     nk0 = it0.ns < kStages ? it0.ns : kStages;
     tma_prefetch_desc(&tmQ);
@@ -419,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t it_cnt = 0;
       int item_cnt = 0;
       for (int rr = 0, w = item_at(0, p.causal); ok && w < nitems; w = item_at(++rr, p.causal), ++item_cnt) {
-        const Item it = make_item<SPLIT>(p, w);
+        const Item it = make_item<SPLIT, PAD>(p, w);
         // the first item's Q and first ring stages were loaded in the setup
         const int pre = item_cnt == 0 ? min(it.ns, kStages) : 0;
         if (kq && item_cnt > 0) {
@@ -482,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t o_col = tmem + kTmemO + x * kHeadDim;
       const uint32_t p_col = tmem + kTmemP + x * 64;
       for (int rr = 0, w = item_at(0, p.causal); ok && w < nitems; w = item_at(++rr, p.causal), ++item_cnt) {
-        const Item it = make_item<SPLIT>(p, w);
+        const Item it = make_item<SPLIT, PAD>(p, w);
         const int mine = sel(it.hi, x) - sel(it.lo, x);
         const uint64_t dq = dq_a + ((it.split ? 0u : x) * kQStep);
         ok = mbar_wait_warp(bar(kBarQFull), item_cnt & 1);
@@ -663,7 +669,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       return true;
     };
     if constexpr (MODE == 0) {
-      const int h0 = next_head<SPLIT>(p, x, 0, nitems);
+      const int h0 = next_head<SPLIT, PAD>(p, x, 0, nitems);
       griddep_wait();
       if (h0 >= 0) {
         if (t < p.t5_nb) hb_next = __ldg(p.bias + t * p.H + h0);
@@ -686,17 +692,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t stag = 0;
     float2* ml = reinterpret_cast<float2*>(aux + fwd_aux_bytes(MODE, p));
     for (int rr = 0, w = item_at(0, p.causal); !err && w < nitems; w = item_at(++rr, p.causal)) {
-      const Item it = make_item<SPLIT>(p, w);
+      const Item it = make_item<SPLIT, PAD>(p, w);
       const int lo_x = sel(it.lo, x);
       const int n_kv = sel(it.hi, x) - lo_x;
       const uint32_t stag_it = stag;
       const bool a_has = it.hi[0] > it.lo[0];
       if (x == 0 ? n_kv > 0 : a_has) ++stag;
-      const int nlen = seq_len(p, it.bh);  // valid rows and keys (padded batches)
+      const int nlen = seq_len<PAD>(p, it.bh);  // valid rows and keys (padded batches)
       if (n_kv == 0) {
         // a padded batch element's query tile past its length: zero rows
         const int r0 = sel(it.row0, x);
-        if (p.lengths && r0 < p.Lq && (!it.split || x == 0)) {
+        if (PAD && r0 < p.Lq) {
           const int row = r0 + t;
           if (row < p.Lq) {
             const size_t base = (static_cast<size_t>(it.bh) * p.Lq + row) * kHeadDim;
@@ -708,7 +714,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         continue;
       }
       const int i0 = sel(it.row0, x);
-      const int lk_eff = min(p.Lk, nlen);
+      const int lk_eff = PAD ? min(p.Lk, nlen) : p.Lk;
       const int prow = i0 + t + p.q_offset;  // absolute position of this row
       const int p_lo = i0 + p.q_offset;      // of the tile's first row
 
@@ -721,7 +727,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // this item's table was filled at the end of the previous item (or in
         // the prologue); fetch the next item's bias row meanwhile
         buf = ocnt & 1;
-        next_h = next_head<SPLIT>(p, x, rr + 1, nitems);
+        next_h = next_head<SPLIT, PAD>(p, x, rr + 1, nitems);
         if (t < p.t5_nb && next_h >= 0) hb_next = __ldg(p.bias + t * p.H + next_h);
         const bool ok = mbar_wait(bar(kBarTab + x), 1);
         err = __any_sync(0xffffffffu, !ok);
@@ -1188,7 +1194,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int row = i0 + t;
       // rows past a padded element's length are zero rows
-      const float inv_l = (l_row > 0.f && row < nlen) ? 1.f / l_row : 0.f;
+      const float inv_l = (l_row > 0.f && (!PAD || row < nlen)) ? 1.f / l_row : 0.f;
       if (row < p.Lq) {
         const size_t base = (static_cast<size_t>(it.bh) * p.Lq + row) * kHeadDim + c0;
         const int ncol = merge ? 32 : kHeadDim;
@@ -1274,34 +1280,32 @@ cudaError_t launch_fwd(int mode, bool out_f32, const CUtensorMap& tmQ, const CUt
   dim3 block(kThreads);
   void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, const FwdParams) =
       nullptr;
-  const int var = p.nsplit > 0 ? 1 : (p.stagger ? 2 : 0);
+  const int var = p.lengths ? 3 : (p.nsplit > 0 ? 1 : (p.stagger ? 2 : 0));
+  // every mode has variants 0, 1 and 3; T5 also 2
+#define RP_FWD_VARIANTS(M)                                                                         \
+  if (var == 0) kern = out_f32 ? relpos_fwd_kernel<M, true, 0> : relpos_fwd_kernel<M, false, 0>;   \
+  if (var == 1) kern = out_f32 ? relpos_fwd_kernel<M, true, 1> : relpos_fwd_kernel<M, false, 1>;   \
+  if (var == 3) kern = out_f32 ? relpos_fwd_kernel<M, true, 3> : relpos_fwd_kernel<M, false, 3>;
   if (mode == 0) {
-    if (var == 2)
-      kern = out_f32 ? relpos_fwd_kernel<0, true, 2> : relpos_fwd_kernel<0, false, 2>;
-    else
-      kern = out_f32 ? (var ? relpos_fwd_kernel<0, true, 1> : relpos_fwd_kernel<0, true, 0>)
-                     : (var ? relpos_fwd_kernel<0, false, 1> : relpos_fwd_kernel<0, false, 0>);
-  } else if (mode == 1 && var < 2) {
-    kern = out_f32 ? (var ? relpos_fwd_kernel<1, true, 1> : relpos_fwd_kernel<1, true, 0>)
-                   : (var ? relpos_fwd_kernel<1, false, 1> : relpos_fwd_kernel<1, false, 0>);
-  } else if (mode == 2 && var < 2) {
-    kern = out_f32 ? (var ? relpos_fwd_kernel<2, true, 1> : relpos_fwd_kernel<2, true, 0>)
-                   : (var ? relpos_fwd_kernel<2, false, 1> : relpos_fwd_kernel<2, false, 0>);
-  } else if (mode == 3 && var < 2) {
-    kern = out_f32 ? (var ? relpos_fwd_kernel<3, true, 1> : relpos_fwd_kernel<3, true, 0>)
-                   : (var ? relpos_fwd_kernel<3, false, 1> : relpos_fwd_kernel<3, false, 0>);
-  } else if (mode == 4 && var < 2) {
-    kern = out_f32 ? (var ? relpos_fwd_kernel<4, true, 1> : relpos_fwd_kernel<4, true, 0>)
-                   : (var ? relpos_fwd_kernel<4, false, 1> : relpos_fwd_kernel<4, false, 0>);
-  } else {
-    return cudaErrorNotSupported;
+    RP_FWD_VARIANTS(0)
+    if (var == 2) kern = out_f32 ? relpos_fwd_kernel<0, true, 2> : relpos_fwd_kernel<0, false, 2>;
+  } else if (mode == 1) {
+    RP_FWD_VARIANTS(1)
+  } else if (mode == 2) {
+    RP_FWD_VARIANTS(2)
+  } else if (mode == 3) {
+    RP_FWD_VARIANTS(3)
+  } else if (mode == 4) {
+    RP_FWD_VARIANTS(4)
   }
+#undef RP_FWD_VARIANTS
+  if (!kern) return cudaErrorNotSupported;
   // raise the kernel's shared-memory limit once per device (the maximum, so
   // that every later launch fits)
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
-  const int slot = mode * 6 + (out_f32 ? 3 : 0) + var;
-  static std::atomic<uint64_t> attr_set[30];
+  const int slot = mode * 8 + (out_f32 ? 4 : 0) + var;
+  static std::atomic<uint64_t> attr_set[40];
   const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
   if (!bit || !(attr_set[slot].load() & bit)) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,

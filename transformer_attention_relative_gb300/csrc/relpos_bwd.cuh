@@ -15,30 +15,40 @@ namespace relpos {
 
 constexpr int kMaxT5Buckets = 128;
 
-// Backward of the T5-bias attention (attn_bwd.cu)
+// Backward of the T5-bias and the ALiBi attention (attn_bwd.cu)
 struct BwdParams {
   int B, H, Lq, Lk;
   int causal, q_offset;
   float scale;       // 1 / sqrt(d)
   float scale_log2;  // scale times log2(e)
+  // T5
   const float* bias;  // [nb, H]
   int nb;
-  int R;  // |offset| >= R: the side's last bucket; offsets in (-R, R) get a table entry each
+  int R;  // |offset| >= R: the side's last bucket; offsets in (-R, R) get a table entry each (ALiBi: 0)
   T5Index t5;
-  float* lse;  // [B*H, Lq] row log-sum-exp of the log2-scaled logits (written by the dQ kernel)
-  float* Dr;   // [B*H, Lq] D_i = sum_j P_ij dP_ij
+  float* dbias;  // [nb, H], zeroed before the kernels, accumulated by the dK / dV kernel
+  // ALiBi
+  const float* slopes;  // [H]
+  float* dslopes;       // [H], zeroed before the kernels
+  float* lse;    // [B*H, lq_pad] row log-sum-exp of the log2-scaled logits (stats kernel)
+  float* Dr;     // [B*H, lq_pad] D_i = sum_j P_ij dP_ij (stats kernel)
+  int lq_pad;    // Lq rounded up to a multiple of 128 (whole query tiles)
+  float* dQacc;  // [B*H, Lq, 64] fp32, zeroed before the kernels: dQ summed over key tiles
   __nv_bfloat16* dQ;  // [B*H, Lq, 64]
   __nv_bfloat16* dK;  // [B*H, Lk, 64]
   __nv_bfloat16* dV;  // [B*H, Lk, 64]
-  float* dbias;       // [nb, H], zeroed before the dQ kernel, accumulated by it
   int* status;
 };
 
-// T5 backward: the dQ kernel (row statistics, dQ, dbias), then the dK / dV
-// kernel; bwd_max_R is the largest saturation distance R they support
+// mode 0 (T5) or 3 (ALiBi): the row-statistics kernel, the dK / dV kernel
+// (which also accumulates dQ and the bias gradient) and the dQ conversion;
+// bwd_max_R is the largest T5 saturation distance R they support
 int bwd_max_R();
-cudaError_t launch_bwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                       const CUtensorMap& tmdO, const BwdParams& p, cudaStream_t stream);
+// tmAcc: the fp32 dQ accumulator [B*H, Lq, 64] as 128-row x 32-column boxes
+// (128-byte swizzle), the target of the dQ tiles' bulk reductions
+cudaError_t launch_bwd(int mode, const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                       const CUtensorMap& tmdO, const CUtensorMap& tmAcc, const BwdParams& p,
+                       cudaStream_t stream);
 
 // 16 consecutive 32-bit TMEM columns of this thread's lane.
 RP_DEVI void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
