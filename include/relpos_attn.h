@@ -275,7 +275,7 @@ int relpos_t5_decode_positions(const void* Q, const void* K, const void* V, cons
  *               the whole batch (the table is shared by it).
  * All pointers 16-byte aligned and caller-owned; the outputs must not overlap
  * the inputs. Limits: the distance R at which the last bucket starts (or the
- * largest offset present, if smaller) must be <= 2048
+ * largest offset present, if smaller) must be <= 1024
  * (RELPOS_ERR_UNSUPPORTED otherwise; max_distance 128 gives R = 91
  * bidirectional, 113 causal). Scratch: about 264 * B * H * Lq bytes (an
  * fp32 dQ accumulator and the row statistics, padded to 128-row tiles) from cudaMallocAsync on `stream`,

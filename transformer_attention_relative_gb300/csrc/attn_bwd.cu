@@ -51,7 +51,7 @@ namespace relpos {
 namespace {
 
 constexpr int kBT = 128;  // rows per tile, queries or keys
-constexpr int kMaxR = 2048;
+constexpr int kMaxR = 1024;
 constexpr uint32_t kTile = kBT * kHeadDim * 2;  // 16 KB
 constexpr uint32_t kHalfTile = kTile / 2;       // 64 rows
 
@@ -63,11 +63,41 @@ RP_DEVI void bwd_error(int* status) {
   if (status) atomicCAS(status, 0, -4);
 }
 
-// The head's log2-scaled bias of every offset in [-R, R] (T5); entries 0 and
-// 2R serve every offset beyond on their side.
-RP_DEVI void build_bias_table(float* tab, const BwdParams& p, int h, int tid, int nthreads) {
-  for (int x = tid; x <= 2 * p.R; x += nthreads)
-    tab[x] = __ldg(p.bias + t5_bucket_dev(x - p.R, p.t5) * p.H + h) * kLog2e;
+// T5 bias tables. A near tile's offsets reach at most 254 beyond the
+// saturation distance R on either side (a 128 x 128 tile spans 255 offsets),
+// so the extended table E covers offsets -R - kTabPad ... R + kTabPad, entry
+// x holding the log2-scaled bias of offset x - R - kTabPad. It is kept as four
+// copies shifted by one entry each, so that any run of 64 consecutive
+// entries starts 16-byte aligned in one of them and is read with 16-byte
+// loads; the copies sit 32 bytes apart modulo 128 (fewer bank conflicts
+// between lanes reading different copies). The query-major statistics
+// kernel reads E by increasing offset; the key-major dK / dV kernel reads
+// it reversed (F[y] = E[n - 1 - y]), so that its offsets also increase with
+// the column.
+constexpr int kTabPad = 256;
+__host__ __device__ inline int tab_len(int R) { return 2 * R + 2 * kTabPad + 1; }
+// floats per copy: room for a 64-entry window at the end, and 8 floats
+// beyond a multiple of 32 (the 32-byte placement above)
+__host__ __device__ inline int tab_stride(int R) { return ((tab_len(R) + 64 + 31) & ~31) + 8; }
+// The head's biases per bucket (log2-scaled) into bsm[nb]; the caller
+// synchronizes before build_bias_copies reads them.
+RP_DEVI void load_bucket_bias(float* bsm, const BwdParams& p, int h, int tid) {
+  if (tid < p.nb) bsm[tid] = __ldg(p.bias + tid * p.H + h) * kLog2e;
+}
+RP_DEVI void build_bias_copies(float* base, const float* bsm, const BwdParams& p, bool reversed, int tid,
+                               int nthreads) {
+  const int n = tab_len(p.R), st = tab_stride(p.R);
+  for (int x = tid; x < 4 * st; x += nthreads) {
+    const int k = x / st, e = x - k * st;
+    int y = min(e + k, n - 1);         // entry of F (reversed) or E
+    if (reversed) y = n - 1 - y;       // F[y] = E[n - 1 - y]
+    base[x] = bsm[t5_bucket_dev(y - p.R - kTabPad, p.t5)];
+  }
+}
+// the 64 entries from index w of a table kept as four shifted copies
+RP_DEVI const float4* tab_window(const float* base, int R, int w) {
+  const int k = w & 3;
+  return reinterpret_cast<const float4*>(base + k * tab_stride(R) + (w - k));
 }
 
 // Tiled bulk reduction shared -> global: element-wise fp32 add of a staged
@@ -134,8 +164,9 @@ __global__ void __launch_bounds__(kStThreads, 1)
   const int i0 = blockIdx.x * kBT;
   auto bar = [&](uint32_t i) { return sb + kStOffBar + 8u * i; };
   volatile int* abort_f = reinterpret_cast<volatile int*>(smem + kStOffBar + kStAbort);
-  float* tab = reinterpret_cast<float*>(smem + kStOffAux);                 // T5 bias by offset
-  float* mrg = tab + (MODE == 0 ? ((2 * p.R + 1 + 3) & ~3) : 0);           // [3][128] merge
+  float* tab = reinterpret_cast<float*>(smem + kStOffAux);                 // T5: 4 copies of E
+  float* mrg = tab + (MODE == 0 ? 4 * tab_stride(p.R) : 0);                // [3][128] merge
+  float* bsm = mrg + 3 * 128;                                               // T5 bias per bucket
 
   const int last_row = min(i0 + kBT, p.Lq) - 1;
   int n_kv = (p.Lk + kBT - 1) / kBT;
@@ -152,7 +183,11 @@ __global__ void __launch_bounds__(kStThreads, 1)
     tmem_relinquish();
   }
   griddep_wait();
-  if constexpr (MODE == 0) build_bias_table(tab, p, h, tid, kStThreads);
+  if constexpr (MODE == 0) {
+    load_bucket_bias(bsm, p, h, tid);
+    __syncthreads();
+    build_bias_copies(tab, bsm, p, false, tid, kStThreads);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -252,8 +287,10 @@ __global__ void __launch_bounds__(kStThreads, 1)
       const bool far_l = MODE == 0 && rel_hi <= -R;
       const bool far_r = MODE == 0 && p.t5.bidir && rel_lo >= R;
       // one row constant: T5 beyond the saturation distance; ALiBi with
-      // every key on one side (the rest is linear in the column)
+      // every key on one side (the rest is linear in the column). T5 near
+      // tiles without masking read their biases 4 at a time.
       const bool fast = nomask && (MODE == 0 ? (far_l || far_r) : (rel_hi <= 0 || rel_lo >= 0));
+      const bool near_t5 = MODE == 0 && nomask && !fast;
 #pragma unroll 1
       for (int c0 = 0; c0 < kBT; c0 += 64) {
         uint32_t sr[64], dr[64];
@@ -272,9 +309,26 @@ __global__ void __launch_bounds__(kStThreads, 1)
         float* xv = reinterpret_cast<float*>(sr);
         float bc = 0.f;  // the row constant of a fast tile (log2 units)
         float mx;
-        if (fast) {
+        if (near_t5) {
+          // E index of column c: j0 + c0 + c - prow + R + kTabPad
+          const float4* bw = tab_window(tab, R, j0 + c0 - prow + R + kTabPad);
+          float m0 = -INFINITY, m1 = -INFINITY;
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            const float4 b4 = bw[q];
+            const float2 a = __ffma2_rn(make_float2(xv[4 * q], xv[4 * q + 1]), sc2, make_float2(b4.x, b4.y));
+            const float2 c = __ffma2_rn(make_float2(xv[4 * q + 2], xv[4 * q + 3]), sc2, make_float2(b4.z, b4.w));
+            xv[4 * q] = a.x;
+            xv[4 * q + 1] = a.y;
+            xv[4 * q + 2] = c.x;
+            xv[4 * q + 3] = c.y;
+            m0 = max3f(m0, a.x, a.y);
+            m1 = max3f(m1, c.x, c.y);
+          }
+          mx = fmaxf(m0, m1);
+        } else if (fast) {
           if constexpr (MODE == 0) {
-            bc = far_l ? tab[0] : tab[2 * R];
+            bc = far_l ? tab[R + kTabPad - R] : tab[R + kTabPad + R];  // biases of offsets -R, R
           } else {
             // -slope |j - p| = g (j - p) with g = slope (keys behind) or -slope (ahead):
             // scaled scores plus g c, then the row constant g (j0 + c0 - p)
@@ -304,7 +358,7 @@ __global__ void __launch_bounds__(kStThreads, 1)
             const bool valid = j0 + c0 + c < p.Lk && (!p.causal || rel <= 0);
             float b;
             if constexpr (MODE == 0)
-              b = tab[min(max(rel + R, 0), 2 * R)];
+              b = tab[min(max(rel + R + kTabPad, 0), tab_len(R) - 1)];
             else
               b = -alibi * fabsf(static_cast<float>(rel));
             xv[c] = valid ? fmaf(xv[c], p.scale_log2, b) : -INFINITY;
@@ -421,10 +475,13 @@ __global__ void __launch_bounds__(kKvThreads, 1)
   const int R = p.R;
   auto bar = [&](uint32_t i) { return sb + kKvOffBar + 8u * i; };
   volatile int* abort_f = reinterpret_cast<volatile int*>(smem + kKvOffBar + kKvAbort);
-  float* tab = reinterpret_cast<float*>(smem + kKvOffAux);   // T5 bias by offset (log2 units)
-  float* hist = tab + (2 * R + 1);                           // T5: dS per offset in (-R, R)
-  float* hist_b = hist + (2 * R + 1);                        // T5: per bucket
-  float* red = hist_b + kMaxT5Buckets;                       // side sums / ALiBi slope partials
+  // T5: 4 copies of F (the reversed extended bias table); dS summed per
+  // offset over the near tiles (entry = E index of the offset); per bucket
+  float* tab = reinterpret_cast<float*>(smem + kKvOffAux);
+  float* hist = tab + (MODE == 0 ? 4 * tab_stride(R) : 0);
+  float* hist_b = hist + (MODE == 0 ? tab_len(R) : 0);
+  float* red = hist_b + kMaxT5Buckets;  // side sums / ALiBi slope partials
+  float* bsm = red + 16;                // T5 bias per bucket
 
   // query tiles that see a key of this tile: rows i with i + q_offset >= j0
   const int nqt = (p.Lq + kBT - 1) / kBT;
@@ -448,8 +505,10 @@ __global__ void __launch_bounds__(kKvThreads, 1)
   }
   griddep_wait();
   if constexpr (MODE == 0) {
-    build_bias_table(tab, p, h, tid, kKvThreads);
-    for (int x = tid; x <= 2 * R; x += kKvThreads) hist[x] = 0.f;
+    load_bucket_bias(bsm, p, h, tid);
+    __syncthreads();
+    build_bias_copies(tab, bsm, p, true, tid, kKvThreads);
+    for (int x = tid; x < tab_len(R); x += kKvThreads) hist[x] = 0.f;
     for (int x = tid; x < kMaxT5Buckets; x += kKvThreads) hist_b[x] = 0.f;
   }
   if (tid < 16) red[tid] = 0.f;
@@ -634,7 +693,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         // one bias per row (T5 beyond the saturation distance), or ALiBi with
         // every key on one side: the logit is s * scale + g (c - rb) with
         // g = -slope (keys behind: |rel| = c - rb) or +slope (ahead: rb - c)
-        const float bc = MODE == 0 ? (far_l ? tab[0] : tab[2 * R]) : 0.f;
+        // F index of offset o: R + kTabPad - o
+        const float bc = MODE == 0 ? (far_l ? tab[2 * R + kTabPad] : tab[kTabPad]) : 0.f;
         const float g = MODE == 0 ? 0.f : (rel_hi <= 0 ? -alibi : alibi);
         const float2 g2 = make_float2(g, g);
         const float nrb = -static_cast<float>(rb);
@@ -691,6 +751,46 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         } else {
           dsl += rel_hi <= 0 ? a : -a;  // |rel| = c - rb behind, rb - c ahead
         }
+      } else if (MODE == 0 && nomask) {
+        // T5 inside the saturation distance, no mask: the biases of the
+        // columns' offsets rb - c read 4 at a time from F (index R + kTabPad
+        // - rb + c), every dS added to its offset's sum (consecutive keys:
+        // consecutive entries, no two lanes on one)
+        const float4* bw = tab_window(tab, R, R + kTabPad - rb);
+        float* hrow = hist + (rb + R + kTabPad);  // entry of column c: hrow - c
+#pragma unroll
+        for (int gi = 0; gi < 4; ++gi) {
+          uint32_t pp[8], pd[8];
+#pragma unroll
+          for (int qq = 0; qq < 4; ++qq) {
+            const int q = 4 * gi + qq;
+            const float4 L = *reinterpret_cast<const float4*>(lse_s + 4 * q);
+            const float4 D = *reinterpret_cast<const float4*>(dd_s + 4 * q);
+            const float4 b4 = bw[q];
+            float2 e0 = __ffma2_rn(make_float2(__uint_as_float(sr[4 * q]), __uint_as_float(sr[4 * q + 1])), sc2,
+                                   make_float2(b4.x - L.x, b4.y - L.y));
+            float2 e1 = __ffma2_rn(make_float2(__uint_as_float(sr[4 * q + 2]), __uint_as_float(sr[4 * q + 3])), sc2,
+                                   make_float2(b4.z - L.z, b4.w - L.w));
+            e0.x = ex2_approx(e0.x);
+            e0.y = ex2_approx(e0.y);
+            e1.x = ex2_approx(e1.x);
+            e1.y = ex2_approx(e1.y);
+            const float2 t0 = __fadd2_rn(make_float2(__uint_as_float(dr[4 * q]), __uint_as_float(dr[4 * q + 1])),
+                                         make_float2(-D.x, -D.y));
+            const float2 t1 = __fadd2_rn(
+                make_float2(__uint_as_float(dr[4 * q + 2]), __uint_as_float(dr[4 * q + 3])), make_float2(-D.z, -D.w));
+            const float2 d0 = __fmul2_rn(e0, t0), d1 = __fmul2_rn(e1, t1);
+            atomicAdd(hrow - 4 * q, d0.x);
+            atomicAdd(hrow - 4 * q - 1, d0.y);
+            atomicAdd(hrow - 4 * q - 2, d1.x);
+            atomicAdd(hrow - 4 * q - 3, d1.y);
+            pp[2 * qq] = pack_bf16x2(e0.x, e0.y);
+            pp[2 * qq + 1] = pack_bf16x2(e1.x, e1.y);
+            pd[2 * qq] = pack_bf16x2(d0.x, d0.y);
+            pd[2 * qq + 1] = pack_bf16x2(d1.x, d1.y);
+          }
+          emit(gi, pp, pd);
+        }
       } else {
         // per element: masks, the bias of each offset, T5 offsets inside the
         // saturation distance summed per offset in shared memory
@@ -707,7 +807,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
               const bool valid = key_ok && q0 + cc < p.Lq && (!p.causal || rel <= 0);
               float b;
               if constexpr (MODE == 0)
-                b = tab[min(max(rel + R, 0), 2 * R)];
+                b = tab[min(max(R + kTabPad - rel, 0), tab_len(R) - 1)];
               else
                 b = -alibi * fabsf(static_cast<float>(rel));
               const float s2 = fmaf(__uint_as_float(sr[cc]), p.scale_log2, b - lse_s[cc]);
@@ -718,7 +818,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
               if constexpr (MODE == 0) {
                 sumL += rel <= -R ? ds : 0.f;
                 sumR += rel >= R ? ds : 0.f;
-                if (valid && rel > -R && rel < R) atomicAdd(&hist[rel + R], ds);
+                if (valid && rel > -R && rel < R) atomicAdd(&hist[rel + R + kTabPad], ds);
               } else {
                 dsl = fmaf(ds, fabsf(static_cast<float>(rel)), dsl);
               }
@@ -751,8 +851,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         atomicAdd(&red[1], sumR);
       }
       const int ct = tid - 128;  // 0 .. 255
-      for (int xo = ct; xo <= 2 * R; xo += 256)
-        if (hist[xo] != 0.f) atomicAdd(&hist_b[t5_bucket_dev(xo - R, p.t5)], hist[xo]);
+      for (int xo = ct; xo < tab_len(R); xo += 256)
+        if (hist[xo] != 0.f) atomicAdd(&hist_b[t5_bucket_dev(xo - R - kTabPad, p.t5)], hist[xo]);
       named_bar_sync(3, 256);
       if (ct == 0) {
         atomicAdd(&hist_b[t5_bucket_dev(-R, p.t5)], red[0]);
@@ -878,15 +978,15 @@ __global__ void relpos_bwd_dq_convert_kernel(const float4* __restrict__ acc, uin
 }
 
 uint32_t stats_smem_bytes(int mode, int R) {
-  const uint32_t tab = mode == 0 ? ((2u * static_cast<uint32_t>(R) + 1u + 3u) & ~3u) * 4u : 0u;
-  return 1024u + kStOffAux + tab + 3u * 128u * 4u;
+  const uint32_t tab = mode == 0 ? 4u * static_cast<uint32_t>(tab_stride(R)) * 4u : 0u;
+  return 1024u + kStOffAux + tab + (3u * 128u + kMaxT5Buckets) * 4u;
 }
 
-// bias table and histogram (2R + 1 each; one entry each for ALiBi, R = 0),
-// bucket sums, then 16 floats of side / slope partials
-uint32_t dkdv_smem_bytes(int R) {
-  const uint32_t aux = (2u * (2u * static_cast<uint32_t>(R) + 1u) + kMaxT5Buckets + 16u) * 4u;
-  return 1024u + kKvOffAux + aux;
+// T5: four bias-table copies and the per-offset sums (ALiBi: none); bucket
+// sums, then 16 floats of side / slope partials
+uint32_t dkdv_smem_bytes(int mode, int R) {
+  const uint32_t t5 = mode == 0 ? (4u * static_cast<uint32_t>(tab_stride(R)) + static_cast<uint32_t>(tab_len(R))) * 4u : 0u;
+  return 1024u + kKvOffAux + t5 + (2u * kMaxT5Buckets + 16u) * 4u;
 }
 
 template <typename K>
@@ -918,7 +1018,7 @@ cudaError_t launch_bwd_mode(const CUtensorMap& tmQ, const CUtensorMap& tmK, cons
                                          static_cast<int>(stats_smem_bytes(MODE, kMaxR)));
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(relpos_bwd_dkdv_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(dkdv_smem_bytes(kMaxR)));
+                               static_cast<int>(dkdv_smem_bytes(MODE, kMaxR)));
     if (e != cudaSuccess) return e;
     attr_set.fetch_or(bit);
   }
@@ -933,7 +1033,7 @@ cudaError_t launch_bwd_mode(const CUtensorMap& tmQ, const CUtensorMap& tmK, cons
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((p.Lk + kBT - 1) / kBT, BH);
     cfg.blockDim = dim3(kKvThreads);
-    cfg.dynamicSmemBytes = dkdv_smem_bytes(p.R);
+    cfg.dynamicSmemBytes = dkdv_smem_bytes(MODE, p.R);
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
