@@ -47,9 +47,10 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from transformer_attention_relative_gb300.workloads import (MODE_DEBERTA, MODE_NAMES,  # noqa: E402
-                                                            MODE_T5, MODE_TXL, WORKLOADS,
-                                                            make_grad_output, make_inputs)
+from transformer_attention_relative_gb300.workloads import (MODE_ALIBI, MODE_DEBERTA,  # noqa: E402
+                                                            MODE_NAMES, MODE_T5, MODE_TXL,
+                                                            WORKLOADS, make_grad_output,
+                                                            make_inputs)
 
 L2_BYTES = 129 * 1024 * 1024
 METRIC = "rel-pos attention fwd TFLOP/s (bf16) and % of GB300 dense BF16 peak"
@@ -83,8 +84,9 @@ KERNEL_SOURCES = {
     "relpos_fwd_kernel": ("attn_fwd.cu",),
     "deberta_band_kernel": ("deberta_band.cu",),
     "relpos_decode_partial_kernel": ("decode.cu",),
-    "relpos_bwd_dq_kernel": ("attn_bwd.cu", "relpos_bwd.cuh"),
+    "relpos_bwd_stats_kernel": ("attn_bwd.cu", "relpos_bwd.cuh"),
     "relpos_bwd_dkdv_kernel": ("attn_bwd.cu", "relpos_bwd.cuh"),
+    "txl_prep_kernel": ("txl_prep.cu",),
 }
 
 
@@ -194,7 +196,7 @@ class ClockSampler:
 def kernels_per_step(w, backward=False):
     """This library's kernels launched by one call (memsets not counted)."""
     if backward:
-        return 2
+        return 3  # row statistics, dK / dV (with dQ and the table gradient), dQ conversion
     decode = w.mode == MODE_T5 and w.Lq <= 8
     n = 2 if decode else 1
     if w.mode in (MODE_DEBERTA, MODE_TXL):
@@ -378,8 +380,9 @@ class GpuRun:
 
 
 class BwdRun(GpuRun):
-    """The T5 backward on the same inputs plus a drawn output gradient dO:
-    one step is one relpos_t5_attn_bwd call (dQ, dK, dV, dbias)."""
+    """The T5 (or ALiBi) backward on the same inputs plus a drawn output
+    gradient dO: one step is one relpos_t5_attn_bwd (relpos_alibi_attn_bwd)
+    call: dQ, dK, dV and the table (slope) gradient."""
 
     def __init__(self, w, device, stream):
         import torch
@@ -399,16 +402,23 @@ class BwdRun(GpuRun):
     def _call(self, d, out=None):
         w = self.w
         p = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
-        rc = self.rp.relpos_t5_attn_bwd(p(d["Q"]), p(d["K"]), p(d["V"]), p(d["dO"]), p(d["table0"]),
-                                        w.B, w.H, w.Lq, w.Lk, w.d, w.num_buckets, w.rel_param,
-                                        int(w.causal), w.q_offset, p(d["dQ"]), p(d["dK"]),
-                                        p(d["dV"]), p(d["dbias"]), self.sptr)
+        if w.mode == MODE_ALIBI:
+            rc = self.rp.relpos_alibi_attn_bwd(p(d["Q"]), p(d["K"]), p(d["V"]), p(d["dO"]),
+                                               p(d["table0"]), w.B, w.H, w.Lq, w.Lk, w.d,
+                                               int(w.causal), w.q_offset, p(d["dQ"]), p(d["dK"]),
+                                               p(d["dV"]), p(d["dbias"]), self.sptr)
+        else:
+            rc = self.rp.relpos_t5_attn_bwd(p(d["Q"]), p(d["K"]), p(d["V"]), p(d["dO"]),
+                                            p(d["table0"]), w.B, w.H, w.Lq, w.Lk, w.d,
+                                            w.num_buckets, w.rel_param, int(w.causal), w.q_offset,
+                                            p(d["dQ"]), p(d["dK"]), p(d["dV"]), p(d["dbias"]),
+                                            self.sptr)
         if rc != 0:
-            raise RuntimeError(f"relpos_t5_attn_bwd failed: {rc}")
+            raise RuntimeError(f"attention backward failed: {rc}")
 
 
 def bwd_flops(w):
-    """Algorithmic flops of the T5 backward: the four gradient products
+    """Algorithmic flops of the T5 / ALiBi backward: the four gradient products
     (dV = P^T dO, dP = dO V^T, dQ = dS K, dK = dS^T Q) over the visible
     (query, key) pairs, twice the forward's two products; the kernels'
     extra recomputations of S and dP are not counted."""
@@ -565,7 +575,7 @@ def config_of(w, world, g, backward=False):
 # every configuration gets a block of its own in the bench line
 BLOCK_WORKLOADS = ("t5_base_bidir", "t5_causal", "shaw", "deberta", "txl_mem", "t5_decode",
                    "t5_decode_evicted", "alibi_bidir", "alibi_causal", "t5_tiny_fp32")
-BACKWARD_WORKLOADS = ("t5_base_bidir", "t5_causal")
+BACKWARD_WORKLOADS = ("t5_base_bidir", "t5_causal", "alibi_causal")
 
 
 def main():
@@ -581,6 +591,8 @@ def main():
                     help="timed region per workload when --steps is not given")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    ap.add_argument("--backward", action="store_true",
+                    help="time the backward of the workload (T5 or ALiBi) as the headline")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", "0"))
@@ -639,7 +651,8 @@ def main():
     cpu_on = rank == 0 and world == 1 and not args.no_cpu
     head = measure_block(w, device, stream, peaks, peak_src, sampler, barrier, world,
                          steps=args.steps, warmup=args.warmup, seconds=args.seconds,
-                         cpu_budget=args.cpu_budget if cpu_on else 0.0)
+                         cpu_budget=args.cpu_budget if cpu_on and not args.backward else 0.0,
+                         backward=args.backward)
     blocks = {}
     if not args.no_others and rank == 0:
         for name in BLOCK_WORKLOADS:

@@ -502,6 +502,7 @@ int attn_fwd_impl(int mode, int dtype, const void* Q, const void* K, const void*
       tp.uv = static_cast<const float*>(table1);
       tp.Q2 = reinterpret_cast<__nv_bfloat16*>(sc + off_q2);
       tp.Ksin = reinterpret_cast<__nv_bfloat16*>(sc + off_sin);
+      tp.status = status;
       for (int m = 0; m < kHeadDim / 2; ++m)
         tp.omega[m] = static_cast<float>(std::pow(10000.0, -2.0 * m / kHeadDim));
       if (launch_txl_prep(tp, s) != cudaSuccess) return fail(RELPOS_ERR_CUDA);

@@ -1010,7 +1010,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const float m_use = (m_run == kNegInf) ? 0.f : m_run;
 
-        // ---- probabilities (in place for Shaw), row sum, bf16 pack; x * 1 + c
+        // ---- probabilities, row sum, bf16 pack; x * 1 + c
         // is exact, so near tiles round exactly as a plain subtraction would
         uint32_t pk[64];
         float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
@@ -1030,41 +1030,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             acc1 = __fadd2_rn(acc1, b);
             pk[c / 2] = pack_bf16x2(a.x, a.y);
             pk[c / 2 + 1] = pack_bf16x2(b.x, b.y);
-            if constexpr (MODE == 1) {
-              xs[c] = a.x;
-              xs[c + 1] = a.y;
-              xs[c + 2] = b.x;
-              xs[c + 3] = b.y;
-            }
           }
         }
         const float tile_sum = (acc0.x + acc0.y) + (acc1.x + acc1.y);
         l_run = l_run * alpha + tile_sum;
-
-        if constexpr (MODE == 1) {
-          if (resc && j > 0) {
-            for (int r = 0; r < nrel; ++r) wbin[r] *= alpha;
-            mass_l *= alpha;
-            mass_r *= alpha;
-          }
-          if (far_l) {
-            mass_l += tile_sum;
-          } else if (far_r) {
-            mass_r += tile_sum;
-          } else {
-            const int r0 = j0 - prow;
-#pragma unroll
-            for (int c = 0; c < 128; ++c) {
-              const int rel = r0 + c;
-              // branch-free: masses beyond the clip in registers, in-band
-              // offsets (-k < rel < k) into their bins
-              const float v = xs[c];
-              mass_l += rel <= -kc ? v : 0.f;
-              mass_r += rel >= kc ? v : 0.f;
-              if (static_cast<unsigned>(rel + kc - 1) < static_cast<unsigned>(2 * kc - 1)) wbin[rel + kc] += v;
-            }
-          }
-        }
 
         // ---- the previous P.V of this tile must be done before P / O change
         if (cnt > 0) {
@@ -1092,6 +1061,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(bar(kBarPFull + x));
+        // Shaw: the value-side mass per clipped offset, after P is handed to
+        // the tensor core (its P.V runs meanwhile)
+        if constexpr (MODE == 1) {
+          if (resc && j > 0) {
+            for (int r = 0; r < nrel; ++r) wbin[r] *= alpha;
+            mass_l *= alpha;
+            mass_r *= alpha;
+          }
+          if (far_l) {
+            mass_l += tile_sum;
+          } else if (far_r) {
+            mass_r += tile_sum;
+          } else {
+            const int r0 = j0 - prow;
+#pragma unroll
+            for (int c = 0; c < 128; ++c) {
+              const int rel = r0 + c;
+              // branch-free: masses beyond the clip in registers, in-band
+              // offsets (-k < rel < k) into their bins; the probabilities
+              // as the P.V product takes them (bf16)
+              const float v = __uint_as_float((c & 1) ? (pk[c >> 1] & 0xffff0000u) : (pk[c >> 1] << 16));
+              mass_l += rel <= -kc ? v : 0.f;
+              mass_r += rel >= kc ? v : 0.f;
+              if (static_cast<unsigned>(rel + kc - 1) < static_cast<unsigned>(2 * kc - 1)) wbin[rel + kc] += v;
+            }
+          }
+        }
+
       }
       if (err) break;
       if constexpr (MODE == 0) {

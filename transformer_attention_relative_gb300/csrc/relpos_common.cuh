@@ -121,6 +121,7 @@ struct TxlParams {
   __nv_bfloat16* Q2;       // [BH, Lq, 128]: q + u, then a = W^T (q + v) rotated by w p
   __nv_bfloat16* Ksin;     // [Lk, 64]: (cos w_m j, sin w_m j)
   float omega[kHeadDim / 2];  // w_m = 10000^(-2m/64)
+  int* status;               // device status word (bounded-wait failures)
 };
 
 struct DecodeParams {

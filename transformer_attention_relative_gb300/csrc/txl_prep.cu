@@ -18,9 +18,11 @@
 //
 // This kernel writes the query side Q2 [BH, Lq, 128] (bf16) and the key
 // sinusoid table S [Lk, 64] (bf16, the same for every head). Query blocks:
-// 128 threads, 32 rows, four threads per row, each forming 16 of the 64
-// components of a (the head's W staged in shared memory). Key blocks
-// (blockIdx.y == BH): one thread per key.
+// 128 rows of one head per CTA; each thread stages its row of q + v (bf16)
+// as the A operand of one tcgen05 product a = (Q + v) W (M128 N64 K64, W as
+// an MN-major bf16 operand in shared memory, fp32 accumulator in TMEM),
+// then takes its row of a out of TMEM, rotates it by its angles and stores
+// both halves. Key blocks (blockIdx.y == BH): one thread per key.
 
 #include <cuda_bf16.h>
 
@@ -34,14 +36,19 @@ namespace relpos {
 namespace {
 
 constexpr int kPrepThreads = 128;
-constexpr int kRowsPerBlock = kPrepThreads / 4;
+constexpr int kRowsPerBlock = kPrepThreads;
+constexpr uint32_t kIdescAW = idesc_bf16_f32(128, kHeadDim, 0, 1);  // A K-major, B MN-major
 
 __global__ void __launch_bounds__(kPrepThreads) txl_prep_kernel(const TxlParams p) {
-  __shared__ __align__(16) float w_s[kHeadDim * kHeadDim];  // W[e][f] of this head
-  __shared__ __align__(16) float wv_s[kHeadDim];            // W^T v
-  griddep_wait();
+  // A: 128 rows x 128 B (q + v, bf16); B: 64 rows (e) x 128 B (W[e][0..63], bf16);
+  // both 128-byte swizzled, 1024-byte aligned
+  __shared__ __align__(1024) uint8_t a_s[128 * 128];
+  __shared__ __align__(1024) uint8_t w_s[64 * 128];
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ uint32_t tmem_slot;
   const int tid = threadIdx.x;
   if (static_cast<int>(blockIdx.y) == p.BH) {
+    griddep_wait();
     // key sinusoid table: row j = (cos w_m j, sin w_m j) for m = 0 .. 31
     const int j = blockIdx.x * kPrepThreads + tid;
     if (j >= p.Lk) return;
@@ -63,86 +70,98 @@ __global__ void __launch_bounds__(kPrepThreads) txl_prep_kernel(const TxlParams 
   const int bh = blockIdx.y;
   const int h = bh % p.H;
   const int row0 = blockIdx.x * kRowsPerBlock;
-  if (row0 >= p.Lq) return;
+  if (row0 >= p.Lq) return;  // uniform over the CTA
+  const int warp = tid >> 5;
+  if (tid == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(&tmem_slot), 64);
+    tmem_relinquish();
+  }
+  griddep_wait();
+  // W (fp32, [e][f]) to bf16: row e of the MN-major operand holds f = 0 .. 63
   {
-    const float4* src = reinterpret_cast<const float4*>(p.W + static_cast<size_t>(h) * kHeadDim * kHeadDim);
-    float4* dst = reinterpret_cast<float4*>(w_s);
-    for (int i = tid; i < kHeadDim * kHeadDim / 4; i += kPrepThreads) dst[i] = __ldg(src + i);
+    const float4* wsrc = reinterpret_cast<const float4*>(p.W + static_cast<size_t>(h) * kHeadDim * kHeadDim);
+    for (int i = tid; i < kHeadDim * kHeadDim / 8; i += kPrepThreads) {  // 8 values (16 B) each
+      const int e = i >> 3, ch = i & 7;
+      const float4 x0 = __ldg(wsrc + 2 * i), x1 = __ldg(wsrc + 2 * i + 1);
+      const uint4 v4 = make_uint4(pack_bf16x2(x0.x, x0.y), pack_bf16x2(x0.z, x0.w), pack_bf16x2(x1.x, x1.y),
+                                  pack_bf16x2(x1.z, x1.w));
+      *reinterpret_cast<uint4*>(w_s + e * 128 + ((ch ^ (e & 7)) << 4)) = v4;
+    }
   }
-  __syncthreads();
-  if (tid < kHeadDim) {  // W^T v, added to every row's a
-    const float* v = p.uv + (static_cast<size_t>(p.H) + h) * kHeadDim;
-    float acc = 0.f;
-    for (int e = 0; e < kHeadDim; ++e) acc = fmaf(__ldg(v + e), w_s[e * kHeadDim + tid], acc);
-    wv_s[tid] = acc;
-  }
-  __syncthreads();
-  const int r = tid >> 2;   // row within the block
-  const int g = tid & 3;    // components 16 g .. 16 g + 15
-  const int row = row0 + r;
-  if (row >= p.Lq) return;
-  const size_t qrow = static_cast<size_t>(bh) * p.Lq + row;
-  float q[kHeadDim];
+  const int row = row0 + tid;
+  const bool row_ok = row < p.Lq;
+  const size_t qrow = static_cast<size_t>(bh) * p.Lq + (row_ok ? row : row0);
+  const float* u = p.uv + static_cast<size_t>(h) * kHeadDim;
+  const float* v = p.uv + (static_cast<size_t>(p.H) + h) * kHeadDim;
+  uint4* dst = reinterpret_cast<uint4*>(p.Q2 + qrow * (2 * kHeadDim));
+  // content half q + u to global; q + v (bf16) to the A operand (zero rows past Lq)
   {
     const uint4* src = reinterpret_cast<const uint4*>(p.Q + qrow * kHeadDim);
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
       const uint4 u4 = __ldg(src + c);
       const uint32_t w4[4] = {u4.x, u4.y, u4.z, u4.w};
+      uint32_t qu[4], qv[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4[e]));
-        q[8 * c + 2 * e] = f.x;
-        q[8 * c + 2 * e + 1] = f.y;
+        const int k = 8 * c + 2 * e;
+        qu[e] = pack_bf16x2(f.x + __ldg(u + k), f.y + __ldg(u + k + 1));
+        qv[e] = row_ok ? pack_bf16x2(f.x + __ldg(v + k), f.y + __ldg(v + k + 1)) : 0u;
       }
+      if (row_ok) dst[c] = make_uint4(qu[0], qu[1], qu[2], qu[3]);
+      *reinterpret_cast<uint4*>(a_s + tid * 128 + ((c ^ (tid & 7)) << 4)) = make_uint4(qv[0], qv[1], qv[2], qv[3]);
     }
   }
-  // a_f = sum_e q_e W[e][f] + (W^T v)_f for this thread's 16 components
-  float a[16];
+  fence_async_smem();  // the operands' generic writes, visible to the tensor core
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  if (tid == 0) {
+    const uint64_t da = smem_desc_sw128(smem_u32(a_s), 16, 1024);
+    const uint64_t dw = smem_desc_sw128(smem_u32(w_s), 8192, 1024);
 #pragma unroll
-  for (int f = 0; f < 16; ++f) a[f] = wv_s[16 * g + f];
+    for (int kk = 0; kk < kHeadDim / 16; ++kk)  // K-step of 16 e: 32 B of A's rows, 2 row groups of W
+      umma_bf16_ss(tmem, da + 2 * kk, dw + 128 * kk, kIdescAW, kk > 0 ? 1u : 0u);
+    tc_commit(smem_u32(&bar));
+  }
+  const bool ok = mbar_wait(smem_u32(&bar), 0);
+  tc_fence_after();
+  // a of this row (TMEM lane tid), rotated by the angles w_m p
+  const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+  const float pos = static_cast<float>(row + p.q_offset);
 #pragma unroll
-  for (int e = 0; e < kHeadDim; ++e) {
-    const float4* wr = reinterpret_cast<const float4*>(w_s + e * kHeadDim + 16 * g);
+  for (int half = 0; half < 2; ++half) {
+    uint32_t r[32];
+    tmem_ld32(tmem + lane_base + 32 * half, r);
+    tmem_ld_wait(r);
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      const float4 w4 = wr[c];
-      a[4 * c] = fmaf(q[e], w4.x, a[4 * c]);
-      a[4 * c + 1] = fmaf(q[e], w4.y, a[4 * c + 1]);
-      a[4 * c + 2] = fmaf(q[e], w4.z, a[4 * c + 2]);
-      a[4 * c + 3] = fmaf(q[e], w4.w, a[4 * c + 3]);
+      uint32_t rot[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int mm = 4 * c + e;          // pair within the half
+        const int m = 16 * half + mm;      // frequency index
+        float sn, cs;
+        sincosf(pos * p.omega[m], &sn, &cs);
+        const float a0 = __uint_as_float(r[2 * mm]), a1 = __uint_as_float(r[2 * mm + 1]);
+        rot[e] = pack_bf16x2(fmaf(a0, sn, a1 * cs), fmaf(a1, sn, -a0 * cs));
+      }
+      if (row_ok && ok) dst[8 + 4 * half + c] = make_uint4(rot[0], rot[1], rot[2], rot[3]);
     }
   }
-  // the query half of the position product: a rotated by the angles w_m p
-  const float pos = static_cast<float>(row + p.q_offset);
-  uint32_t rot[8];
-#pragma unroll
-  for (int m = 0; m < 8; ++m) {
-    float sn, cs;
-    sincosf(pos * p.omega[8 * g + m], &sn, &cs);
-    const float a0 = a[2 * m], a1 = a[2 * m + 1];
-    rot[m] = pack_bf16x2(fmaf(a0, sn, a1 * cs), fmaf(a1, sn, -a0 * cs));
+  if (!ok && tid == 0 && p.status) atomicCAS(p.status, 0, -4);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 64);
   }
-  // the content half: q + u, components 16 g .. 16 g + 15 (reloaded: q[]
-  // is indexed by constants only, so it stays in registers)
-  const float* u = p.uv + static_cast<size_t>(h) * kHeadDim + 16 * g;
-  const uint4* qg = reinterpret_cast<const uint4*>(p.Q + qrow * kHeadDim) + 2 * g;
-  uint32_t qu[8];
-#pragma unroll
-  for (int c = 0; c < 2; ++c) {
-    const uint4 u4 = __ldg(qg + c);
-    const uint32_t w4[4] = {u4.x, u4.y, u4.z, u4.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4[e]));
-      qu[4 * c + e] = pack_bf16x2(f.x + __ldg(u + 8 * c + 2 * e), f.y + __ldg(u + 8 * c + 2 * e + 1));
-    }
-  }
-  uint4* dst = reinterpret_cast<uint4*>(p.Q2 + qrow * (2 * kHeadDim));
-  dst[2 * g] = make_uint4(qu[0], qu[1], qu[2], qu[3]);
-  dst[2 * g + 1] = make_uint4(qu[4], qu[5], qu[6], qu[7]);
-  dst[8 + 2 * g] = make_uint4(rot[0], rot[1], rot[2], rot[3]);
-  dst[8 + 2 * g + 1] = make_uint4(rot[4], rot[5], rot[6], rot[7]);
 }
 
 }  // namespace
