@@ -821,9 +821,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(bar(kBarSFree + x));  // the next S may overwrite this buffer
         float* xs = reinterpret_cast<float*>(&sr[0][0]);
 
-        // ---- tile class: far (one constant per row) or near (per element)
-        const int rel_hi = j0 + kBN - 1 - p_lo;    // largest key - query offset in the tile
-        const int rel_lo = j0 - (p_lo + kBM - 1);  // smallest
+        // ---- tile class, per warp (its 32 rows): far (one constant per row)
+        // or near (per element). Deciding per warp rather than per tile lets
+        // the warps of a tile next to the diagonal whose rows do not reach
+        // the near band take the far path.
+        const int p_lo_w = p_lo + 32 * (warp & 3);    // position of this warp's first row
+        const int rel_hi = j0 + kBN - 1 - p_lo_w;    // largest key - query offset in the warp's rows
+        const int rel_lo = j0 - (p_lo_w + 31);       // smallest
         bool far_l, far_r;
         if constexpr (MODE == 0) {
           far_l = rel_hi <= -p.t5_R;
@@ -834,7 +838,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           far_l = rel_hi <= -kc;
           far_r = rel_lo >= kc;
         }
-        const bool need_mask = (p.causal && j0 + kBN - 1 > p_lo) || (j0 + kBN > lk_eff);
+        const bool need_mask = (p.causal && j0 + kBN - 1 > p_lo_w) || (j0 + kBN > lk_eff);
         int lim = 127;
         if (need_mask) {
           lim = lk_eff - 1 - j0;
