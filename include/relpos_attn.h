@@ -111,7 +111,7 @@ extern "C" {
  *               causal); Shaw: clip k (1 <= k <= 64); DeBERTa: k (1 <= k <= 4096);
  *               ALiBi, TXL: ignored.
  *               Shaw's per-row tables and T5's bias-by-offset table live in
- *               shared memory: this build runs Shaw k <= 21, and T5 as long as
+ *               shared memory: this build runs Shaw k <= 27, and T5 as long as
  *               the distance at which the last bucket starts (about
  *               max_distance, or the longest offset of the call if shorter)
  *               is at most about 2500 (beyond about 480 through a slower

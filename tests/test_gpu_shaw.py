@@ -20,7 +20,8 @@ SHAW = WORKLOADS["shaw"]
     (2, 3, 300, 300, 16, False, 0),
     (1, 2, 300, 300, 16, True, 0),
     (1, 2, 129, 400, 4, False, 0),
-    (1, 2, 64, 300, 21, True, 236),   # the largest clip that fits shared memory
+    (1, 2, 64, 300, 21, True, 236),
+    (1, 2, 300, 300, 27, False, 0),   # the largest clip that fits shared memory
     (1, 1, 1, 500, 16, True, 499),   # one query row (decode-shaped)
     (1, 2, 256, 256, 1, False, 0),
     (1, 2, 1100, 1100, 8, False, 0),   # odd query tiles, many key tiles: a pair with no tile b
@@ -48,7 +49,7 @@ def test_shaw_full_sampled():
 def test_shaw_clip_beyond_shared_memory_is_unsupported():
     import pytest as _pt
     import transformer_attention_relative_gb300 as rp
-    w = SHAW.replace(B=1, H=1, Lq=64, Lk=64, rel_param=22)
+    w = SHAW.replace(B=1, H=1, Lq=64, Lk=64, rel_param=28)
     x = make_inputs(w)
     with _pt.raises(rp.RelposError) as e:
         G.run_gpu(w, x)

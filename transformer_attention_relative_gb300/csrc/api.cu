@@ -325,6 +325,8 @@ int attn_fwd_impl(int mode, int dtype, const void* Q, const void* K, const void*
       (table1 && !aligned16(table1)))
     return RELPOS_ERR_INVALID_ARG;
   if (mode == RELPOS_DEBERTA && rel_param > 4096) return RELPOS_ERR_UNSUPPORTED;
+  // Shaw's 2k + 1 table rows are one 64-row tensor-core operand
+  if (mode == RELPOS_SHAW && 2 * rel_param + 1 > 64) return RELPOS_ERR_UNSUPPORTED;
 
   int* status = status_ptr();
   if (!status) return RELPOS_ERR_CUDA;

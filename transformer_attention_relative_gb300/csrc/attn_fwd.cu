@@ -57,7 +57,7 @@ namespace {
 
 constexpr int kBM = 128;       // query rows per tile (two tiles per item)
 constexpr int kBN = 128;       // keys per tile
-constexpr int kStages = 3;     // K/V ring depth
+constexpr int kStages = 3;     // K/V ring depth (barrier slots; Smem<MODE>::kStages are used)
 constexpr int kThreads = 384;  // 12 warps
 constexpr uint32_t kTileBytes = kBM * kHeadDim * 2;  // 16 KB: 128 rows x 128 B
 // Shared-memory layout: the item's two query tiles, the K ring, the V ring,
@@ -66,6 +66,9 @@ constexpr uint32_t kTileBytes = kBM * kHeadDim * 2;  // 16 KB: 128 rows x 128 B
 // tiles and K stages hold two 64-column halves of kTileBytes each.
 template <int MODE>
 struct Smem {
+  // K / V ring depth: Shaw keeps two stages, for the shared memory of its
+  // per-row tables (k up to 26)
+  static constexpr int kStages = MODE == 1 ? 2 : ::relpos::kStages;
   static constexpr uint32_t kHalves = MODE == 4 ? 2u : 1u;
   static constexpr uint32_t kQBytes = kHalves * kTileBytes;  // one query tile
   static constexpr uint32_t kKBytes = kHalves * kTileBytes;  // one K stage
@@ -98,14 +101,19 @@ enum : uint32_t {
   kBarComb = kBarTab + 2,  // both softmax warpgroups have published a split item's partial state
   kBarStag = kBarComb + 1,  // + item parity: warpgroup a is past the maximum of its first tile
   kBarFinal = kBarStag + 2,
-  kNumBars = kBarFinal + 1,
+  kBarQa = kBarFinal + 1,   // + tile, Shaw: q . a_K of the item's rows in TMEM
+  kBarWb = kBarQa + 2,      // + tile, Shaw: the value-side bins staged as an operand (128 arrivals)
+  kBarOv = kBarWb + 2,      // + tile, Shaw: O += bins . a_V done
+  kBarTbl = kBarOv + 2,     // Shaw: the a_K / a_V operand tiles are written (256 arrivals)
+  kNumBars = kBarTbl + 1,
 };
-constexpr uint32_t kOffTmemSlot = 256;
-constexpr uint32_t kOffAbort = 260;
+constexpr uint32_t kOffTmemSlot = 320;
+constexpr uint32_t kOffAbort = 324;
 static_assert(kNumBars * 8 <= kOffTmemSlot, "barrier block overflow");
 
 constexpr uint32_t kIdescQK = idesc_bf16_f32(kBM, kBN, 0, 0);       // Q, K both K-major
 constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, kHeadDim, 0, 1);  // P (TMEM), V MN-major
+constexpr uint32_t kIdescQa = idesc_bf16_f32(kBM, 64, 0, 0);        // Shaw: Q . a_K^T (64 table rows)
 
 RP_DEVI void record_error(int* status) {
   if (status) atomicCAS(status, 0, -4);
@@ -249,6 +257,29 @@ struct T5Tab {
 
 RP_DEVI int t5_copy_stride(int len4) { return (len4 + 28 + 31) & ~31; }
 
+// Shaw's tables after kOffAux (which sits 512 bytes past a 1024-byte
+// boundary): the a_K and a_V tiles (64 rows x 128 bytes, 128-byte swizzle,
+// rows past 2k zero; the B operands of the q . a_K product and of the value
+// product), then per warpgroup a region holding its rows' q . a_K values
+// during an item and, at the item's end, its rows' value-side bins as the
+// bf16 A operand of the value product (a 16 KB tile), then the bins
+// themselves (fp32, per row).
+struct ShawAux {
+  uint32_t tK, tV, qa0, rq, wbin, end;
+};
+__host__ __device__ inline ShawAux shaw_aux(int row_stride) {
+  ShawAux a;
+  a.tK = 512u;
+  a.tV = a.tK + 8192u;
+  a.qa0 = a.tV + 8192u;
+  uint32_t rq = 128u * static_cast<uint32_t>(row_stride) * 4u;
+  if (rq < 16384u) rq = 16384u;
+  a.rq = (rq + 1023u) & ~1023u;
+  a.wbin = a.qa0 + 2u * a.rq;
+  a.end = a.wbin + 256u * static_cast<uint32_t>(row_stride) * 4u;
+  return a;
+}
+
 // Bytes of the mode's relative-term tables after kOffAux (16-byte multiple);
 // the split-item (m, l) exchange follows them.
 __host__ __device__ inline uint32_t fwd_aux_bytes(int mode, const FwdParams& p) {
@@ -259,9 +290,7 @@ __host__ __device__ inline uint32_t fwd_aux_bytes(int mode, const FwdParams& p) 
     const uint32_t ncopy = p.t5_compact ? 1u : 4u;
     aux = bkt_bytes + 2u * 2u * ncopy * stride * 4u + 2u * 128u * 4u;
   } else if (mode == 1) {
-    const uint32_t nrel = 2u * p.kclip + 1u;
-    const uint32_t tbl = (nrel * kHeadDim * 2u + 15u) & ~15u;
-    aux = 2u * tbl + 4u * 128u * static_cast<uint32_t>(p.row_stride) * 4u;
+    aux = shaw_aux(p.row_stride).end;
   }
   return (aux + 15u) & ~15u;
 }
@@ -305,6 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   using L = Smem<MODE>;
   constexpr uint32_t kOffQ = L::kOffQ, kOffK = L::kOffK, kOffV = L::kOffV, kOffBar = L::kOffBar,
                      kOffAux = L::kOffAux;
+  constexpr int kRing = L::kStages;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t sbase = (raw_addr + 1023u) & ~1023u;
@@ -331,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* aux = smem + kOffAux;
   uint8_t* bkt = aux;  // T5: head-independent bucket of each table offset
   const int nrel = 2 * p.kclip + 1;
-  const uint32_t shaw_tbl = (static_cast<uint32_t>(nrel) * kHeadDim * 2u + 15u) & ~15u;
+  const ShawAux shaw = shaw_aux(p.row_stride);
   if constexpr (MODE == 0) {
     for (int x = threadIdx.x; x < p.t5_tab_len4 + 4; x += kThreads) {
       const int xc = min(x, p.t5_tab_len - 1);
@@ -346,6 +376,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         cnt = 128;  // every thread of a softmax warpgroup
       if (i == kBarOFree || i == kBarOFree + 1 || i == kBarComb)
         cnt = 256;  // both softmax warpgroups (or one, arriving twice)
+      if (i == kBarWb || i == kBarWb + 1) cnt = 128;
+      if (i == kBarTbl) cnt = 256;
       if (i == kBarQEmpty || i == kBarFinal || (i >= kBarKEmpty && i < kBarVEmpty + kStages))
         cnt = 2;    // both MMA issuers
       mbar_init(bar(i), cnt);
@@ -368,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (first_loads) {
     it0 = make_item<SPLIT, PAD>(p, item_at(0, p.causal));
     two0 = !it0.split && it0.hi[1] > 0;
-    nk0 = it0.ns < kStages ? it0.ns : kStages;
+    nk0 = it0.ns < kRing ? it0.ns : kRing;
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
@@ -427,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int rr = 0, w = item_at(0, p.causal); ok && w < nitems; w = item_at(++rr, p.causal), ++item_cnt) {
         const Item it = make_item<SPLIT, PAD>(p, w);
         // the first item's Q and first ring stages were loaded in the setup
-        const int pre = item_cnt == 0 ? min(it.ns, kStages) : 0;
+        const int pre = item_cnt == 0 ? min(it.ns, kRing) : 0;
         if (kq && item_cnt > 0) {
           ok = mbar_wait_warp(bar(kBarQEmpty), (item_cnt - 1) & 1);
           if (!ok) break;
@@ -439,9 +471,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int j = 0; j < it.ns; ++j, ++it_cnt) {
           if (j < pre) continue;
-          const uint32_t st = it_cnt % kStages;
-          if (it_cnt >= kStages) {
-            ok = mbar_wait_warp(bar(empty0 + st), ((it_cnt / kStages) - 1) & 1);
+          const uint32_t st = it_cnt % kRing;
+          if (it_cnt >= kRing) {
+            ok = mbar_wait_warp(bar(empty0 + st), ((it_cnt / kRing) - 1) & 1);
             if (!ok) break;
           }
           mbar_arrive_expect_tx_elect(bar(full0 + st), stage_bytes);
@@ -458,9 +490,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 1;
       }
       // never leave with copies in flight: wait (bounded) for the last loads
-      const uint32_t first = it_cnt > kStages ? it_cnt - kStages : 0;
+      const uint32_t first = it_cnt > kRing ? it_cnt - kRing : 0;
       for (uint32_t k = first; k < it_cnt; ++k)
-        mbar_wait_warp(bar(full0 + k % kStages), (k / kStages) & 1, 100000000ull);
+        mbar_wait_warp(bar(full0 + k % kRing), (k / kRing) & 1, 100000000ull);
       if (kq && item_cnt > 0) mbar_wait_warp(bar(kBarQFull), (item_cnt - 1) & 1, 100000000ull);
     } else if (warp == 1 || warp == 3) {
       // ------------------------------------------------------------ MMA issuers
@@ -500,9 +532,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto advance = [&](int& pos, uint32_t full0, uint32_t empty0) -> int {
           while (pos < it.ns && !stream_uses(it, x, pos)) {
             const uint32_t r = kv_it + pos;
-            ok = mbar_wait_warp(bar(full0 + r % kStages), (r / kStages) & 1);
+            ok = mbar_wait_warp(bar(full0 + r % kRing), (r / kRing) & 1);
             if (!ok) return it.ns;
-            if (lane == 0) mbar_arrive(bar(empty0 + r % kStages));
+            if (lane == 0) mbar_arrive(bar(empty0 + r % kRing));
             ++pos;
           }
           return pos;
@@ -512,8 +544,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int pos = advance(kpos, kBarKFull, kBarKEmpty);
           if (!ok) return false;
           const uint32_t r = kv_it + pos;
-          const uint32_t st = r % kStages;
-          if (!mbar_wait_warp(bar(kBarKFull + st), (r / kStages) & 1)) return false;
+          const uint32_t st = r % kRing;
+          if (!mbar_wait_warp(bar(kBarKFull + st), (r / kRing) & 1)) return false;
           if (sis > 0 && !mbar_wait_warp(bar(kBarSFree + x), (sis - 1) & 1)) return false;
           tc_fence_after();
           const uint64_t dk = dk0 + st * kKStep;
@@ -530,6 +562,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++kpos;
           return true;
         };
+        if constexpr (MODE == 1) {
+          // Shaw: q . a_K[r] of every row of the item's tile (Q . a_K^T, 64
+          // table rows, the rows past 2k zero) into this tile's O accumulator,
+          // which the previous item's epilogue has read; the softmax reads
+          // it back before its first P.V
+          if (mine > 0) {
+            if (ocnt == 0) ok = mbar_wait_warp(bar(kBarTbl), 0);
+            if (ok && ocnt > 0) ok = mbar_wait_warp(bar(kBarOFree + x), (ocnt - 1) & 1);
+            if (!ok) break;
+            tc_fence_after();
+            const uint64_t dta = smem_desc_sw128(sbase + kOffAux + shaw.tK, 16, 1024);
+#pragma unroll
+            for (int kk = 0; kk < kHeadDim / 16; ++kk)
+              umma_bf16_ss_elect(o_col, dq + 2 * kk, dta + 2 * kk, kIdescQa, kk > 0 ? 1u : 0u);
+            tc_commit_elect(bar(kBarQa + x));
+          }
+        }
         if (mine > 0) ok = issue_s(0);
         for (int i = 0; ok && i < mine; ++i) {
           // look ahead: the next key tile's scores (after the last one, free
@@ -545,10 +594,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int pos = advance(vpos, kBarVFull, kBarVEmpty);
           if (!ok) break;
           const uint32_t r = kv_it + pos;
-          const uint32_t st = r % kStages;
+          const uint32_t st = r % kRing;
           ok = mbar_wait_warp(bar(kBarPFull + x), pvc & 1);
-          if (ok && i == 0 && ocnt > 0) ok = mbar_wait_warp(bar(kBarOFree + x), (ocnt - 1) & 1);
-          if (ok) ok = mbar_wait_warp(bar(kBarVFull + st), (r / kStages) & 1);
+          if (MODE != 1 && ok && i == 0 && ocnt > 0) ok = mbar_wait_warp(bar(kBarOFree + x), (ocnt - 1) & 1);
+          if (ok) ok = mbar_wait_warp(bar(kBarVFull + st), (r / kRing) & 1);
           tc_fence_after();
           if (!ok) break;
           const uint64_t dv = dv0 + st * kStageStep;
@@ -560,6 +609,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++pvc;
           ++vpos;
         }
+        if constexpr (MODE == 1) {
+          // Shaw: O += bins . a_V once the softmax has staged its rows' bins
+          if (ok && mine > 0) {
+            ok = mbar_wait_warp(bar(kBarWb + x), ocnt & 1);
+            if (!ok) break;
+            tc_fence_after();
+            const uint64_t dwb = smem_desc_sw128(sbase + kOffAux + shaw.qa0 + x * shaw.rq, 16, 1024);
+            const uint64_t dtv = smem_desc_sw128(sbase + kOffAux + shaw.tV, 8192, 1024);
+#pragma unroll
+            for (int kk = 0; kk < 64 / 16; ++kk)
+              umma_bf16_ss_elect(o_col, dwb + 2 * kk, dtv + 128 * kk, kIdescPV, 1u);
+            tc_commit_elect(bar(kBarOv + x));
+          }
+        }
         // The other tile's remaining positions, K and V stage of each position
         // together: releasing every K stage first could wait for a K load that
         // needs a V stage this warp has not released yet (through the other
@@ -567,12 +630,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int pos = min(kpos, vpos); ok && pos < it.ns; ++pos) {
           const uint32_t r = kv_it + pos;
           if (pos >= kpos) {
-            ok = mbar_wait_warp(bar(kBarKFull + r % kStages), (r / kStages) & 1);
-            if (ok && lane == 0) mbar_arrive(bar(kBarKEmpty + r % kStages));
+            ok = mbar_wait_warp(bar(kBarKFull + r % kRing), (r / kRing) & 1);
+            if (ok && lane == 0) mbar_arrive(bar(kBarKEmpty + r % kRing));
           }
           if (ok && pos >= vpos) {
-            ok = mbar_wait_warp(bar(kBarVFull + r % kStages), (r / kStages) & 1);
-            if (ok && lane == 0) mbar_arrive(bar(kBarVEmpty + r % kStages));
+            ok = mbar_wait_warp(bar(kBarVFull + r % kRing), (r / kRing) & 1);
+            if (ok && lane == 0) mbar_arrive(bar(kBarVEmpty + r % kRing));
           }
         }
         kv_it += it.ns;
@@ -603,18 +666,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float kNegInf = -INFINITY;
     bool err = false;
     if constexpr (MODE == 1) {
-      // the relative key / value tables, read only by the softmax warpgroups
+      // the relative key / value tables as tensor-core operands: row r holds
+      // a_K[r] (a_V[r]), 16-byte chunks swizzled by the row, rows past 2k zero
       griddep_wait();
       const uint4* srcK = reinterpret_cast<const uint4*>(p.aK);
       const uint4* srcV = reinterpret_cast<const uint4*>(p.aV);
-      uint4* dK = reinterpret_cast<uint4*>(aux);
-      uint4* dV = reinterpret_cast<uint4*>(aux + shaw_tbl);
-      const int n16 = nrel * kHeadDim * 2 / 16;
-      for (int i = static_cast<int>(threadIdx.x) - 128; i < n16; i += 256) {
-        dK[i] = __ldg(srcK + i);
-        dV[i] = __ldg(srcV + i);
+      for (int i = static_cast<int>(threadIdx.x) - 128; i < 64 * 8; i += 256) {
+        const int r = i >> 3, c = i & 7;
+        const uint32_t off = static_cast<uint32_t>(r) * 128u + (static_cast<uint32_t>(c ^ (r & 7)) << 4);
+        const bool in = r < nrel;
+        *reinterpret_cast<uint4*>(aux + shaw.tK + off) = in ? __ldg(srcK + r * 8 + c) : make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(aux + shaw.tV + off) = in ? __ldg(srcV + r * 8 + c) : make_uint4(0u, 0u, 0u, 0u);
       }
-      named_bar_sync(1, 256);
+      // visible to the tensor core, then to the issuers (their first
+      // q . a_K product waits for this)
+      fence_async_smem();
+      mbar_arrive(bar(kBarTbl));
     }
 
     T5Tab tab{};
@@ -622,7 +689,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float hb_next = 0.f;     // T5: thread t < num_buckets holds entry t of the next table's row
     float* qa = nullptr;    // Shaw: q . a_K[r] of this row (log2 units)
     float* wbin = nullptr;  // Shaw: probability mass per clipped offset of this row
-    const __nv_bfloat16* aV_s = nullptr;
+    uint8_t* wb_tile = nullptr;  // Shaw: this warpgroup's bins operand (over its q . a_K rows)
     if constexpr (MODE == 0) {
       tab.len4 = p.t5_tab_len4;
       tab.stride = t5_copy_stride(p.t5_tab_len4);
@@ -635,13 +702,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       tab.base = reinterpret_cast<float*>(aux + bkt_bytes) + x * 2 * tab.ncopy * tab.stride;
       hbias = reinterpret_cast<float*>(aux + bkt_bytes) + 2 * 2 * tab.ncopy * tab.stride + x * 128;
     } else if constexpr (MODE == 1) {
-      aV_s = reinterpret_cast<const __nv_bfloat16*>(aux + shaw_tbl);
-      float* qa_all = reinterpret_cast<float*>(aux + 2 * shaw_tbl);
       // rows p.row_stride floats apart: with 2k + 2 (even), the lanes of a
       // near tile, which read offsets r0 - t + c of their rows, hit distinct
       // banks (with 2k + 1 they are 2k words apart: one bank)
-      qa = qa_all + (x * 128 + t) * p.row_stride;
-      wbin = qa_all + 2 * 128 * p.row_stride + (x * 128 + t) * p.row_stride;
+      wb_tile = aux + shaw.qa0 + x * shaw.rq;
+      qa = reinterpret_cast<float*>(wb_tile) + t * p.row_stride;
+      wbin = reinterpret_cast<float*>(aux + shaw.wbin) + (x * 128 + t) * p.row_stride;
     }
     const int kc = p.kclip;
 
@@ -735,38 +801,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         add_l = tab.copy(buf, 0)[p.t5_tab_off - p.t5_R];
         add_r = tab.copy(buf, 0)[p.t5_tab_off + p.t5_R];
       } else if constexpr (MODE == 1) {
-        // q . a_K[r] for every clipped offset r, from this row of Q in global memory
-        float qf[kHeadDim];
-        const int row = i0 + t;
-        if (row < p.Lq) {
-          const uint4* src = reinterpret_cast<const uint4*>(p.Qg + (static_cast<size_t>(it.bh) * p.Lq + row) * kHeadDim);
+        // q . a_K[r] for every clipped offset r: the issuer computed Q . a_K^T
+        // into this tile's O accumulator before the item's first P.V
+        const bool ok = mbar_wait(bar(kBarQa + x), ocnt & 1);
+        err = __any_sync(0xffffffffu, !ok);
+        if (err) break;
+        tc_fence_after();
+        uint32_t qr[2][32];
+        tmem_ld32(tO, qr[0]);
+        tmem_ld32(tO + 32, qr[1]);
+        tmem_ld_wait(qr[0]);
+        tmem_ld_wait(qr[1]);
+        tc_fence_before();
+        const float* qv = reinterpret_cast<const float*>(&qr[0][0]);
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const uint4 u = __ldg(src + c);
-            const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4[e]));
-              qf[c * 8 + 2 * e] = f.x;
-              qf[c * 8 + 2 * e + 1] = f.y;
-            }
+        for (int r = 0; r < 64; ++r) {
+          if (r < nrel) {
+            qa[r] = qv[r] * sl2;
+            wbin[r] = 0.f;
           }
-        } else {
-#pragma unroll
-          for (int c = 0; c < kHeadDim; ++c) qf[c] = 0.f;
-        }
-        const __nv_bfloat16* aK_s = reinterpret_cast<const __nv_bfloat16*>(aux);
-        for (int r = 0; r < nrel; ++r) {
-          const __nv_bfloat162* rowk = reinterpret_cast<const __nv_bfloat162*>(aK_s + r * kHeadDim);
-          float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-          for (int e = 0; e < kHeadDim / 2; ++e) {
-            const float2 f = __bfloat1622float2(rowk[e]);
-            a0 = fmaf(qf[2 * e], f.x, a0);
-            a1 = fmaf(qf[2 * e + 1], f.y, a1);
-          }
-          qa[r] = (a0 + a1) * sl2;
-          wbin[r] = 0.f;
         }
         add_l = qa[0];
         add_r = qa[2 * kc];
@@ -1112,8 +1165,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       __syncwarp();
       if constexpr (MODE == 1) {
+        // the bins (with the masses beyond the clip) as the bf16 A operand of
+        // O += bins . a_V, over this row's q . a_K values (no longer needed)
         wbin[0] += mass_l;
         wbin[2 * kc] += mass_r;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint32_t w4[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int r = 8 * c + 2 * e;
+            w4[e] = pack_bf16x2(r < nrel ? wbin[r] : 0.f, r + 1 < nrel ? wbin[r + 1] : 0.f);
+          }
+          *reinterpret_cast<uint4*>(wb_tile + t * 128 + ((c ^ (t & 7)) << 4)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+        }
+        fence_async_smem();
+        mbar_arrive(bar(kBarWb + x));
+        const bool okv = mbar_wait(bar(kBarOv + x), ocnt & 1);
+        err = __any_sync(0xffffffffu, !okv);
+        if (err) break;
+        tc_fence_after();
       }
       // A split item whose other half also has key tiles: merge the two
       // partial states. Each warpgroup publishes its rows' (m, l), then writes
@@ -1123,29 +1194,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       float sa = 1.f, sb = 0.f, l_row = l_run;
       const int c0 = merge ? x * 32 : 0;
       if (merge) {
-        if constexpr (MODE == 1) {
-          // fold this half's relative-value term into its O first
-          uint32_t of[2][32];
-          tmem_ld32(tO, of[0]);
-          tmem_ld32(tO + 32, of[1]);
-          tmem_ld_wait(of[0]);
-          tmem_ld_wait(of[1]);
-          float* f = reinterpret_cast<float*>(&of[0][0]);
-          for (int r = 0; r < nrel; ++r) {
-            const float wr = wbin[r];
-            const __nv_bfloat162* rowv = reinterpret_cast<const __nv_bfloat162*>(aV_s + r * kHeadDim);
-#pragma unroll
-            for (int e = 0; e < kHeadDim / 2; ++e) {
-              const float2 v2 = __bfloat1622float2(rowv[e]);
-              f[2 * e] = fmaf(wr, v2.x, f[2 * e]);
-              f[2 * e + 1] = fmaf(wr, v2.y, f[2 * e + 1]);
-            }
-          }
-          tmem_st32(tO, of[0]);
-          tmem_st32(tO + 32, of[1]);
-          tmem_st_wait();
-          tc_fence_before();
-        }
         // (one buffer suffices: the partner writes it again only after a P.V
         // that waits for this warpgroup's release of the accumulators below)
         float2* slot = ml;
@@ -1181,17 +1229,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (merge) {
 #pragma unroll
         for (int c = 0; c < 32; ++c) o[c] = o[c] * sa + o[32 + c] * sb;
-      } else if constexpr (MODE == 1) {
-        for (int r = 0; r < nrel; ++r) {
-          const float wr = wbin[r];
-          const __nv_bfloat162* rowv = reinterpret_cast<const __nv_bfloat162*>(aV_s + r * kHeadDim);
-#pragma unroll
-          for (int e = 0; e < kHeadDim / 2; ++e) {
-            const float2 f = __bfloat1622float2(rowv[e]);
-            o[2 * e] = fmaf(wr, f.x, o[2 * e]);
-            o[2 * e + 1] = fmaf(wr, f.y, o[2 * e + 1]);
-          }
-        }
       }
       const int row = i0 + t;
       // rows past a padded element's length are zero rows
@@ -1247,7 +1284,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 uint32_t fwd_smem_bytes(int mode, const FwdParams& p) {
-  const uint32_t aux0 = mode == 4 ? Smem<4>::kOffAux : Smem<0>::kOffAux;
+  const uint32_t aux0 = mode == 4 ? Smem<4>::kOffAux : (mode == 1 ? Smem<1>::kOffAux : Smem<0>::kOffAux);
   return 1024u + aux0 + fwd_aux_bytes(mode, p) + (p.nsplit > 0 ? kCombBytes : 0u);
 }
 
