@@ -689,6 +689,27 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           }
         }
       };
+      // T5 near or masked sub-steps: dS summed per offset along the warp's
+      // diagonals. After column c, lane l's running sum belongs to the
+      // offset (its key - q0 - q_offset) - c, at extended-table index
+      // hbase + l - c; moving to column c + 1 the sums shift one lane up, and
+      // the one leaving lane 31 (no lane of this warp meets that offset
+      // again) goes to shared memory: one shared atomic per column and warp
+      // instead of one per element. Indices past the table (offsets beyond
+      // the saturation distance on a masked tile) clamp to its ends, which
+      // lie in the same saturated buckets.
+      const int hbase = (key - lane) - q0 - p.q_offset + R + kTabPad;
+      const int hlast = tab_len(R) - 1;
+      float dacc = 0.f;
+      auto diag_add = [&](int cc, float ds) {
+        if (cc > 0) {
+          if (lane == 31) atomicAdd(&hist[min(max(hbase + 32 - cc, 0), hlast)], dacc);
+          dacc = __shfl_up_sync(0xffffffffu, dacc, 1);
+          if (lane == 0) dacc = 0.f;
+        }
+        dacc += ds;
+      };
+      bool diag = false;  // a T5 sub-step that summed per offset
       if (nomask && (MODE == 0 ? (far_l || far_r) : (rel_hi <= 0 || rel_lo >= 0))) {
         // one bias per row (T5 beyond the saturation distance), or ALiBi with
         // every key on one side: the logit is s * scale + g (c - rb) with
@@ -752,12 +773,12 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           dsl += rel_hi <= 0 ? a : -a;  // |rel| = c - rb behind, rb - c ahead
         }
       } else if (MODE == 0 && nomask) {
+        diag = true;
         // T5 inside the saturation distance, no mask: the biases of the
         // columns' offsets rb - c read 4 at a time from F (index R + kTabPad
         // - rb + c), every dS added to its offset's sum (consecutive keys:
         // consecutive entries, no two lanes on one)
         const float4* bw = tab_window(tab, R, R + kTabPad - rb);
-        float* hrow = hist + (rb + R + kTabPad);  // entry of column c: hrow - c
 #pragma unroll
         for (int gi = 0; gi < 4; ++gi) {
           uint32_t pp[8], pd[8];
@@ -780,10 +801,10 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             const float2 t1 = __fadd2_rn(
                 make_float2(__uint_as_float(dr[4 * q + 2]), __uint_as_float(dr[4 * q + 3])), make_float2(-D.z, -D.w));
             const float2 d0 = __fmul2_rn(e0, t0), d1 = __fmul2_rn(e1, t1);
-            atomicAdd(hrow - 4 * q, d0.x);
-            atomicAdd(hrow - 4 * q - 1, d0.y);
-            atomicAdd(hrow - 4 * q - 2, d1.x);
-            atomicAdd(hrow - 4 * q - 3, d1.y);
+            diag_add(4 * q, d0.x);
+            diag_add(4 * q + 1, d0.y);
+            diag_add(4 * q + 2, d1.x);
+            diag_add(4 * q + 3, d1.y);
             pp[2 * qq] = pack_bf16x2(e0.x, e0.y);
             pp[2 * qq + 1] = pack_bf16x2(e1.x, e1.y);
             pd[2 * qq] = pack_bf16x2(d0.x, d0.y);
@@ -792,8 +813,9 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           emit(gi, pp, pd);
         }
       } else {
-        // per element: masks, the bias of each offset, T5 offsets inside the
-        // saturation distance summed per offset in shared memory
+        diag = MODE == 0;
+        // per element: masks, the bias of each offset, T5 dS summed per
+        // offset
 #pragma unroll
         for (int gi = 0; gi < 4; ++gi) {
           uint32_t pp[8], pd[8];
@@ -816,9 +838,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
               pv[u] = pr;
               dsv[u] = ds;
               if constexpr (MODE == 0) {
-                sumL += rel <= -R ? ds : 0.f;
-                sumR += rel >= R ? ds : 0.f;
-                if (valid && rel > -R && rel < R) atomicAdd(&hist[rel + R + kTabPad], ds);
+                diag_add(cc, ds);
               } else {
                 dsl = fmaf(ds, fabsf(static_cast<float>(rel)), dsl);
               }
@@ -829,6 +849,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           emit(gi, pp, pd);
         }
       }
+      if (MODE == 0 && diag) atomicAdd(&hist[min(max(hbase + lane - 63, 0), hlast)], dacc);
       tmem_st_wait();
       tc_fence_before();
       fence_async_smem();
