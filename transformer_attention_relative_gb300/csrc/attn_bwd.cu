@@ -355,7 +355,7 @@ __global__ void __launch_bounds__(kStThreads, 1)
 #pragma unroll
           for (int c = 0; c < 64; ++c) {
             const int rel = j0 + c0 + c - prow;
-            const bool valid = j0 + c0 + c < p.Lk && (!p.causal || rel <= 0);
+            const bool valid = (j0 + c0 + c < p.Lk) & (!p.causal | (rel <= 0));
             float b;
             if constexpr (MODE == 0)
               b = tab[min(max(rel + R + kTabPad, 0), tab_len(R) - 1)];
@@ -482,6 +482,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
   float* hist_b = hist + (MODE == 0 ? tab_len(R) : 0);
   float* red = hist_b + kMaxT5Buckets;  // side sums / ALiBi slope partials
   float* bsm = red + 16;                // T5 bias per bucket
+  float* strip = bsm + kMaxT5Buckets;   // T5: per compute warp, its sub-step's per-offset sums
 
   // query tiles that see a key of this tile: rows i with i + q_offset >= j0
   const int nqt = (p.Lq + kBT - 1) / kBT;
@@ -691,19 +692,24 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       };
       // T5 near or masked sub-steps: dS summed per offset along the warp's
       // diagonals. After column c, lane l's running sum belongs to the
-      // offset (its key - q0 - q_offset) - c, at extended-table index
-      // hbase + l - c; moving to column c + 1 the sums shift one lane up, and
-      // the one leaving lane 31 (no lane of this warp meets that offset
-      // again) goes to shared memory: one shared atomic per column and warp
-      // instead of one per element. Indices past the table (offsets beyond
-      // the saturation distance on a masked tile) clamp to its ends, which
-      // lie in the same saturated buckets.
+      // offset (its key - q0 - q_offset) - c = d + (key of lane 0 - q0 -
+      // q_offset) with d = l - c; moving to column c + 1 the sums shift one
+      // lane up, and the one leaving lane 31 (d = 32 - (c + 1): no lane of
+      // this warp meets that offset again) is parked in the warp's strip,
+      // entry d + 63. Each of the 95 diagonals d = -63 .. 31 of the sub-step
+      // ends in the strip exactly once (those still in lanes after the last
+      // column, d = l - 63, included), so plain stores suffice; the strip
+      // then goes into the histogram with three shared atomics per lane.
+      // Histogram indices past the table (offsets beyond the saturation
+      // distance on a masked tile) clamp to its ends, which lie in the same
+      // saturated buckets.
       const int hbase = (key - lane) - q0 - p.q_offset + R + kTabPad;
       const int hlast = tab_len(R) - 1;
+      float* wstrip = strip + (warp - 4) * 96;
       float dacc = 0.f;
       auto diag_add = [&](int cc, float ds) {
         if (cc > 0) {
-          if (lane == 31) atomicAdd(&hist[min(max(hbase + 32 - cc, 0), hlast)], dacc);
+          if (lane == 31) wstrip[95 - cc] = dacc;
           dacc = __shfl_up_sync(0xffffffffu, dacc, 1);
           if (lane == 0) dacc = 0.f;
         }
@@ -826,14 +832,16 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             for (int u = 0; u < 2; ++u) {
               const int cc = 16 * gi + e + u;
               const int rel = rb - cc;
-              const bool valid = key_ok && q0 + cc < p.Lq && (!p.causal || rel <= 0);
+              // branch-free: masked elements take 2^-inf = 0 (a divergent
+              // branch around each exponential costs several times the work)
+              const bool valid = key_ok & (q0 + cc < p.Lq) & (!p.causal | (rel <= 0));
               float b;
               if constexpr (MODE == 0)
                 b = tab[min(max(R + kTabPad - rel, 0), tab_len(R) - 1)];
               else
                 b = -alibi * fabsf(static_cast<float>(rel));
               const float s2 = fmaf(__uint_as_float(sr[cc]), p.scale_log2, b - lse_s[cc]);
-              const float pr = valid ? ex2_approx(s2) : 0.f;
+              const float pr = ex2_approx(valid ? s2 : -INFINITY);
               const float ds = pr * (__uint_as_float(dr[cc]) - dd_s[cc]);
               pv[u] = pr;
               dsv[u] = ds;
@@ -849,7 +857,12 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           emit(gi, pp, pd);
         }
       }
-      if (MODE == 0 && diag) atomicAdd(&hist[min(max(hbase + lane - 63, 0), hlast)], dacc);
+      if (MODE == 0 && diag) {
+        wstrip[lane] = dacc;
+        __syncwarp();
+        for (int e = lane; e < 95; e += 32) atomicAdd(&hist[min(max(hbase + e - 63, 0), hlast)], wstrip[e]);
+        __syncwarp();  // read before the next sub-step writes
+      }
       tmem_st_wait();
       tc_fence_before();
       fence_async_smem();
@@ -1006,7 +1019,8 @@ uint32_t stats_smem_bytes(int mode, int R) {
 // T5: four bias-table copies and the per-offset sums (ALiBi: none); bucket
 // sums, then 16 floats of side / slope partials
 uint32_t dkdv_smem_bytes(int mode, int R) {
-  const uint32_t t5 = mode == 0 ? (4u * static_cast<uint32_t>(tab_stride(R)) + static_cast<uint32_t>(tab_len(R))) * 4u : 0u;
+  const uint32_t t5 =
+      mode == 0 ? (4u * static_cast<uint32_t>(tab_stride(R)) + static_cast<uint32_t>(tab_len(R)) + 8u * 96u) * 4u : 0u;
   return 1024u + kKvOffAux + t5 + (2u * kMaxT5Buckets + 16u) * 4u;
 }
 

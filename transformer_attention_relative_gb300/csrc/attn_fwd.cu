@@ -137,6 +137,24 @@ struct Item {
 // Valid query rows and keys of (batch, head) bh: the batch element's length
 // in a right-padded batch (PAD: the launch variant that takes lengths),
 // otherwise no limit.
+// Predicated shared-memory store without a branch: a lane whose predicate
+// is off does not store.
+RP_DEVI void st_shared_f32_if(uint32_t addr, float v, int pred) {
+  asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t@q st.shared.f32 [%0], %1;\n\t}" ::"r"(addr), "f"(v),
+               "r"(pred)
+               : "memory");
+}
+
+// 8 consecutive 32-bit TMEM columns of this thread's lane, waited for.
+RP_DEVI void tmem_ld8_sync(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+      : "r"(taddr)
+      : "memory");
+}
+
 template <bool PAD>
 RP_DEVI int seq_len(const FwdParams& p, int bh) {
   if constexpr (!PAD) return 0x7fffffff;
@@ -1131,18 +1149,42 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else if (far_r) {
             mass_r += tile_sum;
           } else {
+            // In-band offsets (-k < rel < k) into their bins, masses beyond
+            // the clip in registers, from P as the P.V product takes it
+            // (bf16, read back from TMEM). Each in-band (row, offset) pair
+            // meets exactly one key of the item, so its bin is written once:
+            // a plain (predicated) store, as the lanes (rows one offset
+            // apart) disagree on which columns are in band. Only 16-column
+            // chunks from one end of the tile through the warp's band are
+            // read; the columns beyond lie on one side for every lane, and
+            // their mass is the tile's sum less what was read. The rolled
+            // chunk loop keeps this rarely taken path's code short.
             const int r0 = j0 - prow;
+            const int rlo = 1 - kc - (j0 - p_lo_w);                  // lane 0's first in-band column
+            const int chl = min(max(rlo, 0), 127) >> 4;                // chunks holding band columns
+            const int chh = min(max(rlo + 29 + 2 * kc, 0), 127) >> 4;  // (lane 31's last: rlo + 31 + 2k - 2)
+            const bool from_left = chh + 1 <= 8 - chl;                 // read [0, chh], else [chl, 7]
+            const int ch0 = from_left ? 0 : chl, ch1 = from_left ? chh : 7;
+            const uint32_t wb0 = smem_u32(wbin);
+            float ml = 0.f, mr = 0.f, rd = 0.f;
+#pragma unroll 1
+            for (int ch = ch0; ch <= ch1; ++ch) {
+              uint32_t w8[8];
+              tmem_ld8_sync(tP + 8 * ch, w8);
 #pragma unroll
-            for (int c = 0; c < 128; ++c) {
-              const int rel = r0 + c;
-              // branch-free: masses beyond the clip in registers, in-band
-              // offsets (-k < rel < k) into their bins; the probabilities
-              // as the P.V product takes them (bf16)
-              const float v = __uint_as_float((c & 1) ? (pk[c >> 1] & 0xffff0000u) : (pk[c >> 1] << 16));
-              mass_l += rel <= -kc ? v : 0.f;
-              mass_r += rel >= kc ? v : 0.f;
-              if (static_cast<unsigned>(rel + kc - 1) < static_cast<unsigned>(2 * kc - 1)) wbin[rel + kc] += v;
+              for (int e = 0; e < 16; ++e) {
+                const int rel = r0 + 16 * ch + e;
+                const float v = __uint_as_float((e & 1) ? (w8[e >> 1] & 0xffff0000u) : (w8[e >> 1] << 16));
+                rd += v;
+                ml += rel <= -kc ? v : 0.f;
+                mr += rel >= kc ? v : 0.f;
+                st_shared_f32_if(wb0 + 4u * static_cast<uint32_t>(min(max(rel + kc, 0), 2 * kc)), v,
+                                 static_cast<unsigned>(rel + kc - 1) < static_cast<unsigned>(2 * kc - 1));
+              }
             }
+            const float rest = tile_sum - rd;  // the unread columns, all on the far side
+            mass_l += from_left ? ml : ml + rest;
+            mass_r += from_left ? mr + rest : mr;
           }
         }
 
