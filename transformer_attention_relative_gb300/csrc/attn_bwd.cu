@@ -182,16 +182,11 @@ __global__ void __launch_bounds__(kStThreads, 1)
     tmem_alloc(sb + kStOffBar + kStSlot, 512);
     tmem_relinquish();
   }
-  griddep_wait();
-  if constexpr (MODE == 0) {
-    load_bucket_bias(bsm, p, h, tid);
-    __syncthreads();
-    build_bias_copies(tab, bsm, p, false, tid, kStThreads);
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kStOffBar + kStSlot);
+  griddep_wait();
 
   // registers: the loading and issuing warps need few, the compute
   // warpgroups hold 64 columns of S and dP at a time (4 x 32 x 56 + 8 x 32 x 224 <= 384 x 168)
@@ -256,6 +251,15 @@ __global__ void __launch_bounds__(kStThreads, 1)
   } else {
     setmaxnreg_inc<224>();
     // ---------------------------------------------------------- compute
+    // the bias table, built by the warpgroups that read it while the first
+    // tiles load and the first products run
+    if constexpr (MODE == 0) {
+      const int ct = static_cast<int>(threadIdx.x) - 128;  // 0 .. 255
+      load_bucket_bias(bsm, p, h, ct);
+      named_bar_sync(2, 256);
+      build_bias_copies(tab, bsm, p, false, ct, 256);
+      named_bar_sync(2, 256);
+    }
     const int x = (warp - 4) >> 2;  // TMEM buffer / parity of the key tiles taken
     const int t = ((warp & 3) << 5) | lane;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -504,19 +508,11 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     tmem_alloc(sb + kKvOffBar + kKvSlot, 512);
     tmem_relinquish();
   }
-  griddep_wait();
-  if constexpr (MODE == 0) {
-    load_bucket_bias(bsm, p, h, tid);
-    __syncthreads();
-    build_bias_copies(tab, bsm, p, true, tid, kKvThreads);
-    for (int x = tid; x < tab_len(R); x += kKvThreads) hist[x] = 0.f;
-    for (int x = tid; x < kMaxT5Buckets; x += kKvThreads) hist_b[x] = 0.f;
-  }
-  if (tid < 16) red[tid] = 0.f;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kKvOffBar + kKvSlot);
+  griddep_wait();
 
   if (warp < 4) {
     setmaxnreg_dec<56>();
@@ -627,6 +623,20 @@ __global__ void __launch_bounds__(kKvThreads, 1)
   } else if (warp < 12) {
     setmaxnreg_inc<200>();
     // ---------------------------------------------------------- compute
+    // The tables are built here, while the first tiles load and the first
+    // products run (only these warpgroups read them).
+    {
+      const int ct = static_cast<int>(threadIdx.x) - 128;  // 0 .. 255
+      if constexpr (MODE == 0) {
+        load_bucket_bias(bsm, p, h, ct);
+        named_bar_sync(3, 256);
+        build_bias_copies(tab, bsm, p, true, ct, 256);
+        for (int x = ct; x < tab_len(R); x += 256) hist[x] = 0.f;
+        for (int x = ct; x < kMaxT5Buckets; x += 256) hist_b[x] = 0.f;
+      }
+      if (ct < 16) red[ct] = 0.f;
+      named_bar_sync(3, 256);
+    }
     const int hf = (warp - 4) >> 2;  // query half 0 / 1 of every tile = TMEM buffer
     const int t = ((warp & 3) << 5) | lane;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -691,29 +701,46 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         }
       };
       // T5 near or masked sub-steps: dS summed per offset along the warp's
-      // diagonals. After column c, lane l's running sum belongs to the
-      // offset (its key - q0 - q_offset) - c = d + (key of lane 0 - q0 -
-      // q_offset) with d = l - c; moving to column c + 1 the sums shift one
-      // lane up, and the one leaving lane 31 (d = 32 - (c + 1): no lane of
-      // this warp meets that offset again) is parked in the warp's strip,
-      // entry d + 63. Each of the 95 diagonals d = -63 .. 31 of the sub-step
-      // ends in the strip exactly once (those still in lanes after the last
-      // column, d = l - 63, included), so plain stores suffice; the strip
-      // then goes into the histogram with three shared atomics per lane.
-      // Histogram indices past the table (offsets beyond the saturation
-      // distance on a masked tile) clamp to its ends, which lie in the same
-      // saturated buckets.
+      // diagonals, d = l - c for lane l and column c (offset: its key - q0
+      // - q_offset - c = d + the offset of lane 0 at column 0). The dS
+      // values are kept in dr[] as they are formed; then four independent
+      // chains (columns 16k .. 16k + 15) run their diagonal sums side by
+      // side: after each column a chain's sums shift one lane up, the one
+      // leaving lane 31 (d = 32 - c: no lane of this chain meets it again)
+      // parked in the warp's strip at entry d + 63, and after its last
+      // column the 32 sums still in its lanes (d = l - 16k - 15) are added
+      // to their entries. The 95 entries d = -63 .. 31 then go into the
+      // histogram with three shared atomics per lane. Histogram indices past
+      // the table (offsets beyond the saturation distance on a masked tile)
+      // clamp to its ends, which lie in the same saturated buckets.
       const int hbase = (key - lane) - q0 - p.q_offset + R + kTabPad;
       const int hlast = tab_len(R) - 1;
       float* wstrip = strip + (warp - 4) * 96;
-      float dacc = 0.f;
-      auto diag_add = [&](int cc, float ds) {
-        if (cc > 0) {
-          if (lane == 31) wstrip[95 - cc] = dacc;
-          dacc = __shfl_up_sync(0xffffffffu, dacc, 1);
-          if (lane == 0) dacc = 0.f;
+      auto diag_sums = [&]() {
+        for (int e = lane; e < 96; e += 32) wstrip[e] = 0.f;
+        __syncwarp();
+        float a[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int c = 16 * k + i;
+            if (i > 0) {
+              if (lane == 31) wstrip[95 - c] = a[k];
+              a[k] = __shfl_up_sync(0xffffffffu, a[k], 1);
+              if (lane == 0) a[k] = 0.f;
+            }
+            a[k] += __uint_as_float(dr[c]);
+          }
         }
-        dacc += ds;
+#pragma unroll
+        for (int k = 3; k >= 0; --k) {
+          __syncwarp();
+          wstrip[lane + 48 - 16 * k] += a[k];
+        }
+        __syncwarp();
+        for (int e = lane; e < 95; e += 32) atomicAdd(&hist[min(max(hbase + e - 63, 0), hlast)], wstrip[e]);
+        __syncwarp();  // read before the next sub-step writes
       };
       bool diag = false;  // a T5 sub-step that summed per offset
       if (nomask && (MODE == 0 ? (far_l || far_r) : (rel_hi <= 0 || rel_lo >= 0))) {
@@ -807,10 +834,10 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             const float2 t1 = __fadd2_rn(
                 make_float2(__uint_as_float(dr[4 * q + 2]), __uint_as_float(dr[4 * q + 3])), make_float2(-D.z, -D.w));
             const float2 d0 = __fmul2_rn(e0, t0), d1 = __fmul2_rn(e1, t1);
-            diag_add(4 * q, d0.x);
-            diag_add(4 * q + 1, d0.y);
-            diag_add(4 * q + 2, d1.x);
-            diag_add(4 * q + 3, d1.y);
+            dr[4 * q] = __float_as_uint(d0.x);  // dS, for the per-offset sums
+            dr[4 * q + 1] = __float_as_uint(d0.y);
+            dr[4 * q + 2] = __float_as_uint(d1.x);
+            dr[4 * q + 3] = __float_as_uint(d1.y);
             pp[2 * qq] = pack_bf16x2(e0.x, e0.y);
             pp[2 * qq + 1] = pack_bf16x2(e1.x, e1.y);
             pd[2 * qq] = pack_bf16x2(d0.x, d0.y);
@@ -846,7 +873,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
               pv[u] = pr;
               dsv[u] = ds;
               if constexpr (MODE == 0) {
-                diag_add(cc, ds);
+                dr[cc] = __float_as_uint(ds);  // for the per-offset sums
               } else {
                 dsl = fmaf(ds, fabsf(static_cast<float>(rel)), dsl);
               }
@@ -857,12 +884,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           emit(gi, pp, pd);
         }
       }
-      if (MODE == 0 && diag) {
-        wstrip[lane] = dacc;
-        __syncwarp();
-        for (int e = lane; e < 95; e += 32) atomicAdd(&hist[min(max(hbase + e - 63, 0), hlast)], wstrip[e]);
-        __syncwarp();  // read before the next sub-step writes
-      }
+      if (MODE == 0 && diag) diag_sums();
       tmem_st_wait();
       tc_fence_before();
       fence_async_smem();
@@ -885,8 +907,24 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         atomicAdd(&red[1], sumR);
       }
       const int ct = tid - 128;  // 0 .. 255
-      for (int xo = ct; xo < tab_len(R); xo += 256)
-        if (hist[xo] != 0.f) atomicAdd(&hist_b[t5_bucket_dev(xo - R - kTabPad, p.t5)], hist[xo]);
+      // per-offset sums into their buckets: 32 consecutive offsets per warp
+      // and round, summed per run of one bucket (a segmented scan over the
+      // lanes), one shared atomic per run; a bucket covers a run of offsets
+      // on each side, so few atomics meet on one address
+      for (int x0 = ct - lane; x0 < tab_len(R); x0 += 256) {
+        const int xo = x0 + lane;
+        const bool in = xo < tab_len(R);
+        float v = in ? hist[xo] : 0.f;
+        const int b = in ? t5_bucket_dev(xo - R - kTabPad, p.t5) : -1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float vo = __shfl_up_sync(0xffffffffu, v, o);
+          const int bo = __shfl_up_sync(0xffffffffu, b, o);
+          if (lane >= o && bo == b) v += vo;
+        }
+        const int bn = __shfl_down_sync(0xffffffffu, b, 1);
+        if (b >= 0 && (lane == 31 || bn != b) && v != 0.f) atomicAdd(&hist_b[b], v);
+      }
       named_bar_sync(3, 256);
       if (ct == 0) {
         atomicAdd(&hist_b[t5_bucket_dev(-R, p.t5)], red[0]);
