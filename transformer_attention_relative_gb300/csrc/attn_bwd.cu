@@ -84,14 +84,24 @@ __host__ __device__ inline int tab_stride(int R) { return ((tab_len(R) + 64 + 31
 RP_DEVI void load_bucket_bias(float* bsm, const BwdParams& p, int h, int tid) {
   if (tid < p.nb) bsm[tid] = __ldg(p.bias + tid * p.H + h) * kLog2e;
 }
+// Copy 0 first (with the bucket of each entry into bk[] when given: bk[y]
+// for entry y of E, offset y - R - kTabPad), then, after a named barrier of
+// the nthreads callers, copies 1 .. 3 from copy 0; the caller synchronizes
+// before reading them.
 RP_DEVI void build_bias_copies(float* base, const float* bsm, const BwdParams& p, bool reversed, int tid,
-                               int nthreads) {
+                               int nthreads, int bar_id, uint8_t* bk) {
   const int n = tab_len(p.R), st = tab_stride(p.R);
-  for (int x = tid; x < 4 * st; x += nthreads) {
+  for (int e = tid; e < st; e += nthreads) {
+    int y = min(e, n - 1);           // entry of F (reversed) or E
+    if (reversed) y = n - 1 - y;     // F[y] = E[n - 1 - y]
+    const int b = t5_bucket_dev(y - p.R - kTabPad, p.t5);
+    base[e] = bsm[b];
+    if (bk != nullptr && e < n) bk[y] = static_cast<uint8_t>(b);
+  }
+  named_bar_sync(bar_id, nthreads);
+  for (int x = st + tid; x < 4 * st; x += nthreads) {
     const int k = x / st, e = x - k * st;
-    int y = min(e + k, n - 1);         // entry of F (reversed) or E
-    if (reversed) y = n - 1 - y;       // F[y] = E[n - 1 - y]
-    base[x] = bsm[t5_bucket_dev(y - p.R - kTabPad, p.t5)];
+    base[x] = base[min(e + k, n - 1)];
   }
 }
 // the 64 entries from index w of a table kept as four shifted copies
@@ -257,7 +267,7 @@ __global__ void __launch_bounds__(kStThreads, 1)
       const int ct = static_cast<int>(threadIdx.x) - 128;  // 0 .. 255
       load_bucket_bias(bsm, p, h, ct);
       named_bar_sync(2, 256);
-      build_bias_copies(tab, bsm, p, false, ct, 256);
+      build_bias_copies(tab, bsm, p, false, ct, 256, 2, nullptr);
       named_bar_sync(2, 256);
     }
     const int x = (warp - 4) >> 2;  // TMEM buffer / parity of the key tiles taken
@@ -487,6 +497,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
   float* red = hist_b + kMaxT5Buckets;  // side sums / ALiBi slope partials
   float* bsm = red + 16;                // T5 bias per bucket
   float* strip = bsm + kMaxT5Buckets;   // T5: per compute warp, its sub-step's per-offset sums
+  uint8_t* bk = reinterpret_cast<uint8_t*>(strip + 8 * 96);  // T5: bucket of each offset (hist index)
 
   // query tiles that see a key of this tile: rows i with i + q_offset >= j0
   const int nqt = (p.Lq + kBT - 1) / kBT;
@@ -630,7 +641,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       if constexpr (MODE == 0) {
         load_bucket_bias(bsm, p, h, ct);
         named_bar_sync(3, 256);
-        build_bias_copies(tab, bsm, p, true, ct, 256);
+        build_bias_copies(tab, bsm, p, true, ct, 256, 3, bk);
         for (int x = ct; x < tab_len(R); x += 256) hist[x] = 0.f;
         for (int x = ct; x < kMaxT5Buckets; x += 256) hist_b[x] = 0.f;
       }
@@ -915,7 +926,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         const int xo = x0 + lane;
         const bool in = xo < tab_len(R);
         float v = in ? hist[xo] : 0.f;
-        const int b = in ? t5_bucket_dev(xo - R - kTabPad, p.t5) : -1;
+        const int b = in ? static_cast<int>(bk[xo]) : -1;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
           const float vo = __shfl_up_sync(0xffffffffu, v, o);
@@ -1054,11 +1065,14 @@ uint32_t stats_smem_bytes(int mode, int R) {
   return 1024u + kStOffAux + tab + (3u * 128u + kMaxT5Buckets) * 4u;
 }
 
-// T5: four bias-table copies and the per-offset sums (ALiBi: none); bucket
-// sums, then 16 floats of side / slope partials
+// T5: four bias-table copies, the per-offset sums, the compute warps'
+// strips and the bucket of each offset (ALiBi: none); bucket sums, 16 floats
+// of side / slope partials and the biases per bucket
 uint32_t dkdv_smem_bytes(int mode, int R) {
   const uint32_t t5 =
-      mode == 0 ? (4u * static_cast<uint32_t>(tab_stride(R)) + static_cast<uint32_t>(tab_len(R)) + 8u * 96u) * 4u : 0u;
+      mode == 0 ? (4u * static_cast<uint32_t>(tab_stride(R)) + static_cast<uint32_t>(tab_len(R)) + 8u * 96u) * 4u +
+                      ((static_cast<uint32_t>(tab_len(R)) + 15u) & ~15u)
+                : 0u;
   return 1024u + kKvOffAux + t5 + (2u * kMaxT5Buckets + 16u) * 4u;
 }
 
