@@ -35,9 +35,17 @@ __host__ __device__ inline int t5_bucket_dev(int rel, const T5Index& ix) {
     n = rel < 0 ? -rel : 0;
   }
   if (n < ix.exact) return base + n;
-  int b = ix.exact;
-  for (int q = 0; q < ix.nthr; ++q) b += (n >= ix.thr[q]) ? 1 : 0;
-  return base + b;
+  // the number of thresholds at or below n (they ascend): binary search
+  int lo = 0, hi = ix.nthr;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (n >= ix.thr[mid]) {
+      lo = mid + 1;
+    } else {
+      hi = mid;
+    }
+  }
+  return base + ix.exact + lo;
 }
 
 // Shaw ("Relative Position Embeddings, in depth", section "Shaw et al."):
