@@ -427,7 +427,8 @@ int attn_fwd_impl(int mode, int dtype, const void* Q, const void* K, const void*
     p.scale_log2 = scale * kLog2e;
     p.out = out;
     p.out_v8 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0;
-    p.stagger = mode == RELPOS_T5 && causal;  // long items of mostly far tiles
+    // long items of mostly far tiles: causal T5 and Transformer-XL
+    p.stagger = (mode == RELPOS_T5 || mode == RELPOS_TXL) && causal;
     p.status = status;
     p.kclip = rel_param;
     p.Qg = static_cast<const __nv_bfloat16*>(Qb);

@@ -768,7 +768,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // first tile's maximum, so that the two run about half a tile apart and
     // their exponential phases (MUFU) overlap the other's score and maximum
     // phases instead of each other. It pays on long items of mostly far
-    // tiles (causal T5); on short items the later start of b costs more.
+    // tiles (causal T5, causal Transformer-XL); elsewhere it gains nothing
+    // or, on short items, the later start of b costs more.
     // `stag` counts the items in which a has key tiles; the item's turn goes
     // to one of two alternating barriers: a can lead b by at most two items
     // (b has started the last tile of item n - 2 before a's item n has its
@@ -1377,6 +1378,7 @@ cudaError_t launch_fwd(int mode, bool out_f32, const CUtensorMap& tmQ, const CUt
     RP_FWD_VARIANTS(3)
   } else if (mode == 4) {
     RP_FWD_VARIANTS(4)
+    if (var == 2) kern = out_f32 ? relpos_fwd_kernel<4, true, 2> : relpos_fwd_kernel<4, false, 2>;
   }
 #undef RP_FWD_VARIANTS
   if (!kern) return cudaErrorNotSupported;
