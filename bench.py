@@ -574,7 +574,8 @@ def config_of(w, world, g, backward=False):
 
 # every configuration gets a block of its own in the bench line
 BLOCK_WORKLOADS = ("t5_base_bidir", "t5_causal", "shaw", "deberta", "txl_mem", "t5_decode",
-                   "t5_decode_evicted", "alibi_bidir", "alibi_causal", "t5_tiny_fp32")
+                   "t5_decode_evicted", "alibi_bidir", "alibi_causal", "alibi_d128", "t5_d128",
+                   "t5_tiny_fp32")
 BACKWARD_WORKLOADS = ("t5_base_bidir", "t5_causal", "alibi_causal")
 
 

@@ -73,7 +73,7 @@ extern "C" {
 /* return codes */
 #define RELPOS_OK 0
 #define RELPOS_ERR_INVALID_ARG (-1)    /* null pointer, bad size or parameter */
-#define RELPOS_ERR_UNSUPPORTED (-2)    /* valid request this build does not run (d != 64, ...) */
+#define RELPOS_ERR_UNSUPPORTED (-2)    /* valid request this build does not run (d = 128 Shaw, ...) */
 #define RELPOS_ERR_CUDA (-3)           /* a CUDA runtime call or launch failed */
 #define RELPOS_ERR_DEVICE_TIMEOUT (-4) /* a kernel gave up on a bounded wait */
 #define RELPOS_ERR_SCRATCH_LIMIT (-5)  /* request needs more than the fixed scratch of
@@ -105,7 +105,12 @@ extern "C" {
  *   B, H        batch and heads (>= 0; 0 makes the call a no-op).
  *   Lq, Lk      query and key lengths (Lq >= 0, Lk >= 0). Lk == 0 writes
  *               zeros.
- *   d           head dimension; this build supports d = 64.
+ *   d           head dimension: 64 for every mode; also 128 for T5 and
+ *               ALiBi with dtype BF16 (other modes and FP32 inputs at
+ *               d = 128 return RELPOS_ERR_UNSUPPORTED). At d = 128 a few
+ *               query rows take the prefill kernel, not the split-key
+ *               decode path, and T5 keeps a single table copy when its
+ *               four shifted copies do not fit beside the larger tiles.
  *   num_buckets T5 only: even, 4 <= num_buckets <= 128 (ignored otherwise).
  *   rel_param   T5: max_distance (> num_buckets/4 bidirectional, > num_buckets/2
  *               causal); Shaw: clip k (1 <= k <= 64); DeBERTa: k (1 <= k <= 4096);

@@ -61,7 +61,10 @@ def _fwd(**kw):
     (dict(Lq=-3), rp.RELPOS_ERR_INVALID_ARG),
     (dict(qoff=-1), rp.RELPOS_ERR_INVALID_ARG),
     (dict(d=0), rp.RELPOS_ERR_INVALID_ARG),
-    (dict(d=128), rp.RELPOS_ERR_UNSUPPORTED),
+    (dict(d=96), rp.RELPOS_ERR_UNSUPPORTED),       # d is 64, or 128 for T5 / ALiBi
+    (dict(d=128, mode=1, rp_=16, t1=64), rp.RELPOS_ERR_UNSUPPORTED),
+    (dict(d=128, dtype=1), rp.RELPOS_ERR_UNSUPPORTED),
+    (dict(d=128, Q=8 + 4), rp.RELPOS_ERR_INVALID_ARG),
     (dict(nb=31), rp.RELPOS_ERR_INVALID_ARG),      # odd bucket count
     (dict(nb=2), rp.RELPOS_ERR_INVALID_ARG),
     (dict(nb=256), rp.RELPOS_ERR_INVALID_ARG),

@@ -148,9 +148,10 @@ def test_invalid_arguments_raise():
     bias = torch.zeros(31, 1, device=dev)
     with pytest.raises(rp.RelposError):
         rp.attention(Q, Q, Q, bias, num_buckets=31)
-    Q128 = torch.randn(1, 1, 8, 128, device=dev).to(torch.bfloat16)
-    with pytest.raises(rp.RelposError):
-        rp.attention(Q128, Q128, Q128, torch.zeros(32, 1, device=dev))
+    Q96 = torch.randn(1, 1, 8, 96, device=dev).to(torch.bfloat16)  # d is 64 or 128
+    with pytest.raises(rp.RelposError) as e:
+        rp.attention(Q96, Q96, Q96, torch.zeros(32, 1, device=dev))
+    assert e.value.code == rp.RELPOS_ERR_UNSUPPORTED
 
 
 def test_bounded_wait_reports_timeout():

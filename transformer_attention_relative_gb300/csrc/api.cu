@@ -306,7 +306,10 @@ int attn_fwd_impl(int mode, int dtype, const void* Q, const void* K, const void*
   if (B < 0 || H < 0 || Lq < 0 || Lk < 0 || q_offset < 0 || d <= 0) return RELPOS_ERR_INVALID_ARG;
   int rc = check_rel_params(mode, num_buckets, rel_param, causal);
   if (rc != RELPOS_OK) return rc;
-  if (d != kHeadDim) return RELPOS_ERR_UNSUPPORTED;
+  // d = 64 throughout; d = 128 for T5 and ALiBi with bf16 inputs
+  if (d != kHeadDim &&
+      !(d == 2 * kHeadDim && (mode == RELPOS_T5 || mode == RELPOS_ALIBI) && dtype == RELPOS_BF16))
+    return RELPOS_ERR_UNSUPPORTED;
   if (B == 0 || H == 0 || Lq == 0) return RELPOS_OK;
   if (!Q || !out) return RELPOS_ERR_INVALID_ARG;
   if (static_cast<long long>(B) * H > 65535) return RELPOS_ERR_UNSUPPORTED;
@@ -315,8 +318,9 @@ int attn_fwd_impl(int mode, int dtype, const void* Q, const void* K, const void*
   const size_t esz = dtype == RELPOS_FP32 ? 4 : 2;
   const size_t BH = static_cast<size_t>(B) * H;
   if (Lk == 0) {  // no key is visible: zero rows
-    return cudaMemsetAsync(out, 0, BH * Lq * kHeadDim * esz, s) == cudaSuccess ? RELPOS_OK
-                                                                                 : RELPOS_ERR_CUDA;
+    return cudaMemsetAsync(out, 0, BH * Lq * static_cast<size_t>(d) * esz, s) == cudaSuccess
+               ? RELPOS_OK
+               : RELPOS_ERR_CUDA;
   }
   if (!K || !V || !table0) return RELPOS_ERR_INVALID_ARG;
   if ((mode == RELPOS_SHAW || mode == RELPOS_DEBERTA || mode == RELPOS_TXL) && !table1)
@@ -348,13 +352,13 @@ int attn_fwd_impl(int mode, int dtype, const void* Q, const void* K, const void*
   const void* Qb = Q;
   const void* Kb = K;
   const void* Vb = V;
-  const size_t nq = BH * Lq * kHeadDim, nk = BH * Lk * kHeadDim;
+  const size_t nq = BH * Lq * d, nk = BH * Lk * d;
   auto fail = [&](int code) {
     if (scratch) cudaFreeAsync(scratch, s);
     cudaGetLastError();
     return code;
   };
-  const bool decode = (mode == RELPOS_T5 && Lq <= 8 && !lengths);
+  const bool decode = (mode == RELPOS_T5 && Lq <= 8 && !lengths && d == kHeadDim);
   size_t scratch_bytes = 0, off_conv = 0, off_part = 0;
   if (dtype == RELPOS_FP32) {
     off_conv = scratch_bytes;
@@ -422,6 +426,7 @@ int attn_fwd_impl(int mode, int dtype, const void* Q, const void* K, const void*
     p.H = H;
     p.Lq = Lq;
     p.Lk = Lk;
+    p.dh = d;
     p.causal = causal;
     p.q_offset = q_offset;
     p.scale_log2 = scale * kLog2e;
@@ -512,10 +517,10 @@ int attn_fwd_impl(int mode, int dtype, const void* Q, const void* K, const void*
       if (!make_tmap(&tq, tp.Q2, Lq, static_cast<int>(BH), 2 * kHeadDim) ||
           !make_tmap(&ts, tp.Ksin, Lk, 1))
         return fail(RELPOS_ERR_CUDA);
-    } else if (!make_tmap(&tq, Qb, Lq, static_cast<int>(BH))) {
+    } else if (!make_tmap(&tq, Qb, Lq, static_cast<int>(BH), d)) {
       return fail(RELPOS_ERR_CUDA);
     }
-    if (!make_tmap(&tk, Kb, Lk, static_cast<int>(BH)) || !make_tmap(&tv, Vb, Lk, static_cast<int>(BH)))
+    if (!make_tmap(&tk, Kb, Lk, static_cast<int>(BH), d) || !make_tmap(&tv, Vb, Lk, static_cast<int>(BH), d))
       return fail(RELPOS_ERR_CUDA);
     if (mode != RELPOS_TXL) ts = tk;  // unused
     const int sms = num_sms();

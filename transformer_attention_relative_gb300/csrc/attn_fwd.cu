@@ -60,25 +60,37 @@ constexpr int kBN = 128;       // keys per tile
 constexpr int kStages = 3;     // K/V ring depth (barrier slots; Smem<MODE>::kStages are used)
 constexpr int kThreads = 384;  // 12 warps
 constexpr uint32_t kTileBytes = kBM * kHeadDim * 2;  // 16 KB: 128 rows x 128 B
+// Kernel variants are keyed by MD = mode + 8 for head dimension 128 (T5 and
+// ALiBi): MD & 7 is the mode.
+__host__ __device__ constexpr int md_mode(int md) { return md & 7; }
+__host__ __device__ constexpr int md_dim(int md) { return md >= 8 ? 128 : 64; }
 // Shared-memory layout: the item's two query tiles, the K ring, the V ring,
 // the barriers, then the mode's tables. Transformer-XL (MODE 4) scores
-// against a 128-wide contraction (content and position halves), so its query
-// tiles and K stages hold two 64-column halves of kTileBytes each.
-template <int MODE>
+// against a 128-wide contraction (content and position halves), and at head
+// dimension 128 every row is 128 wide: those query tiles and K stages (and
+// V stages at d = 128) hold two 64-column halves of kTileBytes each.
+template <int MD>
 struct Smem {
+  static constexpr int MODE = md_mode(MD);
+  static constexpr int DH = md_dim(MD);
   // K / V ring depth: Shaw keeps two stages, for the shared memory of its
-  // per-row tables (k up to 26)
-  static constexpr int kStages = MODE == 1 ? 2 : ::relpos::kStages;
-  static constexpr uint32_t kHalves = MODE == 4 ? 2u : 1u;
-  static constexpr uint32_t kQBytes = kHalves * kTileBytes;  // one query tile
-  static constexpr uint32_t kKBytes = kHalves * kTileBytes;  // one K stage
+  // per-row tables (k up to 27); so does d = 128, for its double-size tiles
+  static constexpr int kStages = (MODE == 1 || DH == 128) ? 2 : ::relpos::kStages;
+  static constexpr uint32_t kHalves = (MODE == 4 || DH == 128) ? 2u : 1u;
+  static constexpr uint32_t kQBytes = kHalves * kTileBytes;                         // one query tile
+  static constexpr uint32_t kKBytes = kHalves * kTileBytes;                         // one K stage
+  static constexpr uint32_t kVBytes = static_cast<uint32_t>(DH / 64) * kTileBytes;  // one V stage
   static constexpr uint32_t kOffQ = 0;
   static constexpr uint32_t kOffK = kOffQ + 2 * kQBytes;
   static constexpr uint32_t kOffV = kOffK + kStages * kKBytes;
-  static constexpr uint32_t kOffBar = kOffV + kStages * kTileBytes;
+  static constexpr uint32_t kOffBar = kOffV + kStages * kVBytes;
   static constexpr uint32_t kOffAux = kOffBar + 512;
 };
 constexpr uint32_t kCombBytes = 2 * 128 * 8;  // split items: (m, l) of every row, per tile
+// TMEM columns: S of query tile x at x * 128, O at 256 + x * d, P (bf16
+// pairs) at 384 + x * 64; at d = 128, P takes the first 64 columns of its
+// tile's S (read out by then), whose next S product then waits for the P.V
+// that reads it.
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemS = 0;
 constexpr uint32_t kTmemO = 256;
@@ -316,11 +328,12 @@ __host__ __device__ inline uint32_t fwd_aux_bytes(int mode, const FwdParams& p) 
 // VAR 0: pair items only; 1: with split items (p.nsplit > 0); 2: pair items
 // with the two softmax warpgroups staggered (p.stagger); 3: pair items of a
 // right-padded batch (p.lengths).
-// Loads one query tile (both halves for Transformer-XL) on barrier `bar`.
-template <int MODE, bool ELECT>
+// Loads one query tile (both halves for Transformer-XL and d = 128) on
+// barrier `bar`.
+template <int MD, bool ELECT>
 RP_DEVI void load_q_tile(uint32_t dst, const CUtensorMap* tmQ, uint32_t bar, int row0, int bh) {
 #pragma unroll
-  for (uint32_t h = 0; h < Smem<MODE>::kHalves; ++h) {
+  for (uint32_t h = 0; h < Smem<MD>::kHalves; ++h) {
     if constexpr (ELECT)
       tma_load_3d_elect(dst + h * kTileBytes, tmQ, bar, static_cast<int>(h) * kHeadDim, row0, bh);
     else
@@ -328,28 +341,45 @@ RP_DEVI void load_q_tile(uint32_t dst, const CUtensorMap* tmQ, uint32_t bar, int
   }
 }
 // Loads one K stage: the key tile and, for Transformer-XL, the keys'
-// sinusoid rows (one [Lk, 64] table for every head) as the second half.
-template <int MODE, bool ELECT>
+// sinusoid rows (one [Lk, 64] table for every head) as the second half; at
+// d = 128 the key rows' two halves.
+template <int MD, bool ELECT>
 RP_DEVI void load_k_stage(uint32_t dst, const CUtensorMap* tmK, const CUtensorMap* tmS, uint32_t bar,
                           int key0, int bh) {
+  constexpr int MODE = md_mode(MD);
   if constexpr (ELECT) {
     tma_load_3d_elect(dst, tmK, bar, 0, key0, bh);
     if constexpr (MODE == 4) tma_load_3d_elect(dst + kTileBytes, tmS, bar, 0, key0, 0);
+    if constexpr (md_dim(MD) == 128) tma_load_3d_elect(dst + kTileBytes, tmK, bar, 64, key0, bh);
   } else {
     tma_load_3d(dst, tmK, bar, 0, key0, bh);
     if constexpr (MODE == 4) tma_load_3d(dst + kTileBytes, tmS, bar, 0, key0, 0);
+    if constexpr (md_dim(MD) == 128) tma_load_3d(dst + kTileBytes, tmK, bar, 64, key0, bh);
+  }
+}
+// Loads one V stage (both 64-column halves at d = 128).
+template <int MD, bool ELECT>
+RP_DEVI void load_v_stage(uint32_t dst, const CUtensorMap* tmV, uint32_t bar, int key0, int bh) {
+#pragma unroll
+  for (int h = 0; h < md_dim(MD) / 64; ++h) {
+    if constexpr (ELECT)
+      tma_load_3d_elect(dst + h * kTileBytes, tmV, bar, 64 * h, key0, bh);
+    else
+      tma_load_3d(dst + h * kTileBytes, tmV, bar, 64 * h, key0, bh);
   }
 }
 
-template <int MODE, bool OUT_F32, int VAR>
+template <int MD, bool OUT_F32, int VAR>
 __global__ void __launch_bounds__(kThreads, 1)
     relpos_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmS,
                       const FwdParams p) {
+  constexpr int MODE = md_mode(MD);  // 0 T5, 1 Shaw, 2 DeBERTa, 3 ALiBi, 4 Transformer-XL
+  constexpr int DH = md_dim(MD);     // head dimension
   constexpr bool SPLIT = VAR == 1;
   constexpr bool STAG = VAR == 2;
   constexpr bool PAD = VAR == 3;
-  using L = Smem<MODE>;
+  using L = Smem<MD>;
   constexpr uint32_t kOffQ = L::kOffQ, kOffK = L::kOffK, kOffV = L::kOffV, kOffBar = L::kOffBar,
                      kOffAux = L::kOffAux;
   constexpr int kRing = L::kStages;
@@ -457,20 +487,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       griddep_wait();
       if (first_loads) {
         mbar_arrive_expect_tx(bar(kBarQFull), (two0 ? 2u : 1u) * L::kQBytes);
-        load_q_tile<MODE, false>(sbase + kOffQ, &tmQ, bar(kBarQFull), it0.row0[0], it0.bh);
-        if (two0) load_q_tile<MODE, false>(sbase + kOffQ + L::kQBytes, &tmQ, bar(kBarQFull), it0.row0[1], it0.bh);
+        load_q_tile<MD, false>(sbase + kOffQ, &tmQ, bar(kBarQFull), it0.row0[0], it0.bh);
+        if (two0) load_q_tile<MD, false>(sbase + kOffQ + L::kQBytes, &tmQ, bar(kBarQFull), it0.row0[1], it0.bh);
         for (int s = 0; s < nk0; ++s) {
           const int key0 = stream_key(it0, s) * kBN;
           mbar_arrive_expect_tx(bar(kBarKFull + s), L::kKBytes);
-          load_k_stage<MODE, false>(sbase + kOffK + s * L::kKBytes, &tmK, &tmS, bar(kBarKFull + s), key0, it0.bh);
-          mbar_arrive_expect_tx(bar(kBarVFull + s), kTileBytes);
-          tma_load_3d(sbase + kOffV + s * kTileBytes, &tmV, bar(kBarVFull + s), 0, key0, it0.bh);
+          load_k_stage<MD, false>(sbase + kOffK + s * L::kKBytes, &tmK, &tmS, bar(kBarKFull + s), key0, it0.bh);
+          mbar_arrive_expect_tx(bar(kBarVFull + s), L::kVBytes);
+          load_v_stage<MD, false>(sbase + kOffV + s * L::kVBytes, &tmV, bar(kBarVFull + s), key0, it0.bh);
         }
       }
       const uint32_t full0 = kq ? kBarKFull : kBarVFull;
       const uint32_t empty0 = kq ? kBarKEmpty : kBarVEmpty;
       const uint32_t ring = kq ? kOffK : kOffV;
-      const uint32_t stage_bytes = kq ? L::kKBytes : kTileBytes;
+      const uint32_t stage_bytes = kq ? L::kKBytes : L::kVBytes;
       bool ok = true;
       uint32_t it_cnt = 0;
       int item_cnt = 0;
@@ -484,8 +514,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           // a split item's single query tile goes to the Q_a buffer
           const bool two = !it.split && it.hi[1] > 0;
           mbar_arrive_expect_tx_elect(bar(kBarQFull), (two ? 2u : 1u) * L::kQBytes);
-          load_q_tile<MODE, true>(sbase + kOffQ, &tmQ, bar(kBarQFull), it.row0[0], it.bh);
-          if (two) load_q_tile<MODE, true>(sbase + kOffQ + L::kQBytes, &tmQ, bar(kBarQFull), it.row0[1], it.bh);
+          load_q_tile<MD, true>(sbase + kOffQ, &tmQ, bar(kBarQFull), it.row0[0], it.bh);
+          if (two) load_q_tile<MD, true>(sbase + kOffQ + L::kQBytes, &tmQ, bar(kBarQFull), it.row0[1], it.bh);
         }
         for (int j = 0; j < it.ns; ++j, ++it_cnt) {
           if (j < pre) continue;
@@ -496,11 +526,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           mbar_arrive_expect_tx_elect(bar(full0 + st), stage_bytes);
           if (kq)
-            load_k_stage<MODE, true>(sbase + ring + st * stage_bytes, &tmK, &tmS, bar(full0 + st),
+            load_k_stage<MD, true>(sbase + ring + st * stage_bytes, &tmK, &tmS, bar(full0 + st),
                                      stream_key(it, j) * kBN, it.bh);
           else
-            tma_load_3d_elect(sbase + ring + st * stage_bytes, &tmV, bar(full0 + st), 0,
-                              stream_key(it, j) * kBN, it.bh);
+            load_v_stage<MD, true>(sbase + ring + st * stage_bytes, &tmV, bar(full0 + st),
+                                   stream_key(it, j) * kBN, it.bh);
         }
       }
       if (!ok && lane == 0) {
@@ -533,10 +563,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dk0 = smem_desc_sw128(sbase + kOffK, 16, 1024);
       const uint64_t dv0 = smem_desc_sw128(sbase + kOffV, 8192, 1024);
       constexpr uint64_t kStageStep = kTileBytes >> 4;  // one 64-column tile
-      constexpr uint64_t kQStep = L::kQBytes >> 4, kKStep = L::kKBytes >> 4;
+      constexpr uint64_t kQStep = L::kQBytes >> 4, kKStep = L::kKBytes >> 4, kVStep = L::kVBytes >> 4;
       const uint32_t s_col = tmem + kTmemS + x * kBN;
-      const uint32_t o_col = tmem + kTmemO + x * kHeadDim;
-      const uint32_t p_col = tmem + kTmemP + x * 64;
+      const uint32_t o_col = tmem + kTmemO + x * DH;
+      const uint32_t p_col = DH == 128 ? s_col : tmem + kTmemP + x * 64;
       for (int rr = 0, w = item_at(0, p.causal); ok && w < nitems; w = item_at(++rr, p.causal), ++item_cnt) {
         const Item it = make_item<SPLIT, PAD>(p, w);
         const int mine = sel(it.hi, x) - sel(it.lo, x);
@@ -565,6 +595,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t st = r % kRing;
           if (!mbar_wait_warp(bar(kBarKFull + st), (r / kRing) & 1)) return false;
           if (sis > 0 && !mbar_wait_warp(bar(kBarSFree + x), (sis - 1) & 1)) return false;
+          // d = 128: P lives in this S's columns; the P.V that reads it first
+          if (DH == 128 && pvc > 0 && !mbar_wait_warp(bar(kBarODone + x), (pvc - 1) & 1)) return false;
           tc_fence_after();
           const uint64_t dk = dk0 + st * kKStep;
           // K-steps of 16: 4 per 64-column half (Transformer-XL: content, then position)
@@ -600,13 +632,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (mine > 0) ok = issue_s(0);
         for (int i = 0; ok && i < mine; ++i) {
           // look ahead: the next key tile's scores (after the last one, free
-          // the other tile's remaining K stages at once)
-          if (i + 1 < mine) {
-            ok = issue_s(i + 1);
-            if (!ok) break;
-          } else {
-            advance(kpos, kBarKFull, kBarKEmpty);
-            if (!ok) break;
+          // the other tile's remaining K stages at once); at d = 128 after
+          // this tile's P.V, which reads the columns the next S writes
+          if (DH == 64) {
+            if (i + 1 < mine) {
+              ok = issue_s(i + 1);
+              if (!ok) break;
+            } else {
+              advance(kpos, kBarKFull, kBarKEmpty);
+              if (!ok) break;
+            }
           }
           // this key tile's P.V
           const int pos = advance(vpos, kBarVFull, kBarVEmpty);
@@ -618,14 +653,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (ok) ok = mbar_wait_warp(bar(kBarVFull + st), (r / kRing) & 1);
           tc_fence_after();
           if (!ok) break;
-          const uint64_t dv = dv0 + st * kStageStep;
+          const uint64_t dv = dv0 + st * kVStep;
 #pragma unroll
-          for (int kk = 0; kk < kBN / 16; ++kk)
-            umma_bf16_ts_elect(o_col, p_col + kk * 8, dv + 128 * kk, kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
+          for (int hc = 0; hc < DH / 64; ++hc)  // 64 output columns per V half
+#pragma unroll
+            for (int kk = 0; kk < kBN / 16; ++kk)
+              umma_bf16_ts_elect(o_col + 64 * hc, p_col + kk * 8, dv + hc * kStageStep + 128 * kk, kIdescPV,
+                                 (i > 0 || kk > 0) ? 1u : 0u);
           tc_commit_elect(bar(kBarODone + x));
           tc_commit_elect(bar(kBarVEmpty + st));
           ++pvc;
           ++vpos;
+          if (DH == 128) {
+            if (i + 1 < mine) {
+              ok = issue_s(i + 1);
+              if (!ok) break;
+            } else {
+              advance(kpos, kBarKFull, kBarKEmpty);
+              if (!ok) break;
+            }
+          }
         }
         if constexpr (MODE == 1) {
           // Shaw: O += bins . a_V once the softmax has staged its rows' bins
@@ -678,8 +725,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t = ((warp & 3) << 5) | lane;          // row == TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_base + kTmemS + x * kBN;
-    const uint32_t tO = tmem + lane_base + kTmemO + x * kHeadDim;
-    const uint32_t tP = tmem + lane_base + kTmemP + x * 64;
+    const uint32_t tO = tmem + lane_base + kTmemO + x * DH;
+    const uint32_t tP = DH == 128 ? tS : tmem + lane_base + kTmemP + x * 64;
     const float sl2 = p.scale_log2;
     const float kNegInf = -INFINITY;
     bool err = false;
@@ -790,10 +837,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (PAD && r0 < p.Lq) {
           const int row = r0 + t;
           if (row < p.Lq) {
-            const size_t base = (static_cast<size_t>(it.bh) * p.Lq + row) * kHeadDim;
+            const size_t base = (static_cast<size_t>(it.bh) * p.Lq + row) * DH;
             uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) + base * (OUT_F32 ? 4 : 2));
 #pragma unroll
-            for (int c = 0; c < (OUT_F32 ? 16 : 8); ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+            for (int c = 0; c < (OUT_F32 ? DH / 4 : DH / 8); ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
           }
         }
         continue;
@@ -1120,17 +1167,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
         if (j > 0 && __any_sync(0xffffffffu, resc)) {
-          uint32_t o[2][32];
-          tmem_ld32(tO, o[0]);
-          tmem_ld32(tO + 32, o[1]);
-          tmem_ld_wait(o[0]);
-          tmem_ld_wait(o[1]);
 #pragma unroll
-          for (int q = 0; q < 2; ++q)
+          for (int hc = 0; hc < DH / 64; ++hc) {
+            uint32_t o[2][32];
+            tmem_ld32(tO + 64 * hc, o[0]);
+            tmem_ld32(tO + 64 * hc + 32, o[1]);
+            tmem_ld_wait(o[0]);
+            tmem_ld_wait(o[1]);
 #pragma unroll
-            for (int c = 0; c < 32; ++c) o[q][c] = __float_as_uint(__uint_as_float(o[q][c]) * alpha);
-          tmem_st32(tO, o[0]);
-          tmem_st32(tO + 32, o[1]);
+            for (int q = 0; q < 2; ++q)
+#pragma unroll
+              for (int c = 0; c < 32; ++c) o[q][c] = __float_as_uint(__uint_as_float(o[q][c]) * alpha);
+            tmem_st32(tO + 64 * hc, o[0]);
+            tmem_st32(tO + 64 * hc + 32, o[1]);
+          }
         }
         tmem_st32(tP, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
         tmem_st32(tP + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
@@ -1235,7 +1285,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       // from its own running maximum to the common one.
       const bool merge = it.split && sel(it.hi, x ^ 1) > sel(it.lo, x ^ 1);
       float sa = 1.f, sb = 0.f, l_row = l_run;
-      const int c0 = merge ? x * 32 : 0;
       if (merge) {
         // (one buffer suffices: the partner writes it again only after a P.V
         // that waits for this warpgroup's release of the accumulators below)
@@ -1253,58 +1302,67 @@ __global__ void __launch_bounds__(kThreads, 1)
         sb = other.x == kNegInf ? 0.f : ex2_approx(other.x - m);
         l_row = l_run * sa + other.y * sb;
       }
-      uint32_t orr[2][32];
-      if (merge) {
-        tmem_ld32(tO + c0, orr[0]);
-        tmem_ld32(tmem + lane_base + kTmemO + (x ^ 1) * kHeadDim + c0, orr[1]);
-      } else {
-        tmem_ld32(tO, orr[0]);
-        tmem_ld32(tO + 32, orr[1]);
-      }
-      tmem_ld_wait(orr[0]);
-      tmem_ld_wait(orr[1]);
-      tc_fence_before();
-      // the next items' P.V may overwrite the accumulators read here
-      mbar_arrive(bar(kBarOFree + x));
-      mbar_arrive(bar(kBarOFree + (merge ? (x ^ 1) : x)));
-      ++ocnt;
-      float* o = reinterpret_cast<float*>(&orr[0][0]);
-      if (merge) {
-#pragma unroll
-        for (int c = 0; c < 32; ++c) o[c] = o[c] * sa + o[32 + c] * sb;
-      }
       const int row = i0 + t;
       // rows past a padded element's length are zero rows
       const float inv_l = (l_row > 0.f && (!PAD || row < nlen)) ? 1.f / l_row : 0.f;
-      if (row < p.Lq) {
-        const size_t base = (static_cast<size_t>(it.bh) * p.Lq + row) * kHeadDim + c0;
-        const int ncol = merge ? 32 : kHeadDim;
-        // each store instruction of a warp touches 32 rows, one line each:
-        // 32-byte stores halve those line writes when the output allows them
-        if constexpr (OUT_F32) {
-          float* dst = static_cast<float*>(p.out) + base;
-          auto w = [&](int c) { return __float_as_uint(o[c] * inv_l); };
-          if (p.out_v8) {
+      // 64 columns at a time (32 of each accumulator when merging); the
+      // accumulators are released after the last TMEM load
 #pragma unroll
-            for (int c = 0; c < kHeadDim; c += 8)
-              if (c < ncol) st_global_v8(dst + c, w(c), w(c + 1), w(c + 2), w(c + 3), w(c + 4), w(c + 5), w(c + 6), w(c + 7));
-          } else {
-#pragma unroll
-            for (int c = 0; c < kHeadDim; c += 4)
-              if (c < ncol) st_global_v4(dst + c, w(c), w(c + 1), w(c + 2), w(c + 3));
-          }
+      for (int hc = 0; hc < DH / 64; ++hc) {
+        const int c0 = merge ? x * (DH / 2) + 32 * hc : 64 * hc;
+        uint32_t orr[2][32];
+        if (merge) {
+          tmem_ld32(tO + c0, orr[0]);
+          tmem_ld32(tmem + lane_base + kTmemO + (x ^ 1) * DH + c0, orr[1]);
         } else {
-          __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + base;
-          auto w = [&](int c) { return pack_bf16x2(o[c] * inv_l, o[c + 1] * inv_l); };
-          if (p.out_v8) {
+          tmem_ld32(tO + c0, orr[0]);
+          tmem_ld32(tO + c0 + 32, orr[1]);
+        }
+        tmem_ld_wait(orr[0]);
+        tmem_ld_wait(orr[1]);
+        if (hc == DH / 64 - 1) {
+          tc_fence_before();
+          // the next items' P.V may overwrite the accumulators read here
+          mbar_arrive(bar(kBarOFree + x));
+          mbar_arrive(bar(kBarOFree + (merge ? (x ^ 1) : x)));
+          ++ocnt;
+        }
+        float* o = reinterpret_cast<float*>(&orr[0][0]);
+        if (merge) {
 #pragma unroll
-            for (int c = 0; c < kHeadDim; c += 16)
-              if (c < ncol)
-                st_global_v8(dst + c, w(c), w(c + 2), w(c + 4), w(c + 6), w(c + 8), w(c + 10), w(c + 12), w(c + 14));
+          for (int c = 0; c < 32; ++c) o[c] = o[c] * sa + o[32 + c] * sb;
+        }
+        if (row < p.Lq) {
+          const size_t base = (static_cast<size_t>(it.bh) * p.Lq + row) * DH + c0;
+          const int ncol = merge ? 32 : 64;
+          // each store instruction of a warp touches 32 rows, one line each:
+          // 32-byte stores halve those line writes when the output allows them
+          if constexpr (OUT_F32) {
+            float* dst = static_cast<float*>(p.out) + base;
+            auto w = [&](int c) { return __float_as_uint(o[c] * inv_l); };
+            if (p.out_v8) {
+#pragma unroll
+              for (int c = 0; c < 64; c += 8)
+                if (c < ncol)
+                  st_global_v8(dst + c, w(c), w(c + 1), w(c + 2), w(c + 3), w(c + 4), w(c + 5), w(c + 6), w(c + 7));
+            } else {
+#pragma unroll
+              for (int c = 0; c < 64; c += 4)
+                if (c < ncol) st_global_v4(dst + c, w(c), w(c + 1), w(c + 2), w(c + 3));
+            }
           } else {
+            __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + base;
+            auto w = [&](int c) { return pack_bf16x2(o[c] * inv_l, o[c + 1] * inv_l); };
+            if (p.out_v8) {
 #pragma unroll
-            for (int c = 0; c < kHeadDim; c += 8)
-              if (c < ncol) st_global_v4(dst + c, w(c), w(c + 2), w(c + 4), w(c + 6));
+              for (int c = 0; c < 64; c += 16)
+                if (c < ncol)
+                  st_global_v8(dst + c, w(c), w(c + 2), w(c + 4), w(c + 6), w(c + 8), w(c + 10), w(c + 12), w(c + 14));
+            } else {
+#pragma unroll
+              for (int c = 0; c < 64; c += 8)
+                if (c < ncol) st_global_v4(dst + c, w(c), w(c + 2), w(c + 4), w(c + 6));
+            }
           }
         }
       }
@@ -1327,7 +1385,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 uint32_t fwd_smem_bytes(int mode, const FwdParams& p) {
-  const uint32_t aux0 = mode == 4 ? Smem<4>::kOffAux : (mode == 1 ? Smem<1>::kOffAux : Smem<0>::kOffAux);
+  uint32_t aux0 = mode == 4 ? Smem<4>::kOffAux : (mode == 1 ? Smem<1>::kOffAux : Smem<0>::kOffAux);
+  if (p.dh == 128) aux0 = Smem<8>::kOffAux;  // T5 and ALiBi share the layout
+  static_assert(Smem<8>::kOffAux == Smem<11>::kOffAux, "d = 128 layouts");
   return 1024u + aux0 + fwd_aux_bytes(mode, p) + (p.nsplit > 0 ? kCombBytes : 0u);
 }
 
@@ -1362,12 +1422,25 @@ cudaError_t launch_fwd(int mode, bool out_f32, const CUtensorMap& tmQ, const CUt
   void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, const FwdParams) =
       nullptr;
   const int var = p.lengths ? 3 : (p.nsplit > 0 ? 1 : (p.stagger ? 2 : 0));
-  // every mode has variants 0, 1 and 3; T5 also 2
+  // every mode has variants 0, 1 and 3; T5 and Transformer-XL also 2; d = 128
+  // (T5 and ALiBi, bf16 output) has its own
 #define RP_FWD_VARIANTS(M)                                                                         \
   if (var == 0) kern = out_f32 ? relpos_fwd_kernel<M, true, 0> : relpos_fwd_kernel<M, false, 0>;   \
   if (var == 1) kern = out_f32 ? relpos_fwd_kernel<M, true, 1> : relpos_fwd_kernel<M, false, 1>;   \
   if (var == 3) kern = out_f32 ? relpos_fwd_kernel<M, true, 3> : relpos_fwd_kernel<M, false, 3>;
-  if (mode == 0) {
+  if (p.dh == 128) {
+    if (out_f32 || (mode != 0 && mode != 3)) return cudaErrorNotSupported;
+    if (mode == 0) {
+      if (var == 0) kern = relpos_fwd_kernel<8, false, 0>;
+      if (var == 1) kern = relpos_fwd_kernel<8, false, 1>;
+      if (var == 2) kern = relpos_fwd_kernel<8, false, 2>;
+      if (var == 3) kern = relpos_fwd_kernel<8, false, 3>;
+    } else {
+      if (var == 0) kern = relpos_fwd_kernel<11, false, 0>;
+      if (var == 1) kern = relpos_fwd_kernel<11, false, 1>;
+      if (var == 3) kern = relpos_fwd_kernel<11, false, 3>;
+    }
+  } else if (mode == 0) {
     RP_FWD_VARIANTS(0)
     if (var == 2) kern = out_f32 ? relpos_fwd_kernel<0, true, 2> : relpos_fwd_kernel<0, false, 2>;
   } else if (mode == 1) {
@@ -1386,8 +1459,8 @@ cudaError_t launch_fwd(int mode, bool out_f32, const CUtensorMap& tmQ, const CUt
   // that every later launch fits)
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
-  const int slot = mode * 8 + (out_f32 ? 4 : 0) + var;
-  static std::atomic<uint64_t> attr_set[40];
+  const int slot = (p.dh == 128 ? 5 + (mode == 3 ? 1 : 0) : mode) * 8 + (out_f32 ? 4 : 0) + var;
+  static std::atomic<uint64_t> attr_set[56];
   const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
   if (!bit || !(attr_set[slot].load() & bit)) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,

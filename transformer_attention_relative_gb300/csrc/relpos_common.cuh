@@ -64,6 +64,7 @@ __host__ __device__ inline int deberta_delta_dev(int r, int k) {
 
 struct FwdParams {
   int B, H, Lq, Lk;
+  int dh;  // head dimension: 64, or 128 (T5 and ALiBi)
   int causal, q_offset;
   float scale_log2;  // softmax scale times log2(e)
   void* out;
@@ -84,7 +85,7 @@ struct FwdParams {
   T5Index t5;
   int npairs;         // 256-row query-tile pairs per head
   int nsplit;         // trailing pair items run as two split items each
-  const __nv_bfloat16* Qg;  // Q in global memory (bf16 [B,H,Lq,64])
+  const __nv_bfloat16* Qg;  // Q in global memory (bf16 [B,H,Lq,dh])
   // Shaw
   const __nv_bfloat16* aK;  // [2k+1, 64]
   const __nv_bfloat16* aV;  // [2k+1, 64]

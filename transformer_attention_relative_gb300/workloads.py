@@ -145,6 +145,12 @@ WORKLOADS = {
     # at positions 2048 .. 4095)
     "txl_mem": Workload("txl_mem", 8, MODE_TXL, "bf16", 4, 16, 2048, 4096, 64, causal=True,
                         q_offset=2048, table_sigma=0.1),
+    # head dimension 128 (ALiBi decoders are commonly built so): causal
+    # ALiBi and causal T5 at B=4, H=16, L=2048
+    "alibi_d128": Workload("alibi_d128", 9, MODE_ALIBI, "bf16", 4, 16, 2048, 2048, 128,
+                           causal=True),
+    "t5_d128": Workload("t5_d128", 10, MODE_T5, "bf16", 4, 16, 2048, 2048, 128,
+                        num_buckets=32, rel_param=128, causal=True, table_sigma=0.5),
 }
 
 
