@@ -248,10 +248,16 @@ int relpos_t5_decode_noalloc(const void* Q, const void* K, const void* V, const 
  *               query row with no visible key gets a zero row.
  *   Q, K, V, bias, out, B, H, Lq, Lk, num_buckets, max_distance, causal,
  *   q_offset, stream: as for relpos_attn_fwd with mode RELPOS_T5 and dtype
- *   RELPOS_BF16 (d = 64); Lq must be <= 8 (RELPOS_ERR_UNSUPPORTED otherwise).
- * Scratch: the per-chunk partials (B * H * Lq * ceil(Lk / 256) * 264 bytes)
- * come from cudaMallocAsync on `stream` and go back with cudaFreeAsync before
- * the call returns. Asynchronous on `stream`.
+ *   RELPOS_BF16 (d = 64), any Lq: up to 8 query rows run the split-key
+ *   decode kernels, more rows (a chunk of new tokens against the cache) the
+ *   fused prefill kernel, which then visits every key tile (a key's index
+ *   says nothing about its position) and takes the bias per element from
+ *   the positions on tiles that are neither wholly beyond the saturation
+ *   distance nor free of masked keys.
+ * Scratch: for Lq <= 8 the per-chunk partials (B * H * Lq * ceil(Lk / 256) *
+ * 264 bytes) come from cudaMallocAsync on `stream` and go back with
+ * cudaFreeAsync before the call returns; none otherwise. Asynchronous on
+ * `stream`.
  */
 int relpos_t5_decode_positions(const void* Q, const void* K, const void* V, const void* bias,
                                const int* key_pos, int B, int H, int Lq, int Lk, int num_buckets,

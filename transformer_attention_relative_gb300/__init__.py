@@ -215,8 +215,9 @@ def t5_decode_positions(Q, K, V, bias, key_pos, *, num_buckets: int = 32, max_di
                         causal: bool = True, q_offset: int = 0, out=None, stream=None):
     """Run ``relpos_t5_decode_positions`` on CUDA tensors; returns ``out``.
 
-    Q [B,H,Lq,64] (Lq <= 8), K, V [B,H,Lk,64] bf16; bias [num_buckets, H]
-    fp32; key_pos [B,H,Lk] int32 positions of the kept keys.
+    Q [B,H,Lq,64], K, V [B,H,Lk,64] bf16; bias [num_buckets, H] fp32;
+    key_pos [B,H,Lk] int32 positions of the kept keys. Up to 8 query rows
+    run the split-key decode kernel, more the fused prefill kernel.
     """
     import torch
     B, H, Lq, _ = Q.shape

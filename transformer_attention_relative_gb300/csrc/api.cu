@@ -294,11 +294,12 @@ namespace relpos {
 namespace {
 
 // relpos_attn_fwd and relpos_attn_fwd_padded; lengths (device int32 [B]) is
-// null for an unpadded batch.
+// null for an unpadded batch. key_pos (device int32 [B, H, Lk], T5 only) puts
+// every key at an explicit position; null for keys at their index.
 int attn_fwd_impl(int mode, int dtype, const void* Q, const void* K, const void* V,
-                  const void* table0, const void* table1, const int* lengths, int B, int H, int Lq,
-                  int Lk, int d, int num_buckets, int rel_param, int causal, int q_offset, void* out,
-                  void* stream) {
+                  const void* table0, const void* table1, const int* lengths, const int* key_pos, int B,
+                  int H, int Lq, int Lk, int d, int num_buckets, int rel_param, int causal, int q_offset,
+                  void* out, void* stream) {
   if (mode != RELPOS_T5 && mode != RELPOS_SHAW && mode != RELPOS_DEBERTA && mode != RELPOS_ALIBI &&
       mode != RELPOS_TXL)
     return RELPOS_ERR_INVALID_ARG;
@@ -306,6 +307,8 @@ int attn_fwd_impl(int mode, int dtype, const void* Q, const void* K, const void*
   if (B < 0 || H < 0 || Lq < 0 || Lk < 0 || q_offset < 0 || d <= 0) return RELPOS_ERR_INVALID_ARG;
   int rc = check_rel_params(mode, num_buckets, rel_param, causal);
   if (rc != RELPOS_OK) return rc;
+  if (key_pos && (mode != RELPOS_T5 || dtype != RELPOS_BF16 || d != kHeadDim || lengths))
+    return RELPOS_ERR_UNSUPPORTED;
   // d = 64 throughout; d = 128 for T5 and ALiBi with bf16 inputs
   if (d != kHeadDim &&
       !(d == 2 * kHeadDim && (mode == RELPOS_T5 || mode == RELPOS_ALIBI) && dtype == RELPOS_BF16))
@@ -340,8 +343,10 @@ int attn_fwd_impl(int mode, int dtype, const void* Q, const void* K, const void*
   std::memset(&t5, 0, sizeof(t5));
   int R = 0;
   if (mode == RELPOS_T5) {
-    const long long nmax = std::max(static_cast<long long>(Lk) - 1,
-                                    static_cast<long long>(Lq) - 1 + q_offset);
+    // explicit positions: thresholds for every offset a position in [0, 2^28] can produce
+    const long long nmax = key_pos ? (1ll << 28) + Lq + static_cast<long long>(q_offset)
+                                   : std::max(static_cast<long long>(Lk) - 1,
+                                              static_cast<long long>(Lq) - 1 + q_offset);
     rc = t5_setup(num_buckets, rel_param, causal, nmax, &t5, &R);
     if (rc != RELPOS_OK) return rc;
   }
@@ -358,7 +363,7 @@ int attn_fwd_impl(int mode, int dtype, const void* Q, const void* K, const void*
     cudaGetLastError();
     return code;
   };
-  const bool decode = (mode == RELPOS_T5 && Lq <= 8 && !lengths && d == kHeadDim);
+  const bool decode = (mode == RELPOS_T5 && Lq <= 8 && !lengths && !key_pos && d == kHeadDim);
   size_t scratch_bytes = 0, off_conv = 0, off_part = 0;
   if (dtype == RELPOS_FP32) {
     off_conv = scratch_bytes;
@@ -439,8 +444,11 @@ int attn_fwd_impl(int mode, int dtype, const void* Q, const void* K, const void*
     p.Qg = static_cast<const __nv_bfloat16*>(Qb);
     p.npairs = (Lq + 255) / 256;
     p.lengths = lengths;
+    p.key_pos = key_pos;
+    if (key_pos) p.stagger = 0;
     // split items balance a last pass of equally long items: not with padding
-    p.nsplit = lengths ? 0 : fwd_split_items(B * H * p.npairs, B * H, Lq, causal, num_sms());
+    // or explicit positions
+    p.nsplit = (lengths || key_pos) ? 0 : fwd_split_items(B * H * p.npairs, B * H, Lq, causal, num_sms());
     if (mode == RELPOS_T5) {
       p.bias = static_cast<const float*>(table0);
       p.t5 = t5;
@@ -542,8 +550,8 @@ extern "C" int relpos_attn_fwd(int mode, int dtype, const void* Q, const void* K
                                const void* table0, const void* table1, int B, int H, int Lq, int Lk,
                                int d, int num_buckets, int rel_param, int causal, int q_offset,
                                void* out, void* stream) {
-  return attn_fwd_impl(mode, dtype, Q, K, V, table0, table1, nullptr, B, H, Lq, Lk, d, num_buckets,
-                       rel_param, causal, q_offset, out, stream);
+  return attn_fwd_impl(mode, dtype, Q, K, V, table0, table1, nullptr, nullptr, B, H, Lq, Lk, d,
+                       num_buckets, rel_param, causal, q_offset, out, stream);
 }
 
 extern "C" int relpos_attn_fwd_padded(int mode, int dtype, const void* Q, const void* K,
@@ -552,9 +560,18 @@ extern "C" int relpos_attn_fwd_padded(int mode, int dtype, const void* Q, const 
                                       int num_buckets, int rel_param, int causal, int q_offset,
                                       void* out, void* stream) {
   if (!lengths || (reinterpret_cast<uintptr_t>(lengths) & 3u)) return RELPOS_ERR_INVALID_ARG;
-  return attn_fwd_impl(mode, dtype, Q, K, V, table0, table1, lengths, B, H, Lq, Lk, d, num_buckets,
-                       rel_param, causal, q_offset, out, stream);
+  return attn_fwd_impl(mode, dtype, Q, K, V, table0, table1, lengths, nullptr, B, H, Lq, Lk, d,
+                       num_buckets, rel_param, causal, q_offset, out, stream);
 }
+
+namespace relpos {
+int attn_fwd_t5_positions(const void* Q, const void* K, const void* V, const void* bias, const int* key_pos,
+                          int B, int H, int Lq, int Lk, int num_buckets, int max_distance, int causal,
+                          int q_offset, void* out, void* stream) {
+  return attn_fwd_impl(RELPOS_T5, RELPOS_BF16, Q, K, V, bias, nullptr, nullptr, key_pos, B, H, Lq, Lk,
+                       kHeadDim, num_buckets, max_distance, causal, q_offset, out, stream);
+}
+}  // namespace relpos
 
 namespace relpos {
 namespace {

@@ -176,20 +176,21 @@ RP_DEVI int seq_len(const FwdParams& p, int bh) {
 
 // Key tiles [0, n) one 128-row query tile starting at row r0 visits, for a
 // sequence of nlen valid rows and keys (a padded batch element; rows from
-// nlen on give zero rows).
-template <bool PAD>
+// nlen on give zero rows). With explicit key positions (POS) a key's index
+// says nothing about its position: every tile is visited.
+template <bool PAD, bool POS = false>
 RP_DEVI int tile_keys(const FwdParams& p, int r0, int nlen) {
   const int lq = PAD ? min(p.Lq, nlen) : p.Lq;
   const int lk = PAD ? min(p.Lk, nlen) : p.Lk;
   if (r0 >= lq || (PAD && lk <= 0)) return 0;
   int last_key = lk - 1;
-  if (p.causal) last_key = min(last_key, min(r0 + kBM - 1, lq - 1) + p.q_offset);
+  if (p.causal && !POS) last_key = min(last_key, min(r0 + kBM - 1, lq - 1) + p.q_offset);
   return last_key / kBN + 1;
 }
 
 // SPLIT: the launch has split items (p.nsplit > 0); without, the split paths
 // compile away. PAD: a right-padded batch (p.lengths).
-template <bool SPLIT, bool PAD>
+template <bool SPLIT, bool PAD, bool POS = false>
 RP_DEVI Item make_item(const FwdParams& p, int w) {
   Item it;
   const int BH = p.B * p.H;
@@ -210,13 +211,13 @@ RP_DEVI Item make_item(const FwdParams& p, int w) {
     for (int x = 0; x < 2; ++x) {
       it.row0[x] = i0 + x * kBM;
       it.lo[x] = 0;
-      it.hi[x] = tile_keys<PAD>(p, it.row0[x], nlen);
+      it.hi[x] = tile_keys<PAD, POS>(p, it.row0[x], nlen);
     }
     it.ns = max(it.hi[0], it.hi[1]);
   } else {
     it.split = true;
     const int r0 = i0 + xs * kBM;
-    const int n = tile_keys<PAD>(p, r0, nlen);
+    const int n = tile_keys<PAD, POS>(p, r0, nlen);
     const int na = (n + 1) >> 1;
     it.row0[0] = it.row0[1] = r0;
     it.lo[0] = 0;
@@ -253,10 +254,10 @@ RP_DEVI int item_at(int r, bool snake) {
 
 // Head of the first item from pass r on in which query tile x has key tiles,
 // or -1.
-template <bool SPLIT, bool PAD>
+template <bool SPLIT, bool PAD, bool POS = false>
 RP_DEVI int next_head(const FwdParams& p, int x, int r, int nitems) {
   for (int w = item_at(r, p.causal); w < nitems; w = item_at(++r, p.causal)) {
-    const Item it = make_item<SPLIT, PAD>(p, w);
+    const Item it = make_item<SPLIT, PAD, POS>(p, w);
     if (sel(it.hi, x) > sel(it.lo, x)) return it.h;
   }
   return -1;
@@ -319,6 +320,8 @@ __host__ __device__ inline uint32_t fwd_aux_bytes(int mode, const FwdParams& p) 
     const uint32_t stride = (static_cast<uint32_t>(p.t5_tab_len4) + 28u + 31u) & ~31u;
     const uint32_t ncopy = p.t5_compact ? 1u : 4u;
     aux = bkt_bytes + 2u * 2u * ncopy * stride * 4u + 2u * 128u * 4u;
+    aux = (aux + 15u) & ~15u;
+    if (p.key_pos) aux += 8u * 128u * 4u;  // each softmax warp's key positions of a tile
   } else if (mode == 1) {
     aux = shaw_aux(p.row_stride).end;
   }
@@ -327,7 +330,8 @@ __host__ __device__ inline uint32_t fwd_aux_bytes(int mode, const FwdParams& p) 
 
 // VAR 0: pair items only; 1: with split items (p.nsplit > 0); 2: pair items
 // with the two softmax warpgroups staggered (p.stagger); 3: pair items of a
-// right-padded batch (p.lengths).
+// right-padded batch (p.lengths); 4: T5 pair items over keys at explicit
+// positions (p.key_pos).
 // Loads one query tile (both halves for Transformer-XL and d = 128) on
 // barrier `bar`.
 template <int MD, bool ELECT>
@@ -379,6 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr bool SPLIT = VAR == 1;
   constexpr bool STAG = VAR == 2;
   constexpr bool PAD = VAR == 3;
+  constexpr bool POS = VAR == 4;  // T5 with explicit key positions (p.key_pos)
   using L = Smem<MD>;
   constexpr uint32_t kOffQ = L::kOffQ, kOffK = L::kOffK, kOffV = L::kOffV, kOffBar = L::kOffBar,
                      kOffAux = L::kOffAux;
@@ -446,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   bool two0 = false;
   int nk0 = 0;
   if (first_loads) {
-    it0 = make_item<SPLIT, PAD>(p, item_at(0, p.causal));
+    it0 = make_item<SPLIT, PAD, POS>(p, item_at(0, p.causal));
     two0 = !it0.split && it0.hi[1] > 0;
     nk0 = it0.ns < kRing ? it0.ns : kRing;
     tma_prefetch_desc(&tmQ);
@@ -505,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t it_cnt = 0;
       int item_cnt = 0;
       for (int rr = 0, w = item_at(0, p.causal); ok && w < nitems; w = item_at(++rr, p.causal), ++item_cnt) {
-        const Item it = make_item<SPLIT, PAD>(p, w);
+        const Item it = make_item<SPLIT, PAD, POS>(p, w);
         // the first item's Q and first ring stages were loaded in the setup
         const int pre = item_cnt == 0 ? min(it.ns, kRing) : 0;
         if (kq && item_cnt > 0) {
@@ -568,7 +573,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t o_col = tmem + kTmemO + x * DH;
       const uint32_t p_col = DH == 128 ? s_col : tmem + kTmemP + x * 64;
       for (int rr = 0, w = item_at(0, p.causal); ok && w < nitems; w = item_at(++rr, p.causal), ++item_cnt) {
-        const Item it = make_item<SPLIT, PAD>(p, w);
+        const Item it = make_item<SPLIT, PAD, POS>(p, w);
         const int mine = sel(it.hi, x) - sel(it.lo, x);
         const uint64_t dq = dq_a + ((it.split ? 0u : x) * kQStep);
         ok = mbar_wait_warp(bar(kBarQFull), item_cnt & 1);
@@ -800,7 +805,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       return true;
     };
     if constexpr (MODE == 0) {
-      const int h0 = next_head<SPLIT, PAD>(p, x, 0, nitems);
+      const int h0 = next_head<SPLIT, PAD, POS>(p, x, 0, nitems);
       griddep_wait();
       if (h0 >= 0) {
         if (t < p.t5_nb) hb_next = __ldg(p.bias + t * p.H + h0);
@@ -824,7 +829,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t stag = 0;
     float2* ml = reinterpret_cast<float2*>(aux + fwd_aux_bytes(MODE, p));
     for (int rr = 0, w = item_at(0, p.causal); !err && w < nitems; w = item_at(++rr, p.causal)) {
-      const Item it = make_item<SPLIT, PAD>(p, w);
+      const Item it = make_item<SPLIT, PAD, POS>(p, w);
       const int lo_x = sel(it.lo, x);
       const int n_kv = sel(it.hi, x) - lo_x;
       const uint32_t stag_it = stag;
@@ -859,7 +864,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // this item's table was filled at the end of the previous item (or in
         // the prologue); fetch the next item's bias row meanwhile
         buf = ocnt & 1;
-        next_h = next_head<SPLIT, PAD>(p, x, rr + 1, nitems);
+        next_h = next_head<SPLIT, PAD, POS>(p, x, rr + 1, nitems);
         if (t < p.t5_nb && next_h >= 0) hb_next = __ldg(p.bias + t * p.H + next_h);
         const bool ok = mbar_wait(bar(kBarTab + x), 1);
         err = __any_sync(0xffffffffu, !ok);
@@ -925,6 +930,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (int j = 0; j < n_kv; ++j, ++cnt) {
         const int j0 = (lo_x + j) * kBN;
+        // explicit key positions: this lane's four keys of the tile (columns
+        // lane + 32 q), loaded while S is computed; keys past the end take a
+        // position after every query (masked below)
+        int kp[4] = {0, 0, 0, 0};
+        if constexpr (POS) {
+          const int* kpos = p.key_pos + static_cast<size_t>(it.bh) * p.Lk;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int jj = j0 + 32 * q + lane;
+            kp[q] = jj < p.Lk ? __ldg(kpos + jj) : 0x7fffffff;
+          }
+        }
         bool ok = mbar_wait(bar(kBarSFull + x), cnt & 1);
         err = __any_sync(0xffffffffu, !ok);
         if (err) break;
@@ -945,8 +962,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the warps of a tile next to the diagonal whose rows do not reach
         // the near band take the far path.
         const int p_lo_w = p_lo + 32 * (warp & 3);    // position of this warp's first row
-        const int rel_hi = j0 + kBN - 1 - p_lo_w;    // largest key - query offset in the warp's rows
-        const int rel_lo = j0 - (p_lo_w + 31);       // smallest
+        int rel_hi = j0 + kBN - 1 - p_lo_w;    // largest key - query offset in the warp's rows
+        int rel_lo = j0 - (p_lo_w + 31);       // smallest
+        int* wpos = nullptr;  // POS: this warp's copy of the tile's key positions
+        if constexpr (POS) {
+          wpos = reinterpret_cast<int*>(aux + fwd_aux_bytes(MODE, p) - 8u * 128u * 4u) + (warp - 4) * 128;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) wpos[32 * q + lane] = kp[q];
+          __syncwarp();
+          const int mn = __reduce_min_sync(0xffffffffu, min(min(kp[0], kp[1]), min(kp[2], kp[3])));
+          const int mx = __reduce_max_sync(0xffffffffu, max(max(kp[0], kp[1]), max(kp[2], kp[3])));
+          rel_hi = mx == 0x7fffffff ? 0x3fffffff : mx - p_lo_w;
+          rel_lo = mn - (p_lo_w + 31);
+        }
         bool far_l, far_r;
         if constexpr (MODE == 0) {
           far_l = rel_hi <= -p.t5_R;
@@ -957,7 +985,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           far_l = rel_hi <= -kc;
           far_r = rel_lo >= kc;
         }
-        const bool need_mask = (p.causal && j0 + kBN - 1 > p_lo_w) || (j0 + kBN > lk_eff);
+        const bool need_mask = POS ? ((p.causal && rel_hi > 0) || (j0 + kBN > lk_eff))
+                                   : ((p.causal && j0 + kBN - 1 > p_lo_w) || (j0 + kBN > lk_eff));
         int lim = 127;
         if (need_mask) {
           lim = lk_eff - 1 - j0;
@@ -971,12 +1000,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // 2^(xs * xscale + xoff - m).
         // DeBERTa tiles beyond the band still carry a per-key term, so every
         // DeBERTa tile takes the per-element path.
-        const bool far = MODE == 3 || MODE == 4 || (MODE != 2 && (far_l || far_r));
+        // (explicit positions: a masked tile takes the per-element path)
+        const bool far = MODE == 3 || MODE == 4 || (MODE != 2 && (far_l || far_r) && !(POS && need_mask));
         // a row constant added with the maximum: the far constant of a far
         // tile, for DeBERTa tiles beyond the band the saturated c2p term
         // (their per-key p2c term goes into the scaled scores), for ALiBi
         // tiles on one side of the diagonal the distance term of column 0
-        float addc = (far_l || far_r) ? (far_l ? add_l : add_r) : 0.f;
+        float addc = far && (far_l || far_r) ? (far_l ? add_l : add_r) : 0.f;
         if constexpr (MODE == 3) {
           // bias = -slope |r0 + c| with r0 = j0 - p the offset of column 0:
           // keys all ahead, -slope r0 - slope c; all behind, slope r0 + slope c;
@@ -1007,7 +1037,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (!far) {
-          if (MODE == 0 && p.t5_compact) {
+          if constexpr (POS) {
+            // bias and mask per element from the keys' positions (offset key
+            // position - query position; beyond the table's ends the buckets
+            // are the saturated ones the ends hold)
+            const float* tb = tab.copy(buf, 0);
+            const int4* wp4 = reinterpret_cast<const int4*>(wpos);
+#pragma unroll
+            for (int q = 0; q < 32; ++q) {
+              const int4 k4 = wp4[q];
+              const int kk[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int c = 4 * q + e;
+                const int rel = kk[e] == 0x7fffffff ? 0x3fffffff : kk[e] - prow;
+                const float b = tb[min(max(rel + p.t5_tab_off, 0), p.t5_tab_len - 1)];
+                const bool masked = (p.causal && rel > 0) || (j0 + c >= lk_eff);
+                xs[c] = masked ? kNegInf : fmaf(xs[c], sl2, b);
+              }
+            }
+          } else if (MODE == 0 && p.t5_compact) {
             const float* tb = tab.copy(buf, 0) + (j0 - prow + p.t5_tab_off);
 #pragma unroll
             for (int c = 0; c < 128; ++c) xs[c] = fmaf(xs[c], sl2, tb[c]);
@@ -1104,7 +1153,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        if (need_mask) {
+        if (need_mask && !POS) {
 #pragma unroll
           for (int c = 0; c < 128; ++c) xs[c] = (c > lim) ? kNegInf : xs[c];
         }
@@ -1421,7 +1470,7 @@ cudaError_t launch_fwd(int mode, bool out_f32, const CUtensorMap& tmQ, const CUt
   dim3 block(kThreads);
   void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, const FwdParams) =
       nullptr;
-  const int var = p.lengths ? 3 : (p.nsplit > 0 ? 1 : (p.stagger ? 2 : 0));
+  const int var = p.key_pos ? 4 : (p.lengths ? 3 : (p.nsplit > 0 ? 1 : (p.stagger ? 2 : 0)));
   // every mode has variants 0, 1 and 3; T5 and Transformer-XL also 2; d = 128
   // (T5 and ALiBi, bf16 output) has its own
 #define RP_FWD_VARIANTS(M)                                                                         \
@@ -1443,6 +1492,7 @@ cudaError_t launch_fwd(int mode, bool out_f32, const CUtensorMap& tmQ, const CUt
   } else if (mode == 0) {
     RP_FWD_VARIANTS(0)
     if (var == 2) kern = out_f32 ? relpos_fwd_kernel<0, true, 2> : relpos_fwd_kernel<0, false, 2>;
+    if (var == 4 && !out_f32) kern = relpos_fwd_kernel<0, false, 4>;
   } else if (mode == 1) {
     RP_FWD_VARIANTS(1)
   } else if (mode == 2) {
@@ -1459,8 +1509,8 @@ cudaError_t launch_fwd(int mode, bool out_f32, const CUtensorMap& tmQ, const CUt
   // that every later launch fits)
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
-  const int slot = (p.dh == 128 ? 5 + (mode == 3 ? 1 : 0) : mode) * 8 + (out_f32 ? 4 : 0) + var;
-  static std::atomic<uint64_t> attr_set[56];
+  const int slot = (p.dh == 128 ? 5 + (mode == 3 ? 1 : 0) : mode) * 16 + (out_f32 ? 8 : 0) + var;
+  static std::atomic<uint64_t> attr_set[7 * 16];
   const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
   if (!bit || !(attr_set[slot].load() & bit)) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,

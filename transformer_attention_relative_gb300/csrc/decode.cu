@@ -305,7 +305,7 @@ int decode_entry_check(const void* Q, const void* K, const void* V, const void* 
   int rc = check_rel_params(RELPOS_T5, num_buckets, max_distance, causal);
   if (rc != RELPOS_OK) return rc;
   if (B < 0 || H < 0 || Lq < 0 || Lk < 0 || q_offset < 0) return RELPOS_ERR_INVALID_ARG;
-  if (Lq > 8) return RELPOS_ERR_UNSUPPORTED;  // decode shapes only
+  if (Lq > 8 && !need_key_pos) return RELPOS_ERR_UNSUPPORTED;  // decode shapes only
   if (B == 0 || H == 0 || Lq == 0) {
     *noop = true;
     return RELPOS_OK;
@@ -412,6 +412,11 @@ extern "C" int relpos_t5_decode_positions(const void* Q, const void* K, const vo
   int rc = decode_entry_check(Q, K, V, bias, key_pos, true, out, B, H, Lq, Lk, num_buckets,
                               max_distance, causal, q_offset, &noop);
   if (rc != RELPOS_OK || noop) return rc;
+  // more than a few query rows (a chunk of new tokens against the cache): the
+  // fused prefill kernel
+  if (Lq > 8 && Lk > 0)
+    return attn_fwd_t5_positions(Q, K, V, bias, key_pos, B, H, Lq, Lk, num_buckets, max_distance, causal,
+                                 q_offset, out, stream);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t rows = static_cast<size_t>(B) * H * Lq;
   if (Lk == 0)

@@ -72,6 +72,7 @@ struct FwdParams {
   int stagger;  // offset the two softmax warpgroups by about half a tile
   int* status;
   const int* lengths;  // [B] valid rows and keys per batch element (right-padded batch), or null
+  const int* key_pos;  // T5: [B*H, Lk] position of every key (explicit positions), or null
   // ALiBi
   const float* slopes;  // [H]
   // T5

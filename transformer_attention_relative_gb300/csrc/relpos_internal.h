@@ -31,6 +31,12 @@ cudaError_t launch_deberta_band(const CUtensorMap& tmQ, const CUtensorMap& tmK, 
                                 const CUtensorMap& tmPq, const BandParams& bp, cudaStream_t stream);
 
 cudaError_t launch_txl_prep(const TxlParams& p, cudaStream_t stream);
+// T5 forward over keys at explicit positions through the fused kernel (any
+// number of query rows; the C ABI's positions entry point takes it beyond the
+// decode kernel's rows)
+int attn_fwd_t5_positions(const void* Q, const void* K, const void* V, const void* bias, const int* key_pos,
+                          int B, int H, int Lq, int Lk, int num_buckets, int max_distance, int causal,
+                          int q_offset, void* out, void* stream);
 
 int decode_chunk_keys();
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);
