@@ -479,8 +479,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < 4) {
     // register split (4 x 32 x dec + 8 x 32 x inc <= 384 x 168): T5 needs
-    // fewer in the softmax and gives its issuers room
-    if constexpr (MODE == 0) {
+    // fewer in the softmax and gives its issuers room (not with explicit key
+    // positions, whose per-element path needs the softmax's share)
+    if constexpr (MODE == 0 && !POS) {
       setmaxnreg_dec<88>();
     } else {
       setmaxnreg_dec<72>();
@@ -720,7 +721,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait_warp(bar(kBarFinal), 0, 100000000ull);
     }
   } else {
-    if constexpr (MODE == 0) {
+    if constexpr (MODE == 0 && !POS) {
       setmaxnreg_inc<200>();
     } else {
       setmaxnreg_inc<216>();
@@ -930,17 +931,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (int j = 0; j < n_kv; ++j, ++cnt) {
         const int j0 = (lo_x + j) * kBN;
-        // explicit key positions: this lane's four keys of the tile (columns
-        // lane + 32 q), loaded while S is computed; keys past the end take a
-        // position after every query (masked below)
-        int kp[4] = {0, 0, 0, 0};
+        // explicit key positions: the tile's 128 into this warp's copy in
+        // shared memory (lane l loads columns l + 32 q) and their range, while
+        // S is computed; keys past the end take a position after every query
+        // (masked below)
+        int* wpos = nullptr;
+        int kmin = 0, kmax = 0;
         if constexpr (POS) {
           const int* kpos = p.key_pos + static_cast<size_t>(it.bh) * p.Lk;
+          int kp[4];
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const int jj = j0 + 32 * q + lane;
             kp[q] = jj < p.Lk ? __ldg(kpos + jj) : 0x7fffffff;
           }
+          wpos = reinterpret_cast<int*>(aux + fwd_aux_bytes(MODE, p) - 8u * 128u * 4u) + (warp - 4) * 128;
+          __syncwarp();  // the previous tile's reads are done
+#pragma unroll
+          for (int q = 0; q < 4; ++q) wpos[32 * q + lane] = kp[q];
+          kmin = __reduce_min_sync(0xffffffffu, min(min(kp[0], kp[1]), min(kp[2], kp[3])));
+          kmax = __reduce_max_sync(0xffffffffu, max(max(kp[0], kp[1]), max(kp[2], kp[3])));
+          __syncwarp();
         }
         bool ok = mbar_wait(bar(kBarSFull + x), cnt & 1);
         err = __any_sync(0xffffffffu, !ok);
@@ -964,16 +975,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int p_lo_w = p_lo + 32 * (warp & 3);    // position of this warp's first row
         int rel_hi = j0 + kBN - 1 - p_lo_w;    // largest key - query offset in the warp's rows
         int rel_lo = j0 - (p_lo_w + 31);       // smallest
-        int* wpos = nullptr;  // POS: this warp's copy of the tile's key positions
         if constexpr (POS) {
-          wpos = reinterpret_cast<int*>(aux + fwd_aux_bytes(MODE, p) - 8u * 128u * 4u) + (warp - 4) * 128;
-#pragma unroll
-          for (int q = 0; q < 4; ++q) wpos[32 * q + lane] = kp[q];
-          __syncwarp();
-          const int mn = __reduce_min_sync(0xffffffffu, min(min(kp[0], kp[1]), min(kp[2], kp[3])));
-          const int mx = __reduce_max_sync(0xffffffffu, max(max(kp[0], kp[1]), max(kp[2], kp[3])));
-          rel_hi = mx == 0x7fffffff ? 0x3fffffff : mx - p_lo_w;
-          rel_lo = mn - (p_lo_w + 31);
+          rel_hi = kmax == 0x7fffffff ? 0x3fffffff : kmax - p_lo_w;
+          rel_lo = kmin - (p_lo_w + 31);
         }
         bool far_l, far_r;
         if constexpr (MODE == 0) {
@@ -1000,13 +1004,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         // 2^(xs * xscale + xoff - m).
         // DeBERTa tiles beyond the band still carry a per-key term, so every
         // DeBERTa tile takes the per-element path.
-        // (explicit positions: a masked tile takes the per-element path)
-        const bool far = MODE == 3 || MODE == 4 || (MODE != 2 && (far_l || far_r) && !(POS && need_mask));
+        // (explicit positions: a masked tile takes the per-element path,
+        // unless every key is masked for every row of the warp: that tile
+        // takes the far path with the constant -inf, all its probabilities 0)
+        const bool dead = POS && ((p.causal && rel_lo > 0) || kmin == 0x7fffffff);
+        const bool far =
+            MODE == 3 || MODE == 4 || dead || (MODE != 2 && (far_l || far_r) && !(POS && need_mask));
         // a row constant added with the maximum: the far constant of a far
         // tile, for DeBERTa tiles beyond the band the saturated c2p term
         // (their per-key p2c term goes into the scaled scores), for ALiBi
         // tiles on one side of the diagonal the distance term of column 0
         float addc = far && (far_l || far_r) ? (far_l ? add_l : add_r) : 0.f;
+        if (dead) addc = kNegInf;
         if constexpr (MODE == 3) {
           // bias = -slope |r0 + c| with r0 = j0 - p the offset of column 0:
           // keys all ahead, -slope r0 - slope c; all behind, slope r0 + slope c;
