@@ -79,7 +79,8 @@ struct Smem {
   static constexpr uint32_t kHalves = (MODE == 4 || DH == 128) ? 2u : 1u;
   static constexpr uint32_t kQBytes = kHalves * kTileBytes;                         // one query tile
   static constexpr uint32_t kKBytes = kHalves * kTileBytes;                         // one K stage
-  static constexpr uint32_t kVBytes = static_cast<uint32_t>(DH / 64) * kTileBytes;  // one V stage
+  // one V stage; DeBERTa appends its keys' two saturated p2c values (2 x 128 fp32)
+  static constexpr uint32_t kVBytes = static_cast<uint32_t>(DH / 64) * kTileBytes + (MODE == 2 ? 1024u : 0u);
   static constexpr uint32_t kOffQ = 0;
   static constexpr uint32_t kOffK = kOffQ + 2 * kQBytes;
   static constexpr uint32_t kOffV = kOffK + kStages * kKBytes;
@@ -361,15 +362,43 @@ RP_DEVI void load_k_stage(uint32_t dst, const CUtensorMap* tmK, const CUtensorMa
     if constexpr (md_dim(MD) == 128) tma_load_3d(dst + kTileBytes, tmK, bar, 64, key0, bh);
   }
 }
-// Loads one V stage (both 64-column halves at d = 128).
+// Bulk copy of `bytes` contiguous global bytes into shared memory on barrier
+// `bar` (both addresses 16-byte aligned, bytes a multiple of 16); the _elect
+// form is issued by one elected lane of a converged warp.
+RP_DEVI void bulk_load_1d(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+RP_DEVI void bulk_load_1d_elect(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n\t}" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+// Loads one V stage (both 64-column halves at d = 128; DeBERTa also the
+// keys' saturated p2c values, far behind then far ahead, 512 bytes each).
 template <int MD, bool ELECT>
-RP_DEVI void load_v_stage(uint32_t dst, const CUtensorMap* tmV, uint32_t bar, int key0, int bh) {
+RP_DEVI void load_v_stage(uint32_t dst, const CUtensorMap* tmV, uint32_t bar, int key0, int bh,
+                          const FwdParams& p) {
 #pragma unroll
   for (int h = 0; h < md_dim(MD) / 64; ++h) {
     if constexpr (ELECT)
       tma_load_3d_elect(dst + h * kTileBytes, tmV, bar, 64 * h, key0, bh);
     else
       tma_load_3d(dst + h * kTileBytes, tmV, bar, 64 * h, key0, bh);
+  }
+  if constexpr (md_mode(MD) == 2) {
+    const float* e = p.p2c_ends + static_cast<size_t>(bh) * 2 * p.ends_pitch + key0;
+    if constexpr (ELECT) {
+      bulk_load_1d_elect(dst + kTileBytes, e, 512u, bar);
+      bulk_load_1d_elect(dst + kTileBytes + 512u, e + p.ends_pitch, 512u, bar);
+    } else {
+      bulk_load_1d(dst + kTileBytes, e, 512u, bar);
+      bulk_load_1d(dst + kTileBytes + 512u, e + p.ends_pitch, 512u, bar);
+    }
   }
 }
 
@@ -500,7 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(bar(kBarKFull + s), L::kKBytes);
           load_k_stage<MD, false>(sbase + kOffK + s * L::kKBytes, &tmK, &tmS, bar(kBarKFull + s), key0, it0.bh);
           mbar_arrive_expect_tx(bar(kBarVFull + s), L::kVBytes);
-          load_v_stage<MD, false>(sbase + kOffV + s * L::kVBytes, &tmV, bar(kBarVFull + s), key0, it0.bh);
+          load_v_stage<MD, false>(sbase + kOffV + s * L::kVBytes, &tmV, bar(kBarVFull + s), key0, it0.bh, p);
         }
       }
       const uint32_t full0 = kq ? kBarKFull : kBarVFull;
@@ -536,7 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      stream_key(it, j) * kBN, it.bh);
           else
             load_v_stage<MD, true>(sbase + ring + st * stage_bytes, &tmV, bar(full0 + st),
-                                   stream_key(it, j) * kBN, it.bh);
+                                   stream_key(it, j) * kBN, it.bh, p);
         }
       }
       if (!ok && lane == 0) {
@@ -828,9 +857,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // (b has started the last tile of item n - 2 before a's item n has its
     // Q tiles), so two barriers keep the parities apart.
     uint32_t stag = 0;
+    uint32_t kv_next = 0;  // DeBERTa: ring position of the next item's first key tile
     float2* ml = reinterpret_cast<float2*>(aux + fwd_aux_bytes(MODE, p));
     for (int rr = 0, w = item_at(0, p.causal); !err && w < nitems; w = item_at(++rr, p.causal)) {
       const Item it = make_item<SPLIT, PAD, POS>(p, w);
+      const uint32_t kv_it = kv_next;
+      kv_next += static_cast<uint32_t>(it.ns);
       const int lo_x = sel(it.lo, x);
       const int n_kv = sel(it.hi, x) - lo_x;
       const uint32_t stag_it = stag;
@@ -1014,7 +1046,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // tile, for DeBERTa tiles beyond the band the saturated c2p term
         // (their per-key p2c term goes into the scaled scores), for ALiBi
         // tiles on one side of the diagonal the distance term of column 0
-        float addc = far && (far_l || far_r) ? (far_l ? add_l : add_r) : 0.f;
+        // (a positions tile that takes the per-element path forms its whole
+        // logit there)
+        float addc = (far_l || far_r) && (far || !POS) ? (far_l ? add_l : add_r) : 0.f;
         if (dead) addc = kNegInf;
         if constexpr (MODE == 3) {
           // bias = -slope |r0 + c| with r0 = j0 - p the offset of column 0:
@@ -1094,15 +1128,23 @@ __global__ void __launch_bounds__(kThreads, 1)
               xs[c] = fmaf(xs[c], sl2, qa[r]);
             }
           } else if constexpr (MODE == 2) {
+            // the keys' saturated p2c values came with the tile's V stage
+            // (ring position kv_it + its stream position; the stage is
+            // released only after this tile's P.V, which waits for P)
+            const uint32_t rpos = kv_it + static_cast<uint32_t>(it.split ? 2 * j + x : j);
+            const uint32_t vst = rpos % kRing;
+            const bool okv = mbar_wait(bar(kBarVFull + vst), (rpos / kRing) & 1);
+            err = __any_sync(0xffffffffu, !okv);
+            if (err) break;
+            const float* ends_s = reinterpret_cast<const float*>(smem + kOffV + vst * L::kVBytes + kTileBytes);
             if (far_l || far_r) {
               // p2c: the saturated end column of every key; the c2p row
               // constant is addc
-              const float4* ce = reinterpret_cast<const float4*>(
-                  p.p2c_ends + (static_cast<size_t>(it.bh) * 2 + (far_l ? 0 : 1)) * p.ends_pitch + j0);
+              const float4* ce = reinterpret_cast<const float4*>(ends_s + (far_l ? 0 : 128));
               const float2 sc2 = make_float2(sl2, sl2);
 #pragma unroll
               for (int q = 0; q < 32; ++q) {
-                const float4 e = __ldg(ce + q);
+                const float4 e = ce[q];
                 float2 a = __ffma2_rn(make_float2(xs[4 * q], xs[4 * q + 1]), sc2, make_float2(e.x, e.y));
                 float2 b = __ffma2_rn(make_float2(xs[4 * q + 2], xs[4 * q + 3]), sc2, make_float2(e.z, e.w));
                 xs[4 * q] = a.x;
@@ -1134,9 +1176,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                   }
                 }
               } else {
-                const float4* e0 = reinterpret_cast<const float4*>(
-                    p.p2c_ends + static_cast<size_t>(it.bh) * 2 * p.ends_pitch + j0);
-                const float4* e1 = e0 + p.ends_pitch / 4;
+                const float4* e0 = reinterpret_cast<const float4*>(ends_s);
+                const float4* e1 = e0 + 32;
                 const int clo = 1 - m0, chi = 2 * kc - 1 - m0;  // in-band columns
 #pragma unroll
                 for (int q = 0; q < 16; ++q) {
@@ -1144,8 +1185,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
                   for (int g = 0; g < 2; ++g) {
-                    const float4 f0 = __ldg(e0 + 2 * q + g);
-                    const float4 f1 = __ldg(e1 + 2 * q + g);
+                    const float4 f0 = e0[2 * q + g];
+                    const float4 f1 = e1[2 * q + g];
                     const float l4[4] = {f0.x, f0.y, f0.z, f0.w};
                     const float r4[4] = {f1.x, f1.y, f1.z, f1.w};
 #pragma unroll
@@ -1443,7 +1484,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 uint32_t fwd_smem_bytes(int mode, const FwdParams& p) {
-  uint32_t aux0 = mode == 4 ? Smem<4>::kOffAux : (mode == 1 ? Smem<1>::kOffAux : Smem<0>::kOffAux);
+  uint32_t aux0 = mode == 4   ? Smem<4>::kOffAux
+                  : mode == 2 ? Smem<2>::kOffAux
+                  : mode == 1 ? Smem<1>::kOffAux
+                              : Smem<0>::kOffAux;
+  static_assert(Smem<0>::kOffAux == Smem<3>::kOffAux, "T5 and ALiBi share the layout");
   if (p.dh == 128) aux0 = Smem<8>::kOffAux;  // T5 and ALiBi share the layout
   static_assert(Smem<8>::kOffAux == Smem<11>::kOffAux, "d = 128 layouts");
   return 1024u + aux0 + fwd_aux_bytes(mode, p) + (p.nsplit > 0 ? kCombBytes : 0u);
