@@ -1,8 +1,9 @@
 /*
  * relpos_attn.h -- C ABI of the GB300 (sm_103a) relative-position attention
  * library (librelpos_attn.so): the forward pass (also over right-padded
- * batches), the T5 cached decode and the T5 and ALiBi backward passes
- * (relpos_t5_attn_bwd, relpos_alibi_attn_bwd, at the end of this header).
+ * batches), the T5 cached decode and the T5, Shaw and ALiBi backward passes
+ * (relpos_t5_attn_bwd, relpos_shaw_attn_bwd, relpos_alibi_attn_bwd, at the
+ * end of this header).
  *
  * One forward call computes multi-head attention whose logits carry a relative-
  * position term that is formed inside the kernel and never written to
@@ -318,6 +319,37 @@ int relpos_t5_attn_bwd(const void* Q, const void* K, const void* V, const void* 
 int relpos_alibi_attn_bwd(const void* Q, const void* K, const void* V, const void* dO,
                           const void* slopes, int B, int H, int Lq, int Lk, int d, int causal,
                           int q_offset, void* dQ, void* dK, void* dV, void* dslopes, void* stream);
+
+/*
+ * relpos_shaw_attn_bwd -- gradients of the Shaw attention forward
+ * (relpos_attn_fwd with mode RELPOS_SHAW, dtype RELPOS_BF16; "Relative
+ * Position Embeddings, in depth", section "Shaw et al."). With r_ij =
+ * clip(j - p_i, -k, k) + k the logit is q_i . (k_j + a_K[r_ij]) / sqrt(d) and
+ * the value of key j for query i is v_j + a_V[r_ij]. The chain rule gives
+ *   dP_ij = dO_i . (v_j + a_V[r_ij]),  dS_ij = P_ij (dP_ij - sum_l P_il dP_il),
+ *   dQ_i = sum_j dS_ij (k_j + a_K[r_ij]) / sqrt(d),  dK_j = sum_i dS_ij q_i / sqrt(d),
+ *   dV_j = sum_i P_ij dO_i,
+ *   da_K[r] = sum of dS_ij q_i / sqrt(d) and da_V[r] = sum of P_ij dO_i over
+ *   every (batch, head, i, j) with r_ij = r (the tables are shared by the
+ *   batch and the heads).
+ *
+ *   Q, K, V, dO, B, H, Lq, Lk, d, causal, q_offset, dQ, dK, dV, stream: as for
+ *               relpos_t5_attn_bwd.
+ *   aK, aV      device, bf16 [2k + 1, 64]: the forward call's tables.
+ *   clip_k      k, the forward call's rel_param; 1 <= k <= 16
+ *               (RELPOS_ERR_INVALID_ARG below 1, RELPOS_ERR_UNSUPPORTED above 16).
+ *   daK, daV    device, fp32 [2k + 1, 64], overwritten with the sums over the
+ *               batch and the heads.
+ * Scratch: about (264 + 16 (2k + 2) + 4) * B * H * Lq bytes plus
+ * 2 (2k + 1) * 256 bytes per 128-row query tile and head, from cudaMallocAsync on `stream`,
+ * freed with cudaFreeAsync before the call returns. daK and daV are summed in
+ * a fixed order (the same bits every run); dQ, dK and dV as for
+ * relpos_t5_attn_bwd. Errors and asynchrony as relpos_t5_attn_bwd.
+ */
+int relpos_shaw_attn_bwd(const void* Q, const void* K, const void* V, const void* dO,
+                         const void* aK, const void* aV, int B, int H, int Lq, int Lk, int d,
+                         int clip_k, int causal, int q_offset, void* dQ, void* dK, void* dV,
+                         void* daK, void* daV, void* stream);
 
 #ifdef __cplusplus
 }

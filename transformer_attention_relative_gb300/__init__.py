@@ -28,7 +28,7 @@ RELPOS_ERR_SCRATCH_LIMIT = -5
 
 EXPORTED = ("relpos_attn_fwd", "relpos_attn_fwd_padded", "relpos_index_ids", "relpos_check_status", "relpos_strerror",
             "relpos_selftest_wait_timeout", "relpos_t5_decode_noalloc", "relpos_t5_decode_positions",
-            "relpos_t5_attn_bwd", "relpos_alibi_attn_bwd")
+            "relpos_t5_attn_bwd", "relpos_alibi_attn_bwd", "relpos_shaw_attn_bwd")
 
 _lib = None
 
@@ -69,6 +69,8 @@ def load_library(path: str = LIB_PATH):
     lib.relpos_t5_attn_bwd.restype = i
     lib.relpos_alibi_attn_bwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, vp, vp, vp, vp, vp]
     lib.relpos_alibi_attn_bwd.restype = i
+    lib.relpos_shaw_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, vp, vp, vp, vp, vp, vp]
+    lib.relpos_shaw_attn_bwd.restype = i
     _lib = lib
     return lib
 
@@ -135,6 +137,13 @@ def relpos_alibi_attn_bwd(Q, K, V, dO, slopes, B, H, Lq, Lk, d, causal, q_offset
     """Gradients of the ALiBi attention: dQ, dK, dV and the slopes'."""
     return load_library().relpos_alibi_attn_bwd(Q, K, V, dO, slopes, B, H, Lq, Lk, d, causal,
                                                 q_offset, dQ, dK, dV, dslopes, stream)
+
+
+def relpos_shaw_attn_bwd(Q, K, V, dO, aK, aV, B, H, Lq, Lk, d, clip_k, causal, q_offset, dQ, dK, dV,
+                         daK, daV, stream) -> int:
+    """Gradients of the Shaw attention: dQ, dK, dV and those of a_K and a_V."""
+    return load_library().relpos_shaw_attn_bwd(Q, K, V, dO, aK, aV, B, H, Lq, Lk, d, clip_k, causal,
+                                               q_offset, dQ, dK, dV, daK, daV, stream)
 
 
 strerror = relpos_strerror
@@ -285,3 +294,29 @@ def alibi_attention_backward(Q, K, V, dO, slopes, *, causal: bool = False, q_off
     if rc != RELPOS_OK:
         raise RelposError(rc, "relpos_alibi_attn_bwd")
     return dQ, dK, dV, dslopes
+
+
+def shaw_attention_backward(Q, K, V, dO, aK, aV, *, clip_k: int = 16, causal: bool = False,
+                            q_offset: int = 0, stream=None):
+    """Run ``relpos_shaw_attn_bwd`` on CUDA tensors; returns (dQ, dK, dV, daK, daV).
+
+    Q, dO [B,H,Lq,64] and K, V [B,H,Lk,64] bf16; aK, aV [2k+1, 64] bf16 (k = clip_k). daK and daV
+    come back fp32, summed over the batch and the heads.
+    """
+    import torch
+    B, H, Lq, d = Q.shape
+    Lk = K.shape[2]
+    for t in (Q, K, V, dO, aK, aV):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("tensors must be contiguous CUDA tensors")
+    if any(t.dtype != torch.bfloat16 for t in (Q, K, V, dO, aK, aV)):
+        raise TypeError("Q, K, V, dO, aK, aV must be bf16")
+    dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
+    daK = torch.empty(aK.shape, dtype=torch.float32, device=aK.device)
+    daV = torch.empty(aV.shape, dtype=torch.float32, device=aV.device)
+    rc = relpos_shaw_attn_bwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(dO), _ptr(aK), _ptr(aV), B, H, Lq, Lk, d,
+                              clip_k, int(causal), q_offset, _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(daK),
+                              _ptr(daV), _stream(stream))
+    if rc != RELPOS_OK:
+        raise RelposError(rc, "relpos_shaw_attn_bwd")
+    return dQ, dK, dV, daK, daV

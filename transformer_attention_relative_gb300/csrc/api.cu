@@ -576,18 +576,23 @@ int attn_fwd_t5_positions(const void* Q, const void* K, const void* V, const voi
 namespace relpos {
 namespace {
 
-// relpos_t5_attn_bwd (mode 0: table = bias [nb, H], dtable = dbias) and
+// relpos_t5_attn_bwd (mode 0: table = bias [nb, H], dtable = dbias),
+// relpos_shaw_attn_bwd (mode 1: table / table1 = a_K / a_V [2k + 1, 64] bf16,
+// dtable / dtable1 = their fp32 gradients, max_distance = k) and
 // relpos_alibi_attn_bwd (mode 3: table = slopes [H], dtable = dslopes).
 int attn_bwd_impl(int mode, const void* Q, const void* K, const void* V, const void* dO,
-                  const void* table, int B, int H, int Lq, int Lk, int d, int num_buckets,
+                  const void* table, const void* table1, int B, int H, int Lq, int Lk, int d, int num_buckets,
                   int max_distance, int causal, int q_offset, void* dQ, void* dK, void* dV,
-                  void* dtable, void* stream) {
+                  void* dtable, void* dtable1, void* stream) {
   if (B < 0 || H < 0 || Lq < 0 || Lk < 0 || q_offset < 0 || d <= 0) return RELPOS_ERR_INVALID_ARG;
   int rc = check_rel_params(mode, num_buckets, max_distance, causal);
   if (rc != RELPOS_OK) return rc;
   if (d != kHeadDim) return RELPOS_ERR_UNSUPPORTED;
+  if (mode == RELPOS_SHAW && max_distance > bwd_max_shaw_k()) return RELPOS_ERR_UNSUPPORTED;
   if (B == 0 || H == 0) return RELPOS_OK;
   if (!table || !dtable || !aligned16(table) || !aligned16(dtable)) return RELPOS_ERR_INVALID_ARG;
+  if (mode == RELPOS_SHAW && (!table1 || !dtable1 || !aligned16(table1) || !aligned16(dtable1)))
+    return RELPOS_ERR_INVALID_ARG;
   if (static_cast<long long>(B) * H > 65535) return RELPOS_ERR_UNSUPPORTED;
   if (Lq > (1 << 24) || Lk > (1 << 24) || q_offset > (1 << 28)) return RELPOS_ERR_UNSUPPORTED;
   // every pointer is checked before anything (the table gradient's clear
@@ -612,8 +617,12 @@ int attn_bwd_impl(int mode, const void* Q, const void* K, const void* V, const v
   const size_t BH = static_cast<size_t>(B) * H;
   const size_t row_bytes = kHeadDim * 2;
   const size_t dtable_bytes =
-      (mode == RELPOS_T5 ? static_cast<size_t>(num_buckets) * H : static_cast<size_t>(H)) * sizeof(float);
+      (mode == RELPOS_T5     ? static_cast<size_t>(num_buckets) * H
+       : mode == RELPOS_SHAW ? static_cast<size_t>(2 * max_distance + 1) * kHeadDim
+                             : static_cast<size_t>(H)) *
+      sizeof(float);
   if (cudaMemsetAsync(dtable, 0, dtable_bytes, s) != cudaSuccess) return RELPOS_ERR_CUDA;
+  if (mode == RELPOS_SHAW && cudaMemsetAsync(dtable1, 0, dtable_bytes, s) != cudaSuccess) return RELPOS_ERR_CUDA;
   if (Lq == 0 || Lk == 0) {  // no score: every gradient is zero
     bool ok = true;
     if (Lq > 0) ok = ok && cudaMemsetAsync(dQ, 0, BH * Lq * row_bytes, s) == cudaSuccess;
@@ -625,11 +634,19 @@ int attn_bwd_impl(int mode, const void* Q, const void* K, const void* V, const v
   if (!status) return RELPOS_ERR_CUDA;
 
   // scratch: the fp32 dQ accumulator, then the row statistics (lse, D) with
-  // rows padded to whole 128-row query tiles
+  // rows padded to whole 128-row query tiles; Shaw: the rows' end values,
+  // their T, U and per-offset sums of P and dS (2k + 2 floats a row), and
+  // every query tile's partial table gradients
   const int lq_pad = (Lq + 127) & ~127;
   const size_t n_acc = BH * Lq * kHeadDim, n_stats = 2 * BH * static_cast<size_t>(lq_pad);
+  const int nr = mode == RELPOS_SHAW ? 2 * max_distance + 2 : 0;
+  const size_t n_rows = BH * static_cast<size_t>(lq_pad);
+  const size_t n_shaw = mode == RELPOS_SHAW ? 4 * n_rows + 4 * n_rows * nr +
+                                                  n_rows / 128 * 2 * static_cast<size_t>(2 * max_distance + 1) * kHeadDim
+                                            : 0;
   float* scratch = nullptr;
-  if (cudaMallocAsync(reinterpret_cast<void**>(&scratch), (n_acc + n_stats) * sizeof(float), s) != cudaSuccess) {
+  if (cudaMallocAsync(reinterpret_cast<void**>(&scratch), (n_acc + n_stats + n_shaw) * sizeof(float), s) !=
+      cudaSuccess) {
     cudaGetLastError();
     return RELPOS_ERR_CUDA;
   }
@@ -660,6 +677,22 @@ int attn_bwd_impl(int mode, const void* Q, const void* K, const void* V, const v
     p.R = R;
     p.t5 = t5;
     p.dbias = static_cast<float*>(dtable);
+  } else if (mode == RELPOS_SHAW) {
+    p.aK = static_cast<const __nv_bfloat16*>(table);
+    p.aV = static_cast<const __nv_bfloat16*>(table1);
+    p.kc = max_distance;
+    p.nr = nr;
+    float* sh = scratch + n_acc + n_stats;  // every part a multiple of 128 floats
+    p.shEnds = sh;
+    p.shT = sh + 4 * n_rows;
+    p.shU = p.shT + n_rows * nr;
+    p.shBP = p.shU + n_rows * nr;
+    p.shBdS = p.shBP + n_rows * nr;
+    p.shPart = p.shBdS + n_rows * nr;
+    p.daK = static_cast<float*>(dtable);
+    p.daV = static_cast<float*>(dtable1);
+    p.Qp = static_cast<const __nv_bfloat16*>(Q);
+    p.dOp = static_cast<const __nv_bfloat16*>(dO);
   } else {
     p.slopes = static_cast<const float*>(table);
     p.dslopes = static_cast<float*>(dtable);
@@ -683,14 +716,22 @@ extern "C" int relpos_t5_attn_bwd(const void* Q, const void* K, const void* V, c
                                   const void* bias, int B, int H, int Lq, int Lk, int d, int num_buckets,
                                   int max_distance, int causal, int q_offset, void* dQ, void* dK, void* dV,
                                   void* dbias, void* stream) {
-  return attn_bwd_impl(RELPOS_T5, Q, K, V, dO, bias, B, H, Lq, Lk, d, num_buckets, max_distance, causal,
-                       q_offset, dQ, dK, dV, dbias, stream);
+  return attn_bwd_impl(RELPOS_T5, Q, K, V, dO, bias, nullptr, B, H, Lq, Lk, d, num_buckets, max_distance, causal,
+                       q_offset, dQ, dK, dV, dbias, nullptr, stream);
+}
+
+extern "C" int relpos_shaw_attn_bwd(const void* Q, const void* K, const void* V, const void* dO,
+                                    const void* aK, const void* aV, int B, int H, int Lq, int Lk, int d,
+                                    int clip_k, int causal, int q_offset, void* dQ, void* dK, void* dV,
+                                    void* daK, void* daV, void* stream) {
+  return attn_bwd_impl(RELPOS_SHAW, Q, K, V, dO, aK, aV, B, H, Lq, Lk, d, 0, clip_k, causal, q_offset, dQ, dK,
+                       dV, daK, daV, stream);
 }
 
 extern "C" int relpos_alibi_attn_bwd(const void* Q, const void* K, const void* V, const void* dO,
                                      const void* slopes, int B, int H, int Lq, int Lk, int d, int causal,
                                      int q_offset, void* dQ, void* dK, void* dV, void* dslopes,
                                      void* stream) {
-  return attn_bwd_impl(RELPOS_ALIBI, Q, K, V, dO, slopes, B, H, Lq, Lk, d, 0, 0, causal, q_offset, dQ, dK,
-                       dV, dslopes, stream);
+  return attn_bwd_impl(RELPOS_ALIBI, Q, K, V, dO, slopes, nullptr, B, H, Lq, Lk, d, 0, 0, causal, q_offset, dQ,
+                       dK, dV, dslopes, nullptr, stream);
 }

@@ -52,6 +52,7 @@ namespace {
 
 constexpr int kBT = 128;  // rows per tile, queries or keys
 constexpr int kMaxR = 1024;
+constexpr int kMaxShawK = 16;  // Shaw backward: the statistics kernel holds 6 x 128 rows of 2k + 2 floats
 constexpr uint32_t kTile = kBT * kHeadDim * 2;  // 16 KB
 constexpr uint32_t kHalfTile = kTile / 2;       // 64 rows
 
@@ -142,6 +143,29 @@ RP_DEVI void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t b
 RP_DEVI void st_shared_u16(uint32_t addr, uint16_t v) {
   asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
 }
+// Predicated shared-memory store without a branch (the lanes disagree).
+RP_DEVI void st_shared_f32_if(uint32_t addr, float v, int pred) {
+  asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t@q st.shared.f32 [%0], %1;\n\t}" ::"r"(addr), "f"(v),
+               "r"(pred)
+               : "memory");
+}
+// Dot product of a row of 64 values with a bf16 table row in shared memory
+// (64 values, 128 contiguous bytes; every lane reads the same row).
+RP_DEVI float dot64_bf16(const float (&v)[64], const __nv_bfloat16* row) {
+  const uint4* r4 = reinterpret_cast<const uint4*>(row);
+  float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const uint4 u = r4[c];
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 t = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
+      acc = __ffma2_rn(make_float2(v[8 * c + 2 * e], v[8 * c + 2 * e + 1]), t, acc);
+    }
+  }
+  return acc.x + acc.y;
+}
 
 // ================================================================ stats kernel
 // 12 warps: 0 TMA producer, 1 MMA issuer (TMEM owner), 2-3 idle, 4-7 and 8-11
@@ -175,8 +199,11 @@ __global__ void __launch_bounds__(kStThreads, 1)
   auto bar = [&](uint32_t i) { return sb + kStOffBar + 8u * i; };
   volatile int* abort_f = reinterpret_cast<volatile int*>(smem + kStOffBar + kStAbort);
   float* tab = reinterpret_cast<float*>(smem + kStOffAux);                 // T5: 4 copies of E
-  float* mrg = tab + (MODE == 0 ? 4 * tab_stride(p.R) : 0);                // [3][128] merge
-  float* bsm = mrg + 3 * 128;                                               // T5 bias per bucket
+  // Shaw: a_K, a_V (bf16, 64 rows of 64), then per row q . a_K and dO . a_V
+  // (nr floats), then each warpgroup's sums per clipped offset of P and P dP
+  float* shw = tab + (MODE == 0 ? 4 * tab_stride(p.R) : 0);
+  float* mrg = shw + (MODE == 1 ? 64 * 64 + 6 * 128 * p.nr : 0);            // [7][128] merge
+  float* bsm = mrg + 7 * 128;                                               // T5 bias per bucket
 
   const int last_row = min(i0 + kBT, p.Lq) - 1;
   int n_kv = (p.Lk + kBT - 1) / kBT;
@@ -270,6 +297,52 @@ __global__ void __launch_bounds__(kStThreads, 1)
       build_bias_copies(tab, bsm, p, false, ct, 256, 2, nullptr);
       named_bar_sync(2, 256);
     }
+    if constexpr (MODE == 1) {
+      // Shaw: the tables, the zeroed per-offset sums, then every row's
+      // q . a_K[r] (log2-scaled, warpgroup 0) and dO . a_V[r] (warpgroup 1)
+      // for the clipped offsets r, into shared memory and to global memory
+      // (the dK / dV kernel reads them), with the saturated ends apart
+      const int ct = static_cast<int>(threadIdx.x) - 128;  // 0 .. 255
+      const int nrel = 2 * p.kc + 1;
+      __nv_bfloat16* aKs = reinterpret_cast<__nv_bfloat16*>(shw);
+      __nv_bfloat16* aVs = aKs + 64 * 64;
+      for (int i = ct; i < nrel * 8; i += 256) {
+        reinterpret_cast<uint4*>(aKs)[i] = __ldg(reinterpret_cast<const uint4*>(p.aK) + i);
+        reinterpret_cast<uint4*>(aVs)[i] = __ldg(reinterpret_cast<const uint4*>(p.aV) + i);
+      }
+      float* bins0 = shw + 64 * 64 + 2 * 128 * p.nr;
+      for (int i = ct; i < 4 * 128 * p.nr; i += 256) bins0[i] = 0.f;
+      if (!mbar_wait(bar(kStBarQ), 0)) *abort_f = 1;  // the Q and dO tiles
+      named_bar_sync(2, 256);
+      const int xx = (warp - 4) >> 2, tt = ((warp & 3) << 5) | lane;
+      const uint8_t* tile = smem + (xx == 0 ? kStOffQ : kStOffdO);
+      float v[64];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint4 u = *reinterpret_cast<const uint4*>(tile + tt * 128 + ((c ^ (tt & 7)) << 4));
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
+          v[8 * c + 2 * e] = f.x;
+          v[8 * c + 2 * e + 1] = f.y;
+        }
+      }
+      float* dst = shw + 64 * 64 + (xx * 128 + tt) * p.nr;
+      const __nv_bfloat16* tb = xx == 0 ? aKs : aVs;
+      const float sc = xx == 0 ? p.scale_log2 : 1.f;
+      const size_t grow = static_cast<size_t>(bh) * p.lq_pad + i0 + tt;
+      float* g = (xx == 0 ? p.shT : p.shU) + grow * p.nr;
+#pragma unroll 1
+      for (int r = 0; r < nrel; ++r) {
+        const float val = dot64_bf16(v, tb + r * 64) * sc;
+        dst[r] = val;
+        g[r] = val;
+      }
+      p.shEnds[(static_cast<size_t>(bh) * 4 + 2 * xx) * p.lq_pad + i0 + tt] = dst[0];
+      p.shEnds[(static_cast<size_t>(bh) * 4 + 2 * xx + 1) * p.lq_pad + i0 + tt] = dst[2 * p.kc];
+      named_bar_sync(2, 256);
+    }
     const int x = (warp - 4) >> 2;  // TMEM buffer / parity of the key tiles taken
     const int t = ((warp & 3) << 5) | lane;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -286,6 +359,15 @@ __global__ void __launch_bounds__(kStThreads, 1)
     const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
     bool err = false;
     int cnt = 0;
+    // Shaw: this row's q . a_K and dO . a_V, this warpgroup's sums per
+    // clipped offset of P and P dP (the in-band offsets meet one key each; the
+    // two ends gather the keys beyond the clip, kept in registers), rescaled
+    // with l and dsum
+    const float* Trow = MODE == 1 ? shw + 64 * 64 + t * p.nr : nullptr;
+    const float* Urow = MODE == 1 ? shw + 64 * 64 + (128 + t) * p.nr : nullptr;
+    float* bp_row = MODE == 1 ? shw + 64 * 64 + (2 * 128 + x * 128 + t) * p.nr : nullptr;
+    float* bd_row = MODE == 1 ? shw + 64 * 64 + (4 * 128 + x * 128 + t) * p.nr : nullptr;
+    float sLl = 0.f, sRl = 0.f, sLd = 0.f, sRd = 0.f;
     for (int j = x; j < n_kv; j += 2, ++cnt) {
       const bool ok = mbar_wait(bar(kStBarS + x), cnt & 1);
       err = __any_sync(0xffffffffu, !ok);
@@ -298,12 +380,12 @@ __global__ void __launch_bounds__(kStThreads, 1)
       // statistics are never used)
       const int rel_hi = j0 + kBT - 1 - (i0 + p.q_offset), rel_lo = j0 - (i0 + kBT - 1 + p.q_offset);
       const bool nomask = j0 + kBT <= p.Lk && (!p.causal || rel_hi <= 0);
-      const bool far_l = MODE == 0 && rel_hi <= -R;
-      const bool far_r = MODE == 0 && p.t5.bidir && rel_lo >= R;
-      // one row constant: T5 beyond the saturation distance; ALiBi with
-      // every key on one side (the rest is linear in the column). T5 near
-      // tiles without masking read their biases 4 at a time.
-      const bool fast = nomask && (MODE == 0 ? (far_l || far_r) : (rel_hi <= 0 || rel_lo >= 0));
+      const bool far_l = (MODE == 0 && rel_hi <= -R) || (MODE == 1 && rel_hi <= -p.kc);
+      const bool far_r = (MODE == 0 && p.t5.bidir && rel_lo >= R) || (MODE == 1 && rel_lo >= p.kc);
+      // one row constant: T5 beyond the saturation distance, Shaw beyond the
+      // clip; ALiBi with every key on one side (the rest is linear in the
+      // column). T5 near tiles without masking read their biases 4 at a time.
+      const bool fast = nomask && (MODE != 3 ? (far_l || far_r) : (rel_hi <= 0 || rel_lo >= 0));
       const bool near_t5 = MODE == 0 && nomask && !fast;
 #pragma unroll 1
       for (int c0 = 0; c0 < kBT; c0 += 64) {
@@ -322,6 +404,7 @@ __global__ void __launch_bounds__(kStThreads, 1)
         }
         float* xv = reinterpret_cast<float*>(sr);
         float bc = 0.f;  // the row constant of a fast tile (log2 units)
+        float ue = 0.f;  // Shaw: dO . a_V of the fast tile's side
         float mx;
         if (near_t5) {
           // E index of column c: j0 + c0 + c - prow + R + kTabPad
@@ -343,6 +426,9 @@ __global__ void __launch_bounds__(kStThreads, 1)
         } else if (fast) {
           if constexpr (MODE == 0) {
             bc = far_l ? tab[R + kTabPad - R] : tab[R + kTabPad + R];  // biases of offsets -R, R
+          } else if constexpr (MODE == 1) {
+            bc = Trow[far_l ? 0 : 2 * p.kc];
+            ue = Urow[far_l ? 0 : 2 * p.kc];
           } else {
             // -slope |j - p| = g (j - p) with g = slope (keys behind) or -slope (ahead):
             // scaled scores plus g c, then the row constant g (j0 + c0 - p)
@@ -363,7 +449,7 @@ __global__ void __launch_bounds__(kStThreads, 1)
             m0 = max3f(m0, xv[c], xv[c + 1]);
             m1 = max3f(m1, xv[c + 2], xv[c + 3]);
           }
-          mx = MODE == 0 ? fmaf(fmaxf(m0, m1), p.scale_log2, bc) : fmaxf(m0, m1) + bc;
+          mx = MODE != 3 ? fmaf(fmaxf(m0, m1), p.scale_log2, bc) : fmaxf(m0, m1) + bc;
         } else {
           float m0 = -INFINITY, m1 = -INFINITY;
 #pragma unroll
@@ -371,10 +457,15 @@ __global__ void __launch_bounds__(kStThreads, 1)
             const int rel = j0 + c0 + c - prow;
             const bool valid = (j0 + c0 + c < p.Lk) & (!p.causal | (rel <= 0));
             float b;
-            if constexpr (MODE == 0)
+            if constexpr (MODE == 0) {
               b = tab[min(max(rel + R + kTabPad, 0), tab_len(R) - 1)];
-            else
+            } else if constexpr (MODE == 1) {
+              const int r = min(max(rel, -p.kc), p.kc) + p.kc;
+              b = Trow[r];
+              dr[c] = __float_as_uint(__uint_as_float(dr[c]) + Urow[r]);
+            } else {
               b = -alibi * fabsf(static_cast<float>(rel));
+            }
             xv[c] = valid ? fmaf(xv[c], p.scale_log2, b) : -INFINITY;
             if (c & 1)
               m1 = fmaxf(m1, xv[c]);
@@ -388,20 +479,77 @@ __global__ void __launch_bounds__(kStThreads, 1)
           const float a = ex2_approx(m - mx);  // 0 while m = -inf
           l2 = __fmul2_rn(l2, make_float2(a, a));
           d2 = __fmul2_rn(d2, make_float2(a, a));
+          if constexpr (MODE == 1) {
+            sLl *= a;
+            sRl *= a;
+            sLd *= a;
+            sRd *= a;
+#pragma unroll 1
+            for (int r = 0; r < 2 * p.kc + 1; ++r) {
+              bp_row[r] *= a;
+              bd_row[r] *= a;
+            }
+          }
           m = mx;
         }
         const float mu = m == -INFINITY ? 0.f : m;
-        // 2^(x - m): fast tiles scale the raw scores (T5) inside the FMA
-        const float2 mul2 = (MODE == 0 && fast) ? sc2 : make_float2(1.f, 1.f);
+        // 2^(x - m): fast tiles scale the raw scores (T5, Shaw) inside the FMA
+        const float2 mul2 = (MODE != 3 && fast) ? sc2 : make_float2(1.f, 1.f);
         const float off = bc - mu;
         const float2 off2 = make_float2(off, off);
+        if constexpr (MODE == 1) {
+          if (fast) {
+            // beyond the clip: dP gains dO . a_V of the side; the tile's
+            // sums go to that side
+            float2 tl = make_float2(0.f, 0.f), td = make_float2(0.f, 0.f);
+            const float2 ue2 = make_float2(ue, ue);
 #pragma unroll
-        for (int c = 0; c < 64; c += 2) {
-          float2 e = __ffma2_rn(make_float2(xv[c], xv[c + 1]), mul2, off2);
-          e.x = ex2_approx(e.x);
-          e.y = ex2_approx(e.y);
-          l2 = __fadd2_rn(l2, e);
-          d2 = __ffma2_rn(e, make_float2(__uint_as_float(dr[c]), __uint_as_float(dr[c + 1])), d2);
+            for (int c = 0; c < 64; c += 2) {
+              float2 e = __ffma2_rn(make_float2(xv[c], xv[c + 1]), mul2, off2);
+              e.x = ex2_approx(e.x);
+              e.y = ex2_approx(e.y);
+              tl = __fadd2_rn(tl, e);
+              td = __ffma2_rn(e, __fadd2_rn(make_float2(__uint_as_float(dr[c]), __uint_as_float(dr[c + 1])), ue2), td);
+            }
+            l2 = __fadd2_rn(l2, tl);
+            d2 = __fadd2_rn(d2, td);
+            if (far_l) {
+              sLl += tl.x + tl.y;
+              sLd += td.x + td.y;
+            } else {
+              sRl += tl.x + tl.y;
+              sRd += td.x + td.y;
+            }
+          } else {
+            // per element: in-band offsets into their (row, offset) entries
+            // (one key each), the others to the side sums
+            const uint32_t bp_a = smem_u32(bp_row), bd_a = smem_u32(bd_row);
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+              const float e = ex2_approx(xv[c] - mu);
+              const float dd = e * __uint_as_float(dr[c]);
+              l2.x += e;
+              d2.x += dd;
+              const int rel = j0 + c0 + c - prow;
+              const int inb = (rel > -p.kc) & (rel < p.kc);
+              const uint32_t ra = 4u * static_cast<uint32_t>(min(max(rel, -p.kc), p.kc) + p.kc);
+              st_shared_f32_if(bp_a + ra, e, inb);
+              st_shared_f32_if(bd_a + ra, dd, inb);
+              sLl += rel <= -p.kc ? e : 0.f;
+              sLd += rel <= -p.kc ? dd : 0.f;
+              sRl += rel >= p.kc ? e : 0.f;
+              sRd += rel >= p.kc ? dd : 0.f;
+            }
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 64; c += 2) {
+            float2 e = __ffma2_rn(make_float2(xv[c], xv[c + 1]), mul2, off2);
+            e.x = ex2_approx(e.x);
+            e.y = ex2_approx(e.y);
+            l2 = __fadd2_rn(l2, e);
+            d2 = __ffma2_rn(e, make_float2(__uint_as_float(dr[c]), __uint_as_float(dr[c + 1])), d2);
+          }
         }
       }
     }
@@ -415,18 +563,51 @@ __global__ void __launch_bounds__(kStThreads, 1)
       mrg[t] = m;
       mrg[128 + t] = l;
       mrg[256 + t] = dsum;
+      if constexpr (MODE == 1) {
+        mrg[3 * 128 + t] = sLl;
+        mrg[4 * 128 + t] = sRl;
+        mrg[5 * 128 + t] = sLd;
+        mrg[6 * 128 + t] = sRd;
+      }
     }
     named_bar_sync(1, 256);
     if (x == 0 && !*abort_f) {
       const float m1 = mrg[t], l1 = mrg[128 + t], d1 = mrg[256 + t];
       const float M = fmaxf(m, m1);
-      float lse = 0.f, D = 0.f;
+      float lse = 0.f, D = 0.f, w0 = 0.f, w1 = 0.f;
       if (M != -INFINITY) {
         const float a0 = m == -INFINITY ? 0.f : ex2_approx(m - M);
         const float a1 = m1 == -INFINITY ? 0.f : ex2_approx(m1 - M);
         const float lt = l * a0 + l1 * a1;
         lse = M + log2f(lt);
         D = (dsum * a0 + d1 * a1) / lt;
+        w0 = a0 / lt;
+        w1 = a1 / lt;
+      }
+      if constexpr (MODE == 1) {
+        // per clipped offset: sum of P and of dS = P (dP - D) over the
+        // row's keys at that offset (zero for rows past Lq)
+        if (row >= p.Lq) w0 = w1 = 0.f;
+        const float* bp1 = shw + 64 * 64 + (3 * 128 + t) * p.nr;
+        const float* bd1 = shw + 64 * 64 + (5 * 128 + t) * p.nr;
+        const size_t gr = (static_cast<size_t>(bh) * p.lq_pad + row) * p.nr;
+        const int kc2 = 2 * p.kc;
+#pragma unroll 1
+        for (int r = 0; r <= kc2; ++r) {
+          float sp, sd;
+          if (r == 0) {
+            sp = sLl * w0 + mrg[3 * 128 + t] * w1;
+            sd = sLd * w0 + mrg[5 * 128 + t] * w1;
+          } else if (r == kc2) {
+            sp = sRl * w0 + mrg[4 * 128 + t] * w1;
+            sd = sRd * w0 + mrg[6 * 128 + t] * w1;
+          } else {
+            sp = bp_row[r] * w0 + bp1[r] * w1;
+            sd = bd_row[r] * w0 + bd1[r] * w1;
+          }
+          p.shBP[gr + r] = sp;
+          p.shBdS[gr + r] = fmaf(-D, sp, sd);
+        }
       }
       // rows past Lq (zero-filled Q and dO: D = 0) fill the padding that the
       // dK / dV kernel reads whole
@@ -491,8 +672,9 @@ __global__ void __launch_bounds__(kKvThreads, 1)
   volatile int* abort_f = reinterpret_cast<volatile int*>(smem + kKvOffBar + kKvAbort);
   // T5: 4 copies of F (the reversed extended bias table); dS summed per
   // offset over the near tiles (entry = E index of the offset); per bucket
+  // Shaw: per ring stage, the query tile's T[0], T[2k], U[0], U[2k]
   float* tab = reinterpret_cast<float*>(smem + kKvOffAux);
-  float* hist = tab + (MODE == 0 ? 4 * tab_stride(R) : 0);
+  float* hist = tab + (MODE == 0 ? 4 * tab_stride(R) : MODE == 1 ? 2 * 512 : 0);
   float* hist_b = hist + (MODE == 0 ? tab_len(R) : 0);
   float* red = hist_b + kMaxT5Buckets;  // side sums / ALiBi slope partials
   float* bsm = red + 16;                // T5 bias per bucket
@@ -545,11 +727,17 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           const int q0 = (first + i) * kBT;
           const uint32_t dst = sb + kKvOffRing + st * kKvStage;
           const size_t so = static_cast<size_t>(bh) * p.lq_pad + q0;  // 512-byte aligned rows
-          mbar_arrive_expect_tx(bar(kKvBarFull + st), 2 * kTile + 1024);
+          mbar_arrive_expect_tx(bar(kKvBarFull + st), 2 * kTile + 1024 + (MODE == 1 ? 2048 : 0));
           tma_load_3d(dst, &tmQ, bar(kKvBarFull + st), 0, q0, bh);
           tma_load_3d(dst + kTile, &tmdO, bar(kKvBarFull + st), 0, q0, bh);
           bulk_load(dst + 2 * kTile, p.lse + so, 512, bar(kKvBarFull + st));
           bulk_load(dst + 2 * kTile + 512, p.Dr + so, 512, bar(kKvBarFull + st));
+          if constexpr (MODE == 1) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              bulk_load(smem_u32(tab) + st * 2048u + e * 512u,
+                        p.shEnds + (static_cast<size_t>(bh) * 4 + e) * p.lq_pad + q0, 512, bar(kKvBarFull + st));
+          }
           ++issued;
         }
         if (!ok) {
@@ -683,8 +871,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       const int rb = key - q0 - p.q_offset;
       const int rel_hi = j0 + kBT - 1 - (q0 + p.q_offset), rel_lo = j0 - (q0 + 63 + p.q_offset);
       const bool nomask = j0 + kBT <= p.Lk && q0 + 64 <= p.Lq && (!p.causal || rel_hi <= 0);
-      const bool far_l = MODE == 0 && rel_hi <= -R;
-      const bool far_r = MODE == 0 && p.t5.bidir && rel_lo >= R;
+      const bool far_l = (MODE == 0 && rel_hi <= -R) || (MODE == 1 && rel_hi <= -p.kc);
+      const bool far_r = (MODE == 0 && p.t5.bidir && rel_lo >= R) || (MODE == 1 && rel_lo >= p.kc);
       // dS goes to shared memory as it is formed: the dQ product of tile
       // i - 2 must have read this buffer
       if (i >= 2) {
@@ -754,12 +942,15 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         __syncwarp();  // read before the next sub-step writes
       };
       bool diag = false;  // a T5 sub-step that summed per offset
-      if (nomask && (MODE == 0 ? (far_l || far_r) : (rel_hi <= 0 || rel_lo >= 0))) {
+      if (nomask && (MODE != 3 ? (far_l || far_r) : (rel_hi <= 0 || rel_lo >= 0))) {
         // one bias per row (T5 beyond the saturation distance), or ALiBi with
         // every key on one side: the logit is s * scale + g (c - rb) with
         // g = -slope (keys behind: |rel| = c - rb) or +slope (ahead: rb - c)
-        // F index of offset o: R + kTabPad - o
+        // F index of offset o: R + kTabPad - o. Shaw beyond the clip: each
+        // column's query takes its T and U of the side's end offset.
         const float bc = MODE == 0 ? (far_l ? tab[2 * R + kTabPad] : tab[kTabPad]) : 0.f;
+        const float* te = tab + (i & 1) * 512 + (far_l ? 0 : 128) + hf * 64;  // Shaw
+        const float* ue = te + 256;
         const float g = MODE == 0 ? 0.f : (rel_hi <= 0 ? -alibi : alibi);
         const float2 g2 = make_float2(g, g);
         const float nrb = -static_cast<float>(rb);
@@ -771,9 +962,16 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           for (int qq = 0; qq < 4; ++qq) {
             const int q = 4 * gi + qq;
             const float4 L = *reinterpret_cast<const float4*>(lse_s + 4 * q);
-            const float4 D = *reinterpret_cast<const float4*>(dd_s + 4 * q);
+            float4 D = *reinterpret_cast<const float4*>(dd_s + 4 * q);
             float2 off0 = make_float2(bc - L.x, bc - L.y), off1 = make_float2(bc - L.z, bc - L.w);
             float2 cm0 = make_float2(0.f, 0.f), cm1 = make_float2(0.f, 0.f);
+            if constexpr (MODE == 1) {  // logit + T, dP + U: D - U stands for D
+              const float4 T4 = *reinterpret_cast<const float4*>(te + 4 * q);
+              const float4 U4 = *reinterpret_cast<const float4*>(ue + 4 * q);
+              off0 = __fadd2_rn(off0, make_float2(T4.x, T4.y));
+              off1 = __fadd2_rn(off1, make_float2(T4.z, T4.w));
+              D = make_float4(D.x - U4.x, D.y - U4.y, D.z - U4.z, D.w - U4.w);
+            }
             if constexpr (MODE == 3) {
               cm0 = __fadd2_rn(make_float2(static_cast<float>(4 * q), static_cast<float>(4 * q + 1)),
                                make_float2(nrb, nrb));
@@ -796,7 +994,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             const float2 d0 = __fmul2_rn(e0, t0), d1 = __fmul2_rn(e1, t1);
             if constexpr (MODE == 0) {
               acc = __fadd2_rn(acc, __fadd2_rn(d0, d1));
-            } else {
+            } else if constexpr (MODE == 3) {
               acc = __ffma2_rn(d0, cm0, acc);
               acc = __ffma2_rn(d1, cm1, acc);
             }
@@ -813,7 +1011,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             sumL += a;
           else
             sumR += a;
-        } else {
+        } else if constexpr (MODE == 3) {
           dsl += rel_hi <= 0 ? a : -a;  // |rel| = c - rb behind, rb - c ahead
         }
       } else if (MODE == 0 && nomask) {
@@ -859,7 +1057,9 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       } else {
         diag = MODE == 0;
         // per element: masks, the bias of each offset, T5 dS summed per
-        // offset
+        // offset; Shaw reads each column's T and U rows (the statistics
+        // kernel's, through L2)
+        const size_t srow = (static_cast<size_t>(bh) * p.lq_pad + q0) * p.nr;
 #pragma unroll
         for (int gi = 0; gi < 4; ++gi) {
           uint32_t pp[8], pd[8];
@@ -873,19 +1073,24 @@ __global__ void __launch_bounds__(kKvThreads, 1)
               // branch-free: masked elements take 2^-inf = 0 (a divergent
               // branch around each exponential costs several times the work)
               const bool valid = key_ok & (q0 + cc < p.Lq) & (!p.causal | (rel <= 0));
-              float b;
-              if constexpr (MODE == 0)
+              float b, ua = 0.f;
+              if constexpr (MODE == 0) {
                 b = tab[min(max(R + kTabPad - rel, 0), tab_len(R) - 1)];
-              else
+              } else if constexpr (MODE == 1) {
+                const size_t o = srow + static_cast<size_t>(cc) * p.nr + (min(max(rel, -p.kc), p.kc) + p.kc);
+                b = __ldg(p.shT + o);
+                ua = __ldg(p.shU + o);
+              } else {
                 b = -alibi * fabsf(static_cast<float>(rel));
+              }
               const float s2 = fmaf(__uint_as_float(sr[cc]), p.scale_log2, b - lse_s[cc]);
               const float pr = ex2_approx(valid ? s2 : -INFINITY);
-              const float ds = pr * (__uint_as_float(dr[cc]) - dd_s[cc]);
+              const float ds = pr * (__uint_as_float(dr[cc]) + ua - dd_s[cc]);
               pv[u] = pr;
               dsv[u] = ds;
               if constexpr (MODE == 0) {
                 dr[cc] = __float_as_uint(ds);  // for the per-offset sums
-              } else {
+              } else if constexpr (MODE == 3) {
                 dsl = fmaf(ds, fabsf(static_cast<float>(rel)), dsl);
               }
             }
@@ -945,7 +1150,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       if (!*abort_f)
         for (int xb = ct; xb < p.nb; xb += 256)
           if (hist_b[xb] != 0.f) atomicAdd(p.dbias + xb * p.H + h, hist_b[xb]);
-    } else {
+    } else if constexpr (MODE == 3) {
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) dsl += __shfl_xor_sync(0xffffffffu, dsl, o);
       if (lane == 0) atomicAdd(&red[2], dsl);
@@ -1060,19 +1265,145 @@ __global__ void relpos_bwd_dq_convert_kernel(const float4* __restrict__ acc, uin
   }
 }
 
-uint32_t stats_smem_bytes(int mode, int R) {
+// T5: four bias-table copies; Shaw: a_K and a_V, the rows' T and U and the
+// two warpgroups' per-offset sums (nr floats per row each); then the merge
+// buffer and the T5 bias per bucket
+// ================================================================ Shaw: dQ and the tables' gradients
+// One CTA per 128-row query tile and head. dQ_i = the accumulated (scaled)
+// dS K part + scale * sum_r BdS_i[r] a_K[r], to bf16; and the tile's partial
+// sums over its rows of BdS_i[r] q_i (da_K) and BP_i[r] dO_i (da_V).
+constexpr int kShThreads = 256;
+constexpr int kShQs = 65;  // padded row stride of the staged Q and dO rows (floats)
+
+__global__ void __launch_bounds__(kShThreads) relpos_bwd_shaw_final_kernel(const BwdParams p) {
+  extern __shared__ float shf[];
+  const int nrel = 2 * p.kc + 1, nr = p.nr;
+  float* aKf = shf;               // [2k + 1][64]
+  float* bds = aKf + nrel * 64;   // [128][nr]
+  float* bps = bds + 128 * nr;    // [128][nr]
+  float* qf = bps + 128 * nr;     // [128][kShQs]
+  float* of = qf + 128 * kShQs;   // [128][kShQs]
+  const int tid = threadIdx.x;
+  const int tile = blockIdx.x, bh = blockIdx.y, i0 = tile * kBT;
+  const int rows = min(kBT, p.Lq - i0);
+  griddep_wait();
+  for (int e = tid; e < nrel * 64; e += kShThreads) aKf[e] = __bfloat162float(p.aK[e]);
+  const size_t g0 = (static_cast<size_t>(bh) * p.lq_pad + i0) * nr;
+  for (int e = tid; e < kBT * nr; e += kShThreads) {
+    bds[e] = p.shBdS[g0 + e];
+    bps[e] = p.shBP[g0 + e];
+  }
+  for (int e = tid; e < kBT * 8; e += kShThreads) {  // 8 runs of 8 values per row
+    const int r = e >> 3, ch = e & 7;
+    uint4 uq = make_uint4(0u, 0u, 0u, 0u), uo = uq;
+    if (r < rows) {
+      const size_t off = (static_cast<size_t>(bh) * p.Lq + i0 + r) * kHeadDim + ch * 8;
+      uq = *reinterpret_cast<const uint4*>(p.Qp + off);
+      uo = *reinterpret_cast<const uint4*>(p.dOp + off);
+    }
+    const uint32_t wq[4] = {uq.x, uq.y, uq.z, uq.w}, wo[4] = {uo.x, uo.y, uo.z, uo.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wq[k]));
+      const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wo[k]));
+      qf[r * kShQs + ch * 8 + 2 * k] = a.x;
+      qf[r * kShQs + ch * 8 + 2 * k + 1] = a.y;
+      of[r * kShQs + ch * 8 + 2 * k] = b.x;
+      of[r * kShQs + ch * 8 + 2 * k + 1] = b.y;
+    }
+  }
+  __syncthreads();
+  {  // dQ: a row and 32 columns per thread
+    const int r = tid >> 1, c0 = (tid & 1) * 32;
+    if (r < rows) {
+      const size_t off = (static_cast<size_t>(bh) * p.Lq + i0 + r) * kHeadDim + c0;
+      float acc[32];
+#pragma unroll
+      for (int v = 0; v < 8; ++v) {
+        const float4 a = *reinterpret_cast<const float4*>(p.dQacc + off + 4 * v);
+        acc[4 * v] = a.x;
+        acc[4 * v + 1] = a.y;
+        acc[4 * v + 2] = a.z;
+        acc[4 * v + 3] = a.w;
+      }
+#pragma unroll 1
+      for (int k = 0; k < nrel; ++k) {
+        const float w = bds[r * nr + k] * p.scale;
+#pragma unroll
+        for (int c = 0; c < 32; ++c) acc[c] = fmaf(w, aKf[k * 64 + c0 + c], acc[c]);
+      }
+      uint4* d4 = reinterpret_cast<uint4*>(p.dQ + off);
+#pragma unroll
+      for (int v = 0; v < 4; ++v)
+        d4[v] = make_uint4(pack_bf16x2(acc[8 * v], acc[8 * v + 1]), pack_bf16x2(acc[8 * v + 2], acc[8 * v + 3]),
+                           pack_bf16x2(acc[8 * v + 4], acc[8 * v + 5]), pack_bf16x2(acc[8 * v + 6], acc[8 * v + 7]));
+    }
+  }
+  {  // the tile's partial table gradients: column c, offsets g, g + 4, ...
+    const int c = tid & 63, g = tid >> 6;
+    float* part = p.shPart + (static_cast<size_t>(bh) * gridDim.x + tile) * 2 * nrel * 64;
+#pragma unroll 1
+    for (int k = g; k < nrel; k += 4) {
+      float sk = 0.f, sv = 0.f;
+#pragma unroll 4
+      for (int r = 0; r < rows; ++r) {
+        sk = fmaf(bds[r * nr + k], qf[r * kShQs + c], sk);
+        sv = fmaf(bps[r * nr + k], of[r * kShQs + c], sv);
+      }
+      part[k * 64 + c] = sk;
+      part[(nrel + k) * 64 + c] = sv;
+    }
+  }
+}
+
+// da_K (scaled) and da_V: one table row per CTA, summed over every tile's
+// partial in a fixed order (deterministic)
+__global__ void __launch_bounds__(kShThreads) relpos_bwd_shaw_reduce_kernel(const BwdParams p, int nparts) {
+  __shared__ float red[kShThreads];
+  const int nrel = 2 * p.kc + 1;
+  const int row = blockIdx.x;  // 0 .. 2 nrel - 1: da_K rows, then da_V rows
+  const int tid = threadIdx.x, c = tid & 63, g = tid >> 6;
+  griddep_wait();
+  const size_t stride = static_cast<size_t>(2) * nrel * 64;
+  const float* src = p.shPart + static_cast<size_t>(row) * 64 + c;
+  float s0 = 0.f, s1 = 0.f;
+  int q = g;
+  for (; q + 4 < nparts; q += 8) {
+    s0 += src[static_cast<size_t>(q) * stride];
+    s1 += src[static_cast<size_t>(q + 4) * stride];
+  }
+  if (q < nparts) s0 += src[static_cast<size_t>(q) * stride];
+  red[tid] = s0 + s1;
+  __syncthreads();
+  if (g == 0) {
+    const float v = (red[c] + red[64 + c]) + (red[128 + c] + red[192 + c]);
+    if (row < nrel)
+      p.daK[row * 64 + c] = v * p.scale;
+    else
+      p.daV[(row - nrel) * 64 + c] = v;
+  }
+}
+
+uint32_t shaw_final_smem_bytes(int nr) {
+  const uint32_t nrel = static_cast<uint32_t>(nr) - 1u;
+  return (nrel * 64u + 2u * kBT * static_cast<uint32_t>(nr) + 2u * kBT * kShQs) * 4u;
+}
+
+uint32_t stats_smem_bytes(int mode, int R, int nr) {
   const uint32_t tab = mode == 0 ? 4u * static_cast<uint32_t>(tab_stride(R)) * 4u : 0u;
-  return 1024u + kStOffAux + tab + (3u * 128u + kMaxT5Buckets) * 4u;
+  const uint32_t shaw = mode == 1 ? (64u * 64u + 6u * 128u * static_cast<uint32_t>(nr)) * 4u : 0u;
+  return 1024u + kStOffAux + tab + shaw + (7u * 128u + kMaxT5Buckets) * 4u;
 }
 
 // T5: four bias-table copies, the per-offset sums, the compute warps'
 // strips and the bucket of each offset (ALiBi: none); bucket sums, 16 floats
 // of side / slope partials and the biases per bucket
+// (Shaw: the two ring stages' end values)
 uint32_t dkdv_smem_bytes(int mode, int R) {
   const uint32_t t5 =
       mode == 0 ? (4u * static_cast<uint32_t>(tab_stride(R)) + static_cast<uint32_t>(tab_len(R)) + 8u * 96u) * 4u +
                       ((static_cast<uint32_t>(tab_len(R)) + 15u) & ~15u)
-                : 0u;
+                : mode == 1 ? 2u * 2048u : 0u;
   return 1024u + kKvOffAux + t5 + (2u * kMaxT5Buckets + 16u) * 4u;
 }
 
@@ -1102,16 +1433,19 @@ cudaError_t launch_bwd_mode(const CUtensorMap& tmQ, const CUtensorMap& tmK, cons
   const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
   if (!bit || !(attr_set.load() & bit)) {
     cudaError_t e = cudaFuncSetAttribute(relpos_bwd_stats_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(stats_smem_bytes(MODE, kMaxR)));
+                                         static_cast<int>(stats_smem_bytes(MODE, kMaxR, 2 * kMaxShawK + 2)));
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(relpos_bwd_dkdv_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(dkdv_smem_bytes(MODE, kMaxR)));
+    if (e == cudaSuccess && MODE == 1)
+      e = cudaFuncSetAttribute(relpos_bwd_shaw_final_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(shaw_final_smem_bytes(2 * kMaxShawK + 2)));
     if (e != cudaSuccess) return e;
     attr_set.fetch_or(bit);
   }
   const unsigned BH = static_cast<unsigned>(p.B * p.H);
   cudaError_t e = launch_pdl(relpos_bwd_stats_kernel<MODE>, dim3((p.Lq + kBT - 1) / kBT, BH), dim3(kStThreads),
-                             stats_smem_bytes(MODE, p.R), stream, tmQ, tmK, tmV, tmdO, p);
+                             stats_smem_bytes(MODE, p.R, p.nr), stream, tmQ, tmK, tmV, tmdO, p);
   if (e != cudaSuccess) return e;
   {
     cudaLaunchAttribute attr[1];
@@ -1126,6 +1460,24 @@ cudaError_t launch_bwd_mode(const CUtensorMap& tmQ, const CUtensorMap& tmK, cons
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, relpos_bwd_dkdv_kernel<MODE>, tmQ, tmK, tmV, tmdO, tmAcc, p);
     if (e != cudaSuccess) return e;
+  }
+  if constexpr (MODE == 1) {
+    const int nqt = (p.Lq + kBT - 1) / kBT;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(nqt), BH);
+    cfg.blockDim = dim3(kShThreads);
+    cfg.dynamicSmemBytes = shaw_final_smem_bytes(p.nr);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, relpos_bwd_shaw_final_kernel, p);
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * (2 * p.kc + 1)));
+    cfg.dynamicSmemBytes = 0;
+    return cudaLaunchKernelEx(&cfg, relpos_bwd_shaw_reduce_kernel, p, static_cast<int>(BH) * nqt);
   }
   const size_t n4 = static_cast<size_t>(BH) * p.Lq * kHeadDim / 4;
   cudaLaunchAttribute attr[1];
@@ -1146,6 +1498,7 @@ cudaError_t launch_bwd_mode(const CUtensorMap& tmQ, const CUtensorMap& tmK, cons
 }  // namespace
 
 int bwd_max_R() { return kMaxR; }
+int bwd_max_shaw_k() { return kMaxShawK; }
 
 cudaError_t launch_bwd(int mode, const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                        const CUtensorMap& tmdO, const CUtensorMap& tmAcc, const BwdParams& p,
@@ -1153,6 +1506,10 @@ cudaError_t launch_bwd(int mode, const CUtensorMap& tmQ, const CUtensorMap& tmK,
   if (mode == 0) {
     if (p.R < 1 || p.R > kMaxR || p.nb > kMaxT5Buckets) return cudaErrorInvalidValue;
     return launch_bwd_mode<0>(tmQ, tmK, tmV, tmdO, tmAcc, p, stream);
+  }
+  if (mode == 1) {
+    if (p.kc < 1 || p.kc > kMaxShawK || p.nr != 2 * p.kc + 2) return cudaErrorInvalidValue;
+    return launch_bwd_mode<1>(tmQ, tmK, tmV, tmdO, tmAcc, p, stream);
   }
   if (mode == 3) return launch_bwd_mode<3>(tmQ, tmK, tmV, tmdO, tmAcc, p, stream);
   return cudaErrorInvalidValue;

@@ -30,6 +30,21 @@ struct BwdParams {
   // ALiBi
   const float* slopes;  // [H]
   float* dslopes;       // [H], zeroed before the kernels
+  // Shaw (mode 1): per query row, with rows padded to lq_pad and nr floats
+  // per row (the 2k + 1 clipped offsets r, one spare)
+  const __nv_bfloat16* aK;  // [2k + 1, 64]
+  const __nv_bfloat16* aV;  // [2k + 1, 64]
+  int kc, nr;               // clip k, nr = 2k + 2
+  float* shT;               // [B*H, lq_pad, nr] q_i . a_K[r] * scale_log2 (statistics kernel)
+  float* shU;               // [B*H, lq_pad, nr] dO_i . a_V[r]
+  float* shEnds;            // [B*H, 4, lq_pad] T[0], T[2k], U[0], U[2k] of every row
+  float* shBP;              // [B*H, lq_pad, nr] sum of P_ij over the keys at clipped offset r
+  float* shBdS;             // [B*H, lq_pad, nr] sum of dS_ij over them
+  float* shPart;            // [query tiles * B*H, 2, 2k + 1, 64] per-tile partial da_K, da_V
+  float* daK;               // [2k + 1, 64] fp32, written
+  float* daV;               // [2k + 1, 64] fp32, written
+  const __nv_bfloat16* Qp;   // [B*H, Lq, 64] (Shaw: the final kernel's rows)
+  const __nv_bfloat16* dOp;  // [B*H, Lq, 64]
   float* lse;    // [B*H, lq_pad] row log-sum-exp of the log2-scaled logits (stats kernel)
   float* Dr;     // [B*H, lq_pad] D_i = sum_j P_ij dP_ij (stats kernel)
   int lq_pad;    // Lq rounded up to a multiple of 128 (whole query tiles)
@@ -40,9 +55,13 @@ struct BwdParams {
   int* status;
 };
 
-// mode 0 (T5) or 3 (ALiBi): the row-statistics kernel, the dK / dV kernel
-// (which also accumulates dQ and the bias gradient) and the dQ conversion;
-// bwd_max_R is the largest T5 saturation distance R they support
+// mode 0 (T5), 1 (Shaw) or 3 (ALiBi): the row-statistics kernel (Shaw: also
+// the per-row tables and the per-offset sums), the dK / dV kernel (which also
+// accumulates dQ and the T5 / ALiBi table gradient) and the dQ conversion
+// (Shaw: with the a_K term, then the table gradients); bwd_max_R is the
+// largest T5 saturation distance R they support, bwd_max_shaw_k the largest
+// Shaw clip
+int bwd_max_shaw_k();
 int bwd_max_R();
 // tmAcc: the fp32 dQ accumulator [B*H, Lq, 64] as 128-row x 32-column boxes
 // (128-byte swizzle), the target of the dQ tiles' bulk reductions
