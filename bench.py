@@ -47,7 +47,7 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from transformer_attention_relative_gb300.workloads import (MODE_ALIBI, MODE_DEBERTA,  # noqa: E402
+from transformer_attention_relative_gb300.workloads import (MODE_ALIBI, MODE_DEBERTA, MODE_SHAW,  # noqa: E402
                                                             MODE_NAMES, MODE_T5, MODE_TXL,
                                                             WORKLOADS, make_grad_output,
                                                             make_inputs)
@@ -196,7 +196,10 @@ class ClockSampler:
 def kernels_per_step(w, backward=False):
     """This library's kernels launched by one call (memsets not counted)."""
     if backward:
-        return 3  # row statistics, dK / dV (with dQ and the table gradient), dQ conversion
+        # row statistics, dK / dV (with dQ and the T5 / ALiBi table gradient),
+        # dQ conversion (Shaw: dQ with the a_K term and the table partials,
+        # then their sum)
+        return 4 if w.mode == MODE_SHAW else 3
     decode = w.mode == MODE_T5 and w.Lq <= 8
     n = 2 if decode else 1
     if w.mode in (MODE_DEBERTA, MODE_TXL):
@@ -331,8 +334,12 @@ class GpuRun:
                   for _ in range(nbuf)]
         dsets = [self.sets[b % self.nsets] for b in range(nbuf)]
         if self.nsets < nbuf:  # one resident set only (large inputs): add a second
-            d = {k: (v.to(self.device) if v is not None else None) for k, v in self.host.items()}
-            d["out"] = torch.empty_like(d["Q"])
+            d = {k: (torch.empty_like(v) if v is not None else None) for k, v in self.sets[0].items()}
+            for k, v in self.host.items():
+                if v is not None:
+                    d[k].copy_(v)
+            if "dQ" in d:  # the backward reads dQ back
+                d["out"] = d["dQ"]
             dsets[1] = d
         h2d = sum(v.numel() * v.element_size() for v in pinned.values() if v is not None)
         d2h = outs_h[0].numel() * outs_h[0].element_size()
@@ -380,9 +387,10 @@ class GpuRun:
 
 
 class BwdRun(GpuRun):
-    """The T5 (or ALiBi) backward on the same inputs plus a drawn output
-    gradient dO: one step is one relpos_t5_attn_bwd (relpos_alibi_attn_bwd)
-    call: dQ, dK, dV and the table (slope) gradient."""
+    """The T5, ALiBi or Shaw backward on the same inputs plus a drawn output
+    gradient dO: one step is one relpos_t5_attn_bwd (relpos_alibi_attn_bwd,
+    relpos_shaw_attn_bwd) call: dQ, dK, dV and the table (slope) gradients.
+    Its end-to-end steps copy dO in with the inputs and read dQ back."""
 
     def __init__(self, w, device, stream):
         import torch
@@ -391,18 +399,28 @@ class BwdRun(GpuRun):
         extra = 4 * dO.numel() * dO.element_size()  # dO, dQ, dK, dV
         self.nsets = max(1, min(16, math.ceil(2.5 * L2_BYTES / (self.set_bytes + extra))))
         self.sets = self.sets[:self.nsets]
+        self.host = dict(self.host, dO=dO)
         for d in self.sets:
             d["dO"] = dO.to(device)
             d["dQ"] = torch.empty_like(d["Q"])
+            d["out"] = d["dQ"]
             d["dK"] = torch.empty_like(d["K"])
             d["dV"] = torch.empty_like(d["V"])
-            d["dbias"] = torch.empty_like(d["table0"])
+            d["dbias"] = torch.empty_like(d["table0"], dtype=torch.float32)
+            if w.mode == MODE_SHAW:
+                d["dtab1"] = torch.empty_like(d["table1"], dtype=torch.float32)
         torch.cuda.synchronize()
 
     def _call(self, d, out=None):
         w = self.w
         p = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
-        if w.mode == MODE_ALIBI:
+        if w.mode == MODE_SHAW:
+            rc = self.rp.relpos_shaw_attn_bwd(p(d["Q"]), p(d["K"]), p(d["V"]), p(d["dO"]),
+                                              p(d["table0"]), p(d["table1"]), w.B, w.H, w.Lq, w.Lk, w.d,
+                                              w.rel_param, int(w.causal), w.q_offset, p(d["dQ"]),
+                                              p(d["dK"]), p(d["dV"]), p(d["dbias"]), p(d["dtab1"]),
+                                              self.sptr)
+        elif w.mode == MODE_ALIBI:
             rc = self.rp.relpos_alibi_attn_bwd(p(d["Q"]), p(d["K"]), p(d["V"]), p(d["dO"]),
                                                p(d["table0"]), w.B, w.H, w.Lq, w.Lk, w.d,
                                                int(w.causal), w.q_offset, p(d["dQ"]), p(d["dK"]),
@@ -576,7 +594,7 @@ def config_of(w, world, g, backward=False):
 BLOCK_WORKLOADS = ("t5_base_bidir", "t5_causal", "shaw", "deberta", "txl_mem", "t5_decode",
                    "t5_decode_evicted", "alibi_bidir", "alibi_causal", "alibi_d128", "t5_d128",
                    "t5_tiny_fp32")
-BACKWARD_WORKLOADS = ("t5_base_bidir", "t5_causal", "alibi_causal")
+BACKWARD_WORKLOADS = ("t5_base_bidir", "t5_causal", "alibi_causal", "shaw")
 
 
 def main():

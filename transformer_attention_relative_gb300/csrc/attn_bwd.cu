@@ -1273,16 +1273,17 @@ __global__ void relpos_bwd_dq_convert_kernel(const float4* __restrict__ acc, uin
 // dS K part + scale * sum_r BdS_i[r] a_K[r], to bf16; and the tile's partial
 // sums over its rows of BdS_i[r] q_i (da_K) and BP_i[r] dO_i (da_V).
 constexpr int kShThreads = 256;
-constexpr int kShQs = 65;  // padded row stride of the staged Q and dO rows (floats)
+constexpr int kShQs = 68;  // row stride of the staged Q and dO rows (floats; 16-byte aligned rows)
 
 __global__ void __launch_bounds__(kShThreads) relpos_bwd_shaw_final_kernel(const BwdParams p) {
-  extern __shared__ float shf[];
+  extern __shared__ float4 shf4[];
+  float* shf = reinterpret_cast<float*>(shf4);
   const int nrel = 2 * p.kc + 1, nr = p.nr;
-  float* aKf = shf;               // [2k + 1][64]
+  float* qf = shf;                // [128][kShQs]
+  float* of = qf + kBT * kShQs;   // [128][kShQs]
+  float* aKf = of + kBT * kShQs;  // [2k + 1][64]
   float* bds = aKf + nrel * 64;   // [128][nr]
-  float* bps = bds + 128 * nr;    // [128][nr]
-  float* qf = bps + 128 * nr;     // [128][kShQs]
-  float* of = qf + 128 * kShQs;   // [128][kShQs]
+  float* bps = bds + kBT * nr;    // [128][nr]
   const int tid = threadIdx.x;
   const int tile = blockIdx.x, bh = blockIdx.y, i0 = tile * kBT;
   const int rows = min(kBT, p.Lq - i0);
@@ -1302,56 +1303,76 @@ __global__ void __launch_bounds__(kShThreads) relpos_bwd_shaw_final_kernel(const
       uo = *reinterpret_cast<const uint4*>(p.dOp + off);
     }
     const uint32_t wq[4] = {uq.x, uq.y, uq.z, uq.w}, wo[4] = {uo.x, uo.y, uo.z, uo.w};
+    float fq[8], fo[8];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wq[k]));
       const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wo[k]));
-      qf[r * kShQs + ch * 8 + 2 * k] = a.x;
-      qf[r * kShQs + ch * 8 + 2 * k + 1] = a.y;
-      of[r * kShQs + ch * 8 + 2 * k] = b.x;
-      of[r * kShQs + ch * 8 + 2 * k + 1] = b.y;
+      fq[2 * k] = a.x;
+      fq[2 * k + 1] = a.y;
+      fo[2 * k] = b.x;
+      fo[2 * k + 1] = b.y;
     }
+    float4* dq4 = reinterpret_cast<float4*>(qf + r * kShQs + ch * 8);
+    float4* do4 = reinterpret_cast<float4*>(of + r * kShQs + ch * 8);
+    dq4[0] = make_float4(fq[0], fq[1], fq[2], fq[3]);
+    dq4[1] = make_float4(fq[4], fq[5], fq[6], fq[7]);
+    do4[0] = make_float4(fo[0], fo[1], fo[2], fo[3]);
+    do4[1] = make_float4(fo[4], fo[5], fo[6], fo[7]);
   }
   __syncthreads();
-  {  // dQ: a row and 32 columns per thread
-    const int r = tid >> 1, c0 = (tid & 1) * 32;
+  {  // dQ: a row per thread pair, columns 4 u + 8 v (u = the thread's half)
+    const int r = tid >> 1, u = tid & 1;
     if (r < rows) {
-      const size_t off = (static_cast<size_t>(bh) * p.Lq + i0 + r) * kHeadDim + c0;
-      float acc[32];
+      const size_t off = (static_cast<size_t>(bh) * p.Lq + i0 + r) * kHeadDim + 4 * u;
+      float4 acc[8];
 #pragma unroll
-      for (int v = 0; v < 8; ++v) {
-        const float4 a = *reinterpret_cast<const float4*>(p.dQacc + off + 4 * v);
-        acc[4 * v] = a.x;
-        acc[4 * v + 1] = a.y;
-        acc[4 * v + 2] = a.z;
-        acc[4 * v + 3] = a.w;
-      }
+      for (int v = 0; v < 8; ++v) acc[v] = *reinterpret_cast<const float4*>(p.dQacc + off + 8 * v);
 #pragma unroll 1
       for (int k = 0; k < nrel; ++k) {
         const float w = bds[r * nr + k] * p.scale;
+        const float4* a4 = reinterpret_cast<const float4*>(aKf + k * 64 + 4 * u);
 #pragma unroll
-        for (int c = 0; c < 32; ++c) acc[c] = fmaf(w, aKf[k * 64 + c0 + c], acc[c]);
+        for (int v = 0; v < 8; ++v) {
+          const float4 a = a4[2 * v];
+          acc[v] = make_float4(fmaf(w, a.x, acc[v].x), fmaf(w, a.y, acc[v].y), fmaf(w, a.z, acc[v].z),
+                               fmaf(w, a.w, acc[v].w));
+        }
       }
-      uint4* d4 = reinterpret_cast<uint4*>(p.dQ + off);
 #pragma unroll
-      for (int v = 0; v < 4; ++v)
-        d4[v] = make_uint4(pack_bf16x2(acc[8 * v], acc[8 * v + 1]), pack_bf16x2(acc[8 * v + 2], acc[8 * v + 3]),
-                           pack_bf16x2(acc[8 * v + 4], acc[8 * v + 5]), pack_bf16x2(acc[8 * v + 6], acc[8 * v + 7]));
+      for (int v = 0; v < 8; ++v)
+        *reinterpret_cast<uint2*>(p.dQ + off + 8 * v) =
+            make_uint2(pack_bf16x2(acc[v].x, acc[v].y), pack_bf16x2(acc[v].z, acc[v].w));
     }
   }
-  {  // the tile's partial table gradients: column c, offsets g, g + 4, ...
-    const int c = tid & 63, g = tid >> 6;
-    float* part = p.shPart + (static_cast<size_t>(bh) * gridDim.x + tile) * 2 * nrel * 64;
-#pragma unroll 1
-    for (int k = g; k < nrel; k += 4) {
-      float sk = 0.f, sv = 0.f;
-#pragma unroll 4
-      for (int r = 0; r < rows; ++r) {
-        sk = fmaf(bds[r * nr + k], qf[r * kShQs + c], sk);
-        sv = fmaf(bps[r * nr + k], of[r * kShQs + c], sv);
+  {  // the tile's partial table gradients: columns 4 c4 .. 4 c4 + 3 and the
+     // offsets kg, kg + 16, kg + 32 per thread
+    const int c4 = tid & 15, kg = tid >> 4;
+    float4 sk[3], sv[3];
+#pragma unroll
+    for (int m = 0; m < 3; ++m) sk[m] = sv[m] = make_float4(0.f, 0.f, 0.f, 0.f);
+    int kk[3];
+#pragma unroll
+    for (int m = 0; m < 3; ++m) kk[m] = min(kg + 16 * m, nrel - 1);  // clamped: read, not written
+#pragma unroll 2
+    for (int r = 0; r < rows; ++r) {
+      const float4 q = *reinterpret_cast<const float4*>(qf + r * kShQs + 4 * c4);
+      const float4 o = *reinterpret_cast<const float4*>(of + r * kShQs + 4 * c4);
+#pragma unroll
+      for (int m = 0; m < 3; ++m) {
+        const float a = bds[r * nr + kk[m]], b = bps[r * nr + kk[m]];
+        sk[m] = make_float4(fmaf(a, q.x, sk[m].x), fmaf(a, q.y, sk[m].y), fmaf(a, q.z, sk[m].z), fmaf(a, q.w, sk[m].w));
+        sv[m] = make_float4(fmaf(b, o.x, sv[m].x), fmaf(b, o.y, sv[m].y), fmaf(b, o.z, sv[m].z), fmaf(b, o.w, sv[m].w));
       }
-      part[k * 64 + c] = sk;
-      part[(nrel + k) * 64 + c] = sv;
+    }
+    float* part = p.shPart + (static_cast<size_t>(bh) * gridDim.x + tile) * 2 * nrel * 64;
+#pragma unroll
+    for (int m = 0; m < 3; ++m) {
+      const int k = kg + 16 * m;
+      if (k < nrel) {
+        *reinterpret_cast<float4*>(part + k * 64 + 4 * c4) = sk[m];
+        *reinterpret_cast<float4*>(part + (nrel + k) * 64 + 4 * c4) = sv[m];
+      }
     }
   }
 }
@@ -1366,14 +1387,16 @@ __global__ void __launch_bounds__(kShThreads) relpos_bwd_shaw_reduce_kernel(cons
   griddep_wait();
   const size_t stride = static_cast<size_t>(2) * nrel * 64;
   const float* src = p.shPart + static_cast<size_t>(row) * 64 + c;
-  float s0 = 0.f, s1 = 0.f;
+  float s[8];
+#pragma unroll
+  for (int u = 0; u < 8; ++u) s[u] = 0.f;
   int q = g;
-  for (; q + 4 < nparts; q += 8) {
-    s0 += src[static_cast<size_t>(q) * stride];
-    s1 += src[static_cast<size_t>(q + 4) * stride];
+  for (; q + 28 < nparts; q += 32) {
+#pragma unroll
+    for (int u = 0; u < 8; ++u) s[u] += src[static_cast<size_t>(q + 4 * u) * stride];
   }
-  if (q < nparts) s0 += src[static_cast<size_t>(q) * stride];
-  red[tid] = s0 + s1;
+  for (int u = 0; q < nparts; q += 4, ++u) s[u & 7] += src[static_cast<size_t>(q) * stride];
+  red[tid] = ((s[0] + s[1]) + (s[2] + s[3])) + ((s[4] + s[5]) + (s[6] + s[7]));
   __syncthreads();
   if (g == 0) {
     const float v = (red[c] + red[64 + c]) + (red[128 + c] + red[192 + c]);
@@ -1386,7 +1409,7 @@ __global__ void __launch_bounds__(kShThreads) relpos_bwd_shaw_reduce_kernel(cons
 
 uint32_t shaw_final_smem_bytes(int nr) {
   const uint32_t nrel = static_cast<uint32_t>(nr) - 1u;
-  return (nrel * 64u + 2u * kBT * static_cast<uint32_t>(nr) + 2u * kBT * kShQs) * 4u;
+  return (2u * kBT * kShQs + nrel * 64u + 2u * kBT * static_cast<uint32_t>(nr)) * 4u;
 }
 
 uint32_t stats_smem_bytes(int mode, int R, int nr) {
