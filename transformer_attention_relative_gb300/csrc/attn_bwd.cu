@@ -339,8 +339,6 @@ __global__ void __launch_bounds__(kStThreads, 1)
         dst[r] = val;
         g[r] = val;
       }
-      p.shEnds[(static_cast<size_t>(bh) * 4 + 2 * xx) * p.lq_pad + i0 + tt] = dst[0];
-      p.shEnds[(static_cast<size_t>(bh) * 4 + 2 * xx + 1) * p.lq_pad + i0 + tt] = dst[2 * p.kc];
       named_bar_sync(2, 256);
     }
     const int x = (warp - 4) >> 2;  // TMEM buffer / parity of the key tiles taken
@@ -499,26 +497,26 @@ __global__ void __launch_bounds__(kStThreads, 1)
         const float2 off2 = make_float2(off, off);
         if constexpr (MODE == 1) {
           if (fast) {
-            // beyond the clip: dP gains dO . a_V of the side; the tile's
-            // sums go to that side
+            // beyond the clip: dP gains dO . a_V of the side (added once,
+            // times the tile's sum of P); the tile's sums go to that side
             float2 tl = make_float2(0.f, 0.f), td = make_float2(0.f, 0.f);
-            const float2 ue2 = make_float2(ue, ue);
 #pragma unroll
             for (int c = 0; c < 64; c += 2) {
               float2 e = __ffma2_rn(make_float2(xv[c], xv[c + 1]), mul2, off2);
               e.x = ex2_approx(e.x);
               e.y = ex2_approx(e.y);
               tl = __fadd2_rn(tl, e);
-              td = __ffma2_rn(e, __fadd2_rn(make_float2(__uint_as_float(dr[c]), __uint_as_float(dr[c + 1])), ue2), td);
+              td = __ffma2_rn(e, make_float2(__uint_as_float(dr[c]), __uint_as_float(dr[c + 1])), td);
             }
-            l2 = __fadd2_rn(l2, tl);
-            d2 = __fadd2_rn(d2, td);
+            const float sl = tl.x + tl.y, sd = fmaf(ue, sl, td.x + td.y);
+            l2.x += sl;
+            d2.x += sd;
             if (far_l) {
-              sLl += tl.x + tl.y;
-              sLd += td.x + td.y;
+              sLl += sl;
+              sLd += sd;
             } else {
-              sRl += tl.x + tl.y;
-              sRd += td.x + td.y;
+              sRl += sl;
+              sRd += sd;
             }
           } else {
             // per element: in-band offsets into their (row, offset) entries
@@ -592,6 +590,13 @@ __global__ void __launch_bounds__(kStThreads, 1)
         const float* bd1 = shw + 64 * 64 + (5 * 128 + t) * p.nr;
         const size_t gr = (static_cast<size_t>(bh) * p.lq_pad + row) * p.nr;
         const int kc2 = 2 * p.kc;
+        // for the dK / dV kernel's tiles beyond the clip: lse - T and D - U
+        // of the two end offsets
+        float* ge = p.shEnds + static_cast<size_t>(bh) * 4 * p.lq_pad + row;
+        ge[0] = lse - Trow[0];
+        ge[p.lq_pad] = lse - Trow[kc2];
+        ge[2 * static_cast<size_t>(p.lq_pad)] = D - Urow[0];
+        ge[3 * static_cast<size_t>(p.lq_pad)] = D - Urow[kc2];
 #pragma unroll 1
         for (int r = 0; r <= kc2; ++r) {
           float sp, sd;
@@ -672,7 +677,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
   volatile int* abort_f = reinterpret_cast<volatile int*>(smem + kKvOffBar + kKvAbort);
   // T5: 4 copies of F (the reversed extended bias table); dS summed per
   // offset over the near tiles (entry = E index of the offset); per bucket
-  // Shaw: per ring stage, the query tile's T[0], T[2k], U[0], U[2k]
+  // Shaw: per ring stage, the query tile's lse - T and D - U of the two end
+  // offsets
   float* tab = reinterpret_cast<float*>(smem + kKvOffAux);
   float* hist = tab + (MODE == 0 ? 4 * tab_stride(R) : MODE == 1 ? 2 * 512 : 0);
   float* hist_b = hist + (MODE == 0 ? tab_len(R) : 0);
@@ -949,8 +955,9 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         // F index of offset o: R + kTabPad - o. Shaw beyond the clip: each
         // column's query takes its T and U of the side's end offset.
         const float bc = MODE == 0 ? (far_l ? tab[2 * R + kTabPad] : tab[kTabPad]) : 0.f;
-        const float* te = tab + (i & 1) * 512 + (far_l ? 0 : 128) + hf * 64;  // Shaw
-        const float* ue = te + 256;
+        // Shaw: lse - T and D - U of the side's end offset stand for lse and D
+        const float* lse_f = MODE == 1 ? tab + (i & 1) * 512 + (far_l ? 0 : 128) + hf * 64 : lse_s;
+        const float* dd_f = MODE == 1 ? lse_f + 256 : dd_s;
         const float g = MODE == 0 ? 0.f : (rel_hi <= 0 ? -alibi : alibi);
         const float2 g2 = make_float2(g, g);
         const float nrb = -static_cast<float>(rb);
@@ -961,17 +968,10 @@ __global__ void __launch_bounds__(kKvThreads, 1)
 #pragma unroll
           for (int qq = 0; qq < 4; ++qq) {
             const int q = 4 * gi + qq;
-            const float4 L = *reinterpret_cast<const float4*>(lse_s + 4 * q);
-            float4 D = *reinterpret_cast<const float4*>(dd_s + 4 * q);
+            const float4 L = *reinterpret_cast<const float4*>(lse_f + 4 * q);
+            const float4 D = *reinterpret_cast<const float4*>(dd_f + 4 * q);
             float2 off0 = make_float2(bc - L.x, bc - L.y), off1 = make_float2(bc - L.z, bc - L.w);
             float2 cm0 = make_float2(0.f, 0.f), cm1 = make_float2(0.f, 0.f);
-            if constexpr (MODE == 1) {  // logit + T, dP + U: D - U stands for D
-              const float4 T4 = *reinterpret_cast<const float4*>(te + 4 * q);
-              const float4 U4 = *reinterpret_cast<const float4*>(ue + 4 * q);
-              off0 = __fadd2_rn(off0, make_float2(T4.x, T4.y));
-              off1 = __fadd2_rn(off1, make_float2(T4.z, T4.w));
-              D = make_float4(D.x - U4.x, D.y - U4.y, D.z - U4.z, D.w - U4.w);
-            }
             if constexpr (MODE == 3) {
               cm0 = __fadd2_rn(make_float2(static_cast<float>(4 * q), static_cast<float>(4 * q + 1)),
                                make_float2(nrb, nrb));
