@@ -171,16 +171,20 @@ RP_DEVI float dot64_bf16(const float (&v)[64], const __nv_bfloat16* row) {
 // 12 warps: 0 TMA producer, 1 MMA issuer (TMEM owner), 2-3 idle, 4-7 and 8-11
 // the compute warpgroups of TMEM buffers 0 and 1 (even / odd key tiles).
 constexpr int kStThreads = 384;
-constexpr uint32_t kStOffQ = 0, kStOffdO = kTile, kStOffRing = 2 * kTile;  // ring: 2 x (K, V)
-constexpr uint32_t kStOffBar = kStOffRing + 4 * kTile;
-constexpr uint32_t kStOffAux = kStOffBar + 256;
-enum : uint32_t {
-  kStBarQ = 0,
-  kStBarFull = 1,   // + stage
-  kStBarEmpty = 3,  // + stage
-  kStBarS = 5,      // + buffer
-  kStBarSFree = 7,  // + buffer
-  kStNumBars = 9,
+constexpr uint32_t kStOffQ = 0, kStOffdO = kTile, kStOffRing = 2 * kTile;  // ring: stages x (K, V)
+// the ring's depth (4 stages; Shaw, whose tables fill shared memory, 2), the
+// barriers and the shared-memory offsets that follow from it
+template <int MODE>
+struct StLayout {
+  static constexpr int kStages = MODE == 1 ? 2 : 4;
+  static constexpr uint32_t kOffBar = kStOffRing + kStages * 2 * kTile;
+  static constexpr uint32_t kOffAux = kOffBar + 256;
+  static constexpr uint32_t kBarQ = 0;
+  static constexpr uint32_t kBarFull = 1;                 // + stage
+  static constexpr uint32_t kBarEmpty = 1 + kStages;      // + stage
+  static constexpr uint32_t kBarS = 1 + 2 * kStages;      // + buffer
+  static constexpr uint32_t kBarSFree = 3 + 2 * kStages;  // + buffer
+  static constexpr uint32_t kNumBars = 5 + 2 * kStages;
 };
 constexpr uint32_t kStSlot = 128, kStAbort = 132;
 
@@ -189,6 +193,8 @@ __global__ void __launch_bounds__(kStThreads, 1)
     relpos_bwd_stats_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                             const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                             const BwdParams p) {
+  using L = StLayout<MODE>;
+  constexpr int S = L::kStages;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sb = (raw + 1023u) & ~1023u;
@@ -196,9 +202,9 @@ __global__ void __launch_bounds__(kStThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int bh = blockIdx.y, h = bh % p.H;
   const int i0 = blockIdx.x * kBT;
-  auto bar = [&](uint32_t i) { return sb + kStOffBar + 8u * i; };
-  volatile int* abort_f = reinterpret_cast<volatile int*>(smem + kStOffBar + kStAbort);
-  float* tab = reinterpret_cast<float*>(smem + kStOffAux);                 // T5: 4 copies of E
+  auto bar = [&](uint32_t i) { return sb + L::kOffBar + 8u * i; };
+  volatile int* abort_f = reinterpret_cast<volatile int*>(smem + L::kOffBar + kStAbort);
+  float* tab = reinterpret_cast<float*>(smem + L::kOffAux);                 // T5: 4 copies of E
   // Shaw: a_K, a_V (bf16, 64 rows of 64), then per row q . a_K and dO . a_V
   // (nr floats), then each warpgroup's sums per clipped offset of P and P dP
   float* shw = tab + (MODE == 0 ? 4 * tab_stride(p.R) : 0);
@@ -210,19 +216,19 @@ __global__ void __launch_bounds__(kStThreads, 1)
   if (p.causal) n_kv = min(n_kv, (last_row + p.q_offset) / kBT + 1);
 
   if (tid == 0) {
-    for (uint32_t i = 0; i < kStNumBars; ++i)
-      mbar_init(bar(i), (i == kStBarSFree || i == kStBarSFree + 1) ? 128u : 1u);
+    for (uint32_t i = 0; i < L::kNumBars; ++i)
+      mbar_init(bar(i), (i == L::kBarSFree || i == L::kBarSFree + 1) ? 128u : 1u);
     *abort_f = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(sb + kStOffBar + kStSlot, 512);
+    tmem_alloc(sb + L::kOffBar + kStSlot, 512);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kStOffBar + kStSlot);
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::kOffBar + kStSlot);
   griddep_wait();
 
   // registers: the loading and issuing warps need few, the compute
@@ -238,15 +244,15 @@ __global__ void __launch_bounds__(kStThreads, 1)
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       tma_prefetch_desc(&tmdO);
-      mbar_arrive_expect_tx(bar(kStBarQ), 2 * kTile);
-      tma_load_3d(sb + kStOffQ, &tmQ, bar(kStBarQ), 0, i0, bh);
-      tma_load_3d(sb + kStOffdO, &tmdO, bar(kStBarQ), 0, i0, bh);
+      mbar_arrive_expect_tx(bar(L::kBarQ), 2 * kTile);
+      tma_load_3d(sb + kStOffQ, &tmQ, bar(L::kBarQ), 0, i0, bh);
+      tma_load_3d(sb + kStOffdO, &tmdO, bar(L::kBarQ), 0, i0, bh);
       for (int j = 0; j < n_kv; ++j) {
-        const uint32_t st = j & 1;
-        if (j >= 2 && !(ok = mbar_wait(bar(kStBarEmpty + st), ((j >> 1) - 1) & 1))) break;
-        mbar_arrive_expect_tx(bar(kStBarFull + st), 2 * kTile);
-        tma_load_3d(sb + kStOffRing + st * 2 * kTile, &tmK, bar(kStBarFull + st), 0, j * kBT, bh);
-        tma_load_3d(sb + kStOffRing + st * 2 * kTile + kTile, &tmV, bar(kStBarFull + st), 0, j * kBT, bh);
+        const uint32_t st = j % S;
+        if (j >= S && !(ok = mbar_wait(bar(L::kBarEmpty + st), ((j / S) - 1) & 1))) break;
+        mbar_arrive_expect_tx(bar(L::kBarFull + st), 2 * kTile);
+        tma_load_3d(sb + kStOffRing + st * 2 * kTile, &tmK, bar(L::kBarFull + st), 0, j * kBT, bh);
+        tma_load_3d(sb + kStOffRing + st * 2 * kTile + kTile, &tmV, bar(L::kBarFull + st), 0, j * kBT, bh);
         ++issued;
       }
       if (!ok) {
@@ -254,19 +260,19 @@ __global__ void __launch_bounds__(kStThreads, 1)
         bwd_error(p.status);
       }
       // never leave with copies in flight
-      mbar_wait(bar(kStBarQ), 0, 100000000ull);
-      for (int j = issued > 2 ? issued - 2 : 0; j < issued; ++j)
-        mbar_wait(bar(kStBarFull + (j & 1)), (j >> 1) & 1, 100000000ull);
+      mbar_wait(bar(L::kBarQ), 0, 100000000ull);
+      for (int j = issued > S ? issued - S : 0; j < issued; ++j)
+        mbar_wait(bar(L::kBarFull + (j % S)), (j / S) & 1, 100000000ull);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
-    bool ok = mbar_wait_warp(bar(kStBarQ), 0);
+    bool ok = mbar_wait_warp(bar(L::kBarQ), 0);
     const uint64_t dq = smem_desc_sw128(sb + kStOffQ, 16, 1024);
     const uint64_t ddo = smem_desc_sw128(sb + kStOffdO, 16, 1024);
     for (int j = 0; ok && j < n_kv; ++j) {
-      const uint32_t st = j & 1, x = j & 1;
-      ok = mbar_wait_warp(bar(kStBarFull + st), (j >> 1) & 1);
-      if (ok && j >= 2) ok = mbar_wait_warp(bar(kStBarSFree + x), ((j >> 1) - 1) & 1);
+      const uint32_t st = j % S, x = j & 1;
+      ok = mbar_wait_warp(bar(L::kBarFull + st), (j / S) & 1);
+      if (ok && j >= 2) ok = mbar_wait_warp(bar(L::kBarSFree + x), ((j >> 1) - 1) & 1);
       if (!ok || __any_sync(0xffffffffu, *abort_f != 0)) break;
       tc_fence_after();
       const uint64_t dk = smem_desc_sw128(sb + kStOffRing + st * 2 * kTile, 16, 1024);
@@ -277,8 +283,8 @@ __global__ void __launch_bounds__(kStThreads, 1)
 #pragma unroll
       for (int kk = 0; kk < kHeadDim / 16; ++kk)
         umma_bf16_ss_elect(tmem + x * 256 + 128, ddo + 2 * kk, dv + 2 * kk, kIdS128, kk > 0 ? 1u : 0u);
-      tc_commit_elect(bar(kStBarS + x));
-      tc_commit_elect(bar(kStBarEmpty + st));
+      tc_commit_elect(bar(L::kBarS + x));
+      tc_commit_elect(bar(L::kBarEmpty + st));
     }
     if (!ok && lane == 0) {
       *abort_f = 1;
@@ -312,7 +318,7 @@ __global__ void __launch_bounds__(kStThreads, 1)
       }
       float* bins0 = shw + 64 * 64 + 2 * 128 * p.nr;
       for (int i = ct; i < 4 * 128 * p.nr; i += 256) bins0[i] = 0.f;
-      if (!mbar_wait(bar(kStBarQ), 0)) *abort_f = 1;  // the Q and dO tiles
+      if (!mbar_wait(bar(L::kBarQ), 0)) *abort_f = 1;  // the Q and dO tiles
       named_bar_sync(2, 256);
       const int xx = (warp - 4) >> 2, tt = ((warp & 3) << 5) | lane;
       const uint8_t* tile = smem + (xx == 0 ? kStOffQ : kStOffdO);
@@ -367,7 +373,7 @@ __global__ void __launch_bounds__(kStThreads, 1)
     float* bd_row = MODE == 1 ? shw + 64 * 64 + (4 * 128 + x * 128 + t) * p.nr : nullptr;
     float sLl = 0.f, sRl = 0.f, sLd = 0.f, sRd = 0.f;
     for (int j = x; j < n_kv; j += 2, ++cnt) {
-      const bool ok = mbar_wait(bar(kStBarS + x), cnt & 1);
+      const bool ok = mbar_wait(bar(L::kBarS + x), cnt & 1);
       err = __any_sync(0xffffffffu, !ok);
       // leave together: the TMEM loads below are warp-collective
       if (err || __any_sync(0xffffffffu, *abort_f != 0)) break;
@@ -398,7 +404,7 @@ __global__ void __launch_bounds__(kStThreads, 1)
         tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(&dr[32]));
         if (c0 + 64 == kBT) {  // the buffer is read: the products of tile j + 2 may overwrite it
           tc_fence_before();
-          mbar_arrive(bar(kStBarSFree + x));
+          mbar_arrive(bar(L::kBarSFree + x));
         }
         float* xv = reinterpret_cast<float*>(sr);
         float bc = 0.f;  // the row constant of a fast tile (log2 units)
@@ -1415,7 +1421,8 @@ uint32_t shaw_final_smem_bytes(int nr) {
 uint32_t stats_smem_bytes(int mode, int R, int nr) {
   const uint32_t tab = mode == 0 ? 4u * static_cast<uint32_t>(tab_stride(R)) * 4u : 0u;
   const uint32_t shaw = mode == 1 ? (64u * 64u + 6u * 128u * static_cast<uint32_t>(nr)) * 4u : 0u;
-  return 1024u + kStOffAux + tab + shaw + (7u * 128u + kMaxT5Buckets) * 4u;
+  const uint32_t aux = mode == 1 ? StLayout<1>::kOffAux : StLayout<0>::kOffAux;
+  return 1024u + aux + tab + shaw + (7u * 128u + kMaxT5Buckets) * 4u;
 }
 
 // T5: four bias-table copies, the per-offset sums, the compute warps'
