@@ -464,9 +464,7 @@ __global__ void __launch_bounds__(kStThreads, 1)
             if constexpr (MODE == 0) {
               b = tab[min(max(rel + R + kTabPad, 0), tab_len(R) - 1)];
             } else if constexpr (MODE == 1) {
-              const int r = min(max(rel, -p.kc), p.kc) + p.kc;
-              b = Trow[r];
-              dr[c] = __float_as_uint(__uint_as_float(dr[c]) + Urow[r]);
+              b = Trow[min(max(rel, -p.kc), p.kc) + p.kc];  // (U joins dP in the exponential loop)
             } else {
               b = -alibi * fabsf(static_cast<float>(rel));
             }
@@ -530,13 +528,14 @@ __global__ void __launch_bounds__(kStThreads, 1)
             const uint32_t bp_a = smem_u32(bp_row), bd_a = smem_u32(bd_row);
 #pragma unroll
             for (int c = 0; c < 64; ++c) {
+              const int rel = j0 + c0 + c - prow;
+              const int ri = min(max(rel, -p.kc), p.kc) + p.kc;
               const float e = ex2_approx(xv[c] - mu);
-              const float dd = e * __uint_as_float(dr[c]);
+              const float dd = e * (__uint_as_float(dr[c]) + Urow[ri]);
               l2.x += e;
               d2.x += dd;
-              const int rel = j0 + c0 + c - prow;
               const int inb = (rel > -p.kc) & (rel < p.kc);
-              const uint32_t ra = 4u * static_cast<uint32_t>(min(max(rel, -p.kc), p.kc) + p.kc);
+              const uint32_t ra = 4u * static_cast<uint32_t>(ri);
               st_shared_f32_if(bp_a + ra, e, inb);
               st_shared_f32_if(bd_a + ra, dd, inb);
               sLl += rel <= -p.kc ? e : 0.f;
