@@ -199,7 +199,9 @@ def kernels_per_step(w, backward=False):
         # row statistics, dK / dV (with dQ and the T5 / ALiBi table gradient),
         # dQ conversion (Shaw: dQ with the a_K term and the table partials,
         # then their sum)
-        return 4 if w.mode == MODE_SHAW else 3
+        # (DeBERTa: the band pre-pass, statistics, dK / dV, the far-sum fold
+        # and the dQ, dK conversions; its table products run in cuBLAS)
+        return 4 if w.mode == MODE_SHAW else 6 if w.mode == MODE_DEBERTA else 3
     decode = w.mode == MODE_T5 and w.Lq <= 8
     n = 2 if decode else 1
     if w.mode in (MODE_DEBERTA, MODE_TXL):
@@ -407,14 +409,20 @@ class BwdRun(GpuRun):
             d["dK"] = torch.empty_like(d["K"])
             d["dV"] = torch.empty_like(d["V"])
             d["dbias"] = torch.empty_like(d["table0"], dtype=torch.float32)
-            if w.mode == MODE_SHAW:
+            if w.mode in (MODE_SHAW, MODE_DEBERTA):
                 d["dtab1"] = torch.empty_like(d["table1"], dtype=torch.float32)
         torch.cuda.synchronize()
 
     def _call(self, d, out=None):
         w = self.w
         p = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
-        if w.mode == MODE_SHAW:
+        if w.mode == MODE_DEBERTA:
+            rc = self.rp.relpos_deberta_attn_bwd(p(d["Q"]), p(d["K"]), p(d["V"]), p(d["dO"]),
+                                                 p(d["table0"]), p(d["table1"]), w.B, w.H, w.Lq, w.Lk, w.d,
+                                                 w.rel_param, int(w.causal), w.q_offset, p(d["dQ"]),
+                                                 p(d["dK"]), p(d["dV"]), p(d["dbias"]), p(d["dtab1"]),
+                                                 self.sptr)
+        elif w.mode == MODE_SHAW:
             rc = self.rp.relpos_shaw_attn_bwd(p(d["Q"]), p(d["K"]), p(d["V"]), p(d["dO"]),
                                               p(d["table0"]), p(d["table1"]), w.B, w.H, w.Lq, w.Lk, w.d,
                                               w.rel_param, int(w.causal), w.q_offset, p(d["dQ"]),
@@ -436,10 +444,11 @@ class BwdRun(GpuRun):
 
 
 def bwd_flops(w):
-    """Algorithmic flops of the T5 / ALiBi backward: the four gradient products
-    (dV = P^T dO, dP = dO V^T, dQ = dS K, dK = dS^T Q) over the visible
-    (query, key) pairs, twice the forward's two products; the kernels'
-    extra recomputations of S and dP are not counted."""
+    """Algorithmic flops of the backward: twice the forward's products, i.e.
+    the four gradient products (dV = P^T dO, dP = dO V^T, dQ = dS K,
+    dK = dS^T Q) over the visible (query, key) pairs, plus for Shaw and
+    DeBERTa the table terms' products; the kernels' extra recomputations of
+    S and dP (and DeBERTa's band pre-pass) are not counted."""
     return 2.0 * w.flops()
 
 
@@ -594,7 +603,7 @@ def config_of(w, world, g, backward=False):
 BLOCK_WORKLOADS = ("t5_base_bidir", "t5_causal", "shaw", "deberta", "txl_mem", "t5_decode",
                    "t5_decode_evicted", "alibi_bidir", "alibi_causal", "alibi_d128", "t5_d128",
                    "t5_tiny_fp32")
-BACKWARD_WORKLOADS = ("t5_base_bidir", "t5_causal", "alibi_causal", "shaw")
+BACKWARD_WORKLOADS = ("t5_base_bidir", "t5_causal", "alibi_causal", "shaw", "deberta")
 
 
 def main():

@@ -1,9 +1,9 @@
 /*
  * relpos_attn.h -- C ABI of the GB300 (sm_103a) relative-position attention
  * library (librelpos_attn.so): the forward pass (also over right-padded
- * batches), the T5 cached decode and the T5, Shaw and ALiBi backward passes
- * (relpos_t5_attn_bwd, relpos_shaw_attn_bwd, relpos_alibi_attn_bwd, at the
- * end of this header).
+ * batches), the T5 cached decode and the T5, Shaw, DeBERTa and ALiBi
+ * backward passes (relpos_t5_attn_bwd, relpos_shaw_attn_bwd,
+ * relpos_deberta_attn_bwd, relpos_alibi_attn_bwd, at the end of this header).
  *
  * One forward call computes multi-head attention whose logits carry a relative-
  * position term that is formed inside the kernel and never written to
@@ -350,6 +350,40 @@ int relpos_shaw_attn_bwd(const void* Q, const void* K, const void* V, const void
                          const void* aK, const void* aV, int B, int H, int Lq, int Lk, int d,
                          int clip_k, int causal, int q_offset, void* dQ, void* dK, void* dV,
                          void* daK, void* daV, void* stream);
+
+/*
+ * relpos_deberta_attn_bwd -- gradients of the DeBERTa attention forward
+ * (relpos_attn_fwd with mode RELPOS_DEBERTA, dtype RELPOS_BF16; "Relative
+ * Position Embeddings, in depth", section "DeBERTa: disentangled content and
+ * position"; "DeBERTa > Relative Position", the relative-position formula).
+ * With delta(i, j) = clip(p_i - j, -k, k - 1) + k and s = 1 / sqrt(3 d) the
+ * logit is s (q_i . k_j + q_i . Pk[delta(i, j), h] + k_j . Pq[delta(j, i), h]);
+ * the chain rule gives, with dS as for relpos_t5_attn_bwd,
+ *   dQ_i = s sum_j dS_ij (k_j + Pk[delta(i, j), h]),
+ *   dK_j = s sum_i dS_ij (q_i + Pq[delta(j, i), h]),  dV = P^T dO,
+ *   dPk[r, h] = s sum of dS_ij q_i over every (batch, i, j) of head h with
+ *   delta(i, j) = r, and dPq[r, h] = s sum of dS_ij k_j over delta(j, i) = r.
+ *
+ *   Q, K, V, dO, B, H, Lq, Lk, d, causal, q_offset, dQ, dK, dV, stream: as for
+ *               relpos_t5_attn_bwd.
+ *   Pk, Pq      device, bf16 [2k, H, 64]: the forward call's tables.
+ *   k           the forward call's rel_param; 1 <= k <= 4096
+ *               (RELPOS_ERR_INVALID_ARG below 1, RELPOS_ERR_UNSUPPORTED above).
+ *   dPk, dPq    device, fp32 [2k, H, 64], overwritten with the sums over the
+ *               batch.
+ * The logits' relative part comes from the forward's band pre-pass (c2p +
+ * p2c inside the band, rounded to bf16 as in the forward). Scratch, from
+ * cudaMallocAsync on `stream` and freed before the call returns: about
+ * (300 + 8k) * B * H * Lq bytes plus (280 + 4k) * B * H * Lk bytes (the
+ * band, dS gathered by table row query- and key-major, fp32 dQ and dK).
+ * The table products run as cuBLAS GEMMs (bf16 operands, fp32 accumulation;
+ * the library is loaded with this one). Errors and asynchrony as
+ * relpos_t5_attn_bwd.
+ */
+int relpos_deberta_attn_bwd(const void* Q, const void* K, const void* V, const void* dO,
+                            const void* Pk, const void* Pq, int B, int H, int Lq, int Lk, int d, int k,
+                            int causal, int q_offset, void* dQ, void* dK, void* dV, void* dPk, void* dPq,
+                            void* stream);
 
 #ifdef __cplusplus
 }

@@ -161,3 +161,29 @@ def test_shaw_backward_argument_errors_before_launch(lib, kw, code):
 
 def test_shaw_backward_empty_batch_is_noop(lib):
     assert _shaw_bwd(B=0, Q=0, K=0, V=0, dO=0, aK=0, aV=0, dQ=0, dK=0, dV=0, daK=0, daV=0) == rp.RELPOS_OK
+
+
+def _deberta_bwd(**kw):
+    a = dict(Q=16, K=32, V=48, dO=80, Pk=96, Pq=112, B=1, H=1, Lq=4, Lk=4, d=64, k=8,
+             causal=0, qoff=0, dQ=128, dK=144, dV=160, dPk=176, dPq=192, stream=None)
+    a.update(kw)
+    v = lambda x: ctypes.c_void_p(x) if x else None  # noqa: E731
+    return rp.relpos_deberta_attn_bwd(v(a["Q"]), v(a["K"]), v(a["V"]), v(a["dO"]), v(a["Pk"]), v(a["Pq"]),
+                                      a["B"], a["H"], a["Lq"], a["Lk"], a["d"], a["k"], a["causal"],
+                                      a["qoff"], v(a["dQ"]), v(a["dK"]), v(a["dV"]), v(a["dPk"]),
+                                      v(a["dPq"]), a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(Lq=-1), rp.RELPOS_ERR_INVALID_ARG),
+    (dict(k=0), rp.RELPOS_ERR_INVALID_ARG),
+    (dict(k=4097), rp.RELPOS_ERR_UNSUPPORTED),
+    (dict(d=128), rp.RELPOS_ERR_UNSUPPORTED),
+    (dict(Pq=0), rp.RELPOS_ERR_INVALID_ARG),
+    (dict(dPq=0), rp.RELPOS_ERR_INVALID_ARG),
+    (dict(dPk=176 + 4), rp.RELPOS_ERR_INVALID_ARG),
+    (dict(K=32 + 2), rp.RELPOS_ERR_INVALID_ARG),
+    (dict(B=300, H=300), rp.RELPOS_ERR_UNSUPPORTED),
+])
+def test_deberta_backward_argument_errors_before_launch(lib, kw, code):
+    assert _deberta_bwd(**kw) == code

@@ -28,7 +28,7 @@ RELPOS_ERR_SCRATCH_LIMIT = -5
 
 EXPORTED = ("relpos_attn_fwd", "relpos_attn_fwd_padded", "relpos_index_ids", "relpos_check_status", "relpos_strerror",
             "relpos_selftest_wait_timeout", "relpos_t5_decode_noalloc", "relpos_t5_decode_positions",
-            "relpos_t5_attn_bwd", "relpos_alibi_attn_bwd", "relpos_shaw_attn_bwd")
+            "relpos_t5_attn_bwd", "relpos_alibi_attn_bwd", "relpos_shaw_attn_bwd", "relpos_deberta_attn_bwd")
 
 _lib = None
 
@@ -71,6 +71,8 @@ def load_library(path: str = LIB_PATH):
     lib.relpos_alibi_attn_bwd.restype = i
     lib.relpos_shaw_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, vp, vp, vp, vp, vp, vp]
     lib.relpos_shaw_attn_bwd.restype = i
+    lib.relpos_deberta_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, vp, vp, vp, vp, vp, vp]
+    lib.relpos_deberta_attn_bwd.restype = i
     _lib = lib
     return lib
 
@@ -144,6 +146,13 @@ def relpos_shaw_attn_bwd(Q, K, V, dO, aK, aV, B, H, Lq, Lk, d, clip_k, causal, q
     """Gradients of the Shaw attention: dQ, dK, dV and those of a_K and a_V."""
     return load_library().relpos_shaw_attn_bwd(Q, K, V, dO, aK, aV, B, H, Lq, Lk, d, clip_k, causal,
                                                q_offset, dQ, dK, dV, daK, daV, stream)
+
+
+def relpos_deberta_attn_bwd(Q, K, V, dO, Pk, Pq, B, H, Lq, Lk, d, k, causal, q_offset, dQ, dK, dV,
+                            dPk, dPq, stream) -> int:
+    """Gradients of the DeBERTa attention: dQ, dK, dV and those of Pk and Pq."""
+    return load_library().relpos_deberta_attn_bwd(Q, K, V, dO, Pk, Pq, B, H, Lq, Lk, d, k, causal,
+                                                  q_offset, dQ, dK, dV, dPk, dPq, stream)
 
 
 strerror = relpos_strerror
@@ -320,3 +329,29 @@ def shaw_attention_backward(Q, K, V, dO, aK, aV, *, clip_k: int = 16, causal: bo
     if rc != RELPOS_OK:
         raise RelposError(rc, "relpos_shaw_attn_bwd")
     return dQ, dK, dV, daK, daV
+
+
+def deberta_attention_backward(Q, K, V, dO, Pk, Pq, *, k: int = 256, causal: bool = False,
+                               q_offset: int = 0, stream=None):
+    """Run ``relpos_deberta_attn_bwd`` on CUDA tensors; returns (dQ, dK, dV, dPk, dPq).
+
+    Q, dO [B,H,Lq,64] and K, V [B,H,Lk,64] bf16; Pk, Pq [2k, H, 64] bf16. dPk and dPq come back fp32,
+    summed over the batch.
+    """
+    import torch
+    B, H, Lq, d = Q.shape
+    Lk = K.shape[2]
+    for t in (Q, K, V, dO, Pk, Pq):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("tensors must be contiguous CUDA tensors")
+    if any(t.dtype != torch.bfloat16 for t in (Q, K, V, dO, Pk, Pq)):
+        raise TypeError("Q, K, V, dO, Pk, Pq must be bf16")
+    dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
+    dPk = torch.empty(Pk.shape, dtype=torch.float32, device=Pk.device)
+    dPq = torch.empty(Pq.shape, dtype=torch.float32, device=Pq.device)
+    rc = relpos_deberta_attn_bwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(dO), _ptr(Pk), _ptr(Pq), B, H, Lq, Lk, d,
+                                 k, int(causal), q_offset, _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(dPk),
+                                 _ptr(dPq), _stream(stream))
+    if rc != RELPOS_OK:
+        raise RelposError(rc, "relpos_deberta_attn_bwd")
+    return dQ, dK, dV, dPk, dPq

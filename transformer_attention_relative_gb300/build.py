@@ -56,7 +56,7 @@ def build(verbose: bool = False, extra_flags=None) -> str:
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed for {cmd[-3]}")
     tmp = LIB_PATH + ".tmp"
-    link = [nvcc, *ARCH, "-shared", "-o", tmp, *[j[1] for j in jobs], "-lcudart"]
+    link = [nvcc, *ARCH, "-shared", "-o", tmp, *[j[1] for j in jobs], "-lcudart", "-lcublas"]
     r = subprocess.run(link, capture_output=True, text=True)
     if r.returncode != 0:
         sys.stderr.write(" ".join(link) + "\n" + r.stdout + r.stderr)

@@ -578,6 +578,8 @@ namespace {
 
 // relpos_t5_attn_bwd (mode 0: table = bias [nb, H], dtable = dbias),
 // relpos_shaw_attn_bwd (mode 1: table / table1 = a_K / a_V [2k + 1, 64] bf16,
+// dtable / dtable1 = their fp32 gradients, max_distance = k),
+// relpos_deberta_attn_bwd (mode 2: table / table1 = Pk / Pq [2k, H, 64] bf16,
 // dtable / dtable1 = their fp32 gradients, max_distance = k) and
 // relpos_alibi_attn_bwd (mode 3: table = slopes [H], dtable = dslopes).
 int attn_bwd_impl(int mode, const void* Q, const void* K, const void* V, const void* dO,
@@ -589,9 +591,11 @@ int attn_bwd_impl(int mode, const void* Q, const void* K, const void* V, const v
   if (rc != RELPOS_OK) return rc;
   if (d != kHeadDim) return RELPOS_ERR_UNSUPPORTED;
   if (mode == RELPOS_SHAW && max_distance > bwd_max_shaw_k()) return RELPOS_ERR_UNSUPPORTED;
+  if (mode == RELPOS_DEBERTA && max_distance > 4096) return RELPOS_ERR_UNSUPPORTED;
   if (B == 0 || H == 0) return RELPOS_OK;
   if (!table || !dtable || !aligned16(table) || !aligned16(dtable)) return RELPOS_ERR_INVALID_ARG;
-  if (mode == RELPOS_SHAW && (!table1 || !dtable1 || !aligned16(table1) || !aligned16(dtable1)))
+  if ((mode == RELPOS_SHAW || mode == RELPOS_DEBERTA) &&
+      (!table1 || !dtable1 || !aligned16(table1) || !aligned16(dtable1)))
     return RELPOS_ERR_INVALID_ARG;
   if (static_cast<long long>(B) * H > 65535) return RELPOS_ERR_UNSUPPORTED;
   if (Lq > (1 << 24) || Lk > (1 << 24) || q_offset > (1 << 28)) return RELPOS_ERR_UNSUPPORTED;
@@ -617,12 +621,14 @@ int attn_bwd_impl(int mode, const void* Q, const void* K, const void* V, const v
   const size_t BH = static_cast<size_t>(B) * H;
   const size_t row_bytes = kHeadDim * 2;
   const size_t dtable_bytes =
-      (mode == RELPOS_T5     ? static_cast<size_t>(num_buckets) * H
-       : mode == RELPOS_SHAW ? static_cast<size_t>(2 * max_distance + 1) * kHeadDim
-                             : static_cast<size_t>(H)) *
+      (mode == RELPOS_T5        ? static_cast<size_t>(num_buckets) * H
+       : mode == RELPOS_SHAW    ? static_cast<size_t>(2 * max_distance + 1) * kHeadDim
+       : mode == RELPOS_DEBERTA ? static_cast<size_t>(2 * max_distance) * H * kHeadDim
+                                : static_cast<size_t>(H)) *
       sizeof(float);
   if (cudaMemsetAsync(dtable, 0, dtable_bytes, s) != cudaSuccess) return RELPOS_ERR_CUDA;
-  if (mode == RELPOS_SHAW && cudaMemsetAsync(dtable1, 0, dtable_bytes, s) != cudaSuccess) return RELPOS_ERR_CUDA;
+  if ((mode == RELPOS_SHAW || mode == RELPOS_DEBERTA) && cudaMemsetAsync(dtable1, 0, dtable_bytes, s) != cudaSuccess)
+    return RELPOS_ERR_CUDA;
   if (Lq == 0 || Lk == 0) {  // no score: every gradient is zero
     bool ok = true;
     if (Lq > 0) ok = ok && cudaMemsetAsync(dQ, 0, BH * Lq * row_bytes, s) == cudaSuccess;
@@ -644,8 +650,41 @@ int attn_bwd_impl(int mode, const void* Q, const void* K, const void* V, const v
   const size_t n_shaw = mode == RELPOS_SHAW ? 4 * n_rows + 4 * n_rows * nr +
                                                   n_rows / 128 * 2 * static_cast<size_t>(2 * max_distance + 1) * kHeadDim
                                             : 0;
+  // DeBERTa (in floats, each part a multiple of 64): the band pre-pass arrays
+  // (bf16 band rows with a pad on each side, the rows' saturated c2p values,
+  // the keys' saturated p2c values), dS gathered by table row query- and
+  // key-major (bf16), the rows' and keys' dS beyond the band, the fp32 dK
+  const int lk_pad = (Lk + 127) & ~127;
+  const size_t k2 = 2 * static_cast<size_t>(max_distance);
+  const int band_pitch = static_cast<int>((k2 + 8 + 7) & ~static_cast<size_t>(7));
+  auto r64 = [](size_t n) { return (n + 63) & ~static_cast<size_t>(63); };
+  size_t n_deb = 0, o_band = 0, o_c2p = 0, o_ends = 0, o_dsq = 0, o_dsk = 0, o_rowfar = 0, o_keyfar = 0, o_dk = 0,
+         o_m1 = 0, o_mk = 0;
+  if (mode == RELPOS_DEBERTA) {
+    const size_t base = n_acc + n_stats;
+    o_band = base + 256;  // 1 KB before the band rows
+    n_deb = r64(256 + (BH * Lq * band_pitch + 1) / 2 + 256);
+    o_c2p = base + n_deb;
+    n_deb += r64(BH * 2 * lq_pad);
+    o_ends = base + n_deb;
+    n_deb += r64(BH * 2 * lk_pad);
+    o_dsq = base + n_deb;
+    n_deb += r64(BH * lq_pad * k2 / 2);
+    o_dsk = base + n_deb;
+    n_deb += r64(BH * lk_pad * k2 / 2);
+    o_rowfar = base + n_deb;
+    n_deb += r64(BH * 2 * lq_pad);
+    o_keyfar = base + n_deb;
+    n_deb += r64(2 * BH * 2 * lk_pad);
+    o_dk = base + n_deb;
+    n_deb += r64(BH * Lk * kHeadDim);
+    o_m1 = base + n_deb;  // then the fp32 band members of the saturated rows
+    n_deb += r64(BH * lq_pad);
+    o_mk = base + n_deb;
+    n_deb += r64(BH * lk_pad);
+  }
   float* scratch = nullptr;
-  if (cudaMallocAsync(reinterpret_cast<void**>(&scratch), (n_acc + n_stats + n_shaw) * sizeof(float), s) !=
+  if (cudaMallocAsync(reinterpret_cast<void**>(&scratch), (n_acc + n_stats + n_shaw + n_deb) * sizeof(float), s) !=
       cudaSuccess) {
     cudaGetLastError();
     return RELPOS_ERR_CUDA;
@@ -693,6 +732,60 @@ int attn_bwd_impl(int mode, const void* Q, const void* K, const void* V, const v
     p.daV = static_cast<float*>(dtable1);
     p.Qp = static_cast<const __nv_bfloat16*>(Q);
     p.dOp = static_cast<const __nv_bfloat16*>(dO);
+  } else if (mode == RELPOS_DEBERTA) {
+    p.kc = max_distance;
+    p.band = reinterpret_cast<const __nv_bfloat16*>(scratch + o_band);
+    p.band_pitch = band_pitch;
+    p.c2p_const = scratch + o_c2p;
+    p.const_pitch = lq_pad;
+    p.p2c_ends = scratch + o_ends;
+    p.ends_pitch = lk_pad;
+    p.dSQ = reinterpret_cast<__nv_bfloat16*>(scratch + o_dsq);
+    p.dSK = reinterpret_cast<__nv_bfloat16*>(scratch + o_dsk);
+    p.lk_pad = lk_pad;
+    p.rowfar = scratch + o_rowfar;
+    p.keyfar = scratch + o_keyfar;
+    p.dKacc = scratch + o_dk;
+    p.rowm1 = scratch + o_m1;
+    p.keymk = scratch + o_mk;
+    p.Qp = static_cast<const __nv_bfloat16*>(Q);
+    p.Kp = static_cast<const __nv_bfloat16*>(K);
+    p.Pk = static_cast<const __nv_bfloat16*>(table);
+    p.Pq = static_cast<const __nv_bfloat16*>(table1);
+    p.dPk = static_cast<float*>(dtable);
+    p.dPq = static_cast<float*>(dtable1);
+    // the logit scale is 1 / sqrt(3 d)
+    p.scale = 1.0f / std::sqrt(static_cast<float>(3 * d));
+    p.scale_log2 = p.scale * kLog2e;
+    // the gathered dS starts at zero (entries whose key lies outside the
+    // keys, or that no visible score reaches, stay so); then the band
+    // pre-pass of the forward
+    if (cudaMemsetAsync(p.dSQ, 0, BH * lq_pad * k2 * 2, s) != cudaSuccess ||
+        cudaMemsetAsync(p.dSK, 0, BH * lk_pad * k2 * 2, s) != cudaSuccess ||
+        cudaMemsetAsync(p.rowm1, 0, (r64(BH * lq_pad) + BH * lk_pad) * 4, s) != cudaSuccess)
+      return done(RELPOS_ERR_CUDA);
+    BandParams bp;
+    std::memset(&bp, 0, sizeof(bp));
+    bp.BH = static_cast<int>(BH);
+    bp.H = H;
+    bp.k = max_distance;
+    bp.Lq = Lq;
+    bp.Lk = Lk;
+    bp.q_offset = q_offset;
+    bp.scale = p.scale_log2;
+    bp.K = static_cast<const __nv_bfloat16*>(K);
+    bp.Pq = static_cast<const __nv_bfloat16*>(table1);
+    bp.band = reinterpret_cast<__nv_bfloat16*>(scratch + o_band);
+    bp.band_pitch = band_pitch;
+    bp.c2p_const = scratch + o_c2p;
+    bp.const_pitch = lq_pad;
+    bp.ends = scratch + o_ends;
+    bp.ends_pitch = lk_pad;
+    bp.status = status;
+    CUtensorMap tpk, tpq;
+    if (!make_tmap_table(&tpk, table, H, static_cast<int>(k2)) || !make_tmap_table(&tpq, table1, H, static_cast<int>(k2)))
+      return done(RELPOS_ERR_CUDA);
+    if (launch_deberta_band(tq, tk, tpk, tpq, bp, s) != cudaSuccess) return done(RELPOS_ERR_CUDA);
   } else {
     p.slopes = static_cast<const float*>(table);
     p.dslopes = static_cast<float*>(dtable);
@@ -726,6 +819,14 @@ extern "C" int relpos_shaw_attn_bwd(const void* Q, const void* K, const void* V,
                                     void* daK, void* daV, void* stream) {
   return attn_bwd_impl(RELPOS_SHAW, Q, K, V, dO, aK, aV, B, H, Lq, Lk, d, 0, clip_k, causal, q_offset, dQ, dK,
                        dV, daK, daV, stream);
+}
+
+extern "C" int relpos_deberta_attn_bwd(const void* Q, const void* K, const void* V, const void* dO,
+                                       const void* Pk, const void* Pq, int B, int H, int Lq, int Lk, int d,
+                                       int k, int causal, int q_offset, void* dQ, void* dK, void* dV, void* dPk,
+                                       void* dPq, void* stream) {
+  return attn_bwd_impl(RELPOS_DEBERTA, Q, K, V, dO, Pk, Pq, B, H, Lq, Lk, d, 0, k, causal, q_offset, dQ, dK, dV,
+                       dPk, dPq, stream);
 }
 
 extern "C" int relpos_alibi_attn_bwd(const void* Q, const void* K, const void* V, const void* dO,

@@ -39,9 +39,11 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cublas_v2.h>
 
 #include <atomic>
 #include <cstdint>
+#include <mutex>
 
 #include "ptx.cuh"
 #include "relpos_bwd.cuh"
@@ -165,6 +167,25 @@ RP_DEVI float dot64_bf16(const float (&v)[64], const __nv_bfloat16* row) {
     }
   }
   return acc.x + acc.y;
+}
+
+// DeBERTa: the relative part of the logit (log2 units) of query row i (at
+// position pi) and key j at band offset m = j - pi + k: the band value for
+// 1 <= m <= 2k - 1, else the row's saturated c2p value plus the key's
+// saturated p2c value of that side. i and j are clamped into the arrays
+// (the elements outside them are masked).
+RP_DEVI float deberta_bias(const BwdParams& p, int bh, int i, int pi, int j, int m) {
+  const int ic = min(i, p.Lq - 1), jc = min(j, p.Lk - 1);
+  if (m >= 1 && m <= 2 * p.kc - 1) {
+    const int sh = (ic + p.q_offset - p.kc) & 7;  // the row's own shift
+    const unsigned short u = __ldg(reinterpret_cast<const unsigned short*>(p.band) +
+                                   (static_cast<size_t>(bh) * p.Lq + ic) * p.band_pitch + sh + m);
+    return __uint_as_float(static_cast<uint32_t>(u) << 16);
+  }
+  const int side = m >= 2 * p.kc ? 1 : 0;
+  (void)pi;
+  return __ldg(p.c2p_const + (static_cast<size_t>(bh) * 2 + side) * p.const_pitch + ic) +
+         __ldg(p.p2c_ends + (static_cast<size_t>(bh) * 2 + side) * p.ends_pitch + jc);
 }
 
 // ================================================================ stats kernel
@@ -465,6 +486,8 @@ __global__ void __launch_bounds__(kStThreads, 1)
               b = tab[min(max(rel + R + kTabPad, 0), tab_len(R) - 1)];
             } else if constexpr (MODE == 1) {
               b = Trow[min(max(rel, -p.kc), p.kc) + p.kc];  // (U joins dP in the exponential loop)
+            } else if constexpr (MODE == 2) {
+              b = deberta_bias(p, bh, row, prow, j0 + c0 + c, rel + p.kc);
             } else {
               b = -alibi * fabsf(static_cast<float>(rel));
             }
@@ -481,11 +504,13 @@ __global__ void __launch_bounds__(kStThreads, 1)
           const float a = ex2_approx(m - mx);  // 0 while m = -inf
           l2 = __fmul2_rn(l2, make_float2(a, a));
           d2 = __fmul2_rn(d2, make_float2(a, a));
-          if constexpr (MODE == 1) {
+          if constexpr (MODE == 1 || MODE == 2) {
             sLl *= a;
             sRl *= a;
             sLd *= a;
             sRd *= a;
+          }
+          if constexpr (MODE == 1) {
 #pragma unroll 1
             for (int r = 0; r < 2 * p.kc + 1; ++r) {
               bp_row[r] *= a;
@@ -544,6 +569,21 @@ __global__ void __launch_bounds__(kStThreads, 1)
               sRd += rel >= p.kc ? dd : 0.f;
             }
           }
+        } else if constexpr (MODE == 2) {
+          // DeBERTa: the row's sums over the keys beyond the band on each
+          // side (their dS sums feed the saturated table rows)
+#pragma unroll
+          for (int c = 0; c < 64; ++c) {
+            const float e = ex2_approx(xv[c] - mu);
+            const float dd = e * __uint_as_float(dr[c]);
+            l2.x += e;
+            d2.x += dd;
+            const int rel = j0 + c0 + c - prow;
+            sLl += rel <= -p.kc ? e : 0.f;
+            sLd += rel <= -p.kc ? dd : 0.f;
+            sRl += rel >= p.kc ? e : 0.f;
+            sRd += rel >= p.kc ? dd : 0.f;
+          }
         } else {
 #pragma unroll
           for (int c = 0; c < 64; c += 2) {
@@ -566,7 +606,7 @@ __global__ void __launch_bounds__(kStThreads, 1)
       mrg[t] = m;
       mrg[128 + t] = l;
       mrg[256 + t] = dsum;
-      if constexpr (MODE == 1) {
+      if constexpr (MODE == 1 || MODE == 2) {
         mrg[3 * 128 + t] = sLl;
         mrg[4 * 128 + t] = sRl;
         mrg[5 * 128 + t] = sLd;
@@ -586,6 +626,15 @@ __global__ void __launch_bounds__(kStThreads, 1)
         D = (dsum * a0 + d1 * a1) / lt;
         w0 = a0 / lt;
         w1 = a1 / lt;
+      }
+      if constexpr (MODE == 2) {
+        // the row's dS summed over the keys beyond the band, each side
+        // (zero for rows past Lq)
+        if (row >= p.Lq) w0 = w1 = 0.f;
+        const float pl = sLl * w0 + mrg[3 * 128 + t] * w1, pr = sRl * w0 + mrg[4 * 128 + t] * w1;
+        const float dl = sLd * w0 + mrg[5 * 128 + t] * w1, dq = sRd * w0 + mrg[6 * 128 + t] * w1;
+        p.rowfar[(static_cast<size_t>(bh) * 2) * p.lq_pad + row] = fmaf(-D, pl, dl);
+        p.rowfar[(static_cast<size_t>(bh) * 2 + 1) * p.lq_pad + row] = fmaf(-D, pr, dq);
       }
       if constexpr (MODE == 1) {
         // per clipped offset: sum of P and of dS = P (dP - D) over the
@@ -855,6 +904,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     float alibi = 0.f;
     if constexpr (MODE == 3) alibi = __ldg(p.slopes + h) * kLog2e;
     float sumL = 0.f, sumR = 0.f, dsl = 0.f;  // T5 saturated sides; ALiBi slope gradient
+    float kfl = 0.f, kfr = 0.f;               // DeBERTa: dS over the queries beyond the band
     const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
     bool err = false;
     for (int s = hf, c = 0; s < nsub; s += 2, ++c) {
@@ -1085,6 +1135,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
                 const size_t o = srow + static_cast<size_t>(cc) * p.nr + (min(max(rel, -p.kc), p.kc) + p.kc);
                 b = __ldg(p.shT + o);
                 ua = __ldg(p.shU + o);
+              } else if constexpr (MODE == 2) {
+                b = deberta_bias(p, bh, q0 + cc, q0 + cc + p.q_offset, key, rel + p.kc);
               } else {
                 b = -alibi * fabsf(static_cast<float>(rel));
               }
@@ -1095,6 +1147,22 @@ __global__ void __launch_bounds__(kKvThreads, 1)
               dsv[u] = ds;
               if constexpr (MODE == 0) {
                 dr[cc] = __float_as_uint(ds);  // for the per-offset sums
+              } else if constexpr (MODE == 2) {
+                // inside the band each (query, table row) and (key, table
+                // row) meets one score: c2p row 2k - m, p2c row m
+                const int m = rel + p.kc, k2 = 2 * p.kc;
+                if (m >= 1 && m < k2) {
+                  const __nv_bfloat16 v = __float2bfloat16_rn(ds);
+                  p.dSQ[(static_cast<size_t>(bh) * p.lq_pad + q0 + cc) * k2 + (k2 - m)] = v;
+                  p.dSK[(static_cast<size_t>(bh) * p.lk_pad + key) * k2 + m] = v;
+                  // the saturated rows' band members also in fp32: the fold
+                  // adds the far sums to them before rounding (the sums can
+                  // nearly cancel them)
+                  if (m == 1) p.rowm1[static_cast<size_t>(bh) * p.lq_pad + q0 + cc] = ds;
+                  if (m == k2 - 1) p.keymk[static_cast<size_t>(bh) * p.lk_pad + key] = ds;
+                }
+                kfl += m <= 0 ? ds : 0.f;
+                kfr += m >= k2 ? ds : 0.f;
               } else if constexpr (MODE == 3) {
                 dsl = fmaf(ds, fabsf(static_cast<float>(rel)), dsl);
               }
@@ -1162,12 +1230,20 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       named_bar_sync(3, 256);
       if (tid == 128 && !*abort_f && red[2] != 0.f) atomicAdd(p.dslopes + h, -red[2]);
     }
-    // ---- dV (warpgroup 0) and dK (warpgroup 1)
+    if constexpr (MODE == 2) {  // this query half's far sums of the key
+      const size_t kf = (static_cast<size_t>(hf) * gridDim.y + bh) * 2 * p.lk_pad + key;
+      p.keyfar[kf] = kfl;
+      p.keyfar[kf + p.lk_pad] = kfr;
+    }
+    // ---- dV (warpgroup 0) and dK (warpgroup 1; DeBERTa: fp32, the table
+    // term is added later)
     // warp-uniform: the TMEM loads below are warp-collective
     const bool fin = __all_sync(0xffffffffu, mbar_wait(bar(kKvBarFin), 0) && *abort_f == 0);
     tc_fence_after();
+    const bool f32k = MODE == 2 && hf == 1;
     __nv_bfloat16* dst = (hf == 0 ? p.dV : p.dK) + (static_cast<size_t>(bh) * p.Lk + key) * kHeadDim;
     uint4* d4 = reinterpret_cast<uint4*>(dst);
+    float4* f4 = reinterpret_cast<float4*>(p.dKacc + (static_cast<size_t>(bh) * p.Lk + key) * kHeadDim);
     if (nsub > 0 && fin) {
       uint32_t a[32], b[32];  // every lane loads (warp-collective); rows past Lk are not stored
       tmem_ld32(tmem + lane_base + (hf == 0 ? kColDV : kColDK), a);
@@ -1175,7 +1251,14 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       tmem_ld_wait(a);
       tmem_ld_wait(b);
       const float mul = hf == 0 ? 1.f : p.scale;
-      if (key_ok) {
+      if (key_ok && f32k) {
+#pragma unroll
+        for (int v = 0; v < 16; ++v) {
+          const uint32_t* r = v < 8 ? &a[v * 4] : &b[(v - 8) * 4];
+          f4[v] = make_float4(__uint_as_float(r[0]) * mul, __uint_as_float(r[1]) * mul,
+                              __uint_as_float(r[2]) * mul, __uint_as_float(r[3]) * mul);
+        }
+      } else if (key_ok) {
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
           const uint32_t* r = v < 4 ? &a[v * 8] : &b[(v - 4) * 8];
@@ -1187,8 +1270,13 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         }
       }
     } else if (nsub == 0 && key_ok) {  // no query sees this key
+      if (f32k) {
 #pragma unroll
-      for (int v = 0; v < 8; ++v) d4[v] = make_uint4(0u, 0u, 0u, 0u);
+        for (int v = 0; v < 16; ++v) f4[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+      } else {
+#pragma unroll
+        for (int v = 0; v < 8; ++v) d4[v] = make_uint4(0u, 0u, 0u, 0u);
+      }
     }
     if (!fin && lane == 0) bwd_error(p.status);
   } else {
@@ -1412,6 +1500,37 @@ __global__ void __launch_bounds__(kShThreads) relpos_bwd_shaw_reduce_kernel(cons
   }
 }
 
+// DeBERTa: the rows' and keys' dS beyond the band into the saturated table
+// rows of the gathered dS (c2p row 2k - 1 takes the keys far behind, row 0
+// those far ahead; p2c row 0 the queries with m <= 0, row 2k - 1 those with
+// m >= 2k), after the dK / dV kernel has scattered the band; a saturated row
+// that also holds a band member (c2p 2k - 1: m = 1; p2c 2k - 1: m = 2k - 1)
+// sums it in fp32 first
+__global__ void __launch_bounds__(256) relpos_bwd_deberta_fold_kernel(const BwdParams p) {
+  griddep_wait();
+  const int k2 = 2 * p.kc;
+  const size_t nbh = static_cast<size_t>(p.B) * p.H;
+  const size_t nq = nbh * p.lq_pad, nk = nbh * p.lk_pad;
+  for (size_t x = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; x < nq + nk;
+       x += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    if (x < nq) {
+      const size_t bh = x / p.lq_pad, i = x % p.lq_pad;
+      const float L = p.rowfar[bh * 2 * p.lq_pad + i], R = p.rowfar[(bh * 2 + 1) * p.lq_pad + i];
+      __nv_bfloat16* row = p.dSQ + x * k2;
+      row[k2 - 1] = __float2bfloat16_rn(p.rowm1[x] + L);
+      row[0] = __float2bfloat16_rn(R);
+    } else {
+      const size_t y = x - nq, bh = y / p.lk_pad, j = y % p.lk_pad;
+      const size_t a0 = bh * 2 * p.lk_pad + j, a1 = (nbh + bh) * 2 * p.lk_pad + j;  // query halves 0, 1
+      const float KL = p.keyfar[a0] + p.keyfar[a1];
+      const float KR = p.keyfar[a0 + p.lk_pad] + p.keyfar[a1 + p.lk_pad];
+      __nv_bfloat16* row = p.dSK + y * k2;
+      row[0] = __float2bfloat16_rn(KL);
+      row[k2 - 1] = __float2bfloat16_rn(p.keymk[y] + KR);
+    }
+  }
+}
+
 uint32_t shaw_final_smem_bytes(int nr) {
   const uint32_t nrel = static_cast<uint32_t>(nr) - 1u;
   return (2u * kBT * kShQs + nrel * 64u + 2u * kBT * static_cast<uint32_t>(nr)) * 4u;
@@ -1452,6 +1571,94 @@ cudaError_t launch_pdl(K kern, dim3 grid, dim3 block, uint32_t smem, cudaStream_
   return cudaLaunchKernelEx(&cfg, kern, a, b, c, d, p);
 }
 
+// the fp32 accumulator [rows, 64] to bf16
+cudaError_t launch_convert(const float* acc, __nv_bfloat16* out, size_t rows, cudaStream_t stream) {
+  const size_t n4 = rows * kHeadDim / 4;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  size_t blocks = (n4 + 255) / 256;
+  if (blocks > 152 * 8) blocks = 152 * 8;
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks > 0 ? blocks : 1));
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, relpos_bwd_dq_convert_kernel, reinterpret_cast<const float4*>(acc),
+                            reinterpret_cast<uint2*>(out), n4);
+}
+
+cublasHandle_t cublas_handle_locked(int dev) {
+  static cublasHandle_t handles[64] = {};
+  if (dev < 0 || dev >= 64) return nullptr;
+  if (!handles[dev] && cublasCreate(&handles[dev]) != CUBLAS_STATUS_SUCCESS) handles[dev] = nullptr;
+  return handles[dev];
+}
+
+// DeBERTa after the dK / dV kernel: the far sums folded into the gathered dS,
+// then four plain GEMMs per batch element (batched over the heads; cuBLAS,
+// bf16 operands, fp32 accumulation) add the table terms to dQ and dK and form
+// the tables' gradients, then dQ and dK go to bf16. With s the logit scale:
+//   dQ_bh += s dSQ_bh Pk_h,   dK_bh += s dSK_bh Pq_h,
+//   dPk_h += s dSQ_bh^T Q_bh, dPq_h += s dSK_bh^T K_bh   (summed over b)
+// (row-major operands; cuBLAS sees their transposes).
+cudaError_t launch_deberta_tail(const BwdParams& p, cudaStream_t stream) {
+  {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(152 * 4);
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, relpos_bwd_deberta_fold_kernel, p);
+    if (e != cudaSuccess) return e;
+  }
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+  static std::mutex mu;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    cublasHandle_t h = cublas_handle_locked(dev);
+    if (!h || cublasSetStream(h, stream) != CUBLAS_STATUS_SUCCESS) return cudaErrorUnknown;
+    const int k2 = 2 * p.kc, H = p.H;
+    const float s = p.scale, one = 1.f;
+    const long long sq = static_cast<long long>(p.lq_pad) * k2, sk = static_cast<long long>(p.lk_pad) * k2;
+    for (int b = 0; b < p.B; ++b) {
+      const size_t bh0 = static_cast<size_t>(b) * H;
+      const __nv_bfloat16* dsq = p.dSQ + bh0 * sq;
+      const __nv_bfloat16* dsk = p.dSK + bh0 * sk;
+      cublasStatus_t st = cublasGemmStridedBatchedEx(
+          h, CUBLAS_OP_N, CUBLAS_OP_N, kHeadDim, p.Lq, k2, &s, p.Pk, CUDA_R_16BF, H * kHeadDim, kHeadDim, dsq,
+          CUDA_R_16BF, k2, sq, &one, p.dQacc + bh0 * p.Lq * kHeadDim, CUDA_R_32F, kHeadDim,
+          static_cast<long long>(p.Lq) * kHeadDim, H, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
+      if (st == CUBLAS_STATUS_SUCCESS)
+        st = cublasGemmStridedBatchedEx(
+            h, CUBLAS_OP_N, CUBLAS_OP_N, kHeadDim, p.Lk, k2, &s, p.Pq, CUDA_R_16BF, H * kHeadDim, kHeadDim, dsk,
+            CUDA_R_16BF, k2, sk, &one, p.dKacc + bh0 * p.Lk * kHeadDim, CUDA_R_32F, kHeadDim,
+            static_cast<long long>(p.Lk) * kHeadDim, H, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
+      if (st == CUBLAS_STATUS_SUCCESS)
+        st = cublasGemmStridedBatchedEx(
+            h, CUBLAS_OP_N, CUBLAS_OP_T, kHeadDim, k2, p.Lq, &s, p.Qp + bh0 * p.Lq * kHeadDim, CUDA_R_16BF, kHeadDim,
+            static_cast<long long>(p.Lq) * kHeadDim, dsq, CUDA_R_16BF, k2, sq, &one, p.dPk, CUDA_R_32F,
+            H * kHeadDim, kHeadDim, H, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
+      if (st == CUBLAS_STATUS_SUCCESS)
+        st = cublasGemmStridedBatchedEx(
+            h, CUBLAS_OP_N, CUBLAS_OP_T, kHeadDim, k2, p.Lk, &s, p.Kp + bh0 * p.Lk * kHeadDim, CUDA_R_16BF, kHeadDim,
+            static_cast<long long>(p.Lk) * kHeadDim, dsk, CUDA_R_16BF, k2, sk, &one, p.dPq, CUDA_R_32F,
+            H * kHeadDim, kHeadDim, H, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
+      if (st != CUBLAS_STATUS_SUCCESS) return cudaErrorUnknown;
+    }
+  }
+  const size_t nbh = static_cast<size_t>(p.B) * p.H;
+  cudaError_t e = launch_convert(p.dQacc, p.dQ, nbh * p.Lq, stream);
+  if (e == cudaSuccess) e = launch_convert(p.dKacc, p.dK, nbh * p.Lk, stream);
+  return e;
+}
+
 template <int MODE>
 cudaError_t launch_bwd_mode(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                             const CUtensorMap& tmdO, const CUtensorMap& tmAcc, const BwdParams& p,
@@ -1490,6 +1697,7 @@ cudaError_t launch_bwd_mode(const CUtensorMap& tmQ, const CUtensorMap& tmK, cons
     e = cudaLaunchKernelEx(&cfg, relpos_bwd_dkdv_kernel<MODE>, tmQ, tmK, tmV, tmdO, tmAcc, p);
     if (e != cudaSuccess) return e;
   }
+  if constexpr (MODE == 2) return launch_deberta_tail(p, stream);
   if constexpr (MODE == 1) {
     const int nqt = (p.Lq + kBT - 1) / kBT;
     cudaLaunchAttribute attr[1];
@@ -1539,6 +1747,10 @@ cudaError_t launch_bwd(int mode, const CUtensorMap& tmQ, const CUtensorMap& tmK,
   if (mode == 1) {
     if (p.kc < 1 || p.kc > kMaxShawK || p.nr != 2 * p.kc + 2) return cudaErrorInvalidValue;
     return launch_bwd_mode<1>(tmQ, tmK, tmV, tmdO, tmAcc, p, stream);
+  }
+  if (mode == 2) {
+    if (p.kc < 1 || !p.band || !p.dSQ || !p.dSK) return cudaErrorInvalidValue;
+    return launch_bwd_mode<2>(tmQ, tmK, tmV, tmdO, tmAcc, p, stream);
   }
   if (mode == 3) return launch_bwd_mode<3>(tmQ, tmK, tmV, tmdO, tmAcc, p, stream);
   return cudaErrorInvalidValue;

@@ -45,6 +45,28 @@ struct BwdParams {
   float* daV;               // [2k + 1, 64] fp32, written
   const __nv_bfloat16* Qp;   // [B*H, Lq, 64] (Shaw: the final kernel's rows)
   const __nv_bfloat16* dOp;  // [B*H, Lq, 64]
+  // DeBERTa (mode 2; kc = k): the forward's band pre-pass arrays (c2p + p2c
+  // inside the band, log2 units, bf16; the saturated c2p values per query row
+  // and p2c values per key, fp32), and dS gathered by table row
+  const __nv_bfloat16* band;  // [B*H, Lq, band_pitch], row i's offset m = j - p_i + k at ((p_i - k) & 7) + m
+  int band_pitch;
+  const float* c2p_const;     // [B*H, 2, const_pitch]: keys far behind (m <= 0), far ahead (m >= 2k)
+  int const_pitch;
+  const float* p2c_ends;      // [B*H, 2, ends_pitch]: the same two sides per key
+  int ends_pitch;
+  __nv_bfloat16* dSQ;         // [B*H, lq_pad, 2k]: sum of dS_ij over the keys with c2p row delta(i, j) = r (zeroed)
+  __nv_bfloat16* dSK;         // [B*H, lk_pad, 2k]: sum over the queries with p2c row delta(j, i) = r (zeroed)
+  int lk_pad;                 // Lk rounded up to a multiple of 128
+  float* rowfar;              // [B*H, 2, lq_pad] per row: sum of dS over the keys with m <= 0, with m >= 2k
+  float* keyfar;              // [2 query halves, B*H, 2, lk_pad] per key: the same over the queries
+  float* rowm1;               // [B*H, lq_pad] dS of the row's key at m = 1, fp32 (zeroed)
+  float* keymk;               // [B*H, lk_pad] dS of the key's query at m = 2k - 1, fp32 (zeroed)
+  float* dKacc;               // [B*H, Lk, 64] fp32 dK (scaled), before the table terms
+  const __nv_bfloat16* Kp;    // [B*H, Lk, 64]
+  const __nv_bfloat16* Pk;    // [2k, H, 64]
+  const __nv_bfloat16* Pq;    // [2k, H, 64]
+  float* dPk;                 // [2k, H, 64] fp32, zeroed before the kernels
+  float* dPq;                 // [2k, H, 64] fp32, zeroed before the kernels
   float* lse;    // [B*H, lq_pad] row log-sum-exp of the log2-scaled logits (stats kernel)
   float* Dr;     // [B*H, lq_pad] D_i = sum_j P_ij dP_ij (stats kernel)
   int lq_pad;    // Lq rounded up to a multiple of 128 (whole query tiles)
@@ -55,12 +77,13 @@ struct BwdParams {
   int* status;
 };
 
-// mode 0 (T5), 1 (Shaw) or 3 (ALiBi): the row-statistics kernel (Shaw: also
-// the per-row tables and the per-offset sums), the dK / dV kernel (which also
-// accumulates dQ and the T5 / ALiBi table gradient) and the dQ conversion
-// (Shaw: with the a_K term, then the table gradients); bwd_max_R is the
-// largest T5 saturation distance R they support, bwd_max_shaw_k the largest
-// Shaw clip
+// mode 0 (T5), 1 (Shaw), 2 (DeBERTa) or 3 (ALiBi): the row-statistics kernel
+// (Shaw: also the per-row tables and the per-offset sums; DeBERTa: the rows'
+// dS beyond the band), the dK / dV kernel (which also accumulates dQ and the
+// T5 / ALiBi table gradient; DeBERTa: scatters dS by table row) and the dQ
+// conversion (Shaw: with the a_K term, then the table gradients; DeBERTa:
+// the table products, then dQ and dK); bwd_max_R is the largest T5
+// saturation distance R they support, bwd_max_shaw_k the largest Shaw clip
 int bwd_max_shaw_k();
 int bwd_max_R();
 // tmAcc: the fp32 dQ accumulator [B*H, Lq, 64] as 128-row x 32-column boxes
