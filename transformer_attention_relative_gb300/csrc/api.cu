@@ -659,7 +659,7 @@ int attn_bwd_impl(int mode, const void* Q, const void* K, const void* V, const v
   const int band_pitch = static_cast<int>((k2 + 8 + 7) & ~static_cast<size_t>(7));
   auto r64 = [](size_t n) { return (n + 63) & ~static_cast<size_t>(63); };
   size_t n_deb = 0, o_band = 0, o_c2p = 0, o_ends = 0, o_dsq = 0, o_dsk = 0, o_rowfar = 0, o_keyfar = 0, o_dk = 0,
-         o_m1 = 0, o_mk = 0;
+         o_m1 = 0, o_mk = 0, o_e4 = 0;
   if (mode == RELPOS_DEBERTA) {
     const size_t base = n_acc + n_stats;
     o_band = base + 256;  // 1 KB before the band rows
@@ -682,6 +682,8 @@ int attn_bwd_impl(int mode, const void* Q, const void* K, const void* V, const v
     n_deb += r64(BH * lq_pad);
     o_mk = base + n_deb;
     n_deb += r64(BH * lk_pad);
+    o_e4 = base + n_deb;  // the rows' values for the sub-steps beyond the band
+    n_deb += r64(BH * 4 * lq_pad);
   }
   float* scratch = nullptr;
   if (cudaMallocAsync(reinterpret_cast<void**>(&scratch), (n_acc + n_stats + n_shaw + n_deb) * sizeof(float), s) !=
@@ -748,6 +750,7 @@ int attn_bwd_impl(int mode, const void* Q, const void* K, const void* V, const v
     p.dKacc = scratch + o_dk;
     p.rowm1 = scratch + o_m1;
     p.keymk = scratch + o_mk;
+    p.shEnds = scratch + o_e4;
     p.Qp = static_cast<const __nv_bfloat16*>(Q);
     p.Kp = static_cast<const __nv_bfloat16*>(K);
     p.Pk = static_cast<const __nv_bfloat16*>(table);

@@ -405,11 +405,12 @@ __global__ void __launch_bounds__(kStThreads, 1)
       // statistics are never used)
       const int rel_hi = j0 + kBT - 1 - (i0 + p.q_offset), rel_lo = j0 - (i0 + kBT - 1 + p.q_offset);
       const bool nomask = j0 + kBT <= p.Lk && (!p.causal || rel_hi <= 0);
-      const bool far_l = (MODE == 0 && rel_hi <= -R) || (MODE == 1 && rel_hi <= -p.kc);
-      const bool far_r = (MODE == 0 && p.t5.bidir && rel_lo >= R) || (MODE == 1 && rel_lo >= p.kc);
+      const bool far_l = (MODE == 0 && rel_hi <= -R) || ((MODE == 1 || MODE == 2) && rel_hi <= -p.kc);
+      const bool far_r = (MODE == 0 && p.t5.bidir && rel_lo >= R) || ((MODE == 1 || MODE == 2) && rel_lo >= p.kc);
       // one row constant: T5 beyond the saturation distance, Shaw beyond the
       // clip; ALiBi with every key on one side (the rest is linear in the
-      // column). T5 near tiles without masking read their biases 4 at a time.
+      // column); DeBERTa beyond the band (plus each key's saturated p2c
+      // value). T5 near tiles without masking read their biases 4 at a time.
       const bool fast = nomask && (MODE != 3 ? (far_l || far_r) : (rel_hi <= 0 || rel_lo >= 0));
       const bool near_t5 = MODE == 0 && nomask && !fast;
 #pragma unroll 1
@@ -454,6 +455,21 @@ __global__ void __launch_bounds__(kStThreads, 1)
           } else if constexpr (MODE == 1) {
             bc = Trow[far_l ? 0 : 2 * p.kc];
             ue = Urow[far_l ? 0 : 2 * p.kc];
+          } else if constexpr (MODE == 2) {
+            const size_t side = far_l ? 0 : 1;
+            bc = __ldg(p.c2p_const + (static_cast<size_t>(bh) * 2 + side) * p.const_pitch + min(row, p.Lq - 1));
+            const float4* pe =
+                reinterpret_cast<const float4*>(p.p2c_ends + (static_cast<size_t>(bh) * 2 + side) * p.ends_pitch + j0 + c0);
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+              const float4 e = __ldg(pe + q);
+              const float2 a = __ffma2_rn(make_float2(xv[4 * q], xv[4 * q + 1]), sc2, make_float2(e.x, e.y));
+              const float2 b = __ffma2_rn(make_float2(xv[4 * q + 2], xv[4 * q + 3]), sc2, make_float2(e.z, e.w));
+              xv[4 * q] = a.x;
+              xv[4 * q + 1] = a.y;
+              xv[4 * q + 2] = b.x;
+              xv[4 * q + 3] = b.y;
+            }
           } else {
             // -slope |j - p| = g (j - p) with g = slope (keys behind) or -slope (ahead):
             // scaled scores plus g c, then the row constant g (j0 + c0 - p)
@@ -474,7 +490,7 @@ __global__ void __launch_bounds__(kStThreads, 1)
             m0 = max3f(m0, xv[c], xv[c + 1]);
             m1 = max3f(m1, xv[c + 2], xv[c + 3]);
           }
-          mx = MODE != 3 ? fmaf(fmaxf(m0, m1), p.scale_log2, bc) : fmaxf(m0, m1) + bc;
+          mx = MODE <= 1 ? fmaf(fmaxf(m0, m1), p.scale_log2, bc) : fmaxf(m0, m1) + bc;
         } else {
           float m0 = -INFINITY, m1 = -INFINITY;
 #pragma unroll
@@ -521,7 +537,7 @@ __global__ void __launch_bounds__(kStThreads, 1)
         }
         const float mu = m == -INFINITY ? 0.f : m;
         // 2^(x - m): fast tiles scale the raw scores (T5, Shaw) inside the FMA
-        const float2 mul2 = (MODE != 3 && fast) ? sc2 : make_float2(1.f, 1.f);
+        const float2 mul2 = (MODE <= 1 && fast) ? sc2 : make_float2(1.f, 1.f);
         const float off = bc - mu;
         const float2 off2 = make_float2(off, off);
         if constexpr (MODE == 1) {
@@ -572,6 +588,27 @@ __global__ void __launch_bounds__(kStThreads, 1)
         } else if constexpr (MODE == 2) {
           // DeBERTa: the row's sums over the keys beyond the band on each
           // side (their dS sums feed the saturated table rows)
+          if (fast) {
+            float2 tl = make_float2(0.f, 0.f), td = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int c = 0; c < 64; c += 2) {
+              float2 e = __fadd2_rn(make_float2(xv[c], xv[c + 1]), off2);
+              e.x = ex2_approx(e.x);
+              e.y = ex2_approx(e.y);
+              tl = __fadd2_rn(tl, e);
+              td = __ffma2_rn(e, make_float2(__uint_as_float(dr[c]), __uint_as_float(dr[c + 1])), td);
+            }
+            const float sl = tl.x + tl.y, sd = td.x + td.y;
+            l2.x += sl;
+            d2.x += sd;
+            if (far_l) {
+              sLl += sl;
+              sLd += sd;
+            } else {
+              sRl += sl;
+              sRd += sd;
+            }
+          } else {
 #pragma unroll
           for (int c = 0; c < 64; ++c) {
             const float e = ex2_approx(xv[c] - mu);
@@ -583,6 +620,7 @@ __global__ void __launch_bounds__(kStThreads, 1)
             sLd += rel <= -p.kc ? dd : 0.f;
             sRl += rel >= p.kc ? e : 0.f;
             sRd += rel >= p.kc ? dd : 0.f;
+          }
           }
         } else {
 #pragma unroll
@@ -635,6 +673,14 @@ __global__ void __launch_bounds__(kStThreads, 1)
         const float dl = sLd * w0 + mrg[5 * 128 + t] * w1, dq = sRd * w0 + mrg[6 * 128 + t] * w1;
         p.rowfar[(static_cast<size_t>(bh) * 2) * p.lq_pad + row] = fmaf(-D, pl, dl);
         p.rowfar[(static_cast<size_t>(bh) * 2 + 1) * p.lq_pad + row] = fmaf(-D, pr, dq);
+        // for the dK / dV kernel's sub-steps beyond the band: lse minus the
+        // side's saturated c2p value, and D
+        const int rowc = min(row, p.Lq - 1);
+        float* ge = p.shEnds + static_cast<size_t>(bh) * 4 * p.lq_pad + row;
+        ge[0] = lse - p.c2p_const[static_cast<size_t>(bh) * 2 * p.const_pitch + rowc];
+        ge[p.lq_pad] = lse - p.c2p_const[(static_cast<size_t>(bh) * 2 + 1) * p.const_pitch + rowc];
+        ge[2 * static_cast<size_t>(p.lq_pad)] = D;
+        ge[3 * static_cast<size_t>(p.lq_pad)] = D;
       }
       if constexpr (MODE == 1) {
         // per clipped offset: sum of P and of dS = P (dP - D) over the
@@ -732,9 +778,10 @@ __global__ void __launch_bounds__(kKvThreads, 1)
   // T5: 4 copies of F (the reversed extended bias table); dS summed per
   // offset over the near tiles (entry = E index of the offset); per bucket
   // Shaw: per ring stage, the query tile's lse - T and D - U of the two end
-  // offsets
+  // offsets (DeBERTa: lse minus the saturated c2p values of the two sides,
+  // and D twice)
   float* tab = reinterpret_cast<float*>(smem + kKvOffAux);
-  float* hist = tab + (MODE == 0 ? 4 * tab_stride(R) : MODE == 1 ? 2 * 512 : 0);
+  float* hist = tab + (MODE == 0 ? 4 * tab_stride(R) : (MODE == 1 || MODE == 2) ? 2 * 512 : 0);
   float* hist_b = hist + (MODE == 0 ? tab_len(R) : 0);
   float* red = hist_b + kMaxT5Buckets;  // side sums / ALiBi slope partials
   float* bsm = red + 16;                // T5 bias per bucket
@@ -787,12 +834,12 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           const int q0 = (first + i) * kBT;
           const uint32_t dst = sb + kKvOffRing + st * kKvStage;
           const size_t so = static_cast<size_t>(bh) * p.lq_pad + q0;  // 512-byte aligned rows
-          mbar_arrive_expect_tx(bar(kKvBarFull + st), 2 * kTile + 1024 + (MODE == 1 ? 2048 : 0));
+          mbar_arrive_expect_tx(bar(kKvBarFull + st), 2 * kTile + 1024 + ((MODE == 1 || MODE == 2) ? 2048 : 0));
           tma_load_3d(dst, &tmQ, bar(kKvBarFull + st), 0, q0, bh);
           tma_load_3d(dst + kTile, &tmdO, bar(kKvBarFull + st), 0, q0, bh);
           bulk_load(dst + 2 * kTile, p.lse + so, 512, bar(kKvBarFull + st));
           bulk_load(dst + 2 * kTile + 512, p.Dr + so, 512, bar(kKvBarFull + st));
-          if constexpr (MODE == 1) {
+          if constexpr (MODE == 1 || MODE == 2) {
 #pragma unroll
             for (int e = 0; e < 4; ++e)
               bulk_load(smem_u32(tab) + st * 2048u + e * 512u,
@@ -932,8 +979,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       const int rb = key - q0 - p.q_offset;
       const int rel_hi = j0 + kBT - 1 - (q0 + p.q_offset), rel_lo = j0 - (q0 + 63 + p.q_offset);
       const bool nomask = j0 + kBT <= p.Lk && q0 + 64 <= p.Lq && (!p.causal || rel_hi <= 0);
-      const bool far_l = (MODE == 0 && rel_hi <= -R) || (MODE == 1 && rel_hi <= -p.kc);
-      const bool far_r = (MODE == 0 && p.t5.bidir && rel_lo >= R) || (MODE == 1 && rel_lo >= p.kc);
+      const bool far_l = (MODE == 0 && rel_hi <= -R) || ((MODE == 1 || MODE == 2) && rel_hi <= -p.kc);
+      const bool far_r = (MODE == 0 && p.t5.bidir && rel_lo >= R) || ((MODE == 1 || MODE == 2) && rel_lo >= p.kc);
       // dS goes to shared memory as it is formed: the dQ product of tile
       // i - 2 must have read this buffer
       if (i >= 2) {
@@ -1009,10 +1056,15 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         // g = -slope (keys behind: |rel| = c - rb) or +slope (ahead: rb - c)
         // F index of offset o: R + kTabPad - o. Shaw beyond the clip: each
         // column's query takes its T and U of the side's end offset.
-        const float bc = MODE == 0 ? (far_l ? tab[2 * R + kTabPad] : tab[kTabPad]) : 0.f;
+        // DeBERTa beyond the band: the key's saturated p2c value is the
+        // constant, the column's c2p value joins lse (lse - c2p)
+        float bc = 0.f;
+        if constexpr (MODE == 0) bc = far_l ? tab[2 * R + kTabPad] : tab[kTabPad];
+        if constexpr (MODE == 2)
+          bc = __ldg(p.p2c_ends + (static_cast<size_t>(bh) * 2 + (far_l ? 0 : 1)) * p.ends_pitch + min(key, p.Lk - 1));
         // Shaw: lse - T and D - U of the side's end offset stand for lse and D
-        const float* lse_f = MODE == 1 ? tab + (i & 1) * 512 + (far_l ? 0 : 128) + hf * 64 : lse_s;
-        const float* dd_f = MODE == 1 ? lse_f + 256 : dd_s;
+        const float* lse_f = (MODE == 1 || MODE == 2) ? tab + (i & 1) * 512 + (far_l ? 0 : 128) + hf * 64 : lse_s;
+        const float* dd_f = (MODE == 1 || MODE == 2) ? lse_f + 256 : dd_s;
         const float g = MODE == 0 ? 0.f : (rel_hi <= 0 ? -alibi : alibi);
         const float2 g2 = make_float2(g, g);
         const float nrb = -static_cast<float>(rb);
@@ -1047,7 +1099,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             const float2 t1 = __fadd2_rn(
                 make_float2(__uint_as_float(dr[4 * q + 2]), __uint_as_float(dr[4 * q + 3])), make_float2(-D.z, -D.w));
             const float2 d0 = __fmul2_rn(e0, t0), d1 = __fmul2_rn(e1, t1);
-            if constexpr (MODE == 0) {
+            if constexpr (MODE == 0 || MODE == 2) {
               acc = __fadd2_rn(acc, __fadd2_rn(d0, d1));
             } else if constexpr (MODE == 3) {
               acc = __ffma2_rn(d0, cm0, acc);
@@ -1066,6 +1118,11 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             sumL += a;
           else
             sumR += a;
+        } else if constexpr (MODE == 2) {
+          if (far_l)
+            kfl += a;
+          else
+            kfr += a;
         } else if constexpr (MODE == 3) {
           dsl += rel_hi <= 0 ? a : -a;  // |rel| = c - rb behind, rb - c ahead
         }
@@ -1551,7 +1608,7 @@ uint32_t dkdv_smem_bytes(int mode, int R) {
   const uint32_t t5 =
       mode == 0 ? (4u * static_cast<uint32_t>(tab_stride(R)) + static_cast<uint32_t>(tab_len(R)) + 8u * 96u) * 4u +
                       ((static_cast<uint32_t>(tab_len(R)) + 15u) & ~15u)
-                : mode == 1 ? 2u * 2048u : 0u;
+                : (mode == 1 || mode == 2) ? 2u * 2048u : 0u;
   return 1024u + kKvOffAux + t5 + (2u * kMaxT5Buckets + 16u) * 4u;
 }
 

@@ -38,6 +38,7 @@ struct BwdParams {
   float* shT;               // [B*H, lq_pad, nr] q_i . a_K[r] * scale_log2 (statistics kernel)
   float* shU;               // [B*H, lq_pad, nr] dO_i . a_V[r]
   float* shEnds;            // [B*H, 4, lq_pad] lse - T[0], lse - T[2k], D - U[0], D - U[2k] of every row
+                            // (DeBERTa: lse - the two saturated c2p values, D, D)
   float* shBP;              // [B*H, lq_pad, nr] sum of P_ij over the keys at clipped offset r
   float* shBdS;             // [B*H, lq_pad, nr] sum of dS_ij over them
   float* shPart;            // [query tiles * B*H, 2, 2k + 1, 64] per-tile partial da_K, da_V
