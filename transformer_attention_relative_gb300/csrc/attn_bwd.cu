@@ -1,5 +1,5 @@
-// attn_bwd.cu -- backward of the T5-bias and the ALiBi relative-position
-// attention, sm_103a.
+// attn_bwd.cu -- backward of the T5-bias, ALiBi, Shaw and DeBERTa
+// relative-position attention, sm_103a.
 //
 // The forward ("Relative Position Embeddings, in depth", sections "T5: one
 // scalar per head, looked up by bucket" and "ALiBi and RoPE: the two
@@ -13,6 +13,11 @@
 //   dbias[b, h] = the sum of dS_ij over every (batch, i, j) whose offset falls
 //   in bucket b (every offset of a bucket shares its value: "T5
 //   Relative-Position Bias"), dslope_h = -sum dS_ij |j - p_i|.
+// Shaw (section "Shaw et al.") and DeBERTa (section "DeBERTa: disentangled
+// content and position") put table rows into the logit (and, Shaw, the
+// value); their extra terms are sums of the same dS (Shaw: and P) gathered
+// by table row, formed by the kernels below and the Shaw / DeBERTa ones at
+// the end of the file.
 //
 // Three kernels:
 //   relpos_bwd_stats_kernel  one 128-row query tile per CTA: lse_i (log2
@@ -22,6 +27,8 @@
 //     issues both products per key tile into one of two TMEM buffers, and two
 //     compute warpgroups take the key tiles alternately (thread t = query row
 //     t), each keeping running statistics; the two are merged at the end.
+//     Shaw: also each row's q . a_K and dO . a_V per clipped offset and its
+//     sums of P and dS per offset; DeBERTa: each row's dS beyond the band.
 //   relpos_bwd_dkdv_kernel   one 128-key tile per CTA against every query tile
 //     that sees it, taken in 64-row halves ("sub-steps"): S^T = K Q_h^T and
 //     dP^T = V dO_h^T into the half's TMEM buffer; the half's compute warpgroup
@@ -31,8 +38,12 @@
 //     dQ_i = dS K, one product per query tile). A fourth warpgroup adds each
 //     dQ_i, scaled, into an fp32 accumulator in global memory. The bias
 //     gradient is summed per offset in shared memory (T5) or per thread
-//     (ALiBi's slope) and added once per CTA.
+//     (ALiBi's slope) and added once per CTA; DeBERTa's band dS is scattered
+//     by table row to global memory.
 //   relpos_bwd_dq_convert_kernel  the dQ accumulator to bf16.
+// Shaw then adds its a_K term to dQ and sums the tables' gradients (final and
+// reduce kernels); DeBERTa folds the far sums into its gathered dS and runs
+// its four table products as plain GEMMs (cuBLAS).
 // Products of one CTA queue on the tensor core while the compute warpgroups
 // work on the other buffer. Every wait has a time limit, after which the kernel
 // records RELPOS_ERR_DEVICE_TIMEOUT and winds down without hanging.
