@@ -420,6 +420,35 @@ def t5_attention_key_positions(Q, K, V, bias, key_pos, *, num_buckets: int = 32,
     return out
 
 
+def alibi_attention_key_positions(Q, K, V, slopes, key_pos, *, causal: bool = False,
+                                  q_offset: int = 0) -> np.ndarray:
+    """ALiBi attention over keys at explicit positions, in fp64.
+
+    [RPE] "Kernels and the KV cache": an offset-only bias needs nothing
+    rewritten when the cache evicts middle tokens; [RPE] "ALiBi and RoPE: the
+    two endpoints": the bias is -slope_h times the distance. With the
+    positions of R16 (``key_pos`` [B, H, Lk], query row i at q_offset + i) the
+    logit is q_i . k_j / sqrt(d) - slope_h * |key_pos_j - (q_offset + i)|, and
+    causal masking drops keys positioned after the query.
+    """
+    Q = np.asarray(Q, dtype=np.float64)
+    K = np.asarray(K, dtype=np.float64)
+    V = np.asarray(V, dtype=np.float64)
+    slopes = np.asarray(slopes, dtype=np.float64)
+    key_pos = np.asarray(key_pos, dtype=np.int64)
+    B, H, Lq, d = Q.shape
+    p = np.arange(Lq) + q_offset
+    out = np.zeros((B, H, Lq, d))
+    for b in range(B):
+        for h in range(H):
+            rel = key_pos[b, h][None, :] - p[:, None]
+            lg = Q[b, h] @ K[b, h].T / math.sqrt(d) - slopes[h] * np.abs(rel).astype(np.float64)
+            if causal:
+                lg = np.where(rel > 0, -np.inf, lg)
+            out[b, h] = _softmax_rows(lg) @ V[b, h]
+    return out
+
+
 def shaw_naive(Q, K, V, aK, aV, kclip, causal=False, q_offset=0) -> np.ndarray:
     """Shaw attention with the full L x L x d relative tensors built.
 

@@ -483,6 +483,42 @@ def check_key_positions_shift():
         assert np.max(np.abs(a - b)) < 1e-12
 
 
+def check_alibi_key_positions():
+    """ALiBi over explicit key positions: keys at 0 .. Lk-1 are the plain
+    ALiBi computation; a cache that evicted keys equals the full cache with
+    those keys masked (scores pushed to -1e6, as for T5); shifting every
+    position by a constant changes nothing."""
+    rng = _rng(34)
+    B, H, d, Lk = 1, 3, 16, 40
+    slopes = np.array([0.5, 0.125, 1.0 / 64])
+    for causal, qoff, Lq in ((False, 0, 40), (True, 0, 40), (True, 37, 3)):
+        Q, K, V = (rng.standard_normal((B, H, n, d)) for n in (Lq, Lk, Lk))
+        kp = np.broadcast_to(np.arange(Lk), (B, H, Lk))
+        a = orc.alibi_attention_key_positions(Q, K, V, slopes, kp, causal=causal, q_offset=qoff)
+        b = orc.attention(orc.MODE_ALIBI, Q, K, V, slopes, causal=causal, q_offset=qoff)
+        assert np.max(np.abs(a - b)) < 1e-12, causal
+    L = 300
+    keep = np.append(np.sort(rng.choice(L - 1, 60, replace=False)), L - 1)
+    gone = np.setdiff1d(np.arange(L), keep)
+    sl1 = np.array([0.03])
+    for causal in (False, True):
+        q = rng.standard_normal((1, 1, 1, d))
+        Kf, Vf = rng.standard_normal((1, 1, L, d)), rng.standard_normal((1, 1, L, d))
+        Km = Kf.copy()
+        qv = q[0, 0, 0]
+        Km[0, 0, gone] = -1e6 * math.sqrt(d) * qv / (qv @ qv)
+        full = orc.attention(orc.MODE_ALIBI, q, Km, Vf, sl1, causal=causal, q_offset=L - 1)
+        part = orc.alibi_attention_key_positions(q, Kf[:, :, keep], Vf[:, :, keep], sl1, keep[None, None, :],
+                                                 causal=causal, q_offset=L - 1)
+        assert np.max(np.abs(part - full)) < 1e-10, causal
+    Q, K, V = (rng.standard_normal((1, H, n, d)) for n in (5, 30, 30))
+    kp = np.sort(rng.choice(200, 30, replace=False))[None, None, :].repeat(H, axis=1)
+    for causal in (False, True):
+        a = orc.alibi_attention_key_positions(Q, K, V, slopes, kp, causal=causal, q_offset=150)
+        b = orc.alibi_attention_key_positions(Q, K, V, slopes, kp + 1000, causal=causal, q_offset=1150)
+        assert np.max(np.abs(a - b)) < 1e-12
+
+
 # ---------------------------------------------------------------- backward pins
 
 # (causal, q_offset, num_buckets, max_distance): small tables whose log
@@ -800,6 +836,7 @@ ALL_CHECKS = [
     check_t5_two_token, check_shaw_sign, check_deberta_sign, check_query_offset_consistency,
     check_alibi_zero_slopes_are_sdpa, check_alibi_closed_form,
     check_key_positions_contiguous, check_key_positions_eviction, check_key_positions_shift,
+    check_alibi_key_positions,
     check_t5_backward_finite_differences, check_t5_backward_vs_autograd,
     check_t5_backward_invariants, check_t5_backward_unused_bucket,
     check_backward_finite_differences_all_modes, check_backward_zero_tables_vs_autograd,

@@ -146,6 +146,37 @@ def _kpos_no_query_offset(Q, K, V, bias, key_pos, **kw):
     return _ORIG_KPOS(Q, K, V, bias, key_pos, **kw)
 
 
+def _akpos_index_not_position(Q, K, V, slopes, key_pos, **kw):
+    Lk = np.asarray(K).shape[2]
+    kp = np.broadcast_to(np.arange(Lk), np.asarray(key_pos).shape)
+    return _ORIG_AKPOS(Q, K, V, slopes, kp, **kw)
+
+
+def _akpos_no_query_offset(Q, K, V, slopes, key_pos, **kw):
+    kw = dict(kw)
+    kw["q_offset"] = 0
+    return _ORIG_AKPOS(Q, K, V, slopes, key_pos, **kw)
+
+
+def _akpos_signed_distance(Q, K, V, slopes, key_pos, **kw):
+    # -slope * (key - query) instead of its absolute value: equal behind the
+    # query, wrong ahead of it
+    Q, K, V = (np.asarray(t, dtype=np.float64) for t in (Q, K, V))
+    kp = np.asarray(key_pos, dtype=np.int64)
+    B, H, Lq, d = Q.shape
+    p = np.arange(Lq) + kw.get("q_offset", 0)
+    out = np.zeros((B, H, Lq, d))
+    for b in range(B):
+        for h in range(H):
+            rel = kp[b, h][None, :] - p[:, None]
+            lg = Q[b, h] @ K[b, h].T / np.sqrt(d) + slopes[h] * rel
+            if kw.get("causal", False):
+                lg = np.where(rel > 0, -np.inf, lg)
+            e = np.exp(lg - lg.max(axis=1, keepdims=True))
+            out[b, h] = (e / e.sum(axis=1, keepdims=True)) @ V[b, h]
+    return out
+
+
 def _bwd_mutant(kind):
     """The backward with one planted mistake (the forward part is the oracle's)."""
     def bwd(Q, K, V, bias, dO, *, num_buckets=32, max_distance=128, causal=False, q_offset=0):
@@ -284,6 +315,9 @@ MUTATIONS = {
     "alibi_position_off_by_one": ("alibi_logits", _alibi_position_off_by_one),
     "kpos_index_not_position": ("t5_attention_key_positions", _kpos_index_not_position),
     "kpos_no_query_offset": ("t5_attention_key_positions", _kpos_no_query_offset),
+    "alibi_kpos_index_not_position": ("alibi_attention_key_positions", _akpos_index_not_position),
+    "alibi_kpos_no_query_offset": ("alibi_attention_key_positions", _akpos_no_query_offset),
+    "alibi_kpos_signed_distance": ("alibi_attention_key_positions", _akpos_signed_distance),
     "bwd_no_row_term": ("t5_attention_backward", _bwd_mutant("no_row_term")),
     "bwd_row_term_over_keys": ("t5_attention_backward", _bwd_mutant("row_term_over_keys")),
     "bwd_unscaled_dq": ("t5_attention_backward", _bwd_mutant("unscaled_dq")),
@@ -309,6 +343,7 @@ MUTATIONS = {
     "txl_table_row_shift": ("txl_position_table", _txl_table_row_shift),
 }
 _ORIG_KPOS = orc.t5_attention_key_positions
+_ORIG_AKPOS = orc.alibi_attention_key_positions
 _ORIG_ALIBI = orc.alibi_logits
 _ORIG_SHAW_IDX = orc.shaw_index
 _ORIG_DELTA = orc.deberta_delta
