@@ -202,7 +202,7 @@ def kernels_per_step(w, backward=False):
         # (DeBERTa: the band pre-pass, statistics, dK / dV, the far-sum fold
         # and the dQ, dK conversions; its table products run in cuBLAS)
         return 4 if w.mode == MODE_SHAW else 6 if w.mode == MODE_DEBERTA else 3
-    decode = w.mode == MODE_T5 and w.Lq <= 8
+    decode = (w.mode == MODE_T5 and w.Lq <= 8) or (w.mode == MODE_ALIBI and w.cache_len > 0)
     n = 2 if decode else 1
     if w.mode in (MODE_DEBERTA, MODE_TXL):
         n += 1  # the band / operand pre-pass
@@ -214,7 +214,7 @@ def kernels_per_step(w, backward=False):
 def dominant_kernel(w, backward=False):
     if backward:
         return "relpos_bwd_dkdv_kernel", "tensor"
-    if w.mode == MODE_T5 and w.Lq <= 8:
+    if (w.mode == MODE_T5 and w.Lq <= 8) or (w.mode == MODE_ALIBI and w.cache_len > 0):
         return "relpos_decode_partial_kernel", "hbm"
     return "relpos_fwd_kernel", "tensor"
 
@@ -247,6 +247,13 @@ class GpuRun:
     def _call(self, d, out=None):
         w = self.w
         p = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())  # noqa: E731
+        if w.cache_len and w.mode == MODE_ALIBI:  # keys at explicit positions
+            rc = self.rp.relpos_alibi_decode_positions(
+                p(d["Q"]), p(d["K"]), p(d["V"]), p(d["table0"]), p(d["key_pos"]), w.B, w.H, w.Lq, w.Lk,
+                int(w.causal), w.q_offset, p(out if out is not None else d["out"]), self.sptr)
+            if rc != 0:
+                raise RuntimeError(f"relpos_alibi_decode_positions failed: {rc}")
+            return
         if w.cache_len:  # keys at explicit positions
             rc = self.rp.relpos_t5_decode_positions(
                 p(d["Q"]), p(d["K"]), p(d["V"]), p(d["table0"]), p(d["key_pos"]), w.B, w.H, w.Lq,
@@ -466,7 +473,12 @@ def cpu_baseline(w, budget_s=12.0):
     heads = [(b, h) for b in range(w.B) for h in range(w.H)]
     done = 0
     for (b, h) in heads:
-        if w.cache_len:
+        if w.cache_len and w.mode == MODE_ALIBI:
+            kp = x["key_pos"].numpy()
+            orc.alibi_attention_key_positions(Q[b:b + 1, h:h + 1], K[b:b + 1, h:h + 1], V[b:b + 1, h:h + 1],
+                                              t0[h:h + 1], kp[b:b + 1, h:h + 1], causal=w.causal,
+                                              q_offset=w.q_offset)
+        elif w.cache_len:
             kp = x["key_pos"].numpy()
             orc.t5_attention_key_positions(Q[b:b + 1, h:h + 1], K[b:b + 1, h:h + 1], V[b:b + 1, h:h + 1],
                                            t0[:, h:h + 1], kp[b:b + 1, h:h + 1],
@@ -601,8 +613,8 @@ def config_of(w, world, g, backward=False):
 
 # every configuration gets a block of its own in the bench line
 BLOCK_WORKLOADS = ("t5_base_bidir", "t5_causal", "shaw", "deberta", "txl_mem", "t5_decode",
-                   "t5_decode_evicted", "alibi_bidir", "alibi_causal", "alibi_d128", "t5_d128",
-                   "t5_tiny_fp32")
+                   "t5_decode_evicted", "alibi_decode_evicted", "alibi_bidir", "alibi_causal", "alibi_d128",
+                   "t5_d128", "t5_tiny_fp32")
 BACKWARD_WORKLOADS = ("t5_base_bidir", "t5_causal", "alibi_causal", "shaw", "deberta")
 
 

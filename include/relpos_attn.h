@@ -265,6 +265,25 @@ int relpos_t5_decode_positions(const void* Q, const void* K, const void* V, cons
                                int max_distance, int causal, int q_offset, void* out, void* stream);
 
 /*
+ * relpos_alibi_decode_positions -- ALiBi cached decoding over keys at
+ * explicit positions ("Relative Position Embeddings, in depth", sections
+ * "ALiBi and RoPE: the two endpoints" and "Kernels and the KV cache"): the
+ * logit of query row i and key j is q_i . k_j / sqrt(64) - slope_h *
+ * |key_pos[b, h, j] - (i + q_offset)|.
+ *
+ *   slopes      device, fp32 [H], 4-byte aligned: the heads' slopes.
+ *   key_pos, causal, q_offset, out, B, H, Lk, stream: as for
+ *               relpos_t5_decode_positions (bf16 Q, K, V, out; d = 64).
+ *   Lq          0 .. 8 query rows (RELPOS_ERR_UNSUPPORTED beyond).
+ * The split-key decode kernels, with each key's bias formed from its
+ * position. Scratch and asynchrony as relpos_t5_decode_positions for
+ * Lq <= 8.
+ */
+int relpos_alibi_decode_positions(const void* Q, const void* K, const void* V, const void* slopes,
+                                  const int* key_pos, int B, int H, int Lq, int Lk, int causal,
+                                  int q_offset, void* out, void* stream);
+
+/*
  * relpos_t5_attn_bwd -- gradients of the T5-bias attention forward
  * (relpos_attn_fwd with mode RELPOS_T5, dtype RELPOS_BF16). The bias is a
  * learned table ("Relative Position Embeddings, in depth", section "T5: one

@@ -187,3 +187,30 @@ def _deberta_bwd(**kw):
 ])
 def test_deberta_backward_argument_errors_before_launch(lib, kw, code):
     assert _deberta_bwd(**kw) == code
+
+
+def _alibi_dec(**kw):
+    a = dict(Q=16, K=32, V=48, slopes=64, kp=80, B=1, H=1, Lq=1, Lk=4, causal=1, qoff=3, out=96, stream=None)
+    a.update(kw)
+    v = lambda x: ctypes.c_void_p(x) if x else None  # noqa: E731
+    return rp.relpos_alibi_decode_positions(v(a["Q"]), v(a["K"]), v(a["V"]), v(a["slopes"]), v(a["kp"]),
+                                            a["B"], a["H"], a["Lq"], a["Lk"], a["causal"], a["qoff"],
+                                            v(a["out"]), a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(Lq=9), rp.RELPOS_ERR_UNSUPPORTED),
+    (dict(causal=2), rp.RELPOS_ERR_INVALID_ARG),
+    (dict(B=-1), rp.RELPOS_ERR_INVALID_ARG),
+    (dict(kp=0), rp.RELPOS_ERR_INVALID_ARG),
+    (dict(kp=82), rp.RELPOS_ERR_INVALID_ARG),       # key positions not 4-byte aligned
+    (dict(slopes=66), rp.RELPOS_ERR_INVALID_ARG),   # slopes not 4-byte aligned
+    (dict(K=40), rp.RELPOS_ERR_INVALID_ARG),
+    (dict(out=0), rp.RELPOS_ERR_INVALID_ARG),
+])
+def test_alibi_decode_positions_argument_errors_before_launch(lib, kw, code):
+    assert _alibi_dec(**kw) == code
+
+
+def test_alibi_decode_positions_empty_is_noop(lib):
+    assert _alibi_dec(Lq=0) == rp.RELPOS_OK

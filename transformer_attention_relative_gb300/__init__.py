@@ -28,7 +28,8 @@ RELPOS_ERR_SCRATCH_LIMIT = -5
 
 EXPORTED = ("relpos_attn_fwd", "relpos_attn_fwd_padded", "relpos_index_ids", "relpos_check_status", "relpos_strerror",
             "relpos_selftest_wait_timeout", "relpos_t5_decode_noalloc", "relpos_t5_decode_positions",
-            "relpos_t5_attn_bwd", "relpos_alibi_attn_bwd", "relpos_shaw_attn_bwd", "relpos_deberta_attn_bwd")
+            "relpos_t5_attn_bwd", "relpos_alibi_attn_bwd", "relpos_shaw_attn_bwd", "relpos_deberta_attn_bwd",
+            "relpos_alibi_decode_positions")
 
 _lib = None
 
@@ -73,6 +74,8 @@ def load_library(path: str = LIB_PATH):
     lib.relpos_shaw_attn_bwd.restype = i
     lib.relpos_deberta_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, vp, vp, vp, vp, vp, vp]
     lib.relpos_deberta_attn_bwd.restype = i
+    lib.relpos_alibi_decode_positions.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, vp, vp]
+    lib.relpos_alibi_decode_positions.restype = i
     _lib = lib
     return lib
 
@@ -125,6 +128,13 @@ def relpos_t5_decode_positions(Q, K, V, bias, key_pos, B, H, Lq, Lk, num_buckets
     return load_library().relpos_t5_decode_positions(Q, K, V, bias, key_pos, B, H, Lq, Lk,
                                                      num_buckets, max_distance, causal, q_offset,
                                                      out, stream)
+
+
+def relpos_alibi_decode_positions(Q, K, V, slopes, key_pos, B, H, Lq, Lk, causal, q_offset, out,
+                                  stream) -> int:
+    """ALiBi cached decode over keys at explicit positions (an evicted cache)."""
+    return load_library().relpos_alibi_decode_positions(Q, K, V, slopes, key_pos, B, H, Lq, Lk, causal,
+                                                        q_offset, out, stream)
 
 
 def relpos_t5_attn_bwd(Q, K, V, dO, bias, B, H, Lq, Lk, d, num_buckets, max_distance, causal,
@@ -252,6 +262,30 @@ def t5_decode_positions(Q, K, V, bias, key_pos, *, num_buckets: int = 32, max_di
                                     _stream(stream))
     if rc != RELPOS_OK:
         raise RelposError(rc, "relpos_t5_decode_positions")
+    return out
+
+
+def alibi_decode_positions(Q, K, V, slopes, key_pos, *, causal: bool = True, q_offset: int = 0, out=None,
+                           stream=None):
+    """Run ``relpos_alibi_decode_positions`` on CUDA tensors; returns ``out``.
+
+    Q [B,H,Lq,64] (Lq <= 8), K, V [B,H,Lk,64] bf16; slopes [H] fp32; key_pos [B,H,Lk] int32 positions of
+    the kept keys.
+    """
+    import torch
+    B, H, Lq, _ = Q.shape
+    Lk = K.shape[2]
+    for t in (Q, K, V, slopes, key_pos, out):
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("tensors must be contiguous CUDA tensors")
+    if key_pos.dtype != torch.int32:
+        raise TypeError("key_pos must be int32")
+    if out is None:
+        out = torch.empty_like(Q)
+    rc = relpos_alibi_decode_positions(_ptr(Q), _ptr(K), _ptr(V), _ptr(slopes), _ptr(key_pos), B, H, Lq, Lk,
+                                       int(causal), q_offset, _ptr(out), _stream(stream))
+    if rc != RELPOS_OK:
+        raise RelposError(rc, "relpos_alibi_decode_positions")
     return out
 
 

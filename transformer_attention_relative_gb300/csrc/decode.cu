@@ -1,7 +1,7 @@
-// decode.cu -- T5-bias attention for a few query rows against a long key
-// cache (cached decoding: "T5 Relative-Position Bias", cached-decoder
-// example; "Relative Position Embeddings, in depth", "Kernels and the KV
-// cache"). With one query row per (batch, head) the work is a stream over K
+// decode.cu -- T5-bias (and, over explicit key positions, ALiBi) attention
+// for a few query rows against a long key cache (cached decoding: "T5
+// Relative-Position Bias", cached-decoder example; "Relative Position
+// Embeddings, in depth", "Kernels and the KV cache"). With one query row per (batch, head) the work is a stream over K
 // and V (about one flop per byte), so it runs on CUDA cores, split over key
 // chunks so that every SM keeps many 16-byte loads in flight, followed by a
 // small combine of the per-chunk (max, sum, partial output).
@@ -55,6 +55,10 @@ __global__ void __launch_bounds__(kDecThreads, 3) relpos_decode_partial_kernel(c
   __shared__ float o_s[4][kHeadDim];
 
   griddep_wait();  // the previous kernel of the stream has completed
+  // ALiBi (t5_R < 0): bias holds the heads' slopes, and an offset's bias is
+  // -slope |offset| (log2 units below), with no saturation
+  const bool alibi = p.t5_R < 0;
+  const float slope2 = alibi ? __ldg(p.bias + h) * kLog2e : 0.f;
   const int pos = qi + p.q_offset;
   const int jb = chunk * kDecChunk;
   // explicit key positions (a cache that evicted keys): visibility follows
@@ -92,8 +96,8 @@ __global__ void __launch_bounds__(kDecThreads, 3) relpos_decode_partial_kernel(c
   // lying wholly beyond R needs one bias; otherwise each key's bias is looked
   // up once here rather than by every thread that shares the key.
   const int rel_first = jb - pos, rel_last = je - 1 - pos;
-  const bool sat_l = !kpos && rel_last <= -p.t5_R;
-  const bool sat_r = !kpos && p.t5.bidir && rel_first >= p.t5_R;
+  const bool sat_l = !kpos && !alibi && rel_last <= -p.t5_R;
+  const bool sat_r = !kpos && !alibi && p.t5.bidir && rel_first >= p.t5_R;
   float bias_const = 0.f;
   if (sat_l || sat_r) {
     bias_const = __ldg(p.bias + t5_bucket_dev(sat_l ? -p.t5_R : p.t5_R, p.t5) * p.H + h) * kLog2e;
@@ -108,13 +112,20 @@ __global__ void __launch_bounds__(kDecThreads, 3) relpos_decode_partial_kernel(c
     const int rel1 = (in1 ? __ldg(kpos + jb + r1) : pos) - pos;
     const bool vis0 = in0 && (!p.causal || rel0 <= 0);
     const bool vis1 = in1 && (!p.causal || rel1 <= 0);
-    const float b0 = vis0 ? __ldg(p.bias + t5_bucket_dev(rel0, p.t5) * p.H + h) : 0.f;
-    const float b1 = vis1 ? __ldg(p.bias + t5_bucket_dev(rel1, p.t5) * p.H + h) : 0.f;
-    bias_s[r0] = vis0 ? b0 * kLog2e : -INFINITY;
-    bias_s[r1] = vis1 ? b1 * kLog2e : -INFINITY;
+    float b0 = 0.f, b1 = 0.f;
+    if (alibi) {
+      b0 = -slope2 * fabsf(static_cast<float>(rel0));
+      b1 = -slope2 * fabsf(static_cast<float>(rel1));
+    } else {
+      b0 = vis0 ? __ldg(p.bias + t5_bucket_dev(rel0, p.t5) * p.H + h) * kLog2e : 0.f;
+      b1 = vis1 ? __ldg(p.bias + t5_bucket_dev(rel1, p.t5) * p.H + h) * kLog2e : 0.f;
+    }
+    bias_s[r0] = vis0 ? b0 : -INFINITY;
+    bias_s[r1] = vis1 ? b1 : -INFINITY;
   } else {
     for (int r = tid; r < kDecChunk; r += kDecThreads)
-      bias_s[r] = __ldg(p.bias + t5_bucket_dev(jb + r - pos, p.t5) * p.H + h) * kLog2e;
+      bias_s[r] = alibi ? -slope2 * fabsf(static_cast<float>(jb + r - pos))
+                        : __ldg(p.bias + t5_bucket_dev(jb + r - pos, p.t5) * p.H + h) * kLog2e;
   }
   const bool sat = sat_l || sat_r;
 
@@ -294,15 +305,15 @@ float* noalloc_scratch() {
   return g_noalloc_ptr[dev];
 }
 
-// Checks shared by the two decode-only entry points, before anything is
+// Checks shared by the decode-only entry points, before anything is
 // launched: RELPOS_OK to go on, a return code otherwise. *noop is set when
 // there is nothing to compute (no query row).
-int decode_entry_check(const void* Q, const void* K, const void* V, const void* bias,
+int decode_entry_check(int mode, const void* Q, const void* K, const void* V, const void* bias,
                        const void* key_pos, bool need_key_pos, const void* out, int B, int H,
                        int Lq, int Lk, int num_buckets, int max_distance, int causal,
                        int q_offset, bool* noop) {
   *noop = false;
-  int rc = check_rel_params(RELPOS_T5, num_buckets, max_distance, causal);
+  int rc = check_rel_params(mode, num_buckets, max_distance, causal);
   if (rc != RELPOS_OK) return rc;
   if (B < 0 || H < 0 || Lq < 0 || Lk < 0 || q_offset < 0) return RELPOS_ERR_INVALID_ARG;
   if (Lq > 8 && !need_key_pos) return RELPOS_ERR_UNSUPPORTED;  // decode shapes only
@@ -368,7 +379,7 @@ extern "C" int relpos_t5_decode_noalloc(const void* Q, const void* K, const void
                                         int q_offset, void* out, void* stream) {
   using namespace relpos;
   bool noop = false;
-  int rc = decode_entry_check(Q, K, V, bias, nullptr, false, out, B, H, Lq, Lk, num_buckets,
+  int rc = decode_entry_check(RELPOS_T5, Q, K, V, bias, nullptr, false, out, B, H, Lq, Lk, num_buckets,
                               max_distance, causal, q_offset, &noop);
   if (rc != RELPOS_OK || noop) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -409,7 +420,7 @@ extern "C" int relpos_t5_decode_positions(const void* Q, const void* K, const vo
                                           int causal, int q_offset, void* out, void* stream) {
   using namespace relpos;
   bool noop = false;
-  int rc = decode_entry_check(Q, K, V, bias, key_pos, true, out, B, H, Lq, Lk, num_buckets,
+  int rc = decode_entry_check(RELPOS_T5, Q, K, V, bias, key_pos, true, out, B, H, Lq, Lk, num_buckets,
                               max_distance, causal, q_offset, &noop);
   if (rc != RELPOS_OK || noop) return rc;
   // more than a few query rows (a chunk of new tokens against the cache): the
@@ -435,6 +446,46 @@ extern "C" int relpos_t5_decode_positions(const void* Q, const void* K, const vo
   const float scale_log2 = (1.0f / std::sqrt(static_cast<float>(kHeadDim))) * kLog2e;
   const DecodeParams dp = make_decode_params(Q, K, V, bias, key_pos, B, H, Lq, Lk, causal, q_offset,
                                              scale_log2, t5, R, scratch, out, false);
+  const bool ok = launch_decode(dp, s) == cudaSuccess;
+  const bool freed = cudaFreeAsync(scratch, s) == cudaSuccess;
+  if (!ok || !freed) {
+    cudaGetLastError();
+    return RELPOS_ERR_CUDA;
+  }
+  return RELPOS_OK;
+}
+
+// ALiBi over keys at explicit positions: the same split-key kernels with the
+// bias -slope_h |key position - query position| ("Relative Position
+// Embeddings, in depth", sections "ALiBi and RoPE: the two endpoints" and
+// "Kernels and the KV cache"); decode shapes (up to 8 query rows).
+extern "C" int relpos_alibi_decode_positions(const void* Q, const void* K, const void* V,
+                                             const void* slopes, const int* key_pos, int B, int H,
+                                             int Lq, int Lk, int causal, int q_offset, void* out,
+                                             void* stream) {
+  using namespace relpos;
+  bool noop = false;
+  int rc = decode_entry_check(RELPOS_ALIBI, Q, K, V, slopes, key_pos, true, out, B, H, Lq, Lk, 0, 0, causal,
+                              q_offset, &noop);
+  if (rc != RELPOS_OK || noop) return rc;
+  if (Lq > 8) return RELPOS_ERR_UNSUPPORTED;
+  if (Lk > 0 && (reinterpret_cast<uintptr_t>(slopes) & 3u)) return RELPOS_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t rows = static_cast<size_t>(B) * H * Lq;
+  if (Lk == 0)
+    return cudaMemsetAsync(out, 0, rows * kHeadDim * 2, s) == cudaSuccess ? RELPOS_OK
+                                                                           : RELPOS_ERR_CUDA;
+  float* scratch = nullptr;
+  if (cudaMallocAsync(&scratch, decode_partial_floats(rows, Lk) * sizeof(float), s) != cudaSuccess) {
+    cudaGetLastError();
+    return RELPOS_ERR_CUDA;
+  }
+  T5Index unused;
+  std::memset(&unused, 0, sizeof(unused));
+  const float scale_log2 = (1.0f / std::sqrt(static_cast<float>(kHeadDim))) * kLog2e;
+  // t5_R = -1 selects the ALiBi bias in the partial kernel
+  const DecodeParams dp = make_decode_params(Q, K, V, slopes, key_pos, B, H, Lq, Lk, causal, q_offset,
+                                             scale_log2, unused, -1, scratch, out, false);
   const bool ok = launch_decode(dp, s) == cudaSuccess;
   const bool freed = cudaFreeAsync(scratch, s) == cudaSuccess;
   if (!ok || !freed) {

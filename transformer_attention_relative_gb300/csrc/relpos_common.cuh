@@ -148,7 +148,7 @@ struct DecodeParams {
   float* part_ml;  // [B*H*Lq, nchunks, 2]
   void* out;
   int out_f32;
-  int t5_R;  // |offset| >= R: the side's last bucket
+  int t5_R;  // |offset| >= R: the side's last bucket; -1: ALiBi, bias holds the slopes [H]
   T5Index t5;
   const int* key_pos;  // [B*H, Lk] explicit key positions, or null (key j at position j)
 };

@@ -151,6 +151,9 @@ WORKLOADS = {
                            causal=True),
     "t5_d128": Workload("t5_d128", 10, MODE_T5, "bf16", 4, 16, 2048, 2048, 128,
                         num_buckets=32, rel_param=128, causal=True, table_sigma=0.5),
+    # ALiBi decode over the evicted cache of t5_decode_evicted's shape
+    "alibi_decode_evicted": Workload("alibi_decode_evicted", 11, MODE_ALIBI, "bf16", 32, 16, 1, 2048, 64,
+                                     causal=True, q_offset=4095, cache_len=4096),
 }
 
 
@@ -183,12 +186,13 @@ def make_inputs(w: Workload, seed: int | None = None):
     s0, s1 = w.table_shapes()
     if w.mode == MODE_ALIBI:
         t0 = torch.tensor([2.0 ** (-8.0 * (h + 1) / w.H) for h in range(w.H)], dtype=torch.float32)
-        return {"Q": q, "K": k, "V": v, "table0": t0, "table1": None}
-    tdt0 = torch.float32 if w.mode in (MODE_T5, MODE_TXL) else torch.bfloat16
-    tdt1 = torch.float32 if w.mode == MODE_TXL else torch.bfloat16
-    t0 = draw(s0, w.table_sigma, tdt0)
-    t1 = draw(s1, w.table_sigma, tdt1) if s1 is not None else None
-    x = {"Q": q, "K": k, "V": v, "table0": t0, "table1": t1}
+        x = {"Q": q, "K": k, "V": v, "table0": t0, "table1": None}
+    else:
+        tdt0 = torch.float32 if w.mode in (MODE_T5, MODE_TXL) else torch.bfloat16
+        tdt1 = torch.float32 if w.mode == MODE_TXL else torch.bfloat16
+        t0 = draw(s0, w.table_sigma, tdt0)
+        t1 = draw(s1, w.table_sigma, tdt1) if s1 is not None else None
+        x = {"Q": q, "K": k, "V": v, "table0": t0, "table1": t1}
     if w.cache_len:
         # a cache that kept Lk of its cache_len tokens, always the newest one,
         # each (batch, head) its own choice, in position order
